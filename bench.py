@@ -1,0 +1,392 @@
+#!/usr/bin/env python
+"""Benchmark of the GBLA layer hot path on GB300.
+
+One step = one pass of the whole hot path over one batch: gbla_forward
+(training mode: conv, projections + gate, state reduction + combine, readout
+with the RmsNorm gate) followed by gbla_backward (query side, key side,
+projection GEMMs, conv backward, parameter-gradient sums).  Inputs are seeded
+synthetic tensors of the workload's shape, resident in HBM before timing.
+
+Prints one JSON line (rank 0).  --impl reference times the fp64 CPU oracle on
+a bounded sample of the same workload instead.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GBLA tokens/s fwd & fwd+bwd at L=2k–32k; achieved HBM GB/s vs peak"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes per launch from ncu captures (dram__bytes_read.sum + dram__bytes_write.sum),
+# keyed by launch name: (bytes, workload name, sha1 of the kernel's source file when captured).
+# A source change since the capture makes the figure stale: it is then reported as null.
+NCU_TRAFFIC: dict = {}
+KERNEL_SOURCE = {"projection gemm": "gemm.cu", "dx~ gemm": "gemm.cu", "dW gemm": "gemm.cu",
+                 "reduce": "core_bf16.cu", "readout": "core_bf16.cu", "bwd_q": "core_bf16.cu",
+                 "bwd_kv": "core_bf16.cu", "conv": "layer_misc.cu", "conv bwd": "layer_misc.cu",
+                 "dW sum": "layer_misc.cu"}
+
+
+def source_sha(name: str) -> str | None:
+    f = KERNEL_SOURCE.get(name)
+    if f is None:
+        return None
+    p = os.path.join(ROOT, "generative_retrieval_encoder_gb300", "csrc", f)
+    return hashlib.sha1(open(p, "rb").read()).hexdigest()[:12]
+
+
+def workloads():
+    from generative_retrieval_encoder_gb300 import workloads as W
+    return {"train2k": W.FWD_2K, "long32k": W.LONG_32K, "train8k": W.TRAIN_8K, "varlen": W.VARLEN}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic(wl, T: int, n_wsplit: int | None = None) -> dict:
+    """Algorithmic work of one launch of each kernel, as (bound, amount):
+    bytes for HBM-bound kernels, flops for tensor contractions."""
+    d, H, dh = wl.d, wl.H, wl.dh
+    HD, N1 = H * dh, 4 * H * dh + H
+    th = T * H
+    return {
+        "conv": ("hbm", T * d * 4),                         # x in, x~ out (bf16)
+        "projection gemm": ("tensor", 2 * T * d * N1),
+        "reduce": ("hbm", th * (4 * dh + 4)),               # k, v bf16 + g fp32
+        "readout": ("hbm", th * 6 * dh),                    # q, r in; y out
+        "bwd_q": ("hbm", th * 10 * dh),                     # q, r, dy in; dq, dr out
+        "bwd_kv": ("hbm", th * (8 * dh + 6)),               # k, v, g in; dk, dv, ds out
+        "dx~ gemm": ("tensor", 2 * T * N1 * d),
+        "dW gemm": ("tensor", 2 * T * d * N1),
+        "conv bwd": ("hbm", T * d * 8),                     # x, dx~ (fp32) in; dx out
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        load = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def make_inputs(wl, device):
+    import torch
+    from generative_retrieval_encoder_gb300 import gbla
+    dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    cu = wl.cu_seqlens()
+    kw = {}
+    if cu is not None:
+        kw["cu_seqlens"] = torch.tensor(cu, dtype=torch.int32, device=device)
+        shape = gbla.make_shape(1, cu[-1], wl.d, wl.H, wl.dh, dtype=wl.dtype, gate=wl.gate, eps=wl.eps, **kw)
+    else:
+        shape = gbla.make_shape(wl.B, wl.L, wl.d, wl.H, wl.dh, dtype=wl.dtype, gate=wl.gate, eps=wl.eps)
+    x = wl.x().to(dt)
+    dy = wl.dy().to(dt)
+    P = {n: t.to(dt).to(device) for n, t in wl.params().items()}
+    return shape, x, dy, P
+
+
+def cpu_baseline(wl, budget_s: float = 12.0, max_seqs: int = 64):
+    """The oracle, as it stands, on whole sequences of the workload (fwd + bwd)
+    until about budget_s of CPU time is spent.  Returns (tokens/s, cores, sample)."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    lens = wl.lengths() or [wl.L] * wl.B
+    P = {n: t.to(_torch_dtype(wl)).double().numpy() for n, t in wl.params().items()}
+    rng = np.random.default_rng(0)
+    done, t0, nseq = 0, time.perf_counter(), 0
+    gm = 1 if wl.gate == "softmax" else 0
+    while nseq < min(max_seqs, len(lens)):
+        n = int(lens[nseq])
+        x = rng.standard_normal((n, wl.d))
+        dy = rng.standard_normal((n, wl.H * wl.dh))
+        st, ln = oracle.seqs(1, n)
+        oracle.gbla_forward(x, P, wl.H, wl.dh, st, ln, gm, wl.eps)
+        oracle.gbla_backward(x, P, dy, wl.H, wl.dh, st, ln, gm, wl.eps)
+        done += n
+        nseq += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return done / el, oracle.num_threads(), f"{nseq} whole sequence(s) ({done} tokens) of the workload, fwd+bwd", el
+
+
+def _torch_dtype(wl):
+    import torch
+    return torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+
+
+def run_reference(args, wl, rank: int):
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    oracle.build()
+    lens = wl.lengths() or [wl.L] * wl.B
+    n = int(lens[0]) if wl.lengths() is None else int(sorted(lens)[len(lens) // 2])
+    P = {k: t.to(_torch_dtype(wl)).double().numpy() for k, t in wl.params().items()}
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((n, wl.d))
+    dy = rng.standard_normal((n, wl.H * wl.dh))
+    st, ln = oracle.seqs(1, n)
+    gm = 1 if wl.gate == "softmax" else 0
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.gbla_forward(x, P, wl.H, wl.dh, st, ln, gm, wl.eps)
+        oracle.gbla_backward(x, P, dy, wl.H, wl.dh, st, ln, gm, wl.eps)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = n / (ms / 1e3)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "step": "forward+backward", "sample": f"one sequence of {n} tokens"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"one {n}-token sequence of the workload per step, fwd+bwd"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, wl, rank: int, world: int, local_rank: int):
+    import torch
+    import torch.distributed as dist
+    from generative_retrieval_encoder_gb300 import build as B
+    from generative_retrieval_encoder_gb300 import gbla
+
+    B.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    shape, x_h, dy_h, P = make_inputs(wl, dev)
+    T = gbla.rows(shape)
+    tokens = wl.valid_tokens()
+    x = x_h.to(dev)
+    dy = dy_h.to(dev)
+    y = torch.empty(T, wl.H * wl.dh, dtype=x.dtype, device=dev)
+    saved = torch.empty(gbla.gbla_saved_size(shape), dtype=torch.uint8, device=dev)
+    ws_f = gbla.workspace(shape, gbla.GBLA_OP_FORWARD, dev)
+    ws_b = gbla.workspace(shape, gbla.GBLA_OP_BACKWARD, dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    d, H, dh = wl.d, wl.H, wl.dh
+    grads = {"dx": torch.empty_like(x), "dconv_w": torch.empty(d, 4, **f32), "dconv_b": torch.empty(d, **f32),
+             "dW_q": torch.empty(d, H * dh, **f32), "dW_k": torch.empty(d, H * dh, **f32),
+             "dW_v": torch.empty(d, H * dh, **f32), "dW_r": torch.empty(d, H * dh, **f32),
+             "dw_g": torch.empty(d, H, **f32), "db_g": torch.empty(H, **f32), "drms_w": torch.empty(dh, **f32)}
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def fwd():
+        gbla.gbla_forward(shape, x, P, y=y, saved=saved, ws=ws_f)
+
+    def step():
+        fwd()
+        gbla.gbla_backward(shape, x, P, saved, dy, ws=ws_b, out=grads)
+
+    def timed(fn, k):
+        total = 0.0
+        for _ in range(k):
+            flush.fill_(1.0)  # evicts L2 between steps (outside the events)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            total += e0.elapsed_time(e1)
+        return total / k
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    # per-launch times (CUDA events on the launching stream, from the library)
+    gbla.gbla_profiling_enable(True)
+    gbla.gbla_profiling_read()
+    prof_steps = 3
+    for _ in range(prof_steps):
+        flush.fill_(1.0)
+        step()
+    rec = gbla.gbla_profiling_read()
+    gbla.gbla_profiling_enable(False)
+    per = {}
+    for n, ms in rec:
+        per.setdefault(n, []).append(ms)
+    launches_per_step = len([n for n, _ in rec if n != "memset"]) // prof_steps
+    kern = {n: sum(v) / prof_steps for n, v in per.items()}
+
+    # the timed region: K steps, barrier + synchronize on both sides, max over ranks
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        ms_step = timed(step, args.steps)
+        barrier()
+    ms_step = max_over_ranks(ms_step)
+    barrier()
+    ms_fwd = max_over_ranks(timed(fwd, args.steps))
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # inputs (x, dy) from pinned memory, forward + backward, D2H of the
+    # parameter gradients (the step's result)
+    xp, dyp = x_h.pin_memory(), dy_h.pin_memory()
+    host_g = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in grads.items() if k != "dx"}
+
+    def e2e_step():
+        x.copy_(xp, non_blocking=True)
+        dy.copy_(dyp, non_blocking=True)
+        step()
+        for k, v in host_g.items():
+            v.copy_(grads[k], non_blocking=True)
+
+    barrier()
+    ms_e2e = max_over_ranks(timed(e2e_step, max(3, args.steps // 2)))
+    h2d = x.numel() * x.element_size() + dy.numel() * dy.element_size()
+    d2h = sum(v.numel() * v.element_size() for v in host_g.values())
+
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    alg = algorithmic(wl, T)
+    dom = max((n for n in kern if n in alg), key=lambda n: kern[n])
+    bound, amount = alg[dom]
+    achieved = amount / (kern[dom] * 1e-3) / (1e9 if bound == "hbm" else 1e12)
+    peak = peaks["hbm_gbs"] if bound == "hbm" else peaks["bf16_tflops_sustained"]
+    traffic = None
+    t = NCU_TRAFFIC.get(dom)
+    if t and t[1] == wl.name and t[2] == source_sha(dom):
+        traffic = t[0]
+    roof = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak,
+            "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+            "peak_source": peak_src + (" (HBM copy)" if bound == "hbm" else " (cuBLAS bf16, sustained)"),
+            "algorithmic_per_launch": amount, "ms_per_launch": kern[dom]}
+    per_kernel = {}
+    for n, ms in sorted(kern.items(), key=lambda kv: -kv[1]):
+        e = {"ms": round(ms, 4), "share": round(ms / sum(kern.values()), 4)}
+        if n in alg:
+            b, a = alg[n]
+            e["achieved"] = round(a / (ms * 1e-3) / (1e9 if b == "hbm" else 1e12), 1)
+            e["unit"] = "GB/s" if b == "hbm" else "TFLOP/s"
+            e["frac"] = round(e["achieved"] / (peaks["hbm_gbs"] if b == "hbm" else peaks["bf16_tflops_sustained"]), 3)
+        per_kernel[n] = e
+    cpu = None
+    if world == 1:
+        v, cores, sample, el = cpu_baseline(wl)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
+               "seconds": round(el, 1)}
+    line = {"metric": METRIC, "value": tokens * world / (ms_step * 1e-3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+            "config": {"workload": wl.name, "step": "forward+backward", "tokens_per_gpu": tokens,
+                       "l2": "flushed between timed steps (write of 2x L2 outside the events)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "fwd_tokens_per_s": tokens * world / (ms_fwd * 1e-3), "ms_fwd": ms_fwd,
+            "roofline": roof, "kernels": per_kernel, "cpu_baseline": cpu,
+            "e2e": {"value": tokens * world / (ms_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="train2k", choices=sorted(workloads()))
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = workloads()[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    run_ours(args, wl, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

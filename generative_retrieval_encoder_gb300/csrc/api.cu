@@ -1,0 +1,568 @@
+// C ABI of the GBLA library (include/gbla.h): argument validation, workspace
+// layout, tiling choices and the launch sequence of every entry point.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/gbla.h"
+#include "kernels.h"
+
+using namespace gbla;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+constexpr int kSMs = 152;
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Everything derived from a shape: sequence form, tilings, buffer sizes.
+struct Plan {
+  bool f32;
+  int B, L, d, H, dh, T, n_seq, mode;
+  int HD, N1, NP;        // H*dh, 4*H*dh + H, N1 padded to 64
+  int chunk, chunk_per_seq, n_chunks;  // state-reduction chunks (grid.x)
+  int tile, tile_per_seq, n_tiles;     // readout / key-side tiles (grid.x)
+  int wsplit, n_wsplit;                // dW split over rows
+  int conv_blocks;
+  size_t io;             // bytes per io element
+};
+
+gbla_status make_plan(const gbla_shape* s, Plan& p) {
+  if (!s) return GBLA_ERR_INVALID_ARG;
+  if (s->io_dtype != GBLA_F32 && s->io_dtype != GBLA_BF16) return GBLA_ERR_INVALID_ARG;
+  if (s->gate != GBLA_GATE_SIGMOID && s->gate != GBLA_GATE_SOFTMAX) return GBLA_ERR_INVALID_ARG;
+  if (s->B < 1 || s->L < 1 || s->d < 1 || s->H < 1 || s->d_h < 1) return GBLA_ERR_INVALID_ARG;
+  if (!(s->rms_eps >= 0.f)) return GBLA_ERR_INVALID_ARG;
+  if (s->cu_seqlens && s->seq_lens) return GBLA_ERR_INVALID_ARG;
+  if (s->cu_seqlens && (s->B != 1 || s->num_seqs < 1)) return GBLA_ERR_INVALID_ARG;
+  p.f32 = s->io_dtype == GBLA_F32;
+  p.io = p.f32 ? 4 : 2;
+  p.B = s->B; p.L = s->L; p.d = s->d; p.H = s->H; p.dh = s->d_h;
+  if (p.f32) {
+    if (p.dh % 4 != 0 || p.dh > 128) return GBLA_ERR_UNSUPPORTED;
+  } else {
+    if (p.dh != 32 && p.dh != 64 && p.dh != 128) return GBLA_ERR_UNSUPPORTED;
+  }
+  const long long T = s->cu_seqlens ? (long long)s->L : (long long)s->B * s->L;
+  if (T > (8LL << 20)) return GBLA_ERR_UNSUPPORTED;  // grid rows of the GEMMs
+  if ((long long)s->H * s->d_h > 65536) return GBLA_ERR_UNSUPPORTED;
+  p.T = (int)T;
+  p.mode = s->cu_seqlens ? SEQ_VARLEN : (s->seq_lens ? SEQ_PADDED : SEQ_DENSE);
+  p.n_seq = s->cu_seqlens ? s->num_seqs : s->B;
+  p.HD = p.H * p.dh;
+  p.N1 = 4 * p.HD + p.H;
+  p.NP = (p.N1 + 63) / 64 * 64;
+  const int pairs = p.n_seq * p.H;
+  const int target = kSMs * 8;
+  if (p.mode == SEQ_VARLEN) {
+    const long long want = ((long long)p.T * p.H + target - 1) / target;
+    p.chunk = (int)std::min<long long>(2048, std::max<long long>(256, (want + 63) / 64 * 64));
+    p.chunk_per_seq = 0;
+    p.n_chunks = cdiv(p.T, p.chunk) + p.n_seq;
+  } else {
+    int per = std::max(1, std::min(cdiv(target, pairs), cdiv(p.L, 64)));
+    p.chunk = cdiv(cdiv(p.L, per), 64) * 64;
+    p.chunk_per_seq = cdiv(p.L, p.chunk);
+    p.n_chunks = p.chunk_per_seq * p.n_seq;
+  }
+  p.tile = p.f32 ? 64 : (p.dh == 128 ? 128 : 256);
+  if (p.mode == SEQ_VARLEN) {
+    p.tile_per_seq = 0;
+    p.n_tiles = cdiv(p.T, p.tile) + p.n_seq;
+  } else {
+    p.tile_per_seq = cdiv(p.L, p.tile);
+    p.n_tiles = p.tile_per_seq * p.n_seq;
+  }
+  // dW = x~^T dP: split the T rows so that d/128 x NP/128 tiles x splits fill the GPU
+  const int tiles = cdiv(p.d, 128) * cdiv(p.NP, 128);
+  const int want_split = std::max(1, std::min(cdiv(2 * kSMs, tiles), cdiv(p.T, 1024)));
+  p.wsplit = cdiv(cdiv(p.T, want_split), 64) * 64;
+  p.n_wsplit = cdiv(p.T, p.wsplit);
+  p.conv_blocks = conv_bwd_blocks(p.T);
+  return GBLA_OK;
+}
+
+gbla_status check_layer_shape(const Plan& p) {
+  if (p.d % (p.f32 ? 4 : 64) != 0) return GBLA_ERR_UNSUPPORTED;
+  return GBLA_OK;
+}
+
+// Byte layout of a workspace (or of the saved buffer), in order.
+struct Layout {
+  size_t err, cnt_f, cnt_b, pre_c, pre_t;
+  size_t partial, partial_m, state, state_bf, state_m, center;
+  size_t xt, P, gate, Wt;
+  size_t Wp, dP, dxt, dW, dstate, dstate_bf, gamma_part, bg_part, conv_part;
+  size_t total;
+};
+
+struct Cursor {
+  size_t off = 0;
+  size_t take(size_t bytes) { const size_t o = off; off = align_up(off + bytes); return o; }
+};
+
+
+size_t state_bytes(const Plan& p) { return (size_t)p.n_seq * p.H * p.dh * state_ld(p.dh) * 4; }
+size_t state_bf_bytes(const Plan& p) { return (size_t)p.n_seq * p.H * p.dh * state_bf_ld(p.dh) * 2; }
+
+// Saved activations of a training forward: x~, P = [q|k|v|r], gate, state.
+struct SavedLayout { size_t xt, P, gate, state, state_bf, state_m, center, total; };
+size_t center_bytes(const Plan& p) { return (size_t)p.n_seq * p.H * p.dh * 4; }
+SavedLayout saved_layout(const Plan& p) {
+  Cursor c;
+  SavedLayout s;
+  s.xt = c.take((size_t)p.T * p.d * p.io);
+  s.P = c.take((size_t)p.T * 4 * p.HD * p.io);
+  s.gate = c.take((size_t)p.T * p.H * 4);
+  s.state = c.take(state_bytes(p));
+  s.state_bf = c.take(state_bf_bytes(p));
+  s.state_m = c.take((size_t)p.n_seq * p.H * 4);
+  s.center = c.take(center_bytes(p));
+  s.total = c.off;
+  return s;
+}
+
+Layout ws_layout(const Plan& p, int op) {
+  Cursor c;
+  Layout l;
+  std::memset(&l, 0xff, sizeof(l));
+  const size_t cnt = (size_t)p.n_seq * p.H * 4;
+  l.err = c.take(16 + 2 * cnt);  // err word, then forward and backward counters
+  l.cnt_f = l.err + 16;
+  l.cnt_b = l.cnt_f + cnt;
+  if (p.mode == SEQ_VARLEN) {
+    l.pre_c = c.take((size_t)(p.n_seq + 1) * 4);
+    l.pre_t = c.take((size_t)(p.n_seq + 1) * 4);
+  }
+  l.partial = c.take((size_t)p.n_chunks * p.H * p.dh * state_ld(p.dh) * 4);
+  l.partial_m = c.take((size_t)p.n_chunks * p.H * 4);
+  if (op == GBLA_OP_FORWARD) {  // inference forward keeps its activations here
+    l.state = c.take(state_bytes(p));
+    l.state_bf = c.take(state_bf_bytes(p));
+    l.state_m = c.take((size_t)p.n_seq * p.H * 4);
+    l.center = c.take(center_bytes(p));
+    l.xt = c.take((size_t)p.T * p.d * p.io);
+    l.P = c.take((size_t)p.T * 4 * p.HD * p.io);
+    l.gate = c.take((size_t)p.T * p.H * 4);
+    l.Wt = c.take((size_t)p.N1 * p.d * p.io);
+  } else if (op == GBLA_OP_BACKWARD) {
+    l.Wp = c.take((size_t)p.d * p.NP * p.io);
+    l.dP = c.take((size_t)p.T * p.NP * p.io);
+    l.dxt = c.take((size_t)p.T * p.d * 4);
+    l.dW = c.take((size_t)p.n_wsplit * p.d * p.NP * 4);
+    l.dstate = c.take(state_bytes(p));
+    l.dstate_bf = c.take(state_bf_bytes(p));
+    l.gamma_part = c.take((size_t)p.n_chunks * p.H * p.dh * 4);
+    l.bg_part = c.take((size_t)p.n_tiles * p.H * 4);
+    l.conv_part = c.take((size_t)p.conv_blocks * p.d * 5 * 4);
+  } else {  // core forward / backward
+    l.state = c.take(state_bytes(p));
+    l.state_bf = c.take(state_bf_bytes(p));
+    l.state_m = c.take((size_t)p.n_seq * p.H * 4);
+    l.center = c.take(center_bytes(p));
+    if (op == GBLA_OP_CORE_BACKWARD) {
+      l.dstate = c.take(state_bytes(p));
+      l.dstate_bf = c.take(state_bf_bytes(p));
+    }
+  }
+  l.total = c.off;
+  return l;
+}
+
+template <typename T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+
+gbla_status cuda_fail(cudaError_t e, const char* what) {
+  g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+  return GBLA_ERR_CUDA;
+}
+
+// Per-launch timing (gbla_profiling_*): when on, every launch of this thread
+// is bracketed by two CUDA events recorded on the call's stream.
+struct ProfRecord { const char* name; cudaEvent_t t0, t1; };
+struct Profiler {
+  bool on = false;
+  std::vector<ProfRecord> rec;
+  std::vector<cudaEvent_t> pool;
+  cudaEvent_t event() {
+    if (!pool.empty()) { cudaEvent_t e = pool.back(); pool.pop_back(); return e; }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+};
+thread_local Profiler g_prof;
+
+#define GBLA_CHECK(call, what)                                         \
+  do {                                                                 \
+    cudaEvent_t t0_ = nullptr;                                         \
+    if (g_prof.on) { t0_ = g_prof.event(); cudaEventRecord(t0_, c.st); } \
+    cudaError_t e_ = (call);                                           \
+    if (g_prof.on) {                                                   \
+      cudaEvent_t t1_ = g_prof.event();                                \
+      cudaEventRecord(t1_, c.st);                                      \
+      g_prof.rec.push_back({what, t0_, t1_});                          \
+    }                                                                  \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what);                 \
+  } while (0)
+
+struct Ctx {
+  Plan p;
+  Layout l;
+  SeqDesc seq;
+  Tiling chunks, tiles;
+  int* err;
+  cudaStream_t st;
+};
+
+gbla_status begin(const gbla_shape* s, int op, void* ws, size_t ws_bytes, void* stream, Ctx& c) {
+  gbla_status r = make_plan(s, c.p);
+  if (r != GBLA_OK) return r;
+  c.l = ws_layout(c.p, op);
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0 || ws_bytes < c.l.total) return GBLA_ERR_WORKSPACE;
+  c.st = static_cast<cudaStream_t>(stream);
+  const Plan& p = c.p;
+  c.seq.mode = p.mode;
+  c.seq.n_seq = p.n_seq;
+  c.seq.L = p.mode == SEQ_VARLEN ? p.T : p.L;
+  c.seq.T = p.T;
+  c.seq.lens = s->seq_lens;
+  c.seq.cu = s->cu_seqlens;
+  c.chunks.tile = p.chunk;
+  c.chunks.per_seq = p.chunk_per_seq;
+  c.chunks.prefix = p.mode == SEQ_VARLEN ? at<int32_t>(ws, c.l.pre_c) : nullptr;
+  c.tiles.tile = p.tile;
+  c.tiles.per_seq = p.tile_per_seq;
+  c.tiles.prefix = p.mode == SEQ_VARLEN ? at<int32_t>(ws, c.l.pre_t) : nullptr;
+  c.err = at<int>(ws, c.l.err);
+  GBLA_CHECK(cudaMemsetAsync(ws, 0, c.l.cnt_b + (size_t)p.n_seq * p.H * 4 - c.l.err, c.st), "memset");
+  if (p.mode != SEQ_DENSE) {
+    const int ts[2] = {p.chunk, p.tile};
+    int32_t* pre[2] = {const_cast<int32_t*>(c.chunks.prefix), const_cast<int32_t*>(c.tiles.prefix)};
+    GBLA_CHECK(launch_plan(c.seq, p.mode == SEQ_VARLEN ? 2 : 0, ts, pre, c.err, c.st), "plan");
+  }
+  return GBLA_OK;
+}
+
+// State reduction + combine.  The bf16 path centres the state on the
+// k~-weighted mean of v (center); the fp32 path keeps it uncentred.
+gbla_status run_reduce(Ctx& c, const void* k, const void* v, int64_t ld, const float* g, int gate_kind, float* state,
+                       bf16* state_bf, float* state_m, float* pub_state, float* center, void* ws) {
+  const Plan& p = c.p;
+  ReduceArgs a{};
+  a.k = k; a.v = v; a.ldk = ld; a.ldv = ld;
+  a.g = g; a.ldg = p.H; a.gate_kind = gate_kind;
+  a.H = p.H; a.dh = p.dh;
+  a.seq = c.seq; a.chunks = c.chunks;
+  a.partial = at<float>(ws, c.l.partial);
+  a.partial_m = at<float>(ws, c.l.partial_m);
+  a.counters = at<int>(ws, c.l.cnt_f);
+  a.state = state; a.state_bf = state_bf; a.state_m = state_m; a.pub_state = pub_state;
+  a.center = p.f32 ? nullptr : center;
+  a.err = c.err;
+  GBLA_CHECK(p.f32 ? launch_reduce_f32(a, p.n_chunks, c.st) : launch_reduce_bf16(a, p.n_chunks, c.st), "reduce");
+  return GBLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gbla_status gbla_validate_shape(const gbla_shape* shape) {
+  Plan p;
+  return make_plan(shape, p);
+}
+
+size_t gbla_workspace_size(const gbla_shape* shape, int op) {
+  Plan p;
+  if (make_plan(shape, p) != GBLA_OK) return 0;
+  if (op < GBLA_OP_FORWARD || op > GBLA_OP_CORE_BACKWARD) return 0;
+  return ws_layout(p, op).total;
+}
+
+size_t gbla_saved_size(const gbla_shape* shape) {
+  Plan p;
+  if (make_plan(shape, p) != GBLA_OK) return 0;
+  return saved_layout(p).total;
+}
+
+gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* conv_w, const void* conv_b,
+                         const void* W_q, const void* W_k, const void* W_v, const void* W_r, const void* w_g,
+                         const void* b_g, const void* rms_w, void* y, void* saved, void* ws, size_t ws_bytes,
+                         void* stream) {
+  Plan p0;
+  gbla_status r = make_plan(shape, p0);
+  if (r != GBLA_OK) return r;
+  if ((r = check_layer_shape(p0)) != GBLA_OK) return r;
+  const void* req[] = {x, conv_w, W_q, W_k, W_v, W_r, w_g, y};
+  for (const void* q : req)
+    if (!q || !aligned16(q)) return GBLA_ERR_INVALID_ARG;
+  for (const void* q : {conv_b, b_g, rms_w})
+    if (q && !aligned16(q)) return GBLA_ERR_INVALID_ARG;
+  if (saved && (reinterpret_cast<uintptr_t>(saved) % kAlign) != 0) return GBLA_ERR_INVALID_ARG;
+  Ctx c;
+  if ((r = begin(shape, GBLA_OP_FORWARD, ws, ws_bytes, stream, c)) != GBLA_OK) return r;
+  const Plan& p = c.p;
+  const Layout& l = c.l;
+  void *xt, *P;
+  float *gate, *state, *state_m, *center;
+  bf16* state_bf;
+  if (saved) {
+    const SavedLayout s = saved_layout(p);
+    xt = at<char>(saved, s.xt); P = at<char>(saved, s.P); gate = at<float>(saved, s.gate);
+    state = at<float>(saved, s.state); state_bf = at<bf16>(saved, s.state_bf); state_m = at<float>(saved, s.state_m);
+    center = at<float>(saved, s.center);
+  } else {
+    xt = at<char>(ws, l.xt); P = at<char>(ws, l.P); gate = at<float>(ws, l.gate);
+    state = at<float>(ws, l.state); state_bf = at<bf16>(ws, l.state_bf); state_m = at<float>(ws, l.state_m);
+    center = at<float>(ws, l.center);
+  }
+  if (p.f32) center = nullptr;
+  // Eq. 4: conv
+  ConvArgs ca{};
+  ca.x = x; ca.w = conv_w; ca.b = conv_b; ca.xt = xt; ca.T = p.T; ca.d = p.d; ca.seq = c.seq; ca.err = c.err;
+  GBLA_CHECK(launch_conv_fwd(ca, p.f32, c.st), "conv");
+  // Eq. 4, 5, 7: projections and gate
+  const void* W[4] = {W_q, W_k, W_v, W_r};
+  void* Wt = at<char>(ws, l.Wt);
+  GBLA_CHECK(launch_pack_weights(W, w_g, p.d, p.H, p.dh, p.f32, Wt, nullptr, p.N1, c.st), "pack");
+  GemmArgs ga{};
+  ga.A = xt; ga.lda = p.d; ga.a_kmajor = 1;
+  ga.B = Wt; ga.ldb = p.d; ga.b_kmajor = 1;
+  ga.C = P; ga.ldc = 4 * p.HD;
+  ga.M = p.T; ga.N = p.N1; ga.K = p.d; ga.k_split = (p.d + 31) / 32 * 32;
+  ga.epi = EPI_PROJ; ga.n_main = 4 * p.HD; ga.bias_g = shape->gate == GBLA_GATE_SIGMOID ? b_g : nullptr;
+  ga.gate_mode = shape->gate == GBLA_GATE_SIGMOID ? 0 : 1; ga.gate = gate; ga.ldgate = p.H; ga.io_f32 = p.f32;
+  GBLA_CHECK(p.f32 ? launch_gemm_f32(ga, c.st) : launch_gemm_bf16(ga, c.st), "projection gemm");
+  // Eq. 5/6: state
+  const size_t es = p.io;
+  const char* Pc = static_cast<const char*>(P);
+  r = run_reduce(c, Pc + p.HD * es, Pc + 2 * p.HD * es, 4 * p.HD, gate,
+                 shape->gate == GBLA_GATE_SIGMOID ? GATE_VALUES : GATE_LOGITS, state, state_bf, state_m, nullptr,
+                 center, ws);
+  if (r != GBLA_OK) return r;
+  // Eq. 5/6 readout fused with Eq. 7
+  ReadoutArgs ra{};
+  ra.q = P; ra.ldq = 4 * p.HD;
+  ra.r = Pc + 3 * p.HD * es; ra.ldr = 4 * p.HD;
+  ra.rms_w = rms_w; ra.eps = shape->rms_eps;
+  ra.state = state; ra.state_bf = state_bf; ra.center = center;
+  ra.out = y; ra.ldo = p.HD; ra.den = nullptr;
+  ra.H = p.H; ra.dh = p.dh; ra.seq = c.seq; ra.tiles = c.tiles; ra.err = c.err;
+  GBLA_CHECK(p.f32 ? launch_readout_f32(ra, true, p.n_tiles, c.st) : launch_readout_bf16(ra, true, p.n_tiles, c.st),
+             "readout");
+  return GBLA_OK;
+}
+
+gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* conv_w, const void* conv_b,
+                          const void* W_q, const void* W_k, const void* W_v, const void* W_r, const void* w_g,
+                          const void* b_g, const void* rms_w, const void* saved, const void* dy, void* dx,
+                          float* dconv_w, float* dconv_b, float* dW_q, float* dW_k, float* dW_v, float* dW_r,
+                          float* dw_g, float* db_g, float* drms_w, void* ws, size_t ws_bytes, void* stream) {
+  (void)conv_b; (void)b_g;
+  Plan p0;
+  gbla_status r = make_plan(shape, p0);
+  if (r != GBLA_OK) return r;
+  if ((r = check_layer_shape(p0)) != GBLA_OK) return r;
+  const void* req[] = {x, conv_w, W_q, W_k, W_v, W_r, w_g, saved, dy, dx};
+  for (const void* q : req)
+    if (!q || !aligned16(q)) return GBLA_ERR_INVALID_ARG;
+  if (rms_w && !aligned16(rms_w)) return GBLA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(saved) % kAlign) != 0) return GBLA_ERR_INVALID_ARG;
+  Ctx c;
+  if ((r = begin(shape, GBLA_OP_BACKWARD, ws, ws_bytes, stream, c)) != GBLA_OK) return r;
+  const Plan& p = c.p;
+  const Layout& l = c.l;
+  const SavedLayout s = saved_layout(p);
+  const size_t es = p.io;
+  const char* P = at<const char>(const_cast<void*>(saved), s.P);
+  const void* xt = at<const char>(const_cast<void*>(saved), s.xt);
+  const float* gate = at<const float>(const_cast<void*>(saved), s.gate);
+  char* dP = at<char>(ws, l.dP);
+  const bool sig = shape->gate == GBLA_GATE_SIGMOID;
+  GBLA_CHECK(cudaMemsetAsync(at<char>(ws, l.gamma_part), 0, (size_t)p.n_chunks * p.H * p.dh * 4, c.st), "memset");
+  GBLA_CHECK(cudaMemsetAsync(at<char>(ws, l.bg_part), 0, (size_t)p.n_tiles * p.H * 4, c.st), "memset");
+  const void* W[4] = {W_q, W_k, W_v, W_r};
+  GBLA_CHECK(launch_pack_weights(W, w_g, p.d, p.H, p.dh, p.f32, nullptr, at<char>(ws, l.Wp), p.NP, c.st), "pack");
+  // Eq. 7 + Eq. 5/6 query side: dr, dq, [dS | dz]
+  BwdQArgs q{};
+  q.q = P; q.ldq = 4 * p.HD;
+  q.r = P + 3 * p.HD * es; q.ldr = 4 * p.HD;
+  q.dy = dy; q.lddy = p.HD;
+  q.rms_w = rms_w; q.eps = shape->rms_eps;
+  q.state = at<const float>(const_cast<void*>(saved), s.state);
+  q.state_bf = at<const bf16>(const_cast<void*>(saved), s.state_bf);
+  const float* center = p.f32 ? nullptr : at<const float>(const_cast<void*>(saved), s.center);
+  q.center = center;
+  q.dq = dP; q.lddq = p.NP;
+  q.dr = dP + 3 * p.HD * es; q.lddr = p.NP;
+  q.gamma_part = at<float>(ws, l.gamma_part);
+  q.partial = at<float>(ws, l.partial); q.counters = at<int>(ws, l.cnt_b);
+  q.dstate = at<float>(ws, l.dstate); q.dstate_bf = at<bf16>(ws, l.dstate_bf);
+  q.H = p.H; q.dh = p.dh; q.seq = c.seq; q.chunks = c.chunks; q.err = c.err;
+  GBLA_CHECK(p.f32 ? launch_bwd_q_f32(q, true, p.n_chunks, c.st) : launch_bwd_q_bf16(q, true, p.n_chunks, c.st),
+             "bwd_q");
+  // key side: dk, dv, ds
+  BwdKVArgs kv{};
+  kv.k = P + p.HD * es; kv.ldk = 4 * p.HD;
+  kv.v = P + 2 * p.HD * es; kv.ldv = 4 * p.HD;
+  kv.g = gate; kv.ldg = p.H; kv.gate_kind = sig ? GATE_VALUES : GATE_LOGITS;
+  kv.state_m = at<const float>(const_cast<void*>(saved), s.state_m);
+  kv.dstate = at<float>(ws, l.dstate); kv.dstate_bf = at<bf16>(ws, l.dstate_bf);
+  kv.center = center;
+  kv.dk = dP + p.HD * es; kv.lddk = p.NP;
+  kv.dv = dP + 2 * p.HD * es; kv.lddv = p.NP;
+  kv.ds = dP; kv.ldds = p.NP; kv.gate_grad = sig ? GG_SIGMOID : GG_SOFTMAX;
+  // ds of head h lands in column 4*H*dh + h: offset the pointer, keep the stride
+  kv.ds = dP + (size_t)4 * p.HD * es;
+  kv.zero_cols_from = p.N1 - 4 * p.HD; kv.zero_cols_to = p.NP - 4 * p.HD;
+  kv.bg_part = at<float>(ws, l.bg_part);
+  kv.H = p.H; kv.dh = p.dh; kv.seq = c.seq; kv.tiles = c.tiles; kv.err = c.err;
+  GBLA_CHECK(p.f32 ? launch_bwd_kv_f32(kv, p.n_tiles, c.st) : launch_bwd_kv_bf16(kv, p.n_tiles, c.st), "bwd_kv");
+  // Eq. 4 projections backward: dx~ = dP W_all^T, dW_all = x~^T dP
+  GemmArgs g1{};
+  g1.A = dP; g1.lda = p.NP; g1.a_kmajor = 1;
+  g1.B = at<char>(ws, l.Wp); g1.ldb = p.NP; g1.b_kmajor = 1;
+  g1.C = at<float>(ws, l.dxt); g1.ldc = p.d;
+  g1.M = p.T; g1.N = p.d; g1.K = p.NP; g1.k_split = p.NP; g1.epi = EPI_F32; g1.io_f32 = p.f32;
+  GBLA_CHECK(p.f32 ? launch_gemm_f32(g1, c.st) : launch_gemm_bf16(g1, c.st), "dx~ gemm");
+  GemmArgs g2{};
+  g2.A = xt; g2.lda = p.d; g2.a_kmajor = 0;
+  g2.B = dP; g2.ldb = p.NP; g2.b_kmajor = 0;
+  g2.C = at<float>(ws, l.dW); g2.ldc = p.NP;
+  g2.M = p.d; g2.N = p.NP; g2.K = p.T; g2.k_split = p.wsplit; g2.epi = EPI_SPLITK; g2.io_f32 = p.f32;
+  GBLA_CHECK(p.f32 ? launch_gemm_f32(g2, c.st) : launch_gemm_bf16(g2, c.st), "dW gemm");
+  float* outs[5] = {dW_q, dW_k, dW_v, dW_r, dw_g};
+  GBLA_CHECK(launch_scatter_dw(at<float>(ws, l.dW), p.n_wsplit, p.d, p.NP, p.H, p.dh, outs, c.st), "dW sum");
+  // Eq. 4 conv backward
+  ConvArgs ca{};
+  ca.x = x; ca.w = conv_w; ca.dxt = at<float>(ws, l.dxt); ca.dx = dx; ca.part = at<float>(ws, l.conv_part);
+  ca.T = p.T; ca.d = p.d; ca.seq = c.seq; ca.err = c.err;
+  GBLA_CHECK(launch_conv_bwd(ca, p.f32, p.conv_blocks, c.st), "conv bwd");
+  if (dconv_w || dconv_b)
+    GBLA_CHECK(launch_conv_param_grads(ca.part, p.conv_blocks, p.d, dconv_w, dconv_b, c.st), "conv grads");
+  if (drms_w)
+    GBLA_CHECK(launch_sum_parts(q.gamma_part, p.n_chunks * p.H, p.dh, p.dh, drms_w, c.st), "dgamma");
+  if (db_g)
+    GBLA_CHECK(launch_sum_parts(kv.bg_part, p.n_tiles, p.H, p.H, db_g, c.st), "db_g");
+  return GBLA_OK;
+}
+
+gbla_status bla_core_forward(const gbla_shape* shape, const void* q, const void* k, const void* v, const float* g,
+                             void* o, float* den, float* state, void* ws, size_t ws_bytes, void* stream) {
+  for (const void* ptr : {q, k, v, (const void*)g, (const void*)o})
+    if (!ptr || !aligned16(ptr)) return GBLA_ERR_INVALID_ARG;
+  for (const void* ptr : {(const void*)den, (const void*)state})
+    if (ptr && !aligned16(ptr)) return GBLA_ERR_INVALID_ARG;
+  Ctx c;
+  gbla_status r = begin(shape, GBLA_OP_CORE_FORWARD, ws, ws_bytes, stream, c);
+  if (r != GBLA_OK) return r;
+  const Plan& p = c.p;
+  float* st = at<float>(ws, c.l.state);
+  bf16* sbf = at<bf16>(ws, c.l.state_bf);
+  float* center = p.f32 ? nullptr : at<float>(ws, c.l.center);
+  r = run_reduce(c, k, v, p.HD, g, GATE_VALUES, st, sbf, at<float>(ws, c.l.state_m), state, center, ws);
+  if (r != GBLA_OK) return r;
+  ReadoutArgs ra{};
+  ra.q = q; ra.ldq = p.HD;
+  ra.state = st; ra.state_bf = sbf; ra.center = center;
+  ra.out = o; ra.ldo = p.HD; ra.den = den;
+  ra.H = p.H; ra.dh = p.dh; ra.seq = c.seq; ra.tiles = c.tiles; ra.err = c.err;
+  GBLA_CHECK(p.f32 ? launch_readout_f32(ra, false, p.n_tiles, c.st) : launch_readout_bf16(ra, false, p.n_tiles, c.st),
+             "readout");
+  return GBLA_OK;
+}
+
+gbla_status bla_core_backward(const gbla_shape* shape, const void* q, const void* k, const void* v, const float* g,
+                              const void* d_o, void* dq, void* dk, void* dv, float* dg, void* ws, size_t ws_bytes,
+                              void* stream) {
+  for (const void* ptr : {q, k, v, (const void*)g, d_o, (const void*)dq, (const void*)dk, (const void*)dv, (const void*)dg})
+    if (!ptr || !aligned16(ptr)) return GBLA_ERR_INVALID_ARG;
+  Ctx c;
+  gbla_status r = begin(shape, GBLA_OP_CORE_BACKWARD, ws, ws_bytes, stream, c);
+  if (r != GBLA_OK) return r;
+  const Plan& p = c.p;
+  float* st = at<float>(ws, c.l.state);
+  bf16* sbf = at<bf16>(ws, c.l.state_bf);
+  float* center = p.f32 ? nullptr : at<float>(ws, c.l.center);
+  r = run_reduce(c, k, v, p.HD, g, GATE_VALUES, st, sbf, at<float>(ws, c.l.state_m), nullptr, center, ws);
+  if (r != GBLA_OK) return r;
+  BwdQArgs a{};
+  a.q = q; a.ldq = p.HD; a.dy = d_o; a.lddy = p.HD;
+  a.state = st; a.state_bf = sbf; a.center = center;
+  a.dq = dq; a.lddq = p.HD;
+  a.partial = at<float>(ws, c.l.partial); a.counters = at<int>(ws, c.l.cnt_b);
+  a.dstate = at<float>(ws, c.l.dstate); a.dstate_bf = at<bf16>(ws, c.l.dstate_bf);
+  a.H = p.H; a.dh = p.dh; a.seq = c.seq; a.chunks = c.chunks; a.err = c.err;
+  GBLA_CHECK(p.f32 ? launch_bwd_q_f32(a, false, p.n_chunks, c.st) : launch_bwd_q_bf16(a, false, p.n_chunks, c.st),
+             "bwd_q");
+  BwdKVArgs kv{};
+  kv.k = k; kv.ldk = p.HD; kv.v = v; kv.ldv = p.HD;
+  kv.g = g; kv.ldg = p.H; kv.gate_kind = GATE_VALUES;
+  kv.dstate = a.dstate; kv.dstate_bf = a.dstate_bf; kv.center = center;
+  kv.dk = dk; kv.lddk = p.HD; kv.dv = dv; kv.lddv = p.HD;
+  kv.ds = dg; kv.ldds = p.H; kv.gate_grad = GG_DG;
+  kv.H = p.H; kv.dh = p.dh; kv.seq = c.seq; kv.tiles = c.tiles; kv.err = c.err;
+  GBLA_CHECK(p.f32 ? launch_bwd_kv_f32(kv, p.n_tiles, c.st) : launch_bwd_kv_bf16(kv, p.n_tiles, c.st), "bwd_kv");
+  return GBLA_OK;
+}
+
+gbla_status gbla_check_device_status(const void* ws, void* stream) {
+  if (!ws) return GBLA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int err = 0;
+  cudaError_t e = cudaMemcpyAsync(&err, ws, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "check_device_status");
+  return err ? GBLA_ERR_DEVICE_CHECK : GBLA_OK;
+}
+
+const char* gbla_status_string(int status) {
+  switch (status) {
+    case GBLA_OK: return "GBLA_OK";
+    case GBLA_ERR_INVALID_ARG: return "GBLA_ERR_INVALID_ARG: null or misaligned pointer, or bad dimension";
+    case GBLA_ERR_UNSUPPORTED: return "GBLA_ERR_UNSUPPORTED: no kernel for this shape (d_h, d alignment or size)";
+    case GBLA_ERR_WORKSPACE: return "GBLA_ERR_WORKSPACE: workspace NULL, not 256-byte aligned, or too small";
+    case GBLA_ERR_CUDA: return "GBLA_ERR_CUDA: a CUDA call failed (see gbla_last_error)";
+    case GBLA_ERR_DEVICE_CHECK: return "GBLA_ERR_DEVICE_CHECK: bad cu_seqlens / seq_lens detected on the device";
+    default: return "unknown gbla_status";
+  }
+}
+
+const char* gbla_last_error(void) { return g_last_error.c_str(); }
+
+void gbla_profiling_enable(int on) { g_prof.on = on != 0; }
+
+int gbla_profiling_read(const char** names, float* ms, int cap) {
+  const int n = (int)g_prof.rec.size();
+  if (n > 0) cudaEventSynchronize(g_prof.rec.back().t1);
+  for (int i = 0; i < n; ++i) {
+    ProfRecord& r = g_prof.rec[i];
+    if (i < cap) {
+      float t = -1.f;
+      if (cudaEventElapsedTime(&t, r.t0, r.t1) != cudaSuccess) t = -1.f;
+      if (names) names[i] = r.name;
+      if (ms) ms[i] = t;
+    }
+    g_prof.pool.push_back(r.t0);
+    g_prof.pool.push_back(r.t1);
+  }
+  g_prof.rec.clear();
+  return n;
+}
+
+int gbla_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,124 @@
+// Pieces shared by the fp32 and bf16 state kernels: the deterministic
+// split-L combine of per-chunk partial states.
+#pragma once
+
+#include "kernels.h"
+
+namespace gbla {
+
+// Every CTA of a (sequence, head) calls this after writing its partial.  The
+// CTA that arrives last (atomic ticket; no CTA ever waits) gets `true` and
+// then owns the combine.  Counters are zeroed by the host before the launch.
+__device__ __forceinline__ bool arrive_last(int* counter, int count) {
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(counter, 1) == count - 1);
+  __syncthreads();
+  const bool last = s_last != 0;
+  if (last) __threadfence();
+  return last;
+}
+
+// state[seqh] = sum over the sequence's chunks c = 0 .. count-1, in that
+// order, of scale_c * partial[(first + c) * H + h].  scale_c = 1, or for
+// softmax logits exp(m_c - m) with m the largest chunk maximum (the softmax
+// normaliser cancels in Eq. 5, so only relative scales matter).
+// Also writes the compact public copy [dh][dh+1] of [S | z] and m.
+//
+// Centering (center != null): for any constant vector c,
+//   o_i = S^T q~_i / z.q~_i = c + (S - z c^T)^T q~_i / z.q~_i,
+// so the kernels may work with S' = S - z c^T.  With c the k~-weighted mean
+// of v, c_f = sum_e S[e][f] / sum_e z_e, S' holds only the spread of v around
+// its mean; the differences that the backward takes (S - z o^T, dS v + dz)
+// then no longer cancel in bf16 operands.  S' is formed here in fp32; c goes
+// to center[seqh][dh].  Then `state` and the bf16 copy hold [S' | z | 0].
+__device__ inline void combine_state(const float* partial, const float* partial_m, int first,
+                                     int count, int H, int h, int dh, int seqh, bool logits,
+                                     float* state, bf16* state_bf, float* state_m,
+                                     float* pub_state, float* center = nullptr) {
+  const int LD = state_ld(dh);
+  const int n = dh * LD;
+  float m = 0.f;
+  bool any = true;
+  if (logits) {
+    m = -INFINITY;
+    for (int c = 0; c < count; ++c) m = fmaxf(m, __ldcg(partial_m + (size_t)(first + c) * H + h));
+    any = m > -INFINITY;
+    if (threadIdx.x == 0 && state_m) state_m[seqh] = any ? m : 0.f;
+  }
+  const float4* P = reinterpret_cast<const float4*>(partial);
+  float4* S = reinterpret_cast<float4*>(state + (size_t)seqh * n);
+  for (int i = threadIdx.x; i < n / 4; i += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int c = 0;
+    for (; c + 4 <= count; c += 4) {
+      float4 p[4];
+      float sc[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        p[u] = __ldcg(P + ((size_t)(first + c + u) * H + h) * (n / 4) + i);
+        sc[u] = 1.f;
+        if (logits) {
+          const float mc = __ldcg(partial_m + (size_t)(first + c + u) * H + h);
+          sc[u] = (any && mc > -INFINITY) ? __expf(mc - m) : 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc.x += sc[u] * p[u].x; acc.y += sc[u] * p[u].y;
+        acc.z += sc[u] * p[u].z; acc.w += sc[u] * p[u].w;
+      }
+    }
+    for (; c < count; ++c) {
+      const float4 p = __ldcg(P + ((size_t)(first + c) * H + h) * (n / 4) + i);
+      float sc = 1.f;
+      if (logits) {
+        const float mc = __ldcg(partial_m + (size_t)(first + c) * H + h);
+        sc = (any && mc > -INFINITY) ? __expf(mc - m) : 0.f;
+      }
+      acc.x += sc * p.x; acc.y += sc * p.y; acc.z += sc * p.z; acc.w += sc * p.w;
+    }
+    S[i] = acc;
+    const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = (4 * i + u) / LD, f = (4 * i + u) % LD;
+      if (state_bf && !center) state_bf[((size_t)seqh * dh + e) * state_bf_ld(dh) + f] = __float2bfloat16_rn(v4[u]);
+      if (pub_state && f <= dh) pub_state[((size_t)seqh * dh + e) * (dh + 1) + f] = v4[u];
+    }
+  }
+  if (center) {
+    __shared__ float cbuf[128];
+    float* St = state + (size_t)seqh * n;
+    __syncthreads();  // this CTA's state writes are visible to the whole CTA
+    float Z = 0.f;
+    for (int e = 0; e < dh; ++e) Z += St[e * LD + dh];
+    for (int f = threadIdx.x; f < dh; f += blockDim.x) {
+      float s = 0.f;
+      for (int e = 0; e < dh; ++e) s += St[e * LD + f];
+      const float c = Z > 0.f ? s / Z : 0.f;
+      cbuf[f] = c;
+      center[(size_t)seqh * dh + f] = c;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const int e = i / LD, f = i % LD;
+      float v = St[i];
+      if (f < dh) {
+        v -= St[e * LD + dh] * cbuf[f];
+      }
+      if (state_bf) state_bf[((size_t)seqh * dh + e) * state_bf_ld(dh) + f] = __float2bfloat16_rn(v);
+      St[i] = v;  // the z column (f == dh), which other threads read, is left unchanged
+    }
+  }
+  if (state_bf) {
+    const int BLD = state_bf_ld(dh);
+    for (int i = threadIdx.x; i < dh * (BLD - LD); i += blockDim.x) {
+      const int e = i / (BLD - LD), f = LD + i % (BLD - LD);
+      state_bf[((size_t)seqh * dh + e) * BLD + f] = __float2bfloat16_rn(0.f);
+    }
+  }
+}
+
+}  // namespace gbla

@@ -1,0 +1,159 @@
+// Internal interface between the C-ABI host code (api.cu) and the kernels.
+// Every launcher returns the cudaError_t of its launch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace gbla {
+
+// Row stride (floats) of fp32 state / partial tiles: [S | z | 0 x 7].
+__host__ __device__ constexpr int state_ld(int dh) { return dh + 8; }
+// Row stride (elements) of the bf16 copy of [S | z | 0 x 15].
+__host__ __device__ constexpr int state_bf_ld(int dh) { return dh + 16; }
+
+// Gate input kinds of the state reduction and of the key-side backward.
+enum GateKind {
+  GATE_VALUES = 0,   // g holds gate values g_j >= 0
+  GATE_LOGITS = 1,   // g holds softmax logits s_j; the kernels use exp(s_j - m)
+};
+// What the key-side backward writes in its gate-gradient slot.
+enum GateGrad {
+  GG_DG = 0,         // dL/dg (core API), fp32
+  GG_SIGMOID = 1,    // dL/ds = dg g (1 - g), io dtype into the dP buffer
+  GG_SOFTMAX = 2,    // dL/ds = g' dg with g' = exp(s - m), io dtype into dP
+};
+
+struct ReduceArgs {
+  const void* k; const void* v; int64_t ldk, ldv;  // [rows, ld], head h at column h*dh
+  const float* g; int64_t ldg; int gate_kind;
+  int H, dh;
+  SeqDesc seq; Tiling chunks;
+  float* partial;     // [chunks*H][dh][state_ld]
+  float* partial_m;   // [chunks*H]          (GATE_LOGITS)
+  int* counters;      // [n_seq*H], zero on entry
+  float* state;       // [n_seq*H][dh][state_ld]
+  bf16* state_bf;     // [n_seq*H][dh][state_bf_ld]   (bf16 kernels)
+  float* state_m;     // [n_seq*H]           (GATE_LOGITS)
+  float* pub_state;   // [n_seq, H, dh, dh+1] or null
+  float* center;      // [n_seq*H][dh] or null: centre the state (see combine_state)
+  const int* err;
+};
+
+struct ReadoutArgs {
+  const void* q; int64_t ldq;
+  const void* r; int64_t ldr;       // norm only
+  const void* rms_w; float eps;     // norm only; rms_w may be null
+  const float* state; const bf16* state_bf;
+  const float* center;              // [n_seq*H][dh] or null (state is uncentred)
+  void* out; int64_t ldo;
+  float* den;                       // [rows, H] or null
+  int H, dh;
+  SeqDesc seq; Tiling tiles;
+  const int* err;
+};
+
+struct BwdQArgs {
+  const void* q; int64_t ldq;
+  const void* r; int64_t ldr;       // norm only
+  const void* dy; int64_t lddy;     // norm: dy; core: d_o
+  const void* rms_w; float eps;
+  const float* state; const bf16* state_bf;
+  const float* center;              // [n_seq*H][dh] or null (state is uncentred)
+  void* dq; int64_t lddq;
+  void* dr; int64_t lddr;           // norm only
+  float* gamma_part;                // norm only: [gridDim.x * H][dh]
+  float* partial; int* counters;    // dS partials, [n_seq*H] counters
+  float* dstate; bf16* dstate_bf;   // combined [dS | dz]
+  int H, dh;
+  SeqDesc seq; Tiling chunks;
+  const int* err;
+};
+
+struct BwdKVArgs {
+  const void* k; int64_t ldk;
+  const void* v; int64_t ldv;
+  const float* g; int64_t ldg; int gate_kind;  // GateKind
+  const float* state_m;                         // GATE_LOGITS
+  const float* dstate; const bf16* dstate_bf;
+  const float* center;                         // centre of the forward state, or null
+  void* dk; int64_t lddk;
+  void* dv; int64_t lddv;
+  void* ds; int64_t ldds; int gate_grad;       // GateGrad
+  float* bg_part;                              // [gridDim.x * H] or null
+  int zero_cols_from, zero_cols_to;            // dP pad columns to clear (head 0 CTAs)
+  int H, dh;
+  SeqDesc seq; Tiling tiles;
+  const int* err;
+};
+
+// C[M, N] (+)= sum_k A(m, k) B(n, k).  A is [M][K] (a_kmajor) or [K][M];
+// B is [N][K] (b_kmajor) or [K][N].  blockIdx.z splits K into chunks of
+// k_split (a multiple of the K tile).
+enum GemmEpi {
+  EPI_BF16 = 0,       // C bf16
+  EPI_F32 = 1,        // C fp32
+  EPI_SPLITK = 2,     // fp32 partial C + z * M * ldc
+  EPI_PROJ = 3,       // columns < n_main -> bf16 C; the next H columns -> gate (fp32)
+};
+struct GemmArgs {
+  const void* A; int64_t lda; int a_kmajor;
+  const void* B; int64_t ldb; int b_kmajor;
+  void* C; int64_t ldc;
+  int M, N, K, k_split;
+  int epi;
+  // EPI_PROJ
+  int n_main; const void* bias_g; int gate_mode; float* gate; int64_t ldgate;
+  int io_f32;
+};
+
+struct ConvArgs {
+  const void* x; const void* w; const void* b;  // io dtype; b may be null
+  void* xt;                                     // io dtype [T, d]
+  const float* dxt;                             // backward: fp32 [T, d]
+  void* dx;                                     // backward: io dtype [T, d]
+  float* part;                                  // backward: [gridDim.x][d][5] (dw 0..3, db)
+  int T, d;
+  SeqDesc seq;
+  const int* err;
+};
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_plan(const SeqDesc& s, int ntile, const int* tile_sizes, int32_t* const* prefixes,
+                        int* err, cudaStream_t st);
+
+cudaError_t launch_reduce_bf16(const ReduceArgs& a, int grid_x, cudaStream_t st);
+cudaError_t launch_readout_bf16(const ReadoutArgs& a, bool norm, int grid_x, cudaStream_t st);
+cudaError_t launch_bwd_q_bf16(const BwdQArgs& a, bool norm, int grid_x, cudaStream_t st);
+cudaError_t launch_bwd_kv_bf16(const BwdKVArgs& a, int grid_x, cudaStream_t st);
+
+cudaError_t launch_reduce_f32(const ReduceArgs& a, int grid_x, cudaStream_t st);
+cudaError_t launch_readout_f32(const ReadoutArgs& a, bool norm, int grid_x, cudaStream_t st);
+cudaError_t launch_bwd_q_f32(const BwdQArgs& a, bool norm, int grid_x, cudaStream_t st);
+cudaError_t launch_bwd_kv_f32(const BwdKVArgs& a, int grid_x, cudaStream_t st);
+
+cudaError_t launch_gemm_bf16(const GemmArgs& a, cudaStream_t st);
+cudaError_t launch_gemm_f32(const GemmArgs& a, cudaStream_t st);
+
+cudaError_t launch_conv_fwd(const ConvArgs& a, bool f32, cudaStream_t st);
+cudaError_t launch_conv_bwd(const ConvArgs& a, bool f32, int nblk, cudaStream_t st);
+int conv_bwd_blocks(int T);
+
+// Packs W_q | W_k | W_v | W_r | w_g into Wt [N1][d] (transposed, N1 = 4*H*dh + H)
+// and/or Wp [d][np] (row-major, zero-padded to np columns).  Either may be null.
+cudaError_t launch_pack_weights(const void* const* W, const void* w_g, int d, int H, int dh,
+                                bool f32, void* Wt, void* Wp, int np, cudaStream_t st);
+
+// out[i] = sum_{s < S} part[s * stride + i] for i < n (fixed order); fp32.
+cudaError_t launch_sum_parts(const float* part, int S, int64_t stride, int64_t n, float* out,
+                             cudaStream_t st);
+// Weight-gradient scatter: dW (fp32 [d][np]) -> dW_q, dW_k, dW_v, dW_r [d][H*dh], dw_g [d][H].
+cudaError_t launch_scatter_dw(const float* part, int S, int d, int np, int H, int dh,
+                              float* const* outs, cudaStream_t st);
+// Conv parameter gradients from per-block partials [S][d][5].
+cudaError_t launch_conv_param_grads(const float* part, int S, int d, float* dw, float* db,
+                                    cudaStream_t st);
+
+}  // namespace gbla

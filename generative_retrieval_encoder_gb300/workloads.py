@@ -53,7 +53,10 @@ class Workload:
 
     # ---------------------------------------------------------------- shapes
     def lengths(self) -> list[int]:
-        """Sequence lengths (varlen form), or None for the dense/padded forms."""
+        """Sequence lengths (varlen form), or None for the dense/padded forms.
+        ``extra["lengths"]`` fixes them explicitly."""
+        if self.extra.get("lengths") is not None:
+            return list(self.extra["lengths"])
         if self.varlen is None:
             return None
         n, lo, hi = self.varlen
@@ -75,7 +78,7 @@ class Workload:
         return cu[-1] if cu is not None else self.B * self.L
 
     def valid_tokens(self) -> int:
-        if self.varlen is not None:
+        if self.lengths() is not None:
             return self.total_tokens()
         if self.seq_lens is not None:
             return int(sum(self.seq_lens))

@@ -321,8 +321,8 @@ void oracle_conv1d(int64_t T, int d, int n_seq, const int64_t* start,
 static void project(int d, int n, int n_seq, const int64_t* start,
                     const int64_t* len, const double* xt, const double* W,
                     double* out) {
-#pragma omp parallel for schedule(dynamic)
   for (int b = 0; b < n_seq; ++b)
+#pragma omp parallel for schedule(static)
     for (int64_t t = start[b]; t < start[b] + len[b]; ++t)
       for (int j = 0; j < n; ++j) {
         double acc = 0.0;
@@ -535,8 +535,8 @@ int oracle_gbla_backward(int64_t T, int d, int H, int dh, int n_seq,
     const double* Ws[4] = {Wq, Wk, Wv, Wr};
     const double* dPs[4] = {dq, dk, dv, dr};
     double* dWs[4] = {dWq, dWk, dWv, dWr};
-#pragma omp parallel for schedule(dynamic)
     for (int b = 0; b < n_seq; ++b)
+#pragma omp parallel for schedule(static)
       for (int64_t t = start[b]; t < start[b] + len[b]; ++t)
         for (int c = 0; c < d; ++c) {
           double acc = 0.0;
