@@ -23,7 +23,9 @@ GBLA_OP_FORWARD, GBLA_OP_BACKWARD, GBLA_OP_CORE_FORWARD, GBLA_OP_CORE_BACKWARD =
 
 EXPORTS = ("gbla_workspace_size", "gbla_saved_size", "gbla_validate_shape", "gbla_forward", "gbla_backward",
            "bla_core_forward", "bla_core_backward", "gbla_check_device_status", "gbla_status_string",
-           "gbla_last_error", "gbla_version", "gbla_profiling_enable", "gbla_profiling_read")
+           "gbla_last_error", "gbla_version", "gbla_profiling_enable", "gbla_profiling_read",
+           "bla_core_forward_noalloc")
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class GblaError(RuntimeError):
@@ -68,6 +70,8 @@ def lib() -> ctypes.CDLL:
         L.bla_core_forward.restype = ctypes.c_int
         L.bla_core_backward.argtypes = [sp] + [vp] * 10 + [sz, vp]
         L.bla_core_backward.restype = ctypes.c_int
+        L.bla_core_forward_noalloc.argtypes = [sp] + [vp] * 8
+        L.bla_core_forward_noalloc.restype = ctypes.c_int
         L.gbla_check_device_status.argtypes = [vp, vp]
         L.gbla_check_device_status.restype = ctypes.c_int
         L.gbla_status_string.argtypes = [ctypes.c_int]
@@ -210,6 +214,15 @@ def bla_core_forward(shape: Shape, q, k, v, g, o=None, den=None, state=None, ws=
                                 _stream())
     _check(st, "bla_core_forward")
     return o, den, state
+
+
+def bla_core_forward_noalloc(shape: Shape, q, k, v, g, o, den=None, state=None) -> int:
+    """bla_core_forward with the library's fixed 64 MiB device scratch instead
+    of a workspace, for callers that cannot allocate; o (and den / state when
+    given) must already exist.  Returns the status (GBLA_ERR_WORKSPACE when the
+    shape needs more scratch than the fixed array holds)."""
+    return lib().bla_core_forward_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(o),
+                                          _ptr(den), _ptr(state), _stream())
 
 
 def bla_core_backward(shape: Shape, q, k, v, g, d_o, ws=None):

@@ -173,6 +173,35 @@ gbla_status bla_core_backward(const gbla_shape* shape, const void* q,
                               float* dg, void* ws, size_t ws_bytes,
                               void* stream);
 
+/*
+ * bla_core_forward without a caller workspace (the pages have no counterpart:
+ * this is a deployment convenience).  Some callers cannot call cudaMalloc or
+ * hand the library a scratch buffer: a plugin running inside a host framework
+ * that owns all device memory through its own pool and passes only its
+ * tensors, or a latency-bound serving loop where an allocation would
+ * synchronise the device and stall the other streams.  This entry point
+ * allocates nothing: the split-L partial states, combine counters, error word
+ * and combined state live in one file-scope device array of 64 MiB
+ * (GBLA_NOALLOC_SCRATCH_BYTES) that every GPU which loads the library holds
+ * until the process exits.
+ *   Arguments, layouts and results are those of bla_core_forward.
+ *   GBLA_ERR_WORKSPACE: the shape needs more than 64 MiB of scratch
+ *   (gbla_workspace_size(shape, GBLA_OP_CORE_FORWARD) > 64 MiB); nothing runs.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ *   Every call on a device shares the one array: calls whose kernels overlap
+ *   on the GPU (two streams, or two host threads) race and corrupt each
+ *   other's results.  Order them on one stream.  The counters and the error
+ *   word are cleared at the start of every call; gbla_check_device_status
+ *   cannot be used on the array (it has no host-visible workspace pointer).
+ */
+#define GBLA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+gbla_status bla_core_forward_noalloc(const gbla_shape* shape, const void* q,
+                                     const void* k, const void* v,
+                                     const float* g, void* o, float* den,
+                                     float* state, void* stream);
+
 /* Synchronises `stream` and reads the device error word of the workspace that
  * the last call on it used: GBLA_OK or GBLA_ERR_DEVICE_CHECK (or
  * GBLA_ERR_CUDA if the stream itself failed). */
