@@ -345,7 +345,8 @@ gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* con
   ga.M = p.T; ga.N = p.N1; ga.K = p.d; ga.k_split = (p.d + 31) / 32 * 32;
   ga.epi = EPI_PROJ; ga.n_main = 4 * p.HD; ga.bias_g = shape->gate == GBLA_GATE_SIGMOID ? b_g : nullptr;
   ga.gate_mode = shape->gate == GBLA_GATE_SIGMOID ? 0 : 1; ga.gate = gate; ga.ldgate = p.H; ga.io_f32 = p.f32;
-  GBLA_CHECK(p.f32 ? launch_gemm_f32(ga, c.st) : launch_gemm_bf16(ga, c.st), "projection gemm");
+  ga.err = c.err;
+  GBLA_CHECK(launch_gemm(ga, c.st), "projection gemm");
   // Eq. 5/6: state
   const size_t es = p.io;
   const char* Pc = static_cast<const char*>(P);
@@ -436,14 +437,14 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   g1.A = dP; g1.lda = p.NP; g1.a_kmajor = 1;
   g1.B = at<char>(ws, l.Wp); g1.ldb = p.NP; g1.b_kmajor = 1;
   g1.C = at<float>(ws, l.dxt); g1.ldc = p.d;
-  g1.M = p.T; g1.N = p.d; g1.K = p.NP; g1.k_split = p.NP; g1.epi = EPI_F32; g1.io_f32 = p.f32;
-  GBLA_CHECK(p.f32 ? launch_gemm_f32(g1, c.st) : launch_gemm_bf16(g1, c.st), "dx~ gemm");
+  g1.M = p.T; g1.N = p.d; g1.K = p.NP; g1.k_split = p.NP; g1.epi = EPI_F32; g1.io_f32 = p.f32; g1.err = c.err;
+  GBLA_CHECK(launch_gemm(g1, c.st), "dx~ gemm");
   GemmArgs g2{};
   g2.A = xt; g2.lda = p.d; g2.a_kmajor = 0;
   g2.B = dP; g2.ldb = p.NP; g2.b_kmajor = 0;
   g2.C = at<float>(ws, l.dW); g2.ldc = p.NP;
-  g2.M = p.d; g2.N = p.NP; g2.K = p.T; g2.k_split = p.wsplit; g2.epi = EPI_SPLITK; g2.io_f32 = p.f32;
-  GBLA_CHECK(p.f32 ? launch_gemm_f32(g2, c.st) : launch_gemm_bf16(g2, c.st), "dW gemm");
+  g2.M = p.d; g2.N = p.NP; g2.K = p.T; g2.k_split = p.wsplit; g2.epi = EPI_SPLITK; g2.io_f32 = p.f32; g2.err = c.err;
+  GBLA_CHECK(launch_gemm(g2, c.st), "dW gemm");
   float* outs[5] = {dW_q, dW_k, dW_v, dW_r, dw_g};
   GBLA_CHECK(launch_scatter_dw(at<float>(ws, l.dW), p.n_wsplit, p.d, p.NP, p.H, p.dh, outs, c.st), "dW sum");
   // Eq. 4 conv backward

@@ -107,6 +107,7 @@ struct GemmArgs {
   // EPI_PROJ
   int n_main; const void* bias_g; int gate_mode; float* gate; int64_t ldgate;
   int io_f32;
+  int* err;           // workspace error word (bounded device waits that give up set bit 2)
 };
 
 struct ConvArgs {
@@ -135,7 +136,16 @@ cudaError_t launch_bwd_q_f32(const BwdQArgs& a, bool norm, int grid_x, cudaStrea
 cudaError_t launch_bwd_kv_f32(const BwdKVArgs& a, int grid_x, cudaStream_t st);
 
 cudaError_t launch_gemm_bf16(const GemmArgs& a, cudaStream_t st);
+// tcgen05 + TMA GEMM; cudaErrorNotSupported for shapes it does not take.
+cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_f32(const GemmArgs& a, cudaStream_t st);
+// The GEMM of the layer: tcgen05 where supported, else mma.sync / fp32 SIMT.
+inline cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
+  cudaError_t e = launch_gemm_tc(a, st);
+  if (e != cudaErrorNotSupported) return e;
+  (void)cudaGetLastError();
+  return a.io_f32 ? launch_gemm_f32(a, st) : launch_gemm_bf16(a, st);
+}
 
 cudaError_t launch_conv_fwd(const ConvArgs& a, bool f32, cudaStream_t st);
 cudaError_t launch_conv_bwd(const ConvArgs& a, bool f32, int nblk, cudaStream_t st);
