@@ -154,7 +154,7 @@ Layout ws_layout(const Plan& p, int op) {
     l.xt = c.take((size_t)p.T * p.d * p.io);
     l.P = c.take((size_t)p.T * 4 * p.HD * p.io);
     l.gate = c.take((size_t)p.T * p.H * 4);
-    l.Wt = c.take((size_t)p.N1 * p.d * p.io);
+    l.Wt = c.take((size_t)p.d * p.NP * p.io);  // packed W_all [d][NP]
   } else if (op == GBLA_OP_BACKWARD) {
     l.Wp = c.take((size_t)p.d * p.NP * p.io);
     l.dP = c.take((size_t)p.T * p.NP * p.io);
@@ -337,10 +337,10 @@ gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* con
   // Eq. 4, 5, 7: projections and gate
   const void* W[4] = {W_q, W_k, W_v, W_r};
   void* Wt = at<char>(ws, l.Wt);
-  GBLA_CHECK(launch_pack_weights(W, w_g, p.d, p.H, p.dh, p.f32, Wt, nullptr, p.N1, c.st), "pack");
+  GBLA_CHECK(launch_pack_weights(W, w_g, p.d, p.H, p.dh, p.f32, nullptr, Wt, p.NP, c.st), "pack");
   GemmArgs ga{};
   ga.A = xt; ga.lda = p.d; ga.a_kmajor = 1;
-  ga.B = Wt; ga.ldb = p.d; ga.b_kmajor = 1;
+  ga.B = Wt; ga.ldb = p.NP; ga.b_kmajor = 0;  // B(n, k) = W_all[k][n]: N-major
   ga.C = P; ga.ldc = 4 * p.HD;
   ga.M = p.T; ga.N = p.N1; ga.K = p.d; ga.k_split = (p.d + 31) / 32 * 32;
   ga.epi = EPI_PROJ; ga.n_main = 4 * p.HD; ga.bias_g = shape->gate == GBLA_GATE_SIGMOID ? b_g : nullptr;

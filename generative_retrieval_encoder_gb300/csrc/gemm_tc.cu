@@ -287,8 +287,6 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   const bool amn = !a.a_kmajor, bmn = !a.b_kmajor;
   if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B)) & 15) return cudaErrorNotSupported;
   if ((a.lda % 8) || (a.ldb % 8)) return cudaErrorNotSupported;
-  if (amn && a.M % 64) return cudaErrorNotSupported;
-  if (bmn && a.N % 64) return cudaErrorNotSupported;
   CUtensorMap ta, tb;
   const bool okA = amn ? make_map(&ta, a.A, (uint64_t)a.M, (uint64_t)a.K, (uint64_t)a.lda, 64, TBK)
                        : make_map(&ta, a.A, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.lda, TBK, TBM);

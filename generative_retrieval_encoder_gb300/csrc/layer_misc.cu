@@ -267,11 +267,30 @@ __global__ void k_pack(const T* Wq, const T* Wk, const T* Wv, const T* Wr, const
   }
 }
 
-__global__ void k_sum_parts(const float* part, int S, int64_t stride, int64_t n, float* out) {
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-    float s = 0.f;
-    for (int k = 0; k < S; ++k) s += part[k * stride + i];
-    out[i] = s;
+// Column sums of a [S][stride] partial array in a fixed order: block b owns
+// columns 32 b .. 32 b + 31; warp w adds rows w, w + 32, w + 64, ... (lanes
+// read 32 consecutive floats); then warp 0 adds the 32 warp sums in order.
+// mode 0: out[i];  mode 1 (conv parameters, i = 5 c + t): t < 4 -> out[4 c + t], else out2[c].
+__global__ void __launch_bounds__(1024) k_colsum(const float* part, int S, int64_t stride, int64_t n, float* out,
+                                                 float* out2, int mode) {
+  __shared__ float red[32][33];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t i = (int64_t)blockIdx.x * 32 + lane;
+  float s = 0.f;
+  if (i < n)
+    for (int k = warp; k < S; k += 32) s += part[(int64_t)k * stride + i];
+  red[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && i < n) {
+    float t = 0.f;
+    for (int w = 0; w < 32; ++w) t += red[w][lane];
+    if (mode == 0) {
+      out[i] = t;
+    } else {
+      const int64_t c = i / 5, q = i % 5;
+      if (q < 4) { if (out) out[c * 4 + q] = t; }
+      else if (out2) out2[c] = t;
+    }
   }
 }
 
@@ -290,16 +309,6 @@ __global__ void k_scatter_dw(const float* part, int S, int d, int np, int H, int
     } else if (o4) {
       o4[(size_t)c * H + n - 4 * HD] = s;
     }
-  }
-}
-
-__global__ void k_conv_param_grads(const float* part, int S, int d, float* dw, float* db) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d * 5; i += gridDim.x * blockDim.x) {
-    float s = 0.f;
-    for (int k = 0; k < S; ++k) s += part[(size_t)k * d * 5 + i];
-    const int c = i / 5, t = i % 5;
-    if (t < 4) { if (dw) dw[c * 4 + t] = s; }
-    else if (db) db[c] = s;
   }
 }
 
@@ -347,7 +356,7 @@ cudaError_t launch_pack_weights(const void* const* W, const void* w_g, int d, in
 }
 
 cudaError_t launch_sum_parts(const float* part, int S, int64_t stride, int64_t n, float* out, cudaStream_t st) {
-  k_sum_parts<<<grid_for((size_t)n), 256, 0, st>>>(part, S, stride, n, out);
+  k_colsum<<<(unsigned)((n + 31) / 32), 1024, 0, st>>>(part, S, stride, n, out, nullptr, 0);
   return cudaGetLastError();
 }
 
@@ -359,7 +368,7 @@ cudaError_t launch_scatter_dw(const float* part, int S, int d, int np, int H, in
 }
 
 cudaError_t launch_conv_param_grads(const float* part, int S, int d, float* dw, float* db, cudaStream_t st) {
-  k_conv_param_grads<<<grid_for((size_t)d * 5), 256, 0, st>>>(part, S, d, dw, db);
+  k_colsum<<<(unsigned)((d * 5 + 31) / 32), 1024, 0, st>>>(part, S, (int64_t)d * 5, (int64_t)d * 5, dw, db, 1);
   return cudaGetLastError();
 }
 
