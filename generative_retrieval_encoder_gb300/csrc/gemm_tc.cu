@@ -1,15 +1,25 @@
 // Blackwell tensor-core GEMM for the projection GEMMs of the GBLA layer:
 //   C[M, N] = sum_k A(m, k) B(n, k), bf16 operands, fp32 accumulation in TMEM.
-// tcgen05.mma (cta_group::1, M = 128, N <= 128, K = 16) issued by one thread,
-// operands staged by TMA (cp.async.bulk.tensor, 128-byte swizzle) through a
-// 3-stage mbarrier pipeline, accumulator read back with tcgen05.ld for the
-// epilogue (the same epilogue kinds as the mma.sync GEMM: bf16 / fp32 / split
-// over K / projection + gate).  Operands may be K-major ([rows][K]) or
-// M/N-major ([K][rows]); the latter is the weight-gradient GEMM x~^T dP.
 //
-// Every wait on an mbarrier gives up after a bounded number of polls; the
-// kernel then sets bit 2 of the workspace error word, drains the copies it
-// issued (again bounded), frees its TMEM and returns without storing.
+// Persistent and warp-specialised: one CTA per SM walks a static list of
+// 128 x 256 output tiles (x K splits).
+//   warp 0 (one lane)  TMA producer: cp.async.bulk.tensor loads (128-byte
+//                      swizzle) into a 4-stage shared-memory ring (full/empty
+//                      mbarriers);
+//   warp 1 (one lane)  MMA issuer: tcgen05.mma cta_group::1 M = 128, N <= 256,
+//                      K = 16, into one of two TMEM accumulators (2 x 256
+//                      columns), tcgen05.commit frees ring stages and hands a
+//                      finished accumulator to the epilogue;
+//   warps 2-5          epilogue: tcgen05.ld of their 32-lane quarter, release
+//                      the accumulator, convert and store (bf16 / fp32 / split
+//                      partial / projection + gate).
+// So the epilogue of tile i overlaps the MMAs of tile i + 1.  Operands may be
+// K-major ([rows][K]) or M/N-major ([K][rows], the weight-gradient GEMM
+// x~^T dP and the forward GEMM's packed weights).
+//
+// Every mbarrier wait gives up after a bounded number of polls; the kernel then
+// sets bit 2 of the workspace error word, waits (bounded) for the copies and
+// MMAs it issued, frees its TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -18,9 +28,11 @@
 namespace gbla {
 namespace {
 
-constexpr int TBM = 128, TBN = 128, TBK = 64, TSTAGES = 3;
-constexpr int OP_BYTES = TBM * TBK * 2;  // one operand tile: 16 KB
-constexpr int SMEM_TC = TSTAGES * 2 * OP_BYTES + 1024 + 256;
+constexpr int PBM = 128, PBN = 256, PBK = 64, PST = 4;
+constexpr int A_TILE = PBM * PBK * 2;  // 16 KB
+constexpr int B_TILE = PBN * PBK * 2;  // 32 KB
+constexpr int SMEM_P = PST * (A_TILE + B_TILE) + 1024 + 256;
+constexpr int NTHREADS = 192;
 constexpr uint32_t kPollLimit = 1u << 24;
 constexpr int kErrTimeout = 2;
 
@@ -29,6 +41,9 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -39,10 +54,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: false if the phase did not complete within kPollLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kPollLimit; ++i)
+// Bounded wait: false if the phase did not complete within kPollLimit polls
+// or another role of the CTA has already given up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* fail) {
+  for (uint32_t i = 0; i < kPollLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 1023) == 1023 && *fail) return false;
+  }
+  *fail = 1;
   return false;
 }
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
@@ -77,176 +96,239 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// A (AMN = false): tiles [TBM rows][TBK] loaded as one TMA box {TBK, TBM}.
-// A (AMN = true) : tiles [TBK rows (k)][TBM] loaded as two boxes {64, TBK}
-//                  (64 M-elements x 64 k-rows each, 8 KB apart).
-// Same for B with TBN.
+struct TileSched {
+  int tiles_m, tiles_n, splits, total;
+  __device__ void decode(int t, int& z, int& mt, int& nt) const {
+    z = t / (tiles_m * tiles_n);
+    const int r = t - z * tiles_m * tiles_n;
+    mt = r / tiles_n;
+    nt = r - mt * tiles_n;
+  }
+};
+
+// One 32-column chunk of a finished accumulator row to global memory.
+__device__ __forceinline__ void store_chunk(const GemmArgs& a, int m, int n, int z, const uint32_t (&r)[32]) {
+  const int Hg = a.N - a.n_main;
+  if (a.epi == EPI_BF16 || (a.epi == EPI_PROJ && n < a.n_main)) {
+    bf16* C = (bf16*)a.C + (size_t)m * a.ldc + n;
+    const int lim = a.epi == EPI_PROJ ? a.n_main : a.N;
+    if (n + 32 <= lim) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 u;
+        u.x = pack_bf16(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]));
+        u.y = pack_bf16(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]));
+        u.z = pack_bf16(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]));
+        u.w = pack_bf16(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]));
+        reinterpret_cast<uint4*>(C)[q] = u;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (n + j < lim) C[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+    }
+  } else if (a.epi == EPI_PROJ) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int hh = n + j - a.n_main;
+      if (hh >= 0 && hh < Hg) {
+        float s = __uint_as_float(r[j]);
+        if (a.bias_g) s += __bfloat162float(((const bf16*)a.bias_g)[hh]);
+        a.gate[(size_t)m * a.ldgate + hh] = a.gate_mode == 0 ? 1.f / (1.f + __expf(-s)) : s;
+      }
+    }
+  } else {
+    float* C = (float*)a.C + (a.epi == EPI_SPLITK ? (size_t)z * a.M * a.ldc : 0) + (size_t)m * a.ldc + n;
+    if (n + 32 <= a.N) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        reinterpret_cast<float4*>(C)[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                                      __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (n + j < a.N) C[j] = __uint_as_float(r[j]);
+    }
+  }
+}
+
 template <bool AMN, bool BMN>
-__global__ void __launch_bounds__(128, 2)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs a,
+              const TileSched ts) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sA = smem_u32(smem), sB = sA + TSTAGES * OP_BYTES;
-  const uint32_t bar0 = sB + TSTAGES * OP_BYTES;  // full[s] at bar0 + 8 s, empty[s] at +8 (TSTAGES + s), done after
-  const uint32_t full = bar0, empty = bar0 + 8 * TSTAGES, done = bar0 + 16 * TSTAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 2 * TSTAGES * OP_BYTES + 16 * TSTAGES + 8);
+  const uint32_t sA = smem_u32(smem), sB = sA + PST * A_TILE;
+  const uint32_t bars = sB + PST * B_TILE;
+  const uint32_t full = bars, empty = bars + 8 * PST, accf = bars + 16 * PST, acce = accf + 16, drain = acce + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + PST * (A_TILE + B_TILE) + 16 * PST + 40);
   __shared__ int s_fail;
-  __shared__ int s_issued;
+  __shared__ int s_issued[PST];  // last ring use issued per stage (+1), for the drain
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * TBN, m0 = blockIdx.y * TBM;
-  const int kbeg = blockIdx.z * a.k_split;
-  const int kend = min(a.K, kbeg + a.k_split);
-  const int nk = (kend - kbeg + TBK - 1) / TBK;
-  const int ncols = min(TBN, a.N - n0);
-  const int mma_n = (ncols + 15) / 16 * 16;
-
   if (threadIdx.x == 0) {
-    for (int s = 0; s < TSTAGES; ++s) {
+    for (int s = 0; s < PST; ++s) {
       mbar_init(full + 8 * s, 1);
       mbar_init(empty + 8 * s, 1);
+      s_issued[s] = 0;
     }
-    mbar_init(done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf + 8 * b, 1);
+      mbar_init(acce + 8 * b, 4);  // one arrival per epilogue warp
+    }
+    mbar_init(drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_fail = 0;
-    s_issued = 0;
   }
-  if (warp == 0) {
+  if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(TBN));
+                 "r"(2 * PBN));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  volatile int* fail = &s_fail;
 
-  if (threadIdx.x == 0) {  // TMA producer
-    int kt = 0;
-    for (; kt < nk; ++kt) {
-      const int s = kt % TSTAGES;
-      if (kt >= TSTAGES && !mbar_wait(empty + 8 * s, ((kt / TSTAGES) & 1) ^ 1)) {
-        s_fail = 1;
-        break;
-      }
-      const int k0 = kbeg + kt * TBK;
-      mbar_expect_tx(full + 8 * s, 2 * OP_BYTES);
-      const uint32_t da = sA + s * OP_BYTES, db = sB + s * OP_BYTES;
-      if (AMN) {
-        tma_load_2d(da, &tmA, full + 8 * s, m0, k0);
-        tma_load_2d(da + OP_BYTES / 2, &tmA, full + 8 * s, m0 + 64, k0);
-      } else {
-        tma_load_2d(da, &tmA, full + 8 * s, k0, m0);
-      }
-      if (BMN) {
-        tma_load_2d(db, &tmB, full + 8 * s, n0, k0);
-        tma_load_2d(db + OP_BYTES / 2, &tmB, full + 8 * s, n0 + 64, k0);
-      } else {
-        tma_load_2d(db, &tmB, full + 8 * s, k0, n0);
-      }
-    }
-    s_issued = kt;
-  } else if (threadIdx.x == 32) {  // MMA issuer
-    const uint32_t idesc = idesc_bf16(TBM, mma_n, AMN, BMN);
-    for (int kt = 0; kt < nk; ++kt) {
-      const int s = kt % TSTAGES;
-      if (!mbar_wait(full + 8 * s, (kt / TSTAGES) & 1)) {
-        s_fail = 1;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t ta = sA + s * OP_BYTES, tb = sB + s * OP_BYTES;
+  if (warp == 0) {
+    if (lane == 0) {  // ---------------------------------------------- producer
+      uint32_t kt = 0;
+      for (int t = blockIdx.x; t < ts.total && !*fail; t += gridDim.x) {
+        int z, mt, nt;
+        ts.decode(t, z, mt, nt);
+        const int m0 = mt * PBM, n0 = nt * PBN;
+        const int kbeg = z * a.k_split, kend = min(a.K, kbeg + a.k_split);
+        for (int k0 = kbeg; k0 < kend; k0 += PBK, ++kt) {
+          const int s = kt % PST;
+          const uint32_t use = kt / PST;
+          if (use > 0 && !mbar_wait(empty + 8 * s, (use - 1) & 1, fail)) break;
+          mbar_expect_tx(full + 8 * s, A_TILE + B_TILE);
+          s_issued[s] = (int)use + 1;
+          const uint32_t da = sA + s * A_TILE, db = sB + s * B_TILE;
+          if (AMN) {
+            tma_load_2d(da, &tmA, full + 8 * s, m0, k0);
+            tma_load_2d(da + A_TILE / 2, &tmA, full + 8 * s, m0 + 64, k0);
+          } else {
+            tma_load_2d(da, &tmA, full + 8 * s, k0, m0);
+          }
+          if (BMN) {
 #pragma unroll
-      for (int kk = 0; kk < TBK / 16; ++kk) {
-        // K-major: advance 32 B inside the 128-byte swizzled row.  M/N-major:
-        // advance 16 k-rows (2 x 1024-byte swizzle atoms); the two 64-wide
-        // halves of the tile are LBO = 8 KB apart.
-        const uint64_t da = AMN ? sdesc(ta + kk * 2048, OP_BYTES / 2, 1024) : sdesc(ta + kk * 32, 16, 1024);
-        const uint64_t db = BMN ? sdesc(tb + kk * 2048, OP_BYTES / 2, 1024) : sdesc(tb + kk * 32, 16, 1024);
-        tc_mma(tmem, da, db, idesc, (kt | kk) != 0 ? 1u : 0u);
+            for (int j = 0; j < PBN / 64; ++j) tma_load_2d(db + j * (B_TILE / 4), &tmB, full + 8 * s, n0 + 64 * j, k0);
+          } else {
+            tma_load_2d(db, &tmB, full + 8 * s, k0, n0);
+          }
+        }
       }
-      tc_commit(empty + 8 * s);  // the stage is free once these MMAs have read it
     }
-    tc_commit(done);  // arrives when every MMA issued above has completed
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---------------------------------------------- MMA issuer
+      uint32_t kt = 0;
+      int i = 0;
+      for (int t = blockIdx.x; t < ts.total && !*fail; t += gridDim.x, ++i) {
+        int z, mt, nt;
+        ts.decode(t, z, mt, nt);
+        const int n0 = nt * PBN;
+        const int ncols = min(PBN, a.N - n0);
+        const int mma_n = (ncols + 15) / 16 * 16;
+        const uint32_t idesc = idesc_bf16(PBM, mma_n, AMN, BMN);
+        const int kbeg = z * a.k_split, kend = min(a.K, kbeg + a.k_split);
+        const int b = i & 1;
+        const uint32_t u = (uint32_t)i >> 1;
+        if (u > 0 && !mbar_wait(acce + 8 * b, (u - 1) & 1, fail)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + b * PBN;
+        bool first = true;
+        bool ok = true;
+        for (int k0 = kbeg; k0 < kend; k0 += PBK, ++kt) {
+          const int s = kt % PST;
+          if (!mbar_wait(full + 8 * s, (kt / PST) & 1, fail)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t ta = sA + s * A_TILE, tb = sB + s * B_TILE;
+#pragma unroll
+          for (int kk = 0; kk < PBK / 16; ++kk) {
+            // K-major: advance 32 B inside the 128-byte swizzled row.  M/N-major:
+            // advance 16 k-rows (2 x 1024-byte swizzle atoms); 64-wide M/N
+            // chunks of the tile are LBO = 8 KB apart.
+            const uint64_t da = AMN ? sdesc(ta + kk * 2048, 8192, 1024) : sdesc(ta + kk * 32, 16, 1024);
+            const uint64_t db = BMN ? sdesc(tb + kk * 2048, 8192, 1024) : sdesc(tb + kk * 32, 16, 1024);
+            tc_mma(d, da, db, idesc, first ? 0u : 1u);
+            first = false;
+          }
+          tc_commit(empty + 8 * s);
+        }
+        if (!ok) break;
+        tc_commit(accf + 8 * b);
+      }
+      tc_commit(drain);  // completes once every MMA issued above has finished
+      for (uint32_t k = 0; k < kPollLimit && !mbar_try_wait(drain, 0); ++k) {
+      }
+    }
+  } else {  // ------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    int i = 0;
+    for (int t = blockIdx.x; t < ts.total && !*fail; t += gridDim.x, ++i) {
+      int z, mt, nt;
+      ts.decode(t, z, mt, nt);
+      const int m0 = mt * PBM, n0 = nt * PBN;
+      const int ncols = min(PBN, a.N - n0);
+      const int kbeg = z * a.k_split, kend = min(a.K, kbeg + a.k_split);
+      const int b = i & 1;
+      if (!mbar_wait(accf + 8 * b, ((uint32_t)i >> 1) & 1, fail)) break;
+      tc_fence_after();
+      const int m = m0 + row;
+      if (kend > kbeg) {
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + b * PBN;
+        for (int c = 0; c < ncols; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c, r);  // warp-collective: every lane runs it
+          if (c + 32 >= ncols) {    // last chunk read: hand the accumulator back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce + 8 * b);
+          }
+          if (m < a.M) store_chunk(a, m, n0 + c, z, r);
+        }
+      } else {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce + 8 * b);
+        if (m < a.M && a.epi == EPI_SPLITK)
+          for (int j = 0; j < ncols; ++j) ((float*)a.C)[(size_t)z * a.M * a.ldc + (size_t)m * a.ldc + n0 + j] = 0.f;
+      }
+    }
   }
-  __syncwarp();
-  if (!mbar_wait(done, 0)) s_fail = 1;
-  tc_fence_after();
+
   __syncthreads();
-  if (s_fail) {  // uniform across the CTA
+  if (*fail) {
     if (threadIdx.x == 0) {
       if (a.err) atomicOr(a.err, kErrTimeout);
-      // drain the copies this CTA issued so that none lands after it exits
-      const int issued = s_issued;
-      for (int kt = max(0, issued - TSTAGES); kt < issued; ++kt)
-        mbar_wait(full + 8 * (kt % TSTAGES), (kt / TSTAGES) & 1);
-    }
-  } else if (nk > 0) {
-    const int m = m0 + warp * 32 + lane;
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    const int Hg = a.N - a.n_main;
-    for (int c = 0; c < ncols; c += 16) {
-      uint32_t r[16];
-      tmem_ld16(trow + c, r);  // warp-collective: every lane runs it, rows past M included
-      const int n = n0 + c;
-      if (m < a.M) {
-      if (a.epi == EPI_BF16 || (a.epi == EPI_PROJ && n < a.n_main)) {
-        bf16* C = (bf16*)a.C + (size_t)m * a.ldc + n;
-        const int lim = a.epi == EPI_PROJ ? a.n_main : a.N;
-        if (n + 16 <= lim) {
-          uint4 u0, u1;
-          u0.x = pack_bf16(__uint_as_float(r[0]), __uint_as_float(r[1]));
-          u0.y = pack_bf16(__uint_as_float(r[2]), __uint_as_float(r[3]));
-          u0.z = pack_bf16(__uint_as_float(r[4]), __uint_as_float(r[5]));
-          u0.w = pack_bf16(__uint_as_float(r[6]), __uint_as_float(r[7]));
-          u1.x = pack_bf16(__uint_as_float(r[8]), __uint_as_float(r[9]));
-          u1.y = pack_bf16(__uint_as_float(r[10]), __uint_as_float(r[11]));
-          u1.z = pack_bf16(__uint_as_float(r[12]), __uint_as_float(r[13]));
-          u1.w = pack_bf16(__uint_as_float(r[14]), __uint_as_float(r[15]));
-          reinterpret_cast<uint4*>(C)[0] = u0;
-          reinterpret_cast<uint4*>(C)[1] = u1;
-        } else {
-          for (int j = 0; j < 16 && n + j < lim; ++j) C[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
-        }
-      } else if (a.epi == EPI_PROJ) {
-        for (int j = 0; j < 16; ++j) {
-          const int hh = n + j - a.n_main;
-          if (hh < 0 || hh >= Hg) continue;
-          float s = __uint_as_float(r[j]);
-          if (a.bias_g) s += __bfloat162float(((const bf16*)a.bias_g)[hh]);
-          a.gate[(size_t)m * a.ldgate + hh] = a.gate_mode == 0 ? 1.f / (1.f + __expf(-s)) : s;
-        }
-      } else {
-        float* C = (float*)a.C + (a.epi == EPI_SPLITK ? (size_t)blockIdx.z * a.M * a.ldc : 0) + (size_t)m * a.ldc + n;
-        if (n + 16 <= a.N) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            reinterpret_cast<float4*>(C)[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                                          __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-        } else {
-          for (int j = 0; j < 16 && n + j < a.N; ++j) C[j] = __uint_as_float(r[j]);
-        }
+      // wait (bounded) for the last copy issued into each ring stage
+      for (int s = 0; s < PST; ++s) {
+        const int u = s_issued[s];
+        if (u > 0)
+          for (uint32_t k = 0; k < kPollLimit && !mbar_try_wait(full + 8 * s, (uint32_t)(u - 1) & 1); ++k) {
+          }
       }
-      }  // m < M
     }
-  } else {
-    // empty K range (split past K): this split's partial is zero
-    const int m = m0 + warp * 32 + lane;
-    if (a.epi == EPI_SPLITK && m < a.M)
-      for (int j = 0; j < ncols; ++j) ((float*)a.C)[(size_t)blockIdx.z * a.M * a.ldc + (size_t)m * a.ldc + n0 + j] = 0.f;
+    __syncthreads();
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TBN));
+  if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * PBN));
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
@@ -277,32 +359,47 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  }
+  return n;
+}
+
 }  // namespace
 
 // cudaErrorNotSupported when the shape is outside what this kernel handles
 // (the caller then uses the mma.sync GEMM).
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   if (a.io_f32 || a.M <= 0 || a.N <= 0 || a.K <= 0) return cudaErrorNotSupported;
-  if (a.k_split % TBK != 0 && a.k_split < a.K) return cudaErrorNotSupported;
+  if (a.k_split % PBK != 0 && a.k_split < a.K) return cudaErrorNotSupported;
   const bool amn = !a.a_kmajor, bmn = !a.b_kmajor;
   if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B)) & 15) return cudaErrorNotSupported;
   if ((a.lda % 8) || (a.ldb % 8)) return cudaErrorNotSupported;
+  if (a.epi == EPI_PROJ && a.n_main % 32) return cudaErrorNotSupported;
   CUtensorMap ta, tb;
-  const bool okA = amn ? make_map(&ta, a.A, (uint64_t)a.M, (uint64_t)a.K, (uint64_t)a.lda, 64, TBK)
-                       : make_map(&ta, a.A, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.lda, TBK, TBM);
-  const bool okB = bmn ? make_map(&tb, a.B, (uint64_t)a.N, (uint64_t)a.K, (uint64_t)a.ldb, 64, TBK)
-                       : make_map(&tb, a.B, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.ldb, TBK, TBN);
+  const bool okA = amn ? make_map(&ta, a.A, (uint64_t)a.M, (uint64_t)a.K, (uint64_t)a.lda, 64, PBK)
+                       : make_map(&ta, a.A, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.lda, PBK, PBM);
+  const bool okB = bmn ? make_map(&tb, a.B, (uint64_t)a.N, (uint64_t)a.K, (uint64_t)a.ldb, 64, PBK)
+                       : make_map(&tb, a.B, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.ldb, PBK, PBN);
   if (!okA || !okB) return cudaErrorNotSupported;
-  const int splits = (a.K + a.k_split - 1) / a.k_split;
-  const dim3 grid((a.N + TBN - 1) / TBN, (a.M + TBM - 1) / TBM, splits);
+  TileSched ts;
+  ts.tiles_m = (a.M + PBM - 1) / PBM;
+  ts.tiles_n = (a.N + PBN - 1) / PBN;
+  ts.splits = (a.K + a.k_split - 1) / a.k_split;
+  ts.total = ts.tiles_m * ts.tiles_n * ts.splits;
+  const int grid = ts.total < sm_count() ? ts.total : sm_count();
   cudaError_t e;
-#define GBLA_CASE(AMN, BMN)                                                                                   \
-  if (amn == AMN && bmn == BMN) {                                                                             \
-    if ((e = cudaFuncSetAttribute(k_gemm_tc<AMN, BMN>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TC)) != \
-        cudaSuccess)                                                                                          \
-      return e;                                                                                               \
-    k_gemm_tc<AMN, BMN><<<grid, 128, SMEM_TC, st>>>(ta, tb, a);                                               \
-    return cudaGetLastError();                                                                                \
+#define GBLA_CASE(AMN, BMN)                                                                                  \
+  if (amn == AMN && bmn == BMN) {                                                                            \
+    if ((e = cudaFuncSetAttribute(k_gemm_tc<AMN, BMN>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_P)) != \
+        cudaSuccess)                                                                                         \
+      return e;                                                                                              \
+    k_gemm_tc<AMN, BMN><<<grid, NTHREADS, SMEM_P, st>>>(ta, tb, a, ts);                                      \
+    return cudaGetLastError();                                                                               \
   }
   GBLA_CASE(false, false) GBLA_CASE(true, true) GBLA_CASE(false, true) GBLA_CASE(true, false)
 #undef GBLA_CASE
