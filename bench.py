@@ -77,7 +77,7 @@ def algorithmic(wl, T: int, n_wsplit: int | None = None) -> dict:
         "bwd_kv": ("hbm", th * (8 * dh + 6)),               # k, v, g in; dk, dv, ds out
         "dx~ gemm": ("tensor", 2 * T * N1 * d),
         "dW gemm": ("tensor", 2 * T * d * N1),
-        "conv bwd": ("hbm", T * d * 8),                     # x, dx~ (fp32) in; dx out
+        "conv bwd": ("hbm", T * d * 6),                     # x, dx~ in; dx out (bf16)
     }
 
 

@@ -158,7 +158,7 @@ Layout ws_layout(const Plan& p, int op) {
   } else if (op == GBLA_OP_BACKWARD) {
     l.Wp = c.take((size_t)p.d * p.NP * p.io);
     l.dP = c.take((size_t)p.T * p.NP * p.io);
-    l.dxt = c.take((size_t)p.T * p.d * 4);
+    l.dxt = c.take((size_t)p.T * p.d * p.io);
     l.dW = c.take((size_t)p.n_wsplit * p.d * p.NP * 4);
     l.dstate = c.take(state_bytes(p));
     l.dstate_bf = c.take(state_bf_bytes(p));
@@ -223,7 +223,8 @@ struct Ctx {
   Layout l;
   SeqDesc seq;
   Tiling chunks, tiles;
-  int* err;
+  int* err;          // workspace error word (always valid)
+  const int* kerr;   // what the state / conv kernels read: err, or null in the dense form
   cudaStream_t st;
 };
 
@@ -247,6 +248,9 @@ gbla_status begin(const gbla_shape* s, int op, void* ws, size_t ws_bytes, void* 
   c.tiles.per_seq = p.tile_per_seq;
   c.tiles.prefix = p.mode == SEQ_VARLEN ? at<int32_t>(ws, c.l.pre_t) : nullptr;
   c.err = at<int>(ws, c.l.err);
+  // Only the varlen and padded forms have sequence data to check on the
+  // device; in the dense form the kernels skip the error-word read.
+  c.kerr = p.mode == SEQ_DENSE ? nullptr : c.err;
   GBLA_CHECK(cudaMemsetAsync(ws, 0, c.l.cnt_b + (size_t)p.n_seq * p.H * 4 - c.l.err, c.st), "memset");
   if (p.mode != SEQ_DENSE) {
     const int ts[2] = {p.chunk, p.tile};
@@ -271,7 +275,7 @@ gbla_status run_reduce(Ctx& c, const void* k, const void* v, int64_t ld, const f
   a.counters = at<int>(ws, c.l.cnt_f);
   a.state = state; a.state_bf = state_bf; a.state_m = state_m; a.pub_state = pub_state;
   a.center = p.f32 ? nullptr : center;
-  a.err = c.err;
+  a.err = c.kerr;
   GBLA_CHECK(p.f32 ? launch_reduce_f32(a, p.n_chunks, c.st) : launch_reduce_bf16(a, p.n_chunks, c.st), "reduce");
   return GBLA_OK;
 }
@@ -332,7 +336,7 @@ gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* con
   if (p.f32) center = nullptr;
   // Eq. 4: conv
   ConvArgs ca{};
-  ca.x = x; ca.w = conv_w; ca.b = conv_b; ca.xt = xt; ca.T = p.T; ca.d = p.d; ca.seq = c.seq; ca.err = c.err;
+  ca.x = x; ca.w = conv_w; ca.b = conv_b; ca.xt = xt; ca.T = p.T; ca.d = p.d; ca.seq = c.seq; ca.err = c.kerr;
   GBLA_CHECK(launch_conv_fwd(ca, p.f32, c.st), "conv");
   // Eq. 4, 5, 7: projections and gate
   const void* W[4] = {W_q, W_k, W_v, W_r};
@@ -361,7 +365,7 @@ gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* con
   ra.rms_w = rms_w; ra.eps = shape->rms_eps;
   ra.state = state; ra.state_bf = state_bf; ra.center = center;
   ra.out = y; ra.ldo = p.HD; ra.den = nullptr;
-  ra.H = p.H; ra.dh = p.dh; ra.seq = c.seq; ra.tiles = c.tiles; ra.err = c.err;
+  ra.H = p.H; ra.dh = p.dh; ra.seq = c.seq; ra.tiles = c.tiles; ra.err = c.kerr;
   GBLA_CHECK(p.f32 ? launch_readout_f32(ra, true, p.n_tiles, c.st) : launch_readout_bf16(ra, true, p.n_tiles, c.st),
              "readout");
   return GBLA_OK;
@@ -412,7 +416,7 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   q.gamma_part = at<float>(ws, l.gamma_part);
   q.partial = at<float>(ws, l.partial); q.counters = at<int>(ws, l.cnt_b);
   q.dstate = at<float>(ws, l.dstate); q.dstate_bf = at<bf16>(ws, l.dstate_bf);
-  q.H = p.H; q.dh = p.dh; q.seq = c.seq; q.chunks = c.chunks; q.err = c.err;
+  q.H = p.H; q.dh = p.dh; q.seq = c.seq; q.chunks = c.chunks; q.err = c.kerr;
   GBLA_CHECK(p.f32 ? launch_bwd_q_f32(q, true, p.n_chunks, c.st) : launch_bwd_q_bf16(q, true, p.n_chunks, c.st),
              "bwd_q");
   // key side: dk, dv, ds
@@ -430,14 +434,15 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   kv.ds = dP + (size_t)4 * p.HD * es;
   kv.zero_cols_from = p.N1 - 4 * p.HD; kv.zero_cols_to = p.NP - 4 * p.HD;
   kv.bg_part = at<float>(ws, l.bg_part);
-  kv.H = p.H; kv.dh = p.dh; kv.seq = c.seq; kv.tiles = c.tiles; kv.err = c.err;
+  kv.H = p.H; kv.dh = p.dh; kv.seq = c.seq; kv.tiles = c.tiles; kv.err = c.kerr;
   GBLA_CHECK(p.f32 ? launch_bwd_kv_f32(kv, p.n_tiles, c.st) : launch_bwd_kv_bf16(kv, p.n_tiles, c.st), "bwd_kv");
   // Eq. 4 projections backward: dx~ = dP W_all^T, dW_all = x~^T dP
   GemmArgs g1{};
   g1.A = dP; g1.lda = p.NP; g1.a_kmajor = 1;
   g1.B = at<char>(ws, l.Wp); g1.ldb = p.NP; g1.b_kmajor = 1;
-  g1.C = at<float>(ws, l.dxt); g1.ldc = p.d;
-  g1.M = p.T; g1.N = p.d; g1.K = p.NP; g1.k_split = p.NP; g1.epi = EPI_F32; g1.io_f32 = p.f32; g1.err = c.err;
+  g1.C = at<char>(ws, l.dxt); g1.ldc = p.d;  // dx~ in the io dtype
+  g1.M = p.T; g1.N = p.d; g1.K = p.NP; g1.k_split = p.NP; g1.epi = p.f32 ? EPI_F32 : EPI_BF16; g1.io_f32 = p.f32;
+  g1.err = c.err;
   GBLA_CHECK(launch_gemm(g1, c.st), "dx~ gemm");
   GemmArgs g2{};
   g2.A = xt; g2.lda = p.d; g2.a_kmajor = 0;
@@ -449,8 +454,8 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   GBLA_CHECK(launch_scatter_dw(at<float>(ws, l.dW), p.n_wsplit, p.d, p.NP, p.H, p.dh, outs, c.st), "dW sum");
   // Eq. 4 conv backward
   ConvArgs ca{};
-  ca.x = x; ca.w = conv_w; ca.dxt = at<float>(ws, l.dxt); ca.dx = dx; ca.part = at<float>(ws, l.conv_part);
-  ca.T = p.T; ca.d = p.d; ca.seq = c.seq; ca.err = c.err;
+  ca.x = x; ca.w = conv_w; ca.dxt = at<char>(ws, l.dxt); ca.dx = dx; ca.part = at<float>(ws, l.conv_part);
+  ca.T = p.T; ca.d = p.d; ca.seq = c.seq; ca.err = c.kerr;
   GBLA_CHECK(launch_conv_bwd(ca, p.f32, p.conv_blocks, c.st), "conv bwd");
   if (dconv_w || dconv_b)
     GBLA_CHECK(launch_conv_param_grads(ca.part, p.conv_blocks, p.d, dconv_w, dconv_b, c.st), "conv grads");
@@ -480,7 +485,7 @@ gbla_status bla_core_forward(const gbla_shape* shape, const void* q, const void*
   ra.q = q; ra.ldq = p.HD;
   ra.state = st; ra.state_bf = sbf; ra.center = center;
   ra.out = o; ra.ldo = p.HD; ra.den = den;
-  ra.H = p.H; ra.dh = p.dh; ra.seq = c.seq; ra.tiles = c.tiles; ra.err = c.err;
+  ra.H = p.H; ra.dh = p.dh; ra.seq = c.seq; ra.tiles = c.tiles; ra.err = c.kerr;
   GBLA_CHECK(p.f32 ? launch_readout_f32(ra, false, p.n_tiles, c.st) : launch_readout_bf16(ra, false, p.n_tiles, c.st),
              "readout");
   return GBLA_OK;
@@ -506,7 +511,7 @@ gbla_status bla_core_backward(const gbla_shape* shape, const void* q, const void
   a.dq = dq; a.lddq = p.HD;
   a.partial = at<float>(ws, c.l.partial); a.counters = at<int>(ws, c.l.cnt_b);
   a.dstate = at<float>(ws, c.l.dstate); a.dstate_bf = at<bf16>(ws, c.l.dstate_bf);
-  a.H = p.H; a.dh = p.dh; a.seq = c.seq; a.chunks = c.chunks; a.err = c.err;
+  a.H = p.H; a.dh = p.dh; a.seq = c.seq; a.chunks = c.chunks; a.err = c.kerr;
   GBLA_CHECK(p.f32 ? launch_bwd_q_f32(a, false, p.n_chunks, c.st) : launch_bwd_q_bf16(a, false, p.n_chunks, c.st),
              "bwd_q");
   BwdKVArgs kv{};
@@ -515,7 +520,7 @@ gbla_status bla_core_backward(const gbla_shape* shape, const void* q, const void
   kv.dstate = a.dstate; kv.dstate_bf = a.dstate_bf; kv.center = center;
   kv.dk = dk; kv.lddk = p.HD; kv.dv = dv; kv.lddv = p.HD;
   kv.ds = dg; kv.ldds = p.H; kv.gate_grad = GG_DG;
-  kv.H = p.H; kv.dh = p.dh; kv.seq = c.seq; kv.tiles = c.tiles; kv.err = c.err;
+  kv.H = p.H; kv.dh = p.dh; kv.seq = c.seq; kv.tiles = c.tiles; kv.err = c.kerr;
   GBLA_CHECK(p.f32 ? launch_bwd_kv_f32(kv, p.n_tiles, c.st) : launch_bwd_kv_bf16(kv, p.n_tiles, c.st), "bwd_kv");
   return GBLA_OK;
 }

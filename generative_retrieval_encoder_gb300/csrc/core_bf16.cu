@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(256) k_reduce_bf16(const ReduceArgs a) {
   __shared__ float red8[8];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int wm = warp % R::WM, kg = warp / R::WM;
-  if (*a.err) return;
+  if (a.err && *a.err) return;
   int b, row0, nvalid, cin;
   if (!map_tile(a.seq, a.chunks, blockIdx.x, b, row0, nvalid, cin)) return;
   const int h = blockIdx.y, H = a.H;
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(128) k_readout_bf16(const ReadoutArgs a) {
   uint8_t* qt = smem + DH * C::SPAD * 2;
   uint8_t* rt = qt + 2 * R::TILE;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (*a.err) return;
+  if (a.err && *a.err) return;
   int b, row0, nvalid, tin;
   if (!map_tile(a.seq, a.tiles, blockIdx.x, b, row0, nvalid, tin)) return;
   const int h = blockIdx.y, H = a.H;
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(BqCfg<DH, NORM>::NW * 32) k_bwd_q_bf16(const B
   uint8_t* tiles = reinterpret_cast<uint8_t*>(Dn + R::TT * C::SPAD);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int wm = warp % R::WM, kg = warp / R::WM;
-  if (*a.err) return;
+  if (a.err && *a.err) return;
   int b, row0, nvalid, cin;
   if (!map_tile(a.seq, a.chunks, blockIdx.x, b, row0, nvalid, cin)) return;
   const int h = blockIdx.y, H = a.H;
@@ -421,17 +421,17 @@ __global__ void __launch_bounds__(BqCfg<DH, NORM>::NW * 32) k_bwd_q_bf16(const B
   };
 
   const int g = lane >> 2, t4 = lane & 3, mi = lane >> 3, rr = lane & 7;
-  float gam[DH / 8][2], gacc[DH / 8][2], cen[DH / 8][2];
-#pragma unroll
-  for (int nt = 0; nt < DH / 8; ++nt) {
-    gam[nt][0] = gam[nt][1] = 1.f;
-    gacc[nt][0] = gacc[nt][1] = 0.f;
-    if (NORM && a.rms_w) {
-      gam[nt][0] = __bfloat162float(((const bf16*)a.rms_w)[nt * 8 + 2 * t4]);
-      gam[nt][1] = __bfloat162float(((const bf16*)a.rms_w)[nt * 8 + 2 * t4 + 1]);
-    }
+  // gamma and the state centre live in shared memory (read as float2 at this
+  // lane's columns) to keep registers for the accumulators.
+  __shared__ __align__(16) float s_gam[DH];  // read as float2: needs 8-byte alignment
+  __shared__ __align__(16) float s_cen[DH];
+  for (int f = tid; f < DH; f += NTHR) {
+    s_gam[f] = (NORM && a.rms_w) ? __bfloat162float(((const bf16*)a.rms_w)[f]) : 1.f;
+    s_cen[f] = (NORM && a.center) ? a.center[(size_t)(b * H + h) * DH + f] : 0.f;
   }
-  load_center_cols<DH>(NORM ? a.center : nullptr, b * H + h, t4, cen);
+  float gacc[DH / 8][2];
+#pragma unroll
+  for (int nt = 0; nt < DH / 8; ++nt) gacc[nt][0] = gacc[nt][1] = 0.f;
   float accS[C::NT][4];
 #pragma unroll
   for (int i = 0; i < C::NT; ++i) accS[i][0] = accS[i][1] = accS[i][2] = accS[i][3] = 0.f;
@@ -491,8 +491,9 @@ __global__ void __launch_bounds__(BqCfg<DH, NORM>::NW * 32) k_bwd_q_bf16(const B
       float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
       for (int nt = 0; nt < DH / 8; ++nt) {
-        const float o0 = acc[nt][0] + cv[0] * cen[nt][0], o1 = acc[nt][1] + cv[1] * cen[nt][1];
-        const float o2 = acc[nt][2] + cv[2] * cen[nt][0], o3 = acc[nt][3] + cv[3] * cen[nt][1];
+        const float2 ce = *reinterpret_cast<const float2*>(s_cen + nt * 8 + 2 * t4);
+        const float o0 = acc[nt][0] + cv[0] * ce.x, o1 = acc[nt][1] + cv[1] * ce.y;
+        const float o2 = acc[nt][2] + cv[2] * ce.x, o3 = acc[nt][3] + cv[3] * ce.y;
         ss0 += o0 * o0 + o1 * o1;
         ss1 += o2 * o2 + o3 * o3;
       }
@@ -500,7 +501,7 @@ __global__ void __launch_bounds__(BqCfg<DH, NORM>::NW * 32) k_bwd_q_bf16(const B
       ss1 += __shfl_xor_sync(FULL, ss1, 1); ss1 += __shfl_xor_sync(FULL, ss1, 2);
       const float rs0 = rsqrtf(ss0 / DH + a.eps), rs1 = rsqrtf(ss1 / DH + a.eps);
       float m0 = 0.f, m1 = 0.f;
-      float u[DH / 8][4], dr[DH / 8][4];
+      const float rsv[4] = {rs0, rs0, rs1, rs1};
 #pragma unroll
       for (int nt = 0; nt < DH / 8; ++nt) {
         const uint32_t o0 = swz<C::CPR>(r0w + g, nt) + t4 * 4, o1 = swz<C::CPR>(r0w + g + 8, nt) + t4 * 4;
@@ -510,36 +511,36 @@ __global__ void __launch_bounds__(BqCfg<DH, NORM>::NW * 32) k_bwd_q_bf16(const B
         const uint32_t yv1 = *reinterpret_cast<const uint32_t*>(ytb + o1);
         const float rv[4] = {bf_lo(rv0), bf_hi(rv0), bf_lo(rv1), bf_hi(rv1)};
         const float yv[4] = {bf_lo(yv0), bf_hi(yv0), bf_lo(yv1), bf_hi(yv1)};
+        float dr[4];
+        const float2 gm2 = *reinterpret_cast<const float2*>(s_gam + nt * 8 + 2 * t4);
+        const float2 ce2 = *reinterpret_cast<const float2*>(s_cen + nt * 8 + 2 * t4);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float rs = q < 2 ? rs0 : rs1;
-          const float gm = gam[nt][q & 1];
+          const float gm = (q & 1) ? gm2.y : gm2.x;
           const float sg = 1.f / (1.f + __expf(-rv[q]));
           const float av = rv[q] * sg;
-          u[nt][q] = (acc[nt][q] + cv[q] * cen[nt][q & 1]) * rs;
-          gacc[nt][q & 1] += yv[q] * u[nt][q] * av;
-          dr[nt][q] = yv[q] * u[nt][q] * gm * sg * (1.f + rv[q] * (1.f - sg));
+          const float u = (acc[nt][q] + cv[q] * ((q & 1) ? ce2.y : ce2.x)) * rsv[q];
+          gacc[nt][q & 1] += yv[q] * u * av;
+          dr[q] = cv[q] * yv[q] * u * gm * sg * (1.f + rv[q] * (1.f - sg));
           dO[nt][q] = yv[q] * gm * av;  // du
-          if (q < 2) m0 += dO[nt][q] * u[nt][q]; else m1 += dO[nt][q] * u[nt][q];
+          if (q < 2) m0 += dO[nt][q] * u; else m1 += dO[nt][q] * u;
         }
+        // stage dr into this warp's r rows (consumed)
+        *reinterpret_cast<uint32_t*>(rtb + o0) = pack_bf16(dr[0], dr[1]);
+        *reinterpret_cast<uint32_t*>(rtb + o1) = pack_bf16(dr[2], dr[3]);
       }
       m0 += __shfl_xor_sync(FULL, m0, 1); m0 += __shfl_xor_sync(FULL, m0, 2);
       m1 += __shfl_xor_sync(FULL, m1, 1); m1 += __shfl_xor_sync(FULL, m1, 2);
       m0 /= DH; m1 /= DH;
+      const float mv[4] = {m0, m0, m1, m1};
 #pragma unroll
       for (int nt = 0; nt < DH / 8; ++nt) {
-        dO[nt][0] = rs0 * (dO[nt][0] - u[nt][0] * m0);
-        dO[nt][1] = rs0 * (dO[nt][1] - u[nt][1] * m0);
-        dO[nt][2] = rs1 * (dO[nt][2] - u[nt][2] * m1);
-        dO[nt][3] = rs1 * (dO[nt][3] - u[nt][3] * m1);
-      }
-      // stage dr into this warp's r rows (consumed)
+        const float2 ce2 = *reinterpret_cast<const float2*>(s_cen + nt * 8 + 2 * t4);
 #pragma unroll
-      for (int nt = 0; nt < DH / 8; ++nt) {
-        *reinterpret_cast<uint32_t*>(rtb + swz<C::CPR>(r0w + g, nt) + t4 * 4) =
-            pack_bf16(va ? dr[nt][0] : 0.f, va ? dr[nt][1] : 0.f);
-        *reinterpret_cast<uint32_t*>(rtb + swz<C::CPR>(r0w + g + 8, nt) + t4 * 4) =
-            pack_bf16(vb ? dr[nt][2] : 0.f, vb ? dr[nt][3] : 0.f);
+        for (int q = 0; q < 4; ++q) {
+          const float u = (acc[nt][q] + cv[q] * ((q & 1) ? ce2.y : ce2.x)) * rsv[q];
+          dO[nt][q] = rsv[q] * (dO[nt][q] - u * mv[q]);
+        }
       }
     } else {
 #pragma unroll
@@ -701,7 +702,7 @@ __global__ void __launch_bounds__(BqCfg<DH, NORM>::NW * 32) k_bwd_q_bf16(const B
   seq_tiles(a.seq, a.chunks, b, first, count);
   if (!arrive_last(a.counters + (size_t)b * H + h, count)) return;
   combine_state(a.partial, nullptr, first, count, H, h, DH, b * H + h, false, a.dstate, a.dstate_bf,
-                nullptr, nullptr);
+                nullptr, nullptr, nullptr, a.center);
 }
 
 // =====================================================================
@@ -723,7 +724,7 @@ __global__ void __launch_bounds__(128) k_bwd_kv_bf16(const BwdKVArgs a) {
   bf16* Ss = reinterpret_cast<bf16*>(smem);
   uint8_t* tiles = smem + DH * C::SPAD * 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (*a.err) return;
+  if (a.err && *a.err) return;
   int b, row0, nvalid, tin;
   if (!map_tile(a.seq, a.tiles, blockIdx.x, b, row0, nvalid, tin)) return;
   const int h = blockIdx.y, H = a.H;
@@ -742,6 +743,11 @@ __global__ void __launch_bounds__(128) k_bwd_kv_bf16(const BwdKVArgs a) {
   const float mseq = logits ? a.state_m[b * H + h] : 0.f;
 
   load_state_bf<DH, 128>(Ss, a.dstate_bf + (size_t)(b * H + h) * DH * C::BLD);
+  // dz column in fp32: dz (uncentred forward state) or dz'' = dz' - bf16(dS) c
+  // (centred forward state, see combine_state), so that dk~ = bf16(dS) v + dz
+  // in both cases with the raw bf16 v as the tensor-core operand.
+  __shared__ float s_dz[DH];
+  for (int e = tid; e < DH; e += 128) s_dz[e] = a.dstate[((size_t)(b * H + h) * DH + e) * state_ld(DH) + DH];
   auto kt = [&](int buf) { return tiles + buf * (2 * R::TILE + R::TT * 4); };
   auto load = [&](int buf, int s) {
     const uint32_t kb = smem_u32(kt(buf)), vb = kb + R::TILE, gb = vb + R::TILE;
@@ -790,14 +796,6 @@ __global__ void __launch_bounds__(128) k_bwd_kv_bf16(const BwdKVArgs a) {
     for (int ks = 0; ks < DH / 16; ++ks) {
       uint32_t av[4], ak[4];
       a_rows<DH>(vb, r0w, ks, lane, av);
-      if (a.center) {  // v' = v - c: the forward state was centred, dz holds dz' = dz + dS c
-        const float* cp = a.center + (size_t)(b * H + h) * DH + ks * 16 + 2 * t4;
-        const float c0 = cp[0], c1 = cp[1], c8 = cp[8], c9 = cp[9];
-        av[0] = pack_bf16(bf_lo(av[0]) - c0, bf_hi(av[0]) - c1);
-        av[1] = pack_bf16(bf_lo(av[1]) - c0, bf_hi(av[1]) - c1);
-        av[2] = pack_bf16(bf_lo(av[2]) - c8, bf_hi(av[2]) - c9);
-        av[3] = pack_bf16(bf_lo(av[3]) - c8, bf_hi(av[3]) - c9);
-      }
       a_rows<DH>(kb, r0w, ks, lane, ak);
       ak[0] = pack_bf16(phi_f(bf_lo(ak[0])) * gr0, phi_f(bf_hi(ak[0])) * gr0);
       ak[1] = pack_bf16(phi_f(bf_lo(ak[1])) * gr1, phi_f(bf_hi(ak[1])) * gr1);
@@ -822,8 +820,7 @@ __global__ void __launch_bounds__(128) k_bwd_kv_bf16(const BwdKVArgs a) {
 #pragma unroll
     for (int nt = 0; nt < DH / 8; ++nt) {
       const int e = nt * 8 + 2 * t4;
-      const float dz0 = __bfloat162float(Ss[e * C::SPAD + DH]);
-      const float dz1 = __bfloat162float(Ss[(e + 1) * C::SPAD + DH]);
+      const float dz0 = s_dz[e], dz1 = s_dz[e + 1];
       acck[nt][0] += dz0; acck[nt][1] += dz1; acck[nt][2] += dz0; acck[nt][3] += dz1;
       const uint32_t k0 = *reinterpret_cast<const uint32_t*>(ktb + swz<C::CPR>(r0w + g, nt) + t4 * 4);
       const uint32_t k1 = *reinterpret_cast<const uint32_t*>(ktb + swz<C::CPR>(r0w + g + 8, nt) + t4 * 4);

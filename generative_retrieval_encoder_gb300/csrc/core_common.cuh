@@ -33,10 +33,19 @@ __device__ __forceinline__ bool arrive_last(int* counter, int count) {
 // its mean; the differences that the backward takes (S - z o^T, dS v + dz)
 // then no longer cancel in bf16 operands.  S' is formed here in fp32; c goes
 // to center[seqh][dh].  Then `state` and the bf16 copy hold [S' | z | 0].
+//
+// Backward use (fwd_center != null, the combine of [dS | dz']): the key side
+// computes dk~_j = dS (v_j - c) + dz'.  So that it can feed the exact bf16
+// v_j to the tensor cores, the z column is replaced here, in fp32, by
+// dz'' = dz' - bf16(dS) c, using the same bf16-rounded dS that the key side
+// multiplies with: then bf16(dS) v_j + dz'' = bf16(dS) (v_j - c) + dz' exactly
+// up to fp32 rounding, and no rounding of (v_j - c) enters the gate gradient
+// (whose sum over a sequence cancels to ~1/sqrt(L) of its terms).
 __device__ inline void combine_state(const float* partial, const float* partial_m, int first,
                                      int count, int H, int h, int dh, int seqh, bool logits,
                                      float* state, bf16* state_bf, float* state_m,
-                                     float* pub_state, float* center = nullptr) {
+                                     float* pub_state, float* center = nullptr,
+                                     const float* fwd_center = nullptr) {
   const int LD = state_ld(dh);
   const int n = dh * LD;
   float m = 0.f;
@@ -86,6 +95,17 @@ __device__ inline void combine_state(const float* partial, const float* partial_
       const int e = (4 * i + u) / LD, f = (4 * i + u) % LD;
       if (state_bf && !center) state_bf[((size_t)seqh * dh + e) * state_bf_ld(dh) + f] = __float2bfloat16_rn(v4[u]);
       if (pub_state && f <= dh) pub_state[((size_t)seqh * dh + e) * (dh + 1) + f] = v4[u];
+    }
+  }
+  if (fwd_center) {
+    float* St = state + (size_t)seqh * n;
+    __syncthreads();  // this CTA's state writes are visible to the whole CTA
+    const float* c = fwd_center + (size_t)seqh * dh;
+    for (int e = threadIdx.x; e < dh; e += blockDim.x) {
+      float acc = St[e * LD + dh];
+      for (int f = 0; f < dh; ++f) acc -= __bfloat162float(__float2bfloat16_rn(St[e * LD + f])) * c[f];
+      St[e * LD + dh] = acc;
+      if (state_bf) state_bf[((size_t)seqh * dh + e) * state_bf_ld(dh) + dh] = __float2bfloat16_rn(acc);
     }
   }
   if (center) {

@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(256) k_reduce_f32(const ReduceArgs a) {
   float* kt = sm;            // [FT][dh]  g phi(k)
   float* vt = sm + FT * dh;  // [FT][dh+1]  [v | 1]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (*a.err) return;
+  if (a.err && *a.err) return;
   int b, row0, nvalid, cin;
   if (!map_tile(a.seq, a.chunks, blockIdx.x, b, row0, nvalid, cin)) return;
   const int h = blockIdx.y, H = a.H;
@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(256) k_readout_f32(const ReadoutArgs a) {
   float* S = sm;             // [dh][dh+1]
   float* qs = sm + dh * W;   // [8][dh]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (*a.err) return;
+  if (a.err && *a.err) return;
   int b, row0, nvalid, tin;
   if (!map_tile(a.seq, a.tiles, blockIdx.x, b, row0, nvalid, tin)) return;
   const int h = blockIdx.y, H = a.H;
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(256) k_bwd_q_f32(const BwdQArgs a) {
   float* qt = S + dh * W;       // [FT][dh]    phi(q)
   float* dnt = qt + FT * dh;    // [FT][dh+1]  [dn | dden]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (*a.err) return;
+  if (a.err && *a.err) return;
   int b, row0, nvalid, cin;
   if (!map_tile(a.seq, a.chunks, blockIdx.x, b, row0, nvalid, cin)) return;
   const int h = blockIdx.y, H = a.H;
@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(256) k_bwd_kv_f32(const BwdKVArgs a) {
   float* ks = S + dh * W;        // [8][dh] g phi(k)
   float* vs = ks + 8 * dh;       // [8][dh] v
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (*a.err) return;
+  if (a.err && *a.err) return;
   int b, row0, nvalid, tin;
   if (!map_tile(a.seq, a.tiles, blockIdx.x, b, row0, nvalid, tin)) return;
   const int h = blockIdx.y, H = a.H;

@@ -113,7 +113,7 @@ struct GemmArgs {
 struct ConvArgs {
   const void* x; const void* w; const void* b;  // io dtype; b may be null
   void* xt;                                     // io dtype [T, d]
-  const float* dxt;                             // backward: fp32 [T, d]
+  const void* dxt;                              // backward: io dtype [T, d]
   void* dx;                                     // backward: io dtype [T, d]
   float* part;                                  // backward: [gridDim.x][d][5] (dw 0..3, db)
   int T, d;

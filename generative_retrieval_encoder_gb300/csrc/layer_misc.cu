@@ -2,6 +2,8 @@
 // tile prefix sums + validation), the depthwise causal Conv1d of Eq. 4 and its
 // backward, weight packing, and fixed-order reductions of per-block partial
 // gradients.
+#include <algorithm>
+
 #include "kernels.h"
 
 namespace gbla {
@@ -112,141 +114,196 @@ __device__ __forceinline__ void vstore(T* p, const float* in) {
   *reinterpret_cast<U*>(p) = u;
 }
 
-constexpr int RUN = 16;   // rows per thread, forward conv
-constexpr int RUNB = 64;  // rows per block, backward conv
+constexpr int RUN = 16;    // rows per thread, forward conv
+constexpr int RUNB = 4;    // rows per inner run, backward conv
+constexpr int BW_ROWGROUPS = 4;  // backward: row groups per block (block = 64 channel vectors x 4)
+
+template <typename T>
+__device__ __forceinline__ typename Vec<T>::U vraw(const T* p) {
+  return *reinterpret_cast<const typename Vec<T>::U*>(p);
+}
+template <typename T>
+__device__ __forceinline__ void vcvt(const typename Vec<T>::U& u, float* out) {
+  const T* e = reinterpret_cast<const T*>(&u);
+#pragma unroll
+  for (int i = 0; i < Vec<T>::N; ++i) out[i] = to_f<T>(e[i]);
+}
+
+// The 4 taps of channels c0 .. c0 + V - 1 (w is [d][4], contiguous: 4 vector
+// loads) and their biases (b may be null).
+template <typename T>
+__device__ __forceinline__ void load_taps(const T* w, const T* b, int c0, float (&wt)[Vec<T>::N][4],
+                                          float (&bias)[Vec<T>::N]) {
+  constexpr int V = Vec<T>::N;
+  typedef typename Vec<T>::U U;
+  const U* wp = reinterpret_cast<const U*>(w + (size_t)c0 * 4);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float f[V];
+    vcvt<T>(wp[j], f);
+#pragma unroll
+    for (int i = 0; i < V; ++i) wt[(j * V + i) / 4][(j * V + i) % 4] = f[i];
+  }
+  if (b) {
+    vcvt<T>(*reinterpret_cast<const U*>(b + c0), bias);
+  } else {
+#pragma unroll
+    for (int i = 0; i < V; ++i) bias[i] = 0.f;
+  }
+}
 
 // Eq. 4 Conv1d (depthwise, causal, kernel 4):
 //   x~[l, c] = b[c] + sum_t w[c, t] x[l - 3 + t, c]   (rows before the sequence start read 0)
-// Each thread owns VEC channels and RUN consecutive rows (sliding window).
+// Work item = (channel vector, run of RUN rows); consecutive threads take
+// consecutive channel vectors (coalesced).  The RUN + 3 input rows of a run
+// are loaded up front so that all of them are in flight together.
 template <typename T>
-__global__ void __launch_bounds__(128) k_conv_fwd(const ConvArgs a) {
+__global__ void __launch_bounds__(256) k_conv_fwd(const ConvArgs a) {
   constexpr int V = Vec<T>::N;
-  if (*a.err) return;
-  const int c0 = (blockIdx.y * 128 + threadIdx.x) * V;
-  if (c0 >= a.d) return;
-  const int r0 = blockIdx.x * RUN, r1 = min(a.T, r0 + RUN);
-  if (r0 >= r1) return;
+  typedef typename Vec<T>::U U;
+  if (a.err && *a.err) return;
+  const int CV = a.d / V;
+  const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int cv = (int)(item % CV);
+  const int r0 = (int)(item / CV) * RUN;
+  if (r0 >= a.T) return;
+  const int c0 = cv * V;
   const T* x = (const T*)a.x;
   T* xt = (T*)a.xt;
-  float w[V][4], bias[V];
+  U raw[RUN + 3];
 #pragma unroll
-  for (int i = 0; i < V; ++i) {
-#pragma unroll
-    for (int t = 0; t < 4; ++t) w[i][t] = to_f<T>(((const T*)a.w)[(size_t)(c0 + i) * 4 + t]);
-    bias[i] = a.b ? to_f<T>(((const T*)a.b)[c0 + i]) : 0.f;
+  for (int j = 0; j < RUN + 3; ++j) {
+    const int l = r0 - 3 + j;
+    if (l >= 0 && l < a.T) raw[j] = vraw<T>(x + (size_t)l * a.d + c0);
+    else raw[j] = U{};
   }
+  float w[V][4], bias[V];
+  load_taps<T>((const T*)a.w, (const T*)a.b, c0, w, bias);
   SeqCursor cur(a.seq);
   cur.seek(r0);
-  float p3[V], p2[V], p1[V], xc[V];
 #pragma unroll
-  for (int i = 0; i < V; ++i) p3[i] = p2[i] = p1[i] = 0.f;
-  if (r0 - 3 >= cur.s0) vload<T>(x + (size_t)(r0 - 3) * a.d + c0, p3);
-  if (r0 - 2 >= cur.s0) vload<T>(x + (size_t)(r0 - 2) * a.d + c0, p2);
-  if (r0 - 1 >= cur.s0) vload<T>(x + (size_t)(r0 - 1) * a.d + c0, p1);
-  for (int l = r0; l < r1; ++l) {
-    if (l >= cur.send) {
-      cur.seek(l);
+  for (int i = 0; i < RUN; ++i) {
+    const int l = r0 + i;
+    if (l < a.T) {
+      if (l >= cur.send) cur.seek(l);
+      float o[V];
 #pragma unroll
-      for (int i = 0; i < V; ++i) p3[i] = p2[i] = p1[i] = 0.f;
+      for (int c = 0; c < V; ++c) o[c] = 0.f;
+      if (l < cur.vend) {
+#pragma unroll
+        for (int c = 0; c < V; ++c) o[c] = bias[c];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          if (l - 3 + t >= cur.s0) {
+            float xv[V];
+            vcvt<T>(raw[i + t], xv);
+#pragma unroll
+            for (int c = 0; c < V; ++c) o[c] += w[c][t] * xv[c];
+          }
+        }
+      }
+      vstore<T>(xt + (size_t)l * a.d + c0, o);
     }
-    float o[V];
-    if (l < cur.vend) {
-      vload<T>(x + (size_t)l * a.d + c0, xc);
-#pragma unroll
-      for (int i = 0; i < V; ++i) o[i] = bias[i] + w[i][0] * p3[i] + w[i][1] * p2[i] + w[i][2] * p1[i] + w[i][3] * xc[i];
-    } else {
-#pragma unroll
-      for (int i = 0; i < V; ++i) { xc[i] = 0.f; o[i] = 0.f; }
-    }
-    vstore<T>(xt + (size_t)l * a.d + c0, o);
-#pragma unroll
-    for (int i = 0; i < V; ++i) { p3[i] = p2[i]; p2[i] = p1[i]; p1[i] = xc[i]; }
   }
 }
 
 // Backward of Eq. 4 Conv1d.  For rows l of a sequence (valid rows [s0, vend)):
 //   dx[l]   = sum_t w[t] dx~[l + 3 - t]   (terms with l + 3 - t < vend)
 //   dw[t]  += x[l - 3 + t] dx~[l];   db += dx~[l]
-// Block bx owns rows [bx RUNB, bx RUNB + RUNB); each thread VEC channels.
-// Per-block parameter partials go to part[bx][c][0..4].
+// Block (bx, by): 64 channel vectors x 4 row groups over rows
+// [by rows_per_block, ...); a row group takes runs of RUNB rows, loading the
+// run's x and dx~ rows up front.  The 4 row groups' parameter partials are
+// added in a fixed order into part[by][c][0..4].
 template <typename T>
-__global__ void __launch_bounds__(128) k_conv_bwd(const ConvArgs a) {
+__global__ void __launch_bounds__(256) k_conv_bwd(const ConvArgs a, int rows_per_block) {
   constexpr int V = Vec<T>::N;
-  if (*a.err) return;
-  const int c0 = (blockIdx.y * 128 + threadIdx.x) * V;
-  if (c0 >= a.d) return;
-  const int r0 = blockIdx.x * RUNB, r1 = min(a.T, r0 + RUNB);
+  typedef typename Vec<T>::U U;
+  __shared__ float red[BW_ROWGROUPS - 1][64][5 * V];
+  if (a.err && *a.err) return;
+  const int CV = a.d / V;
+  const int tx = threadIdx.x & 63, rg = threadIdx.x >> 6;
+  const int cv = blockIdx.x * 64 + tx;
+  const bool active = cv < CV;
+  const int c0 = cv * V;
+  const int rb0 = blockIdx.y * rows_per_block, rb1 = min(a.T, rb0 + rows_per_block);
   const T* x = (const T*)a.x;
-  float w[V][4];
-#pragma unroll
-  for (int i = 0; i < V; ++i)
-#pragma unroll
-    for (int t = 0; t < 4; ++t) w[i][t] = to_f<T>(((const T*)a.w)[(size_t)(c0 + i) * 4 + t]);
+  const T* gx = (const T*)a.dxt;
   float dw[V][4], db[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) { db[i] = 0.f; dw[i][0] = dw[i][1] = dw[i][2] = dw[i][3] = 0.f; }
-  auto ldg = [&](int row, float* out) {  // dx~ row (fp32)
-    const float4* p = reinterpret_cast<const float4*>(a.dxt + (size_t)row * a.d + c0);
-#pragma unroll
-    for (int i = 0; i < V / 4; ++i) {
-      const float4 u = p[i];
-      out[4 * i] = u.x; out[4 * i + 1] = u.y; out[4 * i + 2] = u.z; out[4 * i + 3] = u.w;
-    }
-  };
-  if (r0 < r1) {
+  if (active) {
+    float w[V][4], nobias[V];
+    load_taps<T>((const T*)a.w, nullptr, c0, w, nobias);
     SeqCursor cur(a.seq);
-    cur.seek(r0);
-    float p3[V], p2[V], p1[V], xc[V];  // x[l-3], x[l-2], x[l-1], x[l]
-    float g0[V], g1[V], g2[V], g3[V];  // dx~[l .. l+3]
-    auto reset = [&](int l) {
+    for (int r0 = rb0 + rg * RUNB; r0 < rb1; r0 += BW_ROWGROUPS * RUNB) {
+      U xr[RUNB + 3], gr[RUNB + 3];  // x[r0-3 .. r0+RUNB-1], dx~[r0 .. r0+RUNB+2]
 #pragma unroll
-      for (int i = 0; i < V; ++i) p3[i] = p2[i] = p1[i] = g0[i] = g1[i] = g2[i] = 0.f;
-      if (l - 3 >= cur.s0 && l - 3 < cur.vend) vload<T>(x + (size_t)(l - 3) * a.d + c0, p3);
-      if (l - 2 >= cur.s0 && l - 2 < cur.vend) vload<T>(x + (size_t)(l - 2) * a.d + c0, p2);
-      if (l - 1 >= cur.s0 && l - 1 < cur.vend) vload<T>(x + (size_t)(l - 1) * a.d + c0, p1);
-      if (l < cur.vend) ldg(l, g0);
-      if (l + 1 < cur.vend) ldg(l + 1, g1);
-      if (l + 2 < cur.vend) ldg(l + 2, g2);
-    };
-    reset(r0);
-    for (int l = r0; l < r1; ++l) {
-      if (l >= cur.send) {
-        cur.seek(l);
-        reset(l);
+      for (int j = 0; j < RUNB + 3; ++j) {
+        const int lx = r0 - 3 + j, lg = r0 + j;
+        xr[j] = (lx >= 0 && lx < a.T) ? vraw<T>(x + (size_t)lx * a.d + c0) : U{};
+        gr[j] = (lg < a.T) ? vraw<T>(gx + (size_t)lg * a.d + c0) : U{};
       }
-      float o[V];
-      if (l < cur.vend) {
-        vload<T>(x + (size_t)l * a.d + c0, xc);
+      cur.seek(r0);
 #pragma unroll
-        for (int i = 0; i < V; ++i) g3[i] = 0.f;
-        if (l + 3 < cur.vend) ldg(l + 3, g3);
+      for (int i = 0; i < RUNB; ++i) {
+        const int l = r0 + i;
+        if (l < rb1) {
+          if (l >= cur.send) cur.seek(l);
+          float o[V];
 #pragma unroll
-        for (int i = 0; i < V; ++i) {
-          o[i] = w[i][3] * g0[i] + w[i][2] * g1[i] + w[i][1] * g2[i] + w[i][0] * g3[i];
-          dw[i][0] += p3[i] * g0[i];
-          dw[i][1] += p2[i] * g0[i];
-          dw[i][2] += p1[i] * g0[i];
-          dw[i][3] += xc[i] * g0[i];
-          db[i] += g0[i];
+          for (int c = 0; c < V; ++c) o[c] = 0.f;
+          if (l < cur.vend) {
+            float g0[V];
+            vcvt<T>(gr[i], g0);
+#pragma unroll
+            for (int k = 1; k < 4; ++k) {  // dx~[l + k] feeds tap 3 - k
+              if (l + k < cur.vend) {
+                float gk[V];
+                vcvt<T>(gr[i + k], gk);
+#pragma unroll
+                for (int c = 0; c < V; ++c) o[c] += w[c][3 - k] * gk[c];
+              }
+            }
+#pragma unroll
+            for (int c = 0; c < V; ++c) {
+              o[c] += w[c][3] * g0[c];
+              db[c] += g0[c];
+            }
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              if (l - 3 + t >= cur.s0) {
+                float xv[V];
+                vcvt<T>(xr[i + t], xv);
+#pragma unroll
+                for (int c = 0; c < V; ++c) dw[c][t] += xv[c] * g0[c];
+              }
+            }
+          }
+          vstore<T>((T*)a.dx + (size_t)l * a.d + c0, o);
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < V; ++i) { o[i] = 0.f; xc[i] = 0.f; g3[i] = 0.f; }
-      }
-      vstore<T>((T*)a.dx + (size_t)l * a.d + c0, o);
-#pragma unroll
-      for (int i = 0; i < V; ++i) {
-        p3[i] = p2[i]; p2[i] = p1[i]; p1[i] = xc[i];
-        g0[i] = g1[i]; g1[i] = g2[i]; g2[i] = g3[i];
       }
     }
   }
-  float* P = a.part + (size_t)blockIdx.x * a.d * 5;
+  if (rg > 0 && active) {
 #pragma unroll
-  for (int i = 0; i < V; ++i) {
+    for (int c = 0; c < V; ++c) {
 #pragma unroll
-    for (int t = 0; t < 4; ++t) P[(size_t)(c0 + i) * 5 + t] = dw[i][t];
-    P[(size_t)(c0 + i) * 5 + 4] = db[i];
+      for (int t = 0; t < 4; ++t) red[rg - 1][tx][5 * c + t] = dw[c][t];
+      red[rg - 1][tx][5 * c + 4] = db[c];
+    }
+  }
+  __syncthreads();
+  if (rg == 0 && active) {
+    float* P = a.part + (size_t)blockIdx.y * a.d * 5;
+#pragma unroll
+    for (int c = 0; c < V; ++c) {
+#pragma unroll
+      for (int t = 0; t < 5; ++t) {
+        float s = t < 4 ? dw[c][t] : db[c];
+        for (int g = 0; g < BW_ROWGROUPS - 1; ++g) s += red[g][tx][5 * c + t];
+        P[(size_t)(c0 + c) * 5 + t] = s;
+      }
+    }
   }
 }
 
@@ -326,19 +383,22 @@ cudaError_t launch_plan(const SeqDesc& s, int ntile, const int* tile_sizes, int3
 
 cudaError_t launch_conv_fwd(const ConvArgs& a, bool f32, cudaStream_t st) {
   const int V = f32 ? 4 : 8;
-  const dim3 grid((a.T + RUN - 1) / RUN, (a.d / V + 127) / 128);
-  if (f32) k_conv_fwd<float><<<grid, 128, 0, st>>>(a);
-  else k_conv_fwd<bf16><<<grid, 128, 0, st>>>(a);
+  const long long items = (long long)((a.T + RUN - 1) / RUN) * (a.d / V);
+  const unsigned grid = (unsigned)((items + 255) / 256);
+  if (f32) k_conv_fwd<float><<<grid, 256, 0, st>>>(a);
+  else k_conv_fwd<bf16><<<grid, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
-int conv_bwd_blocks(int T) { return (T + RUNB - 1) / RUNB; }
+int conv_bwd_blocks(int T) { return std::max(1, std::min(1024, (T + 127) / 128)); }
 
 cudaError_t launch_conv_bwd(const ConvArgs& a, bool f32, int nblk, cudaStream_t st) {
   const int V = f32 ? 4 : 8;
-  const dim3 grid(nblk, (a.d / V + 127) / 128);
-  if (f32) k_conv_bwd<float><<<grid, 128, 0, st>>>(a);
-  else k_conv_bwd<bf16><<<grid, 128, 0, st>>>(a);
+  const int unit = RUNB * BW_ROWGROUPS;
+  const int rows = ((a.T + nblk - 1) / nblk + unit - 1) / unit * unit;
+  const dim3 grid((a.d / V + 63) / 64, nblk);
+  if (f32) k_conv_bwd<float><<<grid, 256, 0, st>>>(a, rows);
+  else k_conv_bwd<bf16><<<grid, 256, 0, st>>>(a, rows);
   return cudaGetLastError();
 }
 
