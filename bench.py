@@ -215,6 +215,33 @@ def run_reference(args, wl, rank: int):
     print(json.dumps(line), flush=True)
 
 
+def l_scaling(wl, dev, timed, tokens: int = 262144, steps: int = 3):
+    """fwd+bwd and forward tokens/s for L = 2k .. 32k at B L = tokens (the
+    long-history recipe: repeated low-rank pattern); flat means linear in L."""
+    import torch
+    from generative_retrieval_encoder_gb300 import gbla
+    from generative_retrieval_encoder_gb300.workloads import Workload
+    out = {"tokens": tokens, "fwd_bwd_tokens_per_s": {}, "fwd_tokens_per_s": {}}
+    for L in (2048, 4096, 8192, 16384, 32768):
+        w = Workload(f"scaling L={L}", tokens // L, L, wl.d, wl.H, wl.dh, pattern=True, seed=1003)
+        shape, x_h, dy_h, P = make_inputs(w, dev)
+        x, dy = x_h.to(dev), dy_h.to(dev)
+        y = torch.empty(tokens, w.H * w.dh, dtype=x.dtype, device=dev)
+        saved = torch.empty(gbla.gbla_saved_size(shape), dtype=torch.uint8, device=dev)
+        ws_f = gbla.workspace(shape, gbla.GBLA_OP_FORWARD, dev)
+        ws_b = gbla.workspace(shape, gbla.GBLA_OP_BACKWARD, dev)
+        fwd = lambda: gbla.gbla_forward(shape, x, P, y=y, saved=saved, ws=ws_f)
+        step = lambda: (fwd(), gbla.gbla_backward(shape, x, P, saved, dy, ws=ws_b))
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
+        out["fwd_bwd_tokens_per_s"][L] = tokens / (timed(step, steps) * 1e-3)
+        out["fwd_tokens_per_s"][L] = tokens / (timed(fwd, steps) * 1e-3)
+        del x, dy, y, saved, ws_f, ws_b
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, wl, rank: int, world: int, local_rank: int):
     import torch
     import torch.distributed as dist
@@ -317,6 +344,9 @@ def run_ours(args, wl, rank: int, world: int, local_rank: int):
     h2d = x.numel() * x.element_size() + dy.numel() * dy.element_size()
     d2h = sum(v.numel() * v.element_size() for v in host_g.values())
 
+    # linearity in L: the same number of tokens (B L = 262144) at L = 2k .. 32k
+    scaling = l_scaling(wl, dev, timed) if args.scaling else None
+
     if rank != 0:
         return
     peaks, peak_src = load_peaks()
@@ -358,7 +388,8 @@ def run_ours(args, wl, rank: int, world: int, local_rank: int):
             "e2e": {"value": tokens * world / (ms_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
             "gpu_launches": launches_per_step * args.steps,
-            "clocks": clk.summary()}
+            "clocks": clk.summary(),
+            "l_scaling": scaling}
     print(json.dumps(line), flush=True)
 
 
@@ -369,6 +400,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="train2k", choices=sorted(workloads()))
+    ap.add_argument("--no-scaling", dest="scaling", action="store_false",
+                    help="skip the L = 2k .. 32k linearity sweep")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

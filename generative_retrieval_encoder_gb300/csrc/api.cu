@@ -341,7 +341,7 @@ gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* con
   // Eq. 4, 5, 7: projections and gate
   const void* W[4] = {W_q, W_k, W_v, W_r};
   void* Wt = at<char>(ws, l.Wt);
-  GBLA_CHECK(launch_pack_weights(W, w_g, p.d, p.H, p.dh, p.f32, nullptr, Wt, p.NP, c.st), "pack");
+  GBLA_CHECK(launch_pack_weights(W, w_g, p.d, p.H, p.dh, p.f32, Wt, p.NP, c.st), "pack");
   GemmArgs ga{};
   ga.A = xt; ga.lda = p.d; ga.a_kmajor = 1;
   ga.B = Wt; ga.ldb = p.NP; ga.b_kmajor = 0;  // B(n, k) = W_all[k][n]: N-major
@@ -400,7 +400,7 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   GBLA_CHECK(cudaMemsetAsync(at<char>(ws, l.gamma_part), 0, (size_t)p.n_chunks * p.H * p.dh * 4, c.st), "memset");
   GBLA_CHECK(cudaMemsetAsync(at<char>(ws, l.bg_part), 0, (size_t)p.n_tiles * p.H * 4, c.st), "memset");
   const void* W[4] = {W_q, W_k, W_v, W_r};
-  GBLA_CHECK(launch_pack_weights(W, w_g, p.d, p.H, p.dh, p.f32, nullptr, at<char>(ws, l.Wp), p.NP, c.st), "pack");
+  GBLA_CHECK(launch_pack_weights(W, w_g, p.d, p.H, p.dh, p.f32, at<char>(ws, l.Wp), p.NP, c.st), "pack");
   // Eq. 7 + Eq. 5/6 query side: dr, dq, [dS | dz]
   BwdQArgs q{};
   q.q = P; q.ldq = 4 * p.HD;

@@ -151,10 +151,10 @@ cudaError_t launch_conv_fwd(const ConvArgs& a, bool f32, cudaStream_t st);
 cudaError_t launch_conv_bwd(const ConvArgs& a, bool f32, int nblk, cudaStream_t st);
 int conv_bwd_blocks(int T);
 
-// Packs W_q | W_k | W_v | W_r | w_g into Wt [N1][d] (transposed, N1 = 4*H*dh + H)
-// and/or Wp [d][np] (row-major, zero-padded to np columns).  Either may be null.
+// Packs W_q | W_k | W_v | W_r | w_g into Wp [d][np] (row-major, zero-padded
+// past 4*H*dh + H columns).
 cudaError_t launch_pack_weights(const void* const* W, const void* w_g, int d, int H, int dh,
-                                bool f32, void* Wt, void* Wp, int np, cudaStream_t st);
+                                bool f32, void* Wp, int np, cudaStream_t st);
 
 // out[i] = sum_{s < S} part[s * stride + i] for i < n (fixed order); fp32.
 cudaError_t launch_sum_parts(const float* part, int S, int64_t stride, int64_t n, float* out,

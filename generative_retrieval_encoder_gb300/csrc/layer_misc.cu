@@ -307,21 +307,21 @@ __global__ void __launch_bounds__(256) k_conv_bwd(const ConvArgs a, int rows_per
   }
 }
 
-// Wt[n][c] (n < 4*H*dh + H) and/or Wp[c][n] (n < np, zero past 4*H*dh + H).
+// Wp[c][n] = [W_q | W_k | W_v | W_r | w_g | 0][c][n] for n < np: one block
+// row per c (blockIdx.y), consecutive threads take consecutive n.
 template <typename T>
-__global__ void k_pack(const T* Wq, const T* Wk, const T* Wv, const T* Wr, const T* wg, int d, int H,
-                       int dh, T* Wt, T* Wp, int np) {
-  const int HD = H * dh, N1 = 4 * HD + H;
-  const size_t total = (size_t)d * np;
+__global__ void k_pack(const T* Wq, const T* Wk, const T* Wv, const T* Wr, const T* wg, int H, int dh,
+                       T* Wp, int np) {
+  const int HD = H * dh;
+  const int c = blockIdx.y;
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= np) return;
+  const int m = n / HD, j = n - m * HD;
   const T* Ws[4] = {Wq, Wk, Wv, Wr};
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-    const int c = (int)(i / np), n = (int)(i % np);
-    T v = from_f<T>(0.f);
-    if (n < 4 * HD) v = Ws[n / HD][(size_t)c * HD + n % HD];
-    else if (n < N1) v = wg[(size_t)c * H + n - 4 * HD];
-    if (Wp) Wp[i] = v;
-    if (Wt && n < N1) Wt[(size_t)n * d + c] = v;
-  }
+  T v = from_f<T>(0.f);
+  if (m < 4) v = Ws[m][(size_t)c * HD + j];
+  else if (n - 4 * HD < H) v = wg[(size_t)c * H + n - 4 * HD];
+  Wp[(size_t)c * np + n] = v;
 }
 
 // Column sums of a [S][stride] partial array in a fixed order: block b owns
@@ -403,15 +403,14 @@ cudaError_t launch_conv_bwd(const ConvArgs& a, bool f32, int nblk, cudaStream_t 
 }
 
 cudaError_t launch_pack_weights(const void* const* W, const void* w_g, int d, int H, int dh, bool f32,
-                                void* Wt, void* Wp, int np, cudaStream_t st) {
-  const int grid = grid_for((size_t)d * np);
+                                void* Wp, int np, cudaStream_t st) {
+  const dim3 grid((np + 255) / 256, d);
   if (f32)
     k_pack<float><<<grid, 256, 0, st>>>((const float*)W[0], (const float*)W[1], (const float*)W[2],
-                                        (const float*)W[3], (const float*)w_g, d, H, dh, (float*)Wt,
-                                        (float*)Wp, np);
+                                        (const float*)W[3], (const float*)w_g, H, dh, (float*)Wp, np);
   else
     k_pack<bf16><<<grid, 256, 0, st>>>((const bf16*)W[0], (const bf16*)W[1], (const bf16*)W[2],
-                                       (const bf16*)W[3], (const bf16*)w_g, d, H, dh, (bf16*)Wt, (bf16*)Wp, np);
+                                       (const bf16*)W[3], (const bf16*)w_g, H, dh, (bf16*)Wp, np);
   return cudaGetLastError();
 }
 
