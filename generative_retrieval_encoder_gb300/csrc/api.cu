@@ -226,7 +226,12 @@ struct Ctx {
   int* err;          // workspace error word (always valid)
   const int* kerr;   // what the state / conv kernels read: err, or null in the dense form
   cudaStream_t st;
+  int pre = 0;       // P holds [phi(q) | phi(k) | v | r] (the bf16 layer)
 };
+
+// The bf16 layer applies the feature map phi = elu + 1 to q and k in the
+// projection epilogue, so the state kernels read phi(q) and phi(k) directly.
+bool layer_pre(const Plan& p, const gbla_shape*) { return !p.f32; }
 
 gbla_status begin(const gbla_shape* s, int op, void* ws, size_t ws_bytes, void* stream, Ctx& c) {
   gbla_status r = make_plan(s, c.p);
@@ -274,6 +279,7 @@ gbla_status run_reduce(Ctx& c, const void* k, const void* v, int64_t ld, const f
   a.partial_m = at<float>(ws, c.l.partial_m);
   a.counters = at<int>(ws, c.l.cnt_f);
   a.state = state; a.state_bf = state_bf; a.state_m = state_m; a.pub_state = pub_state;
+  a.pre = c.pre;
   a.center = p.f32 ? nullptr : center;
   a.err = c.kerr;
   GBLA_CHECK(p.f32 ? launch_reduce_f32(a, p.n_chunks, c.st) : launch_reduce_bf16(a, p.n_chunks, c.st), "reduce");
@@ -338,6 +344,7 @@ gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* con
   ConvArgs ca{};
   ca.x = x; ca.w = conv_w; ca.b = conv_b; ca.xt = xt; ca.T = p.T; ca.d = p.d; ca.seq = c.seq; ca.err = c.kerr;
   GBLA_CHECK(launch_conv_fwd(ca, p.f32, c.st), "conv");
+  c.pre = layer_pre(p, shape) ? 1 : 0;
   // Eq. 4, 5, 7: projections and gate
   const void* W[4] = {W_q, W_k, W_v, W_r};
   void* Wt = at<char>(ws, l.Wt);
@@ -347,7 +354,8 @@ gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* con
   ga.B = Wt; ga.ldb = p.NP; ga.b_kmajor = 0;  // B(n, k) = W_all[k][n]: N-major
   ga.C = P; ga.ldc = 4 * p.HD;
   ga.M = p.T; ga.N = p.N1; ga.K = p.d; ga.k_split = (p.d + 31) / 32 * 32;
-  ga.epi = EPI_PROJ; ga.n_main = 4 * p.HD; ga.bias_g = shape->gate == GBLA_GATE_SIGMOID ? b_g : nullptr;
+  ga.epi = c.pre ? EPI_PROJ_PRE : EPI_PROJ; ga.n_main = 4 * p.HD; ga.hd = p.HD; ga.dh = p.dh;
+  ga.bias_g = shape->gate == GBLA_GATE_SIGMOID ? b_g : nullptr;
   ga.gate_mode = shape->gate == GBLA_GATE_SIGMOID ? 0 : 1; ga.gate = gate; ga.ldgate = p.H; ga.io_f32 = p.f32;
   ga.err = c.err;
   GBLA_CHECK(launch_gemm(ga, c.st), "projection gemm");
@@ -363,7 +371,7 @@ gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* con
   ra.q = P; ra.ldq = 4 * p.HD;
   ra.r = Pc + 3 * p.HD * es; ra.ldr = 4 * p.HD;
   ra.rms_w = rms_w; ra.eps = shape->rms_eps;
-  ra.state = state; ra.state_bf = state_bf; ra.center = center;
+  ra.state = state; ra.state_bf = state_bf; ra.center = center; ra.pre = c.pre;
   ra.out = y; ra.ldo = p.HD; ra.den = nullptr;
   ra.H = p.H; ra.dh = p.dh; ra.seq = c.seq; ra.tiles = c.tiles; ra.err = c.kerr;
   GBLA_CHECK(p.f32 ? launch_readout_f32(ra, true, p.n_tiles, c.st) : launch_readout_bf16(ra, true, p.n_tiles, c.st),
@@ -397,6 +405,7 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   const float* gate = at<const float>(const_cast<void*>(saved), s.gate);
   char* dP = at<char>(ws, l.dP);
   const bool sig = shape->gate == GBLA_GATE_SIGMOID;
+  const int pre = layer_pre(p, shape) ? 1 : 0;
   GBLA_CHECK(cudaMemsetAsync(at<char>(ws, l.gamma_part), 0, (size_t)p.n_chunks * p.H * p.dh * 4, c.st), "memset");
   GBLA_CHECK(cudaMemsetAsync(at<char>(ws, l.bg_part), 0, (size_t)p.n_tiles * p.H * 4, c.st), "memset");
   const void* W[4] = {W_q, W_k, W_v, W_r};
@@ -411,6 +420,7 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   q.state_bf = at<const bf16>(const_cast<void*>(saved), s.state_bf);
   const float* center = p.f32 ? nullptr : at<const float>(const_cast<void*>(saved), s.center);
   q.center = center;
+  q.pre = pre;
   q.dq = dP; q.lddq = p.NP;
   q.dr = dP + 3 * p.HD * es; q.lddr = p.NP;
   q.gamma_part = at<float>(ws, l.gamma_part);
@@ -427,6 +437,7 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   kv.state_m = at<const float>(const_cast<void*>(saved), s.state_m);
   kv.dstate = at<float>(ws, l.dstate); kv.dstate_bf = at<bf16>(ws, l.dstate_bf);
   kv.center = center;
+  kv.pre = pre;
   kv.dk = dP + p.HD * es; kv.lddk = p.NP;
   kv.dv = dP + 2 * p.HD * es; kv.lddv = p.NP;
   kv.ds = dP; kv.ldds = p.NP; kv.gate_grad = sig ? GG_SIGMOID : GG_SOFTMAX;

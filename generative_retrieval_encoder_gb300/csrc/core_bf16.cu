@@ -50,6 +50,12 @@ __device__ __forceinline__ void a_rows(uint32_t base, int r0, int ks, int lane, 
   ldsm_x4(base + swz<DH / 8>(r0 + ((mi & 1) << 3) + rr, 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
 }
 __device__ __forceinline__ uint32_t phi2(uint32_t v) { return pack_bf16(phi_f(bf_lo(v)), phi_f(bf_hi(v))); }
+// phi' from the raw value x, or (PRE) from the stored phi(x): phi' = min(1, phi).
+template <bool PRE>
+__device__ __forceinline__ float dphi_s(float x) { return PRE ? fminf(1.f, x) : dphi_f(x); }
+// phi(x) from the raw value, or (PRE) the stored phi(x) itself.
+template <bool PRE>
+__device__ __forceinline__ float phik(float x) { return PRE ? x : phi_f(x); }
 
 // =====================================================================
 // reduce: per (chunk, head) CTA, 8 warps.  Warp (wm, kg) owns state rows
@@ -65,7 +71,7 @@ struct RedCfg {
   static constexpr int SMEM = STAGES * (2 * TILE + TT * 4);
 };
 
-template <int DH>
+template <int DH, bool PRE>
 __global__ void __launch_bounds__(256) k_reduce_bf16(const ReduceArgs a) {
   using C = Cfg<DH>;
   using R = RedCfg<DH>;
@@ -144,17 +150,19 @@ __global__ void __launch_bounds__(256) k_reduce_bf16(const ReduceArgs a) {
       const int j0 = kk * 16;
       uint32_t a0, a1, a2, a3;
       ldsm_x4_t(kb + swz<C::CPR>(j0 + ((mi >> 1) << 3) + rr, 2 * wm + (mi & 1)), a0, a1, a2, a3);
-      float gv[4];
+      {  // k~ = g phi(k) on the A fragment (rows past the chunk have g = 0)
+        float gv[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = j0 + 2 * t4 + (u & 1) + ((u >> 1) << 3);
-        const float x = gs[j];
-        gv[u] = (t * R::TT + j < n_in) ? (logits ? __expf(x - mch) : x) : 0.f;
+        for (int u = 0; u < 4; ++u) {
+          const int j = j0 + 2 * t4 + (u & 1) + ((u >> 1) << 3);
+          const float x = gs[j];
+          gv[u] = (t * R::TT + j < n_in) ? (logits ? __expf(x - mch) : x) : 0.f;
+        }
+        a0 = pack_bf16(phik<PRE>(bf_lo(a0)) * gv[0], phik<PRE>(bf_hi(a0)) * gv[1]);
+        a1 = pack_bf16(phik<PRE>(bf_lo(a1)) * gv[0], phik<PRE>(bf_hi(a1)) * gv[1]);
+        a2 = pack_bf16(phik<PRE>(bf_lo(a2)) * gv[2], phik<PRE>(bf_hi(a2)) * gv[3]);
+        a3 = pack_bf16(phik<PRE>(bf_lo(a3)) * gv[2], phik<PRE>(bf_hi(a3)) * gv[3]);
       }
-      a0 = pack_bf16(phi_f(bf_lo(a0)) * gv[0], phi_f(bf_hi(a0)) * gv[1]);
-      a1 = pack_bf16(phi_f(bf_lo(a1)) * gv[0], phi_f(bf_hi(a1)) * gv[1]);
-      a2 = pack_bf16(phi_f(bf_lo(a2)) * gv[2], phi_f(bf_hi(a2)) * gv[3]);
-      a3 = pack_bf16(phi_f(bf_lo(a3)) * gv[2], phi_f(bf_hi(a3)) * gv[3]);
 #pragma unroll
       for (int np = 0; np < DH / 16; ++np) {
         uint32_t b0, b1, b2, b3;
@@ -228,7 +236,7 @@ struct RdCfg {
   static constexpr int SMEM = DH * Cfg<DH>::SPAD * 2 + 2 * TILE * (NORM ? 2 : 1);
 };
 
-template <int DH, bool NORM>
+template <int DH, bool NORM, bool PRE>
 __global__ void __launch_bounds__(128) k_readout_bf16(const ReadoutArgs a) {
   using C = Cfg<DH>;
   using R = RdCfg<DH, NORM>;
@@ -293,8 +301,10 @@ __global__ void __launch_bounds__(128) k_readout_bf16(const ReadoutArgs a) {
     for (int ks = 0; ks < DH / 16; ++ks) {
       uint32_t af[4];
       a_rows<DH>(qb, r0w, ks, lane, af);
+      if (!PRE) {  // PRE: the tile already holds phi(q)
 #pragma unroll
-      for (int u = 0; u < 4; ++u) af[u] = phi2(af[u]);
+        for (int u = 0; u < 4; ++u) af[u] = phi2(af[u]);
+      }
       const uint32_t srow = sb + ((ks * 16 + ((mi & 1) << 3) + rr) * C::SPAD) * 2;
 #pragma unroll
       for (int np = 0; np < DH / 16; ++np) {
@@ -377,7 +387,7 @@ struct BqCfg {
   static constexpr int SMEM = DH * Cfg<DH>::SPAD * 2 + TT * Cfg<DH>::SPAD * 2 + STAGES * NIN * TILE;
 };
 
-template <int DH, bool NORM>
+template <int DH, bool NORM, bool PRE>
 __global__ void __launch_bounds__(BqCfg<DH, NORM>::NW * 32) k_bwd_q_bf16(const BwdQArgs a) {
   using C = Cfg<DH>;
   using R = BqCfg<DH, NORM>;
@@ -461,8 +471,10 @@ __global__ void __launch_bounds__(BqCfg<DH, NORM>::NW * 32) k_bwd_q_bf16(const B
     for (int ks = 0; ks < DH / 16; ++ks) {
       uint32_t af[4];
       a_rows<DH>(qb, r0w, ks, lane, af);
+      if (!PRE) {  // PRE: the tile already holds phi(q)
 #pragma unroll
-      for (int u = 0; u < 4; ++u) af[u] = phi2(af[u]);
+        for (int u = 0; u < 4; ++u) af[u] = phi2(af[u]);
+      }
       const uint32_t srow = sb + ((ks * 16 + ((mi & 1) << 3) + rr) * C::SPAD) * 2;
 #pragma unroll
       for (int np = 0; np < DH / 16; ++np) {
@@ -604,9 +616,9 @@ __global__ void __launch_bounds__(BqCfg<DH, NORM>::NW * 32) k_bwd_q_bf16(const B
       const uint32_t q0 = *reinterpret_cast<const uint32_t*>(qtb + o0);
       const uint32_t q1 = *reinterpret_cast<const uint32_t*>(qtb + o1);
       *reinterpret_cast<uint32_t*>(ytb + o0) =
-          pack_bf16(va ? accq[nt][0] * dphi_f(bf_lo(q0)) : 0.f, va ? accq[nt][1] * dphi_f(bf_hi(q0)) : 0.f);
+          pack_bf16(va ? accq[nt][0] * dphi_s<PRE>(bf_lo(q0)) : 0.f, va ? accq[nt][1] * dphi_s<PRE>(bf_hi(q0)) : 0.f);
       *reinterpret_cast<uint32_t*>(ytb + o1) =
-          pack_bf16(vb ? accq[nt][2] * dphi_f(bf_lo(q1)) : 0.f, vb ? accq[nt][3] * dphi_f(bf_hi(q1)) : 0.f);
+          pack_bf16(vb ? accq[nt][2] * dphi_s<PRE>(bf_lo(q1)) : 0.f, vb ? accq[nt][3] * dphi_s<PRE>(bf_hi(q1)) : 0.f);
     }
     __syncwarp();
     for (int i = lane; i < 16 * C::CPR; i += 32) {
@@ -627,7 +639,7 @@ __global__ void __launch_bounds__(BqCfg<DH, NORM>::NW * 32) k_bwd_q_bf16(const B
       const int j0 = kk * 16;
       uint32_t a0, a1, a2, a3;
       ldsm_x4_t(qb + swz<C::CPR>(j0 + ((mi >> 1) << 3) + rr, 2 * wm + (mi & 1)), a0, a1, a2, a3);
-      a0 = phi2(a0); a1 = phi2(a1); a2 = phi2(a2); a3 = phi2(a3);
+      if (!PRE) { a0 = phi2(a0); a1 = phi2(a1); a2 = phi2(a2); a3 = phi2(a3); }
       const uint32_t drow = dnb + ((j0 + ((mi & 1) << 3) + rr) * C::SPAD) * 2;
 #pragma unroll
       for (int np = 0; np < DH / 16; ++np) {
@@ -715,7 +727,7 @@ struct BkvCfg {
   static constexpr int SMEM = DH * Cfg<DH>::SPAD * 2 + 2 * (2 * TILE + TT * 4);
 };
 
-template <int DH>
+template <int DH, bool PRE>
 __global__ void __launch_bounds__(128) k_bwd_kv_bf16(const BwdKVArgs a) {
   using C = Cfg<DH>;
   using R = BkvCfg<DH>;
@@ -797,10 +809,10 @@ __global__ void __launch_bounds__(128) k_bwd_kv_bf16(const BwdKVArgs a) {
       uint32_t av[4], ak[4];
       a_rows<DH>(vb, r0w, ks, lane, av);
       a_rows<DH>(kb, r0w, ks, lane, ak);
-      ak[0] = pack_bf16(phi_f(bf_lo(ak[0])) * gr0, phi_f(bf_hi(ak[0])) * gr0);
-      ak[1] = pack_bf16(phi_f(bf_lo(ak[1])) * gr1, phi_f(bf_hi(ak[1])) * gr1);
-      ak[2] = pack_bf16(phi_f(bf_lo(ak[2])) * gr0, phi_f(bf_hi(ak[2])) * gr0);
-      ak[3] = pack_bf16(phi_f(bf_lo(ak[3])) * gr1, phi_f(bf_hi(ak[3])) * gr1);
+      ak[0] = pack_bf16(phik<PRE>(bf_lo(ak[0])) * gr0, phik<PRE>(bf_hi(ak[0])) * gr0);
+      ak[1] = pack_bf16(phik<PRE>(bf_lo(ak[1])) * gr1, phik<PRE>(bf_hi(ak[1])) * gr1);
+      ak[2] = pack_bf16(phik<PRE>(bf_lo(ak[2])) * gr0, phik<PRE>(bf_hi(ak[2])) * gr0);
+      ak[3] = pack_bf16(phik<PRE>(bf_lo(ak[3])) * gr1, phik<PRE>(bf_hi(ak[3])) * gr1);
 #pragma unroll
       for (int np = 0; np < DH / 16; ++np) {
         uint32_t b0, b1, b2, b3;
@@ -825,8 +837,8 @@ __global__ void __launch_bounds__(128) k_bwd_kv_bf16(const BwdKVArgs a) {
       const uint32_t k0 = *reinterpret_cast<const uint32_t*>(ktb + swz<C::CPR>(r0w + g, nt) + t4 * 4);
       const uint32_t k1 = *reinterpret_cast<const uint32_t*>(ktb + swz<C::CPR>(r0w + g + 8, nt) + t4 * 4);
       kv[nt][0] = bf_lo(k0); kv[nt][1] = bf_hi(k0); kv[nt][2] = bf_lo(k1); kv[nt][3] = bf_hi(k1);
-      dg0 += phi_f(kv[nt][0]) * acck[nt][0] + phi_f(kv[nt][1]) * acck[nt][1];
-      dg1 += phi_f(kv[nt][2]) * acck[nt][2] + phi_f(kv[nt][3]) * acck[nt][3];
+      dg0 += phik<PRE>(kv[nt][0]) * acck[nt][0] + phik<PRE>(kv[nt][1]) * acck[nt][1];
+      dg1 += phik<PRE>(kv[nt][2]) * acck[nt][2] + phik<PRE>(kv[nt][3]) * acck[nt][3];
     }
     dg0 += __shfl_xor_sync(FULL, dg0, 1); dg0 += __shfl_xor_sync(FULL, dg0, 2);
     dg1 += __shfl_xor_sync(FULL, dg1, 1); dg1 += __shfl_xor_sync(FULL, dg1, 2);
@@ -834,9 +846,9 @@ __global__ void __launch_bounds__(128) k_bwd_kv_bf16(const BwdKVArgs a) {
     for (int nt = 0; nt < DH / 8; ++nt) {
       const uint32_t o0 = swz<C::CPR>(r0w + g, nt) + t4 * 4, o1 = swz<C::CPR>(r0w + g + 8, nt) + t4 * 4;
       *reinterpret_cast<uint32_t*>(ktb + o0) =
-          pack_bf16(gr0 * acck[nt][0] * dphi_f(kv[nt][0]), gr0 * acck[nt][1] * dphi_f(kv[nt][1]));
+          pack_bf16(gr0 * acck[nt][0] * dphi_s<PRE>(kv[nt][0]), gr0 * acck[nt][1] * dphi_s<PRE>(kv[nt][1]));
       *reinterpret_cast<uint32_t*>(ktb + o1) =
-          pack_bf16(gr1 * acck[nt][2] * dphi_f(kv[nt][2]), gr1 * acck[nt][3] * dphi_f(kv[nt][3]));
+          pack_bf16(gr1 * acck[nt][2] * dphi_s<PRE>(kv[nt][2]), gr1 * acck[nt][3] * dphi_s<PRE>(kv[nt][3]));
       *reinterpret_cast<uint32_t*>(vtb + o0) = pack_bf16(accv[nt][0], accv[nt][1]);
       *reinterpret_cast<uint32_t*>(vtb + o1) = pack_bf16(accv[nt][2], accv[nt][3]);
     }
@@ -898,16 +910,18 @@ cudaError_t prep(K kernel, int smem) {
 
 }  // namespace
 
+// Dispatch on (d_h, norm, pre).  The feature-map-free ("pre") variants are
+// built for the layer's sigmoid-gate path.
 cudaError_t launch_reduce_bf16(const ReduceArgs& a, int grid_x, cudaStream_t st) {
   const dim3 grid(grid_x, a.H);
   cudaError_t e;
-  switch (a.dh) {
-#define GBLA_CASE(D)                                                              \
-  case D:                                                                         \
-    if ((e = prep(k_reduce_bf16<D>, RedCfg<D>::SMEM)) != cudaSuccess) return e;   \
-    k_reduce_bf16<D><<<grid, 256, RedCfg<D>::SMEM, st>>>(a);                      \
+  switch (a.dh * 2 + (a.pre ? 1 : 0)) {
+#define GBLA_CASE(D, P)                                                              \
+  case D * 2 + P:                                                                    \
+    if ((e = prep(k_reduce_bf16<D, P>, RedCfg<D>::SMEM)) != cudaSuccess) return e;   \
+    k_reduce_bf16<D, P><<<grid, 256, RedCfg<D>::SMEM, st>>>(a);                      \
     break;
-    GBLA_CASE(32) GBLA_CASE(64) GBLA_CASE(128)
+    GBLA_CASE(32, 0) GBLA_CASE(32, 1) GBLA_CASE(64, 0) GBLA_CASE(64, 1) GBLA_CASE(128, 0) GBLA_CASE(128, 1)
 #undef GBLA_CASE
     default: return cudaErrorInvalidValue;
   }
@@ -917,13 +931,14 @@ cudaError_t launch_reduce_bf16(const ReduceArgs& a, int grid_x, cudaStream_t st)
 cudaError_t launch_readout_bf16(const ReadoutArgs& a, bool norm, int grid_x, cudaStream_t st) {
   const dim3 grid(grid_x, a.H);
   cudaError_t e;
-  switch (a.dh * 2 + (norm ? 1 : 0)) {
-#define GBLA_CASE(D, N)                                                                      \
-  case D * 2 + N:                                                                            \
-    if ((e = prep(k_readout_bf16<D, N>, RdCfg<D, N>::SMEM)) != cudaSuccess) return e;        \
-    k_readout_bf16<D, N><<<grid, 128, RdCfg<D, N>::SMEM, st>>>(a);                           \
+  switch (a.dh * 4 + (norm ? 2 : 0) + (a.pre ? 1 : 0)) {
+#define GBLA_CASE(D, N, P)                                                                      \
+  case D * 4 + N * 2 + P:                                                                       \
+    if ((e = prep(k_readout_bf16<D, N, P>, RdCfg<D, N>::SMEM)) != cudaSuccess) return e;        \
+    k_readout_bf16<D, N, P><<<grid, 128, RdCfg<D, N>::SMEM, st>>>(a);                           \
     break;
-    GBLA_CASE(32, 0) GBLA_CASE(32, 1) GBLA_CASE(64, 0) GBLA_CASE(64, 1) GBLA_CASE(128, 0) GBLA_CASE(128, 1)
+    GBLA_CASE(32, 0, 0) GBLA_CASE(32, 1, 0) GBLA_CASE(64, 0, 0) GBLA_CASE(64, 1, 0) GBLA_CASE(128, 0, 0)
+    GBLA_CASE(128, 1, 0) GBLA_CASE(32, 1, 1) GBLA_CASE(64, 1, 1) GBLA_CASE(128, 1, 1)
 #undef GBLA_CASE
     default: return cudaErrorInvalidValue;
   }
@@ -933,13 +948,14 @@ cudaError_t launch_readout_bf16(const ReadoutArgs& a, bool norm, int grid_x, cud
 cudaError_t launch_bwd_q_bf16(const BwdQArgs& a, bool norm, int grid_x, cudaStream_t st) {
   const dim3 grid(grid_x, a.H);
   cudaError_t e;
-  switch (a.dh * 2 + (norm ? 1 : 0)) {
-#define GBLA_CASE(D, N)                                                                          \
-  case D * 2 + N:                                                                                \
-    if ((e = prep(k_bwd_q_bf16<D, N>, BqCfg<D, N>::SMEM)) != cudaSuccess) return e;              \
-    k_bwd_q_bf16<D, N><<<grid, BqCfg<D, N>::NW * 32, BqCfg<D, N>::SMEM, st>>>(a);                \
+  switch (a.dh * 4 + (norm ? 2 : 0) + (a.pre ? 1 : 0)) {
+#define GBLA_CASE(D, N, P)                                                                          \
+  case D * 4 + N * 2 + P:                                                                           \
+    if ((e = prep(k_bwd_q_bf16<D, N, P>, BqCfg<D, N>::SMEM)) != cudaSuccess) return e;              \
+    k_bwd_q_bf16<D, N, P><<<grid, BqCfg<D, N>::NW * 32, BqCfg<D, N>::SMEM, st>>>(a);                \
     break;
-    GBLA_CASE(32, 0) GBLA_CASE(32, 1) GBLA_CASE(64, 0) GBLA_CASE(64, 1) GBLA_CASE(128, 0) GBLA_CASE(128, 1)
+    GBLA_CASE(32, 0, 0) GBLA_CASE(32, 1, 0) GBLA_CASE(64, 0, 0) GBLA_CASE(64, 1, 0) GBLA_CASE(128, 0, 0)
+    GBLA_CASE(128, 1, 0) GBLA_CASE(32, 1, 1) GBLA_CASE(64, 1, 1) GBLA_CASE(128, 1, 1)
 #undef GBLA_CASE
     default: return cudaErrorInvalidValue;
   }
@@ -949,13 +965,13 @@ cudaError_t launch_bwd_q_bf16(const BwdQArgs& a, bool norm, int grid_x, cudaStre
 cudaError_t launch_bwd_kv_bf16(const BwdKVArgs& a, int grid_x, cudaStream_t st) {
   const dim3 grid(grid_x, a.H);
   cudaError_t e;
-  switch (a.dh) {
-#define GBLA_CASE(D)                                                            \
-  case D:                                                                       \
-    if ((e = prep(k_bwd_kv_bf16<D>, BkvCfg<D>::SMEM)) != cudaSuccess) return e; \
-    k_bwd_kv_bf16<D><<<grid, 128, BkvCfg<D>::SMEM, st>>>(a);                    \
+  switch (a.dh * 2 + (a.pre ? 1 : 0)) {
+#define GBLA_CASE(D, P)                                                            \
+  case D * 2 + P:                                                                  \
+    if ((e = prep(k_bwd_kv_bf16<D, P>, BkvCfg<D>::SMEM)) != cudaSuccess) return e; \
+    k_bwd_kv_bf16<D, P><<<grid, 128, BkvCfg<D>::SMEM, st>>>(a);                    \
     break;
-    GBLA_CASE(32) GBLA_CASE(64) GBLA_CASE(128)
+    GBLA_CASE(32, 0) GBLA_CASE(32, 1) GBLA_CASE(64, 0) GBLA_CASE(64, 1) GBLA_CASE(128, 0) GBLA_CASE(128, 1)
 #undef GBLA_CASE
     default: return cudaErrorInvalidValue;
   }

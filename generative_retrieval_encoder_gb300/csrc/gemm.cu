@@ -119,13 +119,19 @@ __global__ void __launch_bounds__(256) k_gemm_bf16(const GemmArgs a) {
       for (int nt = 0; nt < 4; ++nt) {
         const int n = n0 + wn * 32 + nt * 8 + 2 * t4;
         const float v0 = acc[mt][nt][2 * hr], v1 = acc[mt][nt][2 * hr + 1];
+        if (a.epi == EPI_PROJ_PRE && n < a.n_main) {  // [phi(q) | phi(k) | v | r]; a pair lies in one block
+          const bool ph = n < 2 * a.hd;
+          const float w0 = ph ? phi_f(v0) : v0, w1 = ph ? phi_f(v1) : v1;
+          *reinterpret_cast<uint32_t*>((bf16*)a.C + (size_t)m * a.ldc + n) = pack_bf16(w0, w1);
+          continue;
+        }
         // n is even and n_main a multiple of 8: a pair never straddles n_main
         if (a.epi == EPI_BF16 || (a.epi == EPI_PROJ && n < a.n_main)) {
           bf16* C = (bf16*)a.C + (size_t)m * a.ldc + n;
           const int nlim = a.epi == EPI_PROJ ? a.n_main : a.N;
           if (n + 1 < nlim) *reinterpret_cast<uint32_t*>(C) = pack_bf16(v0, v1);
           else if (n < nlim) C[0] = __float2bfloat16_rn(v0);
-        } else if (a.epi == EPI_PROJ) {
+        } else if (a.epi == EPI_PROJ || a.epi == EPI_PROJ_PRE) {
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             const int hh = n + q - a.n_main;

@@ -121,6 +121,38 @@ struct TileSched {
 // One 32-column chunk of a finished accumulator row to global memory.
 __device__ __forceinline__ void store_chunk(const GemmArgs& a, int m, int n, int z, const uint32_t (&r)[32]) {
   const int Hg = a.N - a.n_main;
+  if (a.epi == EPI_PROJ_PRE && n < a.n_main) {
+    // [q | k | v | r] column blocks of width H*dh, H*dh a multiple of 32: a
+    // 32-column chunk lies in one block.  q, k -> phi(.), v and r unchanged.
+    const int blk = n / a.hd;  // the same for every lane of the warp
+    bf16* C = (bf16*)a.C + (size_t)m * a.ldc + n;
+    if (blk < 2) {  // phi = elu + 1
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float f[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float x = __uint_as_float(r[8 * q + j]);
+          f[j] = fmaxf(x, 0.f) + __expf(fminf(x, 0.f));
+        }
+        uint4 u;
+        u.x = pack_bf16(f[0], f[1]); u.y = pack_bf16(f[2], f[3]);
+        u.z = pack_bf16(f[4], f[5]); u.w = pack_bf16(f[6], f[7]);
+        reinterpret_cast<uint4*>(C)[q] = u;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 u;
+        u.x = pack_bf16(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]));
+        u.y = pack_bf16(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]));
+        u.z = pack_bf16(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]));
+        u.w = pack_bf16(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]));
+        reinterpret_cast<uint4*>(C)[q] = u;
+      }
+    }
+    return;
+  }
   if (a.epi == EPI_BF16 || (a.epi == EPI_PROJ && n < a.n_main)) {
     bf16* C = (bf16*)a.C + (size_t)m * a.ldc + n;
     const int lim = a.epi == EPI_PROJ ? a.n_main : a.N;
@@ -139,7 +171,7 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& a, int m, int n, int
       for (int j = 0; j < 32; ++j)
         if (n + j < lim) C[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
     }
-  } else if (a.epi == EPI_PROJ) {
+  } else if (a.epi == EPI_PROJ || a.epi == EPI_PROJ_PRE) {  // the gate columns
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int hh = n + j - a.n_main;
@@ -380,6 +412,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B)) & 15) return cudaErrorNotSupported;
   if ((a.lda % 8) || (a.ldb % 8)) return cudaErrorNotSupported;
   if (a.epi == EPI_PROJ && a.n_main % 32) return cudaErrorNotSupported;
+  if (a.epi == EPI_PROJ_PRE && (a.n_main != 4 * a.hd || a.hd % 32)) return cudaErrorNotSupported;
   CUtensorMap ta, tb;
   const bool okA = amn ? make_map(&ta, a.A, (uint64_t)a.M, (uint64_t)a.K, (uint64_t)a.lda, 64, PBK)
                        : make_map(&ta, a.A, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.lda, PBK, PBM);

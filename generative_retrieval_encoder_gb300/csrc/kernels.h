@@ -26,7 +26,11 @@ enum GateGrad {
   GG_SOFTMAX = 2,    // dL/ds = g' dg with g' = exp(s - m), io dtype into dP
 };
 
+// "pre" (the bf16 layer): the projection epilogue has already stored phi(q)
+// and phi(k) in place of q and k, so the state kernels skip the feature map;
+// the backward uses phi'(x) = min(1, phi(x)) for phi = elu + 1.
 struct ReduceArgs {
+  int pre;            // k holds phi(k)
   const void* k; const void* v; int64_t ldk, ldv;  // [rows, ld], head h at column h*dh
   const float* g; int64_t ldg; int gate_kind;
   int H, dh;
@@ -43,6 +47,7 @@ struct ReduceArgs {
 };
 
 struct ReadoutArgs {
+  int pre;                          // q holds phi(q)
   const void* q; int64_t ldq;
   const void* r; int64_t ldr;       // norm only
   const void* rms_w; float eps;     // norm only; rms_w may be null
@@ -56,6 +61,7 @@ struct ReadoutArgs {
 };
 
 struct BwdQArgs {
+  int pre;                          // q holds phi(q)
   const void* q; int64_t ldq;
   const void* r; int64_t ldr;       // norm only
   const void* dy; int64_t lddy;     // norm: dy; core: d_o
@@ -73,6 +79,7 @@ struct BwdQArgs {
 };
 
 struct BwdKVArgs {
+  int pre;                          // k holds phi(k)
   const void* k; int64_t ldk;
   const void* v; int64_t ldv;
   const float* g; int64_t ldg; int gate_kind;  // GateKind
@@ -97,6 +104,7 @@ enum GemmEpi {
   EPI_F32 = 1,        // C fp32
   EPI_SPLITK = 2,     // fp32 partial C + z * M * ldc
   EPI_PROJ = 3,       // columns < n_main -> bf16 C; the next H columns -> gate (fp32)
+  EPI_PROJ_PRE = 4,   // as EPI_PROJ, with phi(q), phi(k) stored in place of q, k
 };
 struct GemmArgs {
   const void* A; int64_t lda; int a_kmajor;
@@ -108,6 +116,7 @@ struct GemmArgs {
   int n_main; const void* bias_g; int gate_mode; float* gate; int64_t ldgate;
   int io_f32;
   int* err;           // workspace error word (bounded device waits that give up set bit 2)
+  int hd, dh;         // EPI_PROJ_PRE: H*dh and dh (column -> head)
 };
 
 struct ConvArgs {
