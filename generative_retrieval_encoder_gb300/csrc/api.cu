@@ -88,7 +88,7 @@ gbla_status make_plan(const gbla_shape* s, Plan& p) {
   const int want_split = std::max(1, std::min(cdiv(2 * kSMs, tiles), cdiv(p.T, 1024)));
   p.wsplit = cdiv(cdiv(p.T, want_split), 64) * 64;
   p.n_wsplit = cdiv(p.T, p.wsplit);
-  p.conv_blocks = conv_bwd_blocks(p.T);
+  p.conv_blocks = conv_bwd_parts_max(p.T);
   return GBLA_OK;
 }
 
@@ -342,7 +342,7 @@ gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* con
   if (p.f32) center = nullptr;
   // Eq. 4: conv
   ConvArgs ca{};
-  ca.x = x; ca.w = conv_w; ca.b = conv_b; ca.xt = xt; ca.T = p.T; ca.d = p.d; ca.seq = c.seq; ca.err = c.kerr;
+  ca.x = x; ca.w = conv_w; ca.b = conv_b; ca.xt = xt; ca.T = p.T; ca.d = p.d; ca.seq = c.seq; ca.err = c.kerr; ca.err_out = c.err;
   GBLA_CHECK(launch_conv_fwd(ca, p.f32, c.st), "conv");
   c.pre = layer_pre(p, shape) ? 1 : 0;
   // Eq. 4, 5, 7: projections and gate
@@ -466,10 +466,11 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   // Eq. 4 conv backward
   ConvArgs ca{};
   ca.x = x; ca.w = conv_w; ca.dxt = at<char>(ws, l.dxt); ca.dx = dx; ca.part = at<float>(ws, l.conv_part);
-  ca.T = p.T; ca.d = p.d; ca.seq = c.seq; ca.err = c.kerr;
-  GBLA_CHECK(launch_conv_bwd(ca, p.f32, p.conv_blocks, c.st), "conv bwd");
+  ca.T = p.T; ca.d = p.d; ca.seq = c.seq; ca.err = c.kerr; ca.err_out = c.err;
+  int nparts = 0;
+  GBLA_CHECK(launch_conv_bwd(ca, p.f32, &nparts, c.st), "conv bwd");
   if (dconv_w || dconv_b)
-    GBLA_CHECK(launch_conv_param_grads(ca.part, p.conv_blocks, p.d, dconv_w, dconv_b, c.st), "conv grads");
+    GBLA_CHECK(launch_conv_param_grads(ca.part, nparts, p.d, dconv_w, dconv_b, c.st), "conv grads");
   if (drms_w)
     GBLA_CHECK(launch_sum_parts(q.gamma_part, p.n_chunks * p.H, p.dh, p.dh, drms_w, c.st), "dgamma");
   if (db_g)

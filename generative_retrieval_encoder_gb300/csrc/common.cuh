@@ -32,6 +32,32 @@ struct SeqDesc {
   const int32_t* cu;
 };
 
+// Walks the rows of the sequences: for row l gives the first row s0 of its
+// sequence, the end of its valid rows vend and the end of its slot send.
+struct SeqCursor {
+  const SeqDesc& s;
+  int b, s0, vend, send;
+  __device__ explicit SeqCursor(const SeqDesc& sd) : s(sd), b(0), s0(0), vend(0), send(0) {}
+  __device__ void seek(int l) {
+    if (s.mode != SEQ_VARLEN) {
+      b = l / s.L;
+      s0 = b * s.L;
+      send = s0 + s.L;
+      vend = s0 + (s.mode == SEQ_PADDED ? s.lens[b] : s.L);
+    } else {
+      int lo = 0, hi = s.n_seq - 1;  // last b with cu[b] <= l
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s.cu[mid] <= l) lo = mid; else hi = mid - 1;
+      }
+      b = lo;
+      while (b + 1 < s.n_seq && s.cu[b + 1] <= l) ++b;  // skip empty sequences
+      s0 = s.cu[b];
+      vend = send = s.cu[b + 1];
+    }
+  }
+};
+
 struct Tiling {
   int tile;               // rows per tile
   int per_seq;            // dense/padded: tiles per sequence

@@ -24,6 +24,7 @@
 #include <cudaTypedefs.h>
 
 #include "kernels.h"
+#include "mbarrier.cuh"
 
 namespace gbla {
 namespace {
@@ -33,27 +34,6 @@ constexpr int A_TILE = PBM * PBK * 2;  // 16 KB
 constexpr int B_TILE = PBN * PBK * 2;  // 32 KB
 constexpr int SMEM_P = PST * (A_TILE + B_TILE) + 1024 + 256;
 constexpr int NTHREADS = 192;
-constexpr uint32_t kPollLimit = 1u << 24;
-constexpr int kErrTimeout = 2;
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 // Bounded wait: false if the phase did not complete within kPollLimit polls
 // or another role of the CTA has already given up.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* fail) {
@@ -391,6 +371,8 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+}  // namespace
+
 int sm_count() {
   static int n = 0;
   if (n == 0) {
@@ -400,8 +382,6 @@ int sm_count() {
   }
   return n;
 }
-
-}  // namespace
 
 // cudaErrorNotSupported when the shape is outside what this kernel handles
 // (the caller then uses the mma.sync GEMM).

@@ -127,7 +127,8 @@ struct ConvArgs {
   float* part;                                  // backward: [gridDim.x][d][5] (dw 0..3, db)
   int T, d;
   SeqDesc seq;
-  const int* err;
+  const int* err;       // checked on entry (may be null)
+  int* err_out;         // workspace error word: a bounded wait that gave up sets kErrTimeout
 };
 
 // ---------------------------------------------------------------- launchers
@@ -157,8 +158,18 @@ inline cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_conv_fwd(const ConvArgs& a, bool f32, cudaStream_t st);
-cudaError_t launch_conv_bwd(const ConvArgs& a, bool f32, int nblk, cudaStream_t st);
-int conv_bwd_blocks(int T);
+// Writes the parameter-gradient partials to part[0 .. *nparts)[d][5].
+cudaError_t launch_conv_bwd(const ConvArgs& a, bool f32, int* nparts, cudaStream_t st);
+// Rows of the part buffer the backward may use, at most.
+int conv_bwd_parts_max(int T);
+// bf16 kernels staged through shared memory by bulk copies (conv.cu); usable
+// when conv_tile_ok (16-byte aligned rows).
+bool conv_tile_ok(const ConvArgs& a, bool bwd);
+int conv_tile_parts(int T, int d);
+int conv_tile_parts_max(int T);
+cudaError_t launch_conv_fwd_tile(const ConvArgs& a, cudaStream_t st);
+cudaError_t launch_conv_bwd_tile(const ConvArgs& a, int nparts, cudaStream_t st);
+int sm_count();  // of the current device, cached
 
 // Packs W_q | W_k | W_v | W_r | w_g into Wp [d][np] (row-major, zero-padded
 // past 4*H*dh + H columns).

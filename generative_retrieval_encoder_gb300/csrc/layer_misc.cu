@@ -66,32 +66,6 @@ __global__ void __launch_bounds__(1024) k_plan(SeqDesc s, int ntile, int t0, int
   }
 }
 
-// Walks the rows of the sequences: for row l gives the first row s0 of its
-// sequence, the end of its valid rows vend and the end of its slot send.
-struct SeqCursor {
-  const SeqDesc& s;
-  int b, s0, vend, send;
-  __device__ explicit SeqCursor(const SeqDesc& sd) : s(sd), b(0), s0(0), vend(0), send(0) {}
-  __device__ void seek(int l) {
-    if (s.mode != SEQ_VARLEN) {
-      b = l / s.L;
-      s0 = b * s.L;
-      send = s0 + s.L;
-      vend = s0 + (s.mode == SEQ_PADDED ? s.lens[b] : s.L);
-    } else {
-      int lo = 0, hi = s.n_seq - 1;  // last b with cu[b] <= l
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s.cu[mid] <= l) lo = mid; else hi = mid - 1;
-      }
-      b = lo;
-      while (b + 1 < s.n_seq && s.cu[b + 1] <= l) ++b;  // skip empty sequences
-      s0 = s.cu[b];
-      vend = send = s.cu[b + 1];
-    }
-  }
-};
-
 template <typename T> struct Vec;
 template <> struct Vec<bf16> { static constexpr int N = 8; typedef uint4 U; };
 template <> struct Vec<float> { static constexpr int N = 4; typedef float4 U; };
@@ -382,6 +356,7 @@ cudaError_t launch_plan(const SeqDesc& s, int ntile, const int* tile_sizes, int3
 }
 
 cudaError_t launch_conv_fwd(const ConvArgs& a, bool f32, cudaStream_t st) {
+  if (!f32 && conv_tile_ok(a, false)) return launch_conv_fwd_tile(a, st);
   const int V = f32 ? 4 : 8;
   const long long items = (long long)((a.T + RUN - 1) / RUN) * (a.d / V);
   const unsigned grid = (unsigned)((items + 255) / 256);
@@ -391,8 +366,14 @@ cudaError_t launch_conv_fwd(const ConvArgs& a, bool f32, cudaStream_t st) {
 }
 
 int conv_bwd_blocks(int T) { return std::max(1, std::min(1024, (T + 127) / 128)); }
+int conv_bwd_parts_max(int T) { return std::max(conv_bwd_blocks(T), conv_tile_parts_max(T)); }
 
-cudaError_t launch_conv_bwd(const ConvArgs& a, bool f32, int nblk, cudaStream_t st) {
+cudaError_t launch_conv_bwd(const ConvArgs& a, bool f32, int* nparts, cudaStream_t st) {
+  if (!f32 && conv_tile_ok(a, true)) {
+    *nparts = conv_tile_parts(a.T, a.d);
+    return launch_conv_bwd_tile(a, *nparts, st);
+  }
+  const int nblk = *nparts = conv_bwd_blocks(a.T);
   const int V = f32 ? 4 : 8;
   const int unit = RUNB * BW_ROWGROUPS;
   const int rows = ((a.T + nblk - 1) / nblk + unit - 1) / unit * unit;
