@@ -406,8 +406,7 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   char* dP = at<char>(ws, l.dP);
   const bool sig = shape->gate == GBLA_GATE_SIGMOID;
   const int pre = layer_pre(p, shape) ? 1 : 0;
-  GBLA_CHECK(cudaMemsetAsync(at<char>(ws, l.gamma_part), 0, (size_t)p.n_chunks * p.H * p.dh * 4, c.st), "memset");
-  GBLA_CHECK(cudaMemsetAsync(at<char>(ws, l.bg_part), 0, (size_t)p.n_tiles * p.H * 4, c.st), "memset");
+  // gamma_part and bg_part: every CTA of bwd_q / bwd_kv writes its row (zeros when it has no rows)
   const void* W[4] = {W_q, W_k, W_v, W_r};
   GBLA_CHECK(launch_pack_weights(W, w_g, p.d, p.H, p.dh, p.f32, at<char>(ws, l.Wp), p.NP, c.st), "pack");
   // Eq. 7 + Eq. 5/6 query side: dr, dq, [dS | dz]

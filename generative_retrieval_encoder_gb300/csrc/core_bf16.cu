@@ -401,7 +401,11 @@ __global__ void __launch_bounds__(BqCfg<DH, NORM>::NW * 32) k_bwd_q_bf16(const B
   const int wm = warp % R::WM, kg = warp / R::WM;
   if (a.err && *a.err) return;
   int b, row0, nvalid, cin;
-  if (!map_tile(a.seq, a.chunks, blockIdx.x, b, row0, nvalid, cin)) return;
+  if (!map_tile(a.seq, a.chunks, blockIdx.x, b, row0, nvalid, cin)) {  // no chunk: a zero dgamma partial
+    if (NORM)
+      for (int f = tid; f < DH; f += NTHR) a.gamma_part[((size_t)blockIdx.x * a.H + blockIdx.y) * DH + f] = 0.f;
+    return;
+  }
   const int h = blockIdx.y, H = a.H;
   const int CH = a.chunks.tile;
   const int c0 = cin * CH;
@@ -738,11 +742,17 @@ __global__ void __launch_bounds__(128) k_bwd_kv_bf16(const BwdKVArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (a.err && *a.err) return;
   int b, row0, nvalid, tin;
-  if (!map_tile(a.seq, a.tiles, blockIdx.x, b, row0, nvalid, tin)) return;
+  if (!map_tile(a.seq, a.tiles, blockIdx.x, b, row0, nvalid, tin)) {  // no tile: a zero db_g partial
+    if (a.bg_part && tid == 0) a.bg_part[(size_t)blockIdx.x * a.H + blockIdx.y] = 0.f;
+    return;
+  }
   const int h = blockIdx.y, H = a.H;
   const int R0 = tin * a.tiles.tile;
   const int nrows = min(a.tiles.tile, slot_rows(a.seq, nvalid) - R0);
-  if (nrows <= 0) return;
+  if (nrows <= 0) {
+    if (a.bg_part && tid == 0) a.bg_part[(size_t)blockIdx.x * H + h] = 0.f;
+    return;
+  }
   const int nval = max(0, min(nrows, nvalid - R0));
   const int nsub = (nrows + R::TT - 1) / R::TT;
   const size_t rb = (size_t)row0 + R0;

@@ -192,7 +192,11 @@ __global__ void __launch_bounds__(256) k_bwd_q_f32(const BwdQArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (a.err && *a.err) return;
   int b, row0, nvalid, cin;
-  if (!map_tile(a.seq, a.chunks, blockIdx.x, b, row0, nvalid, cin)) return;
+  if (!map_tile(a.seq, a.chunks, blockIdx.x, b, row0, nvalid, cin)) {  // no chunk: a zero dgamma partial
+    if (a.gamma_part)
+      for (int f = tid; f < dh; f += blockDim.x) a.gamma_part[((size_t)blockIdx.x * a.H + blockIdx.y) * dh + f] = 0.f;
+    return;
+  }
   const int h = blockIdx.y, H = a.H;
   const int c0 = cin * a.chunks.tile;
   const int nrows = max(0, min(a.chunks.tile, slot_rows(a.seq, nvalid) - c0));
@@ -317,11 +321,17 @@ __global__ void __launch_bounds__(256) k_bwd_kv_f32(const BwdKVArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (a.err && *a.err) return;
   int b, row0, nvalid, tin;
-  if (!map_tile(a.seq, a.tiles, blockIdx.x, b, row0, nvalid, tin)) return;
+  if (!map_tile(a.seq, a.tiles, blockIdx.x, b, row0, nvalid, tin)) {  // no tile: a zero db_g partial
+    if (a.bg_part && tid == 0) a.bg_part[(size_t)blockIdx.x * a.H + blockIdx.y] = 0.f;
+    return;
+  }
   const int h = blockIdx.y, H = a.H;
   const int R0 = tin * a.tiles.tile;
   const int nrows = min(a.tiles.tile, slot_rows(a.seq, nvalid) - R0);
-  if (nrows <= 0) return;
+  if (nrows <= 0) {
+    if (a.bg_part && tid == 0) a.bg_part[(size_t)blockIdx.x * H + h] = 0.f;
+    return;
+  }
   const int nval = max(0, min(nrows, nvalid - R0));
   const bool logits = a.gate_kind == GATE_LOGITS;
   const float mseq = logits ? a.state_m[b * H + h] : 0.f;

@@ -281,21 +281,37 @@ __global__ void __launch_bounds__(256) k_conv_bwd(const ConvArgs a, int rows_per
   }
 }
 
-// Wp[c][n] = [W_q | W_k | W_v | W_r | w_g | 0][c][n] for n < np: one block
-// row per c (blockIdx.y), consecutive threads take consecutive n.
+// Wp[c][n] = [W_q | W_k | W_v | W_r | w_g | 0][c][n] for n < np, 16 bytes
+// per thread (grid-stride).  np and H*dh are multiples of the vector width, so
+// a vector lies in one block; `vec`: the W_* rows are 16-byte aligned.
 template <typename T>
-__global__ void k_pack(const T* Wq, const T* Wk, const T* Wv, const T* Wr, const T* wg, int H, int dh,
-                       T* Wp, int np) {
-  const int HD = H * dh;
-  const int c = blockIdx.y;
-  const int n = blockIdx.x * blockDim.x + threadIdx.x;
-  if (n >= np) return;
-  const int m = n / HD, j = n - m * HD;
+__global__ void __launch_bounds__(256) k_pack(const T* Wq, const T* Wk, const T* Wv, const T* Wr, const T* wg,
+                                              int d, int H, int dh, T* Wp, int np, int vec) {
+  constexpr int V = 16 / sizeof(T);
+  typedef uint4 U;
+  const int HD = H * dh, npv = np / V;
   const T* Ws[4] = {Wq, Wk, Wv, Wr};
-  T v = from_f<T>(0.f);
-  if (m < 4) v = Ws[m][(size_t)c * HD + j];
-  else if (n - 4 * HD < H) v = wg[(size_t)c * H + n - 4 * HD];
-  Wp[(size_t)c * np + n] = v;
+  const long long total = (long long)d * npv;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(i / npv), n = (int)(i % npv) * V;
+    const int m = n / HD, j = n - m * HD;
+    U u;
+    if (m < 4 && vec) {
+      u = *reinterpret_cast<const U*>(Ws[m] + (size_t)c * HD + j);
+    } else {
+      T* e = reinterpret_cast<T*>(&u);
+#pragma unroll
+      for (int q = 0; q < V; ++q) {
+        const int nq = n + q, mq = nq / HD;
+        T v = from_f<T>(0.f);
+        if (mq < 4) v = Ws[mq][(size_t)c * HD + nq - mq * HD];
+        else if (nq - 4 * HD < H) v = wg[(size_t)c * H + nq - 4 * HD];
+        e[q] = v;
+      }
+    }
+    *reinterpret_cast<U*>(Wp + (size_t)c * np + n) = u;
+  }
 }
 
 // Column sums of a [S][stride] partial array in a fixed order: block b owns
@@ -385,13 +401,16 @@ cudaError_t launch_conv_bwd(const ConvArgs& a, bool f32, int* nparts, cudaStream
 
 cudaError_t launch_pack_weights(const void* const* W, const void* w_g, int d, int H, int dh, bool f32,
                                 void* Wp, int np, cudaStream_t st) {
-  const dim3 grid((np + 255) / 256, d);
+  int vec = 1;
+  for (int m = 0; m < 4; ++m) vec &= ((uintptr_t)W[m] & 15) == 0;
+  const long long vecs = (long long)d * np / (f32 ? 4 : 8);
+  const unsigned grid = (unsigned)std::max(1LL, std::min((vecs + 255) / 256, (long long)sm_count() * 8));
   if (f32)
     k_pack<float><<<grid, 256, 0, st>>>((const float*)W[0], (const float*)W[1], (const float*)W[2],
-                                        (const float*)W[3], (const float*)w_g, H, dh, (float*)Wp, np);
+                                        (const float*)W[3], (const float*)w_g, d, H, dh, (float*)Wp, np, vec);
   else
     k_pack<bf16><<<grid, 256, 0, st>>>((const bf16*)W[0], (const bf16*)W[1], (const bf16*)W[2],
-                                       (const bf16*)W[3], (const bf16*)w_g, H, dh, (bf16*)Wp, np);
+                                       (const bf16*)W[3], (const bf16*)w_g, d, H, dh, (bf16*)Wp, np, vec);
   return cudaGetLastError();
 }
 
