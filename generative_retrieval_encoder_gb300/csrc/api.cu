@@ -64,14 +64,15 @@ gbla_status make_plan(const gbla_shape* s, Plan& p) {
   p.NP = (p.N1 + 63) / 64 * 64;
   const int pairs = p.n_seq * p.H;
   const int target = kSMs * 8;
+  const int cg = p.f32 ? 64 : 128;  // chunk granule: the row tile of the query-side backward
   if (p.mode == SEQ_VARLEN) {
     const long long want = ((long long)p.T * p.H + target - 1) / target;
-    p.chunk = (int)std::min<long long>(2048, std::max<long long>(256, (want + 63) / 64 * 64));
+    p.chunk = (int)std::min<long long>(2048, std::max<long long>(256, (want + cg - 1) / cg * cg));
     p.chunk_per_seq = 0;
     p.n_chunks = cdiv(p.T, p.chunk) + p.n_seq;
   } else {
-    int per = std::max(1, std::min(cdiv(target, pairs), cdiv(p.L, 64)));
-    p.chunk = cdiv(cdiv(p.L, per), 64) * 64;
+    int per = std::max(1, std::min(cdiv(target, pairs), cdiv(p.L, cg)));
+    p.chunk = cdiv(cdiv(p.L, per), cg) * cg;
     p.chunk_per_seq = cdiv(p.L, p.chunk);
     p.n_chunks = p.chunk_per_seq * p.n_seq;
   }
@@ -116,7 +117,7 @@ size_t state_bytes(const Plan& p) { return (size_t)p.n_seq * p.H * p.dh * state_
 size_t state_bf_bytes(const Plan& p) { return (size_t)p.n_seq * p.H * p.dh * state_bf_ld(p.dh) * 2; }
 
 // Saved activations of a training forward: x~, P = [q|k|v|r], gate, state.
-struct SavedLayout { size_t xt, P, gate, state, state_bf, state_m, center, total; };
+struct SavedLayout { size_t xt, P, gate, state, state_bf, state_m, center, rsinv, total; };
 size_t center_bytes(const Plan& p) { return (size_t)p.n_seq * p.H * p.dh * 4; }
 SavedLayout saved_layout(const Plan& p) {
   Cursor c;
@@ -128,6 +129,7 @@ SavedLayout saved_layout(const Plan& p) {
   s.state_bf = c.take(state_bf_bytes(p));
   s.state_m = c.take((size_t)p.n_seq * p.H * 4);
   s.center = c.take(center_bytes(p));
+  s.rsinv = c.take((size_t)p.T * p.H * 8);  // per row and head: RMSNorm rs and 1/den of the readout
   s.total = c.off;
   return s;
 }
@@ -267,6 +269,14 @@ gbla_status begin(const gbla_shape* s, int op, void* ws, size_t ws_bytes, void* 
 
 // State reduction + combine.  The bf16 path centres the state on the
 // k~-weighted mean of v (center); the fp32 path keeps it uncentred.
+// The layer's bf16 query-side backward: the tcgen05 kernel where it applies.
+cudaError_t launch_bwd_q_layer_bf16(const BwdQArgs& q, int hd, int grid_x, cudaStream_t st) {
+  const cudaError_t e = launch_bwd_q_tc(q, hd, grid_x, st);
+  if (e != cudaErrorNotSupported) return e;
+  (void)cudaGetLastError();
+  return launch_bwd_q_bf16(q, true, grid_x, st);
+}
+
 gbla_status run_reduce(Ctx& c, const void* k, const void* v, int64_t ld, const float* g, int gate_kind, float* state,
                        bf16* state_bf, float* state_m, float* pub_state, float* center, void* ws) {
   const Plan& p = c.p;
@@ -373,6 +383,7 @@ gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* con
   ra.rms_w = rms_w; ra.eps = shape->rms_eps;
   ra.state = state; ra.state_bf = state_bf; ra.center = center; ra.pre = c.pre;
   ra.out = y; ra.ldo = p.HD; ra.den = nullptr;
+  ra.rsinv = (saved && !p.f32) ? at<float>(saved, saved_layout(p).rsinv) : nullptr;
   ra.H = p.H; ra.dh = p.dh; ra.seq = c.seq; ra.tiles = c.tiles; ra.err = c.kerr;
   GBLA_CHECK(p.f32 ? launch_readout_f32(ra, true, p.n_tiles, c.st) : launch_readout_bf16(ra, true, p.n_tiles, c.st),
              "readout");
@@ -425,8 +436,9 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   q.gamma_part = at<float>(ws, l.gamma_part);
   q.partial = at<float>(ws, l.partial); q.counters = at<int>(ws, l.cnt_b);
   q.dstate = at<float>(ws, l.dstate); q.dstate_bf = at<bf16>(ws, l.dstate_bf);
-  q.H = p.H; q.dh = p.dh; q.seq = c.seq; q.chunks = c.chunks; q.err = c.kerr;
-  GBLA_CHECK(p.f32 ? launch_bwd_q_f32(q, true, p.n_chunks, c.st) : launch_bwd_q_bf16(q, true, p.n_chunks, c.st),
+  q.rsinv = at<const float>(const_cast<void*>(saved), s.rsinv);
+  q.H = p.H; q.dh = p.dh; q.seq = c.seq; q.chunks = c.chunks; q.err = c.kerr; q.err_out = c.err;
+  GBLA_CHECK(p.f32 ? launch_bwd_q_f32(q, true, p.n_chunks, c.st) : launch_bwd_q_layer_bf16(q, p.HD, p.n_chunks, c.st),
              "bwd_q");
   // key side: dk, dv, ds
   BwdKVArgs kv{};

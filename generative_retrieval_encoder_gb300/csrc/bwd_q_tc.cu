@@ -1,0 +1,469 @@
+// Query-side backward of the bf16 layer (Eq. 5-7) on the 5th-generation
+// tensor cores, for d_h = 64 with phi(q) stored by the projection epilogue.
+//
+// Per (chunk, head) CTA, over 128-row tiles of the chunk:
+//   (a)  O' = phi(Q) S'                          tcgen05 -> TMEM cols 0..63
+//   epilogue 1 (one thread per row and column range; rs and 1/den of each
+//   row come from the training forward's readout):
+//        o = O'/den + c,  u = o rs,  y = u gamma SiLU(r)   (RMSNorm gate, Eq. 7)
+//        dr, dgamma (accumulated in TMEM cols 192..255), du = dy gamma SiLU(r),
+//        m = mean(du u), do = rs (du - u m), dn = do / den,
+//        dden = -(do . O'/den) / den = -rs (du . o' - m u . o') / den
+//   (d)  dq~ = dn S'^T                           tcgen05 -> TMEM cols 64..127
+//   (e)  [dS' | dz'] += [dn | dden]^T phi(Q)     tcgen05 -> TMEM cols 128..191,
+//                                                accumulated over the chunk
+//   epilogue 2: dq = (dq~ + dden z) min(1, phi(q))   (phi' of elu + 1)
+// then the chunk's [dS' | dz'] and dgamma partials and the deterministic
+// split-L combine, as the mma.sync kernel of the same operation.
+//
+// Warp roles: EW epilogue warps (warp w reads TMEM lanes 32 (w % 4) .. + 31,
+// i.e. tile rows, and the columns of its range w / 4) and one control warp
+// whose lane 0 issues the TMA loads and the MMAs.  (a) of tile t + 1 is issued
+// as soon as epilogue 1 of tile t has read O', so it runs under epilogue 2.
+// Operand tiles are [128 rows][64 bf16] in the 128-byte swizzle shared by
+// TMA and the MMA descriptors; the epilogue writes dn and dden into the dy and
+// r tiles of the same stage (each thread owns its row's columns), which then
+// serve as the A operand of (d) and (e).
+//
+// Every mbarrier wait is bounded; after one gives up, the kernel finishes its
+// loops without waiting (uniform control flow, so no named barrier is left
+// waiting), sets the timeout bit of the error word, waits (bounded) for its
+// copies and MMAs, frees its TMEM and returns.
+#include "core_common.cuh"
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace gbla {
+namespace {
+
+constexpr int QD = 64;               // d_h
+constexpr int QT = 128;              // rows per tile (MMA M)
+constexpr int TILE = QT * 128;       // [128 rows][64 bf16], 16 KB
+constexpr int QST = 2;               // stages
+constexpr int STAGE = 3 * TILE;      // phi(Q) | dy -> dn | r -> du, dden
+
+constexpr int O_S = 0;                       // S' [e][f] (8 KB)
+constexpr int O_ST = O_S + 8192;             // stages (1024-aligned)
+constexpr int O_BAR = O_ST + QST * STAGE;
+constexpr int NBAR = 2 * QST + 4;            // full, empty, a_done, dn_ready, d_done, fin
+constexpr int O_F = O_BAR + 8 * NBAR;        // gamma, centre, z (fp32), row exchange [3][2][128]
+constexpr int O_SLOT = O_F + 4 * (3 * QD + 3 * 2 * QT);
+constexpr int O_FAIL = O_SLOT + 4;
+constexpr int SMEM = O_FAIL + 4 + 1024;      // + alignment slack
+constexpr int TMEM_COLS = 256;               // O' | dq~ | dS' | dgamma
+static_assert(2 * (SMEM + 1024) <= 233472, "two CTAs per SM");
+static_assert(QST == 2, "the control thread tracks two stages");
+
+template <int EW> struct QCfg {
+  static constexpr int NTH = (EW + 1) * 32;  // + the control warp
+  static constexpr int CPT = QD / (EW / 4);  // columns per epilogue thread
+  static constexpr int NC = CPT / 8;         // 8-column chunks per thread
+  // Two CTAs per SM: 2 (EW + 1) warps over 4 sub-partitions of 16K registers.
+  static constexpr int MAXREG = EW == 8 ? 96 : 168;
+};
+
+__device__ __forceinline__ uint32_t swz_off(int row, int chunk) {
+  return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
+  f[0] = bf_lo(u.x); f[1] = bf_hi(u.x); f[2] = bf_lo(u.y); f[3] = bf_hi(u.y);
+  f[4] = bf_lo(u.z); f[5] = bf_hi(u.z); f[6] = bf_lo(u.w); f[7] = bf_hi(u.w);
+}
+// Asynchronous 8-column TMEM load; its registers are valid after tmem_wait().
+__device__ __forceinline__ void tmem_ld8_async(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+// Waits for the thread's TMEM loads; the registers of `r` are tied to the wait
+// so that no use of them moves above it.
+__device__ __forceinline__ void tmem_wait(uint32_t (&r)[8]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
+               :
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait(uint32_t (&r)[8], uint32_t (&s)[8]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(s[0]), "+r"(s[1]), "+r"(s[2]), "+r"(s[3]), "+r"(s[4]), "+r"(s[5]), "+r"(s[6]), "+r"(s[7])
+               :
+               : "memory");
+}
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
+
+template <int EW>
+__global__ void __maxnreg__(QCfg<EW>::MAXREG)
+    k_bwd_q_tc(const BwdQArgs a, const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmY,
+               int roff) {
+  using Q = QCfg<EW>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (a.err && *a.err) return;
+  int b, row0, nvalid, cin;
+  if (!map_tile(a.seq, a.chunks, blockIdx.x, b, row0, nvalid, cin)) {  // no chunk: a zero dgamma partial
+    for (int f = tid; f < QD; f += Q::NTH) a.gamma_part[((size_t)blockIdx.x * a.H + blockIdx.y) * QD + f] = 0.f;
+    return;
+  }
+  const int h = blockIdx.y, H = a.H;
+  const int CH = a.chunks.tile, c0 = cin * CH;
+  const int nrows = max(0, min(CH, slot_rows(a.seq, nvalid) - c0));
+  const int nval = max(0, min(nrows, nvalid - c0));
+  const int ntiles = (nrows + QT - 1) / QT;
+  const size_t rb = (size_t)row0 + c0;
+
+  float* gam = reinterpret_cast<float*>(smem + O_F);
+  float* cen = gam + QD;
+  float* zf = cen + QD;
+  float* xch = zf + QD;
+  uint32_t* slot = reinterpret_cast<uint32_t*>(smem + O_SLOT);
+  volatile int* fail = reinterpret_cast<volatile int*>(smem + O_FAIL);
+  const uint32_t bar0 = sbase + O_BAR;
+  const uint32_t A_DONE = bar0 + 8 * (2 * QST), DN_READY = A_DONE + 8, D_DONE = A_DONE + 16, FIN = A_DONE + 24;
+  auto FULL = [&](int s) { return bar0 + 8 * s; };
+  auto EMPTY = [&](int s) { return bar0 + 8 * (QST + s); };
+
+  // S' into its swizzled rows e; fp32 gamma, centre and z.
+  constexpr int BLD = state_bf_ld(QD);
+  const bf16* sbf = a.state_bf + (size_t)(b * H + h) * QD * BLD;
+  for (int i = tid; i < QD * 8; i += Q::NTH) {
+    const int e = i >> 3, c = i & 7;
+    *reinterpret_cast<uint4*>(smem + O_S + swz_off(e, c)) = *reinterpret_cast<const uint4*>(sbf + e * BLD + c * 8);
+  }
+  for (int f = tid; f < QD; f += Q::NTH) {
+    gam[f] = a.rms_w ? __bfloat162float(((const bf16*)a.rms_w)[f]) : 1.f;
+    cen[f] = a.center ? a.center[(size_t)(b * H + h) * QD + f] : 0.f;
+    zf[f] = __bfloat162float(sbf[f * BLD + QD]);
+  }
+  fence_async_smem();
+  if (tid == 0) {
+    for (int s = 0; s < QST; ++s) {
+      mbar_init(FULL(s), 1);
+      mbar_init(EMPTY(s), EW + 1);  // (e) commit + one arrival per epilogue warp
+    }
+    mbar_init(A_DONE, 1);
+    mbar_init(DN_READY, EW);
+    mbar_init(D_DONE, 1);
+    mbar_init(FIN, 1);
+    mbar_init_fence();
+    *fail = 0;
+  }
+  if (warp == EW) tmem_alloc(smem_u32(slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+
+  if (warp == EW) {
+    // ------------------------------------------------------------ control
+    if (lane == 0 && ntiles > 0) {
+      int issued0 = 0, issued1 = 0;  // 1 + index of the last tile loaded into stage 0 / 1
+      auto load = [&](int t) {
+        const int s = t % QST;
+        const uint32_t st = sbase + O_ST + s * STAGE;
+        const int y = (int)rb + t * QT;
+        mbar_expect_tx(FULL(s), 3 * TILE);
+        tma_load_2d(st, &tmP, FULL(s), h * QD, y);
+        tma_load_2d(st + TILE, &tmY, FULL(s), h * QD, y);
+        tma_load_2d(st + 2 * TILE, &tmP, FULL(s), roff + h * QD, y);
+        if (s == 0) issued0 = t + 1; else issued1 = t + 1;
+      };
+      const uint32_t id_a = idesc_bf16(QT, QD, false, true);
+      const uint32_t id_d = idesc_bf16(QT, QD, false, false), id_e = idesc_bf16(QT, QD, true, true);
+      const uint32_t sS = sbase + O_S;
+      // (a): K = e.  A = phi(Q) K-major (+32 B per 16 e); B = S' N-major (16 e-rows = 2048 B).
+      auto issue_a = [&](int t) {
+        const uint32_t sq = sbase + O_ST + (t % QST) * STAGE;
+#pragma unroll
+        for (int kk = 0; kk < QD / 16; ++kk)
+          tc_mma(tmem, sdesc(sq + 32 * kk, 16, 1024), sdesc(sS + 2048 * kk, 8192, 1024), id_a, kk > 0);
+        tc_commit(A_DONE);
+      };
+      load(0);
+      if (ntiles > 1) load(1);
+      bool ok = mbar_wait(FULL(0), 0, fail);
+      if (ok) {
+        tc_fence_after();
+        issue_a(0);
+      }
+      for (int t = 0; ok && t < ntiles; ++t) {
+        const int s = t % QST;
+        const uint32_t sq = sbase + O_ST + s * STAGE, sy = sq + TILE;
+        if (!mbar_wait(DN_READY, t & 1, fail)) break;
+        tc_fence_after();
+        // (d): K = f.  A = dn (the dy tile) K-major; B = S' K-major (rows e).
+#pragma unroll
+        for (int kk = 0; kk < QD / 16; ++kk)
+          tc_mma(tmem + 64, sdesc(sy + 32 * kk, 16, 1024), sdesc(sS + 32 * kk, 16, 1024), id_d, kk > 0);
+        tc_commit(D_DONE);
+        // (e): K = rows.  A = [dn | dden ...] M-major, its two 64-wide halves the
+        // dy and r tiles (one tile apart); B = phi(Q) N-major.
+#pragma unroll
+        for (int kk = 0; kk < QT / 16; ++kk)
+          tc_mma(tmem + 128, sdesc(sy + 2048 * kk, TILE, 1024), sdesc(sq + 2048 * kk, 8192, 1024), id_e,
+                 (t > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(EMPTY(s));
+        if (t + 1 < ntiles) {
+          if (!mbar_wait(FULL((t + 1) % QST), ((t + 1) / QST) & 1, fail)) break;
+          tc_fence_after();
+          issue_a(t + 1);
+        }
+        if (t + QST < ntiles) {
+          if (!mbar_wait(EMPTY(s), (t / QST) & 1, fail)) break;
+          load(t + QST);
+        }
+      }
+      tc_commit(FIN);  // completes once every MMA issued above has finished
+      for (uint32_t k = 0; k < kPollLimit && !mbar_try_wait(FIN, 0); ++k) {
+      }
+      if (*fail) {  // let the copies still in flight land
+        for (int s = 0; s < QST; ++s) {
+          const int u = s == 0 ? issued0 : issued1;
+          if (u > 0)
+            for (uint32_t k = 0; k < kPollLimit && !mbar_try_wait(FULL(s), (uint32_t)((u - 1) / QST) & 1); ++k) {
+            }
+        }
+      }
+    }
+  } else {
+    // ----------------------------------------------------------- epilogue
+    const int q = warp & 3, part = warp >> 2;
+    const int i = q * 32 + lane;  // tile row = TMEM lane
+    const int f0 = part * Q::CPT;
+    const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
+    for (int t = 0; t < ntiles; ++t) {
+      const int s = t % QST;
+      uint8_t* sq = smem + O_ST + s * STAGE;
+      uint8_t* sy = sq + TILE;
+      uint8_t* sr = sy + TILE;
+      const int rel = t * QT + i;
+      const bool valid = rel < nval, store = rel < nrows;
+      float2 ri = make_float2(0.f, 0.f);
+      if (valid) ri = *reinterpret_cast<const float2*>(a.rsinv + 2 * ((rb + rel) * H + h));
+      const float rs = ri.x, inv = ri.y;  // 0 on rows outside the sequence: u = dn = 0 there
+      mbar_wait(A_DONE, t & 1, fail);
+      tc_fence_after();
+      // pass 1: dr, dgamma, du (into the r tile); sums m = du . u, D1 = du . o', D2 = u . o'
+      float m = 0.f, D1 = 0.f, D2 = 0.f;
+      {
+        uint32_t o[2][8], g[2][8];
+        tmem_ld8_async(tl + f0, o[0]);
+        if (t > 0) {
+          tmem_ld8_async(tl + 192 + f0, g[0]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) g[0][j] = 0u;
+        }
+        tmem_wait(o[0], g[0]);
+#pragma unroll
+        for (int ch = 0; ch < Q::NC; ++ch) {
+          const int cur = ch & 1, nxt = cur ^ 1;
+          const int f = f0 + 8 * ch, cc = f >> 3;
+          if (ch + 1 < Q::NC) {
+            tmem_ld8_async(tl + f + 8, o[nxt]);
+            if (t > 0) {
+              tmem_ld8_async(tl + 192 + f + 8, g[nxt]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) g[nxt][j] = 0u;
+            }
+          }
+          float yv[8], rv[8];
+          unpack8(*reinterpret_cast<const uint4*>(sy + swz_off(i, cc)), yv);
+          unpack8(*reinterpret_cast<const uint4*>(sr + swz_off(i, cc)), rv);
+          uint32_t dup[4], drp[4];
+#pragma unroll
+          for (int j = 0; j < 8; j += 2) {
+            float du2[2], dr2[2];
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+              const int jj = j + w;
+              const float op = __uint_as_float(o[cur][jj]) * inv;  // centred o'
+              const float u = (op + cen[f + jj]) * rs;
+              const float r = rv[jj], dy = yv[jj];
+              const float sg = sigmoid_fast(r);
+              const float av = r * sg;
+              const float dyg = dy * gam[f + jj];
+              du2[w] = dyg * av;
+              g[cur][jj] = __float_as_uint(fmaf(dy * av, u, __uint_as_float(g[cur][jj])));
+              dr2[w] = dyg * u * sg * fmaf(r, 1.f - sg, 1.f);
+              m = fmaf(du2[w], u, m);
+              D1 = fmaf(du2[w], op, D1);
+              D2 = fmaf(u, op, D2);
+            }
+            dup[j / 2] = pack_bf16(du2[0], du2[1]);
+            drp[j / 2] = pack_bf16(dr2[0], dr2[1]);
+          }
+          tmem_st8(tl + 192 + f, g[cur]);
+          *reinterpret_cast<uint4*>(sr + swz_off(i, cc)) = make_uint4(dup[0], dup[1], dup[2], dup[3]);
+          if (store)
+            *reinterpret_cast<uint4*>((bf16*)a.dr + (rb + rel) * a.lddr + (size_t)h * QD + f) =
+                make_uint4(drp[0], drp[1], drp[2], drp[3]);
+          if (ch + 1 < Q::NC) tmem_wait(o[nxt], g[nxt]);
+        }
+        tmem_st_wait();
+      }
+      if (EW == 8) {  // the row's two column ranges, added in a fixed order
+        xch[(0 + part) * QT + i] = m;
+        xch[(2 + part) * QT + i] = D1;
+        xch[(4 + part) * QT + i] = D2;
+        named_bar(1, EW * 32);
+        m = xch[0 * QT + i] + xch[1 * QT + i];
+        D1 = xch[2 * QT + i] + xch[3 * QT + i];
+        D2 = xch[4 * QT + i] + xch[5 * QT + i];
+      }
+      m *= 1.f / QD;
+      const float dden = -rs * fmaf(-m, D2, D1) * inv;
+      // pass 2: dn = rs (du - u m) / den -> the dy tile
+      {
+        uint32_t o[2][8];
+        tmem_ld8_async(tl + f0, o[0]);
+        tmem_wait(o[0]);
+#pragma unroll
+        for (int ch = 0; ch < Q::NC; ++ch) {
+          const int cur = ch & 1, nxt = cur ^ 1;
+          const int f = f0 + 8 * ch, cc = f >> 3;
+          if (ch + 1 < Q::NC) tmem_ld8_async(tl + f + 8, o[nxt]);
+          float du[8];
+          unpack8(*reinterpret_cast<const uint4*>(sr + swz_off(i, cc)), du);
+          uint32_t dn[4];
+#pragma unroll
+          for (int j = 0; j < 8; j += 2) {
+            float d2[2];
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+              const int jj = j + w;
+              const float u = fmaf(__uint_as_float(o[cur][jj]), inv, cen[f + jj]) * rs;
+              d2[w] = rs * fmaf(-u, m, du[jj]) * inv;
+            }
+            dn[j / 2] = pack_bf16(d2[0], d2[1]);
+          }
+          *reinterpret_cast<uint4*>(sy + swz_off(i, cc)) = make_uint4(dn[0], dn[1], dn[2], dn[3]);
+          if (ch + 1 < Q::NC) tmem_wait(o[nxt]);
+        }
+      }
+      // dden in column 64 of [dn | dden] (first element of the r tile's row);
+      // that chunk's du was consumed above by this row's first column range.
+      if (part == 0) *reinterpret_cast<uint4*>(sr + swz_off(i, 0)) = make_uint4(pack_bf16(dden, 0.f), 0u, 0u, 0u);
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(DN_READY);
+      // epilogue 2: dq = (dq~ + dden z) min(1, phi(q))
+      mbar_wait(D_DONE, t & 1, fail);
+      tc_fence_after();
+      {
+        uint32_t o[2][8];
+        tmem_ld8_async(tl + 64 + f0, o[0]);
+        tmem_wait(o[0]);
+#pragma unroll
+        for (int ch = 0; ch < Q::NC; ++ch) {
+          const int cur = ch & 1, nxt = cur ^ 1;
+          const int f = f0 + 8 * ch, cc = f >> 3;
+          if (ch + 1 < Q::NC) tmem_ld8_async(tl + 64 + f + 8, o[nxt]);
+          float qv[8];
+          unpack8(*reinterpret_cast<const uint4*>(sq + swz_off(i, cc)), qv);
+          uint32_t dq[4];
+#pragma unroll
+          for (int j = 0; j < 8; j += 2)
+            dq[j / 2] = pack_bf16(fmaf(dden, zf[f + j], __uint_as_float(o[cur][j])) * fminf(1.f, qv[j]),
+                                  fmaf(dden, zf[f + j + 1], __uint_as_float(o[cur][j + 1])) * fminf(1.f, qv[j + 1]));
+          if (store)
+            *reinterpret_cast<uint4*>((bf16*)a.dq + (rb + rel) * a.lddq + (size_t)h * QD + f) =
+                make_uint4(dq[0], dq[1], dq[2], dq[3]);
+          if (ch + 1 < Q::NC) tmem_wait(o[nxt]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(EMPTY(s));
+    }
+    if (ntiles > 0) {
+      mbar_wait(FIN, 0, fail);
+      tc_fence_after();
+    }
+  }
+  __syncthreads();
+  const bool bad = *fail != 0;
+
+  // The chunk's partials: [dS' | dz'] (TMEM lane f = column f of the state,
+  // columns 128 + e) and dgamma (per-lane sums, reduced over the 128 lanes).
+  constexpr int LD = state_ld(QD);
+  float* red = reinterpret_cast<float*>(smem + O_ST);  // [128][65]: the stages are free now
+  if (!bad && warp < EW) {
+    const int q = warp & 3, part = warp >> 2;
+    const int i = q * 32 + lane;
+    const int f0 = part * Q::CPT;
+    const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
+    float* P = a.partial + ((size_t)blockIdx.x * H + h) * QD * LD;
+#pragma unroll
+    for (int ch = 0; ch < Q::NC; ++ch) {
+      const int e0 = f0 + 8 * ch;
+      uint32_t dsv[8], gv[8];
+      if (ntiles > 0) {
+        tmem_ld8_async(tl + 128 + e0, dsv);
+        tmem_ld8_async(tl + 192 + e0, gv);
+        tmem_wait(dsv, gv);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) dsv[j] = gv[j] = 0u;
+      }
+      if (i < LD)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) P[(size_t)(e0 + j) * LD + i] = i <= QD ? __uint_as_float(dsv[j]) : 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) red[i * (QD + 1) + e0 + j] = __uint_as_float(gv[j]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == EW) tmem_dealloc(tmem, TMEM_COLS);
+  if (bad) {
+    if (tid == 0 && a.err_out) atomicOr(a.err_out, kErrTimeout);
+    return;
+  }
+  for (int f = tid; f < QD; f += Q::NTH) {
+    float v = 0.f;
+    for (int r = 0; r < QT; ++r) v += red[r * (QD + 1) + f];
+    a.gamma_part[((size_t)blockIdx.x * H + h) * QD + f] = v;
+  }
+  int first, count;
+  seq_tiles(a.seq, a.chunks, b, first, count);
+  if (!arrive_last(a.counters + (size_t)b * H + h, count)) return;
+  combine_state(a.partial, nullptr, first, count, H, h, QD, b * H + h, false, a.dstate, a.dstate_bf, nullptr,
+                nullptr, nullptr, a.center);
+}
+
+template <int EW>
+cudaError_t launch_ew(const BwdQArgs& a, const CUtensorMap& tmP, const CUtensorMap& tmY, int roff, int grid_x,
+                      cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(k_bwd_q_tc<EW>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_bwd_q_tc<EW>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  k_bwd_q_tc<EW><<<dim3(grid_x, a.H), QCfg<EW>::NTH, SMEM, st>>>(a, tmP, tmY, roff);
+  return cudaGetLastError();
+}
+
+constexpr int kEpilogueWarps = 8;
+
+}  // namespace
+
+cudaError_t launch_bwd_q_tc(const BwdQArgs& a, int hd, int grid_x, cudaStream_t st) {
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  const long long roff = ((const bf16*)a.r - (const bf16*)a.q);
+  if (a.dh != QD || !a.pre || !a.rms_w || !a.rsinv || hd % 8 || a.ldr != a.ldq || roff < 0 || roff % 8 ||
+      !al16(a.q) || !al16(a.dy) || !al16(a.dq) || !al16(a.dr) || a.ldq % 8 || a.lddy % 8 || a.lddq % 8 ||
+      a.lddr % 8 || a.seq.T <= 0)
+    return cudaErrorNotSupported;
+  CUtensorMap tmP, tmY;
+  if (!make_map(&tmP, a.q, (uint64_t)a.ldq, (uint64_t)a.seq.T, (uint64_t)a.ldq, 64, QT) ||
+      !make_map(&tmY, a.dy, (uint64_t)a.lddy, (uint64_t)a.seq.T, (uint64_t)a.lddy, 64, QT))
+    return cudaErrorNotSupported;
+  return launch_ew<kEpilogueWarps>(a, tmP, tmY, (int)roff, grid_x, st);
+}
+
+}  // namespace gbla

@@ -329,6 +329,7 @@ __global__ void __launch_bounds__(128) k_readout_bf16(const ReadoutArgs a) {
       o[nt][0] = acc[nt][0] * inv0 + c0 * cen[nt][0]; o[nt][1] = acc[nt][1] * inv0 + c0 * cen[nt][1];
       o[nt][2] = acc[nt][2] * inv1 + c1 * cen[nt][0]; o[nt][3] = acc[nt][3] * inv1 + c1 * cen[nt][1];
     }
+    float rs0 = 1.f, rs1 = 1.f;
     if (NORM) {
       float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
@@ -338,7 +339,7 @@ __global__ void __launch_bounds__(128) k_readout_bf16(const ReadoutArgs a) {
       }
       ss0 += __shfl_xor_sync(FULL, ss0, 1); ss0 += __shfl_xor_sync(FULL, ss0, 2);
       ss1 += __shfl_xor_sync(FULL, ss1, 1); ss1 += __shfl_xor_sync(FULL, ss1, 2);
-      const float rs0 = rsqrtf(ss0 / DH + a.eps), rs1 = rsqrtf(ss1 / DH + a.eps);
+      rs0 = rsqrtf(ss0 / DH + a.eps); rs1 = rsqrtf(ss1 / DH + a.eps);
       const uint8_t* rtb = rt + buf * R::TILE;
 #pragma unroll
       for (int nt = 0; nt < DH / 8; ++nt) {
@@ -367,6 +368,10 @@ __global__ void __launch_bounds__(128) k_readout_bf16(const ReadoutArgs a) {
     if (a.den && t4 == 0) {
       if (ra < nrows) a.den[(rb + ra) * H + h] = va ? den0 : 0.f;
       if (rb2 < nrows) a.den[(rb + rb2) * H + h] = vb ? den1 : 0.f;
+    }
+    if (NORM && a.rsinv && t4 == 0) {
+      if (ra < nrows) *reinterpret_cast<float2*>(a.rsinv + 2 * ((rb + ra) * H + h)) = make_float2(va ? rs0 : 0.f, inv0);
+      if (rb2 < nrows) *reinterpret_cast<float2*>(a.rsinv + 2 * ((rb + rb2) * H + h)) = make_float2(vb ? rs1 : 0.f, inv1);
     }
     __syncthreads();
   }

@@ -55,6 +55,7 @@ struct ReadoutArgs {
   const float* center;              // [n_seq*H][dh] or null (state is uncentred)
   void* out; int64_t ldo;
   float* den;                       // [rows, H] or null
+  float* rsinv;                     // norm, bf16: [rows, H] x {rs, 1/den} (0 on invalid rows) or null
   int H, dh;
   SeqDesc seq; Tiling tiles;
   const int* err;
@@ -75,7 +76,9 @@ struct BwdQArgs {
   float* dstate; bf16* dstate_bf;   // combined [dS | dz]
   int H, dh;
   SeqDesc seq; Tiling chunks;
+  const float* rsinv;               // tcgen05 kernel: [rows, H] x {rs, 1/den} from the forward
   const int* err;
+  int* err_out;                     // tcgen05 kernel: timeout bit of the workspace error word
 };
 
 struct BwdKVArgs {
@@ -138,6 +141,9 @@ cudaError_t launch_plan(const SeqDesc& s, int ntile, const int* tile_sizes, int3
 cudaError_t launch_reduce_bf16(const ReduceArgs& a, int grid_x, cudaStream_t st);
 cudaError_t launch_readout_bf16(const ReadoutArgs& a, bool norm, int grid_x, cudaStream_t st);
 cudaError_t launch_bwd_q_bf16(const BwdQArgs& a, bool norm, int grid_x, cudaStream_t st);
+// tcgen05 query-side backward (bwd_q_tc.cu): d_h = 64, the layer's RMSNorm
+// epilogue, phi(q) stored (pre); cudaErrorNotSupported otherwise.
+cudaError_t launch_bwd_q_tc(const BwdQArgs& a, int hd, int grid_x, cudaStream_t st);
 cudaError_t launch_bwd_kv_bf16(const BwdKVArgs& a, int grid_x, cudaStream_t st);
 
 cudaError_t launch_reduce_f32(const ReduceArgs& a, int grid_x, cudaStream_t st);
