@@ -84,9 +84,18 @@ gbla_status make_plan(const gbla_shape* s, Plan& p) {
     p.tile_per_seq = cdiv(p.L, p.tile);
     p.n_tiles = p.tile_per_seq * p.n_seq;
   }
-  // dW = x~^T dP: split the T rows so that d/128 x NP/128 tiles x splits fill the GPU
-  const int tiles = cdiv(p.d, 128) * cdiv(p.NP, 128);
-  const int want_split = std::max(1, std::min(cdiv(2 * kSMs, tiles), cdiv(p.T, 1024)));
+  // dW = x~^T dP: split the T rows so that output tiles x splits fill whole
+  // waves of the GPU (tiles of the bf16 tensor-core GEMM: 128 x 256; of the
+  // fp32 GEMM: 64 x 64), each split at least 1024 rows.
+  const int tiles = p.f32 ? cdiv(p.d, 64) * cdiv(p.NP, 64) : cdiv(p.d, 128) * cdiv(p.NP, 256);
+  const int max_split = std::max(1, std::min(16, p.T / 1024));
+  int want_split = 1;
+  double best = -1.0;
+  for (int sp = 1; sp <= max_split; ++sp) {
+    const int units = tiles * sp;
+    const double eff = (double)units / ((double)cdiv(units, kSMs) * kSMs);
+    if (eff > best + 0.02) { best = eff; want_split = sp; }  // the smallest split within 2% of the best
+  }
   p.wsplit = cdiv(cdiv(p.T, want_split), 64) * 64;
   p.n_wsplit = cdiv(p.T, p.wsplit);
   p.conv_blocks = conv_bwd_parts_max(p.T);

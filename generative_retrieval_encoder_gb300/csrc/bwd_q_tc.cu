@@ -102,12 +102,13 @@ __global__ void __maxnreg__(QCfg<EW>::MAXREG)
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (a.err && *a.err) return;
+  // grid (head, chunk): the heads of a chunk run together and read whole rows of P
+  const int h = blockIdx.x, H = a.H, cb = blockIdx.y;
   int b, row0, nvalid, cin;
-  if (!map_tile(a.seq, a.chunks, blockIdx.x, b, row0, nvalid, cin)) {  // no chunk: a zero dgamma partial
-    for (int f = tid; f < QD; f += Q::NTH) a.gamma_part[((size_t)blockIdx.x * a.H + blockIdx.y) * QD + f] = 0.f;
+  if (!map_tile(a.seq, a.chunks, cb, b, row0, nvalid, cin)) {  // no chunk: a zero dgamma partial
+    for (int f = tid; f < QD; f += Q::NTH) a.gamma_part[((size_t)cb * H + h) * QD + f] = 0.f;
     return;
   }
-  const int h = blockIdx.y, H = a.H;
   const int CH = a.chunks.tile, c0 = cin * CH;
   const int nrows = max(0, min(CH, slot_rows(a.seq, nvalid) - c0));
   const int nval = max(0, min(nrows, nvalid - c0));
@@ -233,16 +234,22 @@ __global__ void __maxnreg__(QCfg<EW>::MAXREG)
     const int i = q * 32 + lane;  // tile row = TMEM lane
     const int f0 = part * Q::CPT;
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
+    // rs and 1/den of this thread's row, one tile ahead (0 on rows outside the sequence: u = dn = 0 there)
+    auto rsinv_of = [&](int t) {
+      const int rel = t * QT + i;
+      return rel < nval ? __ldg(reinterpret_cast<const float2*>(a.rsinv + 2 * ((rb + rel) * H + h)))
+                        : make_float2(0.f, 0.f);
+    };
+    float2 ri_next = ntiles > 0 ? rsinv_of(0) : make_float2(0.f, 0.f);
     for (int t = 0; t < ntiles; ++t) {
       const int s = t % QST;
       uint8_t* sq = smem + O_ST + s * STAGE;
       uint8_t* sy = sq + TILE;
       uint8_t* sr = sy + TILE;
       const int rel = t * QT + i;
-      const bool valid = rel < nval, store = rel < nrows;
-      float2 ri = make_float2(0.f, 0.f);
-      if (valid) ri = *reinterpret_cast<const float2*>(a.rsinv + 2 * ((rb + rel) * H + h));
-      const float rs = ri.x, inv = ri.y;  // 0 on rows outside the sequence: u = dn = 0 there
+      const bool store = rel < nrows;
+      const float rs = ri_next.x, inv = ri_next.y;
+      if (t + 1 < ntiles) ri_next = rsinv_of(t + 1);
       mbar_wait(A_DONE, t & 1, fail);
       tc_fence_after();
       // pass 1: dr, dgamma, du (into the r tile); sums m = du . u, D1 = du . o', D2 = u . o'
@@ -397,7 +404,7 @@ __global__ void __maxnreg__(QCfg<EW>::MAXREG)
     const int i = q * 32 + lane;
     const int f0 = part * Q::CPT;
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
-    float* P = a.partial + ((size_t)blockIdx.x * H + h) * QD * LD;
+    float* P = a.partial + ((size_t)cb * H + h) * QD * LD;
 #pragma unroll
     for (int ch = 0; ch < Q::NC; ++ch) {
       const int e0 = f0 + 8 * ch;
@@ -427,7 +434,7 @@ __global__ void __maxnreg__(QCfg<EW>::MAXREG)
   for (int f = tid; f < QD; f += Q::NTH) {
     float v = 0.f;
     for (int r = 0; r < QT; ++r) v += red[r * (QD + 1) + f];
-    a.gamma_part[((size_t)blockIdx.x * H + h) * QD + f] = v;
+    a.gamma_part[((size_t)cb * H + h) * QD + f] = v;
   }
   int first, count;
   seq_tiles(a.seq, a.chunks, b, first, count);
@@ -444,7 +451,7 @@ cudaError_t launch_ew(const BwdQArgs& a, const CUtensorMap& tmP, const CUtensorM
   e = cudaFuncSetAttribute(k_bwd_q_tc<EW>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  k_bwd_q_tc<EW><<<dim3(grid_x, a.H), QCfg<EW>::NTH, SMEM, st>>>(a, tmP, tmY, roff);
+  k_bwd_q_tc<EW><<<dim3(a.H, grid_x), QCfg<EW>::NTH, SMEM, st>>>(a, tmP, tmY, roff);
   return cudaGetLastError();
 }
 
@@ -457,11 +464,13 @@ cudaError_t launch_bwd_q_tc(const BwdQArgs& a, int hd, int grid_x, cudaStream_t 
   const long long roff = ((const bf16*)a.r - (const bf16*)a.q);
   if (a.dh != QD || !a.pre || !a.rms_w || !a.rsinv || hd % 8 || a.ldr != a.ldq || roff < 0 || roff % 8 ||
       !al16(a.q) || !al16(a.dy) || !al16(a.dq) || !al16(a.dr) || a.ldq % 8 || a.lddy % 8 || a.lddq % 8 ||
-      a.lddr % 8 || a.seq.T <= 0)
+      a.lddr % 8 || a.seq.T <= 0 || grid_x > 65535)
     return cudaErrorNotSupported;
   CUtensorMap tmP, tmY;
-  if (!make_map(&tmP, a.q, (uint64_t)a.ldq, (uint64_t)a.seq.T, (uint64_t)a.ldq, 64, QT) ||
-      !make_map(&tmY, a.dy, (uint64_t)a.lddy, (uint64_t)a.seq.T, (uint64_t)a.lddy, 64, QT))
+  // 128-byte L2 promotion: a box row is one head's 128 bytes; wider promotion
+  // would fetch the neighbouring head's columns, which another CTA reads.
+  if (!make_map(&tmP, a.q, (uint64_t)a.ldq, (uint64_t)a.seq.T, (uint64_t)a.ldq, 64, QT, false) ||
+      !make_map(&tmY, a.dy, (uint64_t)a.lddy, (uint64_t)a.seq.T, (uint64_t)a.lddy, 64, QT, false))
     return cudaErrorNotSupported;
   return launch_ew<kEpilogueWarps>(a, tmP, tmY, (int)roff, grid_x, st);
 }

@@ -107,8 +107,9 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
 
 // Host: 2-D bf16 tensor map over a row-major [outer][inner] array (row pitch
 // ld elements), box {box_inner, box_outer}, 128-byte swizzle, zero fill out of
-// bounds.  False if the driver entry point or the encoding fails.
+// bounds, L2 promotion of 256 bytes (wide) or 128 bytes.  False if the driver
+// entry point or the encoding fails.
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner,
-              uint32_t box_outer);
+              uint32_t box_outer, bool wide_promotion = true);
 
 }  // namespace gbla
