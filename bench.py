@@ -35,9 +35,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # keyed by launch name: (bytes, workload name, sha1 of the kernel's source file when captured).
 # A source change since the capture makes the figure stale: it is then reported as null.
 NCU_TRAFFIC: dict = {}
-KERNEL_SOURCE = {"projection gemm": "gemm.cu", "dx~ gemm": "gemm.cu", "dW gemm": "gemm.cu",
-                 "reduce": "core_bf16.cu", "readout": "core_bf16.cu", "bwd_q": "core_bf16.cu",
-                 "bwd_kv": "core_bf16.cu", "conv": "layer_misc.cu", "conv bwd": "layer_misc.cu",
+KERNEL_SOURCE = {"projection gemm": "gemm_tc.cu", "dx~ gemm": "gemm_tc.cu", "dW gemm": "gemm_tc.cu",
+                 "reduce": "core_bf16.cu", "readout": "core_bf16.cu", "bwd_q": "bwd_q_tc.cu",
+                 "bwd_kv": "core_bf16.cu", "conv": "conv.cu", "conv bwd": "conv.cu",
                  "dW sum": "layer_misc.cu"}
 
 

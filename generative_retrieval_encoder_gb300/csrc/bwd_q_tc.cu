@@ -16,10 +16,12 @@
 // then the chunk's [dS' | dz'] and dgamma partials and the deterministic
 // split-L combine, as the mma.sync kernel of the same operation.
 //
-// Warp roles: EW epilogue warps (warp w reads TMEM lanes 32 (w % 4) .. + 31,
-// i.e. tile rows, and the columns of its range w / 4) and one control warp
-// whose lane 0 issues the TMA loads and the MMAs.  (a) of tile t + 1 is issued
-// as soon as epilogue 1 of tile t has read O', so it runs under epilogue 2.
+// Eight warps: warp w reads TMEM lanes 32 (w % 4) .. + 31 (tile rows) and the
+// columns 32 (w / 4) .. + 31.  Thread 0 also issues the TMA loads and the MMAs,
+// at the points where the tile's data is complete anyway: (d), (e) and (a) of
+// tile t + 1 once every warp has written dn (so (a) of t + 1 runs under
+// epilogue 2 of t), the load of tile t + 2 once every warp is done with t.
+// Without a separate control warp, two CTAs per SM keep 128 registers a thread.
 // Operand tiles are [128 rows][64 bf16] in the 128-byte swizzle shared by
 // TMA and the MMA descriptors; the epilogue writes dn and dden into the dy and
 // r tiles of the same stage (each thread owns its row's columns), which then
@@ -53,14 +55,15 @@ constexpr int SMEM = O_FAIL + 4 + 1024;      // + alignment slack
 constexpr int TMEM_COLS = 256;               // O' | dq~ | dS' | dgamma
 static_assert(2 * (SMEM + 1024) <= 233472, "two CTAs per SM");
 static_assert(QST == 2, "the control thread tracks two stages");
+static_assert(QST * STAGE >= QD * state_ld(QD) * 4 && QST * STAGE >= (QT + 4) * (QD + 1) * 4,
+              "the stage memory holds the end-of-chunk reductions and the combine's staging");
+static_assert(QD / 2 == 32, "a thread holds 32 columns (one 32-column TMEM load)");
 
-template <int EW> struct QCfg {
-  static constexpr int NTH = (EW + 1) * 32;  // + the control warp
-  static constexpr int CPT = QD / (EW / 4);  // columns per epilogue thread
-  static constexpr int NC = CPT / 8;         // 8-column chunks per thread
-  // Two CTAs per SM: 2 (EW + 1) warps over 4 sub-partitions of 16K registers.
-  static constexpr int MAXREG = EW == 8 ? 96 : 168;
-};
+constexpr int EW = 8;                 // warps
+constexpr int NTH = EW * 32;
+constexpr int CPT = QD / (EW / 4);    // columns per thread
+constexpr int NC = CPT / 8;           // 8-column chunks per thread
+static_assert(NTH == 4 * QD, "the dgamma sum maps threads to (quarter, column)");
 
 __device__ __forceinline__ uint32_t swz_off(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
@@ -75,14 +78,8 @@ __device__ __forceinline__ void tmem_ld8_async(uint32_t taddr, uint32_t (&r)[8])
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
                : "r"(taddr));
 }
-// Waits for the thread's TMEM loads; the registers of `r` are tied to the wait
-// so that no use of them moves above it.
-__device__ __forceinline__ void tmem_wait(uint32_t (&r)[8]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
-               :
-               : "memory");
-}
+// Waits for the thread's TMEM loads; the registers are tied to the wait so
+// that no use of them moves above it.
 __device__ __forceinline__ void tmem_wait(uint32_t (&r)[8], uint32_t (&s)[8]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;"
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
@@ -90,13 +87,17 @@ __device__ __forceinline__ void tmem_wait(uint32_t (&r)[8], uint32_t (&s)[8]) {
                :
                : "memory");
 }
-__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
+// sigmoid(x) = (1 + tanh(x / 2)) / 2 with the hardware tanh approximation
+// (relative error about 2^-11, far below the bf16 rounding of the outputs).
+__device__ __forceinline__ float sigmoid_fast(float x) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
+  return fmaf(0.5f, t, 0.5f);
+}
 
-template <int EW>
-__global__ void __maxnreg__(QCfg<EW>::MAXREG)
+__global__ void __launch_bounds__(NTH, 2)
     k_bwd_q_tc(const BwdQArgs a, const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmY,
                int roff) {
-  using Q = QCfg<EW>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -106,7 +107,7 @@ __global__ void __maxnreg__(QCfg<EW>::MAXREG)
   const int h = blockIdx.x, H = a.H, cb = blockIdx.y;
   int b, row0, nvalid, cin;
   if (!map_tile(a.seq, a.chunks, cb, b, row0, nvalid, cin)) {  // no chunk: a zero dgamma partial
-    for (int f = tid; f < QD; f += Q::NTH) a.gamma_part[((size_t)cb * H + h) * QD + f] = 0.f;
+    for (int f = tid; f < QD; f += NTH) a.gamma_part[((size_t)cb * H + h) * QD + f] = 0.f;
     return;
   }
   const int CH = a.chunks.tile, c0 = cin * CH;
@@ -126,23 +127,23 @@ __global__ void __maxnreg__(QCfg<EW>::MAXREG)
   auto FULL = [&](int s) { return bar0 + 8 * s; };
   auto EMPTY = [&](int s) { return bar0 + 8 * (QST + s); };
 
-  // S' into its swizzled rows e; fp32 gamma, centre and z.
-  constexpr int BLD = state_bf_ld(QD);
-  const bf16* sbf = a.state_bf + (size_t)(b * H + h) * QD * BLD;
-  for (int i = tid; i < QD * 8; i += Q::NTH) {
-    const int e = i >> 3, c = i & 7;
-    *reinterpret_cast<uint4*>(smem + O_S + swz_off(e, c)) = *reinterpret_cast<const uint4*>(sbf + e * BLD + c * 8);
-  }
-  for (int f = tid; f < QD; f += Q::NTH) {
-    gam[f] = a.rms_w ? __bfloat162float(((const bf16*)a.rms_w)[f]) : 1.f;
-    cen[f] = a.center ? a.center[(size_t)(b * H + h) * QD + f] : 0.f;
-    zf[f] = __bfloat162float(sbf[f * BLD + QD]);
-  }
-  fence_async_smem();
-  if (tid == 0) {
+  // ---------------------------------------------------------- thread 0: copies and MMAs
+  const bool leader = tid == 0;
+  int issued0 = 0, issued1 = 0;  // 1 + index of the last tile loaded into stage 0 / 1
+  auto load = [&](int t) {
+    const int s = t % QST;
+    const uint32_t st = sbase + O_ST + s * STAGE;
+    const int y = (int)rb + t * QT;
+    mbar_expect_tx(FULL(s), 3 * TILE);
+    tma_load_2d(st, &tmP, FULL(s), h * QD, y);
+    tma_load_2d(st + TILE, &tmY, FULL(s), h * QD, y);
+    tma_load_2d(st + 2 * TILE, &tmP, FULL(s), roff + h * QD, y);
+    if (s == 0) issued0 = t + 1; else issued1 = t + 1;
+  };
+  if (leader) {  // barriers, then the first two tiles' copies before anything else
     for (int s = 0; s < QST; ++s) {
       mbar_init(FULL(s), 1);
-      mbar_init(EMPTY(s), EW + 1);  // (e) commit + one arrival per epilogue warp
+      mbar_init(EMPTY(s), EW + 1);  // (e) commit + one arrival per warp
     }
     mbar_init(A_DONE, 1);
     mbar_init(DN_READY, EW);
@@ -150,89 +151,74 @@ __global__ void __maxnreg__(QCfg<EW>::MAXREG)
     mbar_init(FIN, 1);
     mbar_init_fence();
     *fail = 0;
+    if (ntiles > 0) load(0);
+    if (ntiles > 1) load(1);
   }
-  if (warp == EW) tmem_alloc(smem_u32(slot), TMEM_COLS);
+  // S' into its swizzled rows e; fp32 gamma, centre and z.
+  constexpr int BLD = state_bf_ld(QD);
+  const bf16* sbf = a.state_bf + (size_t)(b * H + h) * QD * BLD;
+  for (int i = tid; i < QD * 8; i += NTH) {
+    const int e = i >> 3, c = i & 7;
+    *reinterpret_cast<uint4*>(smem + O_S + swz_off(e, c)) = *reinterpret_cast<const uint4*>(sbf + e * BLD + c * 8);
+  }
+  for (int f = tid; f < QD; f += NTH) {
+    gam[f] = a.rms_w ? __bfloat162float(((const bf16*)a.rms_w)[f]) : 1.f;
+    cen[f] = a.center ? a.center[(size_t)(b * H + h) * QD + f] : 0.f;
+    zf[f] = __bfloat162float(sbf[f * BLD + QD]);
+  }
+  fence_async_smem();
+  if (warp == 0) tmem_alloc(smem_u32(slot), TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *slot;
 
-  if (warp == EW) {
-    // ------------------------------------------------------------ control
-    if (lane == 0 && ntiles > 0) {
-      int issued0 = 0, issued1 = 0;  // 1 + index of the last tile loaded into stage 0 / 1
-      auto load = [&](int t) {
-        const int s = t % QST;
-        const uint32_t st = sbase + O_ST + s * STAGE;
-        const int y = (int)rb + t * QT;
-        mbar_expect_tx(FULL(s), 3 * TILE);
-        tma_load_2d(st, &tmP, FULL(s), h * QD, y);
-        tma_load_2d(st + TILE, &tmY, FULL(s), h * QD, y);
-        tma_load_2d(st + 2 * TILE, &tmP, FULL(s), roff + h * QD, y);
-        if (s == 0) issued0 = t + 1; else issued1 = t + 1;
-      };
-      const uint32_t id_a = idesc_bf16(QT, QD, false, true);
-      const uint32_t id_d = idesc_bf16(QT, QD, false, false), id_e = idesc_bf16(QT, QD, true, true);
-      const uint32_t sS = sbase + O_S;
-      // (a): K = e.  A = phi(Q) K-major (+32 B per 16 e); B = S' N-major (16 e-rows = 2048 B).
-      auto issue_a = [&](int t) {
-        const uint32_t sq = sbase + O_ST + (t % QST) * STAGE;
+  const uint32_t sS = sbase + O_S;
+  // (a): K = e.  A = phi(Q) K-major (+32 B per 16 e); B = S' N-major (16 e-rows = 2048 B).
+  auto issue_a = [&](int t) {
+    const uint32_t sq = sbase + O_ST + (t % QST) * STAGE;
+    const uint32_t id_a = idesc_bf16(QT, QD, false, true);
 #pragma unroll
-        for (int kk = 0; kk < QD / 16; ++kk)
-          tc_mma(tmem, sdesc(sq + 32 * kk, 16, 1024), sdesc(sS + 2048 * kk, 8192, 1024), id_a, kk > 0);
-        tc_commit(A_DONE);
-      };
-      load(0);
-      if (ntiles > 1) load(1);
-      bool ok = mbar_wait(FULL(0), 0, fail);
-      if (ok) {
-        tc_fence_after();
-        issue_a(0);
-      }
-      for (int t = 0; ok && t < ntiles; ++t) {
-        const int s = t % QST;
-        const uint32_t sq = sbase + O_ST + s * STAGE, sy = sq + TILE;
-        if (!mbar_wait(DN_READY, t & 1, fail)) break;
-        tc_fence_after();
-        // (d): K = f.  A = dn (the dy tile) K-major; B = S' K-major (rows e).
+    for (int kk = 0; kk < QD / 16; ++kk)
+      tc_mma(tmem, sdesc(sq + 32 * kk, 16, 1024), sdesc(sS + 2048 * kk, 8192, 1024), id_a, kk > 0);
+    tc_commit(A_DONE);
+  };
+  // (d), (e) of tile t and (a) of tile t + 1, once every warp has written dn and dden.
+  auto issue_de = [&](int t) {
+    const int s = t % QST;
+    const uint32_t sq = sbase + O_ST + s * STAGE, sy = sq + TILE;
+    if (!mbar_wait(DN_READY, t & 1, fail)) return;
+    tc_fence_after();
+    // (d): K = f.  A = dn (the dy tile) K-major; B = S' K-major (rows e).
+    const uint32_t id_d = idesc_bf16(QT, QD, false, false), id_e = idesc_bf16(QT, QD, true, true);
 #pragma unroll
-        for (int kk = 0; kk < QD / 16; ++kk)
-          tc_mma(tmem + 64, sdesc(sy + 32 * kk, 16, 1024), sdesc(sS + 32 * kk, 16, 1024), id_d, kk > 0);
-        tc_commit(D_DONE);
-        // (e): K = rows.  A = [dn | dden ...] M-major, its two 64-wide halves the
-        // dy and r tiles (one tile apart); B = phi(Q) N-major.
-#pragma unroll
-        for (int kk = 0; kk < QT / 16; ++kk)
-          tc_mma(tmem + 128, sdesc(sy + 2048 * kk, TILE, 1024), sdesc(sq + 2048 * kk, 8192, 1024), id_e,
-                 (t > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(EMPTY(s));
-        if (t + 1 < ntiles) {
-          if (!mbar_wait(FULL((t + 1) % QST), ((t + 1) / QST) & 1, fail)) break;
-          tc_fence_after();
-          issue_a(t + 1);
-        }
-        if (t + QST < ntiles) {
-          if (!mbar_wait(EMPTY(s), (t / QST) & 1, fail)) break;
-          load(t + QST);
-        }
-      }
-      tc_commit(FIN);  // completes once every MMA issued above has finished
-      for (uint32_t k = 0; k < kPollLimit && !mbar_try_wait(FIN, 0); ++k) {
-      }
-      if (*fail) {  // let the copies still in flight land
-        for (int s = 0; s < QST; ++s) {
-          const int u = s == 0 ? issued0 : issued1;
-          if (u > 0)
-            for (uint32_t k = 0; k < kPollLimit && !mbar_try_wait(FULL(s), (uint32_t)((u - 1) / QST) & 1); ++k) {
-            }
-        }
-      }
+    for (int kk = 0; kk < QD / 16; ++kk)
+      tc_mma(tmem + 64, sdesc(sy + 32 * kk, 16, 1024), sdesc(sS + 32 * kk, 16, 1024), id_d, kk > 0);
+    tc_commit(D_DONE);
+    // (a) of the next tile before (e): epilogue 2 and the next epilogue 1 wait
+    // on (d) and (a); (e) only gates the reuse of this stage.
+    if (t + 1 < ntiles && mbar_wait(FULL((t + 1) % QST), ((t + 1) / QST) & 1, fail)) {
+      tc_fence_after();
+      issue_a(t + 1);
     }
-  } else {
-    // ----------------------------------------------------------- epilogue
+    // (e): K = rows.  A = [dn | dden ...] M-major, its two 64-wide halves the
+    // dy and r tiles (one tile apart); B = phi(Q) N-major.
+#pragma unroll
+    for (int kk = 0; kk < QT / 16; ++kk)
+      tc_mma(tmem + 128, sdesc(sy + 2048 * kk, TILE, 1024), sdesc(sq + 2048 * kk, 8192, 1024), id_e,
+             (t > 0 || kk > 0) ? 1u : 0u);
+    tc_commit(EMPTY(s));
+  };
+  if (leader && ntiles > 0) {
+    if (mbar_wait(FULL(0), 0, fail)) {
+      tc_fence_after();
+      issue_a(0);
+    }
+  }
+  {
     const int q = warp & 3, part = warp >> 2;
     const int i = q * 32 + lane;  // tile row = TMEM lane
-    const int f0 = part * Q::CPT;
+    const int f0 = part * CPT;
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
     // rs and 1/den of this thread's row, one tile ahead (0 on rows outside the sequence: u = dn = 0 there)
     auto rsinv_of = [&](int t) {
@@ -252,31 +238,21 @@ __global__ void __maxnreg__(QCfg<EW>::MAXREG)
       if (t + 1 < ntiles) ri_next = rsinv_of(t + 1);
       mbar_wait(A_DONE, t & 1, fail);
       tc_fence_after();
-      // pass 1: dr, dgamma, du (into the r tile); sums m = du . u, D1 = du . o', D2 = u . o'
+      // pass 1: dr, dgamma, du (into the r tile); sums m = du . u, D1 = du . o', D2 = u . o'.
       float m = 0.f, D1 = 0.f, D2 = 0.f;
+      uint32_t o[CPT];
       {
-        uint32_t o[2][8], g[2][8];
-        tmem_ld8_async(tl + f0, o[0]);
+        uint32_t g[CPT];
+        tmem_ld32(tl + f0, o);  // (waits)
         if (t > 0) {
-          tmem_ld8_async(tl + 192 + f0, g[0]);
+          tmem_ld32(tl + 192 + f0, g);
         } else {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) g[0][j] = 0u;
+          for (int j = 0; j < CPT; ++j) g[j] = 0u;
         }
-        tmem_wait(o[0], g[0]);
 #pragma unroll
-        for (int ch = 0; ch < Q::NC; ++ch) {
-          const int cur = ch & 1, nxt = cur ^ 1;
+        for (int ch = 0; ch < NC; ++ch) {
           const int f = f0 + 8 * ch, cc = f >> 3;
-          if (ch + 1 < Q::NC) {
-            tmem_ld8_async(tl + f + 8, o[nxt]);
-            if (t > 0) {
-              tmem_ld8_async(tl + 192 + f + 8, g[nxt]);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) g[nxt][j] = 0u;
-            }
-          }
           float yv[8], rv[8];
           unpack8(*reinterpret_cast<const uint4*>(sy + swz_off(i, cc)), yv);
           unpack8(*reinterpret_cast<const uint4*>(sr + swz_off(i, cc)), rv);
@@ -286,15 +262,15 @@ __global__ void __maxnreg__(QCfg<EW>::MAXREG)
             float du2[2], dr2[2];
 #pragma unroll
             for (int w = 0; w < 2; ++w) {
-              const int jj = j + w;
-              const float op = __uint_as_float(o[cur][jj]) * inv;  // centred o'
+              const int jj = j + w, k = 8 * ch + jj;
+              const float op = __uint_as_float(o[k]) * inv;  // centred o'
               const float u = (op + cen[f + jj]) * rs;
               const float r = rv[jj], dy = yv[jj];
               const float sg = sigmoid_fast(r);
               const float av = r * sg;
               const float dyg = dy * gam[f + jj];
               du2[w] = dyg * av;
-              g[cur][jj] = __float_as_uint(fmaf(dy * av, u, __uint_as_float(g[cur][jj])));
+              g[k] = __float_as_uint(fmaf(dy * av, u, __uint_as_float(g[k])));
               dr2[w] = dyg * u * sg * fmaf(r, 1.f - sg, 1.f);
               m = fmaf(du2[w], u, m);
               D1 = fmaf(du2[w], op, D1);
@@ -303,14 +279,12 @@ __global__ void __maxnreg__(QCfg<EW>::MAXREG)
             dup[j / 2] = pack_bf16(du2[0], du2[1]);
             drp[j / 2] = pack_bf16(dr2[0], dr2[1]);
           }
-          tmem_st8(tl + 192 + f, g[cur]);
           *reinterpret_cast<uint4*>(sr + swz_off(i, cc)) = make_uint4(dup[0], dup[1], dup[2], dup[3]);
           if (store)
             *reinterpret_cast<uint4*>((bf16*)a.dr + (rb + rel) * a.lddr + (size_t)h * QD + f) =
                 make_uint4(drp[0], drp[1], drp[2], drp[3]);
-          if (ch + 1 < Q::NC) tmem_wait(o[nxt], g[nxt]);
         }
-        tmem_st_wait();
+        tmem_st32(tl + 192 + f0, g);
       }
       if (EW == 8) {  // the row's two column ranges, added in a fixed order
         xch[(0 + part) * QT + i] = m;
@@ -324,69 +298,74 @@ __global__ void __maxnreg__(QCfg<EW>::MAXREG)
       m *= 1.f / QD;
       const float dden = -rs * fmaf(-m, D2, D1) * inv;
       // pass 2: dn = rs (du - u m) / den -> the dy tile
-      {
-        uint32_t o[2][8];
-        tmem_ld8_async(tl + f0, o[0]);
-        tmem_wait(o[0]);
+      tmem_ld32(tl + f0, o);  // O' again (waits)
 #pragma unroll
-        for (int ch = 0; ch < Q::NC; ++ch) {
-          const int cur = ch & 1, nxt = cur ^ 1;
-          const int f = f0 + 8 * ch, cc = f >> 3;
-          if (ch + 1 < Q::NC) tmem_ld8_async(tl + f + 8, o[nxt]);
-          float du[8];
-          unpack8(*reinterpret_cast<const uint4*>(sr + swz_off(i, cc)), du);
-          uint32_t dn[4];
+      for (int ch = 0; ch < NC; ++ch) {
+        const int f = f0 + 8 * ch, cc = f >> 3;
+        float du[8];
+        unpack8(*reinterpret_cast<const uint4*>(sr + swz_off(i, cc)), du);
+        uint32_t dn[4];
 #pragma unroll
-          for (int j = 0; j < 8; j += 2) {
-            float d2[2];
+        for (int j = 0; j < 8; j += 2) {
+          float d2[2];
 #pragma unroll
-            for (int w = 0; w < 2; ++w) {
-              const int jj = j + w;
-              const float u = fmaf(__uint_as_float(o[cur][jj]), inv, cen[f + jj]) * rs;
-              d2[w] = rs * fmaf(-u, m, du[jj]) * inv;
-            }
-            dn[j / 2] = pack_bf16(d2[0], d2[1]);
+          for (int w = 0; w < 2; ++w) {
+            const int jj = j + w;
+            const float u = fmaf(__uint_as_float(o[8 * ch + jj]), inv, cen[f + jj]) * rs;
+            d2[w] = rs * fmaf(-u, m, du[jj]) * inv;
           }
-          *reinterpret_cast<uint4*>(sy + swz_off(i, cc)) = make_uint4(dn[0], dn[1], dn[2], dn[3]);
-          if (ch + 1 < Q::NC) tmem_wait(o[nxt]);
+          dn[j / 2] = pack_bf16(d2[0], d2[1]);
         }
+        *reinterpret_cast<uint4*>(sy + swz_off(i, cc)) = make_uint4(dn[0], dn[1], dn[2], dn[3]);
       }
       // dden in column 64 of [dn | dden] (first element of the r tile's row);
       // that chunk's du was consumed above by this row's first column range.
       if (part == 0) *reinterpret_cast<uint4*>(sr + swz_off(i, 0)) = make_uint4(pack_bf16(dden, 0.f), 0u, 0u, 0u);
+      tmem_st_wait();
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(DN_READY);
+      if (leader) issue_de(t);
+      __syncwarp();
       // epilogue 2: dq = (dq~ + dden z) min(1, phi(q))
       mbar_wait(D_DONE, t & 1, fail);
       tc_fence_after();
-      {
-        uint32_t o[2][8];
-        tmem_ld8_async(tl + 64 + f0, o[0]);
-        tmem_wait(o[0]);
+      tmem_ld32(tl + 64 + f0, o);  // dq~ (waits)
 #pragma unroll
-        for (int ch = 0; ch < Q::NC; ++ch) {
-          const int cur = ch & 1, nxt = cur ^ 1;
-          const int f = f0 + 8 * ch, cc = f >> 3;
-          if (ch + 1 < Q::NC) tmem_ld8_async(tl + 64 + f + 8, o[nxt]);
-          float qv[8];
-          unpack8(*reinterpret_cast<const uint4*>(sq + swz_off(i, cc)), qv);
-          uint32_t dq[4];
+      for (int ch = 0; ch < NC; ++ch) {
+        const int f = f0 + 8 * ch, cc = f >> 3;
+        float qv[8];
+        unpack8(*reinterpret_cast<const uint4*>(sq + swz_off(i, cc)), qv);
+        uint32_t dq[4];
 #pragma unroll
-          for (int j = 0; j < 8; j += 2)
-            dq[j / 2] = pack_bf16(fmaf(dden, zf[f + j], __uint_as_float(o[cur][j])) * fminf(1.f, qv[j]),
-                                  fmaf(dden, zf[f + j + 1], __uint_as_float(o[cur][j + 1])) * fminf(1.f, qv[j + 1]));
-          if (store)
-            *reinterpret_cast<uint4*>((bf16*)a.dq + (rb + rel) * a.lddq + (size_t)h * QD + f) =
-                make_uint4(dq[0], dq[1], dq[2], dq[3]);
-          if (ch + 1 < Q::NC) tmem_wait(o[nxt]);
-        }
+        for (int j = 0; j < 8; j += 2)
+          dq[j / 2] = pack_bf16(fmaf(dden, zf[f + j], __uint_as_float(o[8 * ch + j])) * fminf(1.f, qv[j]),
+                                fmaf(dden, zf[f + j + 1], __uint_as_float(o[8 * ch + j + 1])) * fminf(1.f, qv[j + 1]));
+        if (store)
+          *reinterpret_cast<uint4*>((bf16*)a.dq + (rb + rel) * a.lddq + (size_t)h * QD + f) =
+              make_uint4(dq[0], dq[1], dq[2], dq[3]);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(EMPTY(s));
+      if (leader && t + QST < ntiles && mbar_wait(EMPTY(s), (t / QST) & 1, fail)) load(t + QST);
+      __syncwarp();
     }
+    if (leader && ntiles > 0) {
+      tc_commit(FIN);  // completes once every MMA issued above has finished
+      for (uint32_t k = 0; k < kPollLimit && !mbar_try_wait(FIN, 0); ++k) {
+      }
+      if (*fail) {  // let the copies still in flight land
+        for (int s = 0; s < QST; ++s) {
+          const int u = s == 0 ? issued0 : issued1;
+          if (u > 0)
+            for (uint32_t k = 0; k < kPollLimit && !mbar_try_wait(FULL(s), (uint32_t)((u - 1) / QST) & 1); ++k) {
+            }
+        }
+      }
+    }
+    __syncwarp();
     if (ntiles > 0) {
       mbar_wait(FIN, 0, fail);
       tc_fence_after();
@@ -399,14 +378,14 @@ __global__ void __maxnreg__(QCfg<EW>::MAXREG)
   // columns 128 + e) and dgamma (per-lane sums, reduced over the 128 lanes).
   constexpr int LD = state_ld(QD);
   float* red = reinterpret_cast<float*>(smem + O_ST);  // [128][65]: the stages are free now
-  if (!bad && warp < EW) {
+  if (!bad) {
     const int q = warp & 3, part = warp >> 2;
     const int i = q * 32 + lane;
-    const int f0 = part * Q::CPT;
+    const int f0 = part * CPT;
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
     float* P = a.partial + ((size_t)cb * H + h) * QD * LD;
 #pragma unroll
-    for (int ch = 0; ch < Q::NC; ++ch) {
+    for (int ch = 0; ch < NC; ++ch) {
       const int e0 = f0 + 8 * ch;
       uint32_t dsv[8], gv[8];
       if (ntiles > 0) {
@@ -426,36 +405,28 @@ __global__ void __maxnreg__(QCfg<EW>::MAXREG)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == EW) tmem_dealloc(tmem, TMEM_COLS);
+  if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
   if (bad) {
     if (tid == 0 && a.err_out) atomicOr(a.err_out, kErrTimeout);
     return;
   }
-  for (int f = tid; f < QD; f += Q::NTH) {
+  {  // dgamma: column f over the 128 lanes, four quarters then their sum, in a fixed order
+    float* red4 = red + QT * (QD + 1);
+    const int f = tid & (QD - 1), qr = tid / QD;
     float v = 0.f;
-    for (int r = 0; r < QT; ++r) v += red[r * (QD + 1) + f];
-    a.gamma_part[((size_t)cb * H + h) * QD + f] = v;
+    for (int r = qr * (QT / 4); r < (qr + 1) * (QT / 4); ++r) v += red[r * (QD + 1) + f];
+    red4[qr * QD + f] = v;
+    __syncthreads();
+    if (tid < QD)
+      a.gamma_part[((size_t)cb * H + h) * QD + tid] =
+          ((red4[tid] + red4[QD + tid]) + red4[2 * QD + tid]) + red4[3 * QD + tid];
   }
   int first, count;
   seq_tiles(a.seq, a.chunks, b, first, count);
   if (!arrive_last(a.counters + (size_t)b * H + h, count)) return;
   combine_state(a.partial, nullptr, first, count, H, h, QD, b * H + h, false, a.dstate, a.dstate_bf, nullptr,
-                nullptr, nullptr, a.center);
+                nullptr, nullptr, a.center, reinterpret_cast<float*>(smem + O_ST));
 }
-
-template <int EW>
-cudaError_t launch_ew(const BwdQArgs& a, const CUtensorMap& tmP, const CUtensorMap& tmY, int roff, int grid_x,
-                      cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(k_bwd_q_tc<EW>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_bwd_q_tc<EW>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
-  k_bwd_q_tc<EW><<<dim3(a.H, grid_x), QCfg<EW>::NTH, SMEM, st>>>(a, tmP, tmY, roff);
-  return cudaGetLastError();
-}
-
-constexpr int kEpilogueWarps = 8;
 
 }  // namespace
 
@@ -472,7 +443,12 @@ cudaError_t launch_bwd_q_tc(const BwdQArgs& a, int hd, int grid_x, cudaStream_t 
   if (!make_map(&tmP, a.q, (uint64_t)a.ldq, (uint64_t)a.seq.T, (uint64_t)a.ldq, 64, QT, false) ||
       !make_map(&tmY, a.dy, (uint64_t)a.lddy, (uint64_t)a.seq.T, (uint64_t)a.lddy, 64, QT, false))
     return cudaErrorNotSupported;
-  return launch_ew<kEpilogueWarps>(a, tmP, tmY, (int)roff, grid_x, st);
+  cudaError_t e = cudaFuncSetAttribute(k_bwd_q_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_bwd_q_tc, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  k_bwd_q_tc<<<dim3(a.H, grid_x), NTH, SMEM, st>>>(a, tmP, tmY, (int)roff);
+  return cudaGetLastError();
 }
 
 }  // namespace gbla

@@ -211,7 +211,8 @@ __global__ void __launch_bounds__(256) k_reduce_bf16(const ReduceArgs a) {
   seq_tiles(a.seq, a.chunks, b, first, count);
   if (!arrive_last(a.counters + (size_t)b * H + h, count)) return;
   combine_state(a.partial, a.partial_m, first, count, H, h, DH, b * H + h, logits, a.state,
-                a.state_bf, a.state_m, a.pub_state, a.center);
+                a.state_bf, a.state_m, a.pub_state, a.center, nullptr, reinterpret_cast<float*>(smem));
+  static_assert(R::SMEM >= DH * state_ld(DH) * 4, "the combine's staging buffer fits the tile memory");
 }
 
 // The centre c of the state (see combine_state) at the accumulator columns
@@ -722,8 +723,10 @@ __global__ void __launch_bounds__(BqCfg<DH, NORM>::NW * 32) k_bwd_q_bf16(const B
   int first, count;
   seq_tiles(a.seq, a.chunks, b, first, count);
   if (!arrive_last(a.counters + (size_t)b * H + h, count)) return;
+  // stage the combined state in the tile memory where it fits (not for d_h = 128 without the norm inputs)
+  constexpr bool kStage = R::STAGES * R::NIN * R::TILE >= DH * state_ld(DH) * 4;
   combine_state(a.partial, nullptr, first, count, H, h, DH, b * H + h, false, a.dstate, a.dstate_bf,
-                nullptr, nullptr, nullptr, a.center);
+                nullptr, nullptr, nullptr, a.center, kStage ? reinterpret_cast<float*>(tiles) : nullptr);
 }
 
 // =====================================================================

@@ -41,11 +41,15 @@ __device__ __forceinline__ bool arrive_last(int* counter, int count) {
 // multiplies with: then bf16(dS) v_j + dz'' = bf16(dS) (v_j - c) + dz' exactly
 // up to fp32 rounding, and no rounding of (v_j - c) enters the gate gradient
 // (whose sum over a sequence cancels to ~1/sqrt(L) of its terms).
+//
+// sbuf (optional, 16-byte aligned shared memory of dh * state_ld(dh) floats):
+// the combined state is staged there as well, so that the centring passes
+// read shared memory instead of the global copy just written.
 __device__ inline void combine_state(const float* partial, const float* partial_m, int first,
                                      int count, int H, int h, int dh, int seqh, bool logits,
                                      float* state, bf16* state_bf, float* state_m,
                                      float* pub_state, float* center = nullptr,
-                                     const float* fwd_center = nullptr) {
+                                     const float* fwd_center = nullptr, float* sbuf = nullptr) {
   const int LD = state_ld(dh);
   const int n = dh * LD;
   float m = 0.f;
@@ -89,6 +93,7 @@ __device__ inline void combine_state(const float* partial, const float* partial_
       acc.x += sc * p.x; acc.y += sc * p.y; acc.z += sc * p.z; acc.w += sc * p.w;
     }
     S[i] = acc;
+    if (sbuf) reinterpret_cast<float4*>(sbuf)[i] = acc;
     const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -97,13 +102,15 @@ __device__ inline void combine_state(const float* partial, const float* partial_
       if (pub_state && f <= dh) pub_state[((size_t)seqh * dh + e) * (dh + 1) + f] = v4[u];
     }
   }
+  // the combined state as later passes read it: the staged copy, else the global one
+  const float* Sr = sbuf ? sbuf : state + (size_t)seqh * n;
   if (fwd_center) {
     float* St = state + (size_t)seqh * n;
     __syncthreads();  // this CTA's state writes are visible to the whole CTA
     const float* c = fwd_center + (size_t)seqh * dh;
     for (int e = threadIdx.x; e < dh; e += blockDim.x) {
-      float acc = St[e * LD + dh];
-      for (int f = 0; f < dh; ++f) acc -= __bfloat162float(__float2bfloat16_rn(St[e * LD + f])) * c[f];
+      float acc = Sr[e * LD + dh];
+      for (int f = 0; f < dh; ++f) acc -= __bfloat162float(__float2bfloat16_rn(Sr[e * LD + f])) * __ldg(c + f);
       St[e * LD + dh] = acc;
       if (state_bf) state_bf[((size_t)seqh * dh + e) * state_bf_ld(dh) + dh] = __float2bfloat16_rn(acc);
     }
@@ -113,10 +120,10 @@ __device__ inline void combine_state(const float* partial, const float* partial_
     float* St = state + (size_t)seqh * n;
     __syncthreads();  // this CTA's state writes are visible to the whole CTA
     float Z = 0.f;
-    for (int e = 0; e < dh; ++e) Z += St[e * LD + dh];
+    for (int e = 0; e < dh; ++e) Z += Sr[e * LD + dh];
     for (int f = threadIdx.x; f < dh; f += blockDim.x) {
       float s = 0.f;
-      for (int e = 0; e < dh; ++e) s += St[e * LD + f];
+      for (int e = 0; e < dh; ++e) s += Sr[e * LD + f];
       const float c = Z > 0.f ? s / Z : 0.f;
       cbuf[f] = c;
       center[(size_t)seqh * dh + f] = c;
@@ -124,9 +131,9 @@ __device__ inline void combine_state(const float* partial, const float* partial_
     __syncthreads();
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
       const int e = i / LD, f = i % LD;
-      float v = St[i];
+      float v = Sr[i];
       if (f < dh) {
-        v -= St[e * LD + dh] * cbuf[f];
+        v -= Sr[e * LD + dh] * cbuf[f];
       }
       if (state_bf) state_bf[((size_t)seqh * dh + e) * state_bf_ld(dh) + f] = __float2bfloat16_rn(v);
       St[i] = v;  // the z column (f == dh), which other threads read, is left unchanged
