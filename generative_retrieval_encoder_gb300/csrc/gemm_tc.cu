@@ -10,17 +10,19 @@
 //                      K = 16, into one of two TMEM accumulators (2 x 256
 //                      columns), tcgen05.commit frees ring stages and hands a
 //                      finished accumulator to the epilogue;
-//   warps 2-5          epilogue: tcgen05.ld of their 32-lane quarter, release
-//                      the accumulator, convert and store (bf16 / fp32 / split
-//                      partial / projection + gate).
+//   warps 2-9          epilogue: tcgen05.ld of their 32-lane quarter and
+//                      column half, release the accumulator, convert and
+//                      store (bf16 / fp32 / split partial / projection + gate).
 // So the epilogue of tile i overlaps the MMAs of tile i + 1.  Operands may be
 // K-major ([rows][K]) or M/N-major ([K][rows], the weight-gradient GEMM
-// x~^T dP and the forward GEMM's packed weights).
+// x~^T dP and the forward GEMM's packed weights).  With two or more m-tiles
+// the CTAs run in clusters of two that share each B tile (multicast).
 //
 // Every mbarrier wait gives up after a bounded number of polls; the kernel then
 // sets bit 2 of the workspace error word, waits (bounded) for the copies and
 // MMAs it issued, frees its TMEM and returns.
 #include <cuda.h>
+#include <cstring>
 #include <cudaTypedefs.h>
 
 #include "kernels.h"
@@ -30,18 +32,25 @@
 namespace gbla {
 namespace {
 
-constexpr int PBM = 128, PBN = 256, PBK = 64, PST = 4;
+constexpr int PBM = 128, PBN = 256, PBK = 64;
 constexpr int A_TILE = PBM * PBK * 2;  // 16 KB
 constexpr int B_TILE = PBN * PBK * 2;  // 32 KB
-constexpr int SMEM_P = PST * (A_TILE + B_TILE) + 1024 + 256;
-constexpr int NTHREADS = 192;
+constexpr int EPW = 4;                    // epilogue warps, one per TMEM lane quarter
+constexpr int STG = 2048;                 // per epilogue warp and buffer: [32 rows][32 bf16], 64-byte swizzle
+constexpr int NSTG = 2;                   // buffers per epilogue warp
+constexpr int STG_ALL = EPW * NSTG * STG;
+constexpr int SMEM_P = 4 * (A_TILE + B_TILE) + STG_ALL + 1024 + 256;
+constexpr int NTHREADS = 64 + 32 * EPW;
+// Work units: (k split z, m-tile group, n-tile), a group being `cl` adjacent
+// m-tiles that the CTAs of one cluster take (rank r the m-tile cl g + r).
 struct TileSched {
-  int tiles_m, tiles_n, splits, total;
-  __device__ void decode(int t, int& z, int& mt, int& nt) const {
-    z = t / (tiles_m * tiles_n);
-    const int r = t - z * tiles_m * tiles_n;
-    mt = r / tiles_n;
-    nt = r - mt * tiles_n;
+  int tiles_m, tiles_n, splits, cl, groups_m, total;  // total = units
+  __device__ void decode(int t, int rank, int& z, int& mt, int& nt) const {
+    z = t / (groups_m * tiles_n);
+    const int r = t - z * groups_m * tiles_n;
+    const int g = r / tiles_n;
+    nt = r - g * tiles_n;
+    mt = g * cl + rank;
   }
 };
 
@@ -123,86 +132,140 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& a, int m, int n, int
   }
 }
 
-template <bool AMN, bool BMN>
+// Ring geometry per variant.  CL = 1: one CTA, 4 stages of A (16 KB) + B
+// (32 KB).  CL = 2: a CTA pair runs M = 256 MMAs (cta_group::2); each CTA
+// holds its 128 rows of A and half of B's columns, so a stage is 32 KB and 6
+// of them fit.
+template <int CL>
+struct Ring {
+  static constexpr int ST = CL == 2 ? 6 : 4;
+  static constexpr int B_ST = CL == 2 ? B_TILE / 2 : B_TILE;  // B bytes per stage and CTA
+  static constexpr int BYTES = ST * (A_TILE + B_ST);
+};
+static_assert(Ring<1>::BYTES == Ring<2>::BYTES, "one shared-memory layout for both variants");
+
+// CL = 2: the even CTA of each pair (rank 0) issues the MMAs; both CTAs' copies
+// complete on its full barriers (expect-tx armed by its producer for the
+// pair's bytes); its commits arrive, multicast, on both CTAs' empty and
+// accumulator-full barriers; both CTAs' epilogue warps release an accumulator
+// by remote arrivals on its accumulator-empty barrier.
+template <bool AMN, bool BMN, int CL>
 __global__ void __launch_bounds__(NTHREADS, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs a,
-              const TileSched ts) {
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmC, const GemmArgs a, const TileSched ts, int tma_store) {
+  using RG = Ring<CL>;
+  constexpr int ST = RG::ST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sA = smem_u32(smem), sB = sA + PST * A_TILE;
-  const uint32_t bars = sB + PST * B_TILE;
-  const uint32_t full = bars, empty = bars + 8 * PST, accf = bars + 16 * PST, acce = accf + 16, drain = acce + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + PST * (A_TILE + B_TILE) + 16 * PST + 40);
+  const uint32_t sA = smem_u32(smem), sB = sA + ST * A_TILE;
+  const uint32_t stg = sA + RG::BYTES;  // epilogue staging of bf16 output boxes
+  const uint32_t bars = stg + STG_ALL;
+  const uint32_t full = bars, empty = bars + 8 * ST, accf = bars + 16 * ST, acce = accf + 16, drain = acce + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + RG::BYTES + STG_ALL + 16 * ST + 40);
   __shared__ int s_fail;
-  __shared__ int s_issued[PST];  // last ring use issued per stage (+1), for the drain
+  __shared__ int s_issued[ST];  // last ring use issued per stage (+1), for the drain
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = CL == 2 ? (int)cluster_ctarank() : 0;
+  const bool leader = rank == 0;  // issues the MMAs
+  const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
+  constexpr uint16_t kPair = 3;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < PST; ++s) {
+    for (int s = 0; s < ST; ++s) {
       mbar_init(full + 8 * s, 1);
       mbar_init(empty + 8 * s, 1);
       s_issued[s] = 0;
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf + 8 * b, 1);
-      mbar_init(acce + 8 * b, 4);  // one arrival per epilogue warp
+      mbar_init(acce + 8 * b, EPW * CL);  // one arrival per epilogue warp of the pair
     }
     mbar_init(drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_fail = 0;
   }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(2 * PBN));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  if (warp == 1) {  // CL = 2: one warp of each CTA of the pair allocates, collectively
+    if (CL == 2) {
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(2 * PBN));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(2 * PBN));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (CL == 2) cluster_sync();  // the pair's barriers and TMEM exist before either CTA uses them
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   volatile int* fail = &s_fail;
+  // The barriers this CTA's copies complete on, and its accumulator releases go to.
+  const uint32_t full_dst = CL == 2 ? mapa_shared(full, 0) : full;
+  const uint32_t acce_dst = CL == 2 ? mapa_shared(acce, 0) : acce;
 
   if (warp == 0) {
     if (lane == 0) {  // ---------------------------------------------- producer
       uint32_t kt = 0;
-      for (int t = blockIdx.x; t < ts.total && !*fail; t += gridDim.x) {
+      for (int t = cid; t < ts.total && !*fail; t += ncl) {
         int z, mt, nt;
-        ts.decode(t, z, mt, nt);
+        ts.decode(t, rank, z, mt, nt);
         const int m0 = mt * PBM, n0 = nt * PBN;
+        const int ncols = min(PBN, a.N - n0);
+        const int mma_n = (ncols + 15) / 16 * 16;
+        // CL = 2: this CTA holds columns [n0 + rank nh, + nh) of the MMA's N
+        const int nh = mma_n / CL, nb0 = n0 + rank * nh;
+        const int nbox = BMN ? (CL == 2 ? (nh + 63) / 64 : PBN / 64) : 1;
+        const uint32_t bbytes = BMN ? (uint32_t)nbox * (B_TILE / 4) : (uint32_t)RG::B_ST;
         const int kbeg = z * a.k_split, kend = min(a.K, kbeg + a.k_split);
         for (int k0 = kbeg; k0 < kend; k0 += PBK, ++kt) {
-          const int s = kt % PST;
-          const uint32_t use = kt / PST;
+          const int s = kt % ST;
+          const uint32_t use = kt / ST;
           if (use > 0 && !mbar_wait(empty + 8 * s, (use - 1) & 1, fail)) break;
-          mbar_expect_tx(full + 8 * s, A_TILE + B_TILE);
+          if (leader) mbar_expect_tx(full + 8 * s, (uint32_t)CL * (A_TILE + bbytes));
           s_issued[s] = (int)use + 1;
-          const uint32_t da = sA + s * A_TILE, db = sB + s * B_TILE;
-          if (AMN) {
-            tma_load_2d(da, &tmA, full + 8 * s, m0, k0);
-            tma_load_2d(da + A_TILE / 2, &tmA, full + 8 * s, m0 + 64, k0);
+          const uint32_t da = sA + s * A_TILE, db = sB + s * RG::B_ST, fb = full_dst + 8 * s;
+          if (CL == 2) {
+            if (AMN) {
+              tma_load_2d_pair(da, &tmA, fb, m0, k0);
+              tma_load_2d_pair(da + A_TILE / 2, &tmA, fb, m0 + 64, k0);
+            } else {
+              tma_load_2d_pair(da, &tmA, fb, k0, m0);
+            }
+            if (BMN) {
+              for (int j = 0; j < nbox; ++j) tma_load_2d_pair(db + j * (B_TILE / 4), &tmB, fb, nb0 + 64 * j, k0);
+            } else {
+              tma_load_2d_pair(db, &tmB, fb, k0, nb0);
+            }
           } else {
-            tma_load_2d(da, &tmA, full + 8 * s, k0, m0);
-          }
-          if (BMN) {
+            if (AMN) {
+              tma_load_2d(da, &tmA, fb, m0, k0);
+              tma_load_2d(da + A_TILE / 2, &tmA, fb, m0 + 64, k0);
+            } else {
+              tma_load_2d(da, &tmA, fb, k0, m0);
+            }
+            if (BMN) {
 #pragma unroll
-            for (int j = 0; j < PBN / 64; ++j) tma_load_2d(db + j * (B_TILE / 4), &tmB, full + 8 * s, n0 + 64 * j, k0);
-          } else {
-            tma_load_2d(db, &tmB, full + 8 * s, k0, n0);
+              for (int j = 0; j < PBN / 64; ++j) tma_load_2d(db + j * (B_TILE / 4), &tmB, fb, n0 + 64 * j, k0);
+            } else {
+              tma_load_2d(db, &tmB, fb, k0, n0);
+            }
           }
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {  // ---------------------------------------------- MMA issuer
+    if (lane == 0 && leader) {  // ------------------------------------ MMA issuer
       uint32_t kt = 0;
       int i = 0;
-      for (int t = blockIdx.x; t < ts.total && !*fail; t += gridDim.x, ++i) {
+      for (int t = cid; t < ts.total && !*fail; t += ncl, ++i) {
         int z, mt, nt;
-        ts.decode(t, z, mt, nt);
+        ts.decode(t, rank, z, mt, nt);
         const int n0 = nt * PBN;
         const int ncols = min(PBN, a.N - n0);
         const int mma_n = (ncols + 15) / 16 * 16;
-        const uint32_t idesc = idesc_bf16(PBM, mma_n, AMN, BMN);
+        const uint32_t idesc = idesc_bf16(PBM * CL, mma_n, AMN, BMN);
         const int kbeg = z * a.k_split, kend = min(a.K, kbeg + a.k_split);
         const int b = i & 1;
         const uint32_t u = (uint32_t)i >> 1;
@@ -212,10 +275,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         bool first = true;
         bool ok = true;
         for (int k0 = kbeg; k0 < kend; k0 += PBK, ++kt) {
-          const int s = kt % PST;
-          if (!mbar_wait(full + 8 * s, (kt / PST) & 1, fail)) { ok = false; break; }
+          const int s = kt % ST;
+          if (!mbar_wait(full + 8 * s, (kt / ST) & 1, fail)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t ta = sA + s * A_TILE, tb = sB + s * B_TILE;
+          const uint32_t ta = sA + s * A_TILE, tb = sB + s * RG::B_ST;
 #pragma unroll
           for (int kk = 0; kk < PBK / 16; ++kk) {
             // K-major: advance 32 B inside the 128-byte swizzled row.  M/N-major:
@@ -223,25 +286,39 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // chunks of the tile are LBO = 8 KB apart.
             const uint64_t da = AMN ? sdesc(ta + kk * 2048, 8192, 1024) : sdesc(ta + kk * 32, 16, 1024);
             const uint64_t db = BMN ? sdesc(tb + kk * 2048, 8192, 1024) : sdesc(tb + kk * 32, 16, 1024);
-            tc_mma(d, da, db, idesc, first ? 0u : 1u);
+            if (CL == 2) tc_mma_pair(d, da, db, idesc, first ? 0u : 1u);
+            else tc_mma(d, da, db, idesc, first ? 0u : 1u);
             first = false;
           }
-          tc_commit(empty + 8 * s);
+          if (CL == 2) tc_commit_pair_mc(empty + 8 * s, kPair);
+          else tc_commit(empty + 8 * s);
         }
         if (!ok) break;
-        tc_commit(accf + 8 * b);
+        if (CL == 2) tc_commit_pair_mc(accf + 8 * b, kPair);
+        else tc_commit(accf + 8 * b);
       }
-      tc_commit(drain);  // completes once every MMA issued above has finished
+      if (CL == 2) tc_commit_pair(drain);  // completes once every MMA issued above has finished
+      else tc_commit(drain);
       for (uint32_t k = 0; k < kPollLimit && !mbar_try_wait(drain, 0); ++k) {
       }
     }
   } else {  // ------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
+    const int ew = warp - 2;
+    uint32_t sbuf = 0;       // staging buffers used so far by this warp
     int i = 0;
-    for (int t = blockIdx.x; t < ts.total && !*fail; t += gridDim.x, ++i) {
+    auto release = [&](int b) {  // hand accumulator b back to the MMA issuer
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (CL == 2) mbar_arrive_cluster(acce_dst + 8 * b);
+        else mbar_arrive(acce + 8 * b);
+      }
+    };
+    for (int t = cid; t < ts.total && !*fail; t += ncl, ++i) {
       int z, mt, nt;
-      ts.decode(t, z, mt, nt);
+      ts.decode(t, rank, z, mt, nt);
       const int m0 = mt * PBM, n0 = nt * PBN;
       const int ncols = min(PBN, a.N - n0);
       const int kbeg = z * a.k_split, kend = min(a.K, kbeg + a.k_split);
@@ -253,41 +330,65 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + b * PBN;
         for (int c = 0; c < ncols; c += 32) {
           uint32_t r[32];
-          tmem_ld32(taddr + c, r);  // warp-collective: every lane runs it
-          if (c + 32 >= ncols) {    // last chunk read: hand the accumulator back
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acce + 8 * b);
+          tmem_ld32(taddr + c, r);        // warp-collective: every lane runs it
+          if (c + 32 >= ncols) release(b);  // last chunk read
+          const int n = n0 + c;
+          const bool staged = tma_store && a.epi == EPI_BF16;  // uniform per warp
+          if (!staged) {
+            if (m < a.M) store_chunk(a, m, n, z, r);
+            continue;
           }
-          if (m < a.M) store_chunk(a, m, n0 + c, z, r);
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) w[j] = pack_bf16(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+          const uint32_t buf = stg + (uint32_t)((ew * NSTG + (sbuf % NSTG)) * STG);
+          ++sbuf;
+          if (lane == 0) bulk_wait_read<NSTG - 1>();  // the store that last used this buffer has read it
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)),
+                         "r"(w[4 * j]), "r"(w[4 * j + 1]), "r"(w[4 * j + 2]), "r"(w[4 * j + 3])
+                         : "memory");
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0 && m0 + 32 * q < a.M) {
+            tma_store_2d(&tmC, buf, n, m0 + 32 * q);
+            bulk_commit();
+          }
         }
       } else {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(acce + 8 * b);
+        release(b);
         if (m < a.M && a.epi == EPI_SPLITK)
           for (int j = 0; j < ncols; ++j) ((float*)a.C)[(size_t)z * a.M * a.ldc + (size_t)m * a.ldc + n0 + j] = 0.f;
       }
     }
+    if (lane == 0) bulk_wait_all();  // this warp's output stores have completed
   }
 
   __syncthreads();
   if (*fail) {
     if (threadIdx.x == 0) {
       if (a.err) atomicOr(a.err, kErrTimeout);
-      // wait (bounded) for the last copy issued into each ring stage
-      for (int s = 0; s < PST; ++s) {
-        const int u = s_issued[s];
-        if (u > 0)
-          for (uint32_t k = 0; k < kPollLimit && !mbar_try_wait(full + 8 * s, (uint32_t)(u - 1) & 1); ++k) {
-          }
-      }
+      // wait (bounded) for the last copy issued into each ring stage (all of
+      // the pair's copies complete on the leader's barriers)
+      if (leader)
+        for (int s = 0; s < ST; ++s) {
+          const int u = s_issued[s];
+          if (u > 0)
+            for (uint32_t k = 0; k < kPollLimit && !mbar_try_wait(full + 8 * s, (uint32_t)(u - 1) & 1); ++k) {
+            }
+        }
     }
     __syncthreads();
   }
   tc_fence_before();
-  __syncthreads();
-  if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * PBN));
+  if (CL == 2) cluster_sync();  // no copy, MMA or arrival of the pair still targets this CTA
+  else __syncthreads();
+  if (warp == 1) {
+    if (CL == 2) asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * PBN));
+    else asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * PBN));
+  }
 }
 
 }  // namespace
@@ -322,6 +423,18 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
          CUDA_SUCCESS;
 }
 
+bool make_store_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
   static int n = 0;
   if (n == 0) {
@@ -342,26 +455,54 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   if ((a.lda % 8) || (a.ldb % 8)) return cudaErrorNotSupported;
   if (a.epi == EPI_PROJ && a.n_main % 32) return cudaErrorNotSupported;
   if (a.epi == EPI_PROJ_PRE && (a.n_main != 4 * a.hd || a.hd % 32)) return cudaErrorNotSupported;
-  CUtensorMap ta, tb;
-  const bool okA = amn ? make_map(&ta, a.A, (uint64_t)a.M, (uint64_t)a.K, (uint64_t)a.lda, 64, PBK)
-                       : make_map(&ta, a.A, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.lda, PBK, PBM);
-  const bool okB = bmn ? make_map(&tb, a.B, (uint64_t)a.N, (uint64_t)a.K, (uint64_t)a.ldb, 64, PBK)
-                       : make_map(&tb, a.B, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.ldb, PBK, PBN);
-  if (!okA || !okB) return cudaErrorNotSupported;
   TileSched ts;
   ts.tiles_m = (a.M + PBM - 1) / PBM;
   ts.tiles_n = (a.N + PBN - 1) / PBN;
   ts.splits = (a.K + a.k_split - 1) / a.k_split;
-  ts.total = ts.tiles_m * ts.tiles_n * ts.splits;
-  const int grid = ts.total < sm_count() ? ts.total : sm_count();
+  ts.cl = ts.tiles_m >= 2 ? 2 : 1;  // pairs of m-tiles share the B tile
+  ts.groups_m = (ts.tiles_m + ts.cl - 1) / ts.cl;
+  ts.total = ts.groups_m * ts.tiles_n * ts.splits;
+  CUtensorMap ta, tb;
+  // B boxes: N-major 64 x 64 (four per tile); K-major 64 x 256, or 64 x 128 (one half) in pairs
+  const bool okA = amn ? make_map(&ta, a.A, (uint64_t)a.M, (uint64_t)a.K, (uint64_t)a.lda, 64, PBK)
+                       : make_map(&ta, a.A, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.lda, PBK, PBM);
+  const bool okB = bmn ? make_map(&tb, a.B, (uint64_t)a.N, (uint64_t)a.K, (uint64_t)a.ldb, 64, PBK)
+                       : make_map(&tb, a.B, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.ldb, PBK, PBN / ts.cl);
+  if (!okA || !okB) return cudaErrorNotSupported;
+  // bf16 outputs leave by bulk tensor stores (see the kernel)
+  CUtensorMap tc;
+  memset(&tc, 0, sizeof(tc));
+  int tma_store = 0;
+  if (a.epi == EPI_BF16 && (reinterpret_cast<uintptr_t>(a.C) & 15) == 0 && a.ldc % 8 == 0)
+    tma_store = make_store_map(&tc, a.C, (uint64_t)a.N, (uint64_t)a.M, (uint64_t)a.ldc) ? 1 : 0;
+  const int slots = sm_count() / ts.cl;  // clusters resident at once (one CTA per SM)
+  const int grid = ts.cl * (ts.total < slots ? ts.total : slots);
   cudaError_t e;
 #define GBLA_CASE(AMN, BMN)                                                                                  \
   if (amn == AMN && bmn == BMN) {                                                                            \
-    if ((e = cudaFuncSetAttribute(k_gemm_tc<AMN, BMN>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_P)) != \
-        cudaSuccess)                                                                                         \
+    if (ts.cl == 1) {                                                                                        \
+      if ((e = cudaFuncSetAttribute(k_gemm_tc<AMN, BMN, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
+                                    SMEM_P)) != cudaSuccess)                                                 \
+        return e;                                                                                            \
+      k_gemm_tc<AMN, BMN, 1><<<grid, NTHREADS, SMEM_P, st>>>(ta, tb, tc, a, ts, tma_store);                  \
+      return cudaGetLastError();                                                                             \
+    }                                                                                                        \
+    if ((e = cudaFuncSetAttribute(k_gemm_tc<AMN, BMN, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,       \
+                                  SMEM_P)) != cudaSuccess)                                                   \
       return e;                                                                                              \
-    k_gemm_tc<AMN, BMN><<<grid, NTHREADS, SMEM_P, st>>>(ta, tb, a, ts);                                      \
-    return cudaGetLastError();                                                                               \
+    cudaLaunchConfig_t cfg = {};                                                                             \
+    cfg.gridDim = dim3(grid);                                                                                \
+    cfg.blockDim = dim3(NTHREADS);                                                                           \
+    cfg.dynamicSmemBytes = SMEM_P;                                                                           \
+    cfg.stream = st;                                                                                         \
+    cudaLaunchAttribute attr[1];                                                                             \
+    attr[0].id = cudaLaunchAttributeClusterDimension;                                                        \
+    attr[0].val.clusterDim.x = 2;                                                                            \
+    attr[0].val.clusterDim.y = 1;                                                                            \
+    attr[0].val.clusterDim.z = 1;                                                                            \
+    cfg.attrs = attr;                                                                                        \
+    cfg.numAttrs = 1;                                                                                        \
+    return cudaLaunchKernelEx(&cfg, k_gemm_tc<AMN, BMN, 2>, ta, tb, tc, a, ts, tma_store);                   \
   }
   GBLA_CASE(false, false) GBLA_CASE(true, true) GBLA_CASE(false, true) GBLA_CASE(true, false)
 #undef GBLA_CASE
