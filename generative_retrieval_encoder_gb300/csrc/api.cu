@@ -474,12 +474,14 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   g1.C = at<char>(ws, l.dxt); g1.ldc = p.d;  // dx~ in the io dtype
   g1.M = p.T; g1.N = p.d; g1.K = p.NP; g1.k_split = p.NP; g1.epi = p.f32 ? EPI_F32 : EPI_BF16; g1.io_f32 = p.f32;
   g1.err = c.err;
+  g1.pair = 1;  // long K: the operand feed limits, CTA pairs halve it per SM
   GBLA_CHECK(launch_gemm(g1, c.st), "dx~ gemm");
   GemmArgs g2{};
   g2.A = xt; g2.lda = p.d; g2.a_kmajor = 0;
   g2.B = dP; g2.ldb = p.NP; g2.b_kmajor = 0;
   g2.C = at<float>(ws, l.dW); g2.ldc = p.NP;
   g2.M = p.d; g2.N = p.NP; g2.K = p.T; g2.k_split = p.wsplit; g2.epi = EPI_SPLITK; g2.io_f32 = p.f32; g2.err = c.err;
+  g2.pair = 1;  // long K: the operand feed limits, CTA pairs halve it per SM
   GBLA_CHECK(launch_gemm(g2, c.st), "dW gemm");
   float* outs[5] = {dW_q, dW_k, dW_v, dW_r, dw_g};
   GBLA_CHECK(launch_scatter_dw(at<float>(ws, l.dW), p.n_wsplit, p.d, p.NP, p.H, p.dh, outs, c.st), "dW sum");

@@ -6,23 +6,27 @@
 //   warp 0 (one lane)  TMA producer: cp.async.bulk.tensor loads (128-byte
 //                      swizzle) into a 4-stage shared-memory ring (full/empty
 //                      mbarriers);
-//   warp 1 (one lane)  MMA issuer: tcgen05.mma cta_group::1 M = 128, N <= 256,
-//                      K = 16, into one of two TMEM accumulators (2 x 256
-//                      columns), tcgen05.commit frees ring stages and hands a
-//                      finished accumulator to the epilogue;
+//   warp 1 (one lane)  MMA issuer: tcgen05.mma M = 128 (one CTA) or 256 (a
+//                      CTA pair, cta_group::2), N <= 256, K = 16, into one of
+//                      two TMEM accumulators (2 x 256 columns),
+//                      tcgen05.commit frees ring stages and hands a finished
+//                      accumulator to the epilogue;
 //   warps 2-9          epilogue: tcgen05.ld of their 32-lane quarter and
 //                      column half, release the accumulator, convert and
 //                      store (bf16 / fp32 / split partial / projection + gate).
+//                      bf16 columns go 64 at a time through a per-warp staging
+//                      block, so that each warp store writes four whole
+//                      128-byte row segments instead of 32 scattered 16-byte
+//                      pieces.
 // So the epilogue of tile i overlaps the MMAs of tile i + 1.  Operands may be
 // K-major ([rows][K]) or M/N-major ([K][rows], the weight-gradient GEMM
 // x~^T dP and the forward GEMM's packed weights).  With two or more m-tiles
-// the CTAs run in clusters of two that share each B tile (multicast).
+// the CTAs run as pairs (clusters of two).
 //
 // Every mbarrier wait gives up after a bounded number of polls; the kernel then
 // sets bit 2 of the workspace error word, waits (bounded) for the copies and
 // MMAs it issued, frees its TMEM and returns.
 #include <cuda.h>
-#include <cstring>
 #include <cudaTypedefs.h>
 
 #include "kernels.h"
@@ -35,10 +39,9 @@ namespace {
 constexpr int PBM = 128, PBN = 256, PBK = 64;
 constexpr int A_TILE = PBM * PBK * 2;  // 16 KB
 constexpr int B_TILE = PBN * PBK * 2;  // 32 KB
-constexpr int EPW = 4;                    // epilogue warps, one per TMEM lane quarter
-constexpr int STG = 2048;                 // per epilogue warp and buffer: [32 rows][32 bf16], 64-byte swizzle
-constexpr int NSTG = 2;                   // buffers per epilogue warp
-constexpr int STG_ALL = EPW * NSTG * STG;
+constexpr int EPW = 8;                    // epilogue warps: two per TMEM lane quarter, one column half each
+constexpr int STG = 4096;                 // per epilogue warp: [32 rows][64 bf16], 16-byte chunks XOR-swizzled
+constexpr int STG_ALL = EPW * STG;
 constexpr int SMEM_P = 4 * (A_TILE + B_TILE) + STG_ALL + 1024 + 256;
 constexpr int NTHREADS = 64 + 32 * EPW;
 // Work units: (k split z, m-tile group, n-tile), a group being `cl` adjacent
@@ -152,7 +155,7 @@ static_assert(Ring<1>::BYTES == Ring<2>::BYTES, "one shared-memory layout for bo
 template <bool AMN, bool BMN, int CL>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              const __grid_constant__ CUtensorMap tmC, const GemmArgs a, const TileSched ts, int tma_store) {
+              const GemmArgs a, const TileSched ts, int wide_ok) {
   using RG = Ring<CL>;
   constexpr int ST = RG::ST;
   extern __shared__ uint8_t smem_raw[];
@@ -305,8 +308,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else {  // ------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
-    const int ew = warp - 2;
-    uint32_t sbuf = 0;       // staging buffers used so far by this warp
+    const int ew = warp - 2, c_lo = (ew >> 2) * (PBN / 2), c_hi = c_lo + PBN / 2;  // this warp's columns
     int i = 0;
     auto release = [&](int b) {  // hand accumulator b back to the MMA issuer
       tc_fence_before();
@@ -328,42 +330,68 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int m = m0 + row;
       if (kend > kbeg) {
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + b * PBN;
-        for (int c = 0; c < ncols; c += 32) {
-          uint32_t r[32];
-          tmem_ld32(taddr + c, r);        // warp-collective: every lane runs it
-          if (c + 32 >= ncols) release(b);  // last chunk read
+        const int cend = min(ncols, c_hi);
+        if (c_lo >= cend) release(b);  // nothing in this warp's half
+        for (int c = c_lo; c < cend;) {
           const int n = n0 + c;
-          const bool staged = tma_store && a.epi == EPI_BF16;  // uniform per warp
-          if (!staged) {
+          // 64 bf16 columns at once through the staging rows, unless they reach
+          // past the bf16 columns (uniform per warp)
+          const bool wide = wide_ok && c + 64 <= cend && ((a.epi == EPI_BF16 && n + 64 <= a.N) ||
+                                               ((a.epi == EPI_PROJ || a.epi == EPI_PROJ_PRE) && n + 64 <= a.n_main));
+          if (!wide) {
+            uint32_t r[32];
+            tmem_ld32(taddr + c, r);       // warp-collective: every lane runs it
+            if (c + 32 >= cend) release(b);  // last chunk read
             if (m < a.M) store_chunk(a, m, n, z, r);
+            c += 32;
             continue;
           }
-          uint32_t w[16];
+          uint32_t w[32];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) w[j] = pack_bf16(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-          const uint32_t buf = stg + (uint32_t)((ew * NSTG + (sbuf % NSTG)) * STG);
-          ++sbuf;
-          if (lane == 0) bulk_wait_read<NSTG - 1>();  // the store that last used this buffer has read it
-          __syncwarp();
+          for (int h = 0; h < 2; ++h) {
+            uint32_t r[32];
+            tmem_ld32(taddr + c + 32 * h, r);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)),
+            for (int j = 0; j < 16; ++j) {
+              float x0 = __uint_as_float(r[2 * j]), x1 = __uint_as_float(r[2 * j + 1]);
+              if (a.epi == EPI_PROJ_PRE && n + 32 * h + 2 * j < 2 * a.hd) {  // phi = elu + 1 on q and k
+                x0 = fmaxf(x0, 0.f) + __expf(fminf(x0, 0.f));
+                x1 = fmaxf(x1, 0.f) + __expf(fminf(x1, 0.f));
+              }
+              w[16 * h + j] = pack_bf16(x0, x1);
+            }
+          }
+          if (c + 64 >= cend) release(b);
+          // this lane's row into the staging rows (chunk j of row r at chunk j ^ (r & 7))
+          const uint32_t sw = stg + (uint32_t)(ew * STG);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sw + lane * 128 + ((j ^ (lane & 7)) << 4)),
                          "r"(w[4 * j]), "r"(w[4 * j + 1]), "r"(w[4 * j + 2]), "r"(w[4 * j + 3])
                          : "memory");
-          fence_async_smem();
           __syncwarp();
-          if (lane == 0 && m0 + 32 * q < a.M) {
-            tma_store_2d(&tmC, buf, n, m0 + 32 * q);
-            bulk_commit();
+          // eight lanes per row: each warp store writes four whole 128-byte row segments
+          bf16* Cb = (bf16*)a.C;
+          const int ch = lane & 7;
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int rr = 4 * it + (lane >> 3), gm = m0 + 32 * q + rr;
+            uint4 v;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "r"(sw + rr * 128 + ((ch ^ (rr & 7)) << 4)));
+            if (gm < a.M) *reinterpret_cast<uint4*>(Cb + (size_t)gm * a.ldc + n + 8 * ch) = v;
           }
+          __syncwarp();
+          c += 64;
         }
       } else {
         release(b);
         if (m < a.M && a.epi == EPI_SPLITK)
-          for (int j = 0; j < ncols; ++j) ((float*)a.C)[(size_t)z * a.M * a.ldc + (size_t)m * a.ldc + n0 + j] = 0.f;
+          for (int j = c_lo; j < min(ncols, c_hi); ++j)
+            ((float*)a.C)[(size_t)z * a.M * a.ldc + (size_t)m * a.ldc + n0 + j] = 0.f;
       }
     }
-    if (lane == 0) bulk_wait_all();  // this warp's output stores have completed
   }
 
   __syncthreads();
@@ -423,18 +451,6 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
          CUDA_SUCCESS;
 }
 
-bool make_store_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld) {
-  auto enc = encoder();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {ld * 2};
-  cuuint32_t box[2] = {32, 32};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int sm_count() {
   static int n = 0;
   if (n == 0) {
@@ -459,7 +475,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   ts.tiles_m = (a.M + PBM - 1) / PBM;
   ts.tiles_n = (a.N + PBN - 1) / PBN;
   ts.splits = (a.K + a.k_split - 1) / a.k_split;
-  ts.cl = ts.tiles_m >= 2 ? 2 : 1;  // pairs of m-tiles share the B tile
+  ts.cl = a.pair && ts.tiles_m >= 2 ? 2 : 1;  // CTA pairs on adjacent m-tiles
   ts.groups_m = (ts.tiles_m + ts.cl - 1) / ts.cl;
   ts.total = ts.groups_m * ts.tiles_n * ts.splits;
   CUtensorMap ta, tb;
@@ -469,12 +485,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   const bool okB = bmn ? make_map(&tb, a.B, (uint64_t)a.N, (uint64_t)a.K, (uint64_t)a.ldb, 64, PBK)
                        : make_map(&tb, a.B, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.ldb, PBK, PBN / ts.cl);
   if (!okA || !okB) return cudaErrorNotSupported;
-  // bf16 outputs leave by bulk tensor stores (see the kernel)
-  CUtensorMap tc;
-  memset(&tc, 0, sizeof(tc));
-  int tma_store = 0;
-  if (a.epi == EPI_BF16 && (reinterpret_cast<uintptr_t>(a.C) & 15) == 0 && a.ldc % 8 == 0)
-    tma_store = make_store_map(&tc, a.C, (uint64_t)a.N, (uint64_t)a.M, (uint64_t)a.ldc) ? 1 : 0;
+  // 16-byte row stores of the staged bf16 output (see the epilogue)
+  const int wide_ok = (reinterpret_cast<uintptr_t>(a.C) & 15) == 0 && a.ldc % 8 == 0 ? 1 : 0;
   const int slots = sm_count() / ts.cl;  // clusters resident at once (one CTA per SM)
   const int grid = ts.cl * (ts.total < slots ? ts.total : slots);
   cudaError_t e;
@@ -484,7 +496,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
       if ((e = cudaFuncSetAttribute(k_gemm_tc<AMN, BMN, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
                                     SMEM_P)) != cudaSuccess)                                                 \
         return e;                                                                                            \
-      k_gemm_tc<AMN, BMN, 1><<<grid, NTHREADS, SMEM_P, st>>>(ta, tb, tc, a, ts, tma_store);                  \
+      k_gemm_tc<AMN, BMN, 1><<<grid, NTHREADS, SMEM_P, st>>>(ta, tb, a, ts, wide_ok);                  \
       return cudaGetLastError();                                                                             \
     }                                                                                                        \
     if ((e = cudaFuncSetAttribute(k_gemm_tc<AMN, BMN, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,       \
@@ -502,7 +514,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;                                                                            \
     cfg.attrs = attr;                                                                                        \
     cfg.numAttrs = 1;                                                                                        \
-    return cudaLaunchKernelEx(&cfg, k_gemm_tc<AMN, BMN, 2>, ta, tb, tc, a, ts, tma_store);                   \
+    return cudaLaunchKernelEx(&cfg, k_gemm_tc<AMN, BMN, 2>, ta, tb, a, ts, wide_ok);                        \
   }
   GBLA_CASE(false, false) GBLA_CASE(true, true) GBLA_CASE(false, true) GBLA_CASE(true, false)
 #undef GBLA_CASE

@@ -120,6 +120,7 @@ struct GemmArgs {
   int io_f32;
   int* err;           // workspace error word (bounded device waits that give up set bit 2)
   int hd, dh;         // EPI_PROJ_PRE: H*dh and dh (column -> head)
+  int pair;           // tcgen05 GEMM: run CTA pairs (M = 256 MMAs) when there are >= 2 m-tiles
 };
 
 struct ConvArgs {

@@ -35,21 +35,7 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* 
       ::"r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y), "h"(mask)
       : "memory");
 }
-// Bulk tensor store of a shared-memory box to global (out-of-range rows and
-// columns of the box are not written), and its bulk-group bookkeeping.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
-               ::"l"(map), "r"(src), "r"(x), "r"(y)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// All but the newest N bulk groups of this thread have read their shared source.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-// All bulk groups of this thread have completed.
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // 2-SM (CTA pair) forms.  The load completes on an mbarrier that may be the
 // peer CTA's (address from mapa_shared).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
@@ -197,8 +183,6 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
 // entry point or the encoding fails.
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner,
               uint32_t box_outer, bool wide_promotion = true);
-// Host: the same for a bf16 store box of 32 x 32 with the 64-byte swizzle
-// (rows of 64 bytes; conflict-free staging writes of one row per lane).
-bool make_store_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld);
+
 
 }  // namespace gbla
