@@ -278,6 +278,14 @@ gbla_status begin(const gbla_shape* s, int op, void* ws, size_t ws_bytes, void* 
 
 // State reduction + combine.  The bf16 path centres the state on the
 // k~-weighted mean of v (center); the fp32 path keeps it uncentred.
+// The layer's bf16 readout: the tcgen05 kernel where it applies.
+cudaError_t launch_readout_layer_bf16(const ReadoutArgs& ra, int n_tiles, cudaStream_t st) {
+  const cudaError_t e = launch_readout_tc(ra, n_tiles, st);
+  if (e != cudaErrorNotSupported) return e;
+  (void)cudaGetLastError();
+  return launch_readout_bf16(ra, true, n_tiles, st);
+}
+
 // The layer's bf16 query-side backward: the tcgen05 kernel where it applies.
 cudaError_t launch_bwd_q_layer_bf16(const BwdQArgs& q, int hd, int grid_x, cudaStream_t st) {
   const cudaError_t e = launch_bwd_q_tc(q, hd, grid_x, st);
@@ -393,8 +401,8 @@ gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* con
   ra.state = state; ra.state_bf = state_bf; ra.center = center; ra.pre = c.pre;
   ra.out = y; ra.ldo = p.HD; ra.den = nullptr;
   ra.rsinv = (saved && !p.f32) ? at<float>(saved, saved_layout(p).rsinv) : nullptr;
-  ra.H = p.H; ra.dh = p.dh; ra.seq = c.seq; ra.tiles = c.tiles; ra.err = c.kerr;
-  GBLA_CHECK(p.f32 ? launch_readout_f32(ra, true, p.n_tiles, c.st) : launch_readout_bf16(ra, true, p.n_tiles, c.st),
+  ra.H = p.H; ra.dh = p.dh; ra.seq = c.seq; ra.tiles = c.tiles; ra.err = c.kerr; ra.err_out = c.err;
+  GBLA_CHECK(p.f32 ? launch_readout_f32(ra, true, p.n_tiles, c.st) : launch_readout_layer_bf16(ra, p.n_tiles, c.st),
              "readout");
   return GBLA_OK;
 }

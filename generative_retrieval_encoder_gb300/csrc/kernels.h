@@ -59,6 +59,7 @@ struct ReadoutArgs {
   int H, dh;
   SeqDesc seq; Tiling tiles;
   const int* err;
+  int* err_out;                     // tcgen05 kernel: timeout bit of the workspace error word
 };
 
 struct BwdQArgs {
@@ -145,6 +146,9 @@ cudaError_t launch_bwd_q_bf16(const BwdQArgs& a, bool norm, int grid_x, cudaStre
 // tcgen05 query-side backward (bwd_q_tc.cu): d_h = 64, the layer's RMSNorm
 // epilogue, phi(q) stored (pre); cudaErrorNotSupported otherwise.
 cudaError_t launch_bwd_q_tc(const BwdQArgs& a, int hd, int grid_x, cudaStream_t st);
+// tcgen05 readout with the RmsNorm gate (readout_tc.cu): d_h = 64, phi(q)
+// stored (pre), no den output; cudaErrorNotSupported otherwise.
+cudaError_t launch_readout_tc(const ReadoutArgs& a, int n_tiles, cudaStream_t st);
 cudaError_t launch_bwd_kv_bf16(const BwdKVArgs& a, int grid_x, cudaStream_t st);
 
 cudaError_t launch_reduce_f32(const ReduceArgs& a, int grid_x, cudaStream_t st);
