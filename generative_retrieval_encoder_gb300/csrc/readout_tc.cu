@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(NTH, 1)
         if (j % NG != grp) continue;  // another group's tile
         const int s = j % RST;
         const uint8_t* sq = smem + O_ST + s * STAGE;
-        const uint8_t* sr = sq + TILE;
+        uint8_t* sr = smem + O_ST + s * STAGE + TILE;
         const int rel = t * RT + i;
         const bool valid = rel < x.nval, store = rel < x.nrows;
         mbar_wait(ACCF(grp), (j / NG) & 1, fail);
@@ -263,7 +263,6 @@ __global__ void __launch_bounds__(NTH, 1)
           }
         }
         const float rs = rsqrtf(ss * (1.f / RD) + a.eps);
-        bf16* orow = out + (x.rb + rel) * a.ldo + (size_t)x.h * RD;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t o[32];
@@ -288,7 +287,19 @@ __global__ void __launch_bounds__(NTH, 1)
               const float y1 = v1 * rs * gam[F + 1] * (r1 * __fdividef(1.f, 1.f + __expf(-r1)));
               w[jj / 2] = pack_bf16(y0, y1);
             }
-            if (store) *reinterpret_cast<uint4*>(orow + 32 * hh + 8 * c) = make_uint4(w[0], w[1], w[2], w[3]);
+            // y over the r chunk just read (this lane's own row)
+            *reinterpret_cast<uint4*>(sr + swz_off(i, 4 * hh + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        // the warp's 32 rows of y leave as whole 128-byte rows: eight lanes per row
+        __syncwarp();
+        {
+          const int ch = lane & 7;
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int rr = wq * 32 + 4 * it + (lane >> 3), rl = t * RT + rr;
+            const uint4 v = *reinterpret_cast<const uint4*>(sr + swz_off(rr, ch));
+            if (rl < x.nrows) *reinterpret_cast<uint4*>(out + (x.rb + rl) * a.ldo + (size_t)x.h * RD + 8 * ch) = v;
           }
         }
         if (a.rsinv && store)
