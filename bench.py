@@ -34,9 +34,19 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch from ncu captures (dram__bytes_read.sum + dram__bytes_write.sum),
 # keyed by launch name: (bytes, workload name, sha1 of the kernel's source file when captured).
 # A source change since the capture makes the figure stale: it is then reported as null.
-NCU_TRAFFIC: dict = {}
+NCU_TRAFFIC: dict = {
+    "projection gemm": (279593728, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "96c7b224044a"),
+    "dx~ gemm": (328316928, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "96c7b224044a"),
+    "dW gemm": (347562240, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "96c7b224044a"),
+    "bwd_q": (324847360, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "0048d2a17f25"),
+    "readout": (174518528, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "9b2d77f3061f"),
+    "reduce": (144712192, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "9c0148e6206c"),
+    "bwd_kv": (238153984, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "9c0148e6206c"),
+    "conv": (84326656, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "78057339890f"),
+    "conv bwd": (167203328, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "78057339890f"),
+}
 KERNEL_SOURCE = {"projection gemm": "gemm_tc.cu", "dx~ gemm": "gemm_tc.cu", "dW gemm": "gemm_tc.cu",
-                 "reduce": "core_bf16.cu", "readout": "core_bf16.cu", "bwd_q": "bwd_q_tc.cu",
+                 "reduce": "core_bf16.cu", "readout": "readout_tc.cu", "bwd_q": "bwd_q_tc.cu",
                  "bwd_kv": "core_bf16.cu", "conv": "conv.cu", "conv bwd": "conv.cu",
                  "dW sum": "layer_misc.cu"}
 
