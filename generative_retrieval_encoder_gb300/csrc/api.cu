@@ -174,7 +174,7 @@ Layout ws_layout(const Plan& p, int op) {
     l.dstate = c.take(state_bytes(p));
     l.dstate_bf = c.take(state_bf_bytes(p));
     l.gamma_part = c.take((size_t)p.n_chunks * p.H * p.dh * 4);
-    l.bg_part = c.take((size_t)p.n_tiles * p.H * 4);
+    l.bg_part = c.take((size_t)p.n_tiles * 2 * p.H * 4);  // up to two partial rows per tile
     l.conv_part = c.take((size_t)p.conv_blocks * p.d * 5 * 4);
   } else {  // core forward / backward
     l.state = c.take(state_bytes(p));
@@ -284,6 +284,16 @@ cudaError_t launch_readout_layer_bf16(const ReadoutArgs& ra, int n_tiles, cudaSt
   if (e != cudaErrorNotSupported) return e;
   (void)cudaGetLastError();
   return launch_readout_bf16(ra, true, n_tiles, st);
+}
+
+// The layer's bf16 key-side backward: the tcgen05 kernel where it applies;
+// *bg_rows = the rows of db_g partials written.
+cudaError_t launch_bwd_kv_layer_bf16(const BwdKVArgs& kv, int n_tiles, int* bg_rows, cudaStream_t st) {
+  const cudaError_t e = launch_bwd_kv_tc(kv, n_tiles, bg_rows, st);
+  if (e != cudaErrorNotSupported) return e;
+  (void)cudaGetLastError();
+  *bg_rows = n_tiles;
+  return launch_bwd_kv_bf16(kv, n_tiles, st);
 }
 
 // The layer's bf16 query-side backward: the tcgen05 kernel where it applies.
@@ -471,16 +481,20 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   kv.ds = dP; kv.ldds = p.NP; kv.gate_grad = sig ? GG_SIGMOID : GG_SOFTMAX;
   // ds of head h lands in column 4*H*dh + h: offset the pointer, keep the stride
   kv.ds = dP + (size_t)4 * p.HD * es;
-  kv.zero_cols_from = p.N1 - 4 * p.HD; kv.zero_cols_to = p.NP - 4 * p.HD;
+  kv.zero_cols_from = kv.zero_cols_to = 0;  // the pad columns of dP are never read
   kv.bg_part = at<float>(ws, l.bg_part);
-  kv.H = p.H; kv.dh = p.dh; kv.seq = c.seq; kv.tiles = c.tiles; kv.err = c.kerr;
-  GBLA_CHECK(p.f32 ? launch_bwd_kv_f32(kv, p.n_tiles, c.st) : launch_bwd_kv_bf16(kv, p.n_tiles, c.st), "bwd_kv");
+  kv.H = p.H; kv.dh = p.dh; kv.seq = c.seq; kv.tiles = c.tiles; kv.err = c.kerr; kv.err_out = c.err;
+  int bg_rows = p.n_tiles;
+  GBLA_CHECK(p.f32 ? launch_bwd_kv_f32(kv, p.n_tiles, c.st) : launch_bwd_kv_layer_bf16(kv, p.n_tiles, &bg_rows, c.st),
+             "bwd_kv");
   // Eq. 4 projections backward: dx~ = dP W_all^T, dW_all = x~^T dP
   GemmArgs g1{};
   g1.A = dP; g1.lda = p.NP; g1.a_kmajor = 1;
   g1.B = at<char>(ws, l.Wp); g1.ldb = p.NP; g1.b_kmajor = 1;
   g1.C = at<char>(ws, l.dxt); g1.ldc = p.d;  // dx~ in the io dtype
-  g1.M = p.T; g1.N = p.d; g1.K = p.NP; g1.k_split = p.NP; g1.epi = p.f32 ? EPI_F32 : EPI_BF16; g1.io_f32 = p.f32;
+  // K = N1, not the padded NP: the pad columns of dP and W_all are never read (the
+  // tensor-core GEMM's loads zero-fill past N1), so nothing needs to clear them
+  g1.M = p.T; g1.N = p.d; g1.K = p.N1; g1.k_split = p.N1; g1.epi = p.f32 ? EPI_F32 : EPI_BF16; g1.io_f32 = p.f32;
   g1.err = c.err;
   g1.pair = 1;  // long K: the operand feed limits, CTA pairs halve it per SM
   GBLA_CHECK(launch_gemm(g1, c.st), "dx~ gemm");
@@ -488,7 +502,7 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   g2.A = xt; g2.lda = p.d; g2.a_kmajor = 0;
   g2.B = dP; g2.ldb = p.NP; g2.b_kmajor = 0;
   g2.C = at<float>(ws, l.dW); g2.ldc = p.NP;
-  g2.M = p.d; g2.N = p.NP; g2.K = p.T; g2.k_split = p.wsplit; g2.epi = EPI_SPLITK; g2.io_f32 = p.f32; g2.err = c.err;
+  g2.M = p.d; g2.N = p.N1; g2.K = p.T; g2.k_split = p.wsplit; g2.epi = EPI_SPLITK; g2.io_f32 = p.f32; g2.err = c.err;
   g2.pair = 1;  // long K: the operand feed limits, CTA pairs halve it per SM
   GBLA_CHECK(launch_gemm(g2, c.st), "dW gemm");
   float* outs[5] = {dW_q, dW_k, dW_v, dW_r, dw_g};
@@ -504,7 +518,7 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   if (drms_w)
     GBLA_CHECK(launch_sum_parts(q.gamma_part, p.n_chunks * p.H, p.dh, p.dh, drms_w, c.st), "dgamma");
   if (db_g)
-    GBLA_CHECK(launch_sum_parts(kv.bg_part, p.n_tiles, p.H, p.H, db_g, c.st), "db_g");
+    GBLA_CHECK(launch_sum_parts(kv.bg_part, bg_rows, p.H, p.H, db_g, c.st), "db_g");
   return GBLA_OK;
 }
 

@@ -93,11 +93,12 @@ struct BwdKVArgs {
   void* dk; int64_t lddk;
   void* dv; int64_t lddv;
   void* ds; int64_t ldds; int gate_grad;       // GateGrad
-  float* bg_part;                              // [gridDim.x * H] or null
+  float* bg_part;                              // [gridDim.x * H] (tcgen05: [tiles * tile/128 * H]) or null
   int zero_cols_from, zero_cols_to;            // dP pad columns to clear (head 0 CTAs)
   int H, dh;
   SeqDesc seq; Tiling tiles;
   const int* err;
+  int* err_out;                                // tcgen05 kernel: timeout bit of the workspace error word
 };
 
 // C[M, N] (+)= sum_k A(m, k) B(n, k).  A is [M][K] (a_kmajor) or [K][M];
@@ -149,6 +150,9 @@ cudaError_t launch_bwd_q_tc(const BwdQArgs& a, int hd, int grid_x, cudaStream_t 
 // tcgen05 readout with the RmsNorm gate (readout_tc.cu): d_h = 64, phi(q)
 // stored (pre), no den output; cudaErrorNotSupported otherwise.
 cudaError_t launch_readout_tc(const ReadoutArgs& a, int n_tiles, cudaStream_t st);
+// tcgen05 key-side backward (bwd_kv_tc.cu): d_h = 64, phi(k) stored, sigmoid
+// gate; db_g partials in *nparts rows of bg_part.  cudaErrorNotSupported otherwise.
+cudaError_t launch_bwd_kv_tc(const BwdKVArgs& a, int n_tiles, int* nparts, cudaStream_t st);
 cudaError_t launch_bwd_kv_bf16(const BwdKVArgs& a, int grid_x, cudaStream_t st);
 
 cudaError_t launch_reduce_f32(const ReduceArgs& a, int grid_x, cudaStream_t st);
