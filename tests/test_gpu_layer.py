@@ -36,6 +36,9 @@ CASES = [
     W("bf16 padded", 3, 130, 64, 2, 32, seq_lens=[130, 1, 64], seed=17),
     W("bf16 varlen", 1, 0, 128, 2, 64, extra={"lengths": [1, 17, 250, 64, 3, 700]}, seed=18),
     W("bf16 varlen dh128 softmax", 1, 0, 128, 2, 128, gate="softmax", extra={"lengths": [40, 0, 513]}, seed=19),
+    # the d_h = 64 tensor-core kernels on padded slots and on empty sequences
+    W("bf16 padded dh64", 3, 300, 128, 4, 64, seq_lens=[300, 1, 129], seed=20),
+    W("bf16 varlen dh64 empty", 1, 0, 64, 2, 64, extra={"lengths": [0, 5, 129, 0, 256, 1]}, seed=21),
 ]
 
 GRADS = ("dconv_w", "dconv_b", "dW_q", "dW_k", "dW_v", "dW_r", "dw_g", "db_g", "drms_w")
