@@ -57,6 +57,15 @@ struct TileSched {
   }
 };
 
+// phi(x) = elu(x) + 1 = max(x, 0) + exp(min(x, 0)), the exponential as
+// 2^(x log2 e) on the hardware ex2 approximation (relative error ~2^-22,
+// far below the bf16 rounding of the stored value).
+__device__ __forceinline__ float phi_elu1(float x) {
+  float e;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(fminf(x, 0.f) * 1.4426950408889634f));
+  return fmaxf(x, 0.f) + e;
+}
+
 // One 32-column chunk of a finished accumulator row to global memory.
 __device__ __forceinline__ void store_chunk(const GemmArgs& a, int m, int n, int z, const uint32_t (&r)[32]) {
   const int Hg = a.N - a.n_main;
@@ -71,8 +80,7 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& a, int m, int n, int
         float f[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float x = __uint_as_float(r[8 * q + j]);
-          f[j] = fmaxf(x, 0.f) + __expf(fminf(x, 0.f));
+          f[j] = phi_elu1(__uint_as_float(r[8 * q + j]));
         }
         uint4 u;
         u.x = pack_bf16(f[0], f[1]); u.y = pack_bf16(f[2], f[3]);
@@ -346,19 +354,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             c += 32;
             continue;
           }
+          // phi on the q and k blocks: n is a multiple of 64 and so is 2 hd
+          // (hd a multiple of 32), so the 64 columns lie on one side
+          const bool phi = a.epi == EPI_PROJ_PRE && n < 2 * a.hd;
           uint32_t w[32];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t r[32];
             tmem_ld32(taddr + c + 32 * h, r);
+            if (phi) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              float x0 = __uint_as_float(r[2 * j]), x1 = __uint_as_float(r[2 * j + 1]);
-              if (a.epi == EPI_PROJ_PRE && n + 32 * h + 2 * j < 2 * a.hd) {  // phi = elu + 1 on q and k
-                x0 = fmaxf(x0, 0.f) + __expf(fminf(x0, 0.f));
-                x1 = fmaxf(x1, 0.f) + __expf(fminf(x1, 0.f));
-              }
-              w[16 * h + j] = pack_bf16(x0, x1);
+              for (int j = 0; j < 16; ++j)
+                w[16 * h + j] = pack_bf16(phi_elu1(__uint_as_float(r[2 * j])), phi_elu1(__uint_as_float(r[2 * j + 1])));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) w[16 * h + j] = pack_bf16(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
             }
           }
           if (c + 64 >= cend) release(b);
