@@ -63,16 +63,33 @@ gbla_status make_plan(const gbla_shape* s, Plan& p) {
   p.N1 = 4 * p.HD + p.H;
   p.NP = (p.N1 + 63) / 64 * 64;
   const int pairs = p.n_seq * p.H;
-  const int target = kSMs * 8;
   const int cg = p.f32 ? 64 : 128;  // chunk granule: the row tile of the query-side backward
   if (p.mode == SEQ_VARLEN) {
-    const long long want = ((long long)p.T * p.H + target - 1) / target;
+    const long long want = ((long long)p.T * p.H + kSMs - 1) / kSMs;
     p.chunk = (int)std::min<long long>(2048, std::max<long long>(256, (want + cg - 1) / cg * cg));
     p.chunk_per_seq = 0;
     p.n_chunks = cdiv(p.T, p.chunk) + p.n_seq;
   } else {
-    int per = std::max(1, std::min(cdiv(target, pairs), cdiv(p.L, cg)));
-    p.chunk = cdiv(cdiv(p.L, per), cg) * cg;
+    // Chunks per sequence: one CTA per (chunk, head) of the state reduction
+    // and the query-side backward, two resident per SM.  Take the split with
+    // the least work on the busiest SM: its CTAs x (tiles per CTA + one tile
+    // for start-up and the combine), at 3.7 time units a tile when two CTAs
+    // share the SM and 4.5 when one runs alone (measured per-tile times of the
+    // query-side backward).
+    const int tiles = cdiv(p.L, cg);
+    long long best_cost = -1;
+    int best_tpc = tiles;
+    for (int per = 1; per <= std::min(tiles, 64); ++per) {
+      const int tpc = cdiv(tiles, per);
+      const long long ctas = (long long)pairs * cdiv(tiles, tpc);
+      const long long per_sm = (ctas + kSMs - 1) / kSMs;
+      const long long cost = per_sm >= 2 ? per_sm * (tpc + 1) * 37 : (long long)(tpc + 1) * 45;
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best_tpc = tpc;
+      }
+    }
+    p.chunk = best_tpc * cg;
     p.chunk_per_seq = cdiv(p.L, p.chunk);
     p.n_chunks = p.chunk_per_seq * p.n_seq;
   }
@@ -395,6 +412,7 @@ gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* con
   ga.bias_g = shape->gate == GBLA_GATE_SIGMOID ? b_g : nullptr;
   ga.gate_mode = shape->gate == GBLA_GATE_SIGMOID ? 0 : 1; ga.gate = gate; ga.ldgate = p.H; ga.io_f32 = p.f32;
   ga.err = c.err;
+  ga.pair = 1;  // CTA pairs: each CTA loads half of B, a third less operand traffic per SM
   GBLA_CHECK(launch_gemm(ga, c.st), "projection gemm");
   // Eq. 5/6: state
   const size_t es = p.io;
