@@ -23,6 +23,7 @@
 // Every mbarrier wait is bounded; after one gives up, the kernel finishes its
 // loops without waiting, sets the timeout bit of the error word, waits
 // (bounded) for its copies and MMAs, frees its TMEM and returns.
+#include "pdl.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
 
@@ -85,6 +86,7 @@ __device__ __forceinline__ Unit unit_at(const BwdKVArgs& a, int u, int n_units_p
 __global__ void __launch_bounds__(NTH, 1)
     k_bwd_kv_tc(const BwdKVArgs a, const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmS,
                 int voff, int n_units_per_head, int n_units) {
+  pdl_enter();  // the previous kernel's outputs are visible from here on
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -348,9 +350,8 @@ cudaError_t launch_bwd_kv_tc(const BwdKVArgs& a, int n_tiles, int* nparts, cudaS
   if (e != cudaSuccess) return e;
   const int n_units = n_tiles * a.H;
   const int grid = n_units < sm_count() ? n_units : sm_count();
-  k_bwd_kv_tc<<<grid, NTH, SMEM, st>>>(a, tmP, tmS, (int)voff, n_tiles, n_units);
   *nparts = n_tiles * (a.tiles.tile / KT);
-  return cudaGetLastError();
+  return launch_pdl(k_bwd_kv_tc, dim3(grid), dim3(NTH), SMEM, st, a, tmP, tmS, (int)voff, n_tiles, n_units);
 }
 
 }  // namespace gbla

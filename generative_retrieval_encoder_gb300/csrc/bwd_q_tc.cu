@@ -32,6 +32,7 @@
 // waiting), sets the timeout bit of the error word, waits (bounded) for its
 // copies and MMAs, frees its TMEM and returns.
 #include "core_common.cuh"
+#include "pdl.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
 
@@ -98,6 +99,7 @@ __device__ __forceinline__ float sigmoid_fast(float x) {
 __global__ void __launch_bounds__(NTH, 2)
     k_bwd_q_tc(const BwdQArgs a, const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmY,
                int roff) {
+  pdl_enter();  // the previous kernel's outputs are visible from here on
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -447,8 +449,7 @@ cudaError_t launch_bwd_q_tc(const BwdQArgs& a, int hd, int grid_x, cudaStream_t 
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k_bwd_q_tc, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  k_bwd_q_tc<<<dim3(a.H, grid_x), NTH, SMEM, st>>>(a, tmP, tmY, (int)roff);
-  return cudaGetLastError();
+  return launch_pdl(k_bwd_q_tc, dim3(a.H, grid_x), dim3(NTH), SMEM, st, a, tmP, tmY, (int)roff);
 }
 
 }  // namespace gbla

@@ -17,6 +17,7 @@
 // uniform.
 #include <algorithm>
 
+#include "pdl.cuh"
 #include "kernels.h"
 #include "mbarrier.cuh"
 
@@ -126,6 +127,7 @@ __device__ __forceinline__ bool tile_loop(int ntile, uint8_t* smem, Issue issue,
 // x~[l, c] = b[c] + sum_t w[c, t] x[l - 3 + t, c]; taps before the sequence
 // start read 0; padding rows get 0.
 __global__ void __launch_bounds__(NTH, 1) k_conv_fwd_tile(const ConvArgs a, int gx) {
+  pdl_enter();  // the previous kernel's outputs are visible from here on
   typedef ConvSmem<1, FWD_ST> S;
   extern __shared__ __align__(128) uint8_t smem[];
   if (a.err && *a.err) return;
@@ -208,6 +210,7 @@ __global__ void __launch_bounds__(NTH, 1) k_conv_fwd_tile(const ConvArgs a, int 
 // Thread (pair, half) of block (bx, channel tile) writes its partials to
 // part[2 bx + half][c][0..4].
 __global__ void __launch_bounds__(NTH, 1) k_conv_bwd_tile(const ConvArgs a, int gx) {
+  pdl_enter();  // the previous kernel's outputs are visible from here on
   typedef ConvSmem<2, BWD_ST> S;
   extern __shared__ __align__(128) uint8_t smem[];
   if (a.err && *a.err) return;
@@ -323,7 +326,7 @@ cudaError_t launch_conv_fwd_tile(const ConvArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int n_rt = (a.T + CR - 1) / CR, n_ct = (a.d + CW - 1) / CW;
   const int gx = std::max(1, std::min(n_rt, std::max(1, sm_count() / n_ct)));
-  k_conv_fwd_tile<<<dim3(gx, n_ct), NTH, S::BYTES, st>>>(a, gx);
+  return launch_pdl(k_conv_fwd_tile, dim3(gx, n_ct), dim3(NTH), S::BYTES, st, a, gx);
   return cudaGetLastError();
 }
 
@@ -333,7 +336,7 @@ cudaError_t launch_conv_bwd_tile(const ConvArgs& a, int nparts, cudaStream_t st)
   cudaError_t e = cudaFuncSetAttribute(k_conv_bwd_tile, cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
   if (e != cudaSuccess) return e;
   const int gx = nparts / 2, n_ct = (a.d + CW - 1) / CW;
-  k_conv_bwd_tile<<<dim3(gx, n_ct), NTH, S::BYTES, st>>>(a, gx);
+  return launch_pdl(k_conv_bwd_tile, dim3(gx, n_ct), dim3(NTH), S::BYTES, st, a, gx);
   return cudaGetLastError();
 }
 

@@ -15,6 +15,7 @@
 //   bwd_kv : dk~ = dS v + dz; dv = dS^T k~; dg = phi(k).dk~;
 //            dk = g dk~ phi'(k); gate derivative.
 #include "core_common.cuh"
+#include "pdl.cuh"
 
 namespace gbla {
 namespace {
@@ -73,6 +74,7 @@ struct RedCfg {
 
 template <int DH, bool PRE>
 __global__ void __launch_bounds__(256) k_reduce_bf16(const ReduceArgs a) {
+  pdl_enter();  // the previous kernel's outputs are visible from here on
   using C = Cfg<DH>;
   using R = RedCfg<DH>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -937,8 +939,7 @@ cudaError_t launch_reduce_bf16(const ReduceArgs& a, int grid_x, cudaStream_t st)
 #define GBLA_CASE(D, P)                                                              \
   case D * 2 + P:                                                                    \
     if ((e = prep(k_reduce_bf16<D, P>, RedCfg<D>::SMEM)) != cudaSuccess) return e;   \
-    k_reduce_bf16<D, P><<<grid, 256, RedCfg<D>::SMEM, st>>>(a);                      \
-    break;
+    return launch_pdl(k_reduce_bf16<D, P>, grid, dim3(256), RedCfg<D>::SMEM, st, a);
     GBLA_CASE(32, 0) GBLA_CASE(32, 1) GBLA_CASE(64, 0) GBLA_CASE(64, 1) GBLA_CASE(128, 0) GBLA_CASE(128, 1)
 #undef GBLA_CASE
     default: return cudaErrorInvalidValue;

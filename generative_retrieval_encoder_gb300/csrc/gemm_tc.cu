@@ -29,6 +29,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include "pdl.cuh"
 #include "kernels.h"
 #include "mbarrier.cuh"
 #include "tcgen05.cuh"
@@ -164,6 +165,7 @@ template <bool AMN, bool BMN, int CL>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const GemmArgs a, const TileSched ts, int wide_ok) {
+  pdl_enter();  // the previous kernel's outputs are visible from here on
   using RG = Ring<CL>;
   constexpr int ST = RG::ST;
   extern __shared__ uint8_t smem_raw[];
@@ -506,8 +508,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
       if ((e = cudaFuncSetAttribute(k_gemm_tc<AMN, BMN, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
                                     SMEM_P)) != cudaSuccess)                                                 \
         return e;                                                                                            \
-      k_gemm_tc<AMN, BMN, 1><<<grid, NTHREADS, SMEM_P, st>>>(ta, tb, a, ts, wide_ok);                  \
-      return cudaGetLastError();                                                                             \
+      return launch_pdl(k_gemm_tc<AMN, BMN, 1>, dim3(grid), dim3(NTHREADS), SMEM_P, st, ta, tb, a, ts, wide_ok); \
     }                                                                                                        \
     if ((e = cudaFuncSetAttribute(k_gemm_tc<AMN, BMN, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,       \
                                   SMEM_P)) != cudaSuccess)                                                   \
@@ -517,13 +518,14 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
     cfg.blockDim = dim3(NTHREADS);                                                                           \
     cfg.dynamicSmemBytes = SMEM_P;                                                                           \
     cfg.stream = st;                                                                                         \
-    cudaLaunchAttribute attr[1];                                                                             \
+    cudaLaunchAttribute attr[2];                                                                             \
     attr[0].id = cudaLaunchAttributeClusterDimension;                                                        \
     attr[0].val.clusterDim.x = 2;                                                                            \
     attr[0].val.clusterDim.y = 1;                                                                            \
     attr[0].val.clusterDim.z = 1;                                                                            \
+    attr[1] = pdl_attribute();                                                                               \
     cfg.attrs = attr;                                                                                        \
-    cfg.numAttrs = 1;                                                                                        \
+    cfg.numAttrs = 2;                                                                                        \
     return cudaLaunchKernelEx(&cfg, k_gemm_tc<AMN, BMN, 2>, ta, tb, a, ts, wide_ok);                        \
   }
   GBLA_CASE(false, false) GBLA_CASE(true, true) GBLA_CASE(false, true) GBLA_CASE(true, false)

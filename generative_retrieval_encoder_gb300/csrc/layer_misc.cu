@@ -5,6 +5,7 @@
 #include <algorithm>
 
 #include "kernels.h"
+#include "pdl.cuh"
 
 namespace gbla {
 namespace {
@@ -287,6 +288,7 @@ __global__ void __launch_bounds__(256) k_conv_bwd(const ConvArgs a, int rows_per
 template <typename T>
 __global__ void __launch_bounds__(256) k_pack(const T* Wq, const T* Wk, const T* Wv, const T* Wr, const T* wg,
                                               int d, int H, int dh, T* Wp, int np, int vec) {
+  pdl_enter();  // the previous kernel's outputs are visible from here on
   constexpr int V = 16 / sizeof(T);
   typedef uint4 U;
   const int HD = H * dh, npv = np / V;
@@ -320,6 +322,7 @@ __global__ void __launch_bounds__(256) k_pack(const T* Wq, const T* Wk, const T*
 // mode 0: out[i];  mode 1 (conv parameters, i = 5 c + t): t < 4 -> out[4 c + t], else out2[c].
 __global__ void __launch_bounds__(1024) k_colsum(const float* part, int S, int64_t stride, int64_t n, float* out,
                                                  float* out2, int mode) {
+  pdl_enter();  // the previous kernel's outputs are visible from here on
   __shared__ float red[32][33];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t i = (int64_t)blockIdx.x * 32 + lane;
@@ -343,6 +346,7 @@ __global__ void __launch_bounds__(1024) k_colsum(const float* part, int S, int64
 
 __global__ void k_scatter_dw(const float* part, int S, int d, int np, int H, int dh, float* o0, float* o1,
                              float* o2, float* o3, float* o4) {
+  pdl_enter();  // the previous kernel's outputs are visible from here on
   const int HD = H * dh;
   float* outs[4] = {o0, o1, o2, o3};
   const size_t total = (size_t)d * np;
@@ -406,29 +410,26 @@ cudaError_t launch_pack_weights(const void* const* W, const void* w_g, int d, in
   const long long vecs = (long long)d * np / (f32 ? 4 : 8);
   const unsigned grid = (unsigned)std::max(1LL, std::min((vecs + 255) / 256, (long long)sm_count() * 8));
   if (f32)
-    k_pack<float><<<grid, 256, 0, st>>>((const float*)W[0], (const float*)W[1], (const float*)W[2],
-                                        (const float*)W[3], (const float*)w_g, d, H, dh, (float*)Wp, np, vec);
-  else
-    k_pack<bf16><<<grid, 256, 0, st>>>((const bf16*)W[0], (const bf16*)W[1], (const bf16*)W[2],
-                                       (const bf16*)W[3], (const bf16*)w_g, d, H, dh, (bf16*)Wp, np, vec);
-  return cudaGetLastError();
+    return launch_pdl(k_pack<float>, dim3(grid), dim3(256), 0, st, (const float*)W[0], (const float*)W[1],
+                      (const float*)W[2], (const float*)W[3], (const float*)w_g, d, H, dh, (float*)Wp, np, vec);
+  return launch_pdl(k_pack<bf16>, dim3(grid), dim3(256), 0, st, (const bf16*)W[0], (const bf16*)W[1],
+                    (const bf16*)W[2], (const bf16*)W[3], (const bf16*)w_g, d, H, dh, (bf16*)Wp, np, vec);
 }
 
 cudaError_t launch_sum_parts(const float* part, int S, int64_t stride, int64_t n, float* out, cudaStream_t st) {
-  k_colsum<<<(unsigned)((n + 31) / 32), 1024, 0, st>>>(part, S, stride, n, out, nullptr, 0);
-  return cudaGetLastError();
+  return launch_pdl(k_colsum, dim3((unsigned)((n + 31) / 32)), dim3(1024), 0, st, part, S, stride, n, out,
+                    (float*)nullptr, 0);
 }
 
 cudaError_t launch_scatter_dw(const float* part, int S, int d, int np, int H, int dh, float* const* outs,
                               cudaStream_t st) {
-  k_scatter_dw<<<grid_for((size_t)d * np), 256, 0, st>>>(part, S, d, np, H, dh, outs[0], outs[1], outs[2],
-                                                         outs[3], outs[4]);
-  return cudaGetLastError();
+  return launch_pdl(k_scatter_dw, dim3(grid_for((size_t)d * np)), dim3(256), 0, st, part, S, d, np, H, dh, outs[0],
+                    outs[1], outs[2], outs[3], outs[4]);
 }
 
 cudaError_t launch_conv_param_grads(const float* part, int S, int d, float* dw, float* db, cudaStream_t st) {
-  k_colsum<<<(unsigned)((d * 5 + 31) / 32), 1024, 0, st>>>(part, S, (int64_t)d * 5, (int64_t)d * 5, dw, db, 1);
-  return cudaGetLastError();
+  return launch_pdl(k_colsum, dim3((unsigned)((d * 5 + 31) / 32)), dim3(1024), 0, st, part, S, (int64_t)d * 5,
+                    (int64_t)d * 5, dw, db, 1);
 }
 
 }  // namespace gbla

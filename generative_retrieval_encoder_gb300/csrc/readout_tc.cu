@@ -23,6 +23,7 @@
 // Every mbarrier wait is bounded; after one gives up, the kernel finishes its
 // loops without waiting, sets the timeout bit of the error word, waits
 // (bounded) for its copies and MMAs, frees its TMEM and returns.
+#include "pdl.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
 
@@ -93,6 +94,7 @@ __device__ __forceinline__ Unit unit_at(const ReadoutArgs& a, int u, int n_units
 __global__ void __launch_bounds__(NTH, 1)
     k_readout_tc(const ReadoutArgs a, const __grid_constant__ CUtensorMap tmP,
                  const __grid_constant__ CUtensorMap tmS, int roff, int n_units_per_head, int n_units) {
+  pdl_enter();  // the previous kernel's outputs are visible from here on
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -342,8 +344,7 @@ cudaError_t launch_readout_tc(const ReadoutArgs& a, int n_tiles, cudaStream_t st
   if (e != cudaSuccess) return e;
   const int n_units = n_tiles * a.H;
   const int grid = n_units < sm_count() ? n_units : sm_count();
-  k_readout_tc<<<grid, NTH, SMEM, st>>>(a, tmP, tmS, (int)roff, n_tiles, n_units);
-  return cudaGetLastError();
+  return launch_pdl(k_readout_tc, dim3(grid), dim3(NTH), SMEM, st, a, tmP, tmS, (int)roff, n_tiles, n_units);
 }
 
 }  // namespace gbla
