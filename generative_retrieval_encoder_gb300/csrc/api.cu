@@ -18,6 +18,7 @@ namespace {
 thread_local std::string g_last_error;
 
 constexpr int kSMs = 152;
+constexpr int kMaxGrid = 512;  // CTAs of a range-split kernel the workspace provides for (>= 2 x SMs)
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -160,6 +161,11 @@ SavedLayout saved_layout(const Plan& p) {
   return s;
 }
 
+// Partial-state slots: one per (chunk, head) for the split-L kernels; the
+// tcgen05 query-side backward takes one per (sequence, head) plus one per CTA
+// (a CTA boundary inside a (sequence, head)).
+int partial_slots(const Plan& p) { return std::max(p.n_chunks * p.H, p.n_seq * p.H + kMaxGrid); }
+
 Layout ws_layout(const Plan& p, int op) {
   Cursor c;
   Layout l;
@@ -172,7 +178,7 @@ Layout ws_layout(const Plan& p, int op) {
     l.pre_c = c.take((size_t)(p.n_seq + 1) * 4);
     l.pre_t = c.take((size_t)(p.n_seq + 1) * 4);
   }
-  l.partial = c.take((size_t)p.n_chunks * p.H * p.dh * state_ld(p.dh) * 4);
+  l.partial = c.take((size_t)partial_slots(p) * p.dh * state_ld(p.dh) * 4);
   l.partial_m = c.take((size_t)p.n_chunks * p.H * 4);
   if (op == GBLA_OP_FORWARD) {  // inference forward keeps its activations here
     l.state = c.take(state_bytes(p));
@@ -190,7 +196,7 @@ Layout ws_layout(const Plan& p, int op) {
     l.dW = c.take((size_t)p.n_wsplit * p.d * p.NP * 4);
     l.dstate = c.take(state_bytes(p));
     l.dstate_bf = c.take(state_bf_bytes(p));
-    l.gamma_part = c.take((size_t)p.n_chunks * p.H * p.dh * 4);
+    l.gamma_part = c.take((size_t)std::max(p.n_chunks * p.H, kMaxGrid) * p.dh * 4);
     l.bg_part = c.take((size_t)p.n_tiles * 2 * p.H * 4);  // up to two partial rows per tile
     l.conv_part = c.take((size_t)p.conv_blocks * p.d * 5 * 4);
   } else {  // core forward / backward
@@ -314,11 +320,14 @@ cudaError_t launch_bwd_kv_layer_bf16(const BwdKVArgs& kv, int n_tiles, int* bg_r
 }
 
 // The layer's bf16 query-side backward: the tcgen05 kernel where it applies.
-cudaError_t launch_bwd_q_layer_bf16(const BwdQArgs& q, int hd, int grid_x, cudaStream_t st) {
-  const cudaError_t e = launch_bwd_q_tc(q, hd, grid_x, st);
+// *gamma_rows = the rows of dgamma partials written.
+cudaError_t launch_bwd_q_layer_bf16(const BwdQArgs& q, int hd, int n_chunks, int n_tiles, int* gamma_rows,
+                                    cudaStream_t st) {
+  const cudaError_t e = launch_bwd_q_tc(q, hd, n_tiles, gamma_rows, st);
   if (e != cudaErrorNotSupported) return e;
   (void)cudaGetLastError();
-  return launch_bwd_q_bf16(q, true, grid_x, st);
+  *gamma_rows = n_chunks * q.H;
+  return launch_bwd_q_bf16(q, true, n_chunks, st);
 }
 
 gbla_status run_reduce(Ctx& c, const void* k, const void* v, int64_t ld, const float* g, int gate_kind, float* state,
@@ -482,8 +491,11 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   q.partial = at<float>(ws, l.partial); q.counters = at<int>(ws, l.cnt_b);
   q.dstate = at<float>(ws, l.dstate); q.dstate_bf = at<bf16>(ws, l.dstate_bf);
   q.rsinv = at<const float>(const_cast<void*>(saved), s.rsinv);
-  q.H = p.H; q.dh = p.dh; q.seq = c.seq; q.chunks = c.chunks; q.err = c.kerr; q.err_out = c.err;
-  GBLA_CHECK(p.f32 ? launch_bwd_q_f32(q, true, p.n_chunks, c.st) : launch_bwd_q_layer_bf16(q, p.HD, p.n_chunks, c.st),
+  q.H = p.H; q.dh = p.dh; q.seq = c.seq; q.chunks = c.chunks; q.tiles = c.tiles; q.err = c.kerr; q.err_out = c.err;
+  q.partial_slots = partial_slots(p);
+  int gamma_rows = p.n_chunks * p.H;
+  GBLA_CHECK(p.f32 ? launch_bwd_q_f32(q, true, p.n_chunks, c.st)
+                   : launch_bwd_q_layer_bf16(q, p.HD, p.n_chunks, p.n_tiles, &gamma_rows, c.st),
              "bwd_q");
   // key side: dk, dv, ds
   BwdKVArgs kv{};
@@ -534,7 +546,7 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   if (dconv_w || dconv_b)
     GBLA_CHECK(launch_conv_param_grads(ca.part, nparts, p.d, dconv_w, dconv_b, c.st), "conv grads");
   if (drms_w)
-    GBLA_CHECK(launch_sum_parts(q.gamma_part, p.n_chunks * p.H, p.dh, p.dh, drms_w, c.st), "dgamma");
+    GBLA_CHECK(launch_sum_parts(q.gamma_part, gamma_rows, p.dh, p.dh, drms_w, c.st), "dgamma");
   if (db_g)
     GBLA_CHECK(launch_sum_parts(kv.bg_part, bg_rows, p.H, p.H, db_g, c.st), "db_g");
   return GBLA_OK;

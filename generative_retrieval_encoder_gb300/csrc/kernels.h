@@ -72,11 +72,13 @@ struct BwdQArgs {
   const float* center;              // [n_seq*H][dh] or null (state is uncentred)
   void* dq; int64_t lddq;
   void* dr; int64_t lddr;           // norm only
-  float* gamma_part;                // norm only: [gridDim.x * H][dh]
+  float* gamma_part;                // norm only: [gridDim.x * H][dh] (tcgen05: [gridDim.x][dh])
   float* partial; int* counters;    // dS partials, [n_seq*H] counters
+  int partial_slots;                // tcgen05 kernel: slots of `partial` (n_seq H + one per CTA needed)
   float* dstate; bf16* dstate_bf;   // combined [dS | dz]
   int H, dh;
   SeqDesc seq; Tiling chunks;
+  Tiling tiles;                     // tcgen05 kernel: its units are 128-row pieces of these tiles
   const float* rsinv;               // tcgen05 kernel: [rows, H] x {rs, 1/den} from the forward
   const int* err;
   int* err_out;                     // tcgen05 kernel: timeout bit of the workspace error word
@@ -146,7 +148,9 @@ cudaError_t launch_readout_bf16(const ReadoutArgs& a, bool norm, int grid_x, cud
 cudaError_t launch_bwd_q_bf16(const BwdQArgs& a, bool norm, int grid_x, cudaStream_t st);
 // tcgen05 query-side backward (bwd_q_tc.cu): d_h = 64, the layer's RMSNorm
 // epilogue, phi(q) stored (pre); cudaErrorNotSupported otherwise.
-cudaError_t launch_bwd_q_tc(const BwdQArgs& a, int hd, int grid_x, cudaStream_t st);
+// Its CTAs (two per SM) take contiguous ranges of the (128-row tile, head)
+// units of a.tiles (n_tiles tiles); *nparts = the dgamma partial rows written.
+cudaError_t launch_bwd_q_tc(const BwdQArgs& a, int hd, int n_tiles, int* nparts, cudaStream_t st);
 // tcgen05 readout with the RmsNorm gate (readout_tc.cu): d_h = 64, phi(q)
 // stored (pre), no den output; cudaErrorNotSupported otherwise.
 cudaError_t launch_readout_tc(const ReadoutArgs& a, int n_tiles, cudaStream_t st);
