@@ -278,10 +278,13 @@ __global__ void __launch_bounds__(NTH, 2)
     uint32_t o[CPT];
     {
       uint32_t g[CPT];
-      tmem_ld32(tl + f0, o);  // (waits)
-      if (k > 0) {
-        tmem_ld32(tl + 192 + f0, g);
+      tmem_ld32_async(tl + f0, o);
+      if (k > 0) {  // O' and the running dgamma under one wait
+        tmem_ld32_async(tl + 192 + f0, g);
+        tmem_wait32(o);
+        tmem_tie32(g);
       } else {
+        tmem_wait32(o);
 #pragma unroll
         for (int j = 0; j < CPT; ++j) g[j] = 0u;
       }
@@ -332,7 +335,7 @@ __global__ void __launch_bounds__(NTH, 2)
     m *= 1.f / QD;
     const float dden = -rs * fmaf(-m, D2, D1) * inv;
     // pass 2: dn = rs (du - u m) / den -> the dy tile
-    tmem_ld32(tl + f0, o);  // O' again (waits)
+    tmem_ld32(tl + f0, o);  // O' again: held through pass 1's exchange it would spill
 #pragma unroll
     for (int ch = 0; ch < NC; ++ch) {
       const int f = f0 + 8 * ch, cc = f >> 3;
