@@ -6,9 +6,10 @@
 // into a ring of shared-memory stages, issued by warp 0 several tiles ahead,
 // so the copies of later tiles are in flight while the block computes on the
 // current one.  A block is persistent over the row tiles of one channel tile.
-// Each of its 512 threads owns a channel pair (c, c + 1) and half of the tile's
-// rows, slides a 4-row window down its rows, and keeps its own parameter-
-// gradient partials, so the backward needs no reduction inside the block.
+// In the forward a thread computes 4 rows x 8 channels of a tile (16-byte
+// shared loads and global stores); in the backward 8 rows x 4 channels,
+// sliding a 4-row window down x and dx~, and keeps its own parameter-gradient
+// partials, so the backward needs no reduction inside the block.
 //
 // Per-row sequence structure (the first row of the sequence and the end of
 // its valid rows) is folded into a 9-bit mask per tile row, computed by
@@ -49,6 +50,7 @@ struct ConvSmem {
   static constexpr int BYTES = BARS + ST * 8;
 };
 static_assert(ConvSmem<2, BWD_ST>::BYTES <= 227 * 1024, "backward stages exceed shared memory");
+static_assert(ConvSmem<1, FWD_ST>::BYTES <= 227 * 1024, "forward stages exceed shared memory");
 
 __device__ uint32_t row_mask(const SeqDesc& sd, int l) {
   if (l >= sd.T) return 0;
@@ -125,17 +127,29 @@ __device__ __forceinline__ bool tile_loop(int ntile, uint8_t* smem, Issue issue,
 }
 
 // x~[l, c] = b[c] + sum_t w[c, t] x[l - 3 + t, c]; taps before the sequence
-// start read 0; padding rows get 0.
+// start read 0; padding rows get 0.  Thread (channel octet tid % 64, row
+// quarter-group tid / 64) computes 4 rows x 8 channels of a tile from 7
+// 16-byte shared loads and leaves them as 16-byte stores.
+constexpr int FV = 8;                 // channels per thread (16 bytes of bf16)
+constexpr int FRG = NTH / (CW / FV);  // row groups
+constexpr int FRR = CR / FRG;         // rows per thread
+static_assert(FRR == 4 && FRG * FRR == CR, "forward: 8 row groups of 4 rows");
+__device__ __forceinline__ void unpack8f(const uint4& u, float* f) {
+  f[0] = __uint_as_float(u.x << 16); f[1] = __uint_as_float(u.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(u.y << 16); f[3] = __uint_as_float(u.y & 0xFFFF0000u);
+  f[4] = __uint_as_float(u.z << 16); f[5] = __uint_as_float(u.z & 0xFFFF0000u);
+  f[6] = __uint_as_float(u.w << 16); f[7] = __uint_as_float(u.w & 0xFFFF0000u);
+}
 __global__ void __launch_bounds__(NTH, 1) k_conv_fwd_tile(const ConvArgs a, int gx) {
   pdl_enter();  // the previous kernel's outputs are visible from here on
   typedef ConvSmem<1, FWD_ST> S;
   extern __shared__ __align__(128) uint8_t smem[];
   if (a.err && *a.err) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int pr = tid & 255, half = tid >> 8;
+  const int cg = tid % (CW / FV), rg = tid / (CW / FV);
   const int c0 = blockIdx.y * CW, cw = min(CW, a.d - c0);
-  const int c = c0 + 2 * pr;
-  const bool act = 2 * pr < cw;
+  const int c = c0 + FV * cg;
+  const bool act = FV * cg < cw;
   const int n_rt = (a.T + CR - 1) / CR;
   const int ntile = n_rt > (int)blockIdx.x ? (n_rt - 1 - (int)blockIdx.x) / gx + 1 : 0;
   const bf16* x = (const bf16*)a.x;
@@ -143,20 +157,22 @@ __global__ void __launch_bounds__(NTH, 1) k_conv_fwd_tile(const ConvArgs a, int 
   uint32_t* masks = reinterpret_cast<uint32_t*>(smem + S::MASKS);
   const uint32_t bars = smem_u32(smem + S::BARS);
 
-  float2 w[4], bias = make_float2(0.f, 0.f);
-  if (act) {
-    const uint4 wr = *reinterpret_cast<const uint4*>((const bf16*)a.w + (size_t)c * 4);  // taps of c, c + 1
-    const uint32_t wv[4] = {wr.x, wr.y, wr.z, wr.w};
+  float w[4][FV], bias[FV];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const uint32_t lo = wv[t / 2], hi = wv[2 + t / 2];
-      w[t].x = __uint_as_float(t & 1 ? lo & 0xFFFF0000u : lo << 16);
-      w[t].y = __uint_as_float(t & 1 ? hi & 0xFFFF0000u : hi << 16);
+  for (int v = 0; v < FV; ++v) bias[v] = 0.f;
+  if (act) {
+    const bf16* wc = (const bf16*)a.w + (size_t)c * 4;  // [c][4 taps], 8 channels = 64 bytes
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float f[8];
+      unpack8f(*reinterpret_cast<const uint4*>(wc + 8 * q), f);  // channels 2q, 2q + 1
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        w[t][2 * q] = f[t];
+        w[t][2 * q + 1] = f[4 + t];
+      }
     }
-    if (a.b) {
-      const uint32_t bv = *reinterpret_cast<const uint32_t*>((const bf16*)a.b + c);
-      bias = make_float2(__uint_as_float(bv << 16), __uint_as_float(bv & 0xFFFF0000u));
-    }
+    if (a.b) unpack8f(*reinterpret_cast<const uint4*>((const bf16*)a.b + c), bias);
   }
 
   auto issue = [&](int j, int st) {
@@ -176,28 +192,31 @@ __global__ void __launch_bounds__(NTH, 1) k_conv_fwd_tile(const ConvArgs a, int 
     const uint8_t* xs = smem + st * S::STAGE;  // smem row i + t holds x[r0 + i - 3 + t]
     const uint32_t* mk = masks + st * CR;
     if (!act) return;
-    const int i0 = half * HALF;
-    float2 x0 = ld2(xs, i0, cw, pr), x1 = ld2(xs, i0 + 1, cw, pr), x2 = ld2(xs, i0 + 2, cw, pr);
+    const int i0 = rg * FRR;
+    float xv[FRR + 3][FV];
 #pragma unroll
-    for (int ii = 0; ii < HALF; ++ii) {
+    for (int r = 0; r < FRR + 3; ++r)
+      unpack8f(*reinterpret_cast<const uint4*>(xs + ((size_t)(i0 + r) * cw + FV * cg) * 2), xv[r]);
+#pragma unroll
+    for (int ii = 0; ii < FRR; ++ii) {
       const int i = i0 + ii;
-      const float2 x3 = ld2(xs, i + 3, cw, pr);
       const uint32_t m = mk[i];
-      if (m & M_ROW) {
-        float2 o = make_float2(0.f, 0.f);
-        if (m == M_FULL) {
-          o = bias;
-          fma2(o, w[0], x0); fma2(o, w[1], x1); fma2(o, w[2], x2); fma2(o, w[3], x3);
-        } else if (m & M_VALID) {
-          o = bias;
-          if (m & 1u) fma2(o, w[0], x0);
-          if (m & 2u) fma2(o, w[1], x1);
-          if (m & 4u) fma2(o, w[2], x2);
-          fma2(o, w[3], x3);
+      if (!(m & M_ROW)) continue;
+      float o[FV];
+#pragma unroll
+      for (int v = 0; v < FV; ++v) o[v] = 0.f;
+      if (m & M_VALID) {
+#pragma unroll
+        for (int v = 0; v < FV; ++v) {
+          float acc = bias[v];
+          if (m & 1u) acc = fmaf(w[0][v], xv[ii][v], acc);
+          if (m & 2u) acc = fmaf(w[1][v], xv[ii + 1][v], acc);
+          if (m & 4u) acc = fmaf(w[2][v], xv[ii + 2][v], acc);
+          o[v] = fmaf(w[3][v], xv[ii + 3][v], acc);
         }
-        *reinterpret_cast<uint32_t*>(xt + (size_t)(r0 + i) * a.d + c) = pack_bf16(o.x, o.y);
       }
-      x0 = x1; x1 = x2; x2 = x3;
+      *reinterpret_cast<uint4*>(xt + (size_t)(r0 + i) * a.d + c) =
+          make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]), pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
     }
   };
   if (!tile_loop<1, FWD_ST>(ntile, smem, issue, compute) && tid == 0 && a.err_out)
@@ -207,18 +226,28 @@ __global__ void __launch_bounds__(NTH, 1) k_conv_fwd_tile(const ConvArgs a, int 
 // Backward, for rows l of a sequence (valid rows [s0, vend)):
 //   dx[l]  = sum_k w[3 - k] dx~[l + k]   (terms with l + k < vend)
 //   dw[t] += x[l - 3 + t] dx~[l]  (l - 3 + t >= s0);   db += dx~[l]
-// Thread (pair, half) of block (bx, channel tile) writes its partials to
-// part[2 bx + half][c][0..4].
+// Thread (channel quad tid % 128, row group tid / 128) of block (bx, channel
+// tile) computes 8 rows x 4 channels of each tile, sliding a 4-row window of
+// x and dx~ (8-byte shared loads), and writes its parameter partials to
+// part[4 bx + row group][c][0..4].
+constexpr int BV = 4;                 // channels per thread
+constexpr int BRG = NTH / (CW / BV);  // row groups
+constexpr int BRR = CR / BRG;         // rows per thread
+static_assert(BRG == 4 && BRR == 8, "backward: 4 row groups of 8 rows");
+__device__ __forceinline__ void unpack4f(const uint2& u, float* f) {
+  f[0] = __uint_as_float(u.x << 16); f[1] = __uint_as_float(u.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(u.y << 16); f[3] = __uint_as_float(u.y & 0xFFFF0000u);
+}
 __global__ void __launch_bounds__(NTH, 1) k_conv_bwd_tile(const ConvArgs a, int gx) {
   pdl_enter();  // the previous kernel's outputs are visible from here on
   typedef ConvSmem<2, BWD_ST> S;
   extern __shared__ __align__(128) uint8_t smem[];
   if (a.err && *a.err) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int pr = tid & 255, half = tid >> 8;
+  const int cq = tid % (CW / BV), rg = tid / (CW / BV);
   const int c0 = blockIdx.y * CW, cw = min(CW, a.d - c0);
-  const int c = c0 + 2 * pr;
-  const bool act = 2 * pr < cw;
+  const int c = c0 + BV * cq;
+  const bool act = BV * cq < cw;
   const int n_rt = (a.T + CR - 1) / CR;
   const int ntile = n_rt > (int)blockIdx.x ? (n_rt - 1 - (int)blockIdx.x) / gx + 1 : 0;
   const bf16* x = (const bf16*)a.x;
@@ -227,20 +256,29 @@ __global__ void __launch_bounds__(NTH, 1) k_conv_bwd_tile(const ConvArgs a, int 
   uint32_t* masks = reinterpret_cast<uint32_t*>(smem + S::MASKS);
   const uint32_t bars = smem_u32(smem + S::BARS);
 
-  float2 w[4];
+  float w[4][BV];
   if (act) {
-    const uint4 wr = *reinterpret_cast<const uint4*>((const bf16*)a.w + (size_t)c * 4);
-    const uint32_t wv[4] = {wr.x, wr.y, wr.z, wr.w};
+    const uint4* wc = reinterpret_cast<const uint4*>((const bf16*)a.w + (size_t)c * 4);  // [c][4 taps]
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const uint32_t lo = wv[t / 2], hi = wv[2 + t / 2];
-      w[t].x = __uint_as_float(t & 1 ? lo & 0xFFFF0000u : lo << 16);
-      w[t].y = __uint_as_float(t & 1 ? hi & 0xFFFF0000u : hi << 16);
+    for (int q = 0; q < 2; ++q) {  // channels c + 2q, c + 2q + 1
+      float f[8];
+      const uint4 u = wc[q];
+      unpack4f(make_uint2(u.x, u.y), f);
+      unpack4f(make_uint2(u.z, u.w), f + 4);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        w[t][2 * q] = f[t];
+        w[t][2 * q + 1] = f[4 + t];
+      }
     }
   }
-  float2 dw[4], db = make_float2(0.f, 0.f);
+  float dw[4][BV], db[BV];
 #pragma unroll
-  for (int t = 0; t < 4; ++t) dw[t] = make_float2(0.f, 0.f);
+  for (int v = 0; v < BV; ++v) {
+    db[v] = 0.f;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) dw[t][v] = 0.f;
+  }
 
   auto issue = [&](int j, int st) {
     const int r0 = ((int)blockIdx.x + j * gx) * CR;
@@ -262,35 +300,40 @@ __global__ void __launch_bounds__(NTH, 1) k_conv_bwd_tile(const ConvArgs a, int 
     const uint8_t* gs = xs + S::TENSOR;        // row i + k: dx~[r0 + i + k]
     const uint32_t* mk = masks + st * CR;
     if (!act) return;
-    const int i0 = half * HALF;
-    float2 x0 = ld2(xs, i0, cw, pr), x1 = ld2(xs, i0 + 1, cw, pr), x2 = ld2(xs, i0 + 2, cw, pr);
-    float2 g0 = ld2(gs, i0, cw, pr), g1 = ld2(gs, i0 + 1, cw, pr), g2 = ld2(gs, i0 + 2, cw, pr);
+    const int i0 = rg * BRR;
+    float xv[BRR + 3][BV], gv[BRR + 3][BV];  // rows i0 .. i0 + 10, loaded as the window slides
 #pragma unroll
-    for (int ii = 0; ii < HALF; ++ii) {
+    for (int r = 0; r < 3; ++r) {
+      unpack4f(*reinterpret_cast<const uint2*>(xs + ((size_t)(i0 + r) * cw + c - c0) * 2), xv[r]);
+      unpack4f(*reinterpret_cast<const uint2*>(gs + ((size_t)(i0 + r) * cw + c - c0) * 2), gv[r]);
+    }
+#pragma unroll
+    for (int ii = 0; ii < BRR; ++ii) {
       const int i = i0 + ii;
-      const float2 x3 = ld2(xs, i + 3, cw, pr), g3 = ld2(gs, i + 3, cw, pr);
+      unpack4f(*reinterpret_cast<const uint2*>(xs + ((size_t)(i + 3) * cw + c - c0) * 2), xv[ii + 3]);
+      unpack4f(*reinterpret_cast<const uint2*>(gs + ((size_t)(i + 3) * cw + c - c0) * 2), gv[ii + 3]);
       const uint32_t m = mk[i];
-      if (m & M_ROW) {
-        float2 o = make_float2(0.f, 0.f);
-        if (m == M_FULL) {
-          fma2(o, w[3], g0); fma2(o, w[2], g1); fma2(o, w[1], g2); fma2(o, w[0], g3);
-          fma2(dw[0], x0, g0); fma2(dw[1], x1, g0); fma2(dw[2], x2, g0); fma2(dw[3], x3, g0);
-          db.x += g0.x; db.y += g0.y;
-        } else if (m & M_VALID) {
-          fma2(o, w[3], g0);
-          if (m & (M_VALID << 1)) fma2(o, w[2], g1);
-          if (m & (M_VALID << 2)) fma2(o, w[1], g2);
-          if (m & (M_VALID << 3)) fma2(o, w[0], g3);
-          if (m & 1u) fma2(dw[0], x0, g0);
-          if (m & 2u) fma2(dw[1], x1, g0);
-          if (m & 4u) fma2(dw[2], x2, g0);
-          fma2(dw[3], x3, g0);
-          db.x += g0.x; db.y += g0.y;
+      if (!(m & M_ROW)) continue;
+      float o[BV];
+#pragma unroll
+      for (int v = 0; v < BV; ++v) o[v] = 0.f;
+      if (m & M_VALID) {
+#pragma unroll
+        for (int v = 0; v < BV; ++v) {
+          const float g0 = gv[ii][v];
+          float acc = w[3][v] * g0;
+          if (m & (M_VALID << 1)) acc = fmaf(w[2][v], gv[ii + 1][v], acc);
+          if (m & (M_VALID << 2)) acc = fmaf(w[1][v], gv[ii + 2][v], acc);
+          if (m & (M_VALID << 3)) acc = fmaf(w[0][v], gv[ii + 3][v], acc);
+          o[v] = acc;
+          if (m & 1u) dw[0][v] = fmaf(xv[ii][v], g0, dw[0][v]);
+          if (m & 2u) dw[1][v] = fmaf(xv[ii + 1][v], g0, dw[1][v]);
+          if (m & 4u) dw[2][v] = fmaf(xv[ii + 2][v], g0, dw[2][v]);
+          dw[3][v] = fmaf(xv[ii + 3][v], g0, dw[3][v]);
+          db[v] += g0;
         }
-        *reinterpret_cast<uint32_t*>(dx + (size_t)(r0 + i) * a.d + c) = pack_bf16(o.x, o.y);
       }
-      x0 = x1; x1 = x2; x2 = x3;
-      g0 = g1; g1 = g2; g2 = g3;
+      *reinterpret_cast<uint2*>(dx + (size_t)(r0 + i) * a.d + c) = make_uint2(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]));
     }
   };
   if (!tile_loop<2, BWD_ST>(ntile, smem, issue, compute)) {
@@ -298,9 +341,12 @@ __global__ void __launch_bounds__(NTH, 1) k_conv_bwd_tile(const ConvArgs a, int 
     return;
   }
   if (act) {
-    float* P = a.part + ((size_t)(2 * blockIdx.x + half) * a.d + c) * 5;
-    P[0] = dw[0].x; P[1] = dw[1].x; P[2] = dw[2].x; P[3] = dw[3].x; P[4] = db.x;
-    P[5] = dw[0].y; P[6] = dw[1].y; P[7] = dw[2].y; P[8] = dw[3].y; P[9] = db.y;
+    float* P = a.part + ((size_t)(BRG * blockIdx.x + rg) * a.d + c) * 5;
+#pragma unroll
+    for (int v = 0; v < BV; ++v) {
+      P[5 * v + 0] = dw[0][v]; P[5 * v + 1] = dw[1][v]; P[5 * v + 2] = dw[2][v]; P[5 * v + 3] = dw[3][v];
+      P[5 * v + 4] = db[v];
+    }
   }
 }
 
@@ -314,11 +360,11 @@ int conv_gx(int T, int d) {
 bool conv_tile_ok(const ConvArgs& a, bool bwd) {
   auto al = [](const void* p) { return ((uintptr_t)p & 15) == 0; };
   return a.T > 0 && a.d % 8 == 0 && al(a.x) && al(a.w) && (bwd ? al(a.dxt) && al(a.dx) : al(a.xt)) &&
-         (!a.b || ((uintptr_t)a.b & 3) == 0);
+         (bwd || !a.b || al(a.b));  // the forward reads 8 biases at a time
 }
 
-int conv_tile_parts(int T, int d) { return 2 * conv_gx(T, d); }
-int conv_tile_parts_max(int T) { return 2 * std::max(1, std::min((T + CR - 1) / CR, GX_MAX)); }
+int conv_tile_parts(int T, int d) { return BRG * conv_gx(T, d); }
+int conv_tile_parts_max(int T) { return BRG * std::max(1, std::min((T + CR - 1) / CR, GX_MAX)); }
 
 cudaError_t launch_conv_fwd_tile(const ConvArgs& a, cudaStream_t st) {
   typedef ConvSmem<1, FWD_ST> S;
@@ -327,7 +373,6 @@ cudaError_t launch_conv_fwd_tile(const ConvArgs& a, cudaStream_t st) {
   const int n_rt = (a.T + CR - 1) / CR, n_ct = (a.d + CW - 1) / CW;
   const int gx = std::max(1, std::min(n_rt, std::max(1, sm_count() / n_ct)));
   return launch_pdl(k_conv_fwd_tile, dim3(gx, n_ct), dim3(NTH), S::BYTES, st, a, gx);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_conv_bwd_tile(const ConvArgs& a, int nparts, cudaStream_t st) {
@@ -335,9 +380,8 @@ cudaError_t launch_conv_bwd_tile(const ConvArgs& a, int nparts, cudaStream_t st)
   if (nparts != conv_tile_parts(a.T, a.d)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(k_conv_bwd_tile, cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
   if (e != cudaSuccess) return e;
-  const int gx = nparts / 2, n_ct = (a.d + CW - 1) / CW;
+  const int gx = nparts / BRG, n_ct = (a.d + CW - 1) / CW;
   return launch_pdl(k_conv_bwd_tile, dim3(gx, n_ct), dim3(NTH), S::BYTES, st, a, gx);
-  return cudaGetLastError();
 }
 
 }  // namespace gbla
