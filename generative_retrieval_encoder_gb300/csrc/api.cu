@@ -261,13 +261,21 @@ struct Ctx {
   const int* kerr;   // what the state / conv kernels read: err, or null in the dense form
   cudaStream_t st;
   int pre = 0;       // P holds [phi(q) | phi(k) | v | r] (the bf16 layer)
+  // The error word and counters to clear, when the call's first kernel (the
+  // weight pack) clears them instead of a memset; null once cleared.
+  void* zero = nullptr;
+  size_t zero_bytes = 0;
 };
 
 // The bf16 layer applies the feature map phi = elu + 1 to q and k in the
 // projection epilogue, so the state kernels read phi(q) and phi(k) directly.
 bool layer_pre(const Plan& p, const gbla_shape*) { return !p.f32; }
 
-gbla_status begin(const gbla_shape* s, int op, void* ws, size_t ws_bytes, void* stream, Ctx& c) {
+// zero_in_pack: the caller's first kernel is the weight pack, which then
+// clears the error word and counters (dense batches: no sequence-data check
+// runs before it).
+gbla_status begin(const gbla_shape* s, int op, void* ws, size_t ws_bytes, void* stream, Ctx& c,
+                  bool zero_in_pack = false) {
   gbla_status r = make_plan(s, c.p);
   if (r != GBLA_OK) return r;
   c.l = ws_layout(c.p, op);
@@ -290,7 +298,13 @@ gbla_status begin(const gbla_shape* s, int op, void* ws, size_t ws_bytes, void* 
   // Only the varlen and padded forms have sequence data to check on the
   // device; in the dense form the kernels skip the error-word read.
   c.kerr = p.mode == SEQ_DENSE ? nullptr : c.err;
-  GBLA_CHECK(cudaMemsetAsync(ws, 0, c.l.cnt_b + (size_t)p.n_seq * p.H * 4 - c.l.err, c.st), "memset");
+  const size_t zero_bytes = c.l.cnt_b + (size_t)p.n_seq * p.H * 4 - c.l.err;
+  if (zero_in_pack && p.mode == SEQ_DENSE) {
+    c.zero = at<char>(ws, c.l.err);
+    c.zero_bytes = zero_bytes;
+  } else {
+    GBLA_CHECK(cudaMemsetAsync(at<char>(ws, c.l.err), 0, zero_bytes, c.st), "memset");
+  }
   if (p.mode != SEQ_DENSE) {
     const int ts[2] = {p.chunk, p.tile};
     int32_t* pre[2] = {const_cast<int32_t*>(c.chunks.prefix), const_cast<int32_t*>(c.tiles.prefix)};
@@ -386,7 +400,7 @@ gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* con
     if (q && !aligned16(q)) return GBLA_ERR_INVALID_ARG;
   if (saved && (reinterpret_cast<uintptr_t>(saved) % kAlign) != 0) return GBLA_ERR_INVALID_ARG;
   Ctx c;
-  if ((r = begin(shape, GBLA_OP_FORWARD, ws, ws_bytes, stream, c)) != GBLA_OK) return r;
+  if ((r = begin(shape, GBLA_OP_FORWARD, ws, ws_bytes, stream, c, true)) != GBLA_OK) return r;
   const Plan& p = c.p;
   const Layout& l = c.l;
   void *xt, *P;
@@ -403,15 +417,16 @@ gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* con
     center = at<float>(ws, l.center);
   }
   if (p.f32) center = nullptr;
+  // packed weights first: the pack also clears the error word and counters (dense batches)
+  const void* W[4] = {W_q, W_k, W_v, W_r};
+  void* Wt = at<char>(ws, l.Wt);
+  GBLA_CHECK(launch_pack_weights(W, w_g, p.d, p.H, p.dh, p.f32, Wt, p.NP, c.zero, c.zero_bytes, c.st), "pack");
   // Eq. 4: conv
   ConvArgs ca{};
   ca.x = x; ca.w = conv_w; ca.b = conv_b; ca.xt = xt; ca.T = p.T; ca.d = p.d; ca.seq = c.seq; ca.err = c.kerr; ca.err_out = c.err;
   GBLA_CHECK(launch_conv_fwd(ca, p.f32, c.st), "conv");
   c.pre = layer_pre(p, shape) ? 1 : 0;
   // Eq. 4, 5, 7: projections and gate
-  const void* W[4] = {W_q, W_k, W_v, W_r};
-  void* Wt = at<char>(ws, l.Wt);
-  GBLA_CHECK(launch_pack_weights(W, w_g, p.d, p.H, p.dh, p.f32, Wt, p.NP, c.st), "pack");
   GemmArgs ga{};
   ga.A = xt; ga.lda = p.d; ga.a_kmajor = 1;
   ga.B = Wt; ga.ldb = p.NP; ga.b_kmajor = 0;  // B(n, k) = W_all[k][n]: N-major
@@ -460,7 +475,7 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   if (rms_w && !aligned16(rms_w)) return GBLA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(saved) % kAlign) != 0) return GBLA_ERR_INVALID_ARG;
   Ctx c;
-  if ((r = begin(shape, GBLA_OP_BACKWARD, ws, ws_bytes, stream, c)) != GBLA_OK) return r;
+  if ((r = begin(shape, GBLA_OP_BACKWARD, ws, ws_bytes, stream, c, true)) != GBLA_OK) return r;
   const Plan& p = c.p;
   const Layout& l = c.l;
   const SavedLayout s = saved_layout(p);
@@ -473,7 +488,8 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   const int pre = layer_pre(p, shape) ? 1 : 0;
   // gamma_part and bg_part: every CTA of bwd_q / bwd_kv writes its row (zeros when it has no rows)
   const void* W[4] = {W_q, W_k, W_v, W_r};
-  GBLA_CHECK(launch_pack_weights(W, w_g, p.d, p.H, p.dh, p.f32, at<char>(ws, l.Wp), p.NP, c.st), "pack");
+  GBLA_CHECK(launch_pack_weights(W, w_g, p.d, p.H, p.dh, p.f32, at<char>(ws, l.Wp), p.NP, c.zero, c.zero_bytes, c.st),
+             "pack");
   // Eq. 7 + Eq. 5/6 query side: dr, dq, [dS | dz]
   BwdQArgs q{};
   q.q = P; q.ldq = 4 * p.HD;

@@ -191,9 +191,10 @@ cudaError_t launch_conv_bwd_tile(const ConvArgs& a, int nparts, cudaStream_t st)
 int sm_count();  // of the current device, cached
 
 // Packs W_q | W_k | W_v | W_r | w_g into Wp [d][np] (row-major, zero-padded
-// past 4*H*dh + H columns).
+// past 4*H*dh + H columns); also clears zero_bytes (a multiple of 4) at zero
+// when zero is not null.
 cudaError_t launch_pack_weights(const void* const* W, const void* w_g, int d, int H, int dh,
-                                bool f32, void* Wp, int np, cudaStream_t st);
+                                bool f32, void* Wp, int np, void* zero, size_t zero_bytes, cudaStream_t st);
 
 // out[i] = sum_{s < S} part[s * stride + i] for i < n (fixed order); fp32.
 cudaError_t launch_sum_parts(const float* part, int S, int64_t stride, int64_t n, float* out,

@@ -287,10 +287,13 @@ __global__ void __launch_bounds__(256) k_conv_bwd(const ConvArgs a, int rows_per
 // a vector lies in one block; `vec`: the W_* rows are 16-byte aligned.
 template <typename T>
 __global__ void __launch_bounds__(256) k_pack(const T* Wq, const T* Wk, const T* Wv, const T* Wr, const T* wg,
-                                              int d, int H, int dh, T* Wp, int np, int vec) {
+                                              int d, int H, int dh, T* Wp, int np, int vec, uint32_t* zero,
+                                              int zero_words) {
   pdl_enter();  // the previous kernel's outputs are visible from here on
   constexpr int V = 16 / sizeof(T);
   typedef uint4 U;
+  if (zero && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < zero_words; i += blockDim.x) zero[i] = 0u;
   const int HD = H * dh, npv = np / V;
   const T* Ws[4] = {Wq, Wk, Wv, Wr};
   const long long total = (long long)d * npv;
@@ -404,16 +407,18 @@ cudaError_t launch_conv_bwd(const ConvArgs& a, bool f32, int* nparts, cudaStream
 }
 
 cudaError_t launch_pack_weights(const void* const* W, const void* w_g, int d, int H, int dh, bool f32,
-                                void* Wp, int np, cudaStream_t st) {
+                                void* Wp, int np, void* zero, size_t zero_bytes, cudaStream_t st) {
+  uint32_t* zw = static_cast<uint32_t*>(zero);
+  const int zn = (int)(zero_bytes / 4);
   int vec = 1;
   for (int m = 0; m < 4; ++m) vec &= ((uintptr_t)W[m] & 15) == 0;
   const long long vecs = (long long)d * np / (f32 ? 4 : 8);
   const unsigned grid = (unsigned)std::max(1LL, std::min((vecs + 255) / 256, (long long)sm_count() * 8));
   if (f32)
     return launch_pdl(k_pack<float>, dim3(grid), dim3(256), 0, st, (const float*)W[0], (const float*)W[1],
-                      (const float*)W[2], (const float*)W[3], (const float*)w_g, d, H, dh, (float*)Wp, np, vec);
+                      (const float*)W[2], (const float*)W[3], (const float*)w_g, d, H, dh, (float*)Wp, np, vec, zw, zn);
   return launch_pdl(k_pack<bf16>, dim3(grid), dim3(256), 0, st, (const bf16*)W[0], (const bf16*)W[1],
-                    (const bf16*)W[2], (const bf16*)W[3], (const bf16*)w_g, d, H, dh, (bf16*)Wp, np, vec);
+                    (const bf16*)W[2], (const bf16*)W[3], (const bf16*)w_g, d, H, dh, (bf16*)Wp, np, vec, zw, zn);
 }
 
 cudaError_t launch_sum_parts(const float* part, int S, int64_t stride, int64_t n, float* out, cudaStream_t st) {
