@@ -35,19 +35,19 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # keyed by launch name: (bytes, workload name, sha1 of the kernel's source file when captured).
 # A source change since the capture makes the figure stale: it is then reported as null.
 NCU_TRAFFIC: dict = {
-    "projection gemm": (279593728, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "96c7b224044a"),
-    "dx~ gemm": (328316928, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "96c7b224044a"),
-    "dW gemm": (347562240, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "96c7b224044a"),
-    "bwd_q": (324847360, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "0048d2a17f25"),
-    "readout": (174518528, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "9b2d77f3061f"),
-    "reduce": (144712192, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "9c0148e6206c"),
-    "bwd_kv": (238153984, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "9c0148e6206c"),
-    "conv": (84326656, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "78057339890f"),
-    "conv bwd": (167203328, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "78057339890f"),
+    "projection gemm": (280607232, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "96f0c0d32571"),
+    "dx~ gemm": (328179968, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "96f0c0d32571"),
+    "dW gemm": (347604736, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "96f0c0d32571"),
+    "bwd_q": (317969408, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "f2d22e6ad57a"),
+    "readout": (174654720, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "7678cee3a0a3"),
+    "reduce": (139569152, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "46d7c17b681f"),
+    "bwd_kv": (230499072, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "d831baf25b12"),
+    "conv": (83937536, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "80d3b995dceb"),
+    "conv bwd": (168216576, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "80d3b995dceb"),
 }
 KERNEL_SOURCE = {"projection gemm": "gemm_tc.cu", "dx~ gemm": "gemm_tc.cu", "dW gemm": "gemm_tc.cu",
                  "reduce": "core_bf16.cu", "readout": "readout_tc.cu", "bwd_q": "bwd_q_tc.cu",
-                 "bwd_kv": "core_bf16.cu", "conv": "conv.cu", "conv bwd": "conv.cu",
+                 "bwd_kv": "bwd_kv_tc.cu", "conv": "conv.cu", "conv bwd": "conv.cu",
                  "dW sum": "layer_misc.cu"}
 
 
