@@ -559,12 +559,13 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   ca.T = p.T; ca.d = p.d; ca.seq = c.seq; ca.err = c.kerr; ca.err_out = c.err;
   int nparts = 0;
   GBLA_CHECK(launch_conv_bwd(ca, p.f32, &nparts, c.st), "conv bwd");
+  // the parameter gradients from their partials, one launch: conv taps and bias, gamma, b_g
+  ColsumJobs js{};
   if (dconv_w || dconv_b)
-    GBLA_CHECK(launch_conv_param_grads(ca.part, nparts, p.d, dconv_w, dconv_b, c.st), "conv grads");
-  if (drms_w)
-    GBLA_CHECK(launch_sum_parts(q.gamma_part, gamma_rows, p.dh, p.dh, drms_w, c.st), "dgamma");
-  if (db_g)
-    GBLA_CHECK(launch_sum_parts(kv.bg_part, bg_rows, p.H, p.H, db_g, c.st), "db_g");
+    js.j[js.n++] = ColsumJob{ca.part, nparts, (int64_t)p.d * 5, (int64_t)p.d * 5, (float*)dconv_w, (float*)dconv_b, 1};
+  if (drms_w) js.j[js.n++] = ColsumJob{q.gamma_part, gamma_rows, p.dh, p.dh, (float*)drms_w, nullptr, 0};
+  if (db_g) js.j[js.n++] = ColsumJob{kv.bg_part, bg_rows, p.H, p.H, (float*)db_g, nullptr, 0};
+  GBLA_CHECK(launch_colsums(js, c.st), "param sums");
   return GBLA_OK;
 }
 

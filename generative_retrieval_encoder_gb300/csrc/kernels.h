@@ -196,14 +196,21 @@ int sm_count();  // of the current device, cached
 cudaError_t launch_pack_weights(const void* const* W, const void* w_g, int d, int H, int dh,
                                 bool f32, void* Wp, int np, void* zero, size_t zero_bytes, cudaStream_t st);
 
-// out[i] = sum_{s < S} part[s * stride + i] for i < n (fixed order); fp32.
-cudaError_t launch_sum_parts(const float* part, int S, int64_t stride, int64_t n, float* out,
-                             cudaStream_t st);
+// Fixed-order column sums of partial arrays, up to three in one launch: job
+// j adds rows k = 0 .. S-1 of part[k * stride + i] for i < n; mode 0 writes
+// out[i]; mode 1 (conv parameters, i = 5 c + t) writes t < 4 to out[4 c + t]
+// and t = 4 to out2[c] (either may be null).
+struct ColsumJob {
+  const float* part; int S; int64_t stride, n;
+  float* out; float* out2; int mode;
+};
+struct ColsumJobs {
+  ColsumJob j[3];
+  int n;
+};
+cudaError_t launch_colsums(const ColsumJobs& js, cudaStream_t st);
 // Weight-gradient scatter: dW (fp32 [d][np]) -> dW_q, dW_k, dW_v, dW_r [d][H*dh], dw_g [d][H].
 cudaError_t launch_scatter_dw(const float* part, int S, int d, int np, int H, int dh,
                               float* const* outs, cudaStream_t st);
-// Conv parameter gradients from per-block partials [S][d][5].
-cudaError_t launch_conv_param_grads(const float* part, int S, int d, float* dw, float* db,
-                                    cudaStream_t st);
 
 }  // namespace gbla

@@ -323,26 +323,29 @@ __global__ void __launch_bounds__(256) k_pack(const T* Wq, const T* Wk, const T*
 // columns 32 b .. 32 b + 31; warp w adds rows w, w + 32, w + 64, ... (lanes
 // read 32 consecutive floats); then warp 0 adds the 32 warp sums in order.
 // mode 0: out[i];  mode 1 (conv parameters, i = 5 c + t): t < 4 -> out[4 c + t], else out2[c].
-__global__ void __launch_bounds__(1024) k_colsum(const float* part, int S, int64_t stride, int64_t n, float* out,
-                                                 float* out2, int mode) {
+__global__ void __launch_bounds__(1024) k_colsum(const ColsumJobs js) {
   pdl_enter();  // the previous kernel's outputs are visible from here on
   __shared__ float red[32][33];
+  // this block's job: the jobs' column blocks are laid out one after another
+  int jb = blockIdx.x, j = 0;
+  while (j + 1 < js.n && jb >= (int)((js.j[j].n + 31) / 32)) jb -= (int)((js.j[j++].n + 31) / 32);
+  const ColsumJob& J = js.j[j];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t i = (int64_t)blockIdx.x * 32 + lane;
+  const int64_t i = (int64_t)jb * 32 + lane;
   float s = 0.f;
-  if (i < n)
-    for (int k = warp; k < S; k += 32) s += part[(int64_t)k * stride + i];
+  if (i < J.n)
+    for (int k = warp; k < J.S; k += 32) s += J.part[(int64_t)k * J.stride + i];
   red[warp][lane] = s;
   __syncthreads();
-  if (warp == 0 && i < n) {
+  if (warp == 0 && i < J.n) {
     float t = 0.f;
     for (int w = 0; w < 32; ++w) t += red[w][lane];
-    if (mode == 0) {
-      out[i] = t;
+    if (J.mode == 0) {
+      J.out[i] = t;
     } else {
       const int64_t c = i / 5, q = i % 5;
-      if (q < 4) { if (out) out[c * 4 + q] = t; }
-      else if (out2) out2[c] = t;
+      if (q < 4) { if (J.out) J.out[c * 4 + q] = t; }
+      else if (J.out2) J.out2[c] = t;
     }
   }
 }
@@ -421,9 +424,11 @@ cudaError_t launch_pack_weights(const void* const* W, const void* w_g, int d, in
                     (const bf16*)W[2], (const bf16*)W[3], (const bf16*)w_g, d, H, dh, (bf16*)Wp, np, vec, zw, zn);
 }
 
-cudaError_t launch_sum_parts(const float* part, int S, int64_t stride, int64_t n, float* out, cudaStream_t st) {
-  return launch_pdl(k_colsum, dim3((unsigned)((n + 31) / 32)), dim3(1024), 0, st, part, S, stride, n, out,
-                    (float*)nullptr, 0);
+cudaError_t launch_colsums(const ColsumJobs& js, cudaStream_t st) {
+  int blocks = 0;
+  for (int j = 0; j < js.n; ++j) blocks += (int)((js.j[j].n + 31) / 32);
+  if (js.n <= 0 || blocks <= 0) return cudaSuccess;
+  return launch_pdl(k_colsum, dim3((unsigned)blocks), dim3(1024), 0, st, js);
 }
 
 cudaError_t launch_scatter_dw(const float* part, int S, int d, int np, int H, int dh, float* const* outs,
@@ -432,9 +437,5 @@ cudaError_t launch_scatter_dw(const float* part, int S, int d, int np, int H, in
                     outs[1], outs[2], outs[3], outs[4]);
 }
 
-cudaError_t launch_conv_param_grads(const float* part, int S, int d, float* dw, float* db, cudaStream_t st) {
-  return launch_pdl(k_colsum, dim3((unsigned)((d * 5 + 31) / 32)), dim3(1024), 0, st, part, S, (int64_t)d * 5,
-                    (int64_t)d * 5, dw, db, 1);
-}
 
 }  // namespace gbla
