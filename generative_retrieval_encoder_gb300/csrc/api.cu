@@ -551,21 +551,23 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   g2.M = p.d; g2.N = p.N1; g2.K = p.T; g2.k_split = p.wsplit; g2.epi = EPI_SPLITK; g2.io_f32 = p.f32; g2.err = c.err;
   g2.pair = 1;  // long K: the operand feed limits, CTA pairs halve it per SM
   GBLA_CHECK(launch_gemm(g2, c.st), "dW gemm");
-  float* outs[5] = {dW_q, dW_k, dW_v, dW_r, dw_g};
-  GBLA_CHECK(launch_scatter_dw(at<float>(ws, l.dW), p.n_wsplit, p.d, p.NP, p.H, p.dh, outs, c.st), "dW sum");
+
   // Eq. 4 conv backward
   ConvArgs ca{};
   ca.x = x; ca.w = conv_w; ca.dxt = at<char>(ws, l.dxt); ca.dx = dx; ca.part = at<float>(ws, l.conv_part);
   ca.T = p.T; ca.d = p.d; ca.seq = c.seq; ca.err = c.kerr; ca.err_out = c.err;
   int nparts = 0;
   GBLA_CHECK(launch_conv_bwd(ca, p.f32, &nparts, c.st), "conv bwd");
-  // the parameter gradients from their partials, one launch: conv taps and bias, gamma, b_g
+  // the parameter gradients from their partials, one launch: W_all, conv taps and bias, gamma, b_g
   ColsumJobs js{};
+  js.sc.part = at<float>(ws, l.dW);  // and the split-K sum of the weight gradient
+  js.sc.S = p.n_wsplit; js.sc.d = p.d; js.sc.np = p.NP; js.sc.H = p.H; js.sc.dh = p.dh;
+  js.sc.out[0] = dW_q; js.sc.out[1] = dW_k; js.sc.out[2] = dW_v; js.sc.out[3] = dW_r; js.sc.out[4] = dw_g;
   if (dconv_w || dconv_b)
     js.j[js.n++] = ColsumJob{ca.part, nparts, (int64_t)p.d * 5, (int64_t)p.d * 5, (float*)dconv_w, (float*)dconv_b, 1};
   if (drms_w) js.j[js.n++] = ColsumJob{q.gamma_part, gamma_rows, p.dh, p.dh, (float*)drms_w, nullptr, 0};
   if (db_g) js.j[js.n++] = ColsumJob{kv.bg_part, bg_rows, p.H, p.H, (float*)db_g, nullptr, 0};
-  GBLA_CHECK(launch_colsums(js, c.st), "param sums");
+  GBLA_CHECK(launch_colsums(js, c.st), "param grads");
   return GBLA_OK;
 }
 

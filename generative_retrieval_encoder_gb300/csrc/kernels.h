@@ -204,13 +204,19 @@ struct ColsumJob {
   const float* part; int S; int64_t stride, n;
   float* out; float* out2; int mode;
 };
+// The split-K sum of the weight gradient: part [S][d][np] fp32 -> dW_q, dW_k,
+// dW_v, dW_r [d][H*dh] and dw_g [d][H] (out[m] may be null); fixed order.
+struct ScatterJob {
+  const float* part; int S, d, np, H, dh;
+  float* out[5];
+  int blocks;  // set by launch_colsums
+};
 struct ColsumJobs {
   ColsumJob j[3];
   int n;
+  ScatterJob sc;  // part == null: none
 };
-cudaError_t launch_colsums(const ColsumJobs& js, cudaStream_t st);
-// Weight-gradient scatter: dW (fp32 [d][np]) -> dW_q, dW_k, dW_v, dW_r [d][H*dh], dw_g [d][H].
-cudaError_t launch_scatter_dw(const float* part, int S, int d, int np, int H, int dh,
-                              float* const* outs, cudaStream_t st);
+// The scatter job (if any) and the column sums in one launch.
+cudaError_t launch_colsums(ColsumJobs js, cudaStream_t st);
 
 }  // namespace gbla

@@ -326,8 +326,25 @@ __global__ void __launch_bounds__(256) k_pack(const T* Wq, const T* Wk, const T*
 __global__ void __launch_bounds__(1024) k_colsum(const ColsumJobs js) {
   pdl_enter();  // the previous kernel's outputs are visible from here on
   __shared__ float red[32][33];
+  if ((int)blockIdx.x < js.sc.blocks) {  // the split-K sum of dW into its five outputs
+    const ScatterJob& X = js.sc;
+    const int HD = X.H * X.dh;
+    const size_t total = (size_t)X.d * X.np;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)X.blocks * blockDim.x) {
+      const int c = (int)(i / X.np), n = (int)(i % X.np);
+      if (n >= 4 * HD + X.H) continue;
+      float s = 0.f;
+      for (int k = 0; k < X.S; ++k) s += X.part[(size_t)k * total + i];
+      if (n < 4 * HD) {
+        if (X.out[n / HD]) X.out[n / HD][(size_t)c * HD + n % HD] = s;
+      } else if (X.out[4]) {
+        X.out[4][(size_t)c * X.H + n - 4 * HD] = s;
+      }
+    }
+    return;
+  }
   // this block's job: the jobs' column blocks are laid out one after another
-  int jb = blockIdx.x, j = 0;
+  int jb = blockIdx.x - js.sc.blocks, j = 0;
   while (j + 1 < js.n && jb >= (int)((js.j[j].n + 31) / 32)) jb -= (int)((js.j[j++].n + 31) / 32);
   const ColsumJob& J = js.j[j];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -350,24 +367,6 @@ __global__ void __launch_bounds__(1024) k_colsum(const ColsumJobs js) {
   }
 }
 
-__global__ void k_scatter_dw(const float* part, int S, int d, int np, int H, int dh, float* o0, float* o1,
-                             float* o2, float* o3, float* o4) {
-  pdl_enter();  // the previous kernel's outputs are visible from here on
-  const int HD = H * dh;
-  float* outs[4] = {o0, o1, o2, o3};
-  const size_t total = (size_t)d * np;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-    const int c = (int)(i / np), n = (int)(i % np);
-    if (n >= 4 * HD + H) continue;
-    float s = 0.f;
-    for (int k = 0; k < S; ++k) s += part[(size_t)k * total + i];
-    if (n < 4 * HD) {
-      if (outs[n / HD]) outs[n / HD][(size_t)c * HD + n % HD] = s;
-    } else if (o4) {
-      o4[(size_t)c * H + n - 4 * HD] = s;
-    }
-  }
-}
 
 int grid_for(size_t n) { const size_t g = (n + 255) / 256; return (int)(g < 2432 ? (g > 0 ? g : 1) : 2432); }
 
@@ -424,18 +423,18 @@ cudaError_t launch_pack_weights(const void* const* W, const void* w_g, int d, in
                     (const bf16*)W[2], (const bf16*)W[3], (const bf16*)w_g, d, H, dh, (bf16*)Wp, np, vec, zw, zn);
 }
 
-cudaError_t launch_colsums(const ColsumJobs& js, cudaStream_t st) {
-  int blocks = 0;
+cudaError_t launch_colsums(ColsumJobs js, cudaStream_t st) {
+  js.sc.blocks = 0;
+  if (js.sc.part) {
+    const size_t n = (size_t)js.sc.d * js.sc.np;
+    js.sc.blocks = (int)std::min<size_t>((n + 1023) / 1024, (size_t)sm_count() * 2);
+  }
+  int blocks = js.sc.blocks;
   for (int j = 0; j < js.n; ++j) blocks += (int)((js.j[j].n + 31) / 32);
-  if (js.n <= 0 || blocks <= 0) return cudaSuccess;
+  if (blocks <= 0) return cudaSuccess;
   return launch_pdl(k_colsum, dim3((unsigned)blocks), dim3(1024), 0, st, js);
 }
 
-cudaError_t launch_scatter_dw(const float* part, int S, int d, int np, int H, int dh, float* const* outs,
-                              cudaStream_t st) {
-  return launch_pdl(k_scatter_dw, dim3(grid_for((size_t)d * np)), dim3(256), 0, st, part, S, d, np, H, dh, outs[0],
-                    outs[1], outs[2], outs[3], outs[4]);
-}
 
 
 }  // namespace gbla
