@@ -249,7 +249,9 @@ __global__ void __launch_bounds__(NTH, 1)
         const bool valid = rel < x.nval, store = rel < x.nrows;
         mbar_wait(ACCF(grp), (j / NG) & 1, fail);
         tc_fence_after();
-        // den = z . phi(q) from the row's phi(q) in shared memory
+        // O' columns 0..31 load under den = z . phi(q) (the row's phi(q) in shared memory)
+        uint32_t o0[32], o1[32];
+        tmem_ld32_async(tl, o0);
         float den = 0.f;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -260,19 +262,23 @@ __global__ void __launch_bounds__(NTH, 1)
         }
         const float inv = valid ? 1.f / den : 0.f;
         const float cv = valid ? 1.f : 0.f;
-        // o = O'/den + c and its sum of squares, 32 columns at a time
+        tmem_wait32(o0);
+        tmem_ld32_async(tl + 32, o1);  // columns 32..63 under the first half's sums
+        // o = O'/den + c and its sum of squares
         float ss = 0.f;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t o[32];
-          tmem_ld32(tl + 32 * hh, o);
+        for (int f = 0; f < 32; ++f) {
+          const float v = fmaf(__uint_as_float(o0[f]), inv, cv * cb[f]);
+          ss = fmaf(v, v, ss);
+        }
+        tmem_wait32(o1);
 #pragma unroll
-          for (int f = 0; f < 32; ++f) {
-            const float v = fmaf(__uint_as_float(o[f]), inv, cv * cb[32 * hh + f]);
-            ss = fmaf(v, v, ss);
-          }
+        for (int f = 0; f < 32; ++f) {
+          const float v = fmaf(__uint_as_float(o1[f]), inv, cv * cb[32 + f]);
+          ss = fmaf(v, v, ss);
         }
         const float rs = rsqrtf(ss * (1.f / RD) + a.eps);
+        // y = RMSNorm(o) * gamma * SiLU(r); O' is read again, 32 columns at a time
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t o[32];
