@@ -250,10 +250,14 @@ __global__ void __launch_bounds__(NTH, 1)
         tc_fence_after();
         // dk~ = D1 + dz'', dg = phi(k) . dk~, dk = g dk~ min(1, phi(k)) -> the phi(k) row
         float dg = 0.f;
+        uint32_t ob[2][32];
+        tmem_ld32_async(tl, ob[0]);
+        tmem_wait32(ob[0]);
+        tmem_ld32_async(tl + 32, ob[1]);  // D1 columns 32..63 under the first half
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          uint32_t o[32];
-          tmem_ld32(tl + 32 * hh, o);
+          const uint32_t* o = ob[hh];
+          if (hh == 1) tmem_wait32(ob[1]);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             float kv[8];
@@ -271,11 +275,14 @@ __global__ void __launch_bounds__(NTH, 1)
           }
         }
         // dv = g D2 -> the v row
+        tmem_ld32_async(tl + KD, ob[0]);
+        tmem_wait32(ob[0]);
+        tmem_ld32_async(tl + KD + 32, ob[1]);  // D2 columns 32..63 under the first half
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          uint32_t o[32];
-          tmem_ld32(tl + KD + 32 * hh, o);
+          const uint32_t* o = ob[hh];
           if (hh == 1) {  // the accumulators are read: hand them back
+            tmem_wait32(ob[1]);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(ACCE(grp));
