@@ -39,9 +39,9 @@ NCU_TRAFFIC: dict = {
     "dx~ gemm": (328179968, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "96f0c0d32571"),
     "dW gemm": (347604736, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "96f0c0d32571"),
     "bwd_q": (317969408, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "f2d22e6ad57a"),
-    "readout": (174654720, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "7678cee3a0a3"),
+    "readout": (171571712, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "6f790bb002a8"),
     "reduce": (139569152, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "46d7c17b681f"),
-    "bwd_kv": (230499072, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "d831baf25b12"),
+    "bwd_kv": (230319104, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "78f218ea5b14"),
     "conv": (83937536, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "80d3b995dceb"),
     "conv bwd": (168216576, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "80d3b995dceb"),
 }
