@@ -51,8 +51,13 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t a, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
   return r;
 }
+// Arrival on an mbarrier of another CTA of the cluster, with the default
+// (CTA-scope release) semantics: it publishes no global data, so it need not
+// wait for this thread's outstanding global stores as a cluster-scope release
+// would.  Ordering of tcgen05 operations across the arrival comes from the
+// tcgen05 fences on either side.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
