@@ -316,11 +316,22 @@ gbla_status begin(const gbla_shape* s, int op, void* ws, size_t ws_bytes, void* 
 // State reduction + combine.  The bf16 path centres the state on the
 // k~-weighted mean of v (center); the fp32 path keeps it uncentred.
 // The layer's bf16 readout: the tcgen05 kernel where it applies.
-cudaError_t launch_readout_layer_bf16(const ReadoutArgs& ra, int n_tiles, cudaStream_t st) {
+// The mma.sync readout loads a (sequence, head) state per CTA: it takes a
+// chunk of rows (up to 2048) per CTA, not a tile, so that the load is spread
+// over more rows.  Every row is written by its own index, whatever the tiling.
+cudaError_t launch_readout_chunks_bf16(const ReadoutArgs& ra, bool norm, const Tiling& chunks, int n_chunks,
+                                       cudaStream_t st) {
+  ReadoutArgs rc = ra;
+  rc.tiles = chunks;
+  return launch_readout_bf16(rc, norm, n_chunks, st);
+}
+
+cudaError_t launch_readout_layer_bf16(const ReadoutArgs& ra, int n_tiles, const Tiling& chunks, int n_chunks,
+                                      cudaStream_t st) {
   const cudaError_t e = launch_readout_tc(ra, n_tiles, st);
   if (e != cudaErrorNotSupported) return e;
   (void)cudaGetLastError();
-  return launch_readout_bf16(ra, true, n_tiles, st);
+  return launch_readout_chunks_bf16(ra, true, chunks, n_chunks, st);
 }
 
 // The layer's bf16 key-side backward: the tcgen05 kernel where it applies;
@@ -454,7 +465,7 @@ gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* con
   ra.out = y; ra.ldo = p.HD; ra.den = nullptr;
   ra.rsinv = (saved && !p.f32) ? at<float>(saved, saved_layout(p).rsinv) : nullptr;
   ra.H = p.H; ra.dh = p.dh; ra.seq = c.seq; ra.tiles = c.tiles; ra.err = c.kerr; ra.err_out = c.err;
-  GBLA_CHECK(p.f32 ? launch_readout_f32(ra, true, p.n_tiles, c.st) : launch_readout_layer_bf16(ra, p.n_tiles, c.st),
+  GBLA_CHECK(p.f32 ? launch_readout_f32(ra, true, p.n_tiles, c.st) : launch_readout_layer_bf16(ra, p.n_tiles, c.chunks, p.n_chunks, c.st),
              "readout");
   return GBLA_OK;
 }
@@ -591,7 +602,7 @@ gbla_status bla_core_forward(const gbla_shape* shape, const void* q, const void*
   ra.state = st; ra.state_bf = sbf; ra.center = center;
   ra.out = o; ra.ldo = p.HD; ra.den = den;
   ra.H = p.H; ra.dh = p.dh; ra.seq = c.seq; ra.tiles = c.tiles; ra.err = c.kerr;
-  GBLA_CHECK(p.f32 ? launch_readout_f32(ra, false, p.n_tiles, c.st) : launch_readout_bf16(ra, false, p.n_tiles, c.st),
+  GBLA_CHECK(p.f32 ? launch_readout_f32(ra, false, p.n_tiles, c.st) : launch_readout_chunks_bf16(ra, false, c.chunks, p.n_chunks, c.st),
              "readout");
   return GBLA_OK;
 }
