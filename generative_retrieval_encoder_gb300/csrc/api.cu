@@ -197,7 +197,8 @@ Layout ws_layout(const Plan& p, int op) {
     l.dstate = c.take(state_bytes(p));
     l.dstate_bf = c.take(state_bf_bytes(p));
     l.gamma_part = c.take((size_t)std::max(p.n_chunks * p.H, kMaxGrid) * p.dh * 4);
-    l.bg_part = c.take((size_t)p.n_tiles * 2 * p.H * 4);  // up to two partial rows per tile
+    // db_g partial rows: two per tile (tcgen05 kernel) or one per chunk
+    l.bg_part = c.take((size_t)std::max(2 * p.n_tiles, p.n_chunks) * p.H * 4);
     l.conv_part = c.take((size_t)p.conv_blocks * p.d * 5 * 4);
   } else {  // core forward / backward
     l.state = c.take(state_bytes(p));
@@ -336,12 +337,22 @@ cudaError_t launch_readout_layer_bf16(const ReadoutArgs& ra, int n_tiles, const 
 
 // The layer's bf16 key-side backward: the tcgen05 kernel where it applies;
 // *bg_rows = the rows of db_g partials written.
-cudaError_t launch_bwd_kv_layer_bf16(const BwdKVArgs& kv, int n_tiles, int* bg_rows, cudaStream_t st) {
+// The mma.sync key-side backward, like the readout, takes a chunk of rows per
+// CTA (one load of [dS | dz] for up to 2048 rows).  Its db_g partials are one
+// row per CTA: n_chunks <= 2 n_tiles rows, which the partial buffer holds.
+cudaError_t launch_bwd_kv_chunks_bf16(const BwdKVArgs& kv, const Tiling& chunks, int n_chunks, cudaStream_t st) {
+  BwdKVArgs kc = kv;
+  kc.tiles = chunks;
+  return launch_bwd_kv_bf16(kc, n_chunks, st);
+}
+
+cudaError_t launch_bwd_kv_layer_bf16(const BwdKVArgs& kv, int n_tiles, const Tiling& chunks, int n_chunks,
+                                     int* bg_rows, cudaStream_t st) {
   const cudaError_t e = launch_bwd_kv_tc(kv, n_tiles, bg_rows, st);
   if (e != cudaErrorNotSupported) return e;
   (void)cudaGetLastError();
-  *bg_rows = n_tiles;
-  return launch_bwd_kv_bf16(kv, n_tiles, st);
+  *bg_rows = n_chunks;
+  return launch_bwd_kv_chunks_bf16(kv, chunks, n_chunks, st);
 }
 
 // The layer's bf16 query-side backward: the tcgen05 kernel where it applies.
@@ -542,7 +553,7 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   kv.bg_part = at<float>(ws, l.bg_part);
   kv.H = p.H; kv.dh = p.dh; kv.seq = c.seq; kv.tiles = c.tiles; kv.err = c.kerr; kv.err_out = c.err;
   int bg_rows = p.n_tiles;
-  GBLA_CHECK(p.f32 ? launch_bwd_kv_f32(kv, p.n_tiles, c.st) : launch_bwd_kv_layer_bf16(kv, p.n_tiles, &bg_rows, c.st),
+  GBLA_CHECK(p.f32 ? launch_bwd_kv_f32(kv, p.n_tiles, c.st) : launch_bwd_kv_layer_bf16(kv, p.n_tiles, c.chunks, p.n_chunks, &bg_rows, c.st),
              "bwd_kv");
   // Eq. 4 projections backward: dx~ = dP W_all^T, dW_all = x~^T dP
   GemmArgs g1{};
@@ -637,7 +648,8 @@ gbla_status bla_core_backward(const gbla_shape* shape, const void* q, const void
   kv.dk = dk; kv.lddk = p.HD; kv.dv = dv; kv.lddv = p.HD;
   kv.ds = dg; kv.ldds = p.H; kv.gate_grad = GG_DG;
   kv.H = p.H; kv.dh = p.dh; kv.seq = c.seq; kv.tiles = c.tiles; kv.err = c.kerr;
-  GBLA_CHECK(p.f32 ? launch_bwd_kv_f32(kv, p.n_tiles, c.st) : launch_bwd_kv_bf16(kv, p.n_tiles, c.st), "bwd_kv");
+  GBLA_CHECK(p.f32 ? launch_bwd_kv_f32(kv, p.n_tiles, c.st) : launch_bwd_kv_chunks_bf16(kv, c.chunks, p.n_chunks, c.st),
+             "bwd_kv");
   return GBLA_OK;
 }
 
