@@ -392,7 +392,11 @@ struct BqCfg {
   static constexpr int STAGES = DH == 128 ? 1 : 2;
   static constexpr int TILE = TT * DH * 2;
   static constexpr int NIN = NORM ? 3 : 2;  // q, dy|d_o, [r]
-  static constexpr int SMEM = DH * Cfg<DH>::SPAD * 2 + TT * Cfg<DH>::SPAD * 2 + STAGES * NIN * TILE;
+  // d_h = 128: each thread's dgamma sums (d_h / 4 floats) live in shared
+  // memory, [slot][thread], to keep registers for the accumulators
+  static constexpr bool GSM = NORM && DH == 128;
+  static constexpr int GSM_BYTES = GSM ? NW * 32 * (DH / 4) * 4 : 0;
+  static constexpr int SMEM = DH * Cfg<DH>::SPAD * 2 + TT * Cfg<DH>::SPAD * 2 + STAGES * NIN * TILE + GSM_BYTES;
 };
 
 template <int DH, bool NORM, bool PRE>
@@ -451,9 +455,15 @@ __global__ void __launch_bounds__(BqCfg<DH, NORM>::NW * 32) k_bwd_q_bf16(const B
     s_gam[f] = (NORM && a.rms_w) ? __bfloat162float(((const bf16*)a.rms_w)[f]) : 1.f;
     s_cen[f] = (NORM && a.center) ? a.center[(size_t)(b * H + h) * DH + f] : 0.f;
   }
-  float gacc[DH / 8][2];
+  float gacc[R::GSM ? 1 : DH / 8][2];
+  float* gsm = reinterpret_cast<float*>(tiles + R::STAGES * R::NIN * R::TILE) + tid;  // slot j at gsm[j * NTHR]
+  if (R::GSM) {
 #pragma unroll
-  for (int nt = 0; nt < DH / 8; ++nt) gacc[nt][0] = gacc[nt][1] = 0.f;
+    for (int j = 0; j < DH / 4; ++j) gsm[j * NTHR] = 0.f;
+  } else {
+#pragma unroll
+    for (int nt = 0; nt < DH / 8; ++nt) gacc[nt][0] = gacc[nt][1] = 0.f;
+  }
   float accS[C::NT][4];
 #pragma unroll
   for (int i = 0; i < C::NT; ++i) accS[i][0] = accS[i][1] = accS[i][2] = accS[i][3] = 0.f;
@@ -535,7 +545,7 @@ __global__ void __launch_bounds__(BqCfg<DH, NORM>::NW * 32) k_bwd_q_bf16(const B
         const uint32_t yv1 = *reinterpret_cast<const uint32_t*>(ytb + o1);
         const float rv[4] = {bf_lo(rv0), bf_hi(rv0), bf_lo(rv1), bf_hi(rv1)};
         const float yv[4] = {bf_lo(yv0), bf_hi(yv0), bf_lo(yv1), bf_hi(yv1)};
-        float dr[4];
+        float dr[4], gd[2] = {0.f, 0.f};
         const float2 gm2 = *reinterpret_cast<const float2*>(s_gam + nt * 8 + 2 * t4);
         const float2 ce2 = *reinterpret_cast<const float2*>(s_cen + nt * 8 + 2 * t4);
 #pragma unroll
@@ -544,10 +554,17 @@ __global__ void __launch_bounds__(BqCfg<DH, NORM>::NW * 32) k_bwd_q_bf16(const B
           const float sg = 1.f / (1.f + __expf(-rv[q]));
           const float av = rv[q] * sg;
           const float u = (acc[nt][q] + cv[q] * ((q & 1) ? ce2.y : ce2.x)) * rsv[q];
-          gacc[nt][q & 1] += yv[q] * u * av;
+          gd[q & 1] += yv[q] * u * av;
           dr[q] = cv[q] * yv[q] * u * gm * sg * (1.f + rv[q] * (1.f - sg));
           dO[nt][q] = yv[q] * gm * av;  // du
           if (q < 2) m0 += dO[nt][q] * u; else m1 += dO[nt][q] * u;
+        }
+        if (R::GSM) {
+          gsm[(2 * nt) * NTHR] += gd[0];
+          gsm[(2 * nt + 1) * NTHR] += gd[1];
+        } else {
+          gacc[R::GSM ? 0 : nt][0] += gd[0];
+          gacc[R::GSM ? 0 : nt][1] += gd[1];
         }
         // stage dr into this warp's r rows (consumed)
         *reinterpret_cast<uint32_t*>(rtb + o0) = pack_bf16(dr[0], dr[1]);
@@ -679,7 +696,7 @@ __global__ void __launch_bounds__(BqCfg<DH, NORM>::NW * 32) k_bwd_q_bf16(const B
     for (int nt = 0; nt < DH / 8; ++nt)
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        float v = gacc[nt][q];
+        float v = R::GSM ? gsm[(2 * nt + q) * NTHR] : gacc[R::GSM ? 0 : nt][q];
         v += __shfl_xor_sync(FULL, v, 4);
         v += __shfl_xor_sync(FULL, v, 8);
         v += __shfl_xor_sync(FULL, v, 16);
