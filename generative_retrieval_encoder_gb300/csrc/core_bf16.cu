@@ -72,8 +72,10 @@ struct RedCfg {
   static constexpr int SMEM = STAGES * (2 * TILE + TT * 4);
 };
 
+// Resident CTAs per SM as their shared memory allows: three up to d_h = 64,
+// two at d_h = 128 (at most 128 registers a thread; 129 left room for one).
 template <int DH, bool PRE>
-__global__ void __launch_bounds__(256) k_reduce_bf16(const ReduceArgs a) {
+__global__ void __launch_bounds__(256, DH == 128 ? 2 : 3) k_reduce_bf16(const ReduceArgs a) {
   pdl_enter();  // the previous kernel's outputs are visible from here on
   using C = Cfg<DH>;
   using R = RedCfg<DH>;
