@@ -48,7 +48,7 @@ NCU_TRAFFIC: dict = {
 KERNEL_SOURCE = {"projection gemm": "gemm_tc.cu", "dx~ gemm": "gemm_tc.cu", "dW gemm": "gemm_tc.cu",
                  "reduce": "core_bf16.cu", "readout": "readout_tc.cu", "bwd_q": "bwd_q_tc.cu",
                  "bwd_kv": "bwd_kv_tc.cu", "conv": "conv.cu", "conv bwd": "conv.cu",
-                 "dW sum": "layer_misc.cu"}
+                 "param grads": "layer_misc.cu"}
 
 
 def source_sha(name: str) -> str | None:
