@@ -476,7 +476,8 @@ gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* con
   ra.out = y; ra.ldo = p.HD; ra.den = nullptr;
   ra.rsinv = (saved && !p.f32) ? at<float>(saved, saved_layout(p).rsinv) : nullptr;
   ra.H = p.H; ra.dh = p.dh; ra.seq = c.seq; ra.tiles = c.tiles; ra.err = c.kerr; ra.err_out = c.err;
-  GBLA_CHECK(p.f32 ? launch_readout_f32(ra, true, p.n_tiles, c.st) : launch_readout_layer_bf16(ra, p.n_tiles, c.chunks, p.n_chunks, c.st),
+  GBLA_CHECK(p.f32 ? launch_readout_f32(ra, true, p.n_tiles, c.st)
+                   : launch_readout_layer_bf16(ra, p.n_tiles, c.chunks, p.n_chunks, c.st),
              "readout");
   return GBLA_OK;
 }
@@ -553,7 +554,8 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   kv.bg_part = at<float>(ws, l.bg_part);
   kv.H = p.H; kv.dh = p.dh; kv.seq = c.seq; kv.tiles = c.tiles; kv.err = c.kerr; kv.err_out = c.err;
   int bg_rows = p.n_tiles;
-  GBLA_CHECK(p.f32 ? launch_bwd_kv_f32(kv, p.n_tiles, c.st) : launch_bwd_kv_layer_bf16(kv, p.n_tiles, c.chunks, p.n_chunks, &bg_rows, c.st),
+  GBLA_CHECK(p.f32 ? launch_bwd_kv_f32(kv, p.n_tiles, c.st)
+                   : launch_bwd_kv_layer_bf16(kv, p.n_tiles, c.chunks, p.n_chunks, &bg_rows, c.st),
              "bwd_kv");
   // Eq. 4 projections backward: dx~ = dP W_all^T, dW_all = x~^T dP
   GemmArgs g1{};
@@ -613,7 +615,8 @@ gbla_status bla_core_forward(const gbla_shape* shape, const void* q, const void*
   ra.state = st; ra.state_bf = sbf; ra.center = center;
   ra.out = o; ra.ldo = p.HD; ra.den = den;
   ra.H = p.H; ra.dh = p.dh; ra.seq = c.seq; ra.tiles = c.tiles; ra.err = c.kerr;
-  GBLA_CHECK(p.f32 ? launch_readout_f32(ra, false, p.n_tiles, c.st) : launch_readout_chunks_bf16(ra, false, c.chunks, p.n_chunks, c.st),
+  GBLA_CHECK(p.f32 ? launch_readout_f32(ra, false, p.n_tiles, c.st)
+                   : launch_readout_chunks_bf16(ra, false, c.chunks, p.n_chunks, c.st),
              "readout");
   return GBLA_OK;
 }
