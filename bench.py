@@ -252,6 +252,23 @@ def l_scaling(wl, dev, timed, tokens: int = 262144, steps: int = 3):
     return out
 
 
+def rank_max(v: float, world: int, device) -> float:
+    """The largest v over the ranks: a job's time is that of its slowest rank."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: the units every rank processed (replicas of the
+    same per-GPU work) over the slowest rank's time in milliseconds."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 def run_ours(args, wl, rank: int, world: int, local_rank: int):
     import torch
     import torch.distributed as dist
@@ -303,11 +320,7 @@ def run_ours(args, wl, rank: int, world: int, local_rank: int):
         torch.cuda.synchronize()
 
     def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return rank_max(v, world, dev)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -418,15 +431,15 @@ def run_ours(args, wl, rank: int, world: int, local_rank: int):
         v, cores, sample, el = cpu_baseline(wl)
         cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
                "seconds": round(el, 1)}
-    line = {"metric": METRIC, "value": tokens * world / (ms_step * 1e-3), "unit": "tokens/s", "n_gpus": world,
+    line = {"metric": METRIC, "value": job_rate(tokens, world, ms_step), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
             "config": {"workload": wl.name, "step": "forward+backward", "tokens_per_gpu": tokens,
                        "l2": "flushed between timed steps (write of 2x L2 outside the events)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "fwd_tokens_per_s": tokens * world / (ms_fwd * 1e-3), "ms_fwd": ms_fwd,
+            "fwd_tokens_per_s": job_rate(tokens, world, ms_fwd), "ms_fwd": ms_fwd,
             "roofline": roof, "kernels": per_kernel, "cpu_baseline": cpu,
-            "e2e": {"value": tokens * world / (ms_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": job_rate(tokens, world, ms_e2e), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
                     "pipeline": "step k+1's H2D on a second stream under step k's compute"},
             "gpu_launches": launches_per_step * args.steps,
