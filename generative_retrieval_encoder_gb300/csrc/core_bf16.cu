@@ -231,8 +231,10 @@ __device__ __forceinline__ void load_center_cols(const float* center, int seqh, 
 }
 
 // =====================================================================
-// readout: per (row tile, head) CTA, 4 warps x 16 rows per 64-row sub-tile,
-// double-buffered.  o = phi(q) [S | z] with the division in the epilogue.
+// readout: per (row range of `tiles`, head) CTA -- the library passes its
+// chunks (up to 2048 rows), so that one load of the state serves them all --
+// 4 warps x 16 rows per 64-row sub-tile, double-buffered.  o = phi(q) [S | z]
+// with the division in the epilogue.
 // =====================================================================
 template <int DH, bool NORM>
 struct RdCfg {
@@ -751,7 +753,8 @@ __global__ void __launch_bounds__(BqCfg<DH, NORM>::NW * 32) k_bwd_q_bf16(const B
 }
 
 // =====================================================================
-// bwd_kv: per (row tile, head) CTA, 4 warps x 16 rows per 64-row sub-tile.
+// bwd_kv: per (row range of `tiles`, head) CTA (the library passes its
+// chunks, as for the readout), 4 warps x 16 rows per 64-row sub-tile.
 // =====================================================================
 template <int DH>
 struct BkvCfg {

@@ -4,8 +4,9 @@
 // Persistent and warp-specialised: one CTA per SM walks a static list of
 // 128 x 256 output tiles (x K splits).
 //   warp 0 (one lane)  TMA producer: cp.async.bulk.tensor loads (128-byte
-//                      swizzle) into a 4-stage shared-memory ring (full/empty
-//                      mbarriers);
+//                      swizzle) into a shared-memory ring (full/empty
+//                      mbarriers) of 4 stages, or 6 on a CTA pair, whose CTAs
+//                      each hold half of B;
 //   warp 1 (one lane)  MMA issuer: tcgen05.mma M = 128 (one CTA) or 256 (a
 //                      CTA pair, cta_group::2), N <= 256, K = 16, into one of
 //                      two TMEM accumulators (2 x 256 columns),
