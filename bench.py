@@ -334,9 +334,12 @@ def run_ours(args, wl, rank: int, world: int, local_rank: int):
         step()
     rec = gbla.gbla_profiling_read()
     gbla.gbla_profiling_enable(False)
-    per = {}
+    per, variant = {}, {}
     for n, ms in rec:
-        per.setdefault(n, []).append(ms)
+        base = n.split("[")[0]  # launch names carry the kernel variant that ran, e.g. "bwd_q[tc]"
+        per.setdefault(base, []).append(ms)
+        if "[" in n:
+            variant[base] = n[len(base) + 1:-1]
     launches_per_step = len([n for n, _ in rec if n != "memset"]) // prof_steps
     kern = {n: sum(v) / prof_steps for n, v in per.items()}
 
@@ -351,13 +354,16 @@ def run_ours(args, wl, rank: int, world: int, local_rank: int):
 
     # end to end through the public API with host buffers: every step copies
     # its inputs (x, dy) host -> device from pinned memory, runs forward +
-    # backward and reads its parameter gradients (the step's result) back.  As
-    # a training loop that prefetches its next batch, the copy of step k + 1's
-    # inputs runs on a second stream, into a second pair of input buffers,
-    # while step k computes; K steps are timed back to back (their working
-    # set, ~0.8 GB, is far larger than L2).
+    # backward and reads its results back: the layer output y, the input
+    # gradient dx and the parameter gradients.  As a training loop that
+    # prefetches its next batch, the copy of step k + 1's inputs runs on a
+    # second stream, into a second pair of input buffers, while step k
+    # computes; K steps are timed back to back (their working set, ~0.8 GB,
+    # is far larger than L2).
     xp, dyp = x_h.pin_memory(), dy_h.pin_memory()
-    host_g = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in grads.items() if k != "dx"}
+    host_g = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in grads.items()}
+    host_g["y"] = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    results = dict(grads, y=y)
     xb, dyb = [x, torch.empty_like(x)], [dy, torch.empty_like(dy)]
     copy_stream = torch.cuda.Stream(device=dev)
 
@@ -387,7 +393,7 @@ def run_ours(args, wl, rank: int, world: int, local_rank: int):
             gbla.gbla_backward(shape, xb[c], P, saved, dyb[c], ws=ws_b, out=grads)
             freed[c].record(main)
             for n, v in host_g.items():
-                v.copy_(grads[n], non_blocking=True)
+                v.copy_(results[n], non_blocking=True)
         e1.record(main)
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / k
@@ -405,6 +411,8 @@ def run_ours(args, wl, rank: int, world: int, local_rank: int):
         return
     peaks, peak_src = load_peaks()
     alg = algorithmic(wl, T)
+    if not all(v == "tc" for n, v in variant.items() if n in alg and "gemm" not in n) and wl.dh == 64:
+        print(f"warning: a d_h = 64 state kernel ran without tcgen05: {variant}", file=sys.stderr)
     dom = max((n for n in kern if n in alg), key=lambda n: kern[n])
     bound, amount = alg[dom]
     achieved = amount / (kern[dom] * 1e-3) / (1e9 if bound == "hbm" else 1e12)
@@ -420,6 +428,8 @@ def run_ours(args, wl, rank: int, world: int, local_rank: int):
     per_kernel = {}
     for n, ms in sorted(kern.items(), key=lambda kv: -kv[1]):
         e = {"ms": round(ms, 4), "share": round(ms / sum(kern.values()), 4)}
+        if n in variant:
+            e["variant"] = variant[n]
         if n in alg:
             b, a = alg[n]
             e["achieved"] = round(a / (ms * 1e-3) / (1e9 if b == "hbm" else 1e12), 1)

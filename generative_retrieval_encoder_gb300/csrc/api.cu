@@ -10,6 +10,7 @@
 
 #include "../../include/gbla.h"
 #include "kernels.h"
+#include "mbarrier.cuh"
 
 using namespace gbla;
 
@@ -17,14 +18,19 @@ namespace {
 
 thread_local std::string g_last_error;
 
-constexpr int kSMs = 152;
-constexpr int kMaxGrid = 512;  // CTAs of a range-split kernel the workspace provides for (>= 2 x SMs)
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Per-launch profiler names of the GEMMs, by Variant: the projection, dx~ and dW GEMMs.
+const char* const kGemmNames[3][3] = {
+    {"projection gemm[tc]", "projection gemm[mma]", "projection gemm[f32]"},
+    {"dx~ gemm[tc]", "dx~ gemm[mma]", "dx~ gemm[f32]"},
+    {"dW gemm[tc]", "dW gemm[mma]", "dW gemm[f32]"},
+};
 
 // Everything derived from a shape: sequence form, tilings, buffer sizes.
 struct Plan {
@@ -35,6 +41,8 @@ struct Plan {
   int tile, tile_per_seq, n_tiles;     // readout / key-side tiles (grid.x)
   int wsplit, n_wsplit;                // dW split over rows
   int conv_blocks;
+  int sms;               // SMs of the current device
+  int max_grid;          // CTAs of a range-split kernel the workspace provides for (>= 2 x SMs)
   size_t io;             // bytes per io element
 };
 
@@ -49,6 +57,9 @@ gbla_status make_plan(const gbla_shape* s, Plan& p) {
   p.f32 = s->io_dtype == GBLA_F32;
   p.io = p.f32 ? 4 : 2;
   p.B = s->B; p.L = s->L; p.d = s->d; p.H = s->H; p.dh = s->d_h;
+  p.sms = sm_count();
+  p.max_grid = std::max(512, 2 * p.sms);
+  const int kSMs = p.sms;
   if (p.f32) {
     if (p.dh % 4 != 0 || p.dh > 128) return GBLA_ERR_UNSUPPORTED;
   } else {
@@ -164,7 +175,7 @@ SavedLayout saved_layout(const Plan& p) {
 // Partial-state slots: one per (chunk, head) for the split-L kernels; the
 // tcgen05 query-side backward takes one per (sequence, head) plus one per CTA
 // (a CTA boundary inside a (sequence, head)).
-int partial_slots(const Plan& p) { return std::max(p.n_chunks * p.H, p.n_seq * p.H + kMaxGrid); }
+int partial_slots(const Plan& p) { return std::max(p.n_chunks * p.H, p.n_seq * p.H + p.max_grid); }
 
 Layout ws_layout(const Plan& p, int op) {
   Cursor c;
@@ -196,7 +207,7 @@ Layout ws_layout(const Plan& p, int op) {
     l.dW = c.take((size_t)p.n_wsplit * p.d * p.NP * 4);
     l.dstate = c.take(state_bytes(p));
     l.dstate_bf = c.take(state_bf_bytes(p));
-    l.gamma_part = c.take((size_t)std::max(p.n_chunks * p.H, kMaxGrid) * p.dh * 4);
+    l.gamma_part = c.take((size_t)std::max(p.n_chunks * p.H, p.max_grid) * p.dh * 4);
     // db_g partial rows: two per tile (tcgen05 kernel) or one per chunk
     l.bg_part = c.take((size_t)std::max(2 * p.n_tiles, p.n_chunks) * p.H * 4);
     l.conv_part = c.take((size_t)p.conv_blocks * p.d * 5 * 4);
@@ -328,10 +339,12 @@ cudaError_t launch_readout_chunks_bf16(const ReadoutArgs& ra, bool norm, const T
 }
 
 cudaError_t launch_readout_layer_bf16(const ReadoutArgs& ra, int n_tiles, const Tiling& chunks, int n_chunks,
-                                      cudaStream_t st) {
+                                      cudaStream_t st, const char** nm) {
+  *nm = "readout[tc]";
   const cudaError_t e = launch_readout_tc(ra, n_tiles, st);
   if (e != cudaErrorNotSupported) return e;
   (void)cudaGetLastError();
+  *nm = "readout[mma]";
   return launch_readout_chunks_bf16(ra, true, chunks, n_chunks, st);
 }
 
@@ -347,10 +360,12 @@ cudaError_t launch_bwd_kv_chunks_bf16(const BwdKVArgs& kv, const Tiling& chunks,
 }
 
 cudaError_t launch_bwd_kv_layer_bf16(const BwdKVArgs& kv, int n_tiles, const Tiling& chunks, int n_chunks,
-                                     int* bg_rows, cudaStream_t st) {
+                                     int* bg_rows, cudaStream_t st, const char** nm) {
+  *nm = "bwd_kv[tc]";
   const cudaError_t e = launch_bwd_kv_tc(kv, n_tiles, bg_rows, st);
   if (e != cudaErrorNotSupported) return e;
   (void)cudaGetLastError();
+  *nm = "bwd_kv[mma]";
   *bg_rows = n_chunks;
   return launch_bwd_kv_chunks_bf16(kv, chunks, n_chunks, st);
 }
@@ -358,10 +373,12 @@ cudaError_t launch_bwd_kv_layer_bf16(const BwdKVArgs& kv, int n_tiles, const Til
 // The layer's bf16 query-side backward: the tcgen05 kernel where it applies.
 // *gamma_rows = the rows of dgamma partials written.
 cudaError_t launch_bwd_q_layer_bf16(const BwdQArgs& q, int hd, int n_chunks, int n_tiles, int* gamma_rows,
-                                    cudaStream_t st) {
+                                    cudaStream_t st, const char** nm) {
+  *nm = "bwd_q[tc]";
   const cudaError_t e = launch_bwd_q_tc(q, hd, n_tiles, gamma_rows, st);
   if (e != cudaErrorNotSupported) return e;
   (void)cudaGetLastError();
+  *nm = "bwd_q[mma]";
   *gamma_rows = n_chunks * q.H;
   return launch_bwd_q_bf16(q, true, n_chunks, st);
 }
@@ -381,7 +398,8 @@ gbla_status run_reduce(Ctx& c, const void* k, const void* v, int64_t ld, const f
   a.pre = c.pre;
   a.center = p.f32 ? nullptr : center;
   a.err = c.kerr;
-  GBLA_CHECK(p.f32 ? launch_reduce_f32(a, p.n_chunks, c.st) : launch_reduce_bf16(a, p.n_chunks, c.st), "reduce");
+  GBLA_CHECK(p.f32 ? launch_reduce_f32(a, p.n_chunks, c.st) : launch_reduce_bf16(a, p.n_chunks, c.st),
+             p.f32 ? "reduce[f32]" : "reduce[mma]");
   return GBLA_OK;
 }
 
@@ -446,7 +464,8 @@ gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* con
   // Eq. 4: conv
   ConvArgs ca{};
   ca.x = x; ca.w = conv_w; ca.b = conv_b; ca.xt = xt; ca.T = p.T; ca.d = p.d; ca.seq = c.seq; ca.err = c.kerr; ca.err_out = c.err;
-  GBLA_CHECK(launch_conv_fwd(ca, p.f32, c.st), "conv");
+  int tiled = 0;
+  GBLA_CHECK(launch_conv_fwd(ca, p.f32, c.st, &tiled), tiled ? "conv[bulk]" : "conv[plain]");
   c.pre = layer_pre(p, shape) ? 1 : 0;
   // Eq. 4, 5, 7: projections and gate
   GemmArgs ga{};
@@ -459,7 +478,8 @@ gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* con
   ga.gate_mode = shape->gate == GBLA_GATE_SIGMOID ? 0 : 1; ga.gate = gate; ga.ldgate = p.H; ga.io_f32 = p.f32;
   ga.err = c.err;
   ga.pair = 1;  // CTA pairs: each CTA loads half of B, a third less operand traffic per SM
-  GBLA_CHECK(launch_gemm(ga, c.st), "projection gemm");
+  int var = VAR_TC;
+  GBLA_CHECK(launch_gemm(ga, c.st, &var), kGemmNames[0][var]);
   // Eq. 5/6: state
   const size_t es = p.io;
   const char* Pc = static_cast<const char*>(P);
@@ -476,9 +496,10 @@ gbla_status gbla_forward(const gbla_shape* shape, const void* x, const void* con
   ra.out = y; ra.ldo = p.HD; ra.den = nullptr;
   ra.rsinv = (saved && !p.f32) ? at<float>(saved, saved_layout(p).rsinv) : nullptr;
   ra.H = p.H; ra.dh = p.dh; ra.seq = c.seq; ra.tiles = c.tiles; ra.err = c.kerr; ra.err_out = c.err;
+  const char* nm = "readout[f32]";
   GBLA_CHECK(p.f32 ? launch_readout_f32(ra, true, p.n_tiles, c.st)
-                   : launch_readout_layer_bf16(ra, p.n_tiles, c.chunks, p.n_chunks, c.st),
-             "readout");
+                   : launch_readout_layer_bf16(ra, p.n_tiles, c.chunks, p.n_chunks, c.st, &nm),
+             nm);
   return GBLA_OK;
 }
 
@@ -533,9 +554,10 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   q.H = p.H; q.dh = p.dh; q.seq = c.seq; q.chunks = c.chunks; q.tiles = c.tiles; q.err = c.kerr; q.err_out = c.err;
   q.partial_slots = partial_slots(p);
   int gamma_rows = p.n_chunks * p.H;
+  const char* nm = "bwd_q[f32]";
   GBLA_CHECK(p.f32 ? launch_bwd_q_f32(q, true, p.n_chunks, c.st)
-                   : launch_bwd_q_layer_bf16(q, p.HD, p.n_chunks, p.n_tiles, &gamma_rows, c.st),
-             "bwd_q");
+                   : launch_bwd_q_layer_bf16(q, p.HD, p.n_chunks, p.n_tiles, &gamma_rows, c.st, &nm),
+             nm);
   // key side: dk, dv, ds
   BwdKVArgs kv{};
   kv.k = P + p.HD * es; kv.ldk = 4 * p.HD;
@@ -554,9 +576,10 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   kv.bg_part = at<float>(ws, l.bg_part);
   kv.H = p.H; kv.dh = p.dh; kv.seq = c.seq; kv.tiles = c.tiles; kv.err = c.kerr; kv.err_out = c.err;
   int bg_rows = p.n_tiles;
+  nm = "bwd_kv[f32]";
   GBLA_CHECK(p.f32 ? launch_bwd_kv_f32(kv, p.n_tiles, c.st)
-                   : launch_bwd_kv_layer_bf16(kv, p.n_tiles, c.chunks, p.n_chunks, &bg_rows, c.st),
-             "bwd_kv");
+                   : launch_bwd_kv_layer_bf16(kv, p.n_tiles, c.chunks, p.n_chunks, &bg_rows, c.st, &nm),
+             nm);
   // Eq. 4 projections backward: dx~ = dP W_all^T, dW_all = x~^T dP
   GemmArgs g1{};
   g1.A = dP; g1.lda = p.NP; g1.a_kmajor = 1;
@@ -567,21 +590,22 @@ gbla_status gbla_backward(const gbla_shape* shape, const void* x, const void* co
   g1.M = p.T; g1.N = p.d; g1.K = p.N1; g1.k_split = p.N1; g1.epi = p.f32 ? EPI_F32 : EPI_BF16; g1.io_f32 = p.f32;
   g1.err = c.err;
   g1.pair = 1;  // long K: the operand feed limits, CTA pairs halve it per SM
-  GBLA_CHECK(launch_gemm(g1, c.st), "dx~ gemm");
+  int var = VAR_TC;
+  GBLA_CHECK(launch_gemm(g1, c.st, &var), kGemmNames[1][var]);
   GemmArgs g2{};
   g2.A = xt; g2.lda = p.d; g2.a_kmajor = 0;
   g2.B = dP; g2.ldb = p.NP; g2.b_kmajor = 0;
   g2.C = at<float>(ws, l.dW); g2.ldc = p.NP;
   g2.M = p.d; g2.N = p.N1; g2.K = p.T; g2.k_split = p.wsplit; g2.epi = EPI_SPLITK; g2.io_f32 = p.f32; g2.err = c.err;
   g2.pair = 1;  // long K: the operand feed limits, CTA pairs halve it per SM
-  GBLA_CHECK(launch_gemm(g2, c.st), "dW gemm");
+  GBLA_CHECK(launch_gemm(g2, c.st, &var), kGemmNames[2][var]);
 
   // Eq. 4 conv backward
   ConvArgs ca{};
   ca.x = x; ca.w = conv_w; ca.dxt = at<char>(ws, l.dxt); ca.dx = dx; ca.part = at<float>(ws, l.conv_part);
   ca.T = p.T; ca.d = p.d; ca.seq = c.seq; ca.err = c.kerr; ca.err_out = c.err;
-  int nparts = 0;
-  GBLA_CHECK(launch_conv_bwd(ca, p.f32, &nparts, c.st), "conv bwd");
+  int nparts = 0, tiled = 0;
+  GBLA_CHECK(launch_conv_bwd(ca, p.f32, &nparts, c.st, &tiled), tiled ? "conv bwd[bulk]" : "conv bwd[plain]");
   // the parameter gradients from their partials, one launch: W_all, conv taps and bias, gamma, b_g
   ColsumJobs js{};
   js.sc.part = at<float>(ws, l.dW);  // and the split-K sum of the weight gradient
@@ -617,7 +641,7 @@ gbla_status bla_core_forward(const gbla_shape* shape, const void* q, const void*
   ra.H = p.H; ra.dh = p.dh; ra.seq = c.seq; ra.tiles = c.tiles; ra.err = c.kerr;
   GBLA_CHECK(p.f32 ? launch_readout_f32(ra, false, p.n_tiles, c.st)
                    : launch_readout_chunks_bf16(ra, false, c.chunks, p.n_chunks, c.st),
-             "readout");
+             p.f32 ? "readout[f32]" : "readout[mma]");
   return GBLA_OK;
 }
 
@@ -643,7 +667,7 @@ gbla_status bla_core_backward(const gbla_shape* shape, const void* q, const void
   a.dstate = at<float>(ws, c.l.dstate); a.dstate_bf = at<bf16>(ws, c.l.dstate_bf);
   a.H = p.H; a.dh = p.dh; a.seq = c.seq; a.chunks = c.chunks; a.err = c.kerr;
   GBLA_CHECK(p.f32 ? launch_bwd_q_f32(a, false, p.n_chunks, c.st) : launch_bwd_q_bf16(a, false, p.n_chunks, c.st),
-             "bwd_q");
+             p.f32 ? "bwd_q[f32]" : "bwd_q[mma]");
   BwdKVArgs kv{};
   kv.k = k; kv.ldk = p.HD; kv.v = v; kv.ldv = p.HD;
   kv.g = g; kv.ldg = p.H; kv.gate_kind = GATE_VALUES;
@@ -652,7 +676,7 @@ gbla_status bla_core_backward(const gbla_shape* shape, const void* q, const void
   kv.ds = dg; kv.ldds = p.H; kv.gate_grad = GG_DG;
   kv.H = p.H; kv.dh = p.dh; kv.seq = c.seq; kv.tiles = c.tiles; kv.err = c.kerr;
   GBLA_CHECK(p.f32 ? launch_bwd_kv_f32(kv, p.n_tiles, c.st) : launch_bwd_kv_chunks_bf16(kv, c.chunks, p.n_chunks, c.st),
-             "bwd_kv");
+             p.f32 ? "bwd_kv[f32]" : "bwd_kv[mma]");
   return GBLA_OK;
 }
 
@@ -663,7 +687,19 @@ gbla_status gbla_check_device_status(const void* ws, void* stream) {
   cudaError_t e = cudaMemcpyAsync(&err, ws, sizeof(int), cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "check_device_status");
+  if (err & 1) return GBLA_ERR_DEVICE_CHECK;
+  if (err & kErrTimeout) return GBLA_ERR_DEVICE_TIMEOUT;
   return err ? GBLA_ERR_DEVICE_CHECK : GBLA_OK;
+}
+
+gbla_status gbla_diag_bounded_wait(void* ws, size_t ws_bytes, unsigned polls, void* stream) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0 || ws_bytes < 16) return GBLA_ERR_WORKSPACE;
+  if (polls < 1 || polls > (1u << 20)) return GBLA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int), st);
+  if (e == cudaSuccess) e = launch_diag_wait(static_cast<int*>(ws), polls, st);
+  if (e != cudaSuccess) return cuda_fail(e, "diag_bounded_wait");
+  return GBLA_OK;
 }
 
 const char* gbla_status_string(int status) {
@@ -674,6 +710,8 @@ const char* gbla_status_string(int status) {
     case GBLA_ERR_WORKSPACE: return "GBLA_ERR_WORKSPACE: workspace NULL, not 256-byte aligned, or too small";
     case GBLA_ERR_CUDA: return "GBLA_ERR_CUDA: a CUDA call failed (see gbla_last_error)";
     case GBLA_ERR_DEVICE_CHECK: return "GBLA_ERR_DEVICE_CHECK: bad cu_seqlens / seq_lens detected on the device";
+    case GBLA_ERR_DEVICE_TIMEOUT:
+      return "GBLA_ERR_DEVICE_TIMEOUT: a kernel's bounded wait for its copies or MMAs gave up; results are invalid";
     default: return "unknown gbla_status";
   }
 }

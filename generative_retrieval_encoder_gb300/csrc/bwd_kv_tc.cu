@@ -1,10 +1,14 @@
-// Key-side backward of the bf16 layer (Eq. 5/6, sigmoid gate) on the
-// 5th-generation tensor cores, for d_h = 64 with phi(k) stored by the
-// projection epilogue.  Per token j of a sequence and head, with [dS | dz''] the
-// combined state gradient (dz'' the centring-corrected z column):
+// Key-side backward of the bf16 layer (Eq. 5/6) on the 5th-generation tensor
+// cores, for d_h = 64 with phi(k) stored by the projection epilogue.  Per token
+// j of a sequence and head, with [dS | dz''] the combined state gradient (dz''
+// the centring-corrected z column):
 //   dk~_j = bf16(dS) v_j + dz'',   dv_j = g_j dS^T phi(k_j),
-//   dg_j = phi(k_j) . dk~_j,  dk_j = g_j dk~_j min(1, phi(k_j)),  ds_j = dg_j g_j (1 - g_j)
+//   dg_j = phi(k_j) . dk~_j,  dk_j = g_j dk~_j min(1, phi(k_j)),
+//   ds_j = dg_j g_j (1 - g_j)  (sigmoid gate)   or   dg_j g_j  (softmax gate)
 // (phi' of elu + 1 from the stored phi; ds is the gradient of the gate logit).
+// Softmax gate: the stored gate holds the logits s_j and g_j = exp(s_j - m)
+// with m the sequence's maximum logit from the forward combine; the softmax
+// normaliser cancels in Eq. 5, so ds_j = dg_j g_j is the logit gradient.
 //
 // Persistent: one CTA per SM walks a contiguous range of (row tile, head)
 // units, head-major, so that consecutive units mostly share a (sequence,
@@ -47,7 +51,8 @@ constexpr int O_BAR = O_S + 2 * SBUF;
 constexpr int NBAR = 2 * KST + 4 + 2 * NG + 1;
 constexpr int O_DZ = O_BAR + 8 * NBAR;           // [group][2 buffers][dz'' 64] fp32
 constexpr int O_RED = O_DZ + 4 * NG * 2 * KD;    // [group][4 warps] ds sums
-constexpr int O_SLOT = O_RED + 4 * NG * 4;
+constexpr int O_M = O_RED + 4 * NG * 4;          // [group][2 buffers] maximum logit (softmax gate)
+constexpr int O_SLOT = O_M + 4 * NG * 2;
 constexpr int O_FAIL = O_SLOT + 4;
 constexpr int SMEM = O_FAIL + 4 + 1024;
 constexpr int TMEM_COLS = NG * 2 * KD;           // per group: D1 | D2
@@ -106,6 +111,8 @@ __global__ void __launch_bounds__(NTH, 1)
   const uint32_t DRAIN = bar0 + 8 * (2 * KST + 4 + 2 * NG);
   float* dzs = reinterpret_cast<float*>(smem + O_DZ);
   float* red = reinterpret_cast<float*>(smem + O_RED);
+  float* mgs = reinterpret_cast<float*>(smem + O_M);
+  const bool logits = a.gate_kind == GATE_LOGITS;
   uint32_t* slot = reinterpret_cast<uint32_t*>(smem + O_SLOT);
   volatile int* fail = reinterpret_cast<volatile int*>(smem + O_FAIL);
 
@@ -217,6 +224,7 @@ __global__ void __launch_bounds__(NTH, 1)
     const int i = wq * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16) + grp * 2 * KD;
     float* dzg = dzs + grp * 2 * KD;
+    float* mg = mgs + grp * 2;
     int j = 0, k = -1, prev = -1;
     for (int u = u0; u < u1; ++u) {
       const Unit x = unit_at(a, u, n_units_per_head);
@@ -232,9 +240,11 @@ __global__ void __launch_bounds__(NTH, 1)
         prev = x.seqh;
         // the buffer replaced here served the state before the previous one
         if (i < KD) dzg[(k & 1) * KD + i] = a.dstate[((size_t)x.seqh * KD + i) * state_ld(KD) + KD];
+        else if (i == KD) mg[k & 1] = logits ? a.state_m[x.seqh] : 0.f;
         named_bar(1 + grp, 128);
       }
       const float* dz = dzg + (k & 1) * KD;
+      const float mseq = mg[k & 1];
       if (grp == 0 && wq == 0 && lane == 0 && a.bg_part)  // slots of MMA tiles the unit lacks
         for (int t = x.ntl; t < tiles_per_unit; ++t) a.bg_part[((size_t)x.ti * tiles_per_unit + t) * a.H + x.h] = 0.f;
       for (int t = 0; t < x.ntl; ++t, ++j) {
@@ -245,7 +255,8 @@ __global__ void __launch_bounds__(NTH, 1)
         const int rel = t * KT + i;
         const bool valid = rel < x.nval, store = rel < x.nrows;
         const size_t row = x.rb + rel;
-        const float g = valid ? __ldg(a.g + row * a.ldg + x.h) : 0.f;
+        const float gin = valid ? __ldg(a.g + row * a.ldg + x.h) : 0.f;
+        const float g = logits ? (valid ? __expf(gin - mseq) : 0.f) : gin;
         mbar_wait(ACCF(grp), (j / NG) & 1, fail);
         tc_fence_after();
         // dk~ = D1 + dz'', dg = phi(k) . dk~, dk = g dk~ min(1, phi(k)) -> the phi(k) row
@@ -297,7 +308,7 @@ __global__ void __launch_bounds__(NTH, 1)
           }
         }
         // the gate-logit gradient
-        const float ds = valid ? dg * g * (1.f - g) : 0.f;
+        const float ds = valid ? (logits ? dg * g : dg * g * (1.f - g)) : 0.f;
         if (store) reinterpret_cast<bf16*>(a.ds)[row * a.ldds + x.h] = __float2bfloat16_rn(ds);
         // the warp's 32 rows of dk and dv leave as whole 128-byte rows
         __syncwarp();
@@ -343,7 +354,9 @@ __global__ void __launch_bounds__(NTH, 1)
 cudaError_t launch_bwd_kv_tc(const BwdKVArgs& a, int n_tiles, int* nparts, cudaStream_t st) {
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   const long long voff = ((const bf16*)a.v - (const bf16*)a.k);
-  if (a.dh != KD || !a.pre || a.gate_kind != GATE_VALUES || a.gate_grad != GG_SIGMOID || a.ldv != a.ldk ||
+  const bool sig = a.gate_kind == GATE_VALUES && a.gate_grad == GG_SIGMOID;
+  const bool soft = a.gate_kind == GATE_LOGITS && a.gate_grad == GG_SOFTMAX && a.state_m;
+  if (a.dh != KD || !a.pre || !(sig || soft) || a.ldv != a.ldk ||
       voff < 0 || voff % 8 || !al16(a.k) || !al16(a.dk) || !al16(a.dv) || !al16(a.dstate_bf) || a.ldk % 8 ||
       a.lddk % 8 || a.lddv % 8 || a.seq.T <= 0 || n_tiles <= 0 || a.tiles.tile % KT ||
       a.zero_cols_to > a.zero_cols_from)

@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(NTH, 2)
 cudaError_t launch_bwd_q_tc(const BwdQArgs& a, int hd, int n_tiles, int* nparts, cudaStream_t st) {
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   const long long roff = ((const bf16*)a.r - (const bf16*)a.q);
-  if (a.dh != QD || !a.pre || !a.rms_w || !a.rsinv || hd % 8 || a.ldr != a.ldq || roff < 0 || roff % 8 ||
+  if (a.dh != QD || !a.pre || !a.rsinv || hd % 8 || a.ldr != a.ldq || roff < 0 || roff % 8 ||
       !al16(a.q) || !al16(a.dy) || !al16(a.dq) || !al16(a.dr) || !al16(a.partial) || a.ldq % 8 || a.lddy % 8 ||
       a.lddq % 8 || a.lddr % 8 || a.seq.T <= 0 || n_tiles <= 0 || a.tiles.tile % QT)
     return cudaErrorNotSupported;

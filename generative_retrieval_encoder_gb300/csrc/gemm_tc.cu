@@ -30,6 +30,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 #include "pdl.cuh"
 #include "kernels.h"
 #include "mbarrier.cuh"
@@ -465,13 +467,25 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
 }
 
 int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  // Per device, looked up once.  Without a usable device (a host that only
+  // sizes workspaces) the GB300's 152 SMs stand in, so that the sizes a
+  // host computes agree with those of the GPU it targets.
+  constexpr int kMaxDev = 256;
+  static std::atomic<int> n[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+    (void)cudaGetLastError();
+    return 152;
   }
-  return n;
+  int v = n[dev].load(std::memory_order_relaxed);
+  if (v <= 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+      (void)cudaGetLastError();
+      v = 152;
+    }
+    n[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
 }
 
 // cudaErrorNotSupported when the shape is outside what this kernel handles

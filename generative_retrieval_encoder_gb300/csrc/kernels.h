@@ -155,7 +155,8 @@ cudaError_t launch_bwd_q_tc(const BwdQArgs& a, int hd, int n_tiles, int* nparts,
 // stored (pre), no den output; cudaErrorNotSupported otherwise.
 cudaError_t launch_readout_tc(const ReadoutArgs& a, int n_tiles, cudaStream_t st);
 // tcgen05 key-side backward (bwd_kv_tc.cu): d_h = 64, phi(k) stored, sigmoid
-// gate; db_g partials in *nparts rows of bg_part.  cudaErrorNotSupported otherwise.
+// gate (ds = dg g (1 - g)) or softmax logits (ds = dg g, g = exp(s - m));
+// db_g partials in *nparts rows of bg_part.  cudaErrorNotSupported otherwise.
 cudaError_t launch_bwd_kv_tc(const BwdKVArgs& a, int n_tiles, int* nparts, cudaStream_t st);
 cudaError_t launch_bwd_kv_bf16(const BwdKVArgs& a, int grid_x, cudaStream_t st);
 
@@ -168,17 +169,26 @@ cudaError_t launch_gemm_bf16(const GemmArgs& a, cudaStream_t st);
 // tcgen05 + TMA GEMM; cudaErrorNotSupported for shapes it does not take.
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_f32(const GemmArgs& a, cudaStream_t st);
+// Which kernel variant a launcher ran (reported by the per-launch profiler).
+enum Variant { VAR_TC = 0, VAR_MMA = 1, VAR_F32 = 2 };
 // The GEMM of the layer: tcgen05 where supported, else mma.sync / fp32 SIMT.
-inline cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
+inline cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st, int* variant = nullptr) {
+  if (variant) *variant = VAR_TC;
   cudaError_t e = launch_gemm_tc(a, st);
   if (e != cudaErrorNotSupported) return e;
   (void)cudaGetLastError();
+  if (variant) *variant = a.io_f32 ? VAR_F32 : VAR_MMA;
   return a.io_f32 ? launch_gemm_f32(a, st) : launch_gemm_bf16(a, st);
 }
 
-cudaError_t launch_conv_fwd(const ConvArgs& a, bool f32, cudaStream_t st);
+// *tiled = 1 when the bulk-copy staged bf16 kernel ran, 0 for the plain one.
+cudaError_t launch_conv_fwd(const ConvArgs& a, bool f32, cudaStream_t st, int* tiled = nullptr);
 // Writes the parameter-gradient partials to part[0 .. *nparts)[d][5].
-cudaError_t launch_conv_bwd(const ConvArgs& a, bool f32, int* nparts, cudaStream_t st);
+cudaError_t launch_conv_bwd(const ConvArgs& a, bool f32, int* nparts, cudaStream_t st, int* tiled = nullptr);
+// Diagnostic: one CTA waits, with the kernels' bounded mbarrier wait limited
+// to `polls` polls, on a barrier that nothing arrives at, and sets the
+// timeout bit of *err when the wait gives up.
+cudaError_t launch_diag_wait(int* err, unsigned polls, cudaStream_t st);
 // Rows of the part buffer the backward may use, at most.
 int conv_bwd_parts_max(int T);
 // bf16 kernels staged through shared memory by bulk copies (conv.cu); usable

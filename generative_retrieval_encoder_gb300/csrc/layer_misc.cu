@@ -6,6 +6,7 @@
 
 #include "kernels.h"
 #include "pdl.cuh"
+#include "tcgen05.cuh"
 
 namespace gbla {
 namespace {
@@ -370,7 +371,30 @@ __global__ void __launch_bounds__(1024) k_colsum(const ColsumJobs js) {
 
 int grid_for(size_t n) { const size_t g = (n + 255) / 256; return (int)(g < 2432 ? (g > 0 ? g : 1) : 2432); }
 
+// ------------------------------------------------------------ diagnostic
+// The bounded mbarrier wait of the tensor-core kernels, run out on purpose:
+// one thread waits for a phase of a barrier that nothing arrives at, gives up
+// after `polls` polls (a bounded loop; nothing faults or hangs) and reports
+// it through the timeout bit of the error word, as the kernels do.
+__global__ void k_diag_wait(int* err, unsigned polls) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int fail;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    mbar_init_fence();
+    fail = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(b, 0, &fail, polls)) atomicOr(err, kErrTimeout);
+}
+
 }  // namespace
+
+cudaError_t launch_diag_wait(int* err, unsigned polls, cudaStream_t st) {
+  k_diag_wait<<<1, 32, 0, st>>>(err, polls);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_plan(const SeqDesc& s, int ntile, const int* tile_sizes, int32_t* const* prefixes,
                         int* err, cudaStream_t st) {
@@ -380,8 +404,10 @@ cudaError_t launch_plan(const SeqDesc& s, int ntile, const int* tile_sizes, int3
   return cudaGetLastError();
 }
 
-cudaError_t launch_conv_fwd(const ConvArgs& a, bool f32, cudaStream_t st) {
-  if (!f32 && conv_tile_ok(a, false)) return launch_conv_fwd_tile(a, st);
+cudaError_t launch_conv_fwd(const ConvArgs& a, bool f32, cudaStream_t st, int* tiled) {
+  const bool tile = !f32 && conv_tile_ok(a, false);
+  if (tiled) *tiled = tile ? 1 : 0;
+  if (tile) return launch_conv_fwd_tile(a, st);
   const int V = f32 ? 4 : 8;
   const long long items = (long long)((a.T + RUN - 1) / RUN) * (a.d / V);
   const unsigned grid = (unsigned)((items + 255) / 256);
@@ -393,8 +419,10 @@ cudaError_t launch_conv_fwd(const ConvArgs& a, bool f32, cudaStream_t st) {
 int conv_bwd_blocks(int T) { return std::max(1, std::min(1024, (T + 127) / 128)); }
 int conv_bwd_parts_max(int T) { return std::max(conv_bwd_blocks(T), conv_tile_parts_max(T)); }
 
-cudaError_t launch_conv_bwd(const ConvArgs& a, bool f32, int* nparts, cudaStream_t st) {
-  if (!f32 && conv_tile_ok(a, true)) {
+cudaError_t launch_conv_bwd(const ConvArgs& a, bool f32, int* nparts, cudaStream_t st, int* tiled) {
+  const bool tile = !f32 && conv_tile_ok(a, true);
+  if (tiled) *tiled = tile ? 1 : 0;
+  if (tile) {
     *nparts = conv_tile_parts(a.T, a.d);
     return launch_conv_bwd_tile(a, *nparts, st);
   }

@@ -9,10 +9,11 @@
 
 namespace gbla {
 
-// Bounded wait: false if the phase did not complete within kPollLimit polls
+// Bounded wait: false if the phase did not complete within `limit` polls
 // or another role of the CTA has already given up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* fail) {
-  for (uint32_t i = 0; i < kPollLimit; ++i) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* fail,
+                                          uint32_t limit = kPollLimit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 1023) == 1023 && *fail) return false;
   }
@@ -25,17 +26,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       ::"r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
-// TMA load multicast to the CTAs of `mask` in the cluster: the same shared
-// offset and mbarrier offset in each of them receive the box and the bytes.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;"
-      ::"r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y), "h"(mask)
-      : "memory");
-}
-
 // 2-SM (CTA pair) forms.  The load completes on an mbarrier that may be the
 // peer CTA's (address from mapa_shared).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {

@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_PKG, "libgbla.so")
 
 GBLA_OK, GBLA_ERR_INVALID_ARG, GBLA_ERR_UNSUPPORTED, GBLA_ERR_WORKSPACE, GBLA_ERR_CUDA, GBLA_ERR_DEVICE_CHECK = \
     0, -1, -2, -3, -4, -5
+GBLA_ERR_DEVICE_TIMEOUT = -6
 GBLA_F32, GBLA_BF16 = 0, 1
 GBLA_GATE_SIGMOID, GBLA_GATE_SOFTMAX = 0, 1
 GBLA_OP_FORWARD, GBLA_OP_BACKWARD, GBLA_OP_CORE_FORWARD, GBLA_OP_CORE_BACKWARD = 0, 1, 2, 3
@@ -24,7 +25,7 @@ GBLA_OP_FORWARD, GBLA_OP_BACKWARD, GBLA_OP_CORE_FORWARD, GBLA_OP_CORE_BACKWARD =
 EXPORTS = ("gbla_workspace_size", "gbla_saved_size", "gbla_validate_shape", "gbla_forward", "gbla_backward",
            "bla_core_forward", "bla_core_backward", "gbla_check_device_status", "gbla_status_string",
            "gbla_last_error", "gbla_version", "gbla_profiling_enable", "gbla_profiling_read",
-           "bla_core_forward_noalloc")
+           "bla_core_forward_noalloc", "bla_core_noalloc_check_device_status", "gbla_diag_bounded_wait")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -72,6 +73,10 @@ def lib() -> ctypes.CDLL:
         L.bla_core_backward.restype = ctypes.c_int
         L.bla_core_forward_noalloc.argtypes = [sp] + [vp] * 8
         L.bla_core_forward_noalloc.restype = ctypes.c_int
+        L.bla_core_noalloc_check_device_status.argtypes = [vp]
+        L.bla_core_noalloc_check_device_status.restype = ctypes.c_int
+        L.gbla_diag_bounded_wait.argtypes = [vp, sz, ctypes.c_uint, vp]
+        L.gbla_diag_bounded_wait.restype = ctypes.c_int
         L.gbla_check_device_status.argtypes = [vp, vp]
         L.gbla_check_device_status.restype = ctypes.c_int
         L.gbla_status_string.argtypes = [ctypes.c_int]
@@ -239,6 +244,16 @@ def bla_core_backward(shape: Shape, q, k, v, g, d_o, ws=None):
 
 def gbla_check_device_status(ws: torch.Tensor) -> int:
     return lib().gbla_check_device_status(_ptr(ws), _stream())
+
+
+def bla_core_noalloc_check_device_status() -> int:
+    """The error word of the last bla_core_forward_noalloc call on the current device."""
+    return lib().bla_core_noalloc_check_device_status(_stream())
+
+
+def gbla_diag_bounded_wait(ws: torch.Tensor, polls: int = 4096) -> int:
+    """Runs the kernels' bounded mbarrier wait out on purpose (see gbla.h)."""
+    return lib().gbla_diag_bounded_wait(_ptr(ws), ws.numel(), polls, _stream())
 
 
 def gbla_profiling_enable(on: bool) -> None:

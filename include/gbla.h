@@ -45,6 +45,10 @@
  *   or not ending at T; seq_lens outside [0, L]) sets an error word in the
  *   workspace, every kernel then skips its work, and gbla_check_device_status()
  *   reports GBLA_ERR_DEVICE_CHECK.  No kernel traps or waits on another CTA.
+ *   The tensor-core kernels wait on their own copies and MMAs through
+ *   mbarriers; every such wait is bounded, and one that gives up (a device
+ *   that stopped making progress) sets a timeout bit in the error word instead
+ *   of hanging: gbla_check_device_status() then reports GBLA_ERR_DEVICE_TIMEOUT.
  */
 #ifndef GBLA_H
 #define GBLA_H
@@ -62,7 +66,8 @@ typedef enum {
   GBLA_ERR_UNSUPPORTED = -2,  /* a valid shape this build has no kernel for  */
   GBLA_ERR_WORKSPACE = -3,    /* ws NULL, misaligned, or ws_bytes too small  */
   GBLA_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed        */
-  GBLA_ERR_DEVICE_CHECK = -5  /* bad sequence data detected on the device    */
+  GBLA_ERR_DEVICE_CHECK = -5, /* bad sequence data detected on the device   */
+  GBLA_ERR_DEVICE_TIMEOUT = -6 /* a kernel's bounded wait gave up            */
 } gbla_status;
 
 typedef enum { GBLA_F32 = 0, GBLA_BF16 = 1 } gbla_dtype;
@@ -193,8 +198,8 @@ gbla_status bla_core_backward(const gbla_shape* shape, const void* q,
  *   Every call on a device shares the one array: calls whose kernels overlap
  *   on the GPU (two streams, or two host threads) race and corrupt each
  *   other's results.  Order them on one stream.  The counters and the error
- *   word are cleared at the start of every call; gbla_check_device_status
- *   cannot be used on the array (it has no host-visible workspace pointer).
+ *   word are cleared at the start of every call; the error word of the last
+ *   call is read by bla_core_noalloc_check_device_status (below).
  */
 #define GBLA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 gbla_status bla_core_forward_noalloc(const gbla_shape* shape, const void* q,
@@ -203,9 +208,24 @@ gbla_status bla_core_forward_noalloc(const gbla_shape* shape, const void* q,
                                      float* state, void* stream);
 
 /* Synchronises `stream` and reads the device error word of the workspace that
- * the last call on it used: GBLA_OK or GBLA_ERR_DEVICE_CHECK (or
- * GBLA_ERR_CUDA if the stream itself failed). */
+ * the last call on it used: GBLA_OK, GBLA_ERR_DEVICE_CHECK (bad cu_seqlens /
+ * seq_lens; reported first), GBLA_ERR_DEVICE_TIMEOUT (a bounded wait gave up),
+ * or GBLA_ERR_CUDA if the stream itself failed. */
 gbla_status gbla_check_device_status(const void* ws, void* stream);
+
+/* gbla_check_device_status for bla_core_forward_noalloc: synchronises
+ * `stream` and reads the error word of the library's fixed scratch array on
+ * the current device (the last no-allocation call's).  It allocates nothing. */
+gbla_status bla_core_noalloc_check_device_status(void* stream);
+
+/* Diagnostic of the timeout path (no counterpart on the pages).  Clears the
+ * error word at the start of `ws` (any workspace of at least 16 bytes,
+ * 256-byte aligned) and launches one CTA that waits, with the kernels' own
+ * bounded mbarrier wait cut to `polls` polls (1 .. 2^20), on a barrier that
+ * nothing arrives at.  The wait gives up, sets the timeout bit, and the kernel
+ * returns; nothing faults or hangs.  gbla_check_device_status(ws, stream)
+ * then reports GBLA_ERR_DEVICE_TIMEOUT.  Asynchronous on `stream`. */
+gbla_status gbla_diag_bounded_wait(void* ws, size_t ws_bytes, unsigned polls, void* stream);
 
 /* Static text for a status code. */
 const char* gbla_status_string(int status);
@@ -222,7 +242,10 @@ int gbla_version(void);
  * on that call's stream.  gbla_profiling_read() synchronises on the last
  * event, writes up to `cap` entries (static name strings, milliseconds) and
  * returns the number of launches recorded since the previous read, then
- * clears the record.  Either output array may be NULL. */
+ * clears the record.  Either output array may be NULL.  A name is the step
+ * followed by the kernel variant that ran, e.g. "bwd_q[tc]" (5th-generation
+ * tensor cores, tcgen05), "bwd_q[mma]" (mma.sync), "bwd_q[f32]" (fp32 I/O),
+ * "conv[bulk]" (bulk-copy staged) or "conv[plain]". */
 void gbla_profiling_enable(int on);
 int gbla_profiling_read(const char** names, float* ms, int cap);
 

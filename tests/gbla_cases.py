@@ -85,6 +85,31 @@ def layer_case(wl: Workload):
     return shape, x, P, dy, R, (st, ln), T
 
 
+def launch_names(fn) -> list[str]:
+    """Runs fn() with the library's per-launch profiler on and returns the
+    launch names it recorded, each carrying the kernel variant that ran
+    (e.g. "bwd_q[tc]": tcgen05; "bwd_q[mma]": the mma.sync fallback)."""
+    gbla.gbla_profiling_enable(True)
+    gbla.gbla_profiling_read()
+    try:
+        fn()
+        return [n for n, _ in gbla.gbla_profiling_read()]
+    finally:
+        gbla.gbla_profiling_enable(False)
+
+
+# The steps that run on the 5th-generation tensor cores (tcgen05) in the bf16
+# layer at d_h = 64: any fallback to another variant is a regression.
+TC_STEPS_DH64 = ("projection gemm", "readout", "bwd_q", "bwd_kv", "dx~ gemm", "dW gemm")
+
+
+def assert_tc_variants(names, steps=TC_STEPS_DH64):
+    ran = {n.split("[")[0]: n for n in names}
+    for step in steps:
+        assert step in ran, (step, names)
+        assert ran[step] == step + "[tc]", (step, ran[step], names)
+
+
 def oracle_layer(R, wl: Workload, st, ln, backward=False):
     gm = 1 if wl.gate == "softmax" else 0
     out = oracle.gbla_forward(R["x"], R["P"], wl.H, wl.dh, st, ln, gm, wl.eps)

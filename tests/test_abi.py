@@ -33,7 +33,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings_and_version(L):
-    for s in (0, -1, -2, -3, -4, -5):
+    for s in (0, -1, -2, -3, -4, -5, -6):
         assert L.gbla_status_string(s).startswith(b"GBLA_")
     assert L.gbla_version() >= 100
 
@@ -97,3 +97,26 @@ def test_host_argument_errors_launch_nothing(L):
     st = L.gbla_backward(ctypes.byref(s), *[fake] * 10, None, fake, fake, *[None] * 9, fake, n, None)
     assert st == gbla.GBLA_ERR_INVALID_ARG  # saved missing
     assert L.gbla_check_device_status(None, None) == gbla.GBLA_ERR_WORKSPACE
+
+
+def test_diag_and_noalloc_host_errors(L):
+    """Host-side errors of the diagnostic and the no-allocation entry points:
+    statuses, no launch, no out-of-range access of the per-device address
+    cache (which is keyed by device, with no fixed device count)."""
+    fake = ctypes.c_void_p(1 << 20)
+    assert L.gbla_diag_bounded_wait(None, 1 << 20, 16, None) == gbla.GBLA_ERR_WORKSPACE
+    assert L.gbla_diag_bounded_wait(ctypes.c_void_p((1 << 20) + 16), 1 << 20, 16, None) == gbla.GBLA_ERR_WORKSPACE
+    assert L.gbla_diag_bounded_wait(fake, 8, 16, None) == gbla.GBLA_ERR_WORKSPACE
+    assert L.gbla_diag_bounded_wait(fake, 1 << 20, 0, None) == gbla.GBLA_ERR_INVALID_ARG
+    assert L.gbla_diag_bounded_wait(fake, 1 << 20, (1 << 20) + 1, None) == gbla.GBLA_ERR_INVALID_ARG
+    big = gbla.make_shape(1024, 64, 64, 16, 128)
+    st = L.bla_core_forward_noalloc(ctypes.byref(big), fake, fake, fake, fake, fake, None, None, None)
+    assert st == gbla.GBLA_ERR_WORKSPACE  # needs more than the fixed array; refused before any CUDA call
+    small = gbla.make_shape(2, 64, 64, 2, 32)
+    st = L.bla_core_forward_noalloc(ctypes.byref(small), None, None, None, None, None, None, None, None)
+    import torch
+    if torch.cuda.is_available():  # the array's address is found, then the null pointers are refused
+        assert st == gbla.GBLA_ERR_INVALID_ARG
+    else:  # no device: the address lookup fails and is reported, nothing else runs
+        assert st == gbla.GBLA_ERR_CUDA
+        assert L.bla_core_noalloc_check_device_status(None) == gbla.GBLA_ERR_CUDA

@@ -1,15 +1,25 @@
 """Parity at the full workload sizes, in the launch configuration that
-bench.py times: the whole batch runs on the GPU, and the oracle recomputes a
-few whole sequences of it (sequences are independent, so their outputs and
-input gradients are checked row for row).  Parameter gradients are sums over
-all sequences; they are checked on a GPU rerun of the sampled sequences alone
-against the oracle on the same sequences.
+bench.py times.
+
+* B=32 L=2048 d=512 H=8 d_h=64 (the bench workload) and B=16 L=8192 (the
+  training workload): one forward + backward of the whole batch on the GPU,
+  compared with the oracle on the whole batch: y and dx on every row, and
+  every parameter gradient, whose sums over all 65536 / 131072 rows include
+  the dW split over rows and the fixed-order sums that the bench times.
+* B=8 L=32768 long-history forward (repeated low-rank pattern): y of all
+  eight sequences.
+* 256 varlen sequences of 64..16384 rows, d=1024, H=8, d_h=128, training
+  step: the oracle recomputes a short, a middling and the longest sequence
+  (sequences are independent, so their y and dx are checked row for row); the
+  parameter gradients are checked on a GPU rerun of those sequences alone
+  against the oracle on the same sequences (the whole batch would take the
+  oracle most of an hour).
+
+Every run also checks, from the library's launch names, that the d_h = 64
+steps ran their tcgen05 kernels (no silent fallback).
 
 Workloads (seeded, synthetic; the pages' private long listening histories are
-stood in for by their shapes):
-  B=32 L=2048 d=512 H=8 d_h=64 forward;  B=8 L=32768 long-history forward
-  (repeated low-rank pattern);  B=16 L=8192 training step;  256 varlen
-  sequences of 64..16384 rows, d=1024, H=8, d_h=128, training step."""
+stood in for by their shapes)."""
 import numpy as np
 import pytest
 import torch
@@ -17,9 +27,11 @@ import torch
 import oracle
 from generative_retrieval_encoder_gb300 import build, gbla
 from generative_retrieval_encoder_gb300 import workloads as W
-from gbla_cases import TOL, f64, max_err
+from gbla_cases import TOL, assert_tc_variants, f64, launch_names, max_err
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+GRADS = ("dconv_w", "dconv_b", "dW_q", "dW_k", "dW_v", "dW_r", "dw_g", "db_g", "drms_w")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -42,69 +54,91 @@ def _inputs(wl):
     return shape, x, P, dy, cu
 
 
-def _ranges(wl, cu, picks):
-    if cu is not None:
-        return [(cu[b], cu[b + 1]) for b in picks]
-    return [(b * wl.L, (b + 1) * wl.L) for b in picks]
-
-
-def _check_rows(got, ref, tol, what):
+def _check(got, ref, tol, what):
     e = max_err(got, ref)
     assert e <= tol, (what, e)
 
 
-def _oracle_seq(wl, x, P, dy, a, e, backward):
+def _gate(wl):
+    return 1 if wl.gate == "softmax" else 0
+
+
+def _run(shape, x, P, dy, backward):
+    out = {}
+
+    def fn():
+        out["y"], saved = gbla.gbla_forward(shape, x, P, saved=backward or None)
+        if backward:
+            out["g"] = gbla.gbla_backward(shape, x, P, saved, dy)
+        torch.cuda.synchronize()
+
+    return out, launch_names(fn)
+
+
+@pytest.mark.parametrize("name", ["train2k", "train8k"])
+def test_training_step_whole_batch(name):
+    wl = {"train2k": W.FWD_2K, "train8k": W.TRAIN_8K}[name]
+    shape, x, P, dy, _ = _inputs(wl)
+    out, names = _run(shape, x, P, dy, backward=True)
+    assert_tc_variants(names)
     Pr = {n: f64(t) for n, t in P.items()}
-    st, ln = oracle.seqs(1, e - a)
-    out = oracle.gbla_forward(f64(x[a:e]), Pr, wl.H, wl.dh, st, ln, 0, wl.eps)
-    g = oracle.gbla_backward(f64(x[a:e]), Pr, f64(dy[a:e]), wl.H, wl.dh, st, ln, 0, wl.eps) if backward else None
-    return out, g
-
-
-@pytest.mark.parametrize("name,picks", [("train2k", [0, 31]), ("long32k", [7])])
-def test_forward_full_size(name, picks):
-    wl = {"train2k": W.FWD_2K, "long32k": W.LONG_32K}[name]
-    shape, x, P, dy, cu = _inputs(wl)
-    y, _ = gbla.gbla_forward(shape, x, P)
-    torch.cuda.synchronize()
-    for a, e in _ranges(wl, cu, picks):
-        out, _ = _oracle_seq(wl, x, P, dy, a, e, False)
-        _check_rows(f64(y[a:e]), out["y"], TOL["bf16"], (name, a, "y"))
-
-
-@pytest.mark.parametrize("name,picks", [("train8k", [3]), ("varlen", None)])
-def test_training_step_full_size(name, picks):
-    wl = {"train8k": W.TRAIN_8K, "varlen": W.VARLEN}[name]
-    shape, x, P, dy, cu = _inputs(wl)
-    if picks is None:  # varlen: a short, a middling and a long sequence
-        lens = np.diff(cu)
-        order = np.argsort(lens)
-        picks = [int(order[len(order) // 10]), int(order[len(order) // 2]), int(order[int(len(order) * 0.7)])]
-    y, saved = gbla.gbla_forward(shape, x, P, saved=True)
-    g = gbla.gbla_backward(shape, x, P, saved, dy)
-    torch.cuda.synchronize()
+    st, ln = oracle.seqs(wl.B, wl.L)
+    xr, dyr = f64(x), f64(dy)
+    ref = oracle.gbla_forward(xr, Pr, wl.H, wl.dh, st, ln, _gate(wl), wl.eps)
     tol = TOL["bf16"]
-    rows = _ranges(wl, cu, picks)
+    _check(f64(out["y"]), ref["y"], tol, (name, "y"))
+    del ref
+    og = oracle.gbla_backward(xr, Pr, dyr, wl.H, wl.dh, st, ln, _gate(wl), wl.eps)
+    g = out["g"]
+    _check(f64(g["dx"]), og["dx"], tol, (name, "dx"))
+    for n in GRADS:
+        _check(f64(g[n]), og[n], tol, (name, n))
+
+
+def test_long_history_forward_all_sequences():
+    wl = W.LONG_32K
+    shape, x, P, dy, _ = _inputs(wl)
+    out, names = _run(shape, x, P, dy, backward=False)
+    assert_tc_variants(names, ("projection gemm", "readout"))
+    Pr = {n: f64(t) for n, t in P.items()}
+    st, ln = oracle.seqs(wl.B, wl.L)
+    ref = oracle.gbla_forward(f64(x), Pr, wl.H, wl.dh, st, ln, _gate(wl), wl.eps)
+    y = f64(out["y"])
+    for b in range(wl.B):
+        a, e = b * wl.L, (b + 1) * wl.L
+        _check(y[a:e], ref["y"][a:e], TOL["bf16"], ("long32k", b, "y"))
+
+
+def test_varlen_training_step():
+    wl = W.VARLEN
+    shape, x, P, dy, cu = _inputs(wl)
+    lens = np.diff(cu)
+    order = np.argsort(lens, kind="stable")
+    picks = [int(order[len(order) // 10]), int(order[len(order) // 2]), int(order[-1])]  # ... and the longest
+    out, _ = _run(shape, x, P, dy, backward=True)
+    y, g = out["y"], out["g"]
+    tol = TOL["bf16"]
+    Pr = {n: f64(t) for n, t in P.items()}
+    rows = [(int(cu[b]), int(cu[b + 1])) for b in picks]
     for a, e in rows:
-        out, og = _oracle_seq(wl, x, P, dy, a, e, True)
-        _check_rows(f64(y[a:e]), out["y"], tol, (name, a, "y"))
-        _check_rows(f64(g["dx"][a:e]), og["dx"], tol, (name, a, "dx"))
+        st, ln = oracle.seqs(1, e - a)
+        ref = oracle.gbla_forward(f64(x[a:e]), Pr, wl.H, wl.dh, st, ln, _gate(wl), wl.eps)
+        og = oracle.gbla_backward(f64(x[a:e]), Pr, f64(dy[a:e]), wl.H, wl.dh, st, ln, _gate(wl), wl.eps)
+        _check(f64(y[a:e]), ref["y"], tol, ("varlen", a, e, "y"))
+        _check(f64(g["dx"][a:e]), og["dx"], tol, ("varlen", a, e, "dx"))
     # parameter gradients: rerun the sampled sequences alone on the GPU
     sub = torch.cat([torch.arange(a, e) for a, e in rows]).cuda()
-    lens = [e - a for a, e in rows]
-    cu2 = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32).cuda()
-    s2 = gbla.make_shape(1, int(sum(lens)), wl.d, wl.H, wl.dh, gate=wl.gate, eps=wl.eps, cu_seqlens=cu2)
+    sl = [e - a for a, e in rows]
+    cu2 = torch.tensor(np.concatenate([[0], np.cumsum(sl)]), dtype=torch.int32).cuda()
+    s2 = gbla.make_shape(1, int(sum(sl)), wl.d, wl.H, wl.dh, gate=wl.gate, eps=wl.eps, cu_seqlens=cu2)
     x2, dy2 = x[sub].contiguous(), dy[sub].contiguous()
-    y2, saved2 = gbla.gbla_forward(s2, x2, P, saved=True)
-    g2 = gbla.gbla_backward(s2, x2, P, saved2, dy2)
-    torch.cuda.synchronize()
-    Pr = {n: f64(t) for n, t in P.items()}
+    out2, _ = _run(s2, x2, P, dy2, backward=True)
     st, ln = oracle.seqs(cu_seqlens=cu2.cpu().numpy())
-    og = oracle.gbla_backward(f64(x2), Pr, f64(dy2), wl.H, wl.dh, st, ln, 0, wl.eps)
-    for n in ("dconv_w", "dconv_b", "dW_q", "dW_k", "dW_v", "dW_r", "dw_g", "db_g", "drms_w"):
-        _check_rows(f64(g2[n]), og[n], tol, (name, n))
+    og = oracle.gbla_backward(f64(x2), Pr, f64(dy2), wl.H, wl.dh, st, ln, _gate(wl), wl.eps)
+    for n in GRADS:
+        _check(f64(out2["g"][n]), og[n], tol, ("varlen", n))
     # the subset's rows are the same computation as inside the full batch
     off = 0
     for a, e in rows:
-        _check_rows(f64(y2[off:off + e - a]), f64(y[a:e]), 1e-2, (name, a, "subset y"))
+        _check(f64(out2["y"][off:off + e - a]), f64(y[a:e]), 1e-2, ("varlen", a, "subset y"))
         off += e - a

@@ -8,7 +8,7 @@ import torch
 
 from generative_retrieval_encoder_gb300 import build, gbla
 from generative_retrieval_encoder_gb300.workloads import TINY_F32, Workload
-from gbla_cases import TOL, f64, layer_case, max_err, oracle_layer, valid_rows
+from gbla_cases import TOL, assert_tc_variants, f64, launch_names, layer_case, max_err, oracle_layer, valid_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -46,9 +46,17 @@ GRADS = ("dconv_w", "dconv_b", "dW_q", "dW_k", "dW_v", "dW_r", "dw_g", "db_g", "
 
 def check_layer(wl: Workload):
     shape, x, P, dy, R, (st, ln), T = layer_case(wl)
-    y, saved = gbla.gbla_forward(shape, x, P, saved=True)
-    g = gbla.gbla_backward(shape, x, P, saved, dy)
-    torch.cuda.synchronize()
+    out = {}
+
+    def run():
+        out["y"], out["saved"] = gbla.gbla_forward(shape, x, P, saved=True)
+        out["g"] = gbla.gbla_backward(shape, x, P, out["saved"], dy)
+        torch.cuda.synchronize()
+
+    names = launch_names(run)
+    if wl.dtype == "bf16" and wl.dh == 64:
+        assert_tc_variants(names)
+    y, g = out["y"], out["g"]
     ref = oracle_layer(R, wl, st, ln, backward=True)
     tol = TOL[wl.dtype]
     m = valid_rows(st, ln, T)
@@ -61,7 +69,12 @@ def check_layer(wl: Workload):
     errs["dx"] = max_err(gx[m], ref["grads"]["dx"][m])
     for n in GRADS:
         if n == "db_g" and wl.gate == "softmax":
-            continue  # b_g cancels under the softmax gate: its gradient is rounding noise around 0
+            # b_g cancels under the softmax gate: the exact gradient is 0 and the
+            # kernels' is the rounding noise of a sum of logit gradients that
+            # cancel.  dw_g is the same logit gradients weighted by x~, so its
+            # size sets the scale the noise is measured against.
+            errs[n] = float(np.abs(f64(g[n])).max()) / float(np.abs(ref["grads"]["dw_g"]).max())
+            continue
         errs[n] = max_err(f64(g[n]), ref["grads"][n])
     bad = {k: v for k, v in errs.items() if not v <= tol}
     assert not bad, (wl.name, bad, errs)
@@ -92,3 +105,20 @@ def test_inference_forward_equals_training_forward():
     y1, _ = gbla.gbla_forward(shape, x, P)
     y2, _ = gbla.gbla_forward(shape, x, P, saved=True)
     assert torch.equal(y1, y2)
+
+
+def test_bounded_wait_reports_timeout_and_context_stays_usable():
+    """The tensor-core kernels' bounded mbarrier wait, run out on purpose by the
+    diagnostic entry point (a barrier that nothing arrives at, a wait cut to a
+    few thousand polls): the kernel returns, the error word carries the
+    timeout bit, gbla_check_device_status reports GBLA_ERR_DEVICE_TIMEOUT, and
+    the next call on the same workspace runs and reports GBLA_OK."""
+    wl = W("after-timeout", 2, 300, 128, 2, 64, seed=23)
+    shape, x, P, dy, R, (st, ln), T = layer_case(wl)
+    ws = gbla.workspace(shape, gbla.GBLA_OP_FORWARD)
+    assert gbla.gbla_diag_bounded_wait(ws, 4096) == gbla.GBLA_OK
+    assert gbla.gbla_check_device_status(ws) == gbla.GBLA_ERR_DEVICE_TIMEOUT
+    y, _ = gbla.gbla_forward(shape, x, P, ws=ws)
+    assert gbla.gbla_check_device_status(ws) == gbla.GBLA_OK
+    ref = oracle_layer(R, wl, st, ln)
+    assert max_err(f64(y), ref["y"]) <= TOL["bf16"]
