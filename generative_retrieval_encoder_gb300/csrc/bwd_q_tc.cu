@@ -8,8 +8,7 @@
 //        o = O'/den + c,  u = o rs,  y = u gamma SiLU(r)   (RMSNorm gate, Eq. 7)
 //        dr, dgamma (accumulated in TMEM cols 192..255), du = dy gamma SiLU(r),
 //        m = mean(du u), do = rs (du - u m), dn = do / den,
-//        dden = -(do . O'/den) / den = -rs (du . O' - m u . O') / den^2
-//   (the elementwise work on packed f32x2 instructions, two columns at a time)
+//        dden = -(do . O'/den) / den = -rs (du . o' - m u . o') / den
 //   (d)  dq~ = dn S'^T                           tcgen05 -> TMEM cols 64..127
 //   (e)  [dS' | dz'] += [dn | dden]^T phi(Q)     tcgen05 -> TMEM cols 128..191
 //   epilogue 2: dq = (dq~ + dden z) min(1, phi(q))   (phi' of elu + 1)
@@ -70,7 +69,6 @@ static_assert(2 * (SMEM + 1024) <= 233472, "two CTAs per SM");
 static_assert(QST == 2, "the control thread tracks two stages");
 static_assert(QST * STAGE >= (QT + 4) * (QD + 1) * 4, "the stage memory holds the dgamma reduction");
 static_assert(QD / 2 == 32, "a thread holds 32 columns (one 32-column TMEM load)");
-static_assert(O_F % 16 == 0, "gamma, centre and z are read as float4");
 
 constexpr int EW = 8;                 // warps
 constexpr int NTH = EW * 32;
@@ -81,28 +79,16 @@ static_assert(NTH == 4 * QD, "the dgamma sum maps threads to (quarter, column)")
 __device__ __forceinline__ uint32_t swz_off(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
-// Column pairs as packed fp32x2 values (the f32x2 instructions of sm_100+).
-__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
-__device__ __forceinline__ float2 bf2(uint32_t v) { return make_float2(bf_lo(v), bf_hi(v)); }
-__device__ __forceinline__ uint32_t pk2(float2 v) { return pack_bf16(v.x, v.y); }
-// Columns j, j + 1 of a TMEM load.
-__device__ __forceinline__ float2 tm2(const uint32_t* o, int j) {
-  return make_float2(__uint_as_float(o[j]), __uint_as_float(o[j + 1]));
-}
-// Eight consecutive fp32 values of a 16-byte aligned shared array, as four pairs.
-__device__ __forceinline__ void cols8(const float* p, float2 (&v)[4]) {
-  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
-  v[0] = make_float2(a.x, a.y); v[1] = make_float2(a.z, a.w);
-  v[2] = make_float2(b.x, b.y); v[3] = make_float2(b.z, b.w);
+__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
+  f[0] = bf_lo(u.x); f[1] = bf_hi(u.x); f[2] = bf_lo(u.y); f[3] = bf_hi(u.y);
+  f[4] = bf_lo(u.z); f[5] = bf_hi(u.z); f[6] = bf_lo(u.w); f[7] = bf_hi(u.w);
 }
 // sigmoid(x) = (1 + tanh(x / 2)) / 2 with the hardware tanh approximation
 // (relative error about 2^-11, far below the bf16 rounding of the outputs).
-__device__ __forceinline__ float2 sigmoid2(float2 x) {
-  const float2 h = __fmul2_rn(x, f2(0.5f));
-  float tx, ty;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(tx) : "f"(h.x));
-  asm("tanh.approx.f32 %0, %1;" : "=f"(ty) : "f"(h.y));
-  return __ffma2_rn(make_float2(tx, ty), f2(0.5f), f2(0.5f));
+__device__ __forceinline__ float sigmoid_fast(float x) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
+  return fmaf(0.5f, t, 0.5f);
 }
 
 // One unit = (128-row tile, head): sub-tile `sub` of tile ti of a.tiles
@@ -223,13 +209,6 @@ __global__ void __launch_bounds__(NTH, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *slot;
-  {  // dgamma starts at zero: this thread's lane, its 32 columns of 192..255
-    uint32_t zero[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) zero[j] = 0u;
-    tmem_st32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + 192 + (warp >> 2) * CPT, zero);
-    tmem_st_wait();
-  }
 
   const uint32_t sS = sbase + O_S;
   // (a): K = e.  A = phi(Q) K-major (+32 B per 16 e); B = S' N-major (16 e-rows = 2048 B).
@@ -294,96 +273,87 @@ __global__ void __launch_bounds__(NTH, 2)
     const float rs = ri_cur.x, inv = ri_cur.y;
     mbar_wait(A_DONE, k & 1, fail);
     tc_fence_after();
-    // pass 1: dr, dgamma, du (into the r tile); sums m = du . u, D1 = du . O', D2 = u . O'
-    // (on the raw accumulator O' = den o'; scaled by 1/den once per row below).
-    // Column pairs run on packed f32x2 instructions.
-    const float2 ir2 = f2(inv * rs), rs2 = f2(rs);
-    float2 m2 = f2(0.f), D12 = f2(0.f), D22 = f2(0.f);
+    // pass 1: dr, dgamma, du (into the r tile); sums m = du . u, D1 = du . o', D2 = u . o'.
+    float m = 0.f, D1 = 0.f, D2 = 0.f;
     uint32_t o[CPT];
     {
-      // the running dgamma is read, updated and written back 16 columns at a
-      // time (all 32 held next to O' and the pairs' temporaries would spill)
-      uint32_t g[16];
+      uint32_t g[CPT];
       tmem_ld32_async(tl + f0, o);
-      tmem_ld16_async(tl + 192 + f0, g);  // O' and the first dgamma half under one wait
-      tmem_wait32(o);
-      tmem_tie16(g);
+      if (k > 0) {  // O' and the running dgamma under one wait
+        tmem_ld32_async(tl + 192 + f0, g);
+        tmem_wait32(o);
+        tmem_tie32(g);
+      } else {
+        tmem_wait32(o);
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) g[j] = 0u;
+      }
 #pragma unroll
       for (int ch = 0; ch < NC; ++ch) {
         const int f = f0 + 8 * ch, cc = f >> 3;
-        if (ch == 2) {  // the second dgamma half
-          tmem_st16(tl + 192 + f0, g);
-          tmem_ld16_async(tl + 192 + f0 + 16, g);
-          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-          tmem_tie16(g);
-        }
-        const uint4 yu = *reinterpret_cast<const uint4*>(sy + swz_off(i, cc));
-        const uint4 ru = *reinterpret_cast<const uint4*>(sr + swz_off(i, cc));
-        float2 gm[4], cn[4];
-        cols8(gam + f, gm);
-        cols8(cen + f, cn);
-        const uint32_t yw[4] = {yu.x, yu.y, yu.z, yu.w}, rw[4] = {ru.x, ru.y, ru.z, ru.w};
+        float yv[8], rv[8];
+        unpack8(*reinterpret_cast<const uint4*>(sy + swz_off(i, cc)), yv);
+        unpack8(*reinterpret_cast<const uint4*>(sr + swz_off(i, cc)), rv);
         uint32_t dup[4], drp[4];
 #pragma unroll
-        for (int p2 = 0; p2 < 4; ++p2) {
-          const int kk = 8 * ch + 2 * p2, gk = kk & 15;
-          const float2 O2 = tm2(o, kk);
-          const float2 u = __ffma2_rn(O2, ir2, __fmul2_rn(cn[p2], rs2));
-          const float2 r = bf2(rw[p2]), dy = bf2(yw[p2]);
-          const float2 sg = sigmoid2(r);
-          const float2 av = __fmul2_rn(r, sg);                 // SiLU(r)
-          const float2 dyg = __fmul2_rn(dy, gm[p2]);
-          const float2 du = __fmul2_rn(dyg, av);
-          const float2 G = __ffma2_rn(__fmul2_rn(dy, av), u, tm2(g, gk));
-          g[gk] = __float_as_uint(G.x);
-          g[gk + 1] = __float_as_uint(G.y);
-          // SiLU'(r) = sg (1 + r (1 - sg))
-          const float2 w = __ffma2_rn(r, __ffma2_rn(sg, f2(-1.f), f2(1.f)), f2(1.f));
-          const float2 dr = __fmul2_rn(__fmul2_rn(dyg, u), __fmul2_rn(sg, w));
-          m2 = __ffma2_rn(du, u, m2);
-          D12 = __ffma2_rn(du, O2, D12);
-          D22 = __ffma2_rn(u, O2, D22);
-          dup[p2] = pk2(du);
-          drp[p2] = pk2(dr);
+        for (int j = 0; j < 8; j += 2) {
+          float du2[2], dr2[2];
+#pragma unroll
+          for (int w = 0; w < 2; ++w) {
+            const int jj = j + w, kk = 8 * ch + jj;
+            const float op = __uint_as_float(o[kk]) * inv;  // centred o'
+            const float u = (op + cen[f + jj]) * rs;
+            const float r = rv[jj], dy = yv[jj];
+            const float sg = sigmoid_fast(r);
+            const float av = r * sg;
+            const float dyg = dy * gam[f + jj];
+            du2[w] = dyg * av;
+            g[kk] = __float_as_uint(fmaf(dy * av, u, __uint_as_float(g[kk])));
+            dr2[w] = dyg * u * sg * fmaf(r, 1.f - sg, 1.f);
+            m = fmaf(du2[w], u, m);
+            D1 = fmaf(du2[w], op, D1);
+            D2 = fmaf(u, op, D2);
+          }
+          dup[j / 2] = pack_bf16(du2[0], du2[1]);
+          drp[j / 2] = pack_bf16(dr2[0], dr2[1]);
         }
         *reinterpret_cast<uint4*>(sr + swz_off(i, cc)) = make_uint4(dup[0], dup[1], dup[2], dup[3]);
         if (store)
           *reinterpret_cast<uint4*>((bf16*)a.dr + row * a.lddr + (size_t)h * QD + f) =
               make_uint4(drp[0], drp[1], drp[2], drp[3]);
       }
-      tmem_st16(tl + 192 + f0 + 16, g);
+      tmem_st32(tl + 192 + f0, g);
     }
-    // O' again for pass 2, loading while the row sums are exchanged
-    tmem_ld32_async(tl + f0, o);
     // the row's two column ranges, added in a fixed order
-    xch[(0 + part) * QT + i] = m2.x + m2.y;
-    xch[(2 + part) * QT + i] = D12.x + D12.y;
-    xch[(4 + part) * QT + i] = D22.x + D22.y;
+    xch[(0 + part) * QT + i] = m;
+    xch[(2 + part) * QT + i] = D1;
+    xch[(4 + part) * QT + i] = D2;
     named_bar(1, EW * 32);
-    const float m = (xch[0 * QT + i] + xch[1 * QT + i]) * (1.f / QD);
-    const float D1 = xch[2 * QT + i] + xch[3 * QT + i];
-    const float D2 = xch[4 * QT + i] + xch[5 * QT + i];
-    // dden = -(do . o') / den with do = rs (du - u m) and o' = O' / den
-    const float dden = -rs * inv * inv * fmaf(-m, D2, D1);
+    m = xch[0 * QT + i] + xch[1 * QT + i];
+    D1 = xch[2 * QT + i] + xch[3 * QT + i];
+    D2 = xch[4 * QT + i] + xch[5 * QT + i];
+    m *= 1.f / QD;
+    const float dden = -rs * fmaf(-m, D2, D1) * inv;
     // pass 2: dn = rs (du - u m) / den -> the dy tile
-    tmem_wait32(o);
-    {
-      const float2 mm2 = f2(-m), sc2 = f2(rs * inv);
+    tmem_ld32(tl + f0, o);  // O' again: held through pass 1's exchange it would spill
 #pragma unroll
-      for (int ch = 0; ch < NC; ++ch) {
-        const int f = f0 + 8 * ch, cc = f >> 3;
-        const uint4 dv = *reinterpret_cast<const uint4*>(sr + swz_off(i, cc));
-        const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
-        float2 cn[4];
-        cols8(cen + f, cn);
-        uint32_t dn[4];
+    for (int ch = 0; ch < NC; ++ch) {
+      const int f = f0 + 8 * ch, cc = f >> 3;
+      float du[8];
+      unpack8(*reinterpret_cast<const uint4*>(sr + swz_off(i, cc)), du);
+      uint32_t dn[4];
 #pragma unroll
-        for (int p2 = 0; p2 < 4; ++p2) {
-          const float2 u = __ffma2_rn(tm2(o, 8 * ch + 2 * p2), ir2, __fmul2_rn(cn[p2], rs2));
-          dn[p2] = pk2(__fmul2_rn(__ffma2_rn(u, mm2, bf2(dw[p2])), sc2));
+      for (int j = 0; j < 8; j += 2) {
+        float d2[2];
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          const int jj = j + w;
+          const float u = fmaf(__uint_as_float(o[8 * ch + jj]), inv, cen[f + jj]) * rs;
+          d2[w] = rs * fmaf(-u, m, du[jj]) * inv;
         }
-        *reinterpret_cast<uint4*>(sy + swz_off(i, cc)) = make_uint4(dn[0], dn[1], dn[2], dn[3]);
+        dn[j / 2] = pack_bf16(d2[0], d2[1]);
       }
+      *reinterpret_cast<uint4*>(sy + swz_off(i, cc)) = make_uint4(dn[0], dn[1], dn[2], dn[3]);
     }
     // dden in column 64 of [dn | dden] (first element of the r tile's row);
     // that chunk's du was consumed above by this row's first column range.
@@ -399,26 +369,18 @@ __global__ void __launch_bounds__(NTH, 2)
     mbar_wait(D_DONE, k & 1, fail);
     tc_fence_after();
     tmem_ld32(tl + 64 + f0, o);  // dq~ (waits)
-    {
-      const float2 dd2 = f2(dden);
 #pragma unroll
-      for (int ch = 0; ch < NC; ++ch) {
-        const int f = f0 + 8 * ch, cc = f >> 3;
-        const uint4 qu = *reinterpret_cast<const uint4*>(sq + swz_off(i, cc));
-        const uint32_t qw[4] = {qu.x, qu.y, qu.z, qu.w};
-        float2 zz[4];
-        cols8(zf + f, zz);
-        uint32_t dq[4];
+    for (int ch = 0; ch < NC; ++ch) {
+      const int f = f0 + 8 * ch, cc = f >> 3;
+      float qv[8];
+      unpack8(*reinterpret_cast<const uint4*>(sq + swz_off(i, cc)), qv);
+      uint32_t dq[4];
 #pragma unroll
-        for (int p2 = 0; p2 < 4; ++p2) {
-          const float2 q2 = bf2(qw[p2]);
-          const float2 dphi = make_float2(fminf(1.f, q2.x), fminf(1.f, q2.y));
-          dq[p2] = pk2(__fmul2_rn(__ffma2_rn(dd2, zz[p2], tm2(o, 8 * ch + 2 * p2)), dphi));
-        }
-        if (store)
-          *reinterpret_cast<uint4*>((bf16*)a.dq + row * a.lddq + (size_t)h * QD + f) =
-              make_uint4(dq[0], dq[1], dq[2], dq[3]);
-      }
+      for (int j = 0; j < 8; j += 2)
+        dq[j / 2] = pack_bf16(fmaf(dden, zf[f + j], __uint_as_float(o[8 * ch + j])) * fminf(1.f, qv[j]),
+                              fmaf(dden, zf[f + j + 1], __uint_as_float(o[8 * ch + j + 1])) * fminf(1.f, qv[j + 1]));
+      if (store)
+        *reinterpret_cast<uint4*>((bf16*)a.dq + row * a.lddq + (size_t)h * QD + f) = make_uint4(dq[0], dq[1], dq[2], dq[3]);
     }
     tc_fence_before();
     __syncwarp();
