@@ -46,7 +46,7 @@ NCU_TRAFFIC: dict = {
     "conv bwd": (168216576, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "80d3b995dceb"),
 }
 KERNEL_SOURCE = {"projection gemm": "gemm_tc.cu", "dx~ gemm": "gemm_tc.cu", "dW gemm": "gemm_tc.cu",
-                 "reduce": "core_bf16.cu", "readout": "readout_tc.cu", "bwd_q": "bwd_q_tc.cu",
+                 "reduce": "reduce_tc.cu", "readout": "readout_tc.cu", "bwd_q": "bwd_q_tc.cu",
                  "bwd_kv": "bwd_kv_tc.cu", "conv": "conv.cu", "conv bwd": "conv.cu",
                  "param grads": "layer_misc.cu"}
 
@@ -425,7 +425,7 @@ def run_ours(args, wl, rank: int, world: int, local_rank: int):
         return
     peaks, peak_src = load_peaks()
     alg = algorithmic(wl, T)
-    if any(variant.get(n) not in (None, "tc") for n in ("readout", "bwd_q", "bwd_kv")) and wl.dh == 64:
+    if any(variant.get(n) not in (None, "tc") for n in ("reduce", "readout", "bwd_q", "bwd_kv")) and wl.dh == 64:
         print(f"warning: a d_h = 64 state kernel ran without tcgen05: {variant}", file=sys.stderr)
     dom = max((n for n in kern if n in alg), key=lambda n: kern[n])
     bound, amount = alg[dom]

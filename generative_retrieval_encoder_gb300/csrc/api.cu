@@ -383,6 +383,18 @@ cudaError_t launch_bwd_q_layer_bf16(const BwdQArgs& q, int hd, int n_chunks, int
   return launch_bwd_q_bf16(q, true, n_chunks, st);
 }
 
+// The bf16 state reduction: the tcgen05 kernel where it applies (gate values,
+// d_h = 64), else the mma.sync kernel (softmax logits, other d_h).
+cudaError_t launch_reduce_layer_bf16(const ReduceArgs& a, int n_chunks, int n_tiles, cudaStream_t st,
+                                     const char** nm) {
+  *nm = "reduce[tc]";
+  const cudaError_t e = launch_reduce_tc(a, n_tiles, st);
+  if (e != cudaErrorNotSupported) return e;
+  (void)cudaGetLastError();
+  *nm = "reduce[mma]";
+  return launch_reduce_bf16(a, n_chunks, st);
+}
+
 gbla_status run_reduce(Ctx& c, const void* k, const void* v, int64_t ld, const float* g, int gate_kind, float* state,
                        bf16* state_bf, float* state_m, float* pub_state, float* center, void* ws) {
   const Plan& p = c.p;
@@ -398,8 +410,12 @@ gbla_status run_reduce(Ctx& c, const void* k, const void* v, int64_t ld, const f
   a.pre = c.pre;
   a.center = p.f32 ? nullptr : center;
   a.err = c.kerr;
-  GBLA_CHECK(p.f32 ? launch_reduce_f32(a, p.n_chunks, c.st) : launch_reduce_bf16(a, p.n_chunks, c.st),
-             p.f32 ? "reduce[f32]" : "reduce[mma]");
+  a.tiles = c.tiles;
+  a.partial_slots = partial_slots(p);
+  a.err_out = c.err;
+  const char* nm = "reduce[f32]";
+  GBLA_CHECK(p.f32 ? launch_reduce_f32(a, p.n_chunks, c.st) : launch_reduce_layer_bf16(a, p.n_chunks, p.n_tiles, c.st, &nm),
+             nm);
   return GBLA_OK;
 }
 

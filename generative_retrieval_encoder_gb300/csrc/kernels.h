@@ -44,6 +44,11 @@ struct ReduceArgs {
   float* pub_state;   // [n_seq, H, dh, dh+1] or null
   float* center;      // [n_seq*H][dh] or null: centre the state (see combine_state)
   const int* err;
+  // tcgen05 kernel: its units are 128-row pieces of `tiles` (n_tiles tiles);
+  // one partial slot per (sequence, head) plus one per CTA
+  Tiling tiles;
+  int partial_slots;
+  int* err_out;       // timeout bit of the workspace error word
 };
 
 struct ReadoutArgs {
@@ -144,6 +149,9 @@ cudaError_t launch_plan(const SeqDesc& s, int ntile, const int* tile_sizes, int3
                         int* err, cudaStream_t st);
 
 cudaError_t launch_reduce_bf16(const ReduceArgs& a, int grid_x, cudaStream_t st);
+// tcgen05 state reduction (reduce_tc.cu): d_h = 64, gate values (sigmoid gate
+// or the core API); cudaErrorNotSupported otherwise.
+cudaError_t launch_reduce_tc(const ReduceArgs& a, int n_tiles, cudaStream_t st);
 cudaError_t launch_readout_bf16(const ReadoutArgs& a, bool norm, int grid_x, cudaStream_t st);
 cudaError_t launch_bwd_q_bf16(const BwdQArgs& a, bool norm, int grid_x, cudaStream_t st);
 // tcgen05 query-side backward (bwd_q_tc.cu): d_h = 64, the layer's RMSNorm

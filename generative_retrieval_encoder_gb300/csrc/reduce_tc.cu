@@ -1,0 +1,398 @@
+// State reduction of the bf16 layer and core (Eq. 5/6, gate values) on the
+// 5th-generation tensor cores, for d_h = 64:
+//   [S | z] = sum_j k~_j [v_j | 1]^T,   k~_j = bf16(g_j phi(k_j))
+// ("Gated Bidirectional Linear Attention for Generative Retrieval", section
+// "Core method": the d_h x d_h state formed first, in the order of Eq. 3).  The
+// gated key is rounded to bf16 as the tensor-core operand and z comes from the
+// same rounded values through a column of ones.
+//
+// Work split: the (128-row tile, head) units, head-major, are cut into one
+// contiguous range per CTA (one CTA per SM).  A run of units of one
+// (sequence, head) inside a range is a segment: its [S | z]^T accumulates in
+// one of two TMEM buffers (lane f = state column, lane 64 = z; column e =
+// state row) and, at the segment's end, leaves as one partial, in slot
+// p + blockIdx.x of the partial array (p = h n_seq + b: pairs in unit order, so
+// the slot is unique).  The CTA whose partial completes a (sequence, head)
+// sums the partials in slot order (a fixed order) and centres the state, with
+// the arithmetic of combine_state.
+//
+// Roles, all walking the same units in the same order:
+//   warp 12, lane 0  producer: TMA loads of the phi(k) and v boxes (128 rows x
+//                    128 bytes, 128-byte swizzle) into a 5-stage ring;
+//   warps 0-7        two transform groups of four warps, tile j to group
+//                    j % 2: each thread scales its row of phi(k) by its gate in
+//                    shared memory (k~ = bf16(g phi(k)));
+//   warp 13, lane 0  MMA issuer: D[f][e] += [V | 1]^T k~ with M = 128 (A
+//                    M-major: the V tile, then a constant block whose first
+//                    column is one, so that TMEM lane 64 holds z), N = 64 (the
+//                    k~ tile, N-major), K = 128 rows; its commit frees the stage;
+//   warps 8-11       drain group: at each segment end, the accumulator into
+//                    the partial slot, the arrival count, and the combine when
+//                    this partial completes its (sequence, head).  It never
+//                    holds up the stream: the other accumulator serves the next
+//                    segment meanwhile.
+//
+// Every mbarrier wait is bounded; after one gives up, the kernel finishes its
+// loops without waiting, sets the timeout bit of the error word, waits
+// (bounded) for its copies and MMAs, frees its TMEM and returns.
+#include "core_common.cuh"
+#include "pdl.cuh"
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace gbla {
+namespace {
+
+constexpr int KD = 64;                 // d_h
+constexpr int KT = 128;                // rows per tile (MMA K)
+constexpr int TILE = KT * 128;         // [128 rows][64 bf16], 16 KB
+constexpr int RST = 5;                 // ring stages (phi(k) | v)
+constexpr int STAGE = 2 * TILE;
+constexpr int NG = 2;                  // transform groups of 4 warps
+constexpr int W_DRAIN = 4 * NG;        // first warp of the drain group
+constexpr int W_PROD = W_DRAIN + 4, W_MMA = W_PROD + 1;
+constexpr int NTH = (W_MMA + 1) * 32;
+constexpr int LD = state_ld(KD);       // partial row: 64 S + z + pad
+constexpr int BLD = state_bf_ld(KD);   // bf16 state row
+
+constexpr int O_ST = 0;
+constexpr int O_ONE = O_ST + RST * STAGE;  // 16 rows x 128 B: logical column 0 is one, A's second atom
+constexpr int O_SB = O_ONE + 2048;         // the combine's staging [64][LD] fp32, then the centre [64]
+constexpr int SB = KD * LD * 4 + KD * 4;
+constexpr int O_BAR = O_SB + SB;
+// full[RST], scaled[RST], empty[RST], segf[2], sege[2], drain
+constexpr int NBAR = 3 * RST + 5;
+constexpr int O_MISC = O_BAR + 8 * NBAR;   // TMEM slot, fail, combine flag, first slot, count
+constexpr int SMEM = O_MISC + 32 + 1024;   // + alignment slack
+constexpr int TMEM_COLS = 128;             // two 64-column accumulators
+static_assert(SMEM <= 227 * 1024, "shared memory");
+static_assert(O_ONE % 1024 == 0, "the constant block keeps the swizzle phase of a tile");
+
+__device__ __forceinline__ uint32_t swz_off(int row, int chunk) {
+  return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// One unit = (128-row tile, head): sub-tile `sub` of tile ti of a.tiles,
+// head h.  u = h (n_tiles spt) + ti spt + sub.
+struct RTile {
+  int h, b, seqh;   // head, sequence, b H + h (-1: no rows)
+  int nval;         // valid rows in the tile (rows past them get gate 0)
+  size_t rb;        // first row
+};
+__device__ __forceinline__ RTile rtile_at(const ReduceArgs& a, int u, int upt, int spt) {
+  RTile x;
+  x.h = u / upt;
+  const int r = u - x.h * upt, ti = r / spt, sub = r - ti * spt;
+  int row0, nvalid, tin;
+  x.b = 0; x.nval = 0; x.rb = 0; x.seqh = -1;
+  if (!map_tile(a.seq, a.tiles, ti, x.b, row0, nvalid, tin)) return x;
+  const int R0 = tin * a.tiles.tile + sub * KT;
+  // a tile without rows is no unit, except the first of an empty sequence:
+  // its gates are all 0, so it leaves a zero partial and the state is zero
+  const int rows = slot_rows(a.seq, nvalid);
+  if (min(KT, rows - R0) <= 0 && !(rows == 0 && R0 == 0)) return x;
+  x.nval = max(0, min(KT, nvalid - R0));
+  x.rb = (size_t)row0 + R0;
+  x.seqh = x.b * a.H + x.h;
+  return x;
+}
+// The next unit of [u, u1) with rows, from u on; u1 if none.
+__device__ __forceinline__ int next_rtile(const ReduceArgs& a, int u, int u1, int upt, int spt, RTile& x) {
+  for (; u < u1; ++u) {
+    x = rtile_at(a, u, upt, spt);
+    if (x.seqh >= 0) return u;
+  }
+  x.seqh = -1;
+  return u1;
+}
+// The CTA whose range [floor(N c / G), floor(N (c + 1) / G)) holds unit u.
+__device__ __forceinline__ int cta_of(int u, int n_units, int grid) {
+  return (int)((((long long)u + 1) * grid + n_units - 1) / n_units) - 1;
+}
+
+// The state of one (sequence, head) from its partials in slots first ..
+// first + count - 1, by the 128 threads of the drain group (gt, named barrier
+// bar), with the arithmetic of combine_state in the same order: the partials
+// summed in slot order; the public copy of [S | z]; the centre c_f =
+// sum_e S[e][f] / sum_e z_e; S' = S - z c^T into the fp32 and bf16 states (z
+// column kept).
+__device__ void group_combine(const ReduceArgs& a, int first, int count, int seqh, float* sb, float* cv, int gt,
+                              int bar) {
+  constexpr int N4 = KD * LD / 4;
+  const float4* P = reinterpret_cast<const float4*>(a.partial) + (size_t)first * N4;
+  for (int i = gt; i < N4; i += 128) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < count; ++c) {
+      const float4 q = __ldcg(P + (size_t)c * N4 + i);
+      acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
+    }
+    reinterpret_cast<float4*>(sb)[i] = acc;
+    if (a.pub_state) {
+      const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int e = (4 * i + q) / LD, f = (4 * i + q) % LD;
+        if (f <= KD) a.pub_state[((size_t)seqh * KD + e) * (KD + 1) + f] = v4[q];
+      }
+    }
+  }
+  named_bar(bar, 128);
+  if (a.center) {
+    if (gt < KD) {
+      float Z = 0.f, sf = 0.f;
+      for (int e = 0; e < KD; ++e) Z += sb[e * LD + KD];
+      for (int e = 0; e < KD; ++e) sf += sb[e * LD + gt];
+      const float c = Z > 0.f ? sf / Z : 0.f;
+      cv[gt] = c;
+      a.center[(size_t)seqh * KD + gt] = c;
+    }
+    named_bar(bar, 128);
+  }
+  float* St = a.state + (size_t)seqh * KD * LD;
+  for (int i = gt; i < KD * LD; i += 128) {
+    const int e = i / LD, f = i % LD;
+    float v = sb[i];
+    if (a.center && f < KD) v -= sb[e * LD + KD] * cv[f];
+    St[i] = v;
+    if (a.state_bf) a.state_bf[((size_t)seqh * KD + e) * BLD + f] = __float2bfloat16_rn(v);
+  }
+  if (a.state_bf)
+    for (int i = gt; i < KD * (BLD - LD); i += 128)
+      a.state_bf[((size_t)seqh * KD + i / (BLD - LD)) * BLD + LD + i % (BLD - LD)] = __float2bfloat16_rn(0.f);
+}
+
+__global__ void __launch_bounds__(NTH, 1)
+    k_reduce_tc(const ReduceArgs a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                int upt, int spt, int n_units) {
+  pdl_enter();  // the previous kernel's outputs are visible from here on
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (a.err && *a.err) return;
+  const int G = gridDim.x, nseq = a.seq.n_seq;
+  const int u0 = (int)(((long long)n_units * blockIdx.x) / G);
+  const int u1 = (int)(((long long)n_units * (blockIdx.x + 1)) / G);
+  {
+    RTile x;
+    if (next_rtile(a, u0, u1, upt, spt, x) >= u1) return;  // no rows in this range
+  }
+  uint32_t* slot = reinterpret_cast<uint32_t*>(smem + O_MISC);
+  volatile int* fail = reinterpret_cast<volatile int*>(smem + O_MISC + 4);
+  volatile int* gf = reinterpret_cast<volatile int*>(smem + O_MISC + 16);  // combine flag, first slot, count
+  const uint32_t bar0 = sbase + O_BAR;
+  auto FULL = [&](int s) { return bar0 + 8 * s; };
+  auto SCALED = [&](int s) { return bar0 + 8 * (RST + s); };
+  auto EMPTY = [&](int s) { return bar0 + 8 * (2 * RST + s); };
+  auto SEGF = [&](int b) { return bar0 + 8 * (3 * RST + b); };
+  auto SEGE = [&](int b) { return bar0 + 8 * (3 * RST + 2 + b); };
+  const uint32_t DRAIN = bar0 + 8 * (3 * RST + 4);
+  if (tid == 0) {
+    for (int s = 0; s < RST; ++s) {
+      mbar_init(FULL(s), 1);
+      mbar_init(SCALED(s), 4);  // the four warps of the tile's group
+      mbar_init(EMPTY(s), 1);   // the MMA commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(SEGF(b), 1);
+      mbar_init(SEGE(b), 1);
+    }
+    mbar_init(DRAIN, 1);
+    mbar_init_fence();
+    *fail = 0;
+  }
+  if (tid < 16)  // the constant block: row r holds (1, 0, ..., 0); swz_off places logical chunk c
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<uint4*>(smem + O_ONE + swz_off(tid, c)) = make_uint4(c == 0 ? pack_bf16(1.f, 0.f) : 0u, 0u, 0u, 0u);
+  fence_async_smem();
+  if (warp == 0) tmem_alloc(smem_u32(slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+
+  if (warp == W_PROD) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int j = 0;
+      int last_s[RST];
+#pragma unroll
+      for (int s = 0; s < RST; ++s) last_s[s] = 0;
+      RTile x;
+      for (int u = next_rtile(a, u0, u1, upt, spt, x); u < u1 && !*fail; u = next_rtile(a, u + 1, u1, upt, spt, x), ++j) {
+        const int s = j % RST;
+        if (j >= RST && !mbar_wait(EMPTY(s), ((j / RST) - 1) & 1, fail)) break;
+        const uint32_t st = sbase + O_ST + s * STAGE;
+        mbar_expect_tx(FULL(s), STAGE);
+        tma_load_2d(st, &tmK, FULL(s), x.h * KD, (int)x.rb);
+        tma_load_2d(st + TILE, &tmV, FULL(s), x.h * KD, (int)x.rb);
+        last_s[s] = j + 1;
+      }
+      if (*fail)  // let the copies still in flight land
+        for (int s = 0; s < RST; ++s)
+          if (last_s[s] > 0)
+            for (uint32_t it = 0; it < kPollLimit && !mbar_try_wait(FULL(s), (uint32_t)((last_s[s] - 1) / RST) & 1);
+                 ++it) {
+            }
+    }
+  } else if (warp == W_MMA) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id = idesc_bf16(128, KD, true, true);
+      int j = 0, k = -1, prev = -1;
+      bool first = false;
+      RTile x, y;
+      int u = next_rtile(a, u0, u1, upt, spt, x);
+      while (u < u1 && !*fail) {
+        const int un = next_rtile(a, u + 1, u1, upt, spt, y);
+        const bool last = un >= u1 || y.seqh != x.seqh;
+        if (x.seqh != prev) {  // a new segment: its accumulator is drained by now
+          ++k;
+          prev = x.seqh;
+          first = true;
+          if (k >= 2 && !mbar_wait(SEGE(k & 1), ((k >> 1) - 1) & 1, fail)) break;
+        }
+        const int s = j % RST;
+        if (!mbar_wait(SCALED(s), (j / RST) & 1, fail)) break;
+        tc_fence_after();
+        const uint32_t ka = sbase + O_ST + s * STAGE, va = ka + TILE;
+#pragma unroll
+        for (int kk = 0; kk < KT / 16; ++kk) {
+          // A's second 64-row atom is the constant block, the same 16 rows for
+          // every k step (rows 16 apart share the swizzle phase)
+          const uint32_t a0 = va + 2048 * kk;
+          tc_mma(tmem + (k & 1) * KD, sdesc(a0, sbase + O_ONE - a0, 1024), sdesc(ka + 2048 * kk, 8192, 1024), id,
+                 (first && kk == 0) ? 0u : 1u);
+        }
+        first = false;
+        tc_commit(EMPTY(s));
+        if (last) tc_commit(SEGF(k & 1));
+        u = un;
+        x = y;
+        ++j;
+      }
+      tc_commit(DRAIN);  // completes once every MMA issued above has finished
+      for (uint32_t it = 0; it < kPollLimit && !mbar_try_wait(DRAIN, 0); ++it) {
+      }
+    }
+  } else if (warp < W_DRAIN) {
+    // ------------------------------------------------ transform groups
+    const int grp = warp >> 2, wq = warp & 3;
+    const int row = wq * 32 + lane;
+    int j = 0;
+    RTile x;
+    for (int u = next_rtile(a, u0, u1, upt, spt, x); u < u1; u = next_rtile(a, u + 1, u1, upt, spt, x), ++j) {
+      if (j % NG != grp) continue;
+      // k~ = bf16(g phi(k)) over this thread's row, in place
+      const float g = row < x.nval ? __ldg(a.g + (x.rb + row) * a.ldg + x.h) : 0.f;
+      const int s = j % RST;
+      uint8_t* sk = smem + O_ST + s * STAGE;
+      mbar_wait(FULL(s), (j / RST) & 1, fail);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4* q = reinterpret_cast<uint4*>(sk + swz_off(row, c));
+        const uint4 w4 = *q;
+        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float lo = a.pre ? bf_lo(w[i]) : phi_f(bf_lo(w[i]));
+          const float hi = a.pre ? bf_hi(w[i]) : phi_f(bf_hi(w[i]));
+          o[i] = pack_bf16(lo * g, hi * g);
+        }
+        *q = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(SCALED(s));
+    }
+  } else {
+    // ------------------------------------------------------ drain group
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;  // TMEM lane
+    float* sb = reinterpret_cast<float*>(smem + O_SB);
+    int k = -1, prev = -1;
+    RTile x, y;
+    int u = next_rtile(a, u0, u1, upt, spt, x);
+    while (u < u1) {
+      const int un = next_rtile(a, u + 1, u1, upt, spt, y);
+      const bool last = un >= u1 || y.seqh != x.seqh;
+      if (x.seqh != prev) {
+        ++k;
+        prev = x.seqh;
+      }
+      if (last) {
+        // segment k ends here: [S | z]^T (TMEM lane f = column f of the state,
+        // lane 64 = z; column e = row e) leaves as this CTA's partial of the pair
+        mbar_wait(SEGF(k & 1), (k >> 1) & 1, fail);
+        tc_fence_after();
+        float* P = a.partial + (size_t)(x.h * nseq + x.b + blockIdx.x) * KD * LD;
+        const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16) + (k & 1) * KD;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t v[32];
+          tmem_ld32(tl + 32 * hh, v);
+          if (row < LD)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) P[(size_t)(32 * hh + e) * LD + row] = row <= KD ? __uint_as_float(v[e]) : 0.f;
+        }
+        tc_fence_before();
+        __threadfence();
+        named_bar(1, 128);
+        if (wq == 0 && lane == 0) {
+          mbar_arrive(SEGE(k & 1));  // the accumulator is read
+          // the CTAs holding units of (b, h): c0 .. c0 + count - 1
+          int first, cnt;
+          seq_tiles(a.seq, a.tiles, x.b, first, cnt);
+          const int U0 = x.h * upt + spt * first;
+          int U1 = U0 + spt * max(cnt, 1) - 1;  // the pair's last unit with rows
+          while (U1 > U0 && rtile_at(a, U1, upt, spt).seqh < 0) --U1;
+          const int c0 = cta_of(U0, n_units, G), count = cta_of(U1, n_units, G) - c0 + 1;
+          const bool lastp = atomicAdd(a.counters + x.seqh, 1) == count - 1;
+          gf[0] = (lastp && !*fail) ? 1 : 0;
+          gf[1] = x.h * nseq + x.b + c0;
+          gf[2] = count;
+        }
+        named_bar(1, 128);
+        if (gf[0]) {  // this partial completes (b, h)
+          __threadfence();
+          group_combine(a, gf[1], gf[2], x.seqh, sb, sb + KD * LD, row, 1);
+          named_bar(1, 128);  // the staging and the flags are free again
+        }
+      }
+      u = un;
+      x = y;
+    }
+  }
+  __syncthreads();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+  if (*fail && tid == 0 && a.err_out) atomicOr(a.err_out, kErrTimeout);
+}
+
+}  // namespace
+
+cudaError_t launch_reduce_tc(const ReduceArgs& a, int n_tiles, cudaStream_t st) {
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  if (a.dh != KD || a.gate_kind != GATE_VALUES || !al16(a.k) || !al16(a.v) || !al16(a.partial) || a.ldk % 8 ||
+      a.ldv % 8 || a.seq.T <= 0 || n_tiles <= 0 || a.tiles.tile % KT)
+    return cudaErrorNotSupported;
+  const int spt = a.tiles.tile / KT, upt = n_tiles * spt, n_units = upt * a.H;
+  int grid = n_units < sm_count() ? n_units : sm_count();
+  const int room = a.partial_slots - a.seq.n_seq * a.H;  // partial slots beyond one per (sequence, head)
+  if (room < grid) grid = room;
+  if (grid <= 0) return cudaErrorNotSupported;
+  CUtensorMap tmK, tmV;
+  const uint64_t hd = (uint64_t)a.H * KD;  // the heads' columns of a row
+  // 128-byte L2 promotion: a box row is one head's 128 bytes
+  if (!make_map(&tmK, a.k, hd, (uint64_t)a.seq.T, (uint64_t)a.ldk, 64, KT, false) ||
+      !make_map(&tmV, a.v, hd, (uint64_t)a.seq.T, (uint64_t)a.ldv, 64, KT, false))
+    return cudaErrorNotSupported;
+  cudaError_t e = cudaFuncSetAttribute(k_reduce_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_reduce_tc, dim3(grid), dim3(NTH), SMEM, st, a, tmK, tmV, upt, spt, n_units);
+}
+
+}  // namespace gbla

@@ -101,6 +101,9 @@ def launch_names(fn) -> list[str]:
 # The steps that run on the 5th-generation tensor cores (tcgen05) in the bf16
 # layer at d_h = 64: any fallback to another variant is a regression.
 TC_STEPS_DH64 = ("projection gemm", "readout", "bwd_q", "bwd_kv", "dx~ gemm", "dW gemm")
+# ... and the state reduction, where the gate holds values (sigmoid gate, core
+# API); under the softmax gate it runs the mma.sync kernel (chunk maxima).
+TC_STEPS_DH64_SIGMOID = TC_STEPS_DH64 + ("reduce",)
 
 
 def assert_tc_variants(names, steps=TC_STEPS_DH64):

@@ -27,7 +27,7 @@ import torch
 import oracle
 from generative_retrieval_encoder_gb300 import build, gbla
 from generative_retrieval_encoder_gb300 import workloads as W
-from gbla_cases import TOL, assert_tc_variants, f64, launch_names, max_err
+from gbla_cases import TC_STEPS_DH64_SIGMOID, TOL, assert_tc_variants, f64, launch_names, max_err
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -80,7 +80,7 @@ def test_training_step_whole_batch(name):
     wl = {"train2k": W.FWD_2K, "train8k": W.TRAIN_8K}[name]
     shape, x, P, dy, _ = _inputs(wl)
     out, names = _run(shape, x, P, dy, backward=True)
-    assert_tc_variants(names)
+    assert_tc_variants(names, TC_STEPS_DH64_SIGMOID)
     Pr = {n: f64(t) for n, t in P.items()}
     st, ln = oracle.seqs(wl.B, wl.L)
     xr, dyr = f64(x), f64(dy)
@@ -99,7 +99,7 @@ def test_long_history_forward_all_sequences():
     wl = W.LONG_32K
     shape, x, P, dy, _ = _inputs(wl)
     out, names = _run(shape, x, P, dy, backward=False)
-    assert_tc_variants(names, ("projection gemm", "readout"))
+    assert_tc_variants(names, ("projection gemm", "reduce", "readout"))
     Pr = {n: f64(t) for n, t in P.items()}
     st, ln = oracle.seqs(wl.B, wl.L)
     ref = oracle.gbla_forward(f64(x), Pr, wl.H, wl.dh, st, ln, _gate(wl), wl.eps)
