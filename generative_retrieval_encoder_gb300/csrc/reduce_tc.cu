@@ -63,7 +63,7 @@ constexpr int O_BAR = O_SB + SB;
 // full[RST], scaled[RST], empty[RST], segf[2], sege[2], drain
 constexpr int NBAR = 3 * RST + 5;
 constexpr int O_MISC = O_BAR + 8 * NBAR;   // TMEM slot, fail, combine flag, first slot, count
-constexpr int SMEM = O_MISC + 32 + 1024;   // + alignment slack
+constexpr int SMEM = O_MISC + 48 + 1024;   // + alignment slack
 constexpr int TMEM_COLS = 128;             // two 64-column accumulators
 static_assert(SMEM <= 227 * 1024, "shared memory");
 static_assert(O_ONE % 1024 == 0, "the constant block keeps the swizzle phase of a tile");
@@ -111,56 +111,81 @@ __device__ __forceinline__ int cta_of(int u, int n_units, int grid) {
 }
 
 // The state of one (sequence, head) from its partials in slots first ..
-// first + count - 1, by the 128 threads of the drain group (gt, named barrier
-// bar), with the arithmetic of combine_state in the same order: the partials
-// summed in slot order; the public copy of [S | z]; the centre c_f =
-// sum_e S[e][f] / sum_e z_e; S' = S - z c^T into the fp32 and bf16 states (z
-// column kept).
-__device__ void group_combine(const ReduceArgs& a, int first, int count, int seqh, float* sb, float* cv, int gt,
-                              int bar) {
+// first + count - 1, by NT threads (gt = thread index among them; bar = their
+// named barrier, 0 for the whole CTA), with the arithmetic of combine_state in
+// the same order: the partials summed in slot order; the public copy of
+// [S | z]; the centre c_f = sum_e S[e][f] / sum_e z_e; S' = S - z c^T into the
+// fp32 and bf16 states (z column kept).  The partial loads of a thread are
+// independent and issued together.
+template <int NT>
+__device__ void combine(const ReduceArgs& a, int first, int count, int seqh, float* sb, float* cv, int gt, int bar) {
   constexpr int N4 = KD * LD / 4;
-  const float4* P = reinterpret_cast<const float4*>(a.partial) + (size_t)first * N4;
-  for (int i = gt; i < N4; i += 128) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = 0; c < count; ++c) {
-      const float4 q = __ldcg(P + (size_t)c * N4 + i);
-      acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
-    }
-    reinterpret_cast<float4*>(sb)[i] = acc;
-    if (a.pub_state) {
-      const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
+  constexpr int PER = (N4 + NT - 1) / NT;
+  const float4* __restrict__ P = reinterpret_cast<const float4*>(a.partial) + (size_t)first * N4;
+  float4 acc[PER];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int e = (4 * i + q) / LD, f = (4 * i + q) % LD;
-        if (f <= KD) a.pub_state[((size_t)seqh * KD + e) * (KD + 1) + f] = v4[q];
+  for (int q = 0; q < PER; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c = 0; c < count; ++c) {
+    float4 v[PER];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int i = gt + q * NT;
+      v[q] = i < N4 ? __ldcg(P + (size_t)c * N4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      acc[q].x += v[q].x; acc[q].y += v[q].y; acc[q].z += v[q].z; acc[q].w += v[q].w;
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int i = gt + q * NT;
+    if (i >= N4) continue;
+    reinterpret_cast<float4*>(sb)[i] = acc[q];
+    if (a.pub_state) {
+      const float v4[4] = {acc[q].x, acc[q].y, acc[q].z, acc[q].w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int e = (4 * i + w) / LD, f = (4 * i + w) % LD;
+        if (f <= KD) a.pub_state[((size_t)seqh * KD + e) * (KD + 1) + f] = v4[w];
       }
     }
   }
-  named_bar(bar, 128);
+  named_bar(bar, NT);
   if (a.center) {
     if (gt < KD) {
       float Z = 0.f, sf = 0.f;
+#pragma unroll 16
       for (int e = 0; e < KD; ++e) Z += sb[e * LD + KD];
+#pragma unroll 16
       for (int e = 0; e < KD; ++e) sf += sb[e * LD + gt];
       const float c = Z > 0.f ? sf / Z : 0.f;
       cv[gt] = c;
       a.center[(size_t)seqh * KD + gt] = c;
     }
-    named_bar(bar, 128);
+    named_bar(bar, NT);
   }
-  float* St = a.state + (size_t)seqh * KD * LD;
-  for (int i = gt; i < KD * LD; i += 128) {
-    const int e = i / LD, f = i % LD;
-    float v = sb[i];
-    if (a.center && f < KD) v -= sb[e * LD + KD] * cv[f];
+  // S' = S - z c^T: LD = 72 floats a row, so a float4 never straddles a row
+  float4* St = reinterpret_cast<float4*>(a.state + (size_t)seqh * KD * LD);
+  for (int i = gt; i < N4; i += NT) {
+    const int e = (4 * i) / LD, f = (4 * i) % LD;
+    float4 v = reinterpret_cast<const float4*>(sb)[i];
+    if (a.center && f < KD) {
+      const float z = sb[e * LD + KD];
+      v.x -= z * cv[f]; v.y -= z * cv[f + 1]; v.z -= z * cv[f + 2]; v.w -= z * cv[f + 3];
+    }
     St[i] = v;
-    if (a.state_bf) a.state_bf[((size_t)seqh * KD + e) * BLD + f] = __float2bfloat16_rn(v);
+    if (a.state_bf)
+      *reinterpret_cast<uint2*>(a.state_bf + ((size_t)seqh * KD + e) * BLD + f) =
+          make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
   }
-  if (a.state_bf)
-    for (int i = gt; i < KD * (BLD - LD); i += 128)
-      a.state_bf[((size_t)seqh * KD + i / (BLD - LD)) * BLD + LD + i % (BLD - LD)] = __float2bfloat16_rn(0.f);
+  if (a.state_bf)  // the row's last BLD - LD (= 8) columns
+    for (int e = gt; e < KD; e += NT)
+      *reinterpret_cast<uint4*>(a.state_bf + ((size_t)seqh * KD + e) * BLD + LD) = make_uint4(0u, 0u, 0u, 0u);
 }
+static_assert(LD % 4 == 0 && (BLD - LD) == 8 && BLD % 8 == 0, "vector stores of the state rows");
 
+template <bool PRE>
 __global__ void __launch_bounds__(NTH, 1)
     k_reduce_tc(const ReduceArgs a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 int upt, int spt, int n_units) {
@@ -179,7 +204,8 @@ __global__ void __launch_bounds__(NTH, 1)
   }
   uint32_t* slot = reinterpret_cast<uint32_t*>(smem + O_MISC);
   volatile int* fail = reinterpret_cast<volatile int*>(smem + O_MISC + 4);
-  volatile int* gf = reinterpret_cast<volatile int*>(smem + O_MISC + 16);  // combine flag, first slot, count
+  // combine flag, first slot, count, and the (sequence, head) whose combine waits for the end (-1: none)
+  volatile int* gf = reinterpret_cast<volatile int*>(smem + O_MISC + 16);
   const uint32_t bar0 = sbase + O_BAR;
   auto FULL = [&](int s) { return bar0 + 8 * s; };
   auto SCALED = [&](int s) { return bar0 + 8 * (RST + s); };
@@ -200,6 +226,8 @@ __global__ void __launch_bounds__(NTH, 1)
     mbar_init(DRAIN, 1);
     mbar_init_fence();
     *fail = 0;
+    gf[0] = 0;
+    gf[3] = -1;
   }
   if (tid < 16)  // the constant block: row r holds (1, 0, ..., 0); swz_off places logical chunk c
 #pragma unroll
@@ -280,32 +308,44 @@ __global__ void __launch_bounds__(NTH, 1)
     // ------------------------------------------------ transform groups
     const int grp = warp >> 2, wq = warp & 3;
     const int row = wq * 32 + lane;
+    auto gate_of = [&](const RTile& t) { return row < t.nval ? __ldg(a.g + (t.rb + row) * a.ldg + t.h) : 0.f; };
+    // this group's tiles j = grp, grp + NG, ...; the gate of the next one loads under the current one
     int j = 0;
     RTile x;
-    for (int u = next_rtile(a, u0, u1, upt, spt, x); u < u1; u = next_rtile(a, u + 1, u1, upt, spt, x), ++j) {
-      if (j % NG != grp) continue;
+    int u = next_rtile(a, u0, u1, upt, spt, x);
+    for (; u < u1 && j < grp; ++j) u = next_rtile(a, u + 1, u1, upt, spt, x);
+    float g = u < u1 ? gate_of(x) : 0.f;
+    while (u < u1) {
+      RTile xn = x;
+      int un = u;
+      for (int t = 0; t < NG && un < u1; ++t) un = next_rtile(a, un + 1, u1, upt, spt, xn);
+      const float gn = un < u1 ? gate_of(xn) : 0.f;
       // k~ = bf16(g phi(k)) over this thread's row, in place
-      const float g = row < x.nval ? __ldg(a.g + (x.rb + row) * a.ldg + x.h) : 0.f;
       const int s = j % RST;
       uint8_t* sk = smem + O_ST + s * STAGE;
       mbar_wait(FULL(s), (j / RST) & 1, fail);
+      uint4 w4[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) w4[c] = *reinterpret_cast<const uint4*>(sk + swz_off(row, c));
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        uint4* q = reinterpret_cast<uint4*>(sk + swz_off(row, c));
-        const uint4 w4 = *q;
-        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+        const uint32_t w[4] = {w4[c].x, w4[c].y, w4[c].z, w4[c].w};
         uint32_t o[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float lo = a.pre ? bf_lo(w[i]) : phi_f(bf_lo(w[i]));
-          const float hi = a.pre ? bf_hi(w[i]) : phi_f(bf_hi(w[i]));
+          const float lo = PRE ? bf_lo(w[i]) : phi_f(bf_lo(w[i]));
+          const float hi = PRE ? bf_hi(w[i]) : phi_f(bf_hi(w[i]));
           o[i] = pack_bf16(lo * g, hi * g);
         }
-        *q = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(sk + swz_off(row, c)) = make_uint4(o[0], o[1], o[2], o[3]);
       }
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(SCALED(s));
+      x = xn;
+      u = un;
+      g = gn;
+      j += NG;
     }
   } else {
     // ------------------------------------------------------ drain group
@@ -356,9 +396,13 @@ __global__ void __launch_bounds__(NTH, 1)
         }
         named_bar(1, 128);
         if (gf[0]) {  // this partial completes (b, h)
-          __threadfence();
-          group_combine(a, gf[1], gf[2], x.seqh, sb, sb + KD * LD, row, 1);
-          named_bar(1, 128);  // the staging and the flags are free again
+          if (un >= u1) {  // the CTA's last segment: every warp combines it after the loops
+            if (row == 0) gf[3] = x.seqh;
+          } else {
+            __threadfence();
+            combine<128>(a, gf[1], gf[2], x.seqh, sb, sb + KD * LD, row, 1);
+            named_bar(1, 128);  // the staging and the flags are free again
+          }
         }
       }
       u = un;
@@ -366,6 +410,11 @@ __global__ void __launch_bounds__(NTH, 1)
     }
   }
   __syncthreads();
+  if (gf[0] && gf[3] >= 0 && !*fail) {
+    __threadfence();
+    combine<NTH>(a, gf[1], gf[2], gf[3], reinterpret_cast<float*>(smem + O_SB),
+                 reinterpret_cast<float*>(smem + O_SB) + KD * LD, tid, 0);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
@@ -390,9 +439,10 @@ cudaError_t launch_reduce_tc(const ReduceArgs& a, int n_tiles, cudaStream_t st) 
   if (!make_map(&tmK, a.k, hd, (uint64_t)a.seq.T, (uint64_t)a.ldk, 64, KT, false) ||
       !make_map(&tmV, a.v, hd, (uint64_t)a.seq.T, (uint64_t)a.ldv, 64, KT, false))
     return cudaErrorNotSupported;
-  cudaError_t e = cudaFuncSetAttribute(k_reduce_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  auto kern = a.pre ? k_reduce_tc<true> : k_reduce_tc<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_reduce_tc, dim3(grid), dim3(NTH), SMEM, st, a, tmK, tmV, upt, spt, n_units);
+  return launch_pdl(kern, dim3(grid), dim3(NTH), SMEM, st, a, tmK, tmV, upt, spt, n_units);
 }
 
 }  // namespace gbla
