@@ -6,7 +6,7 @@
 // gated key is rounded to bf16 as the tensor-core operand and z comes from the
 // same rounded values through a column of ones.
 //
-// Work split: the (128-row tile, head) units, head-major, are cut into one
+// Work split: the (256-row tile, head) units, head-major, are cut into one
 // contiguous range per CTA (one CTA per SM).  A run of units of one
 // (sequence, head) inside a range is a segment: its [S | z]^T accumulates in
 // one of two TMEM buffers (lane f = state column, lane 64 = z; column e =
@@ -18,14 +18,18 @@
 //
 // Roles, all walking the same units in the same order:
 //   warp 12, lane 0  producer: TMA loads of the phi(k) and v boxes (128 rows x
-//                    128 bytes, 128-byte swizzle) into a 5-stage ring;
-//   warps 0-7        two transform groups of four warps, tile j to group
-//                    j % 2: each thread scales its row of phi(k) by its gate in
-//                    shared memory (k~ = bf16(g phi(k)));
+//                    128 bytes, 128-byte swizzle; two of each per tile) into a
+//                    3-stage ring, and the tile's descriptor (segment, segment
+//                    end) into a small shared ring read by the MMA issuer;
+//   warps 0-7        two transform groups of four warps, group g on rows
+//                    128 g .. 128 g + 127 of every tile: each thread scales its
+//                    row of phi(k) by its gate in shared memory
+//                    (k~ = bf16(g phi(k)));
 //   warp 13, lane 0  MMA issuer: D[f][e] += [V | 1]^T k~ with M = 128 (A
 //                    M-major: the V tile, then a constant block whose first
 //                    column is one, so that TMEM lane 64 holds z), N = 64 (the
-//                    k~ tile, N-major), K = 128 rows; its commit frees the stage;
+//                    k~ tile, N-major), K = the tile's rows in 16-row steps; its
+//                    commit frees the stage;
 //   warps 8-11       drain group: at each segment end, the accumulator into
 //                    the partial slot, the arrival count, and the combine when
 //                    this partial completes its (sequence, head).  It never
@@ -44,10 +48,11 @@ namespace gbla {
 namespace {
 
 constexpr int KD = 64;                 // d_h
-constexpr int KT = 128;                // rows per tile (MMA K)
+constexpr int KT = 128;                // rows per copy box (and per transform group)
+constexpr int TT = 2 * KT;             // rows per tile (MMA K, in 16-row steps)
 constexpr int TILE = KT * 128;         // [128 rows][64 bf16], 16 KB
-constexpr int RST = 5;                 // ring stages (phi(k) | v)
-constexpr int STAGE = 2 * TILE;
+constexpr int RST = 3;                 // ring stages: phi(k) rows 0-127 | 128-255, v rows 0-127 | 128-255
+constexpr int STAGE = 4 * TILE;
 constexpr int NG = 2;                  // transform groups of 4 warps
 constexpr int W_DRAIN = 4 * NG;        // first warp of the drain group
 constexpr int W_PROD = W_DRAIN + 4, W_MMA = W_PROD + 1;
@@ -62,7 +67,8 @@ constexpr int SB = KD * LD * 4 + KD * 4;
 constexpr int O_BAR = O_SB + SB;
 // full[RST], scaled[RST], empty[RST], segf[2], sege[2], drain
 constexpr int NBAR = 3 * RST + 5;
-constexpr int O_MISC = O_BAR + 8 * NBAR;   // TMEM slot, fail, combine flag, first slot, count
+constexpr int O_DESC = O_BAR + 8 * NBAR;   // per stage: (sequence, head), segment end, halves
+constexpr int O_MISC = O_DESC + 16 * RST;  // TMEM slot, fail, combine flag, first slot, count, pending
 constexpr int SMEM = O_MISC + 48 + 1024;   // + alignment slack
 constexpr int TMEM_COLS = 128;             // two 64-column accumulators
 static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -72,11 +78,12 @@ __device__ __forceinline__ uint32_t swz_off(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-// One unit = (128-row tile, head): sub-tile `sub` of tile ti of a.tiles,
+// One unit = (256-row tile, head): sub-tile `sub` of tile ti of a.tiles,
 // head h.  u = h (n_tiles spt) + ti spt + sub.
 struct RTile {
   int h, b, seqh;   // head, sequence, b H + h (-1: no rows)
   int nval;         // valid rows in the tile (rows past them get gate 0)
+  int halves;       // 128-row halves holding rows of the sequence slot (1 or 2)
   size_t rb;        // first row
 };
 __device__ __forceinline__ RTile rtile_at(const ReduceArgs& a, int u, int upt, int spt) {
@@ -84,14 +91,15 @@ __device__ __forceinline__ RTile rtile_at(const ReduceArgs& a, int u, int upt, i
   x.h = u / upt;
   const int r = u - x.h * upt, ti = r / spt, sub = r - ti * spt;
   int row0, nvalid, tin;
-  x.b = 0; x.nval = 0; x.rb = 0; x.seqh = -1;
+  x.b = 0; x.nval = 0; x.rb = 0; x.seqh = -1; x.halves = 1;
   if (!map_tile(a.seq, a.tiles, ti, x.b, row0, nvalid, tin)) return x;
-  const int R0 = tin * a.tiles.tile + sub * KT;
+  const int R0 = tin * a.tiles.tile + sub * TT;
   // a tile without rows is no unit, except the first of an empty sequence:
   // its gates are all 0, so it leaves a zero partial and the state is zero
   const int rows = slot_rows(a.seq, nvalid);
-  if (min(KT, rows - R0) <= 0 && !(rows == 0 && R0 == 0)) return x;
-  x.nval = max(0, min(KT, nvalid - R0));
+  if (min(TT, rows - R0) <= 0 && !(rows == 0 && R0 == 0)) return x;
+  x.halves = rows - R0 > KT ? 2 : 1;
+  x.nval = max(0, min(TT, nvalid - R0));
   x.rb = (size_t)row0 + R0;
   x.seqh = x.b * a.H + x.h;
   return x;
@@ -104,6 +112,13 @@ __device__ __forceinline__ int next_rtile(const ReduceArgs& a, int u, int u1, in
   }
   x.seqh = -1;
   return u1;
+}
+// The units with rows in [u0, u1).
+__device__ __forceinline__ int n_tiles_cta(const ReduceArgs& a, int u0, int u1, int upt, int spt) {
+  int n = 0;
+  RTile x;
+  for (int u = next_rtile(a, u0, u1, upt, spt, x); u < u1; u = next_rtile(a, u + 1, u1, upt, spt, x)) ++n;
+  return n;
 }
 // The CTA whose range [floor(N c / G), floor(N (c + 1) / G)) holds unit u.
 __device__ __forceinline__ int cta_of(int u, int n_units, int grid) {
@@ -189,6 +204,10 @@ template <bool PRE>
 __global__ void __launch_bounds__(NTH, 1)
     k_reduce_tc(const ReduceArgs a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 int upt, int spt, int n_units) {
+  if (threadIdx.x == W_PROD * 32) {  // the descriptors load while the previous kernel finishes
+    tma_prefetch_map(&tmK);
+    tma_prefetch_map(&tmV);
+  }
   pdl_enter();  // the previous kernel's outputs are visible from here on
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -206,6 +225,7 @@ __global__ void __launch_bounds__(NTH, 1)
   volatile int* fail = reinterpret_cast<volatile int*>(smem + O_MISC + 4);
   // combine flag, first slot, count, and the (sequence, head) whose combine waits for the end (-1: none)
   volatile int* gf = reinterpret_cast<volatile int*>(smem + O_MISC + 16);
+  int* desc = reinterpret_cast<int*>(smem + O_DESC);  // [stage][seqh, segment end, halves, -]
   const uint32_t bar0 = sbase + O_BAR;
   auto FULL = [&](int s) { return bar0 + 8 * s; };
   auto SCALED = [&](int s) { return bar0 + 8 * (RST + s); };
@@ -216,8 +236,8 @@ __global__ void __launch_bounds__(NTH, 1)
   if (tid == 0) {
     for (int s = 0; s < RST; ++s) {
       mbar_init(FULL(s), 1);
-      mbar_init(SCALED(s), 4);  // the four warps of the tile's group
-      mbar_init(EMPTY(s), 1);   // the MMA commit
+      mbar_init(SCALED(s), 4 * NG);  // the eight transform warps
+      mbar_init(EMPTY(s), 1);        // the MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(SEGF(b), 1);
@@ -247,15 +267,25 @@ __global__ void __launch_bounds__(NTH, 1)
       int last_s[RST];
 #pragma unroll
       for (int s = 0; s < RST; ++s) last_s[s] = 0;
-      RTile x;
-      for (int u = next_rtile(a, u0, u1, upt, spt, x); u < u1 && !*fail; u = next_rtile(a, u + 1, u1, upt, spt, x), ++j) {
+      RTile x, y;
+      int u = next_rtile(a, u0, u1, upt, spt, x);
+      while (u < u1 && !*fail) {
+        const int un = next_rtile(a, u + 1, u1, upt, spt, y);
         const int s = j % RST;
         if (j >= RST && !mbar_wait(EMPTY(s), ((j / RST) - 1) & 1, fail)) break;
+        desc[4 * s + 0] = x.seqh;
+        desc[4 * s + 1] = (un >= u1 || y.seqh != x.seqh) ? 1 : 0;
+        desc[4 * s + 2] = x.halves;
         const uint32_t st = sbase + O_ST + s * STAGE;
-        mbar_expect_tx(FULL(s), STAGE);
-        tma_load_2d(st, &tmK, FULL(s), x.h * KD, (int)x.rb);
-        tma_load_2d(st + TILE, &tmV, FULL(s), x.h * KD, (int)x.rb);
+        mbar_expect_tx(FULL(s), 2 * x.halves * TILE);
+        for (int hf = 0; hf < x.halves; ++hf) {
+          tma_load_2d(st + hf * TILE, &tmK, FULL(s), x.h * KD, (int)x.rb + hf * KT);
+          tma_load_2d(st + (2 + hf) * TILE, &tmV, FULL(s), x.h * KD, (int)x.rb + hf * KT);
+        }
         last_s[s] = j + 1;
+        u = un;
+        x = y;
+        ++j;
       }
       if (*fail)  // let the copies still in flight land
         for (int s = 0; s < RST; ++s)
@@ -268,37 +298,33 @@ __global__ void __launch_bounds__(NTH, 1)
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t id = idesc_bf16(128, KD, true, true);
-      int j = 0, k = -1, prev = -1;
-      bool first = false;
-      RTile x, y;
-      int u = next_rtile(a, u0, u1, upt, spt, x);
-      while (u < u1 && !*fail) {
-        const int un = next_rtile(a, u + 1, u1, upt, spt, y);
-        const bool last = un >= u1 || y.seqh != x.seqh;
-        if (x.seqh != prev) {  // a new segment: its accumulator is drained by now
-          ++k;
-          prev = x.seqh;
-          first = true;
-          if (k >= 2 && !mbar_wait(SEGE(k & 1), ((k >> 1) - 1) & 1, fail)) break;
-        }
+      int k = -1, prev = -1;
+      const int nj = n_tiles_cta(a, u0, u1, upt, spt);
+      for (int j = 0; j < nj && !*fail; ++j) {
         const int s = j % RST;
         if (!mbar_wait(SCALED(s), (j / RST) & 1, fail)) break;
         tc_fence_after();
-        const uint32_t ka = sbase + O_ST + s * STAGE, va = ka + TILE;
-#pragma unroll
-        for (int kk = 0; kk < KT / 16; ++kk) {
-          // A's second 64-row atom is the constant block, the same 16 rows for
-          // every k step (rows 16 apart share the swizzle phase)
-          const uint32_t a0 = va + 2048 * kk;
-          tc_mma(tmem + (k & 1) * KD, sdesc(a0, sbase + O_ONE - a0, 1024), sdesc(ka + 2048 * kk, 8192, 1024), id,
+        const int seqh = desc[4 * s + 0], last = desc[4 * s + 1], halves = desc[4 * s + 2];
+        bool first = false;
+        if (seqh != prev) {  // a new segment: its accumulator is drained by now
+          ++k;
+          prev = seqh;
+          first = true;
+          if (k >= 2 && !mbar_wait(SEGE(k & 1), ((k >> 1) - 1) & 1, fail)) break;
+          tc_fence_after();
+        }
+        const uint32_t st = sbase + O_ST + s * STAGE;
+        for (int kk = 0; kk < 8 * halves; ++kk) {
+          // K step kk: rows 16 kk .. of the tile, in the half kk / 8.  A's
+          // second 64-row atom is the constant block, the same 16 rows for
+          // every step (rows 16 apart share the swizzle phase).
+          const uint32_t off = (kk >> 3) * TILE + 2048 * (kk & 7);
+          const uint32_t a0 = st + 2 * TILE + off;
+          tc_mma(tmem + (k & 1) * KD, sdesc(a0, sbase + O_ONE - a0, 1024), sdesc(st + off, 8192, 1024), id,
                  (first && kk == 0) ? 0u : 1u);
         }
-        first = false;
         tc_commit(EMPTY(s));
         if (last) tc_commit(SEGF(k & 1));
-        u = un;
-        x = y;
-        ++j;
       }
       tc_commit(DRAIN);  // completes once every MMA issued above has finished
       for (uint32_t it = 0; it < kPollLimit && !mbar_try_wait(DRAIN, 0); ++it) {
@@ -307,45 +333,45 @@ __global__ void __launch_bounds__(NTH, 1)
   } else if (warp < W_DRAIN) {
     // ------------------------------------------------ transform groups
     const int grp = warp >> 2, wq = warp & 3;
-    const int row = wq * 32 + lane;
+    const int row = grp * KT + wq * 32 + lane;  // tile row
     auto gate_of = [&](const RTile& t) { return row < t.nval ? __ldg(a.g + (t.rb + row) * a.ldg + t.h) : 0.f; };
-    // this group's tiles j = grp, grp + NG, ...; the gate of the next one loads under the current one
+    // every tile; the gate of the next one loads under the current one
     int j = 0;
     RTile x;
     int u = next_rtile(a, u0, u1, upt, spt, x);
-    for (; u < u1 && j < grp; ++j) u = next_rtile(a, u + 1, u1, upt, spt, x);
     float g = u < u1 ? gate_of(x) : 0.f;
     while (u < u1) {
-      RTile xn = x;
-      int un = u;
-      for (int t = 0; t < NG && un < u1; ++t) un = next_rtile(a, un + 1, u1, upt, spt, xn);
+      RTile xn;
+      const int un = next_rtile(a, u + 1, u1, upt, spt, xn);
       const float gn = un < u1 ? gate_of(xn) : 0.f;
-      // k~ = bf16(g phi(k)) over this thread's row, in place
       const int s = j % RST;
-      uint8_t* sk = smem + O_ST + s * STAGE;
       mbar_wait(FULL(s), (j / RST) & 1, fail);
-      uint4 w4[8];
+      if (grp < x.halves) {  // k~ = bf16(g phi(k)) over this thread's row, in place
+        uint8_t* sk = smem + O_ST + s * STAGE + grp * TILE;
+        const int r = wq * 32 + lane;
+        uint4 w4[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) w4[c] = *reinterpret_cast<const uint4*>(sk + swz_off(row, c));
+        for (int c = 0; c < 8; ++c) w4[c] = *reinterpret_cast<const uint4*>(sk + swz_off(r, c));
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t w[4] = {w4[c].x, w4[c].y, w4[c].z, w4[c].w};
-        uint32_t o[4];
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t w[4] = {w4[c].x, w4[c].y, w4[c].z, w4[c].w};
+          uint32_t o[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float lo = PRE ? bf_lo(w[i]) : phi_f(bf_lo(w[i]));
-          const float hi = PRE ? bf_hi(w[i]) : phi_f(bf_hi(w[i]));
-          o[i] = pack_bf16(lo * g, hi * g);
+          for (int i = 0; i < 4; ++i) {
+            const float lo = PRE ? bf_lo(w[i]) : phi_f(bf_lo(w[i]));
+            const float hi = PRE ? bf_hi(w[i]) : phi_f(bf_hi(w[i]));
+            o[i] = pack_bf16(lo * g, hi * g);
+          }
+          *reinterpret_cast<uint4*>(sk + swz_off(r, c)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        *reinterpret_cast<uint4*>(sk + swz_off(row, c)) = make_uint4(o[0], o[1], o[2], o[3]);
+        fence_async_smem();
       }
-      fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(SCALED(s));
       x = xn;
       u = un;
       g = gn;
-      j += NG;
+      ++j;
     }
   } else {
     // ------------------------------------------------------ drain group
@@ -426,9 +452,9 @@ __global__ void __launch_bounds__(NTH, 1)
 cudaError_t launch_reduce_tc(const ReduceArgs& a, int n_tiles, cudaStream_t st) {
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   if (a.dh != KD || a.gate_kind != GATE_VALUES || !al16(a.k) || !al16(a.v) || !al16(a.partial) || a.ldk % 8 ||
-      a.ldv % 8 || a.seq.T <= 0 || n_tiles <= 0 || a.tiles.tile % KT)
+      a.ldv % 8 || a.seq.T <= 0 || n_tiles <= 0 || a.tiles.tile % TT)
     return cudaErrorNotSupported;
-  const int spt = a.tiles.tile / KT, upt = n_tiles * spt, n_units = upt * a.H;
+  const int spt = a.tiles.tile / TT, upt = n_tiles * spt, n_units = upt * a.H;
   int grid = n_units < sm_count() ? n_units : sm_count();
   const int room = a.partial_slots - a.seq.n_seq * a.H;  // partial slots beyond one per (sequence, head)
   if (room < grid) grid = room;
