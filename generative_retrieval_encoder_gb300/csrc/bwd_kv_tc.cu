@@ -341,6 +341,7 @@ __global__ void __launch_bounds__(NTH, 1)
       }
     }
   }
+  __syncwarp();  // single-lane roles rejoin their warps: the CTA barrier below is warp-aligned
   __syncthreads();
   const bool bad = *fail != 0;
   tc_fence_before();

@@ -444,6 +444,7 @@ __global__ void __launch_bounds__(NTH, 2)
         for (uint32_t it = 0; it < kPollLimit && !mbar_try_wait(FULL(s), (uint32_t)((issued[s] - 1) / QST) & 1);
              ++it) {
         }
+  __syncwarp();  // single-lane roles rejoin their warps: the CTA barrier below is warp-aligned
   __syncthreads();
   const bool bad = *fail != 0;
 

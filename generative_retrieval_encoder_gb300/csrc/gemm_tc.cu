@@ -409,6 +409,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   }
 
+  __syncwarp();  // single-lane roles rejoin their warps: the CTA barrier below is warp-aligned
   __syncthreads();
   if (*fail) {
     if (threadIdx.x == 0) {
@@ -423,6 +424,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
     }
+    __syncwarp();
     __syncthreads();
   }
   tc_fence_before();

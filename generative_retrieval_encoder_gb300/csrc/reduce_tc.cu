@@ -130,10 +130,11 @@ __device__ __forceinline__ int cta_of(int u, int n_units, int grid) {
 // named barrier, 0 for the whole CTA), with the arithmetic of combine_state in
 // the same order: the partials summed in slot order; the public copy of
 // [S | z]; the centre c_f = sum_e S[e][f] / sum_e z_e; S' = S - z c^T into the
-// fp32 and bf16 states (z column kept).  The partial loads of a thread are
-// independent and issued together.
+// fp32 and bf16 states (z column kept).  combine_sum stages the sum in sb
+// [64][LD]; combine_finish centres and writes it.  The partial loads of a
+// thread are independent and issued together.
 template <int NT>
-__device__ void combine(const ReduceArgs& a, int first, int count, int seqh, float* sb, float* cv, int gt, int bar) {
+__device__ void combine_sum(const ReduceArgs& a, int first, int count, int seqh, float* sb, int gt) {
   constexpr int N4 = KD * LD / 4;
   constexpr int PER = (N4 + NT - 1) / NT;
   const float4* __restrict__ P = reinterpret_cast<const float4*>(a.partial) + (size_t)first * N4;
@@ -166,7 +167,10 @@ __device__ void combine(const ReduceArgs& a, int first, int count, int seqh, flo
       }
     }
   }
-  named_bar(bar, NT);
+}
+template <int NT>
+__device__ void combine_finish(const ReduceArgs& a, int seqh, float* sb, float* cv, int gt, int bar) {
+  constexpr int N4 = KD * LD / 4;
   if (a.center) {
     if (gt < KD) {
       float Z = 0.f, sf = 0.f;
@@ -197,6 +201,12 @@ __device__ void combine(const ReduceArgs& a, int first, int count, int seqh, flo
   if (a.state_bf)  // the row's last BLD - LD (= 8) columns
     for (int e = gt; e < KD; e += NT)
       *reinterpret_cast<uint4*>(a.state_bf + ((size_t)seqh * KD + e) * BLD + LD) = make_uint4(0u, 0u, 0u, 0u);
+}
+template <int NT>
+__device__ void combine(const ReduceArgs& a, int first, int count, int seqh, float* sb, float* cv, int gt, int bar) {
+  combine_sum<NT>(a, first, count, seqh, sb, gt);
+  named_bar(bar, NT);
+  combine_finish<NT>(a, seqh, sb, cv, gt, bar);
 }
 static_assert(LD % 4 == 0 && (BLD - LD) == 8 && BLD % 8 == 0, "vector stores of the state rows");
 
@@ -390,44 +400,83 @@ __global__ void __launch_bounds__(NTH, 1)
       }
       if (last) {
         // segment k ends here: [S | z]^T (TMEM lane f = column f of the state,
-        // lane 64 = z; column e = row e) leaves as this CTA's partial of the pair
+        // lane 64 = z; column e = row e) is this CTA's partial of the pair
         mbar_wait(SEGF(k & 1), (k >> 1) & 1, fail);
         tc_fence_after();
-        float* P = a.partial + (size_t)(x.h * nseq + x.b + blockIdx.x) * KD * LD;
+        const int p = x.h * nseq + x.b;
         const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16) + (k & 1) * KD;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t v[32];
-          tmem_ld32(tl + 32 * hh, v);
-          if (row < LD)
-#pragma unroll
-            for (int e = 0; e < 32; ++e) P[(size_t)(32 * hh + e) * LD + row] = row <= KD ? __uint_as_float(v[e]) : 0.f;
-        }
-        tc_fence_before();
-        __threadfence();
-        named_bar(1, 128);
-        if (wq == 0 && lane == 0) {
-          mbar_arrive(SEGE(k & 1));  // the accumulator is read
-          // the CTAs holding units of (b, h): c0 .. c0 + count - 1
+        if (row == 0) {  // the CTAs holding units of (b, h): c0 .. c0 + count - 1
           int first, cnt;
           seq_tiles(a.seq, a.tiles, x.b, first, cnt);
           const int U0 = x.h * upt + spt * first;
           int U1 = U0 + spt * max(cnt, 1) - 1;  // the pair's last unit with rows
           while (U1 > U0 && rtile_at(a, U1, upt, spt).seqh < 0) --U1;
           const int c0 = cta_of(U0, n_units, G), count = cta_of(U1, n_units, G) - c0 + 1;
-          const bool lastp = atomicAdd(a.counters + x.seqh, 1) == count - 1;
-          gf[0] = (lastp && !*fail) ? 1 : 0;
-          gf[1] = x.h * nseq + x.b + c0;
+          // every other CTA of the pair has left its partial already: this one
+          // completes the pair straight from TMEM
+          const int done = *reinterpret_cast<volatile int*>(a.counters + x.seqh);
+          gf[0] = (done == count - 1 && !*fail) ? 2 : 0;
+          gf[1] = p + c0;
           gf[2] = count;
         }
         named_bar(1, 128);
-        if (gf[0]) {  // this partial completes (b, h)
-          if (un >= u1) {  // the CTA's last segment: every warp combines it after the loops
-            if (row == 0) gf[3] = x.seqh;
-          } else {
-            __threadfence();
-            combine<128>(a, gf[1], gf[2], x.seqh, sb, sb + KD * LD, row, 1);
-            named_bar(1, 128);  // the staging and the flags are free again
+        if (gf[0] == 2) {
+          __threadfence();
+          // the sum over the pair's partials in slot order, this CTA's own
+          // (slot p + blockIdx.x) from TMEM, into the staging
+          const int first = gf[1], count = gf[2], q = p + blockIdx.x - first;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t v[32];
+            tmem_ld32(tl + 32 * hh, v);
+            if (row < LD) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const int E = 32 * hh + e;
+                float acc = 0.f;
+                for (int c = 0; c < count; ++c)
+                  acc += c == q ? (row <= KD ? __uint_as_float(v[e]) : 0.f)
+                                : __ldcg(a.partial + ((size_t)(first + c) * KD + E) * LD + row);
+                sb[E * LD + row] = acc;
+                if (a.pub_state && row <= KD) a.pub_state[((size_t)x.seqh * KD + E) * (KD + 1) + row] = acc;
+              }
+            }
+          }
+          tc_fence_before();
+          named_bar(1, 128);
+          if (row == 0) {
+            mbar_arrive(SEGE(k & 1));  // the accumulator is read
+            atomicAdd(a.counters + x.seqh, 1);
+          }
+          combine_finish<128>(a, x.seqh, sb, sb + KD * LD, row, 1);
+          named_bar(1, 128);  // the staging and the flags are free again
+        } else {
+          float* P = a.partial + (size_t)(p + blockIdx.x) * KD * LD;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t v[32];
+            tmem_ld32(tl + 32 * hh, v);
+            if (row < LD)
+#pragma unroll
+              for (int e = 0; e < 32; ++e) P[(size_t)(32 * hh + e) * LD + row] = row <= KD ? __uint_as_float(v[e]) : 0.f;
+          }
+          tc_fence_before();
+          __threadfence();
+          named_bar(1, 128);
+          if (row == 0) {
+            mbar_arrive(SEGE(k & 1));  // the accumulator is read
+            const bool lastp = atomicAdd(a.counters + x.seqh, 1) == gf[2] - 1;
+            gf[0] = (lastp && !*fail) ? 1 : 0;
+          }
+          named_bar(1, 128);
+          if (gf[0]) {  // this partial completes (b, h)
+            if (un >= u1) {  // the CTA's last segment: every warp combines it after the loops
+              if (row == 0) gf[3] = x.seqh;
+            } else {
+              __threadfence();
+              combine<128>(a, gf[1], gf[2], x.seqh, sb, sb + KD * LD, row, 1);
+              named_bar(1, 128);  // the staging and the flags are free again
+            }
           }
         }
       }
@@ -435,8 +484,9 @@ __global__ void __launch_bounds__(NTH, 1)
       x = y;
     }
   }
+  __syncwarp();  // single-lane roles rejoin their warps: the CTA barrier below is warp-aligned
   __syncthreads();
-  if (gf[0] && gf[3] >= 0 && !*fail) {
+  if (gf[0] == 1 && gf[3] >= 0 && !*fail) {
     __threadfence();
     combine<NTH>(a, gf[1], gf[2], gf[3], reinterpret_cast<float*>(smem + O_SB),
                  reinterpret_cast<float*>(smem + O_SB) + KD * LD, tid, 0);
