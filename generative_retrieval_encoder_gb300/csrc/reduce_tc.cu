@@ -426,19 +426,31 @@ __global__ void __launch_bounds__(NTH, 1)
           // (slot p + blockIdx.x) from TMEM, into the staging
           const int first = gf[1], count = gf[2], q = p + blockIdx.x - first;
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t v[32];
-            tmem_ld32(tl + 32 * hh, v);
-            if (row < LD) {
+          for (int qq = 0; qq < 4; ++qq) {  // 16 state rows at a time
+            uint32_t v[16];
+            tmem_ld16(tl + 16 * qq, v);
+            float acc[16];
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const int E = 32 * hh + e;
-                float acc = 0.f;
-                for (int c = 0; c < count; ++c)
-                  acc += c == q ? (row <= KD ? __uint_as_float(v[e]) : 0.f)
-                                : __ldcg(a.partial + ((size_t)(first + c) * KD + E) * LD + row);
-                sb[E * LD + row] = acc;
-                if (a.pub_state && row <= KD) a.pub_state[((size_t)x.seqh * KD + E) * (KD + 1) + row] = acc;
+            for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+            if (row < LD) {
+              for (int c = 0; c < count; ++c) {
+                if (c == q) {
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) acc[e] += row <= KD ? __uint_as_float(v[e]) : 0.f;
+                } else {
+                  const float* Pc = a.partial + ((size_t)(first + c) * KD + 16 * qq) * LD + row;
+                  float w[16];
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) w[e] = __ldcg(Pc + (size_t)e * LD);
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) acc[e] += w[e];
+                }
+              }
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const int E = 16 * qq + e;
+                sb[E * LD + row] = acc[e];
+                if (a.pub_state && row <= KD) a.pub_state[((size_t)x.seqh * KD + E) * (KD + 1) + row] = acc[e];
               }
             }
           }
