@@ -17,6 +17,7 @@ using namespace gbla;
 namespace {
 
 thread_local std::string g_last_error;
+thread_local int g_policy = GBLA_POLICY_AUTO;  // gbla_set_kernel_policy
 
 constexpr size_t kAlign = 256;
 
@@ -384,13 +385,20 @@ cudaError_t launch_bwd_q_layer_bf16(const BwdQArgs& q, int hd, int n_chunks, int
 }
 
 // The bf16 state reduction: the tcgen05 kernel where it applies (gate values,
-// d_h = 64), else the mma.sync kernel (softmax logits, other d_h).
-cudaError_t launch_reduce_layer_bf16(const ReduceArgs& a, int n_chunks, int n_tiles, cudaStream_t st,
+// d_h = 64) and each SM streams at least 20 of its 256-row tiles, else the
+// mma.sync kernel (softmax logits, other d_h; and shorter batches, where the
+// tcgen05 kernel's fixed start and final drain outweigh its faster stream:
+// measured 51 against 47 us at 13 tiles an SM, 80 against 81 at 27, 129
+// against 132 at 54).
+cudaError_t launch_reduce_layer_bf16(const ReduceArgs& a, int n_chunks, int n_tiles, int sms, cudaStream_t st,
                                      const char** nm) {
-  *nm = "reduce[tc]";
-  const cudaError_t e = launch_reduce_tc(a, n_tiles, st);
-  if (e != cudaErrorNotSupported) return e;
-  (void)cudaGetLastError();
+  const long long units = (long long)a.seq.T * a.H / 256;
+  if (units >= 20LL * sms || g_policy == GBLA_POLICY_TC) {
+    *nm = "reduce[tc]";
+    const cudaError_t e = launch_reduce_tc(a, n_tiles, st);
+    if (e != cudaErrorNotSupported) return e;
+    (void)cudaGetLastError();
+  }
   *nm = "reduce[mma]";
   return launch_reduce_bf16(a, n_chunks, st);
 }
@@ -414,7 +422,7 @@ gbla_status run_reduce(Ctx& c, const void* k, const void* v, int64_t ld, const f
   a.partial_slots = partial_slots(p);
   a.err_out = c.err;
   const char* nm = "reduce[f32]";
-  GBLA_CHECK(p.f32 ? launch_reduce_f32(a, p.n_chunks, c.st) : launch_reduce_layer_bf16(a, p.n_chunks, p.n_tiles, c.st, &nm),
+  GBLA_CHECK(p.f32 ? launch_reduce_f32(a, p.n_chunks, c.st) : launch_reduce_layer_bf16(a, p.n_chunks, p.n_tiles, p.sms, c.st, &nm),
              nm);
   return GBLA_OK;
 }
@@ -735,6 +743,12 @@ const char* gbla_status_string(int status) {
 const char* gbla_last_error(void) { return g_last_error.c_str(); }
 
 void gbla_profiling_enable(int on) { g_prof.on = on != 0; }
+
+gbla_status gbla_set_kernel_policy(int policy) {
+  if (policy != GBLA_POLICY_AUTO && policy != GBLA_POLICY_TC) return GBLA_ERR_INVALID_ARG;
+  g_policy = policy;
+  return GBLA_OK;
+}
 
 int gbla_profiling_read(const char** names, float* ms, int cap) {
   const int n = (int)g_prof.rec.size();

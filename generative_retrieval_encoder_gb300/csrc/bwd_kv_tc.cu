@@ -91,6 +91,10 @@ __device__ __forceinline__ Unit unit_at(const BwdKVArgs& a, int u, int n_units_p
 __global__ void __launch_bounds__(NTH, 1)
     k_bwd_kv_tc(const BwdKVArgs a, const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmS,
                 int voff, int n_units_per_head, int n_units) {
+  if (threadIdx.x == 0) {  // the descriptors load while the previous kernel finishes
+    tma_prefetch_map(&tmP);
+    tma_prefetch_map(&tmS);
+  }
   pdl_enter();  // the previous kernel's outputs are visible from here on
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

@@ -130,6 +130,10 @@ __device__ __forceinline__ int cta_of(int u, int n_units, int grid) {
 __global__ void __launch_bounds__(NTH, 2)
     k_bwd_q_tc(const BwdQArgs a, const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmY,
                int roff, int upt, int spt, int n_units) {
+  if (threadIdx.x == 0) {  // the descriptors load while the previous kernel finishes
+    tma_prefetch_map(&tmP);
+    tma_prefetch_map(&tmY);
+  }
   pdl_enter();  // the previous kernel's outputs are visible from here on
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

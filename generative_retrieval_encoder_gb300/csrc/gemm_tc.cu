@@ -168,6 +168,10 @@ template <bool AMN, bool BMN, int CL>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const GemmArgs a, const TileSched ts, int wide_ok) {
+  if (threadIdx.x == 0) {  // the descriptors load while the previous kernel finishes
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+  }
   pdl_enter();  // the previous kernel's outputs are visible from here on
   using RG = Ring<CL>;
   constexpr int ST = RG::ST;

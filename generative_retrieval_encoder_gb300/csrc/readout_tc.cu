@@ -94,6 +94,10 @@ __device__ __forceinline__ Unit unit_at(const ReadoutArgs& a, int u, int n_units
 __global__ void __launch_bounds__(NTH, 1)
     k_readout_tc(const ReadoutArgs a, const __grid_constant__ CUtensorMap tmP,
                  const __grid_constant__ CUtensorMap tmS, int roff, int n_units_per_head, int n_units) {
+  if (threadIdx.x == 0) {  // the descriptors load while the previous kernel finishes
+    tma_prefetch_map(&tmP);
+    tma_prefetch_map(&tmS);
+  }
   pdl_enter();  // the previous kernel's outputs are visible from here on
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

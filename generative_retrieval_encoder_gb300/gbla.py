@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libgbla.so")
 GBLA_OK, GBLA_ERR_INVALID_ARG, GBLA_ERR_UNSUPPORTED, GBLA_ERR_WORKSPACE, GBLA_ERR_CUDA, GBLA_ERR_DEVICE_CHECK = \
     0, -1, -2, -3, -4, -5
 GBLA_ERR_DEVICE_TIMEOUT = -6
+GBLA_POLICY_AUTO, GBLA_POLICY_TC = 0, 1
 GBLA_F32, GBLA_BF16 = 0, 1
 GBLA_GATE_SIGMOID, GBLA_GATE_SOFTMAX = 0, 1
 GBLA_OP_FORWARD, GBLA_OP_BACKWARD, GBLA_OP_CORE_FORWARD, GBLA_OP_CORE_BACKWARD = 0, 1, 2, 3
@@ -25,7 +26,8 @@ GBLA_OP_FORWARD, GBLA_OP_BACKWARD, GBLA_OP_CORE_FORWARD, GBLA_OP_CORE_BACKWARD =
 EXPORTS = ("gbla_workspace_size", "gbla_saved_size", "gbla_validate_shape", "gbla_forward", "gbla_backward",
            "bla_core_forward", "bla_core_backward", "gbla_check_device_status", "gbla_status_string",
            "gbla_last_error", "gbla_version", "gbla_profiling_enable", "gbla_profiling_read",
-           "bla_core_forward_noalloc", "bla_core_noalloc_check_device_status", "gbla_diag_bounded_wait")
+           "bla_core_forward_noalloc", "bla_core_noalloc_check_device_status", "gbla_diag_bounded_wait",
+           "gbla_set_kernel_policy")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -77,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.bla_core_noalloc_check_device_status.restype = ctypes.c_int
         L.gbla_diag_bounded_wait.argtypes = [vp, sz, ctypes.c_uint, vp]
         L.gbla_diag_bounded_wait.restype = ctypes.c_int
+        L.gbla_set_kernel_policy.argtypes = [ctypes.c_int]
+        L.gbla_set_kernel_policy.restype = ctypes.c_int
         L.gbla_check_device_status.argtypes = [vp, vp]
         L.gbla_check_device_status.restype = ctypes.c_int
         L.gbla_status_string.argtypes = [ctypes.c_int]
@@ -254,6 +258,11 @@ def bla_core_noalloc_check_device_status() -> int:
 def gbla_diag_bounded_wait(ws: torch.Tensor, polls: int = 4096) -> int:
     """Runs the kernels' bounded mbarrier wait out on purpose (see gbla.h)."""
     return lib().gbla_diag_bounded_wait(_ptr(ws), ws.numel(), polls, _stream())
+
+
+def gbla_set_kernel_policy(policy: int) -> None:
+    """GBLA_POLICY_AUTO (default) or GBLA_POLICY_TC for this thread's later calls (see gbla.h)."""
+    _check(lib().gbla_set_kernel_policy(policy), "gbla_set_kernel_policy")
 
 
 def gbla_profiling_enable(on: bool) -> None:

@@ -249,6 +249,17 @@ int gbla_version(void);
 void gbla_profiling_enable(int on);
 int gbla_profiling_read(const char** names, float* ms, int cap);
 
+/* Kernel selection of the CALLING THREAD's later calls (no counterpart on the
+ * pages).  GBLA_POLICY_AUTO (the default) picks, per step, the kernel that is
+ * fastest for the shape: e.g. the state reduction runs on the 5th-generation
+ * tensor cores only when every SM gets at least 20 of its 256-row tiles, and
+ * on mma.sync otherwise.  GBLA_POLICY_TC takes the tcgen05 kernel wherever it
+ * applies (d_h and gate permitting), whatever the size: for tests that check
+ * those kernels on small shapes.  Results agree within the tolerances either
+ * way.  GBLA_ERR_INVALID_ARG for another value. */
+typedef enum { GBLA_POLICY_AUTO = 0, GBLA_POLICY_TC = 1 } gbla_policy;
+gbla_status gbla_set_kernel_policy(int policy);
+
 #ifdef __cplusplus
 }
 #endif

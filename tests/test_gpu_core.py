@@ -18,6 +18,11 @@ pytestmark = pytest.mark.gpu
 def _lib():
     build.build()
     gbla.lib()
+    # the tcgen05 kernels wherever they apply, also on the small shapes here
+    # (by default the state reduction takes them only from 20 tiles an SM on)
+    gbla.gbla_set_kernel_policy(gbla.GBLA_POLICY_TC)
+    yield
+    gbla.gbla_set_kernel_policy(gbla.GBLA_POLICY_AUTO)
 
 
 # (dtype, B, L, H, dh, seq_lens, varlen lengths)

@@ -27,7 +27,7 @@ import torch
 import oracle
 from generative_retrieval_encoder_gb300 import build, gbla
 from generative_retrieval_encoder_gb300 import workloads as W
-from gbla_cases import TC_STEPS_DH64_SIGMOID, TOL, assert_tc_variants, f64, launch_names, max_err
+from gbla_cases import TC_STEPS_DH64, TC_STEPS_DH64_SIGMOID, TOL, assert_tc_variants, f64, launch_names, max_err
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -80,7 +80,9 @@ def test_training_step_whole_batch(name):
     wl = {"train2k": W.FWD_2K, "train8k": W.TRAIN_8K}[name]
     shape, x, P, dy, _ = _inputs(wl)
     out, names = _run(shape, x, P, dy, backward=True)
-    assert_tc_variants(names, TC_STEPS_DH64_SIGMOID)
+    # the state reduction runs on tcgen05 from 20 256-row tiles an SM on
+    # (131072 x 8 / 256 = 4096 tiles), on mma.sync below (train2k: 2048)
+    assert_tc_variants(names, TC_STEPS_DH64_SIGMOID if name == "train8k" else TC_STEPS_DH64)
     Pr = {n: f64(t) for n, t in P.items()}
     st, ln = oracle.seqs(wl.B, wl.L)
     xr, dyr = f64(x), f64(dy)
