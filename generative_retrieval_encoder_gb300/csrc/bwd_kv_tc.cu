@@ -1,5 +1,5 @@
 // Key-side backward of the bf16 layer (Eq. 5/6) on the 5th-generation tensor
-// cores, for d_h = 64 with phi(k) stored by the projection epilogue.  Per token
+// cores, for d_h = 64 and 128 with phi(k) stored by the projection epilogue.  Per token
 // j of a sequence and head, with [dS | dz''] the combined state gradient (dz''
 // the centring-corrected z column):
 //   dk~_j = bf16(dS) v_j + dz'',   dv_j = g_j dS^T phi(k_j),
@@ -13,15 +13,16 @@
 // Persistent: one CTA per SM walks a contiguous range of (row tile, head)
 // units, head-major, so that consecutive units mostly share a (sequence,
 // head) and its [dS | dz''].  Roles:
-//   warp 16, lane 0  producer: TMA loads of the 128-row phi(k) and v boxes of
-//                    each MMA tile into a 6-stage ring; bf16 dS (128-byte
-//                    swizzle) into one of two buffers when the (sequence,
-//                    head) changes;
-//   warp 17, lane 0  MMA issuer: D1 = V dS^T and D2 = phi(K) dS (M = 128,
-//                    N = 64, K = 64) into the TMEM columns of the tile's group;
-//   warps 0-15       epilogue, four groups of four warps taking MMA tiles in
-//                    turn, one thread per row; dk and dv replace phi(k) and v
-//                    in the consumed tiles and leave as whole 128-byte rows.
+//   producer warp    lane 0: TMA loads of the 128-row phi(k) and v boxes of
+//                    each MMA tile (one box per 64 columns) into a ring (6
+//                    stages at d_h = 64, 2 at 128); bf16 dS (128-byte swizzle)
+//                    into one of two buffers when the (sequence, head) changes;
+//   MMA warp         lane 0: D1 = V dS^T and D2 = phi(K) dS (M = 128,
+//                    N = K = d_h) into the TMEM columns of the tile's group;
+//   epilogue warps   groups of four warps (4 at d_h = 64, 2 at 128) taking MMA
+//                    tiles in turn, one thread per row; dk and dv replace phi(k)
+//                    and v in the consumed tiles and leave as whole 128-byte
+//                    lines.
 // The gate multiplies dv after the MMA, so both MMAs read the loaded tiles.
 //
 // Every mbarrier wait is bounded; after one gives up, the kernel finishes its
@@ -34,30 +35,35 @@
 namespace gbla {
 namespace {
 
-constexpr int KD = 64;                   // d_h
 constexpr int KT = 128;                  // rows per MMA tile
-constexpr int TILE = KT * 128;           // [128 rows][64 bf16], 16 KB
-constexpr int KST = 6;                   // ring stages (phi(k) | v)
-constexpr int STAGE = 2 * TILE;
-constexpr int SBUF = KD * 128;           // dS [e][f], 8 KB
-constexpr int NG = 4;                    // epilogue groups of 4 warps; MMA tile j goes to group j % NG
-constexpr int EW = 4 * NG;
-constexpr int NTH = (EW + 2) * 32;
+constexpr int TILE = KT * 128;           // one 64-column atom of a tile: [128 rows][64 bf16], 16 KB
 
-constexpr int O_ST = 0;
-constexpr int O_S = O_ST + KST * STAGE;          // two dS buffers
-constexpr int O_BAR = O_S + 2 * SBUF;
-// full[KST], empty[KST], sfull[2], sfree[2], accf[NG], acce[NG], drain
-constexpr int NBAR = 2 * KST + 4 + 2 * NG + 1;
-constexpr int O_DZ = O_BAR + 8 * NBAR;           // [group][2 buffers][dz'' 64] fp32
-constexpr int O_RED = O_DZ + 4 * NG * 2 * KD;    // [group][4 warps] ds sums
-constexpr int O_M = O_RED + 4 * NG * 4;          // [group][2 buffers] maximum logit (softmax gate)
-constexpr int O_SLOT = O_M + 4 * NG * 2;
-constexpr int O_FAIL = O_SLOT + 4;
-constexpr int SMEM = O_FAIL + 4 + 1024;
-constexpr int TMEM_COLS = NG * 2 * KD;           // per group: D1 | D2
-static_assert(SMEM <= 227 * 1024, "shared memory");
-static_assert(TMEM_COLS <= 512, "TMEM");
+// Shapes and shared-memory layout by head width D (64 or 128).
+template <int D>
+struct KCfg {
+  static constexpr int NH = D / 64;                 // 64-column atoms of a row
+  static constexpr int KST = D == 64 ? 6 : 2;       // ring stages (phi(k) atoms | v atoms)
+  static constexpr int NG = D == 64 ? 4 : 2;        // epilogue groups of 4 warps; MMA tile j goes to group j % NG
+  static constexpr int STAGE = 2 * NH * TILE;
+  static constexpr int SATOM = D * 128;             // one 64-column atom of dS [e][f]
+  static constexpr int SBUF = NH * SATOM;
+  static constexpr int EW = 4 * NG;
+  static constexpr int NTH = (EW + 2) * 32;
+  static constexpr int O_ST = 0;
+  static constexpr int O_S = O_ST + KST * STAGE;    // two dS buffers
+  static constexpr int O_BAR = O_S + 2 * SBUF;
+  // full[KST], empty[KST], sfull[2], sfree[2], accf[NG], acce[NG], drain
+  static constexpr int NBAR = 2 * KST + 4 + 2 * NG + 1;
+  static constexpr int O_DZ = O_BAR + 8 * NBAR;     // [group][2 buffers][dz'' D] fp32
+  static constexpr int O_RED = O_DZ + 4 * NG * 2 * D;  // [group][4 warps] ds sums
+  static constexpr int O_M = O_RED + 4 * NG * 4;    // [group][2 buffers] maximum logit (softmax gate)
+  static constexpr int O_SLOT = O_M + 4 * NG * 2;
+  static constexpr int O_FAIL = O_SLOT + 4;
+  static constexpr int SMEM = O_FAIL + 4 + 1024;
+  static constexpr int TMEM_COLS = NG * 2 * D;      // per group: D1 | D2
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(TMEM_COLS <= 512, "TMEM");
+};
 
 __device__ __forceinline__ uint32_t swz_off(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
@@ -88,9 +94,15 @@ __device__ __forceinline__ Unit unit_at(const BwdKVArgs& a, int u, int n_units_p
   return x;
 }
 
-__global__ void __launch_bounds__(NTH, 1)
+template <int D>
+__global__ void __launch_bounds__(KCfg<D>::NTH, 1)
     k_bwd_kv_tc(const BwdKVArgs a, const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmS,
                 int voff, int n_units_per_head, int n_units) {
+  using C = KCfg<D>;
+  constexpr int NH = C::NH, KST = C::KST, NG = C::NG, STAGE = C::STAGE, SBUF = C::SBUF, EW = C::EW,
+                NTH = C::NTH, O_ST = C::O_ST, O_S = C::O_S, O_BAR = C::O_BAR, O_DZ = C::O_DZ, O_RED = C::O_RED,
+                O_M = C::O_M, O_SLOT = C::O_SLOT, O_FAIL = C::O_FAIL, TMEM_COLS = C::TMEM_COLS;
+  (void)NTH;
   if (threadIdx.x == 0) {  // the descriptors load while the previous kernel finishes
     tma_prefetch_map(&tmP);
     tma_prefetch_map(&tmS);
@@ -159,7 +171,9 @@ __global__ void __launch_bounds__(NTH, 1)
           const int pb = k & 1;
           if (k >= 2 && !mbar_wait(SFREE(pb), ((k >> 1) - 1) & 1, fail)) break;
           mbar_expect_tx(SFULL(pb), SBUF);
-          tma_load_2d(sbase + O_S + pb * SBUF, &tmS, SFULL(pb), 0, x.seqh * KD);
+#pragma unroll
+          for (int hf = 0; hf < NH; ++hf)
+            tma_load_2d(sbase + O_S + pb * SBUF + hf * C::SATOM, &tmS, SFULL(pb), 64 * hf, x.seqh * D);
         }
         bool ok = true;
         for (int t = 0; t < x.ntl; ++t, ++j) {
@@ -168,8 +182,11 @@ __global__ void __launch_bounds__(NTH, 1)
           const uint32_t st = sbase + O_ST + s * STAGE;
           const int y = (int)x.rb + t * KT;
           mbar_expect_tx(FULL(s), STAGE);
-          tma_load_2d(st, &tmP, FULL(s), x.h * KD, y);
-          tma_load_2d(st + TILE, &tmP, FULL(s), voff + x.h * KD, y);
+#pragma unroll
+          for (int hf = 0; hf < NH; ++hf) {
+            tma_load_2d(st + hf * TILE, &tmP, FULL(s), x.h * D + 64 * hf, y);
+            tma_load_2d(st + (NH + hf) * TILE, &tmP, FULL(s), voff + x.h * D + 64 * hf, y);
+          }
           last_s[s] = j + 1;
         }
         if (!ok) break;
@@ -184,7 +201,7 @@ __global__ void __launch_bounds__(NTH, 1)
   } else if (warp == EW + 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t id_k = idesc_bf16(KT, KD, false, false), id_v = idesc_bf16(KT, KD, false, true);
+      const uint32_t id_k = idesc_bf16(KT, D, false, false), id_v = idesc_bf16(KT, D, false, true);
       int j = 0, k = -1, prev = -1;
       for (int u = u0; u < u1 && !*fail; ++u) {
         const Unit x = unit_at(a, u, n_units_per_head);
@@ -202,16 +219,20 @@ __global__ void __launch_bounds__(NTH, 1)
           if (!mbar_wait(FULL(s), (j / KST) & 1, fail)) { ok = false; break; }
           if (j >= NG && !mbar_wait(ACCE(g), ((j / NG) - 1) & 1, fail)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sk = sbase + O_ST + s * STAGE, sv = sk + TILE;
-          const uint32_t d = tmem + g * 2 * KD;
-          // D1[j][e] = sum_f v[j][f] dS[e][f]: A = V K-major, B = dS K-major (rows e).
+          const uint32_t sk = sbase + O_ST + s * STAGE, sv = sk + NH * TILE;
+          const uint32_t d = tmem + g * 2 * D;
+          // D1[j][e] = sum_f v[j][f] dS[e][f]: A = V K-major (atom kk / 4), B = dS
+          // K-major (rows e; its K = f runs through the atoms SATOM apart).
 #pragma unroll
-          for (int kk = 0; kk < KD / 16; ++kk)
-            tc_mma(d, sdesc(sv + 32 * kk, 16, 1024), sdesc(sS + 32 * kk, 16, 1024), id_k, kk > 0);
-          // D2[j][f] = sum_e phi(k)[j][e] dS[e][f]: A = phi(K) K-major, B = dS N-major (16 e-rows = 2048 B).
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc_mma(d, sdesc(sv + (kk >> 2) * TILE + 32 * (kk & 3), 16, 1024),
+                   sdesc(sS + (kk >> 2) * C::SATOM + 32 * (kk & 3), 16, 1024), id_k, kk > 0);
+          // D2[j][f] = sum_e phi(k)[j][e] dS[e][f]: A = phi(K) K-major (atom kk / 4),
+          // B = dS N-major (16 e-rows = 2048 B; its 64-column atoms SATOM apart).
 #pragma unroll
-          for (int kk = 0; kk < KD / 16; ++kk)
-            tc_mma(d + KD, sdesc(sk + 32 * kk, 16, 1024), sdesc(sS + 2048 * kk, 8192, 1024), id_v, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc_mma(d + D, sdesc(sk + (kk >> 2) * TILE + 32 * (kk & 3), 16, 1024),
+                   sdesc(sS + 2048 * kk, C::SATOM, 1024), id_v, kk > 0);
           tc_commit(ACCF(g));
           tc_commit(EMPTY(s));
         }
@@ -226,8 +247,8 @@ __global__ void __launch_bounds__(NTH, 1)
     // ----------------------------------------------------------- epilogue
     const int grp = warp >> 2, wq = warp & 3;
     const int i = wq * 32 + lane;
-    const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16) + grp * 2 * KD;
-    float* dzg = dzs + grp * 2 * KD;
+    const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16) + grp * 2 * D;
+    float* dzg = dzs + grp * 2 * D;
     float* mg = mgs + grp * 2;
     int j = 0, k = -1, prev = -1;
     for (int u = u0; u < u1; ++u) {
@@ -243,11 +264,11 @@ __global__ void __launch_bounds__(NTH, 1)
         ++k;
         prev = x.seqh;
         // the buffer replaced here served the state before the previous one
-        if (i < KD) dzg[(k & 1) * KD + i] = a.dstate[((size_t)x.seqh * KD + i) * state_ld(KD) + KD];
-        else if (i == KD) mg[k & 1] = logits ? a.state_m[x.seqh] : 0.f;
+        for (int e = i; e < D; e += 128) dzg[(k & 1) * D + e] = a.dstate[((size_t)x.seqh * D + e) * state_ld(D) + D];
+        if (i == 0) mg[k & 1] = logits ? a.state_m[x.seqh] : 0.f;
         named_bar(1 + grp, 128);
       }
-      const float* dz = dzg + (k & 1) * KD;
+      const float* dz = dzg + (k & 1) * D;
       const float mseq = mg[k & 1];
       if (grp == 0 && wq == 0 && lane == 0 && a.bg_part)  // slots of MMA tiles the unit lacks
         for (int t = x.ntl; t < tiles_per_unit; ++t) a.bg_part[((size_t)x.ti * tiles_per_unit + t) * a.H + x.h] = 0.f;
@@ -255,7 +276,7 @@ __global__ void __launch_bounds__(NTH, 1)
         if (j % NG != grp) continue;  // another group's tile
         const int s = j % KST;
         uint8_t* sk = smem + O_ST + s * STAGE;
-        uint8_t* sv = sk + TILE;
+        uint8_t* sv = sk + NH * TILE;
         const int rel = t * KT + i;
         const bool valid = rel < x.nval, store = rel < x.nrows;
         const size_t row = x.rb + rel;
@@ -263,20 +284,22 @@ __global__ void __launch_bounds__(NTH, 1)
         const float g = logits ? (valid ? __expf(gin - mseq) : 0.f) : gin;
         mbar_wait(ACCF(grp), (j / NG) & 1, fail);
         tc_fence_after();
-        // dk~ = D1 + dz'', dg = phi(k) . dk~, dk = g dk~ min(1, phi(k)) -> the phi(k) row
+        // dk~ = D1 + dz'', dg = phi(k) . dk~, dk = g dk~ min(1, phi(k)) -> the phi(k) row;
+        // 32 accumulator columns at a time, the next 32 loading under the current ones
         float dg = 0.f;
         uint32_t ob[2][32];
         tmem_ld32_async(tl, ob[0]);
-        tmem_wait32(ob[0]);
-        tmem_ld32_async(tl + 32, ob[1]);  // D1 columns 32..63 under the first half
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const uint32_t* o = ob[hh];
-          if (hh == 1) tmem_wait32(ob[1]);
+        for (int hh = 0; hh < D / 32; ++hh) {
+          tmem_wait32(ob[hh & 1]);
+          if (hh + 1 < D / 32) tmem_ld32_async(tl + 32 * (hh + 1), ob[(hh + 1) & 1]);
+          const uint32_t* o = ob[hh & 1];
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
+            const int cc = 4 * hh + c;  // 8-column chunk of the row
+            uint8_t* kp = sk + (cc >> 3) * TILE + swz_off(i, cc & 7);
             float kv[8];
-            unpack8(*reinterpret_cast<const uint4*>(sk + swz_off(i, 4 * hh + c)), kv);
+            unpack8(*reinterpret_cast<const uint4*>(kp), kv);
             uint32_t w[4];
 #pragma unroll
             for (int jj = 0; jj < 8; jj += 2) {
@@ -286,48 +309,50 @@ __global__ void __launch_bounds__(NTH, 1)
               dg = fmaf(kv[jj + 1], d1, dg);
               w[jj / 2] = pack_bf16(g * d0 * fminf(1.f, kv[jj]), g * d1 * fminf(1.f, kv[jj + 1]));
             }
-            *reinterpret_cast<uint4*>(sk + swz_off(i, 4 * hh + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(kp) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
         // dv = g D2 -> the v row
-        tmem_ld32_async(tl + KD, ob[0]);
-        tmem_wait32(ob[0]);
-        tmem_ld32_async(tl + KD + 32, ob[1]);  // D2 columns 32..63 under the first half
+        tmem_ld32_async(tl + D, ob[0]);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const uint32_t* o = ob[hh];
-          if (hh == 1) {  // the accumulators are read: hand them back
-            tmem_wait32(ob[1]);
+        for (int hh = 0; hh < D / 32; ++hh) {
+          tmem_wait32(ob[hh & 1]);
+          if (hh + 1 < D / 32) tmem_ld32_async(tl + D + 32 * (hh + 1), ob[(hh + 1) & 1]);
+          const uint32_t* o = ob[hh & 1];
+          if (hh == D / 32 - 1) {  // the accumulators are read: hand them back
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(ACCE(grp));
           }
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
+            const int cc = 4 * hh + c;
             uint32_t w[4];
 #pragma unroll
             for (int jj = 0; jj < 8; jj += 2)
               w[jj / 2] = pack_bf16(g * __uint_as_float(o[8 * c + jj]), g * __uint_as_float(o[8 * c + jj + 1]));
-            *reinterpret_cast<uint4*>(sv + swz_off(i, 4 * hh + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(sv + (cc >> 3) * TILE + swz_off(i, cc & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
         // the gate-logit gradient
         const float ds = valid ? (logits ? dg * g : dg * g * (1.f - g)) : 0.f;
         if (store) reinterpret_cast<bf16*>(a.ds)[row * a.ldds + x.h] = __float2bfloat16_rn(ds);
-        // the warp's 32 rows of dk and dv leave as whole 128-byte rows
+        // the warp's 32 rows of dk and dv leave as whole 128-byte lines
         __syncwarp();
         {
           const int ch = lane & 7;
 #pragma unroll
-          for (int it = 0; it < 8; ++it) {
-            const int rr = wq * 32 + 4 * it + (lane >> 3), rl = t * KT + rr;
-            const uint4 vk = *reinterpret_cast<const uint4*>(sk + swz_off(rr, ch));
-            const uint4 vvv = *reinterpret_cast<const uint4*>(sv + swz_off(rr, ch));
-            if (rl < x.nrows) {
-              *reinterpret_cast<uint4*>((bf16*)a.dk + (x.rb + rl) * a.lddk + (size_t)x.h * KD + 8 * ch) = vk;
-              *reinterpret_cast<uint4*>((bf16*)a.dv + (x.rb + rl) * a.lddv + (size_t)x.h * KD + 8 * ch) = vvv;
+          for (int hf = 0; hf < NH; ++hf)
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+              const int rr = wq * 32 + 4 * it + (lane >> 3), rl = t * KT + rr;
+              const uint4 vk = *reinterpret_cast<const uint4*>(sk + hf * TILE + swz_off(rr, ch));
+              const uint4 vvv = *reinterpret_cast<const uint4*>(sv + hf * TILE + swz_off(rr, ch));
+              if (rl < x.nrows) {
+                *reinterpret_cast<uint4*>((bf16*)a.dk + (x.rb + rl) * a.lddk + (size_t)x.h * D + 64 * hf + 8 * ch) = vk;
+                *reinterpret_cast<uint4*>((bf16*)a.dv + (x.rb + rl) * a.lddv + (size_t)x.h * D + 64 * hf + 8 * ch) = vvv;
+              }
             }
-          }
         }
         // db_g partial of this MMA tile: the group's 128 rows, in a fixed order
         if (a.bg_part) {
@@ -354,6 +379,22 @@ __global__ void __launch_bounds__(NTH, 1)
   if (bad && tid == 0 && a.err_out) atomicOr(a.err_out, kErrTimeout);
 }
 
+template <int D>
+cudaError_t launch_bwd_kv_tc_d(const BwdKVArgs& a, int n_tiles, long long voff, int* nparts, cudaStream_t st) {
+  using C = KCfg<D>;
+  CUtensorMap tmP, tmS;
+  if (!make_map(&tmP, a.k, (uint64_t)(voff + a.H * D), (uint64_t)a.seq.T, (uint64_t)a.ldk, 64, KT, false) ||
+      !make_map(&tmS, a.dstate_bf, (uint64_t)state_bf_ld(D), (uint64_t)a.seq.n_seq * a.H * D,
+                (uint64_t)state_bf_ld(D), 64, D, false))
+    return cudaErrorNotSupported;
+  cudaError_t e = cudaFuncSetAttribute(k_bwd_kv_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const int n_units = n_tiles * a.H;
+  const int grid = n_units < sm_count() ? n_units : sm_count();
+  *nparts = n_tiles * (a.tiles.tile / KT);
+  return launch_pdl(k_bwd_kv_tc<D>, dim3(grid), dim3(C::NTH), C::SMEM, st, a, tmP, tmS, (int)voff, n_tiles, n_units);
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_kv_tc(const BwdKVArgs& a, int n_tiles, int* nparts, cudaStream_t st) {
@@ -361,22 +402,12 @@ cudaError_t launch_bwd_kv_tc(const BwdKVArgs& a, int n_tiles, int* nparts, cudaS
   const long long voff = ((const bf16*)a.v - (const bf16*)a.k);
   const bool sig = a.gate_kind == GATE_VALUES && a.gate_grad == GG_SIGMOID;
   const bool soft = a.gate_kind == GATE_LOGITS && a.gate_grad == GG_SOFTMAX && a.state_m;
-  if (a.dh != KD || !a.pre || !(sig || soft) || a.ldv != a.ldk ||
-      voff < 0 || voff % 8 || !al16(a.k) || !al16(a.dk) || !al16(a.dv) || !al16(a.dstate_bf) || a.ldk % 8 ||
-      a.lddk % 8 || a.lddv % 8 || a.seq.T <= 0 || n_tiles <= 0 || a.tiles.tile % KT ||
-      a.zero_cols_to > a.zero_cols_from)
+  if ((a.dh != 64 && a.dh != 128) || !a.pre || !(sig || soft) || a.ldv != a.ldk || voff < 0 || voff % 8 ||
+      !al16(a.k) || !al16(a.dk) || !al16(a.dv) || !al16(a.dstate_bf) || a.ldk % 8 || a.lddk % 8 || a.lddv % 8 ||
+      a.seq.T <= 0 || n_tiles <= 0 || a.tiles.tile % KT || a.zero_cols_to > a.zero_cols_from)
     return cudaErrorNotSupported;
-  CUtensorMap tmP, tmS;
-  if (!make_map(&tmP, a.k, (uint64_t)(voff + a.H * KD), (uint64_t)a.seq.T, (uint64_t)a.ldk, 64, KT, false) ||
-      !make_map(&tmS, a.dstate_bf, (uint64_t)state_bf_ld(KD), (uint64_t)a.seq.n_seq * a.H * KD,
-                (uint64_t)state_bf_ld(KD), 64, KD, false))
-    return cudaErrorNotSupported;
-  cudaError_t e = cudaFuncSetAttribute(k_bwd_kv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-  if (e != cudaSuccess) return e;
-  const int n_units = n_tiles * a.H;
-  const int grid = n_units < sm_count() ? n_units : sm_count();
-  *nparts = n_tiles * (a.tiles.tile / KT);
-  return launch_pdl(k_bwd_kv_tc, dim3(grid), dim3(NTH), SMEM, st, a, tmP, tmS, (int)voff, n_tiles, n_units);
+  return a.dh == 64 ? launch_bwd_kv_tc_d<64>(a, n_tiles, voff, nparts, st)
+                    : launch_bwd_kv_tc_d<128>(a, n_tiles, voff, nparts, st);
 }
 
 }  // namespace gbla

@@ -1,22 +1,24 @@
 // Readout of the bf16 layer (Eq. 5/6 fused with the RmsNorm gate of Eq. 7) on
-// the 5th-generation tensor cores, for d_h = 64 with phi(q) stored by the
-// projection epilogue:
+// the 5th-generation tensor cores, for d_h = 64 and 128 with phi(q) stored by
+// the projection epilogue:
 //   o_i = S'^T phi(q_i) / (z . phi(q_i)) + c,   y_i = RmsNorm(o_i) gamma SiLU(r_i)
 // (S' the centred state, c its centre; rs and 1/den saved for the backward).
 //
 // Persistent: one CTA per SM walks a contiguous range of (row tile, head)
 // units, head-major, so that consecutive units mostly share a (sequence,
 // head) and its state.  Roles:
-//   warp 16, lane 0  producer: TMA loads of the 128-row phi(q) and r boxes of
-//                    each MMA tile into a 6-stage ring; the state S' (bf16,
-//                    128-byte swizzle) into one of two buffers when the
+//   producer warp    lane 0: TMA loads of the 128-row phi(q) and r boxes of
+//                    each MMA tile (one box per 64 columns, 128-byte swizzle)
+//                    into a ring (6 stages at d_h = 64, 2 at d_h = 128); the
+//                    state S' (bf16) into one of two buffers when the
 //                    (sequence, head) changes;
-//   warp 17, lane 0  MMA issuer: O' = phi(Q) S' (M = 128, N = 64, K = 64) into
-//                    the TMEM accumulator of the tile's epilogue group;
-//   warps 0-15       epilogue, four groups of four warps taking MMA tiles in
-//                    turn; one thread per row: den = z . phi(q) on the CUDA
-//                    cores, o and the row's sum of squares, then y from a
-//                    second read of the accumulator; 16-byte stores.
+//   MMA warp         lane 0: O' = phi(Q) S' (M = 128, N = K = d_h) into the
+//                    TMEM accumulator of the tile's epilogue group;
+//   epilogue warps   groups of four warps (4 groups at d_h = 64, 2 at 128)
+//                    taking MMA tiles in turn; one thread per row: den =
+//                    z . phi(q) on the CUDA cores, o and the row's sum of
+//                    squares, then y from a second read of the accumulator;
+//                    16-byte stores.
 // A ring stage is free once the MMA has read phi(q) and the epilogue group has
 // read phi(q) and r (its empty barrier counts the MMA commit and four warps).
 //
@@ -30,27 +32,33 @@
 namespace gbla {
 namespace {
 
-constexpr int RD = 64;                   // d_h
 constexpr int RT = 128;                  // rows per MMA tile
-constexpr int TILE = RT * 128;           // [128 rows][64 bf16], 16 KB
-constexpr int RST = 6;                   // ring stages (phi(q) | r)
-constexpr int STAGE = 2 * TILE;
-constexpr int SBUF = RD * 128;           // S' [e][f], 8 KB
-constexpr int NG = 4;                    // epilogue groups of 4 warps; MMA tile j goes to group j % NG
-constexpr int EW = 4 * NG;               // epilogue warps
-constexpr int NTH = (EW + 2) * 32;
+constexpr int TILE = RT * 128;           // one 64-column atom of a tile: [128 rows][64 bf16], 16 KB
 
-constexpr int O_ST = 0;
-constexpr int O_S = O_ST + RST * STAGE;          // two S' buffers
-constexpr int O_BAR = O_S + 2 * SBUF;
-// full[RST], empty[RST], sfull[2], sfree[2], accf[NG], acce[NG], drain
-constexpr int NBAR = 2 * RST + 4 + 2 * NG + 1;
-constexpr int O_CZ = O_BAR + 8 * NBAR;           // [group][2 buffers][c | z] fp32, gamma
-constexpr int O_SLOT = O_CZ + 4 * (NG * 2 * 2 * RD + RD);
-constexpr int O_FAIL = O_SLOT + 4;
-constexpr int SMEM = O_FAIL + 4 + 1024;
-constexpr int TMEM_COLS = NG * RD;               // one 64-column accumulator per group
-static_assert(SMEM <= 227 * 1024, "shared memory");
+// Shapes and shared-memory layout by head width D (64 or 128).
+template <int D>
+struct RCfg {
+  static constexpr int NH = D / 64;                 // 64-column atoms of a row
+  static constexpr int RST = D == 64 ? 6 : 2;       // ring stages (phi(q) atoms | r atoms)
+  static constexpr int NG = D == 64 ? 4 : 2;        // epilogue groups of 4 warps; MMA tile j goes to group j % NG
+  static constexpr int STAGE = 2 * NH * TILE;
+  static constexpr int SATOM = D * 128;             // one 64-column atom of S' [e][f]
+  static constexpr int SBUF = NH * SATOM;
+  static constexpr int EW = 4 * NG;                 // epilogue warps
+  static constexpr int NTH = (EW + 2) * 32;
+  static constexpr int O_ST = 0;
+  static constexpr int O_S = O_ST + RST * STAGE;    // two S' buffers
+  static constexpr int O_BAR = O_S + 2 * SBUF;
+  // full[RST], empty[RST], sfull[2], sfree[2], accf[NG], acce[NG], drain
+  static constexpr int NBAR = 2 * RST + 4 + 2 * NG + 1;
+  static constexpr int O_CZ = O_BAR + 8 * NBAR;     // [group][2 buffers][c | z] fp32, gamma
+  static constexpr int O_SLOT = O_CZ + 4 * (NG * 2 * 2 * D + D);
+  static constexpr int O_FAIL = O_SLOT + 4;
+  static constexpr int SMEM = O_FAIL + 4 + 1024;
+  static constexpr int TMEM_COLS = NG * D;          // one D-column accumulator per group
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation");
+};
 
 __device__ __forceinline__ uint32_t swz_off(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
@@ -91,9 +99,14 @@ __device__ __forceinline__ Unit unit_at(const ReadoutArgs& a, int u, int n_units
   return x;
 }
 
-__global__ void __launch_bounds__(NTH, 1)
+template <int D>
+__global__ void __launch_bounds__(RCfg<D>::NTH, 1)
     k_readout_tc(const ReadoutArgs a, const __grid_constant__ CUtensorMap tmP,
                  const __grid_constant__ CUtensorMap tmS, int roff, int n_units_per_head, int n_units) {
+  using C = RCfg<D>;
+  constexpr int NH = C::NH, RST = C::RST, NG = C::NG, STAGE = C::STAGE, SBUF = C::SBUF, EW = C::EW,
+                NTH = C::NTH, O_ST = C::O_ST, O_S = C::O_S, O_BAR = C::O_BAR, O_CZ = C::O_CZ,
+                O_SLOT = C::O_SLOT, O_FAIL = C::O_FAIL, TMEM_COLS = C::TMEM_COLS;
   if (threadIdx.x == 0) {  // the descriptors load while the previous kernel finishes
     tma_prefetch_map(&tmP);
     tma_prefetch_map(&tmS);
@@ -116,8 +129,8 @@ __global__ void __launch_bounds__(NTH, 1)
   auto ACCF = [&](int g) { return bar0 + 8 * (2 * RST + 4 + g); };
   auto ACCE = [&](int g) { return bar0 + 8 * (2 * RST + 4 + NG + g); };
   const uint32_t DRAIN = bar0 + 8 * (2 * RST + 4 + 2 * NG);
-  float* cz = reinterpret_cast<float*>(smem + O_CZ);  // [group][2][c 64 | z 64]
-  float* gam = cz + NG * 2 * 2 * RD;
+  float* cz = reinterpret_cast<float*>(smem + O_CZ);  // [group][2][c D | z D]
+  float* gam = cz + NG * 2 * 2 * D;
   uint32_t* slot = reinterpret_cast<uint32_t*>(smem + O_SLOT);
   volatile int* fail = reinterpret_cast<volatile int*>(smem + O_FAIL);
 
@@ -138,7 +151,7 @@ __global__ void __launch_bounds__(NTH, 1)
     mbar_init_fence();
     *fail = 0;
   }
-  for (int f = tid; f < RD; f += NTH) gam[f] = a.rms_w ? __bfloat162float(((const bf16*)a.rms_w)[f]) : 1.f;
+  for (int f = tid; f < D; f += NTH) gam[f] = a.rms_w ? __bfloat162float(((const bf16*)a.rms_w)[f]) : 1.f;
   if (warp == EW + 1) tmem_alloc(smem_u32(slot), TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -161,7 +174,9 @@ __global__ void __launch_bounds__(NTH, 1)
           const int pb = k & 1;
           if (k >= 2 && !mbar_wait(SFREE(pb), ((k >> 1) - 1) & 1, fail)) break;
           mbar_expect_tx(SFULL(pb), SBUF);
-          tma_load_2d(sbase + O_S + pb * SBUF, &tmS, SFULL(pb), 0, x.seqh * RD);
+#pragma unroll
+          for (int hf = 0; hf < NH; ++hf)
+            tma_load_2d(sbase + O_S + pb * SBUF + hf * C::SATOM, &tmS, SFULL(pb), 64 * hf, x.seqh * D);
         }
         bool ok = true;
         for (int t = 0; t < x.ntl; ++t, ++j) {
@@ -170,8 +185,11 @@ __global__ void __launch_bounds__(NTH, 1)
           const uint32_t st = sbase + O_ST + s * STAGE;
           const int y = (int)x.rb + t * RT;
           mbar_expect_tx(FULL(s), STAGE);
-          tma_load_2d(st, &tmP, FULL(s), x.h * RD, y);
-          tma_load_2d(st + TILE, &tmP, FULL(s), roff + x.h * RD, y);
+#pragma unroll
+          for (int hf = 0; hf < NH; ++hf) {
+            tma_load_2d(st + hf * TILE, &tmP, FULL(s), x.h * D + 64 * hf, y);
+            tma_load_2d(st + (NH + hf) * TILE, &tmP, FULL(s), roff + x.h * D + 64 * hf, y);
+          }
           last_s[s] = j + 1;
         }
         if (!ok) break;
@@ -186,7 +204,7 @@ __global__ void __launch_bounds__(NTH, 1)
   } else if (warp == EW + 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(RT, RD, false, true);
+      const uint32_t idesc = idesc_bf16(RT, D, false, true);
       int j = 0, k = -1, prev = -1;
       for (int u = u0; u < u1 && !*fail; ++u) {
         const Unit x = unit_at(a, u, n_units_per_head);
@@ -205,10 +223,12 @@ __global__ void __launch_bounds__(NTH, 1)
           if (j >= NG && !mbar_wait(ACCE(ab), ((j / NG) - 1) & 1, fail)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sq = sbase + O_ST + s * STAGE;
-          // K = e.  A = phi(Q) K-major (+32 B per 16 e); B = S' N-major (16 e-rows = 2048 B).
+          // K = e.  A = phi(Q) K-major (atom kk / 4, +32 B per 16 e inside it);
+          // B = S' N-major (16 e-rows = 2048 B; its 64-column atoms SATOM apart).
 #pragma unroll
-          for (int kk = 0; kk < RD / 16; ++kk)
-            tc_mma(tmem + ab * RD, sdesc(sq + 32 * kk, 16, 1024), sdesc(sS + 2048 * kk, 8192, 1024), idesc, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc_mma(tmem + ab * D, sdesc(sq + (kk >> 2) * TILE + 32 * (kk & 3), 16, 1024),
+                   sdesc(sS + 2048 * kk, C::SATOM, 1024), idesc, kk > 0);
           tc_commit(ACCF(ab));
           tc_commit(EMPTY(s));
         }
@@ -223,9 +243,9 @@ __global__ void __launch_bounds__(NTH, 1)
     // ----------------------------------------------------------- epilogue
     const int grp = warp >> 2, wq = warp & 3;  // group, TMEM lane quarter
     const int i = wq * 32 + lane;              // tile row = TMEM lane
-    const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16) + grp * RD;
+    const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16) + grp * D;
     bf16* out = (bf16*)a.out;
-    float* czg = cz + grp * 2 * 2 * RD;
+    float* czg = cz + grp * 2 * 2 * D;
     int j = 0, k = -1, prev = -1;
     for (int u = u0; u < u1; ++u) {
       const Unit x = unit_at(a, u, n_units_per_head);
@@ -236,66 +256,68 @@ __global__ void __launch_bounds__(NTH, 1)
         // the buffer replaced here served the state before the previous one:
         // every thread of the group passed the barrier below for the previous
         // state, so none still reads it
-        float* czb = czg + (k & 1) * 2 * RD;
-        const int e = i & (RD - 1);
-        if (i < RD) czb[e] = a.center ? a.center[(size_t)x.seqh * RD + e] : 0.f;
-        else czb[RD + e] = __bfloat162float(a.state_bf[((size_t)x.seqh * RD + e) * state_bf_ld(RD) + RD]);
+        float* czb = czg + (k & 1) * 2 * D;
+        for (int idx = i; idx < 2 * D; idx += 128) {
+          const int e = idx & (D - 1);
+          if (idx < D) czb[e] = a.center ? a.center[(size_t)x.seqh * D + e] : 0.f;
+          else czb[D + e] = __bfloat162float(a.state_bf[((size_t)x.seqh * D + e) * state_bf_ld(D) + D]);
+        }
         named_bar(1 + grp, 128);
       }
-      const float* cb = czg + (k & 1) * 2 * RD;
-      const float* zb = cb + RD;
+      const float* cb = czg + (k & 1) * 2 * D;
+      const float* zb = cb + D;
       for (int t = 0; t < x.ntl; ++t, ++j) {
         if (j % NG != grp) continue;  // another group's tile
         const int s = j % RST;
         const uint8_t* sq = smem + O_ST + s * STAGE;
-        uint8_t* sr = smem + O_ST + s * STAGE + TILE;
+        uint8_t* sr = smem + O_ST + s * STAGE + NH * TILE;
         const int rel = t * RT + i;
         const bool valid = rel < x.nval, store = rel < x.nrows;
         mbar_wait(ACCF(grp), (j / NG) & 1, fail);
         tc_fence_after();
         // O' columns 0..31 load under den = z . phi(q) (the row's phi(q) in shared memory)
-        uint32_t o0[32], o1[32];
-        tmem_ld32_async(tl, o0);
+        uint32_t ob[2][32];
+        tmem_ld32_async(tl, ob[0]);
         float den = 0.f;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 8 * NH; ++c) {
           float qv[8];
-          unpack8(*reinterpret_cast<const uint4*>(sq + swz_off(i, c)), qv);
+          unpack8(*reinterpret_cast<const uint4*>(sq + (c >> 3) * TILE + swz_off(i, c & 7)), qv);
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) den = fmaf(qv[jj], zb[8 * c + jj], den);
         }
         const float inv = valid ? 1.f / den : 0.f;
         const float cv = valid ? 1.f : 0.f;
-        tmem_wait32(o0);
-        tmem_ld32_async(tl + 32, o1);  // columns 32..63 under the first half's sums
-        // o = O'/den + c and its sum of squares
+        // o = O'/den + c and its sum of squares, 32 columns at a time, the next
+        // 32 loading under the current ones
         float ss = 0.f;
 #pragma unroll
-        for (int f = 0; f < 32; ++f) {
-          const float v = fmaf(__uint_as_float(o0[f]), inv, cv * cb[f]);
-          ss = fmaf(v, v, ss);
-        }
-        tmem_wait32(o1);
+        for (int q = 0; q < D / 32; ++q) {
+          tmem_wait32(ob[q & 1]);
+          if (q + 1 < D / 32) tmem_ld32_async(tl + 32 * (q + 1), ob[(q + 1) & 1]);
 #pragma unroll
-        for (int f = 0; f < 32; ++f) {
-          const float v = fmaf(__uint_as_float(o1[f]), inv, cv * cb[32 + f]);
-          ss = fmaf(v, v, ss);
+          for (int f = 0; f < 32; ++f) {
+            const float v = fmaf(__uint_as_float(ob[q & 1][f]), inv, cv * cb[32 * q + f]);
+            ss = fmaf(v, v, ss);
+          }
         }
-        const float rs = rsqrtf(ss * (1.f / RD) + a.eps);
+        const float rs = rsqrtf(ss * (1.f / D) + a.eps);
         // y = RMSNorm(o) * gamma * SiLU(r); O' is read again, 32 columns at a time
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        for (int hh = 0; hh < D / 32; ++hh) {
           uint32_t o[32];
           tmem_ld32(tl + 32 * hh, o);
-          if (hh == 1) {  // the accumulator is read: hand it back
+          if (hh == D / 32 - 1) {  // the accumulator is read: hand it back
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(ACCE(grp));
           }
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
+            const int cc = 4 * hh + c;  // 8-column chunk of the row
+            uint8_t* rp = sr + (cc >> 3) * TILE + swz_off(i, cc & 7);
             float rv[8];
-            unpack8(*reinterpret_cast<const uint4*>(sr + swz_off(i, 4 * hh + c)), rv);
+            unpack8(*reinterpret_cast<const uint4*>(rp), rv);
             uint32_t w[4];
 #pragma unroll
             for (int jj = 0; jj < 8; jj += 2) {
@@ -308,19 +330,22 @@ __global__ void __launch_bounds__(NTH, 1)
               w[jj / 2] = pack_bf16(y0, y1);
             }
             // y over the r chunk just read (this lane's own row)
-            *reinterpret_cast<uint4*>(sr + swz_off(i, 4 * hh + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(rp) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
-        // the warp's 32 rows of y leave as whole 128-byte rows: eight lanes per row
+        // the warp's 32 rows of y leave as whole 128-byte lines: eight lanes per line
         __syncwarp();
         {
           const int ch = lane & 7;
 #pragma unroll
-          for (int it = 0; it < 8; ++it) {
-            const int rr = wq * 32 + 4 * it + (lane >> 3), rl = t * RT + rr;
-            const uint4 v = *reinterpret_cast<const uint4*>(sr + swz_off(rr, ch));
-            if (rl < x.nrows) *reinterpret_cast<uint4*>(out + (x.rb + rl) * a.ldo + (size_t)x.h * RD + 8 * ch) = v;
-          }
+          for (int hf = 0; hf < NH; ++hf)
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+              const int rr = wq * 32 + 4 * it + (lane >> 3), rl = t * RT + rr;
+              const uint4 v = *reinterpret_cast<const uint4*>(sr + hf * TILE + swz_off(rr, ch));
+              if (rl < x.nrows)
+                *reinterpret_cast<uint4*>(out + (x.rb + rl) * a.ldo + (size_t)x.h * D + 64 * hf + 8 * ch) = v;
+            }
         }
         if (a.rsinv && store)
           *reinterpret_cast<float2*>(a.rsinv + 2 * ((x.rb + rel) * a.H + x.h)) = make_float2(valid ? rs : 0.f, inv);
@@ -338,24 +363,30 @@ __global__ void __launch_bounds__(NTH, 1)
   if (bad && tid == 0 && a.err_out) atomicOr(a.err_out, kErrTimeout);
 }
 
+template <int D>
+cudaError_t launch_readout_tc_d(const ReadoutArgs& a, int n_tiles, long long roff, cudaStream_t st) {
+  using C = RCfg<D>;
+  CUtensorMap tmP, tmS;
+  if (!make_map(&tmP, a.q, (uint64_t)a.ldq, (uint64_t)a.seq.T, (uint64_t)a.ldq, 64, RT, false) ||
+      !make_map(&tmS, a.state_bf, (uint64_t)state_bf_ld(D), (uint64_t)a.seq.n_seq * a.H * D,
+                (uint64_t)state_bf_ld(D), 64, D, false))
+    return cudaErrorNotSupported;
+  cudaError_t e = cudaFuncSetAttribute(k_readout_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const int n_units = n_tiles * a.H;
+  const int grid = n_units < sm_count() ? n_units : sm_count();
+  return launch_pdl(k_readout_tc<D>, dim3(grid), dim3(C::NTH), C::SMEM, st, a, tmP, tmS, (int)roff, n_tiles, n_units);
+}
+
 }  // namespace
 
 cudaError_t launch_readout_tc(const ReadoutArgs& a, int n_tiles, cudaStream_t st) {
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   const long long roff = ((const bf16*)a.r - (const bf16*)a.q);
-  if (a.dh != RD || !a.pre || a.ldr != a.ldq || roff < 0 || roff % 8 || !al16(a.q) || !al16(a.out) ||
-      !al16(a.state_bf) || a.ldq % 8 || a.ldo % 8 || a.seq.T <= 0 || n_tiles <= 0 || a.den)
+  if ((a.dh != 64 && a.dh != 128) || !a.pre || a.ldr != a.ldq || roff < 0 || roff % 8 || !al16(a.q) ||
+      !al16(a.out) || !al16(a.state_bf) || a.ldq % 8 || a.ldo % 8 || a.seq.T <= 0 || n_tiles <= 0 || a.den)
     return cudaErrorNotSupported;
-  CUtensorMap tmP, tmS;
-  if (!make_map(&tmP, a.q, (uint64_t)a.ldq, (uint64_t)a.seq.T, (uint64_t)a.ldq, 64, RT, false) ||
-      !make_map(&tmS, a.state_bf, (uint64_t)state_bf_ld(RD), (uint64_t)a.seq.n_seq * a.H * RD,
-                (uint64_t)state_bf_ld(RD), 64, RD, false))
-    return cudaErrorNotSupported;
-  cudaError_t e = cudaFuncSetAttribute(k_readout_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-  if (e != cudaSuccess) return e;
-  const int n_units = n_tiles * a.H;
-  const int grid = n_units < sm_count() ? n_units : sm_count();
-  return launch_pdl(k_readout_tc, dim3(grid), dim3(NTH), SMEM, st, a, tmP, tmS, (int)roff, n_tiles, n_units);
+  return a.dh == 64 ? launch_readout_tc_d<64>(a, n_tiles, roff, st) : launch_readout_tc_d<128>(a, n_tiles, roff, st);
 }
 
 }  // namespace gbla

@@ -15,8 +15,8 @@ bench.py times.
   against the oracle on the same sequences (the whole batch would take the
   oracle most of an hour).
 
-Every run also checks, from the library's launch names, that the d_h = 64
-steps ran their tcgen05 kernels (no silent fallback).
+Every run also checks, from the library's launch names, that the steps with
+a tcgen05 kernel for the shape ran it (no silent fallback).
 
 Workloads (seeded, synthetic; the pages' private long listening histories are
 stood in for by their shapes)."""
@@ -27,7 +27,7 @@ import torch
 import oracle
 from generative_retrieval_encoder_gb300 import build, gbla
 from generative_retrieval_encoder_gb300 import workloads as W
-from gbla_cases import TC_STEPS_DH64, TC_STEPS_DH64_SIGMOID, TOL, assert_tc_variants, f64, launch_names, max_err
+from gbla_cases import TC_STEPS_DH64, TC_STEPS_DH64_SIGMOID, TC_STEPS_DH128, TOL, assert_tc_variants, f64, launch_names, max_err
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -117,7 +117,8 @@ def test_varlen_training_step():
     lens = np.diff(cu)
     order = np.argsort(lens, kind="stable")
     picks = [int(order[len(order) // 10]), int(order[len(order) // 2]), int(order[-1])]  # ... and the longest
-    out, _ = _run(shape, x, P, dy, backward=True)
+    out, names = _run(shape, x, P, dy, backward=True)
+    assert_tc_variants(names, TC_STEPS_DH128)
     y, g = out["y"], out["g"]
     tol = TOL["bf16"]
     Pr = {n: f64(t) for n, t in P.items()}

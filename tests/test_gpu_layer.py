@@ -8,7 +8,7 @@ import torch
 
 from generative_retrieval_encoder_gb300 import build, gbla
 from generative_retrieval_encoder_gb300.workloads import TINY_F32, Workload
-from gbla_cases import (TC_STEPS_DH64, TC_STEPS_DH64_SIGMOID, TOL, assert_tc_variants, f64, launch_names, layer_case,
+from gbla_cases import (TC_STEPS_DH64, TC_STEPS_DH64_SIGMOID, TC_STEPS_DH128, TOL, assert_tc_variants, f64, launch_names, layer_case,
                         max_err, oracle_layer, valid_rows)
 
 pytestmark = pytest.mark.gpu
@@ -62,6 +62,8 @@ def check_layer(wl: Workload):
     names = launch_names(run)
     if wl.dtype == "bf16" and wl.dh == 64:
         assert_tc_variants(names, TC_STEPS_DH64_SIGMOID if wl.gate == "sigmoid" else TC_STEPS_DH64)
+    elif wl.dtype == "bf16" and wl.dh == 128:
+        assert_tc_variants(names, TC_STEPS_DH128)
     y, g = out["y"], out["g"]
     ref = oracle_layer(R, wl, st, ln, backward=True)
     tol = TOL[wl.dtype]
