@@ -53,6 +53,8 @@ def _load():
             lib.oracle_core_explicit.argtypes = seq + [_D] * 5
             lib.oracle_core_lion_rnn.argtypes = seq + [_D] * 5
             lib.oracle_core_backward.argtypes = seq + [_D] * 9
+            lib.oracle_decay_core_explicit.argtypes = seq + [_D] * 7
+            lib.oracle_decay_core_rnn.argtypes = seq + [_D] * 6
             lib.oracle_conv1d.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, _I64, _I64] + [_D] * 4
             layer = ([ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _I64, _I64]
                      + [_D] * 10 + [ctypes.c_int, ctypes.c_double])
@@ -135,6 +137,28 @@ def core_lion_rnn(q, k, v, g, start, ln, H: int, dh: int):
     start, ln, ps, pl = _seqargs(start, ln)
     o = np.zeros((T, H * dh))
     _load().oracle_core_lion_rnn(T, H, dh, len(start), ps, pl, _p(q), _p(k), _p(v), _p(g), _p(o))
+    return o
+
+
+def decay_core_forward(q, k, v, g, lam, start, ln, H: int, dh: int):
+    """The core under LION's decay masks (oracle_decay_core_explicit): lam [T, H]
+    holds lambda_t in [0, 1].  Returns (o [T, H*dh], den [T, H])."""
+    q, k, v, g, lam = map(_f64, (q, k, v, g, lam))
+    T = q.shape[0]
+    start, ln, ps, pl = _seqargs(start, ln)
+    o = np.zeros((T, H * dh)); den = np.zeros((T, H))
+    _load().oracle_decay_core_explicit(T, H, dh, len(start), ps, pl, _p(q), _p(k), _p(v), _p(g), _p(lam), _p(o),
+                                       _p(den))
+    return o, den
+
+
+def decay_core_rnn(q, k, v, g, lam, start, ln, H: int, dh: int):
+    """The same through LION's bidirectional RNN with the decays (Theorem 3.1)."""
+    q, k, v, g, lam = map(_f64, (q, k, v, g, lam))
+    T = q.shape[0]
+    start, ln, ps, pl = _seqargs(start, ln)
+    o = np.zeros((T, H * dh))
+    _load().oracle_decay_core_rnn(T, H, dh, len(start), ps, pl, _p(q), _p(k), _p(v), _p(g), _p(lam), _p(o))
     return o
 
 

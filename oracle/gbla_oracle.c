@@ -17,6 +17,9 @@
  *     all-ones mask, from "Linear Attention for Efficient Bidirectional
  *     Sequence Modeling" (LION notes), "Bidirectional RNN" (Theorem 3.1)
  *     (oracle_core_lion_rnn).
+ * The core under LION's decay masks (Lion-d, Lion-s; LION notes, mask
+ * construction and instantiated models) is stated the same two ways:
+ * oracle_decay_core_explicit (the definition) and oracle_decay_core_rnn.
  *
  * Readings where the pages are silent (each one is listed in the design notes):
  *   phi(x) = elu(x) + 1 with alpha = 1, no 1/sqrt(d_h) scale;
@@ -201,6 +204,112 @@ void oracle_core_lion_rnn(int64_t T, int H, int dh, int n_seq,
           const double kt = g[i * H + h] * phi(k[i * ld + h * dh + e]);
           for (int f = 0; f < W; ++f)
             S[e * W + f] += kt * (f < dh ? v[i * ld + h * dh + f] : 1.0);
+        }
+        double y[1025];
+        for (int f = 0; f < W; ++f) {
+          double acc = 0.0;
+          for (int e = 0; e < dh; ++e) {
+            const double kt = g[i * H + h] * phi(k[i * ld + h * dh + e]);
+            const double vf = f < dh ? v[i * ld + h * dh + f] : 1.0;
+            acc += phi(q[i * ld + h * dh + e]) * (S[e * W + f] - 0.5 * kt * vf);
+          }
+          y[f] = yF[t * W + f] + acc;
+        }
+        for (int f = 0; f < dh; ++f) o[i * ld + h * dh + f] = y[f] / y[dh];
+      }
+      free(yF);
+      free(S);
+    }
+}
+
+/*
+ * The gated core under LION's decay masks ("Linear Attention for Efficient
+ * Bidirectional Sequence Modeling" notes, "Bidirectional mask construction"
+ * and the table of instantiated models): with a decay lambda_t in [0, 1] per
+ * token t (and head),
+ *   M^F_ij = prod_{t=j+1..i} lambda_t (j <= i),  M^B_ij = prod_{t=i+1..j} lambda_t (j >= i),
+ *   M = M^F + M^B - I  (so M_ii = 1),
+ *   o_i = sum_j M_ij g_j (phi(q_i) . phi(k_j)) v_j / sum_j M_ij g_j (phi(q_i) . phi(k_j)),
+ * the row scaling of Y = Scale(Q K^T (.) M) V with this layer's feature map and
+ * key gate.  Lion-d is a constant lambda_t = lambda (M_ij = lambda^|i-j|),
+ * Lion-s a per-token lambda_t = sigmoid(W x_t + b); lambda == 1 gives the
+ * all-ones mask of Eq. 5.  Written as the O(L^2) definition; den_i is the
+ * denominator.
+ */
+void oracle_decay_core_explicit(int64_t T, int H, int dh, int n_seq,
+                                const int64_t* start, const int64_t* len,
+                                const double* q, const double* k, const double* v,
+                                const double* g, const double* lam, double* o, double* den) {
+  (void)T;
+  const int64_t ld = (int64_t)H * dh;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+  for (int b = 0; b < n_seq; ++b)
+    for (int h = 0; h < H; ++h)
+      for (int64_t i = start[b]; i < start[b] + len[b]; ++i) {
+        double num[1024];
+        double dsum = 0.0;
+        for (int f = 0; f < dh; ++f) num[f] = 0.0;
+        for (int64_t j = start[b]; j < start[b] + len[b]; ++j) {
+          /* M_ij: the decays strictly after min(i, j), up to max(i, j) */
+          double m = 1.0;
+          const int64_t lo = i < j ? i : j, hi = i < j ? j : i;
+          for (int64_t t = lo + 1; t <= hi; ++t) m *= lam[t * H + h];
+          double sim = 0.0;
+          for (int e = 0; e < dh; ++e)
+            sim += phi(q[i * ld + h * dh + e]) * phi(k[j * ld + h * dh + e]);
+          const double w = m * g[j * H + h] * sim;
+          for (int f = 0; f < dh; ++f) num[f] += w * v[j * ld + h * dh + f];
+          dsum += w;
+        }
+        for (int f = 0; f < dh; ++f) o[i * ld + h * dh + f] = num[f] / dsum;
+        if (den) den[i * H + h] = dsum;
+      }
+}
+
+/*
+ * The same output from LION's bidirectional RNN (Theorem 3.1) with the decays
+ * as the state transitions, keys k~_j = g_j phi(k_j):
+ *   S^F_i = lambda_i S^F_{i-1} + k~_i v_i^T,      y^F_i = q~_i^T (S^F_i - 1/2 k~_i v_i^T)
+ *   S^B_i = lambda_{i+1} S^B_{i+1} + k~_i v_i^T,  y^B_i = q~_i^T (S^B_i - 1/2 k~_i v_i^T)
+ *   y_i = y^F_i + y^B_i  (numerator with v, denominator with v == 1),
+ * which unrolls to the M^F and M^B of oracle_decay_core_explicit.
+ */
+void oracle_decay_core_rnn(int64_t T, int H, int dh, int n_seq,
+                           const int64_t* start, const int64_t* len,
+                           const double* q, const double* k, const double* v,
+                           const double* g, const double* lam, double* o) {
+  (void)T;
+  const int64_t ld = (int64_t)H * dh;
+  const int W = dh + 1;
+  for (int b = 0; b < n_seq; ++b)
+    for (int h = 0; h < H; ++h) {
+      const int64_t n = len[b], s0 = start[b];
+      double* S = (double*)calloc((size_t)dh * W, sizeof(double));
+      double* yF = (double*)calloc((size_t)(n > 0 ? n : 1) * W, sizeof(double));
+      for (int64_t t = 0; t < n; ++t) {  /* forward */
+        const int64_t i = s0 + t;
+        const double a = t > 0 ? lam[i * H + h] : 0.0;  /* S^F_{-1} = 0 */
+        for (int e = 0; e < dh; ++e) {
+          const double kt = g[i * H + h] * phi(k[i * ld + h * dh + e]);
+          for (int f = 0; f < W; ++f) S[e * W + f] = a * S[e * W + f] + kt * (f < dh ? v[i * ld + h * dh + f] : 1.0);
+        }
+        for (int f = 0; f < W; ++f) {
+          double acc = 0.0;
+          for (int e = 0; e < dh; ++e) {
+            const double kt = g[i * H + h] * phi(k[i * ld + h * dh + e]);
+            const double vf = f < dh ? v[i * ld + h * dh + f] : 1.0;
+            acc += phi(q[i * ld + h * dh + e]) * (S[e * W + f] - 0.5 * kt * vf);
+          }
+          yF[t * W + f] = acc;
+        }
+      }
+      memset(S, 0, sizeof(double) * dh * W);
+      for (int64_t t = n - 1; t >= 0; --t) {  /* backward */
+        const int64_t i = s0 + t;
+        const double a = t + 1 < n ? lam[(i + 1) * H + h] : 0.0;  /* S^B_n = 0 */
+        for (int e = 0; e < dh; ++e) {
+          const double kt = g[i * H + h] * phi(k[i * ld + h * dh + e]);
+          for (int f = 0; f < W; ++f) S[e * W + f] = a * S[e * W + f] + kt * (f < dh ? v[i * ld + h * dh + f] : 1.0);
         }
         double y[1025];
         for (int f = 0; f < W; ++f) {

@@ -47,7 +47,23 @@ CASES = load_cases()
 def test_every_case_cites_the_page():
     assert CASES, "no worked examples found"
     for name, c in CASES.items():
-        assert "Gated Bidirectional Linear Attention" in c.get("cite", ""), name
+        cite = c.get("cite", "")
+        assert "Gated Bidirectional Linear Attention" in cite, name
+        if name.startswith("decay_"):
+            assert "Linear Attention for Efficient Bidirectional Sequence Modeling" in cite, name
+
+
+@pytest.mark.parametrize("name", [n for n in CASES if n.startswith("decay_")])
+def test_decay_core_worked_example(name):
+    c = CASES[name]
+    H, dh = int(c["shape"]["H"]), int(c["shape"]["dh"])
+    T = c["q"].shape[0]
+    start, ln = oracle.seqs(B=1, L=T)
+    o, den = oracle.decay_core_forward(c["q"], c["k"], c["v"], c["g"], c["lam"], start, ln, H, dh)
+    np.testing.assert_allclose(o, c["o"], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(den, c["den"], rtol=1e-14, atol=0)
+    np.testing.assert_allclose(oracle.decay_core_rnn(c["q"], c["k"], c["v"], c["g"], c["lam"], start, ln, H, dh),
+                               c["o"], rtol=0, atol=1e-14)
 
 
 @pytest.mark.parametrize("name", [n for n in CASES if n.startswith("core_")])

@@ -327,3 +327,66 @@ def test_backward_homogeneity_invariants():
         np.testing.assert_allclose((g[sl] * dg[sl]).sum(0), 0, atol=1e-11)
         np.testing.assert_allclose(dv[sl].sum(0), d_o[sl].sum(0), rtol=1e-11, atol=1e-11)
     np.testing.assert_allclose((qt * dqt).reshape(B * L, H, dh).sum(-1), 0, atol=1e-11)
+
+
+# ------------------------------------------------- LION decay masks (Lion-d, Lion-s)
+
+@pytest.mark.parametrize("B,L,H,dh", SHAPES)
+@pytest.mark.parametrize("kind", ["lion-s", "lion-d"])
+def test_decay_core_definition_equals_bidirectional_rnn(B, L, H, dh, kind):
+    """LION Theorem 3.1 with the decays as state transitions (forward and
+    backward scans, -1/2 k_i v_i^T each) equals the masked definition with
+    M = M^F + M^B - I."""
+    q, k, v, g = _rand_core(B * L, H, dh, 21)
+    r = np.random.default_rng(22)
+    lam = r.uniform(0.2, 1.0, (B * L, H)) if kind == "lion-s" else np.full((B * L, H), 0.8)
+    st, ln = oracle.seqs(B, L)
+    o, den = oracle.decay_core_forward(q, k, v, g, lam, st, ln, H, dh)
+    np.testing.assert_allclose(oracle.decay_core_rnn(q, k, v, g, lam, st, ln, H, dh), o, rtol=1e-11, atol=1e-11)
+    assert (den > 0).all()
+
+
+def test_decay_core_with_no_decay_is_the_gbla_core():
+    """lambda = 1 everywhere is the all-ones mask: Eq. 5 exactly."""
+    q, k, v, g = _rand_core(90, 2, 8, 23)
+    st, ln = oracle.seqs(cu_seqlens=[0, 40, 41, 90])
+    o, den = oracle.decay_core_forward(q, k, v, g, np.ones((90, 2)), st, ln, 2, 8)
+    o2, den2, _ = oracle.core_forward(q, k, v, g, st, ln, 2, 8)
+    np.testing.assert_allclose(o, o2, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(den, den2, rtol=1e-12)
+
+
+def test_decay_core_full_decay_returns_each_value():
+    """lambda = 0: every product off the diagonal holds a zero, M = I, o = v."""
+    q, k, v, g = _rand_core(30, 2, 4, 24)
+    st, ln = oracle.seqs(3, 10)
+    o, _ = oracle.decay_core_forward(q, k, v, g, np.zeros((30, 2)), st, ln, 2, 4)
+    np.testing.assert_allclose(o, v, rtol=1e-14, atol=1e-14)
+
+
+def test_lion_d_is_symmetric_under_reversal():
+    """A constant decay gives M_ij = lambda^|i-j|, symmetric in i and j: the
+    outputs of a reversed sequence are the reversed outputs.  (A selective
+    decay shifts by one position under reversal, so this holds for Lion-d.)"""
+    q, k, v, g = _rand_core(25, 2, 8, 25)
+    lam = np.full((25, 2), 0.7)
+    st, ln = oracle.seqs(1, 25)
+    o, _ = oracle.decay_core_forward(q, k, v, g, lam, st, ln, 2, 8)
+    rev = lambda a: np.ascontiguousarray(a[::-1])
+    o2, _ = oracle.decay_core_forward(rev(q), rev(k), rev(v), rev(g), lam, st, ln, 2, 8)
+    np.testing.assert_allclose(rev(o2), o, rtol=1e-12, atol=1e-12)
+
+
+def test_decay_core_outputs_are_convex_combinations_and_sequences_independent():
+    """Mask entries and weights are >= 0, so o_i lies between the smallest and
+    largest v_j of its sequence; a packed sequence equals itself alone."""
+    q, k, v, g = _rand_core(60, 1, 4, 26)
+    lam = np.random.default_rng(27).uniform(0.0, 1.0, (60, 1))
+    st, ln = oracle.seqs(cu_seqlens=[0, 25, 60])
+    o, _ = oracle.decay_core_forward(q, k, v, g, lam, st, ln, 1, 4)
+    for a, n in zip(st, ln):
+        seg = v[a:a + n]
+        assert (o[a:a + n] >= seg.min(0) - 1e-12).all() and (o[a:a + n] <= seg.max(0) + 1e-12).all()
+        s1, l1 = oracle.seqs(1, int(n))
+        alone, _ = oracle.decay_core_forward(q[a:a + n], k[a:a + n], v[a:a + n], g[a:a + n], lam[a:a + n], s1, l1, 1, 4)
+        np.testing.assert_allclose(o[a:a + n], alone, rtol=1e-13, atol=1e-13)
