@@ -143,8 +143,14 @@ struct Layout {
   size_t partial, partial_m, state, state_bf, state_m, center;
   size_t xt, P, gate, Wt;
   size_t Wp, dP, dxt, dW, dstate, dstate_bf, gamma_part, bg_part, conv_part;
+  size_t pre_d, LF, LB, lamc, HF, HB;  // the decay core: its chunks' prefix, chunk and scan states
   size_t total;
 };
+
+// Chunks (128 rows, per sequence) of the decay core.
+int decay_chunks(const Plan& p) {
+  return p.mode == SEQ_VARLEN ? cdiv(p.T, kDecayChunk) + p.n_seq : cdiv(p.L, kDecayChunk) * p.n_seq;
+}
 
 struct Cursor {
   size_t off = 0;
@@ -212,6 +218,14 @@ Layout ws_layout(const Plan& p, int op) {
     // db_g partial rows: two per tile (tcgen05 kernel) or one per chunk
     l.bg_part = c.take((size_t)std::max(2 * p.n_tiles, p.n_chunks) * p.H * 4);
     l.conv_part = c.take((size_t)p.conv_blocks * p.d * 5 * 4);
+  } else if (op == GBLA_OP_DECAY_FORWARD) {
+    const size_t ch = (size_t)decay_chunks(p) * p.H;
+    if (p.mode == SEQ_VARLEN) l.pre_d = c.take((size_t)(p.n_seq + 1) * 4);
+    l.LF = c.take(ch * p.dh * state_ld(p.dh) * 4);
+    l.LB = c.take(ch * p.dh * state_ld(p.dh) * 4);
+    l.lamc = c.take(ch * 4);
+    l.HF = c.take(ch * p.dh * state_bf_ld(p.dh) * 2);
+    l.HB = c.take(ch * p.dh * state_bf_ld(p.dh) * 2);
   } else {  // core forward / backward
     l.state = c.take(state_bytes(p));
     l.state_bf = c.take(state_bf_bytes(p));
@@ -439,7 +453,7 @@ gbla_status gbla_validate_shape(const gbla_shape* shape) {
 size_t gbla_workspace_size(const gbla_shape* shape, int op) {
   Plan p;
   if (make_plan(shape, p) != GBLA_OK) return 0;
-  if (op < GBLA_OP_FORWARD || op > GBLA_OP_CORE_BACKWARD) return 0;
+  if (op < GBLA_OP_FORWARD || op > GBLA_OP_DECAY_FORWARD) return 0;
   return ws_layout(p, op).total;
 }
 
@@ -701,6 +715,41 @@ gbla_status bla_core_backward(const gbla_shape* shape, const void* q, const void
   kv.H = p.H; kv.dh = p.dh; kv.seq = c.seq; kv.tiles = c.tiles; kv.err = c.kerr;
   GBLA_CHECK(p.f32 ? launch_bwd_kv_f32(kv, p.n_tiles, c.st) : launch_bwd_kv_chunks_bf16(kv, c.chunks, p.n_chunks, c.st),
              p.f32 ? "bwd_kv[f32]" : "bwd_kv[mma]");
+  return GBLA_OK;
+}
+
+gbla_status bla_decay_core_forward(const gbla_shape* shape, const void* q, const void* k, const void* v,
+                                   const float* g, const float* lam, void* o, float* den, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  for (const void* ptr : {q, k, v, (const void*)g, (const void*)lam, (const void*)o})
+    if (!ptr || !aligned16(ptr)) return GBLA_ERR_INVALID_ARG;
+  if (den && !aligned16(den)) return GBLA_ERR_INVALID_ARG;
+  Plan p0;
+  gbla_status r = make_plan(shape, p0);
+  if (r != GBLA_OK) return r;
+  if (p0.f32 || p0.dh != 64) return GBLA_ERR_UNSUPPORTED;
+  Ctx c;
+  if ((r = begin(shape, GBLA_OP_DECAY_FORWARD, ws, ws_bytes, stream, c)) != GBLA_OK) return r;
+  const Plan& p = c.p;
+  DecayArgs a{};
+  a.q = q; a.k = k; a.v = v; a.ld = p.HD;
+  a.g = g; a.lam = lam; a.ldg = p.H;
+  a.o = o; a.den = den;
+  a.LF = at<float>(ws, c.l.LF); a.LB = at<float>(ws, c.l.LB); a.Lam = at<float>(ws, c.l.lamc);
+  a.HF = at<bf16>(ws, c.l.HF); a.HB = at<bf16>(ws, c.l.HB);
+  a.H = p.H; a.dh = p.dh; a.seq = c.seq; a.err = c.kerr;
+  a.tiles.tile = kDecayChunk;
+  a.tiles.per_seq = p.mode == SEQ_VARLEN ? 0 : cdiv(p.L, kDecayChunk);
+  a.tiles.prefix = p.mode == SEQ_VARLEN ? at<int32_t>(ws, c.l.pre_d) : nullptr;
+  if (p.mode == SEQ_VARLEN) {
+    const int ts[1] = {kDecayChunk};
+    int32_t* pre[1] = {at<int32_t>(ws, c.l.pre_d)};
+    GBLA_CHECK(launch_plan(c.seq, 1, ts, pre, c.err, c.st), "plan");
+  }
+  // the launcher records its own launches; bracket them as one timed step
+  const char* names[4] = {"", "", "", ""};
+  int launches = 0;
+  GBLA_CHECK(launch_decay_forward(a, decay_chunks(p), p.n_seq, c.st, names, &launches), "decay core[mma]");
   return GBLA_OK;
 }
 

@@ -144,6 +144,19 @@ struct ConvArgs {
   int* err_out;         // workspace error word: a bounded wait that gave up sets kErrTimeout
 };
 
+// The core under LION's decay masks (decay.cu): raw q, k, v (bf16, phi
+// applied inside), gate values g and decays lam in [0, 1] per row and head.
+struct DecayArgs {
+  const void* q; const void* k; const void* v; int64_t ld;  // [rows, ld], head h at column h*dh
+  const float* g; const float* lam; int64_t ldg;            // [rows, ldg]
+  void* o; float* den;                                      // o like q; den [rows, ldg] or null
+  float* LF; float* LB; float* Lam;                         // chunk states [chunks*H][dh][dh+8] fp32, decays [chunks*H]
+  bf16* HF; bf16* HB;                                       // scan states [chunks*H][dh][dh+16] bf16
+  int H, dh;
+  SeqDesc seq; Tiling tiles;                                // tiles: the 128-row chunks
+  const int* err;
+};
+
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_plan(const SeqDesc& s, int ntile, const int* tile_sizes, int32_t* const* prefixes,
                         int* err, cudaStream_t st);
@@ -190,6 +203,12 @@ inline cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st, int* variant 
 }
 
 // *tiled = 1 when the bulk-copy staged bf16 kernel ran, 0 for the plain one.
+// The three (four with padding) launches of the decay core; names[i] and
+// *launches report what ran.  cudaErrorNotSupported unless d_h = 64.
+cudaError_t launch_decay_forward(const DecayArgs& a, int n_chunks, int n_seq, cudaStream_t st, const char** names,
+                                 int* launches);
+constexpr int kDecayChunk = 128;  // rows per chunk of the decay core
+
 cudaError_t launch_conv_fwd(const ConvArgs& a, bool f32, cudaStream_t st, int* tiled = nullptr);
 // Writes the parameter-gradient partials to part[0 .. *nparts)[d][5].
 cudaError_t launch_conv_bwd(const ConvArgs& a, bool f32, int* nparts, cudaStream_t st, int* tiled = nullptr);

@@ -21,13 +21,13 @@ GBLA_ERR_DEVICE_TIMEOUT = -6
 GBLA_POLICY_AUTO, GBLA_POLICY_TC = 0, 1
 GBLA_F32, GBLA_BF16 = 0, 1
 GBLA_GATE_SIGMOID, GBLA_GATE_SOFTMAX = 0, 1
-GBLA_OP_FORWARD, GBLA_OP_BACKWARD, GBLA_OP_CORE_FORWARD, GBLA_OP_CORE_BACKWARD = 0, 1, 2, 3
+GBLA_OP_FORWARD, GBLA_OP_BACKWARD, GBLA_OP_CORE_FORWARD, GBLA_OP_CORE_BACKWARD, GBLA_OP_DECAY_FORWARD = 0, 1, 2, 3, 4
 
 EXPORTS = ("gbla_workspace_size", "gbla_saved_size", "gbla_validate_shape", "gbla_forward", "gbla_backward",
            "bla_core_forward", "bla_core_backward", "gbla_check_device_status", "gbla_status_string",
            "gbla_last_error", "gbla_version", "gbla_profiling_enable", "gbla_profiling_read",
            "bla_core_forward_noalloc", "bla_core_noalloc_check_device_status", "gbla_diag_bounded_wait",
-           "gbla_set_kernel_policy")
+           "gbla_set_kernel_policy", "bla_decay_core_forward")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -73,6 +73,8 @@ def lib() -> ctypes.CDLL:
         L.bla_core_forward.restype = ctypes.c_int
         L.bla_core_backward.argtypes = [sp] + [vp] * 10 + [sz, vp]
         L.bla_core_backward.restype = ctypes.c_int
+        L.bla_decay_core_forward.argtypes = [sp] + [vp] * 9 + [sz, vp]
+        L.bla_decay_core_forward.restype = ctypes.c_int
         L.bla_core_forward_noalloc.argtypes = [sp] + [vp] * 8
         L.bla_core_forward_noalloc.restype = ctypes.c_int
         L.bla_core_noalloc_check_device_status.argtypes = [vp]
@@ -223,6 +225,22 @@ def bla_core_forward(shape: Shape, q, k, v, g, o=None, den=None, state=None, ws=
                                 _stream())
     _check(st, "bla_core_forward")
     return o, den, state
+
+
+def bla_decay_core_forward(shape: Shape, q, k, v, g, lam, o=None, den=None, ws=None):
+    """The core under LION's decay masks (see gbla.h): returns (o, den)."""
+    dev = q.device
+    if o is None:
+        o = torch.empty_like(q)
+    if den is True:
+        den = torch.empty(rows(shape), shape.H, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(shape, GBLA_OP_DECAY_FORWARD, dev)
+    st = lib().bla_decay_core_forward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(lam), _ptr(o),
+                                      _ptr(den if isinstance(den, torch.Tensor) else None), _ptr(ws), ws.numel(),
+                                      _stream())
+    _check(st, "bla_decay_core_forward")
+    return o, den
 
 
 def bla_core_forward_noalloc(shape: Shape, q, k, v, g, o, den=None, state=None) -> int:

@@ -83,7 +83,8 @@ typedef enum {
   GBLA_OP_FORWARD = 0,        /* gbla_forward                                */
   GBLA_OP_BACKWARD = 1,       /* gbla_backward                               */
   GBLA_OP_CORE_FORWARD = 2,   /* bla_core_forward                            */
-  GBLA_OP_CORE_BACKWARD = 3   /* bla_core_backward                           */
+  GBLA_OP_CORE_BACKWARD = 3,  /* bla_core_backward                           */
+  GBLA_OP_DECAY_FORWARD = 4   /* bla_decay_core_forward                      */
 } gbla_op;
 
 typedef struct {
@@ -177,6 +178,31 @@ gbla_status bla_core_backward(const gbla_shape* shape, const void* q,
                               const void* d_o, void* dq, void* dk, void* dv,
                               float* dg, void* ws, size_t ws_bytes,
                               void* stream);
+
+/*
+ * The gated core under LION's decay masks ("Linear Attention for Efficient
+ * Bidirectional Sequence Modeling": mask construction and the Lion-d /
+ * Lion-s models), with this layer's phi = elu + 1 and key gate (Eq. 5):
+ *   M^F_ij = prod_{t=j+1..i} lam_t (j <= i),  M^B_ij = prod_{t=i+1..j} lam_t (j >= i),
+ *   M = M^F + M^B - I,
+ *   o_i = sum_j M_ij g_j (phi(q_i).phi(k_j)) v_j / sum_j M_ij g_j (phi(q_i).phi(k_j)).
+ * Lion-d passes one constant decay for every token (M_ij = lam^|i-j|), Lion-s
+ * a decay per token (e.g. sigmoid(W x_t + b)); lam = 1 everywhere is
+ * bla_core_forward.  Computed in the bidirectional chunkwise form: 128-row
+ * chunks, their local states, a forward and a backward scan over the chunk
+ * states, then each chunk's decayed attention plus the two scanned states.
+ *   q, k, v (bf16) [rows, H*d_h] (phi is applied inside); g fp32 [rows, H]
+ *   gate values >= 0; lam fp32 [rows, H] decays in [0, 1] (lam_t of a
+ *   sequence's first token enters no product); o (bf16) [rows, H*d_h];
+ *   den fp32 [rows, H] or NULL.
+ *   bf16 I/O and d_h = 64 only (GBLA_ERR_UNSUPPORTED otherwise).  Workspace:
+ *   gbla_workspace_size(shape, GBLA_OP_DECAY_FORWARD).  The shape's d, gate and
+ *   rms_eps are ignored.
+ */
+gbla_status bla_decay_core_forward(const gbla_shape* shape, const void* q,
+                                   const void* k, const void* v, const float* g,
+                                   const float* lam, void* o, float* den,
+                                   void* ws, size_t ws_bytes, void* stream);
 
 /*
  * bla_core_forward without a caller workspace (the pages have no counterpart:

@@ -240,8 +240,14 @@ void oracle_decay_core_explicit(int64_t T, int H, int dh, int n_seq,
                                 const int64_t* start, const int64_t* len,
                                 const double* q, const double* k, const double* v,
                                 const double* g, const double* lam, double* o, double* den) {
-  (void)T;
   const int64_t ld = (int64_t)H * dh;
+  /* phi(q) and phi(k), once */
+  double* pq = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * ld);
+  double* pk = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * ld);
+  for (int64_t i = 0; i < T * ld; ++i) {
+    pq[i] = phi(q[i]);
+    pk[i] = phi(k[i]);
+  }
 #pragma omp parallel for collapse(2) schedule(dynamic)
   for (int b = 0; b < n_seq; ++b)
     for (int h = 0; h < H; ++h)
@@ -249,21 +255,26 @@ void oracle_decay_core_explicit(int64_t T, int H, int dh, int n_seq,
         double num[1024];
         double dsum = 0.0;
         for (int f = 0; f < dh; ++f) num[f] = 0.0;
-        for (int64_t j = start[b]; j < start[b] + len[b]; ++j) {
-          /* M_ij: the decays strictly after min(i, j), up to max(i, j) */
+        /* M_ij for j = i, then outward: going down, M_ij = M_i(j+1) lambda_{j+1};
+         * going up, M_ij = M_i(j-1) lambda_j (the decays strictly after
+         * min(i, j) and up to max(i, j)) */
+        for (int dir = 0; dir < 2; ++dir) {
           double m = 1.0;
-          const int64_t lo = i < j ? i : j, hi = i < j ? j : i;
-          for (int64_t t = lo + 1; t <= hi; ++t) m *= lam[t * H + h];
-          double sim = 0.0;
-          for (int e = 0; e < dh; ++e)
-            sim += phi(q[i * ld + h * dh + e]) * phi(k[j * ld + h * dh + e]);
-          const double w = m * g[j * H + h] * sim;
-          for (int f = 0; f < dh; ++f) num[f] += w * v[j * ld + h * dh + f];
-          dsum += w;
+          for (int64_t j = dir == 0 ? i : i + 1; dir == 0 ? j >= start[b] : j < start[b] + len[b]; j += dir == 0 ? -1 : 1) {
+            if (dir == 0 && j < i) m *= lam[(j + 1) * H + h];
+            if (dir == 1) m *= lam[j * H + h];
+            double sim = 0.0;
+            for (int e = 0; e < dh; ++e) sim += pq[i * ld + h * dh + e] * pk[j * ld + h * dh + e];
+            const double w = m * g[j * H + h] * sim;
+            for (int f = 0; f < dh; ++f) num[f] += w * v[j * ld + h * dh + f];
+            dsum += w;
+          }
         }
         for (int f = 0; f < dh; ++f) o[i * ld + h * dh + f] = num[f] / dsum;
         if (den) den[i * H + h] = dsum;
       }
+  free(pq);
+  free(pk);
 }
 
 /*
