@@ -73,7 +73,7 @@ def lib() -> ctypes.CDLL:
         L.bla_core_forward.restype = ctypes.c_int
         L.bla_core_backward.argtypes = [sp] + [vp] * 10 + [sz, vp]
         L.bla_core_backward.restype = ctypes.c_int
-        L.bla_decay_core_forward.argtypes = [sp] + [vp] * 9 + [sz, vp]
+        L.bla_decay_core_forward.argtypes = [sp] + [vp] * 8 + [sz, vp]
         L.bla_decay_core_forward.restype = ctypes.c_int
         L.bla_core_forward_noalloc.argtypes = [sp] + [vp] * 8
         L.bla_core_forward_noalloc.restype = ctypes.c_int
