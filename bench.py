@@ -252,6 +252,118 @@ def l_scaling(wl, dev, timed, tokens: int = 262144, steps: int = 3):
     return out
 
 
+def profile(fn, flush, reps: int = 3):
+    """Per-launch times (library CUDA events on the launching stream) of fn,
+    averaged over reps runs: ({step name: ms}, {step name: kernel variant})."""
+    from generative_retrieval_encoder_gb300 import gbla
+    gbla.gbla_profiling_enable(True)
+    gbla.gbla_profiling_read()
+    for _ in range(reps):
+        flush.fill_(1.0)
+        fn()
+    rec = gbla.gbla_profiling_read()
+    gbla.gbla_profiling_enable(False)
+    per, variant = {}, {}
+    for n, ms in rec:
+        base = n.split("[")[0]
+        per.setdefault(base, []).append(ms)
+        if "[" in n:
+            variant[base] = n[len(base) + 1:-1]
+    return {n: sum(v) / reps for n, v in per.items()}, variant
+
+
+def roof_entry(name, ms, amount, bound, peaks, variant=None):
+    """One kernel's line: time, achieved rate on its algorithmic work, fraction of the measured peak."""
+    e = {"ms": round(ms, 4)}
+    if variant:
+        e["variant"] = variant
+    if amount is not None:
+        ach = amount / (ms * 1e-3) / (1e9 if bound == "hbm" else 1e12)
+        e["achieved"] = round(ach, 1)
+        e["unit"] = "GB/s" if bound == "hbm" else "TFLOP/s"
+        e["frac"] = round(ach / (peaks["hbm_gbs"] if bound == "hbm" else peaks["bf16_tflops_sustained"]), 3)
+    return e
+
+
+def other_workloads(dev, timed, flush, peaks, steps: int = 5):
+    """fwd+bwd and forward tokens/s of the other workloads (B=8 L=32768 long
+    history, B=16 L=8192 training, 256 varlen sequences at d=1024, d_h=128),
+    with the top kernels and their roofline fractions."""
+    import torch
+    from generative_retrieval_encoder_gb300 import gbla
+    out = {}
+    for name, wl in workloads().items():
+        if name == "train2k":
+            continue
+        shape, x_h, dy_h, P = make_inputs(wl, dev)
+        T = gbla.rows(shape)
+        x, dy = x_h.to(dev), dy_h.to(dev)
+        del x_h, dy_h
+        y = torch.empty(T, wl.H * wl.dh, dtype=x.dtype, device=dev)
+        saved = torch.empty(gbla.gbla_saved_size(shape), dtype=torch.uint8, device=dev)
+        ws_f = gbla.workspace(shape, gbla.GBLA_OP_FORWARD, dev)
+        ws_b = gbla.workspace(shape, gbla.GBLA_OP_BACKWARD, dev)
+        fwd = lambda: gbla.gbla_forward(shape, x, P, y=y, saved=saved, ws=ws_f)
+        step = lambda: (fwd(), gbla.gbla_backward(shape, x, P, saved, dy, ws=ws_b))
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        kern, variant = profile(step, flush, reps=2)
+        alg = algorithmic(wl, T)
+        tops = sorted(((n, ms) for n, ms in kern.items() if n in alg), key=lambda kv: -kv[1])[:4]
+        tokens = wl.valid_tokens()
+        ms_step, ms_fwd = timed(step, steps), timed(fwd, steps)
+        out[name] = {"workload": wl.name, "tokens": tokens, "ms_per_step": round(ms_step, 3),
+                     "fwd_bwd_tokens_per_s": tokens / (ms_step * 1e-3), "fwd_tokens_per_s": tokens / (ms_fwd * 1e-3),
+                     "top_kernels": {n: roof_entry(n, ms, alg[n][1], alg[n][0], peaks, variant.get(n)) for n, ms in tops}}
+        del x, dy, y, saved, ws_f, ws_b
+        torch.cuda.empty_cache()
+    return out
+
+
+def cores(wl, dev, timed, flush, peaks, steps: int = 10):
+    """The gated core alone (bla_core_forward / bla_core_backward) and the core
+    under LION's decay masks (bla_decay_core_forward) on the workload's
+    tokens and heads: tokens/s and HBM rate on their algorithmic bytes per
+    token-head (core forward 8 d_h + 4: q, k, v, g in, o out; backward
+    14 d_h + 8: q, k, v, g, do in, dq, dk, dv, dg out; decay forward
+    8 d_h + 8: q, k, v, g, lambda in, o out)."""
+    import torch
+    from generative_retrieval_encoder_gb300 import gbla
+    B, L, H, dh = wl.B, wl.L, wl.H, wl.dh
+    T = B * L
+    shape = gbla.make_shape(B, L, H * dh, H, dh)
+    r = torch.Generator().manual_seed(1234)
+    q, k, v, d_o = (torch.randn(T, H * dh, generator=r).to(torch.bfloat16).to(dev) for _ in range(4))
+    g = (torch.rand(T, H, generator=r) * 0.98 + 0.01).to(dev)
+    lam = (0.85 + 0.15 * torch.rand(T, H, generator=r)).to(dev)
+    o = torch.empty_like(q)
+    ws_f = gbla.workspace(shape, gbla.GBLA_OP_CORE_FORWARD, dev)
+    ws_b = gbla.workspace(shape, gbla.GBLA_OP_CORE_BACKWARD, dev)
+    ws_d = gbla.workspace(shape, gbla.GBLA_OP_DECAY_FORWARD, dev)
+    fwd = lambda: gbla.bla_core_forward(shape, q, k, v, g, o=o, ws=ws_f)
+    bwd = lambda: gbla.bla_core_backward(shape, q, k, v, g, d_o, ws=ws_b)
+    dec = lambda: gbla.bla_decay_core_forward(shape, q, k, v, g, lam, o=o, ws=ws_d)
+    for fn in (fwd, bwd, dec):
+        for _ in range(3):
+            fn()
+    torch.cuda.synchronize()
+    th = T * H
+    out = {"shape": f"B={B} L={L} H={H} d_h={dh} bf16"}
+    for name, fn, per_th in (("core_forward", fwd, 8 * dh + 4), ("core_backward", bwd, 14 * dh + 8),
+                             ("decay_core_forward", dec, 8 * dh + 8)):
+        ms = timed(fn, steps)
+        kern, variant = profile(fn, flush)
+        out[name] = {"ms": round(ms, 4), "tokens_per_s": T / (ms * 1e-3),
+                     "algorithmic_bytes": th * per_th, "achieved_GBps": round(th * per_th / (ms * 1e-3) / 1e9, 1),
+                     "frac": round(th * per_th / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3),
+                     "kernels": {n: roof_entry(n, t, None, None, peaks, variant.get(n))
+                                 for n, t in sorted(kern.items(), key=lambda kv: -kv[1]) if n != "memset"}}
+    del q, k, v, d_o, g, lam, o, ws_f, ws_b, ws_d
+    torch.cuda.empty_cache()
+    return out
+
+
 def rank_max(v: float, world: int, device) -> float:
     """The largest v over the ranks: a job's time is that of its slowest rank."""
     if world == 1:
@@ -420,10 +532,12 @@ def run_ours(args, wl, rank: int, world: int, local_rank: int):
 
     # linearity in L: the same number of tokens (B L = 262144) at L = 2k .. 32k
     scaling = l_scaling(wl, dev, timed) if args.scaling else None
+    peaks, peak_src = load_peaks()
+    extra = other_workloads(dev, timed, flush, peaks) if args.scaling and wl.name == workloads()["train2k"].name else None
+    core = cores(wl, dev, timed, flush, peaks) if wl.dh == 64 and wl.dtype == "bf16" and wl.lengths() is None else None
 
     if rank != 0:
         return
-    peaks, peak_src = load_peaks()
     alg = algorithmic(wl, T)
     if any(variant.get(n) not in (None, "tc") for n in ("reduce", "readout", "bwd_q", "bwd_kv")) and wl.dh == 64:
         print(f"warning: a d_h = 64 state kernel ran without tcgen05: {variant}", file=sys.stderr)
@@ -468,7 +582,9 @@ def run_ours(args, wl, rank: int, world: int, local_rank: int):
                     "pipeline": "step k+1's H2D and step k-1's D2H on two more streams under step k's compute"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
-            "l_scaling": scaling}
+            "l_scaling": scaling,
+            "other_workloads": extra,
+            "cores": core}
     print(json.dumps(line), flush=True)
 
 

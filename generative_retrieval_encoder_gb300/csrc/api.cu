@@ -746,10 +746,9 @@ gbla_status bla_decay_core_forward(const gbla_shape* shape, const void* q, const
     int32_t* pre[1] = {at<int32_t>(ws, c.l.pre_d)};
     GBLA_CHECK(launch_plan(c.seq, 1, ts, pre, c.err, c.st), "plan");
   }
-  // the launcher records its own launches; bracket them as one timed step
-  const char* names[4] = {"", "", "", ""};
-  int launches = 0;
-  GBLA_CHECK(launch_decay_forward(a, decay_chunks(p), p.n_seq, c.st, names, &launches), "decay core[mma]");
+  GBLA_CHECK(launch_decay_states(a, decay_chunks(p), c.st), "decay states[mma]");
+  GBLA_CHECK(launch_decay_scan(a, p.n_seq, c.st), "decay scan");
+  GBLA_CHECK(launch_decay_out(a, decay_chunks(p), c.st), "decay out[mma]");
   return GBLA_OK;
 }
 

@@ -398,30 +398,25 @@ __global__ void k_decay_pad(const DecayArgs a) {
 
 }  // namespace
 
-cudaError_t launch_decay_forward(const DecayArgs& a, int n_chunks, int n_seq, cudaStream_t st, const char** names,
-                                 int* launches) {
-  *launches = 0;
+cudaError_t launch_decay_states(const DecayArgs& a, int n_chunks, cudaStream_t st) {
   if (a.dh != DD) return cudaErrorNotSupported;
-  cudaError_t e;
-  names[0] = "decay states[mma]";
-  if ((e = launch_pdl(k_decay_states, dim3(n_chunks, a.H), dim3(256), STATES_SMEM, st, a)) != cudaSuccess) return e;
-  ++*launches;
-  names[1] = "decay scan";
-  if ((e = launch_pdl(k_decay_scan, dim3(n_seq, a.H), dim3(256), 0, st, a)) != cudaSuccess) return e;
-  ++*launches;
-  names[2] = "decay out[mma]";
-  if ((e = cudaFuncSetAttribute(k_decay_out, cudaFuncAttributeMaxDynamicSharedMemorySize, OUT_SMEM)) != cudaSuccess)
-    return e;
-  if ((e = launch_pdl(k_decay_out, dim3(n_chunks, a.H), dim3(256), OUT_SMEM, st, a)) != cudaSuccess) return e;
-  ++*launches;
-  if (a.seq.mode == SEQ_PADDED) {
-    names[3] = "decay pad";
-    const long long n = (long long)a.seq.T * a.H * DD;
-    k_decay_pad<<<(unsigned)std::min<long long>((n + 255) / 256, 4096), 256, 0, st>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    ++*launches;
-  }
-  return cudaSuccess;
+  return launch_pdl(k_decay_states, dim3(n_chunks, a.H), dim3(256), STATES_SMEM, st, a);
+}
+
+cudaError_t launch_decay_scan(const DecayArgs& a, int n_seq, cudaStream_t st) {
+  if (a.dh != DD) return cudaErrorNotSupported;
+  return launch_pdl(k_decay_scan, dim3(n_seq, a.H), dim3(256), 0, st, a);
+}
+
+cudaError_t launch_decay_out(const DecayArgs& a, int n_chunks, cudaStream_t st) {
+  if (a.dh != DD) return cudaErrorNotSupported;
+  cudaError_t e = cudaFuncSetAttribute(k_decay_out, cudaFuncAttributeMaxDynamicSharedMemorySize, OUT_SMEM);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(k_decay_out, dim3(n_chunks, a.H), dim3(256), OUT_SMEM, st, a);
+  if (e != cudaSuccess || a.seq.mode != SEQ_PADDED) return e;
+  const long long n = (long long)a.seq.T * a.H * DD;
+  k_decay_pad<<<(unsigned)std::min<long long>((n + 255) / 256, 4096), 256, 0, st>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace gbla

@@ -203,10 +203,12 @@ inline cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st, int* variant 
 }
 
 // *tiled = 1 when the bulk-copy staged bf16 kernel ran, 0 for the plain one.
-// The three (four with padding) launches of the decay core; names[i] and
-// *launches report what ran.  cudaErrorNotSupported unless d_h = 64.
-cudaError_t launch_decay_forward(const DecayArgs& a, int n_chunks, int n_seq, cudaStream_t st, const char** names,
-                                 int* launches);
+// The launches of the decay core, in order: the chunks' local states, the
+// scans per (sequence, head), the outputs (and, with padding, the zero rows).
+// cudaErrorNotSupported unless d_h = 64.
+cudaError_t launch_decay_states(const DecayArgs& a, int n_chunks, cudaStream_t st);
+cudaError_t launch_decay_scan(const DecayArgs& a, int n_seq, cudaStream_t st);
+cudaError_t launch_decay_out(const DecayArgs& a, int n_chunks, cudaStream_t st);
 constexpr int kDecayChunk = 128;  // rows per chunk of the decay core
 
 cudaError_t launch_conv_fwd(const ConvArgs& a, bool f32, cudaStream_t st, int* tiled = nullptr);

@@ -64,7 +64,7 @@ def test_decay_core_matches_oracle(case):
     names = launch_names(lambda: out.update(zip(("o", "den"), gbla.bla_decay_core_forward(
         shape, D["q"], D["k"], D["v"], D["g"], lam, den=True))))
     torch.cuda.synchronize()
-    assert any(n.startswith("decay core") for n in names), names
+    assert [n for n in names if n.startswith("decay")] == ["decay states[mma]", "decay scan", "decay out[mma]"], names
     ro, rden = oracle.decay_core_forward(R["q"], R["k"], R["v"], R["g"], f64(lam), st, ln, H, 64)
     m = valid_rows(st, ln, T)
     go, gden = f64(out["o"]), f64(out["den"])
