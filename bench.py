@@ -321,7 +321,7 @@ def other_workloads(dev, timed, flush, peaks, steps: int = 5):
     return out
 
 
-def cores(wl, dev, timed, flush, peaks, steps: int = 10):
+def core_lines(wl, dev, timed, flush, peaks, steps: int = 10):
     """The gated core alone (bla_core_forward / bla_core_backward) and the core
     under LION's decay masks (bla_decay_core_forward) on the workload's
     tokens and heads: tokens/s and HBM rate on their algorithmic bytes per
@@ -534,7 +534,7 @@ def run_ours(args, wl, rank: int, world: int, local_rank: int):
     scaling = l_scaling(wl, dev, timed) if args.scaling else None
     peaks, peak_src = load_peaks()
     extra = other_workloads(dev, timed, flush, peaks) if args.scaling and wl.name == workloads()["train2k"].name else None
-    core = cores(wl, dev, timed, flush, peaks) if wl.dh == 64 and wl.dtype == "bf16" and wl.lengths() is None else None
+    core = core_lines(wl, dev, timed, flush, peaks) if wl.dh == 64 and wl.dtype == "bf16" and wl.lengths() is None else None
 
     if rank != 0:
         return
