@@ -539,7 +539,7 @@ def run_ours(args, wl, rank: int, world: int, local_rank: int):
     if rank != 0:
         return
     alg = algorithmic(wl, T)
-    if any(variant.get(n) not in (None, "tc") for n in ("reduce", "readout", "bwd_q", "bwd_kv")) and wl.dh == 64:
+    if any(variant.get(n) not in (None, "tc") for n in ("readout", "bwd_q", "bwd_kv")) and wl.dh == 64:
         print(f"warning: a d_h = 64 state kernel ran without tcgen05: {variant}", file=sys.stderr)
     dom = max((n for n in kern if n in alg), key=lambda n: kern[n])
     bound, amount = alg[dom]
