@@ -390,7 +390,10 @@ cudaError_t launch_bwd_kv_layer_bf16(const BwdKVArgs& kv, int n_tiles, const Til
 cudaError_t launch_bwd_q_layer_bf16(const BwdQArgs& q, int hd, int n_chunks, int n_tiles, int* gamma_rows,
                                     cudaStream_t st, const char** nm) {
   *nm = "bwd_q[tc]";
-  const cudaError_t e = launch_bwd_q_tc(q, hd, n_tiles, gamma_rows, st);
+  cudaError_t e = launch_bwd_q_tc(q, hd, n_tiles, gamma_rows, st);
+  if (e != cudaErrorNotSupported) return e;
+  (void)cudaGetLastError();
+  e = launch_bwd_q_tc128(q, hd, n_tiles, gamma_rows, st);
   if (e != cudaErrorNotSupported) return e;
   (void)cudaGetLastError();
   *nm = "bwd_q[mma]";

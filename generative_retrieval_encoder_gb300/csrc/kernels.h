@@ -172,6 +172,8 @@ cudaError_t launch_bwd_q_bf16(const BwdQArgs& a, bool norm, int grid_x, cudaStre
 // Its CTAs (two per SM) take contiguous ranges of the (128-row tile, head)
 // units of a.tiles (n_tiles tiles); *nparts = the dgamma partial rows written.
 cudaError_t launch_bwd_q_tc(const BwdQArgs& a, int hd, int n_tiles, int* nparts, cudaStream_t st);
+// The same at d_h = 128 (bwd_q_tc128.cu), one CTA per SM.
+cudaError_t launch_bwd_q_tc128(const BwdQArgs& a, int hd, int n_tiles, int* nparts, cudaStream_t st);
 // tcgen05 readout with the RmsNorm gate (readout_tc.cu): d_h = 64, phi(q)
 // stored (pre), no den output; cudaErrorNotSupported otherwise.
 cudaError_t launch_readout_tc(const ReadoutArgs& a, int n_tiles, cudaStream_t st);

@@ -104,8 +104,8 @@ TC_STEPS_DH64 = ("projection gemm", "readout", "bwd_q", "bwd_kv", "dx~ gemm", "d
 # ... and the state reduction, where the gate holds values (sigmoid gate, core
 # API); under the softmax gate it runs the mma.sync kernel (chunk maxima).
 TC_STEPS_DH64_SIGMOID = TC_STEPS_DH64 + ("reduce",)
-# At d_h = 128: the GEMMs, the readout and the key-side backward.
-TC_STEPS_DH128 = ("projection gemm", "readout", "bwd_kv", "dx~ gemm", "dW gemm")
+# At d_h = 128: the GEMMs, the readout and both backward steps.
+TC_STEPS_DH128 = ("projection gemm", "readout", "bwd_q", "bwd_kv", "dx~ gemm", "dW gemm")
 
 
 def assert_tc_variants(names, steps=TC_STEPS_DH64):
