@@ -20,10 +20,10 @@
 // head) units, one CTA per SM (the shared memory holds two 96 KB stages and
 // the 32 KB state); runs of one (sequence, head) leave [dS' | dz'] as a
 // partial in slot h n_seq + b + CTA, and the CTA completing a (sequence, head)
-// combines its partials in slot order.  Eight warps: warp w reads TMEM lanes
-// 32 (w % 4) .. + 31 (tile rows) and owns the 64 columns 64 (w / 4) .. + 63 of
-// its row, one swizzle atom of each tile; the two owners of a row exchange
-// their row sums through TMEM columns 400..407.  Thread 0 issues the copies
+// combines its partials in slot order.  Sixteen warps: warp w reads TMEM
+// lanes 32 (w % 4) .. + 31 (tile rows) and owns the 32 columns 32 (w / 4) ..
+// + 31 of its row (half a swizzle atom); the four owners of a row exchange
+// their row sums through TMEM columns 400..415.  Thread 0 issues the copies
 // and the MMAs.  O' and dq~ share TMEM columns, so (a) of the next tile is
 // issued once every warp has finished epilogue 2.
 //
@@ -58,13 +58,16 @@ constexpr int O_FAIL = O_SLOT + 4;
 constexpr int O_LAST = O_FAIL + 4;
 constexpr int SMEM = O_LAST + 12 + 1024;     // last-arrival flag, c0, count; alignment slack
 constexpr int TMEM_COLS = 512;
-constexpr int C_DS = 128, C_DG = 272, C_X = 400;  // TMEM columns: [dS' | dz'], dgamma, row-sum exchange
+constexpr int C_DS = 128, C_DG = 272, C_X = 400;  // TMEM columns: [dS' | dz'], dgamma, row-sum exchange (16)
 static_assert(SMEM <= 227 * 1024, "shared memory");
 static_assert(QST * STAGE >= QT * (QD + 1) * 4, "the stage memory holds the dgamma reduction");
 static_assert(O_F % 16 == 0, "float4 reads of gamma, centre and z");
 
-constexpr int EW = 8;                 // warps
+constexpr int EW = 16;                // warps
 constexpr int NTH = EW * 32;
+constexpr int NPART = EW / 4;         // owners of a row
+constexpr int CPT = QD / NPART;       // columns per thread (32)
+static_assert(CPT == 32, "a thread holds one 32-column TMEM load");
 
 __device__ __forceinline__ uint32_t swz_off(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
@@ -212,14 +215,14 @@ __global__ void __launch_bounds__(NTH, 1)
 
   const int q = warp & 3, part = warp >> 2;
   const int i = q * 32 + lane;  // tile row = TMEM lane
-  const int f0 = part * 64;     // this thread's columns: atom `part` of each tile
+  const int f0 = part * CPT;    // this thread's columns: half of atom part / 2 of each tile
+  const int c0 = (part & 1) * 4;  // its first 8-column chunk inside that atom
   const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
   {  // dgamma starts at zero
     uint32_t zero[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) zero[j] = 0u;
     tmem_st32(tl + C_DG + f0, zero);
-    tmem_st32(tl + C_DG + f0 + 32, zero);
     tmem_st_wait();
   }
 
@@ -271,7 +274,7 @@ __global__ void __launch_bounds__(NTH, 1)
     const bool has_next = unxt < u1, same = has_next && nxt.seqh == cur.seqh;
     const float2 ri_next = has_next ? rsinv_of(nxt) : make_float2(0.f, 0.f);
     const int s = k % QST, h = cur.h;
-    uint8_t* sq = smem + O_ST + s * STAGE + part * ATOM;  // this thread's atom of each tile
+    uint8_t* sq = smem + O_ST + s * STAGE + (part >> 1) * ATOM;  // the atom holding this thread's columns
     uint8_t* sy = sq + TILE;
     uint8_t* sr = sy + TILE;
     const bool store = i < cur.nrows;
@@ -281,16 +284,15 @@ __global__ void __launch_bounds__(NTH, 1)
     tc_fence_after();
     // pass 1: dr, dgamma, du (into the r tile); sums m = du . u, D1 = du . o', D2 = u . o'.
     float m = 0.f, D1 = 0.f, D2 = 0.f;
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
+    {
       uint32_t o[32], g[32];
-      tmem_ld32_async(tl + f0 + 32 * hh, o);
-      tmem_ld32_async(tl + C_DG + f0 + 32 * hh, g);
+      tmem_ld32_async(tl + f0, o);
+      tmem_ld32_async(tl + C_DG + f0, g);
       tmem_wait32(o);
       tmem_tie32(g);
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
-        const int cc = 4 * hh + ch, f = f0 + 8 * cc;
+        const int cc = c0 + ch, f = f0 + 8 * ch;
         float yv[8], rv[8];
         unpack8(*reinterpret_cast<const uint4*>(sy + swz_off(i, cc)), yv);
         unpack8(*reinterpret_cast<const uint4*>(sr + swz_off(i, cc)), rv);
@@ -322,30 +324,30 @@ __global__ void __launch_bounds__(NTH, 1)
           *reinterpret_cast<uint4*>((bf16*)a.dr + row * a.lddr + (size_t)h * QD + f) =
               make_uint4(drp[0], drp[1], drp[2], drp[3]);
       }
-      tmem_st32(tl + C_DG + f0 + 32 * hh, g);
+      tmem_st32(tl + C_DG + f0, g);
     }
-    // the row's two owners add their sums in a fixed order, through TMEM
+    // the row's four owners add their sums in a fixed order, through TMEM
     tmem_st4(tl + C_X + 4 * part, m, D1, D2, 0.f);
     tmem_st_wait();
     tc_fence_before();
     named_bar(1, EW * 32);
     tc_fence_after();
     {
-      uint32_t xv[8];
-      tmem_ld8(tl + C_X, xv);
-      m = (__uint_as_float(xv[0]) + __uint_as_float(xv[4])) * (1.f / QD);
-      D1 = __uint_as_float(xv[1]) + __uint_as_float(xv[5]);
-      D2 = __uint_as_float(xv[2]) + __uint_as_float(xv[6]);
+      uint32_t xv[16];
+      tmem_ld16(tl + C_X, xv);
+      m = (((__uint_as_float(xv[0]) + __uint_as_float(xv[4])) + __uint_as_float(xv[8])) + __uint_as_float(xv[12])) *
+          (1.f / QD);
+      D1 = ((__uint_as_float(xv[1]) + __uint_as_float(xv[5])) + __uint_as_float(xv[9])) + __uint_as_float(xv[13]);
+      D2 = ((__uint_as_float(xv[2]) + __uint_as_float(xv[6])) + __uint_as_float(xv[10])) + __uint_as_float(xv[14]);
     }
     const float dden = -rs * fmaf(-m, D2, D1) * inv;
     // pass 2: dn = rs (du - u m) / den -> the dy tile
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
+    {
       uint32_t o[32];
-      tmem_ld32(tl + f0 + 32 * hh, o);
+      tmem_ld32(tl + f0, o);
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
-        const int cc = 4 * hh + ch, f = f0 + 8 * cc;
+        const int cc = c0 + ch, f = f0 + 8 * ch;
         float du[8];
         unpack8(*reinterpret_cast<const uint4*>(sr + swz_off(i, cc)), du);
         uint32_t dn[4];
@@ -364,7 +366,7 @@ __global__ void __launch_bounds__(NTH, 1)
       }
     }
     // dden in column 128 of [dn | dden]: the first element of the r tile's
-    // first atom (part 0 consumed that chunk's du above)
+    // first atom (part 0, the owner of that chunk, consumed its du above)
     if (part == 0) *reinterpret_cast<uint4*>(sr + swz_off(i, 0)) = make_uint4(pack_bf16(dden, 0.f), 0u, 0u, 0u);
     tmem_st_wait();
     fence_async_smem();
@@ -376,13 +378,12 @@ __global__ void __launch_bounds__(NTH, 1)
     // epilogue 2: dq = (dq~ + dden z) min(1, phi(q))
     mbar_wait(D_DONE, k & 1, fail);
     tc_fence_after();
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
+    {
       uint32_t o[32];
-      tmem_ld32(tl + f0 + 32 * hh, o);  // dq~
+      tmem_ld32(tl + f0, o);  // dq~
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
-        const int cc = 4 * hh + ch, f = f0 + 8 * cc;
+        const int cc = c0 + ch, f = f0 + 8 * ch;
         float qv[8];
         unpack8(*reinterpret_cast<const uint4*>(sq + swz_off(i, cc)), qv);
         uint32_t dq[4];
@@ -413,21 +414,20 @@ __global__ void __launch_bounds__(NTH, 1)
       const int b = cur.b, p = h * nseq + b;
       {
         float* P = a.partial + (size_t)(p + blockIdx.x) * QD * LD + (size_t)i * LD;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        {
           uint32_t dsv[32];
-          tmem_ld32(tl + C_DS + f0 + 32 * hh, dsv);
+          tmem_ld32(tl + C_DS + f0, dsv);
 #pragma unroll
           for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<float4*>(P + f0 + 32 * hh + j) =
+            *reinterpret_cast<float4*>(P + f0 + j) =
                 make_float4(__uint_as_float(dsv[j]), __uint_as_float(dsv[j + 1]), __uint_as_float(dsv[j + 2]),
                             __uint_as_float(dsv[j + 3]));
         }
         uint32_t zv[8];
         tmem_ld8(tl + C_DS + QD, zv);  // dz' in column 128, then zero padding
-        if (part == 1)
+        if (part == 3)
           *reinterpret_cast<float4*>(P + QD) = make_float4(__uint_as_float(zv[0]), 0.f, 0.f, 0.f);
-        else
+        else if (part == 2)
           *reinterpret_cast<float4*>(P + QD + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
       tc_fence_before();
@@ -478,13 +478,10 @@ __global__ void __launch_bounds__(NTH, 1)
   // dgamma: per-lane sums in TMEM, reduced over the 128 lanes in a fixed order
   float* red = reinterpret_cast<float*>(smem + O_ST);  // [128][129]: the stages are free now
   if (!bad) {
+    uint32_t gv[32];
+    tmem_ld32(tl + C_DG + f0, gv);
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      uint32_t gv[32];
-      tmem_ld32(tl + C_DG + f0 + 32 * hh, gv);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) red[i * (QD + 1) + f0 + 32 * hh + j] = __uint_as_float(gv[j]);
-    }
+    for (int j = 0; j < 32; ++j) red[i * (QD + 1) + f0 + j] = __uint_as_float(gv[j]);
   }
   tc_fence_before();
   __syncthreads();
@@ -494,14 +491,15 @@ __global__ void __launch_bounds__(NTH, 1)
     return;
   }
   float* red2 = red + QT * (QD + 1);
-  {  // two row halves per column, then their sum: a fixed order
+  {  // four row quarters per column, then their sum: a fixed order
     const int f = tid & (QD - 1), qr = tid / QD;
     float v = 0.f;
-    for (int r = qr * (QT / 2); r < (qr + 1) * (QT / 2); ++r) v += red[r * (QD + 1) + f];
+    for (int r = qr * (QT / 4); r < (qr + 1) * (QT / 4); ++r) v += red[r * (QD + 1) + f];
     red2[qr * QD + f] = v;
   }
   __syncthreads();
-  if (tid < QD) a.gamma_part[(size_t)blockIdx.x * QD + tid] = red2[tid] + red2[QD + tid];
+  if (tid < QD)
+    a.gamma_part[(size_t)blockIdx.x * QD + tid] = ((red2[tid] + red2[QD + tid]) + red2[2 * QD + tid]) + red2[3 * QD + tid];
 }
 
 }  // namespace
