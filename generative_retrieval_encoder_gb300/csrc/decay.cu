@@ -16,6 +16,8 @@
 //   L^B_c = sum_{j in c} e^{A_j} g_j phi(k_j) [v_j | 1]^T,   Lambda_c = e^{A_e}
 //   H^F_0 = 0,  H^F_{c+1} = Lambda_c H^F_c + L^F_c        (chunks before c)
 //   H^B_last = 0, H^B_{c-1} = Lambda_c H^B_c + L^B_c       (chunks after c)
+// (phi(K) is formed once per chunk in shared memory; phi(Q) per warp in its
+// fragments.)
 //   num|den_i = sum_{j in c} M_ij g_j (phi(q_i).phi(k_j)) [v_j | 1]
 //             + e^{A_i} phi(q_i)^T H^F_c + e^{A_e - A_i} phi(q_i)^T H^B_c.
 // Three kernels: the chunks' local states (k_decay_states), the two scans per
@@ -280,6 +282,13 @@ __global__ void __launch_bounds__(256, 2) k_decay_out(const DecayArgs a) {
   cp_async_wait<0>();
   __syncthreads();
   if (c.n_in == 0) return;
+  // phi(K) once, in place: every warp reads all the keys
+  for (int i = tid; i < CC * CPR; i += 256) {
+    uint4* p = reinterpret_cast<uint4*>(smem + TBYTES + swz<CPR>(i / CPR, i % CPR));
+    const uint4 w = *p;
+    *p = make_uint4(phi2(w.x), phi2(w.y), phi2(w.z), phi2(w.w));
+  }
+  __syncthreads();
   const float Ae = As[c.n_in - 1];
 
   const int mi = lane >> 3, rr = lane & 7, g8 = lane >> 2, t4 = lane & 3;
@@ -315,7 +324,6 @@ __global__ void __launch_bounds__(256, 2) k_decay_out(const DecayArgs a) {
       for (int np = 0; np < 4; ++np) {
         uint32_t b0, b1, b2, b3;
         ldsm_x4(kb + swz<CPR>(k0 + 16 * np + ((mi >> 1) << 3) + rr, 2 * ks + (mi & 1)), b0, b1, b2, b3);
-        b0 = phi2(b0); b1 = phi2(b1); b2 = phi2(b2); b3 = phi2(b3);
         mma_bf16(s[2 * np], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
         mma_bf16(s[2 * np + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
       }
