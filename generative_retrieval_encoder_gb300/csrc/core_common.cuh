@@ -20,6 +20,35 @@ __device__ __forceinline__ bool arrive_last(int* counter, int count) {
   return last;
 }
 
+// Dot products of length dh spread over the CTA: `per` threads (a power of two,
+// at most 32) share one, each summing every per-th term, and a butterfly of
+// shuffles adds their sums (the same value in every lane of the group, since
+// fp32 addition commutes).  Rows are visited in passes of blockDim / per; every
+// thread runs every pass, so the shuffles see whole warps (blockDim is a
+// multiple of 32).  term(r, t) is the t-th term of row r; done(r, sum) is called
+// by the group's first thread.
+__device__ __forceinline__ int dot_split(int dh) {
+  int per = 32;
+  while (per > 1 && per * dh > (int)blockDim.x) per >>= 1;
+  return per;
+}
+template <class Term, class Done>
+__device__ __forceinline__ void rows_dot(int rows, int dh, Term term, Done done) {
+  const int per = dot_split(dh), rpp = blockDim.x / per;
+  const int j = threadIdx.x % per;
+  for (int r0 = 0; r0 < rows; r0 += rpp) {
+    const int r = r0 + threadIdx.x / per;
+    const bool on = r < rows && (int)threadIdx.x < rpp * per;
+    float acc = 0.f;
+    if (on) {
+#pragma unroll 8
+      for (int t = j; t < dh; t += per) acc += term(r, t);
+    }
+    for (int o = per >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (on && j == 0) done(r, acc);
+  }
+}
+
 // state[seqh] = sum over the sequence's chunks c = 0 .. count-1, in that
 // order, of scale_c * partial[(first + c) * H + h].  scale_c = 1, or for
 // softmax logits exp(m_c - m) with m the largest chunk maximum (the softmax
@@ -62,44 +91,47 @@ __device__ inline void combine_state(const float* partial, const float* partial_
   }
   const float4* P = reinterpret_cast<const float4*>(partial);
   float4* S = reinterpret_cast<float4*>(state + (size_t)seqh * n);
-  for (int i = threadIdx.x; i < n / 4; i += blockDim.x) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int c = 0;
-    for (; c + 4 <= count; c += 4) {
-      float4 p[4];
-      float sc[4];
+  // Each thread sums PER float4s at a time, so that a partial's PER loads are
+  // in flight together (the partials live in L2, whose latency the sum would
+  // otherwise pay once per float4 and partial).
+  constexpr int PER = 5;
+  const int n4 = n / 4;
+  for (int i0 = threadIdx.x; i0 < n4; i0 += PER * blockDim.x) {
+    float4 acc[PER];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        p[u] = __ldcg(P + ((size_t)(first + c + u) * H + h) * (n / 4) + i);
-        sc[u] = 1.f;
-        if (logits) {
-          const float mc = __ldcg(partial_m + (size_t)(first + c + u) * H + h);
-          sc[u] = (any && mc > -INFINITY) ? __expf(mc - m) : 0.f;
-        }
-      }
+    for (int u = 0; u < PER; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < count; ++c) {
+      const float4* Pc = P + ((size_t)(first + c) * H + h) * n4;
+      float4 p[PER];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        acc.x += sc[u] * p[u].x; acc.y += sc[u] * p[u].y;
-        acc.z += sc[u] * p[u].z; acc.w += sc[u] * p[u].w;
+      for (int u = 0; u < PER; ++u) {
+        const int i = i0 + u * blockDim.x;
+        p[u] = i < n4 ? __ldcg(Pc + i) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-    }
-    for (; c < count; ++c) {
-      const float4 p = __ldcg(P + ((size_t)(first + c) * H + h) * (n / 4) + i);
       float sc = 1.f;
       if (logits) {
         const float mc = __ldcg(partial_m + (size_t)(first + c) * H + h);
         sc = (any && mc > -INFINITY) ? __expf(mc - m) : 0.f;
       }
-      acc.x += sc * p.x; acc.y += sc * p.y; acc.z += sc * p.z; acc.w += sc * p.w;
-    }
-    S[i] = acc;
-    if (sbuf) reinterpret_cast<float4*>(sbuf)[i] = acc;
-    const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int e = (4 * i + u) / LD, f = (4 * i + u) % LD;
-      if (state_bf && !center) state_bf[((size_t)seqh * dh + e) * state_bf_ld(dh) + f] = __float2bfloat16_rn(v4[u]);
-      if (pub_state && f <= dh) pub_state[((size_t)seqh * dh + e) * (dh + 1) + f] = v4[u];
+      for (int u = 0; u < PER; ++u) {
+        acc[u].x += sc * p[u].x; acc[u].y += sc * p[u].y;
+        acc[u].z += sc * p[u].z; acc[u].w += sc * p[u].w;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i >= n4) continue;
+      S[i] = acc[u];
+      if (sbuf) reinterpret_cast<float4*>(sbuf)[i] = acc[u];
+      const float v4[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int e = (4 * i + w) / LD, f = (4 * i + w) % LD;
+        if (state_bf && !center) state_bf[((size_t)seqh * dh + e) * state_bf_ld(dh) + f] = __float2bfloat16_rn(v4[w]);
+        if (pub_state && f <= dh) pub_state[((size_t)seqh * dh + e) * (dh + 1) + f] = v4[w];
+      }
     }
   }
   // the combined state as later passes read it: the staged copy, else the global one
@@ -108,23 +140,25 @@ __device__ inline void combine_state(const float* partial, const float* partial_
     float* St = state + (size_t)seqh * n;
     __syncthreads();  // this CTA's state writes are visible to the whole CTA
     const float* c = fwd_center + (size_t)seqh * dh;
-    for (int e = threadIdx.x; e < dh; e += blockDim.x) {
-      float acc = Sr[e * LD + dh];
-      for (int f = 0; f < dh; ++f) acc -= __bfloat162float(__float2bfloat16_rn(Sr[e * LD + f])) * __ldg(c + f);
-      St[e * LD + dh] = acc;
-      if (state_bf) state_bf[((size_t)seqh * dh + e) * state_bf_ld(dh) + dh] = __float2bfloat16_rn(acc);
-    }
+    rows_dot(
+        dh, dh, [&](int e, int f) { return __bfloat162float(__float2bfloat16_rn(Sr[e * LD + f])) * __ldg(c + f); },
+        [&](int e, float dot) {
+          const float acc = Sr[e * LD + dh] - dot;
+          St[e * LD + dh] = acc;
+          if (state_bf) state_bf[((size_t)seqh * dh + e) * state_bf_ld(dh) + dh] = __float2bfloat16_rn(acc);
+        });
   }
   if (center) {
-    __shared__ float cbuf[128];
+    __shared__ float cbuf[129];  // column sums of S, then sum_e z_e
     float* St = state + (size_t)seqh * n;
     __syncthreads();  // this CTA's state writes are visible to the whole CTA
-    float Z = 0.f;
-    for (int e = 0; e < dh; ++e) Z += Sr[e * LD + dh];
+    // column f < dh: sum_e S[e][f]; "column" dh: Z = sum_e z_e
+    rows_dot(dh + 1, dh, [&](int f, int e) { return Sr[e * LD + f]; }, [&](int f, float sum) { cbuf[f] = sum; });
+    __syncthreads();
+    const float Z = cbuf[dh];
+    __syncthreads();  // every thread has read Z before cbuf[f] becomes c_f
     for (int f = threadIdx.x; f < dh; f += blockDim.x) {
-      float s = 0.f;
-      for (int e = 0; e < dh; ++e) s += Sr[e * LD + f];
-      const float c = Z > 0.f ? s / Z : 0.f;
+      const float c = Z > 0.f ? cbuf[f] / Z : 0.f;
       cbuf[f] = c;
       center[(size_t)seqh * dh + f] = c;
     }
