@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(NTH, 1)
   }
   pdl_enter();  // the previous kernel's outputs are visible from here on
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align1024(smem_raw);
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (a.err && *a.err) return;

@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   using RG = Ring<CL>;
   constexpr int ST = RG::ST;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align1024(smem_raw);
   const uint32_t sA = smem_u32(smem), sB = sA + ST * A_TILE;
   const uint32_t stg = sA + RG::BYTES;  // epilogue staging of bf16 output boxes
   const uint32_t bars = stg + STG_ALL;

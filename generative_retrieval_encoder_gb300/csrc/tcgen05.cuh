@@ -210,6 +210,14 @@ __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
 }
+// The first 1024-byte boundary at or after the dynamic shared array `raw`
+// (the 128-byte swizzle atoms of TMA and the MMA descriptors repeat every
+// 1024 bytes).  Offsetting the array itself, rather than rounding an integer
+// address, keeps the pointer in the shared window for the compiler, so that
+// accesses through it stay 32-bit shared loads and stores.
+__device__ __forceinline__ uint8_t* smem_align1024(uint8_t* raw) {
+  return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
 // Generic-proxy shared-memory writes -> visible to the async proxy (MMA operands).
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 // Named barrier over `nthreads` threads (whole warps).
