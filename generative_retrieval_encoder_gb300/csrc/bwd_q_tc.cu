@@ -23,13 +23,15 @@
 // fixed order) and forms dz''; the CTA then loads the next segment's S' and
 // goes on.  dgamma accumulates over the whole range.
 //
-// Eight warps: warp w reads TMEM lanes 32 (w % 4) .. + 31 (tile rows) and the
-// columns 32 (w / 4) .. + 31.  Thread 0 also issues the TMA loads and the MMAs,
-// at the points where the tile's data is complete anyway: (d), (e) and (a) of
-// the next tile once every warp has written dn (so (a) of the next tile runs
-// under epilogue 2 of this one, unless a segment ends here), the load of the
-// tile after next once every warp is done with this one.  Without a separate
-// control warp, two CTAs per SM keep 128 registers a thread.  Operand tiles are
+// Nine warps.  Warps 0-7 compute: warp w reads TMEM lanes 32 (w % 4) .. + 31
+// (tile rows) and the columns 32 (w / 4) .. + 31, in rounds of 16 columns (18
+// warps an SM leave 96 registers a thread).  Warp 8 only issues: the TMA
+// copies (two stages ahead) and the MMAs, each group once its inputs are
+// complete: (d), (a) of the next tile and (e) once every compute warp has
+// written dn, so (a) of the next tile runs under epilogue 2 of this one.  A
+// compute warp that issued them would reach the row-sum exchange of the next
+// tile last, every tile (an MMA issue takes 100+ cycles under this load), and
+// hold up the other seven there.  Operand tiles are
 // [128 rows][64 bf16] in the 128-byte swizzle shared by TMA and the MMA
 // descriptors; the epilogue writes dn and dden into the dy and r tiles of the
 // same stage (each thread owns its row's columns), which then serve as the A
@@ -58,7 +60,7 @@ constexpr int BLD = state_bf_ld(QD);  // bf16 state row
 constexpr int O_S = 0;                       // S' [e][f] (8 KB)
 constexpr int O_ST = O_S + 8192;             // stages (1024-aligned)
 constexpr int O_BAR = O_ST + QST * STAGE;
-constexpr int NBAR = 2 * QST + 4;            // full, empty, a_done, dn_ready, d_done, seg
+constexpr int NBAR = 2 * QST + 4;            // full, empty, a_done, dn_ready, d_done, s_ready
 constexpr int O_F = O_BAR + 8 * NBAR;        // gamma, centre, z (fp32), row exchange [3][2][128]
 constexpr int O_SLOT = O_F + 4 * (3 * QD + 3 * 2 * QT);
 constexpr int O_FAIL = O_SLOT + 4;
@@ -66,15 +68,16 @@ constexpr int O_LAST = O_FAIL + 4;
 constexpr int SMEM = O_LAST + 12 + 1024;     // last-arrival flag, c0, count; alignment slack
 constexpr int TMEM_COLS = 256;               // O' | dq~ | dS' | dgamma
 static_assert(2 * (SMEM + 1024) <= 233472, "two CTAs per SM");
-static_assert(QST == 2, "the control thread tracks two stages");
+static_assert(QST == 2, "the issuing thread tracks two stages");
 static_assert(QST * STAGE >= (QT + 4) * (QD + 1) * 4, "the stage memory holds the dgamma reduction");
-static_assert(QD / 2 == 32, "a thread holds 32 columns (one 32-column TMEM load)");
 
-constexpr int EW = 8;                 // warps
-constexpr int NTH = EW * 32;
-constexpr int CPT = QD / (EW / 4);    // columns per thread
-constexpr int NC = CPT / 8;           // 8-column chunks per thread
-static_assert(NTH == 4 * QD, "the dgamma sum maps threads to (quarter, column)");
+constexpr int EW = 8;                 // compute warps
+constexpr int NCT = EW * 32;          // compute threads
+constexpr int NTH = NCT + 32;         // + the issuing warp
+constexpr int CPT = QD / (EW / 4);    // columns per thread (32)
+constexpr int RC = 16;                // columns per round: one 16-column TMEM load
+constexpr int NR = CPT / RC;          // rounds
+static_assert(NCT == 4 * QD, "the dgamma sum maps threads to (quarter, column)");
 
 __device__ __forceinline__ uint32_t swz_off(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
@@ -127,10 +130,15 @@ __device__ __forceinline__ int cta_of(int u, int n_units, int grid) {
   return (int)((((long long)u + 1) * grid + n_units - 1) / n_units) - 1;
 }
 
+__device__ __forceinline__ void tmem_wait16(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  tmem_tie16(r);
+}
+
 __global__ void __launch_bounds__(NTH, 2)
     k_bwd_q_tc(const BwdQArgs a, const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmY,
                int roff, int upt, int spt, int n_units) {
-  if (threadIdx.x == 0) {  // the descriptors load while the previous kernel finishes
+  if (threadIdx.x == NCT) {  // the descriptors load while the previous kernel finishes
     tma_prefetch_map(&tmP);
     tma_prefetch_map(&tmY);
   }
@@ -158,12 +166,12 @@ __global__ void __launch_bounds__(NTH, 2)
   volatile int* fail = reinterpret_cast<volatile int*>(smem + O_FAIL);
   volatile int* lastf = reinterpret_cast<volatile int*>(smem + O_LAST);
   const uint32_t bar0 = sbase + O_BAR;
-  const uint32_t A_DONE = bar0 + 8 * (2 * QST), DN_READY = A_DONE + 8, D_DONE = A_DONE + 16, SEG = A_DONE + 24;
+  const uint32_t A_DONE = bar0 + 8 * (2 * QST), DN_READY = A_DONE + 8, D_DONE = A_DONE + 16, S_READY = A_DONE + 24;
   auto FULL = [&](int s) { return bar0 + 8 * s; };
   auto EMPTY = [&](int s) { return bar0 + 8 * (QST + s); };
+  const bool issuer = tid == NCT;  // lane 0 of warp 8
 
-  // ---------------------------------------------------------- thread 0: copies and MMAs
-  const bool leader = tid == 0;
+  // ---------------------------------------------------------- copies (issuer)
   int issued[QST] = {0, 0};  // 1 + index of the last tile loaded into each stage
   int ld_k = 0, ld_u = ucur;  // the next tile to load: its index and unit
   QTile ld_x = cur;
@@ -179,286 +187,328 @@ __global__ void __launch_bounds__(NTH, 2)
     ++ld_k;
     ld_u = next_unit(a, ld_u + 1, u1, upt, spt, ld_x);
   };
-  if (leader) {  // barriers, then the first two tiles' copies before anything else
+  if (issuer) {  // barriers, then the first two tiles' copies before anything else
     for (int s = 0; s < QST; ++s) {
       mbar_init(FULL(s), 1);
-      mbar_init(EMPTY(s), EW + 1);  // (e) commit + one arrival per warp
+      mbar_init(EMPTY(s), EW + 1);  // (e) commit + one arrival per compute warp
     }
     mbar_init(A_DONE, 1);
     mbar_init(DN_READY, EW);
     mbar_init(D_DONE, 1);
-    mbar_init(SEG, 1);
+    mbar_init(S_READY, EW);
     mbar_init_fence();
     *fail = 0;
     load_next();
     if (ld_u < u1) load_next();
   }
-  // S' of (sequence, head) seqh into its swizzled rows e; fp32 centre and z.
+  // S' of (sequence, head) seqh into its swizzled rows e; fp32 centre and z (compute threads).
   auto load_state = [&](int seqh) {
     const bf16* sbf = a.state_bf + (size_t)seqh * QD * BLD;
-    for (int i = tid; i < QD * 8; i += NTH) {
+    for (int i = tid; i < QD * 8; i += NCT) {
       const int e = i >> 3, c = i & 7;
       *reinterpret_cast<uint4*>(smem + O_S + swz_off(e, c)) = *reinterpret_cast<const uint4*>(sbf + e * BLD + c * 8);
     }
-    for (int f = tid; f < QD; f += NTH) {
+    for (int f = tid; f < QD; f += NCT) {
       cen[f] = a.center ? a.center[(size_t)seqh * QD + f] : 0.f;
       zf[f] = __bfloat162float(sbf[f * BLD + QD]);
     }
     fence_async_smem();
   };
-  for (int f = tid; f < QD; f += NTH) gam[f] = a.rms_w ? __bfloat162float(((const bf16*)a.rms_w)[f]) : 1.f;
-  load_state(cur.seqh);
+  if (tid < NCT) {
+    for (int f = tid; f < QD; f += NCT) gam[f] = a.rms_w ? __bfloat162float(((const bf16*)a.rms_w)[f]) : 1.f;
+    load_state(cur.seqh);
+  }
   if (warp == 0) tmem_alloc(smem_u32(slot), TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *slot;
-
   const uint32_t sS = sbase + O_S;
-  // (a): K = e.  A = phi(Q) K-major (+32 B per 16 e); B = S' N-major (16 e-rows = 2048 B).
-  auto issue_a = [&](int k) {
-    if (!mbar_wait(FULL(k % QST), (k / QST) & 1, fail)) return;
-    tc_fence_after();
-    const uint32_t sq = sbase + O_ST + (k % QST) * STAGE;
-    const uint32_t id_a = idesc_bf16(QT, QD, false, true);
-#pragma unroll
-    for (int kk = 0; kk < QD / 16; ++kk)
-      tc_mma(tmem, sdesc(sq + 32 * kk, 16, 1024), sdesc(sS + 2048 * kk, 8192, 1024), id_a, kk > 0);
-    tc_commit(A_DONE);
-  };
-  // (d), (e) of tile k and, if the next tile is in the same segment, its (a),
-  // once every warp has written dn and dden.  first: k opens its segment.
-  auto issue_de = [&](int k, bool next_same, bool first) {
-    const int s = k % QST;
-    const uint32_t sq = sbase + O_ST + s * STAGE, sy = sq + TILE;
-    if (!mbar_wait(DN_READY, k & 1, fail)) return;
-    tc_fence_after();
-    // (d): K = f.  A = dn (the dy tile) K-major; B = S' K-major (rows e).
-    const uint32_t id_d = idesc_bf16(QT, QD, false, false), id_e = idesc_bf16(QT, QD, true, true);
-#pragma unroll
-    for (int kk = 0; kk < QD / 16; ++kk)
-      tc_mma(tmem + 64, sdesc(sy + 32 * kk, 16, 1024), sdesc(sS + 32 * kk, 16, 1024), id_d, kk > 0);
-    tc_commit(D_DONE);
-    // (a) of the next tile before (e): epilogue 2 and the next epilogue 1 wait
-    // on (d) and (a); (e) only gates the reuse of this stage.
-    if (next_same) issue_a(k + 1);
-    // (e): K = rows.  A = [dn | dden ...] M-major, its two 64-wide halves the
-    // dy and r tiles (one tile apart); B = phi(Q) N-major.
-#pragma unroll
-    for (int kk = 0; kk < QT / 16; ++kk)
-      tc_mma(tmem + 128, sdesc(sy + 2048 * kk, TILE, 1024), sdesc(sq + 2048 * kk, 8192, 1024), id_e,
-             (first && kk == 0) ? 0u : 1u);
-    tc_commit(EMPTY(s));
-  };
-  if (leader) issue_a(0);
 
-  const int q = warp & 3, part = warp >> 2;
-  const int i = q * 32 + lane;  // tile row = TMEM lane
-  const int f0 = part * CPT;
-  const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
-  // rs and 1/den of this thread's row of a tile (0 on rows outside the sequence: u = dn = 0 there)
-  auto rsinv_of = [&](const QTile& x) {
-    return i < x.nval ? __ldg(reinterpret_cast<const float2*>(a.rsinv + 2 * ((x.rb + i) * H + x.h)))
-                      : make_float2(0.f, 0.f);
-  };
-  float2 ri_cur = rsinv_of(cur);
-  int k = 0, kseg = 0, ns = 0;  // tile, first tile of the current segment, segments finished
-  while (true) {
-    QTile nxt;
-    const int unxt = next_unit(a, ucur + 1, u1, upt, spt, nxt);
-    const bool has_next = unxt < u1, same = has_next && nxt.seqh == cur.seqh;
-    const float2 ri_next = has_next ? rsinv_of(nxt) : make_float2(0.f, 0.f);
-    const int s = k % QST, h = cur.h;
-    uint8_t* sq = smem + O_ST + s * STAGE;
-    uint8_t* sy = sq + TILE;
-    uint8_t* sr = sy + TILE;
-    const bool store = i < cur.nrows;
-    const size_t row = cur.rb + i;
-    const float rs = ri_cur.x, inv = ri_cur.y;
-    mbar_wait(A_DONE, k & 1, fail);
-    tc_fence_after();
-    // pass 1: dr, dgamma, du (into the r tile); sums m = du . u, D1 = du . o', D2 = u . o'.
-    float m = 0.f, D1 = 0.f, D2 = 0.f;
-    uint32_t o[CPT];
-    {
-      uint32_t g[CPT];
-      tmem_ld32_async(tl + f0, o);
-      if (k > 0) {  // O' and the running dgamma under one wait
-        tmem_ld32_async(tl + 192 + f0, g);
-        tmem_wait32(o);
-        tmem_tie32(g);
-      } else {
-        tmem_wait32(o);
+  if (warp == EW) {
+    // ======================================================== issuing warp
+    if (lane == 0) {
+      // (a): K = e.  A = phi(Q) K-major (+32 B per 16 e); B = S' N-major (16 e-rows = 2048 B).
+      auto issue_a = [&](int k) {
+        if (!mbar_wait(FULL(k % QST), (k / QST) & 1, fail)) return;
+        tc_fence_after();
+        const uint32_t sq = sbase + O_ST + (k % QST) * STAGE;
+        const uint32_t id_a = idesc_bf16(QT, QD, false, true);
 #pragma unroll
-        for (int j = 0; j < CPT; ++j) g[j] = 0u;
-      }
-#pragma unroll
-      for (int ch = 0; ch < NC; ++ch) {
-        const int f = f0 + 8 * ch, cc = f >> 3;
-        float yv[8], rv[8];
-        unpack8(*reinterpret_cast<const uint4*>(sy + swz_off(i, cc)), yv);
-        unpack8(*reinterpret_cast<const uint4*>(sr + swz_off(i, cc)), rv);
-        uint32_t dup[4], drp[4];
-#pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-          float du2[2], dr2[2];
-#pragma unroll
-          for (int w = 0; w < 2; ++w) {
-            const int jj = j + w, kk = 8 * ch + jj;
-            const float op = __uint_as_float(o[kk]) * inv;  // centred o'
-            const float u = (op + cen[f + jj]) * rs;
-            const float r = rv[jj], dy = yv[jj];
-            const float sg = sigmoid_fast(r);
-            const float av = r * sg;
-            const float dyg = dy * gam[f + jj];
-            du2[w] = dyg * av;
-            g[kk] = __float_as_uint(fmaf(dy * av, u, __uint_as_float(g[kk])));
-            dr2[w] = dyg * u * sg * fmaf(r, 1.f - sg, 1.f);
-            m = fmaf(du2[w], u, m);
-            D1 = fmaf(du2[w], op, D1);
-            D2 = fmaf(u, op, D2);
+        for (int kk = 0; kk < QD / 16; ++kk)
+          tc_mma(tmem, sdesc(sq + 32 * kk, 16, 1024), sdesc(sS + 2048 * kk, 8192, 1024), id_a, kk > 0);
+        tc_commit(A_DONE);
+      };
+      QTile x = cur;
+      int ux = ucur, k = 0, kseg = 0, nsr = 0;  // tile, first tile of its segment, S_READY phases seen
+      while (true) {
+        QTile nx;
+        const int unx = next_unit(a, ux + 1, u1, upt, spt, nx);
+        const bool has_next = unx < u1, same = has_next && nx.seqh == x.seqh;
+        const int s = k % QST;
+        if (k == kseg) {  // a segment's first tile: (a) once its S' is in shared memory
+          if (k > 0) {
+            mbar_wait(S_READY, nsr & 1, fail);
+            ++nsr;
           }
-          dup[j / 2] = pack_bf16(du2[0], du2[1]);
-          drp[j / 2] = pack_bf16(dr2[0], dr2[1]);
+          issue_a(k);
         }
-        *reinterpret_cast<uint4*>(sr + swz_off(i, cc)) = make_uint4(dup[0], dup[1], dup[2], dup[3]);
-        if (store)
-          *reinterpret_cast<uint4*>((bf16*)a.dr + row * a.lddr + (size_t)h * QD + f) =
-              make_uint4(drp[0], drp[1], drp[2], drp[3]);
-      }
-      tmem_st32(tl + 192 + f0, g);
-    }
-    // the row's two column ranges, added in a fixed order
-    xch[(0 + part) * QT + i] = m;
-    xch[(2 + part) * QT + i] = D1;
-    xch[(4 + part) * QT + i] = D2;
-    named_bar(1, EW * 32);
-    m = xch[0 * QT + i] + xch[1 * QT + i];
-    D1 = xch[2 * QT + i] + xch[3 * QT + i];
-    D2 = xch[4 * QT + i] + xch[5 * QT + i];
-    m *= 1.f / QD;
-    const float dden = -rs * fmaf(-m, D2, D1) * inv;
-    // pass 2: dn = rs (du - u m) / den -> the dy tile
-    tmem_ld32(tl + f0, o);  // O' again: held through pass 1's exchange it would spill
+        // (d), (a) of the next tile, (e) once every compute warp has written dn and dden
+        if (mbar_wait(DN_READY, k & 1, fail)) {
+          tc_fence_after();
+          const uint32_t sq = sbase + O_ST + s * STAGE, sy = sq + TILE;
+          // (d): K = f.  A = dn (the dy tile) K-major; B = S' K-major (rows e).
+          const uint32_t id_d = idesc_bf16(QT, QD, false, false), id_e = idesc_bf16(QT, QD, true, true);
 #pragma unroll
-    for (int ch = 0; ch < NC; ++ch) {
-      const int f = f0 + 8 * ch, cc = f >> 3;
-      float du[8];
-      unpack8(*reinterpret_cast<const uint4*>(sr + swz_off(i, cc)), du);
-      uint32_t dn[4];
+          for (int kk = 0; kk < QD / 16; ++kk)
+            tc_mma(tmem + 64, sdesc(sy + 32 * kk, 16, 1024), sdesc(sS + 32 * kk, 16, 1024), id_d, kk > 0);
+          tc_commit(D_DONE);
+          // (a) of the next tile before (e): epilogue 2 and the next pass 1 wait
+          // on (d) and (a); (e) only gates the reuse of this stage.
+          if (same) issue_a(k + 1);
+          // (e): K = rows.  A = [dn | dden ...] M-major, its two 64-wide halves the
+          // dy and r tiles (one tile apart); B = phi(Q) N-major.
 #pragma unroll
-      for (int j = 0; j < 8; j += 2) {
-        float d2[2];
-#pragma unroll
-        for (int w = 0; w < 2; ++w) {
-          const int jj = j + w;
-          const float u = fmaf(__uint_as_float(o[8 * ch + jj]), inv, cen[f + jj]) * rs;
-          d2[w] = rs * fmaf(-u, m, du[jj]) * inv;
+          for (int kk = 0; kk < QT / 16; ++kk)
+            tc_mma(tmem + 128, sdesc(sy + 2048 * kk, TILE, 1024), sdesc(sq + 2048 * kk, 8192, 1024), id_e,
+                   (k == kseg && kk == 0) ? 0u : 1u);
+          tc_commit(EMPTY(s));
         }
-        dn[j / 2] = pack_bf16(d2[0], d2[1]);
+        // the tile after next into this stage once it is free
+        if (ld_k == k + QST && ld_u < u1 && mbar_wait(EMPTY(s), (k / QST) & 1, fail)) load_next();
+        if (!has_next) break;
+        if (!same) kseg = k + 1;
+        x = nx;
+        ux = unx;
+        ++k;
       }
-      *reinterpret_cast<uint4*>(sy + swz_off(i, cc)) = make_uint4(dn[0], dn[1], dn[2], dn[3]);
+      if (*fail)  // let the copies still in flight land
+        for (int s = 0; s < QST; ++s)
+          if (issued[s] > 0)
+            for (uint32_t it = 0; it < kPollLimit && !mbar_try_wait(FULL(s), (uint32_t)((issued[s] - 1) / QST) & 1);
+                 ++it) {
+            }
     }
-    // dden in column 64 of [dn | dden] (first element of the r tile's row);
-    // that chunk's du was consumed above by this row's first column range.
-    if (part == 0) *reinterpret_cast<uint4*>(sr + swz_off(i, 0)) = make_uint4(pack_bf16(dden, 0.f), 0u, 0u, 0u);
-    tmem_st_wait();
-    fence_async_smem();
-    tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(DN_READY);
-    if (leader) issue_de(k, same, k == kseg);
-    __syncwarp();
-    // epilogue 2: dq = (dq~ + dden z) min(1, phi(q))
-    mbar_wait(D_DONE, k & 1, fail);
-    tc_fence_after();
-    tmem_ld32(tl + 64 + f0, o);  // dq~ (waits)
-#pragma unroll
-    for (int ch = 0; ch < NC; ++ch) {
-      const int f = f0 + 8 * ch, cc = f >> 3;
-      float qv[8];
-      unpack8(*reinterpret_cast<const uint4*>(sq + swz_off(i, cc)), qv);
-      uint32_t dq[4];
-#pragma unroll
-      for (int j = 0; j < 8; j += 2)
-        dq[j / 2] = pack_bf16(fmaf(dden, zf[f + j], __uint_as_float(o[8 * ch + j])) * fminf(1.f, qv[j]),
-                              fmaf(dden, zf[f + j + 1], __uint_as_float(o[8 * ch + j + 1])) * fminf(1.f, qv[j + 1]));
-      if (store)
-        *reinterpret_cast<uint4*>((bf16*)a.dq + row * a.lddq + (size_t)h * QD + f) = make_uint4(dq[0], dq[1], dq[2], dq[3]);
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(EMPTY(s));
-    if (leader && ld_k == k + QST && ld_u < u1 && mbar_wait(EMPTY(s), (k / QST) & 1, fail)) load_next();
-    __syncwarp();
-    if (!same) {
-      // The segment ends with tile k.  Once SEG completes, every MMA issued so
-      // far has finished: [dS' | dz'] (TMEM lane f = column f of the state,
-      // column 128 + e = row e) leaves as this CTA's partial of the pair.
-      if (leader) tc_commit(SEG);
-      mbar_wait(SEG, ns & 1, fail);
+  } else {
+    // ======================================================== compute warps
+    const int q = warp & 3, part = warp >> 2;
+    const int i = q * 32 + lane;  // tile row = TMEM lane
+    const int f0 = part * CPT;
+    const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
+    // rs and 1/den of this thread's row of a tile (0 on rows outside the sequence: u = dn = 0 there)
+    auto rsinv_of = [&](const QTile& x) {
+      return i < x.nval ? __ldg(reinterpret_cast<const float2*>(a.rsinv + 2 * ((x.rb + i) * H + x.h)))
+                        : make_float2(0.f, 0.f);
+    };
+    float2 ri_cur = rsinv_of(cur);
+    int k = 0;
+    while (true) {
+      QTile nxt;
+      const int unxt = next_unit(a, ucur + 1, u1, upt, spt, nxt);
+      const bool has_next = unxt < u1, same = has_next && nxt.seqh == cur.seqh;
+      const float2 ri_next = has_next ? rsinv_of(nxt) : make_float2(0.f, 0.f);
+      const int s = k % QST, h = cur.h;
+      uint8_t* sq = smem + O_ST + s * STAGE;
+      uint8_t* sy = sq + TILE;
+      uint8_t* sr = sy + TILE;
+      const bool store = i < cur.nrows;
+      const size_t row = cur.rb + i;
+      const float rs = ri_cur.x, inv = ri_cur.y;
+      mbar_wait(A_DONE, k & 1, fail);
       tc_fence_after();
-      const int b = cur.b, p = h * nseq + b;
-      {
-        float* P = a.partial + (size_t)(p + blockIdx.x) * QD * LD;
-        uint32_t dsv[CPT];
-        tmem_ld32(tl + 128 + f0, dsv);
-        if (i < LD)
+      // pass 1 in rounds of 16 columns: dr, dgamma, du (into the r tile);
+      // sums m = du . u, D1 = du . o', D2 = u . o'.
+      float m = 0.f, D1 = 0.f, D2 = 0.f;
 #pragma unroll
-          for (int e = 0; e < CPT; ++e) P[(size_t)(f0 + e) * LD + i] = i <= QD ? __uint_as_float(dsv[e]) : 0.f;
+      for (int rd = 0; rd < NR; ++rd) {
+        const int fr = f0 + RC * rd;
+        uint32_t o[RC], g[RC];
+        tmem_ld16_async(tl + fr, o);
+        if (k > 0) {
+          tmem_ld16_async(tl + 192 + fr, g);
+          tmem_wait16(o);
+          tmem_tie16(g);
+        } else {
+          tmem_wait16(o);
+#pragma unroll
+          for (int j = 0; j < RC; ++j) g[j] = 0u;
+        }
+#pragma unroll
+        for (int ch = 0; ch < RC / 8; ++ch) {
+          const int f = fr + 8 * ch, cc = f >> 3;
+          float yv[8], rv[8];
+          unpack8(*reinterpret_cast<const uint4*>(sy + swz_off(i, cc)), yv);
+          unpack8(*reinterpret_cast<const uint4*>(sr + swz_off(i, cc)), rv);
+          uint32_t dup[4], drp[4];
+#pragma unroll
+          for (int j = 0; j < 8; j += 2) {
+            float du2[2], dr2[2];
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+              const int jj = j + w, kk = 8 * ch + jj;
+              const float op = __uint_as_float(o[kk]) * inv;  // centred o'
+              const float u = (op + cen[f + jj]) * rs;
+              const float r = rv[jj], dy = yv[jj];
+              const float sg = sigmoid_fast(r);
+              const float av = r * sg;
+              const float dyg = dy * gam[f + jj];
+              du2[w] = dyg * av;
+              g[kk] = __float_as_uint(fmaf(dy * av, u, __uint_as_float(g[kk])));
+              dr2[w] = dyg * u * sg * fmaf(r, 1.f - sg, 1.f);
+              m = fmaf(du2[w], u, m);
+              D1 = fmaf(du2[w], op, D1);
+              D2 = fmaf(u, op, D2);
+            }
+            dup[j / 2] = pack_bf16(du2[0], du2[1]);
+            drp[j / 2] = pack_bf16(dr2[0], dr2[1]);
+          }
+          *reinterpret_cast<uint4*>(sr + swz_off(i, cc)) = make_uint4(dup[0], dup[1], dup[2], dup[3]);
+          if (store)
+            *reinterpret_cast<uint4*>((bf16*)a.dr + row * a.lddr + (size_t)h * QD + f) =
+                make_uint4(drp[0], drp[1], drp[2], drp[3]);
+        }
+        tmem_st16(tl + 192 + fr, g);
+      }
+      // the row's two column ranges, added in a fixed order
+      xch[(0 + part) * QT + i] = m;
+      xch[(2 + part) * QT + i] = D1;
+      xch[(4 + part) * QT + i] = D2;
+      named_bar(1, NCT);
+      m = xch[0 * QT + i] + xch[1 * QT + i];
+      D1 = xch[2 * QT + i] + xch[3 * QT + i];
+      D2 = xch[4 * QT + i] + xch[5 * QT + i];
+      m *= 1.f / QD;
+      const float dden = -rs * fmaf(-m, D2, D1) * inv;
+      // pass 2: dn = rs (du - u m) / den -> the dy tile
+#pragma unroll
+      for (int rd = 0; rd < NR; ++rd) {
+        const int fr = f0 + RC * rd;
+        uint32_t o[RC];
+        tmem_ld16(tl + fr, o);  // O' again
+#pragma unroll
+        for (int ch = 0; ch < RC / 8; ++ch) {
+          const int f = fr + 8 * ch, cc = f >> 3;
+          float du[8];
+          unpack8(*reinterpret_cast<const uint4*>(sr + swz_off(i, cc)), du);
+          uint32_t dn[4];
+#pragma unroll
+          for (int j = 0; j < 8; j += 2) {
+            float d2[2];
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+              const int jj = j + w;
+              const float u = fmaf(__uint_as_float(o[8 * ch + jj]), inv, cen[f + jj]) * rs;
+              d2[w] = rs * fmaf(-u, m, du[jj]) * inv;
+            }
+            dn[j / 2] = pack_bf16(d2[0], d2[1]);
+          }
+          *reinterpret_cast<uint4*>(sy + swz_off(i, cc)) = make_uint4(dn[0], dn[1], dn[2], dn[3]);
+        }
+      }
+      // dden in column 64 of [dn | dden] (first element of the r tile's row);
+      // that chunk's du was consumed above by this row's first column range.
+      if (part == 0) *reinterpret_cast<uint4*>(sr + swz_off(i, 0)) = make_uint4(pack_bf16(dden, 0.f), 0u, 0u, 0u);
+      tmem_st_wait();
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(DN_READY);
+      // epilogue 2: dq = (dq~ + dden z) min(1, phi(q))
+      mbar_wait(D_DONE, k & 1, fail);
+      tc_fence_after();
+#pragma unroll
+      for (int rd = 0; rd < NR; ++rd) {
+        const int fr = f0 + RC * rd;
+        uint32_t o[RC];
+        tmem_ld16(tl + 64 + fr, o);  // dq~
+#pragma unroll
+        for (int ch = 0; ch < RC / 8; ++ch) {
+          const int f = fr + 8 * ch, cc = f >> 3;
+          float qv[8];
+          unpack8(*reinterpret_cast<const uint4*>(sq + swz_off(i, cc)), qv);
+          uint32_t dq[4];
+#pragma unroll
+          for (int j = 0; j < 8; j += 2)
+            dq[j / 2] = pack_bf16(fmaf(dden, zf[f + j], __uint_as_float(o[8 * ch + j])) * fminf(1.f, qv[j]),
+                                  fmaf(dden, zf[f + j + 1], __uint_as_float(o[8 * ch + j + 1])) * fminf(1.f, qv[j + 1]));
+          if (store)
+            *reinterpret_cast<uint4*>((bf16*)a.dq + row * a.lddq + (size_t)h * QD + f) =
+                make_uint4(dq[0], dq[1], dq[2], dq[3]);
+        }
       }
       tc_fence_before();
-      __threadfence();
-      __syncthreads();
-      if (tid == 0) {  // the CTAs holding units of (b, h): c0 .. c0 + count - 1
-        int first, cnt;
-        seq_tiles(a.seq, a.tiles, b, first, cnt);
-        const int U0 = h * upt + spt * first;
-        int U1 = U0 + spt * cnt - 1;  // the pair's last unit with rows
-        while (U1 > U0 && qtile_at(a, U1, upt, spt).seqh < 0) --U1;
-        const int c0 = cta_of(U0, n_units, G), count = cta_of(U1, n_units, G) - c0 + 1;
-        const bool last = atomicAdd(a.counters + (size_t)b * H + h, 1) == count - 1;
-        lastf[0] = (last && !*fail) ? 1 : 0;
-        lastf[1] = c0;
-        lastf[2] = count;
-      }
-      __syncthreads();
-      if (lastf[0]) {  // this partial completes (b, h): [dS | dz''] in slot order
+      __syncwarp();
+      if (lane == 0) mbar_arrive(EMPTY(s));
+      if (!same) {
+        // The segment ends with tile k.  Once its stage's EMPTY phase completes,
+        // every compute warp is past epilogue 2 and (e), the segment's last MMA,
+        // has finished: [dS' | dz'] (TMEM lane f = column f of the state, column
+        // 128 + e = row e) leaves as this CTA's partial of the pair.
+        mbar_wait(EMPTY(s), (k / QST) & 1, fail);
+        tc_fence_after();
+        const int b = cur.b, p = h * nseq + b;
+        {
+          float* P = a.partial + (size_t)(p + blockIdx.x) * QD * LD;
+#pragma unroll
+          for (int rd = 0; rd < NR; ++rd) {
+            uint32_t dsv[RC];
+            tmem_ld16(tl + 128 + f0 + RC * rd, dsv);
+            if (i < LD)
+#pragma unroll
+              for (int e = 0; e < RC; ++e)
+                P[(size_t)(f0 + RC * rd + e) * LD + i] = i <= QD ? __uint_as_float(dsv[e]) : 0.f;
+          }
+        }
+        tc_fence_before();
         __threadfence();
-        combine_state(a.partial, nullptr, p + lastf[1], lastf[2], 1, 0, QD, cur.seqh, false, a.dstate,
-                      a.dstate_bf, nullptr, nullptr, nullptr, a.center, nullptr);
-      }
-      ++ns;
-      if (!has_next) break;
-      load_state(nxt.seqh);  // every thread is done with tile k (the barrier above)
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-      if (leader) issue_a(k + 1);
-      kseg = k + 1;
-    }
-    cur = nxt;
-    ucur = unxt;
-    ri_cur = ri_next;
-    ++k;
-  }
-  if (leader && *fail)  // let the copies still in flight land
-    for (int s = 0; s < QST; ++s)
-      if (issued[s] > 0)
-        for (uint32_t it = 0; it < kPollLimit && !mbar_try_wait(FULL(s), (uint32_t)((issued[s] - 1) / QST) & 1);
-             ++it) {
+        named_bar(1, NCT);
+        if (tid == 0) {  // the CTAs holding units of (b, h): c0 .. c0 + count - 1
+          int first, cnt;
+          seq_tiles(a.seq, a.tiles, b, first, cnt);
+          const int U0 = h * upt + spt * first;
+          int U1 = U0 + spt * cnt - 1;  // the pair's last unit with rows
+          while (U1 > U0 && qtile_at(a, U1, upt, spt).seqh < 0) --U1;
+          const int c0 = cta_of(U0, n_units, G), count = cta_of(U1, n_units, G) - c0 + 1;
+          const bool last = atomicAdd(a.counters + (size_t)b * H + h, 1) == count - 1;
+          lastf[0] = (last && !*fail) ? 1 : 0;
+          lastf[1] = c0;
+          lastf[2] = count;
         }
-  __syncwarp();  // single-lane roles rejoin their warps: the CTA barrier below is warp-aligned
+        named_bar(1, NCT);
+        if (lastf[0]) {  // this partial completes (b, h): [dS | dz''] in slot order
+          __threadfence();
+          combine_state(a.partial, nullptr, p + lastf[1], lastf[2], 1, 0, QD, cur.seqh, false, a.dstate,
+                        a.dstate_bf, nullptr, nullptr, nullptr, a.center, nullptr, NCT, 1);
+        }
+        if (!has_next) break;
+        named_bar(1, NCT);  // every compute thread has read lastf
+        load_state(nxt.seqh);
+        tc_fence_before();
+        named_bar(1, NCT);
+        if (lane == 0) mbar_arrive(S_READY);  // the issuing warp may start (a) of the new segment
+      }
+      cur = nxt;
+      ucur = unxt;
+      ri_cur = ri_next;
+      ++k;
+    }
+    __syncwarp();
+  }
   __syncthreads();
   const bool bad = *fail != 0;
 
   // dgamma: per-lane sums in TMEM, reduced over the 128 lanes in a fixed order
   float* red = reinterpret_cast<float*>(smem + O_ST);  // [128][65]: the stages are free now
-  if (!bad) {
-    uint32_t gv[CPT];
-    tmem_ld32(tl + 192 + f0, gv);
+  if (!bad && tid < NCT) {
+    const int q = warp & 3, f0 = (warp >> 2) * CPT, i = q * 32 + lane;
 #pragma unroll
-    for (int j = 0; j < CPT; ++j) red[i * (QD + 1) + f0 + j] = __uint_as_float(gv[j]);
+    for (int rd = 0; rd < NR; ++rd) {
+      uint32_t gv[RC];
+      tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + 192 + f0 + RC * rd, gv);
+#pragma unroll
+      for (int j = 0; j < RC; ++j) red[i * (QD + 1) + f0 + RC * rd + j] = __uint_as_float(gv[j]);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -468,7 +518,7 @@ __global__ void __launch_bounds__(NTH, 2)
     return;
   }
   float* red4 = red + QT * (QD + 1);
-  {
+  if (tid < NCT) {
     const int f = tid & (QD - 1), qr = tid / QD;
     float v = 0.f;
     for (int r = qr * (QT / 4); r < (qr + 1) * (QT / 4); ++r) v += red[r * (QD + 1) + f];

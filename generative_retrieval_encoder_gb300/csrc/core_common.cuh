@@ -20,21 +20,33 @@ __device__ __forceinline__ bool arrive_last(int* counter, int count) {
   return last;
 }
 
-// Dot products of length dh spread over the CTA: `per` threads (a power of two,
-// at most 32) share one, each summing every per-th term, and a butterfly of
-// shuffles adds their sums (the same value in every lane of the group, since
-// fp32 addition commutes).  Rows are visited in passes of blockDim / per; every
-// thread runs every pass, so the shuffles see whole warps (blockDim is a
-// multiple of 32).  term(r, t) is the t-th term of row r; done(r, sum) is called
-// by the group's first thread.
-__device__ __forceinline__ int dot_split(int dh) {
+// The threads that run a combine: the first n of the CTA (whole warps),
+// synchronised by named barrier `id`; id 0 stands for the whole CTA.
+struct Team {
+  int n, id;
+};
+__device__ __forceinline__ void team_sync(const Team& t) {
+  if (t.id == 0)
+    __syncthreads();
+  else
+    asm volatile("bar.sync %0, %1;" ::"r"(t.id), "r"(t.n) : "memory");
+}
+
+// Dot products of length dh spread over a team of nt threads: `per` threads (a
+// power of two, at most 32) share one, each summing every per-th term, and a
+// butterfly of shuffles adds their sums (the same value in every lane of the
+// group, since fp32 addition commutes).  Rows are visited in passes of
+// nt / per; every thread of the team runs every pass, so the shuffles see
+// whole warps (nt is a multiple of 32).  term(r, t) is the t-th term of row r;
+// done(r, sum) is called by the group's first thread.
+__device__ __forceinline__ int dot_split(int dh, int nt) {
   int per = 32;
-  while (per > 1 && per * dh > (int)blockDim.x) per >>= 1;
+  while (per > 1 && per * dh > nt) per >>= 1;
   return per;
 }
 template <class Term, class Done>
-__device__ __forceinline__ void rows_dot(int rows, int dh, Term term, Done done) {
-  const int per = dot_split(dh), rpp = blockDim.x / per;
+__device__ __forceinline__ void rows_dot(int rows, int dh, int nt, Term term, Done done) {
+  const int per = dot_split(dh, nt), rpp = nt / per;
   const int j = threadIdx.x % per;
   for (int r0 = 0; r0 < rows; r0 += rpp) {
     const int r = r0 + threadIdx.x / per;
@@ -74,11 +86,16 @@ __device__ __forceinline__ void rows_dot(int rows, int dh, Term term, Done done)
 // sbuf (optional, 16-byte aligned shared memory of dh * state_ld(dh) floats):
 // the combined state is staged there as well, so that the centring passes
 // read shared memory instead of the global copy just written.
+// team_n, team_id: the combine runs on the first team_n threads of the CTA,
+// which meet at named barrier team_id (0: every thread, __syncthreads).
 __device__ inline void combine_state(const float* partial, const float* partial_m, int first,
                                      int count, int H, int h, int dh, int seqh, bool logits,
                                      float* state, bf16* state_bf, float* state_m,
                                      float* pub_state, float* center = nullptr,
-                                     const float* fwd_center = nullptr, float* sbuf = nullptr) {
+                                     const float* fwd_center = nullptr, float* sbuf = nullptr,
+                                     int team_n = 0, int team_id = 0) {
+  const Team team{team_n ? team_n : (int)blockDim.x, team_n ? team_id : 0};
+  const int nt = team.n;
   const int LD = state_ld(dh);
   const int n = dh * LD;
   float m = 0.f;
@@ -96,7 +113,7 @@ __device__ inline void combine_state(const float* partial, const float* partial_
   // otherwise pay once per float4 and partial).
   constexpr int PER = 5;
   const int n4 = n / 4;
-  for (int i0 = threadIdx.x; i0 < n4; i0 += PER * blockDim.x) {
+  for (int i0 = threadIdx.x; i0 < n4; i0 += PER * nt) {
     float4 acc[PER];
 #pragma unroll
     for (int u = 0; u < PER; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -105,7 +122,7 @@ __device__ inline void combine_state(const float* partial, const float* partial_
       float4 p[PER];
 #pragma unroll
       for (int u = 0; u < PER; ++u) {
-        const int i = i0 + u * blockDim.x;
+        const int i = i0 + u * nt;
         p[u] = i < n4 ? __ldcg(Pc + i) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
       float sc = 1.f;
@@ -121,7 +138,7 @@ __device__ inline void combine_state(const float* partial, const float* partial_
     }
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
-      const int i = i0 + u * blockDim.x;
+      const int i = i0 + u * nt;
       if (i >= n4) continue;
       S[i] = acc[u];
       if (sbuf) reinterpret_cast<float4*>(sbuf)[i] = acc[u];
@@ -138,10 +155,10 @@ __device__ inline void combine_state(const float* partial, const float* partial_
   const float* Sr = sbuf ? sbuf : state + (size_t)seqh * n;
   if (fwd_center) {
     float* St = state + (size_t)seqh * n;
-    __syncthreads();  // this CTA's state writes are visible to the whole CTA
+    team_sync(team);  // the team's state writes are visible to the whole team
     const float* c = fwd_center + (size_t)seqh * dh;
     rows_dot(
-        dh, dh, [&](int e, int f) { return __bfloat162float(__float2bfloat16_rn(Sr[e * LD + f])) * __ldg(c + f); },
+        dh, dh, nt, [&](int e, int f) { return __bfloat162float(__float2bfloat16_rn(Sr[e * LD + f])) * __ldg(c + f); },
         [&](int e, float dot) {
           const float acc = Sr[e * LD + dh] - dot;
           St[e * LD + dh] = acc;
@@ -151,19 +168,19 @@ __device__ inline void combine_state(const float* partial, const float* partial_
   if (center) {
     __shared__ float cbuf[129];  // column sums of S, then sum_e z_e
     float* St = state + (size_t)seqh * n;
-    __syncthreads();  // this CTA's state writes are visible to the whole CTA
+    team_sync(team);  // the team's state writes are visible to the whole team
     // column f < dh: sum_e S[e][f]; "column" dh: Z = sum_e z_e
-    rows_dot(dh + 1, dh, [&](int f, int e) { return Sr[e * LD + f]; }, [&](int f, float sum) { cbuf[f] = sum; });
-    __syncthreads();
+    rows_dot(dh + 1, dh, nt, [&](int f, int e) { return Sr[e * LD + f]; }, [&](int f, float sum) { cbuf[f] = sum; });
+    team_sync(team);
     const float Z = cbuf[dh];
-    __syncthreads();  // every thread has read Z before cbuf[f] becomes c_f
-    for (int f = threadIdx.x; f < dh; f += blockDim.x) {
+    team_sync(team);  // every thread has read Z before cbuf[f] becomes c_f
+    for (int f = threadIdx.x; f < dh; f += nt) {
       const float c = Z > 0.f ? cbuf[f] / Z : 0.f;
       cbuf[f] = c;
       center[(size_t)seqh * dh + f] = c;
     }
-    __syncthreads();
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    team_sync(team);
+    for (int i = threadIdx.x; i < n; i += nt) {
       const int e = i / LD, f = i % LD;
       float v = Sr[i];
       if (f < dh) {
@@ -175,7 +192,7 @@ __device__ inline void combine_state(const float* partial, const float* partial_
   }
   if (state_bf) {
     const int BLD = state_bf_ld(dh);
-    for (int i = threadIdx.x; i < dh * (BLD - LD); i += blockDim.x) {
+    for (int i = threadIdx.x; i < dh * (BLD - LD); i += nt) {
       const int e = i / (BLD - LD), f = LD + i % (BLD - LD);
       state_bf[((size_t)seqh * dh + e) * BLD + f] = __float2bfloat16_rn(0.f);
     }
