@@ -353,12 +353,30 @@ cudaError_t launch_readout_chunks_bf16(const ReadoutArgs& ra, bool norm, const T
   return launch_readout_bf16(rc, norm, n_chunks, st);
 }
 
+// The core readout: tcgen05 where it applies (unless the policy asks for
+// mma.sync), else the mma.sync kernel over the chunks.
+cudaError_t launch_readout_core_bf16(const ReadoutArgs& ra, int n_tiles, const Tiling& chunks, int n_chunks,
+                                     cudaStream_t st, const char** name) {
+  if (g_policy != GBLA_POLICY_MMA) {
+    const cudaError_t e = launch_readout_core_tc(ra, n_tiles, st);
+    if (e != cudaErrorNotSupported) {
+      *name = "readout[tc]";
+      return e;
+    }
+    (void)cudaGetLastError();
+  }
+  *name = "readout[mma]";
+  return launch_readout_chunks_bf16(ra, false, chunks, n_chunks, st);
+}
+
 cudaError_t launch_readout_layer_bf16(const ReadoutArgs& ra, int n_tiles, const Tiling& chunks, int n_chunks,
                                       cudaStream_t st, const char** nm) {
-  *nm = "readout[tc]";
-  const cudaError_t e = launch_readout_tc(ra, n_tiles, st);
-  if (e != cudaErrorNotSupported) return e;
-  (void)cudaGetLastError();
+  if (g_policy != GBLA_POLICY_MMA) {
+    *nm = "readout[tc]";
+    const cudaError_t e = launch_readout_tc(ra, n_tiles, st);
+    if (e != cudaErrorNotSupported) return e;
+    (void)cudaGetLastError();
+  }
   *nm = "readout[mma]";
   return launch_readout_chunks_bf16(ra, true, chunks, n_chunks, st);
 }
@@ -376,10 +394,12 @@ cudaError_t launch_bwd_kv_chunks_bf16(const BwdKVArgs& kv, const Tiling& chunks,
 
 cudaError_t launch_bwd_kv_layer_bf16(const BwdKVArgs& kv, int n_tiles, const Tiling& chunks, int n_chunks,
                                      int* bg_rows, cudaStream_t st, const char** nm) {
-  *nm = "bwd_kv[tc]";
-  const cudaError_t e = launch_bwd_kv_tc(kv, n_tiles, bg_rows, st);
-  if (e != cudaErrorNotSupported) return e;
-  (void)cudaGetLastError();
+  if (g_policy != GBLA_POLICY_MMA) {
+    *nm = "bwd_kv[tc]";
+    const cudaError_t e = launch_bwd_kv_tc(kv, n_tiles, bg_rows, st);
+    if (e != cudaErrorNotSupported) return e;
+    (void)cudaGetLastError();
+  }
   *nm = "bwd_kv[mma]";
   *bg_rows = n_chunks;
   return launch_bwd_kv_chunks_bf16(kv, chunks, n_chunks, st);
@@ -389,13 +409,15 @@ cudaError_t launch_bwd_kv_layer_bf16(const BwdKVArgs& kv, int n_tiles, const Til
 // *gamma_rows = the rows of dgamma partials written.
 cudaError_t launch_bwd_q_layer_bf16(const BwdQArgs& q, int hd, int n_chunks, int n_tiles, int* gamma_rows,
                                     cudaStream_t st, const char** nm) {
-  *nm = "bwd_q[tc]";
-  cudaError_t e = launch_bwd_q_tc(q, hd, n_tiles, gamma_rows, st);
-  if (e != cudaErrorNotSupported) return e;
-  (void)cudaGetLastError();
-  e = launch_bwd_q_tc128(q, hd, n_tiles, gamma_rows, st);
-  if (e != cudaErrorNotSupported) return e;
-  (void)cudaGetLastError();
+  if (g_policy != GBLA_POLICY_MMA) {
+    *nm = "bwd_q[tc]";
+    cudaError_t e = launch_bwd_q_tc(q, hd, n_tiles, gamma_rows, st);
+    if (e != cudaErrorNotSupported) return e;
+    (void)cudaGetLastError();
+    e = launch_bwd_q_tc128(q, hd, n_tiles, gamma_rows, st);
+    if (e != cudaErrorNotSupported) return e;
+    (void)cudaGetLastError();
+  }
   *nm = "bwd_q[mma]";
   *gamma_rows = n_chunks * q.H;
   return launch_bwd_q_bf16(q, true, n_chunks, st);
@@ -410,7 +432,7 @@ cudaError_t launch_bwd_q_layer_bf16(const BwdQArgs& q, int hd, int n_chunks, int
 cudaError_t launch_reduce_layer_bf16(const ReduceArgs& a, int n_chunks, int n_tiles, int sms, cudaStream_t st,
                                      const char** nm) {
   const long long units = (long long)a.seq.T * a.H / 256;
-  if (units >= 20LL * sms || g_policy == GBLA_POLICY_TC) {
+  if ((units >= 20LL * sms && g_policy != GBLA_POLICY_MMA) || g_policy == GBLA_POLICY_TC) {
     *nm = "reduce[tc]";
     const cudaError_t e = launch_reduce_tc(a, n_tiles, st);
     if (e != cudaErrorNotSupported) return e;
@@ -680,9 +702,10 @@ gbla_status bla_core_forward(const gbla_shape* shape, const void* q, const void*
   ra.state = st; ra.state_bf = sbf; ra.center = center;
   ra.out = o; ra.ldo = p.HD; ra.den = den;
   ra.H = p.H; ra.dh = p.dh; ra.seq = c.seq; ra.tiles = c.tiles; ra.err = c.kerr;
+  const char* nm = "readout[f32]";
   GBLA_CHECK(p.f32 ? launch_readout_f32(ra, false, p.n_tiles, c.st)
-                   : launch_readout_chunks_bf16(ra, false, c.chunks, p.n_chunks, c.st),
-             p.f32 ? "readout[f32]" : "readout[mma]");
+                   : launch_readout_core_bf16(ra, p.n_tiles, c.chunks, p.n_chunks, c.st, &nm),
+             nm);
   return GBLA_OK;
 }
 
@@ -796,7 +819,7 @@ const char* gbla_last_error(void) { return g_last_error.c_str(); }
 void gbla_profiling_enable(int on) { g_prof.on = on != 0; }
 
 gbla_status gbla_set_kernel_policy(int policy) {
-  if (policy != GBLA_POLICY_AUTO && policy != GBLA_POLICY_TC) return GBLA_ERR_INVALID_ARG;
+  if (policy != GBLA_POLICY_AUTO && policy != GBLA_POLICY_TC && policy != GBLA_POLICY_MMA) return GBLA_ERR_INVALID_ARG;
   g_policy = policy;
   return GBLA_OK;
 }

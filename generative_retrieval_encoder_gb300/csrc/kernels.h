@@ -177,6 +177,9 @@ cudaError_t launch_bwd_q_tc128(const BwdQArgs& a, int hd, int n_tiles, int* npar
 // tcgen05 readout with the RmsNorm gate (readout_tc.cu): d_h = 64, phi(q)
 // stored (pre), no den output; cudaErrorNotSupported otherwise.
 cudaError_t launch_readout_tc(const ReadoutArgs& a, int n_tiles, cudaStream_t st);
+// The core form on tcgen05 (q as given, phi applied in shared memory, o and den
+// out, no gate); bf16, d_h = 64 or 128.  cudaErrorNotSupported otherwise.
+cudaError_t launch_readout_core_tc(const ReadoutArgs& a, int n_tiles, cudaStream_t st);
 // tcgen05 key-side backward (bwd_kv_tc.cu): d_h = 64, phi(k) stored, sigmoid
 // gate (ds = dg g (1 - g)) or softmax logits (ds = dg g, g = exp(s - m));
 // db_g partials in *nparts rows of bg_part.  cudaErrorNotSupported otherwise.

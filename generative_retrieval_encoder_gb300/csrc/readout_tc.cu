@@ -4,6 +4,13 @@
 //   o_i = S'^T phi(q_i) / (z . phi(q_i)) + c,   y_i = RmsNorm(o_i) gamma SiLU(r_i)
 // (S' the centred state, c its centre; rs and 1/den saved for the backward).
 //
+// Core form (CORE = true, the core entry point of Eq. 5): q as given, o_i the
+// output (no gate), den_i optionally stored.  The ring then holds q alone;
+// the epilogue group that owns an MMA tile first rewrites its rows of the
+// tile as phi(q) in place (one thread per row, den = z . phi(q) on the way),
+// and the MMA waits for that rewrite instead of the copy.  o leaves through
+// the same rows of the tile (phi(q) is no longer needed once the MMA is done).
+//
 // Persistent: one CTA per SM walks a contiguous range of (row tile, head)
 // units, head-major, so that consecutive units mostly share a (sequence,
 // head) and its state.  Roles:
@@ -35,13 +42,13 @@ namespace {
 constexpr int RT = 128;                  // rows per MMA tile
 constexpr int TILE = RT * 128;           // one 64-column atom of a tile: [128 rows][64 bf16], 16 KB
 
-// Shapes and shared-memory layout by head width D (64 or 128).
-template <int D>
+// Shapes and shared-memory layout by head width D (64 or 128) and form.
+template <int D, bool CORE>
 struct RCfg {
   static constexpr int NH = D / 64;                 // 64-column atoms of a row
-  static constexpr int RST = D == 64 ? 6 : 2;       // ring stages (phi(q) atoms | r atoms)
+  static constexpr int RST = CORE ? (D == 64 ? 8 : 4) : (D == 64 ? 6 : 2);  // ring stages (phi(q) atoms | r atoms)
   static constexpr int NG = D == 64 ? 4 : 2;        // epilogue groups of 4 warps; MMA tile j goes to group j % NG
-  static constexpr int STAGE = 2 * NH * TILE;
+  static constexpr int STAGE = (CORE ? 1 : 2) * NH * TILE;
   static constexpr int SATOM = D * 128;             // one 64-column atom of S' [e][f]
   static constexpr int SBUF = NH * SATOM;
   static constexpr int EW = 4 * NG;                 // epilogue warps
@@ -49,8 +56,8 @@ struct RCfg {
   static constexpr int O_ST = 0;
   static constexpr int O_S = O_ST + RST * STAGE;    // two S' buffers
   static constexpr int O_BAR = O_S + 2 * SBUF;
-  // full[RST], empty[RST], sfull[2], sfree[2], accf[NG], acce[NG], drain
-  static constexpr int NBAR = 2 * RST + 4 + 2 * NG + 1;
+  // full[RST], empty[RST], sfull[2], sfree[2], accf[NG], acce[NG], drain, phi[RST] (core)
+  static constexpr int NBAR = 3 * RST + 4 + 2 * NG + 1;
   static constexpr int O_CZ = O_BAR + 8 * NBAR;     // [group][2 buffers][c | z] fp32, gamma
   static constexpr int O_SLOT = O_CZ + 4 * (NG * 2 * 2 * D + D);
   static constexpr int O_FAIL = O_SLOT + 4;
@@ -99,11 +106,11 @@ __device__ __forceinline__ Unit unit_at(const ReadoutArgs& a, int u, int n_units
   return x;
 }
 
-template <int D>
-__global__ void __launch_bounds__(RCfg<D>::NTH, 1)
+template <int D, bool CORE>
+__global__ void __launch_bounds__(RCfg<D, CORE>::NTH, 1)
     k_readout_tc(const ReadoutArgs a, const __grid_constant__ CUtensorMap tmP,
                  const __grid_constant__ CUtensorMap tmS, int roff, int n_units_per_head, int n_units) {
-  using C = RCfg<D>;
+  using C = RCfg<D, CORE>;
   constexpr int NH = C::NH, RST = C::RST, NG = C::NG, STAGE = C::STAGE, SBUF = C::SBUF, EW = C::EW,
                 NTH = C::NTH, O_ST = C::O_ST, O_S = C::O_S, O_BAR = C::O_BAR, O_CZ = C::O_CZ,
                 O_SLOT = C::O_SLOT, O_FAIL = C::O_FAIL, TMEM_COLS = C::TMEM_COLS;
@@ -129,6 +136,7 @@ __global__ void __launch_bounds__(RCfg<D>::NTH, 1)
   auto ACCF = [&](int g) { return bar0 + 8 * (2 * RST + 4 + g); };
   auto ACCE = [&](int g) { return bar0 + 8 * (2 * RST + 4 + NG + g); };
   const uint32_t DRAIN = bar0 + 8 * (2 * RST + 4 + 2 * NG);
+  auto PHI = [&](int s) { return bar0 + 8 * (2 * RST + 4 + 2 * NG + 1 + s); };  // core: phi(q) written
   float* cz = reinterpret_cast<float*>(smem + O_CZ);  // [group][2][c D | z D]
   float* gam = cz + NG * 2 * 2 * D;
   uint32_t* slot = reinterpret_cast<uint32_t*>(smem + O_SLOT);
@@ -138,6 +146,7 @@ __global__ void __launch_bounds__(RCfg<D>::NTH, 1)
     for (int s = 0; s < RST; ++s) {
       mbar_init(FULL(s), 1);
       mbar_init(EMPTY(s), 1 + 4);  // the MMA commit + the four warps of the tile's group
+      if (CORE) mbar_init(PHI(s), 4);  // the four warps of the tile's group
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(SFULL(k), 1);
@@ -188,7 +197,7 @@ __global__ void __launch_bounds__(RCfg<D>::NTH, 1)
 #pragma unroll
           for (int hf = 0; hf < NH; ++hf) {
             tma_load_2d(st + hf * TILE, &tmP, FULL(s), x.h * D + 64 * hf, y);
-            tma_load_2d(st + (NH + hf) * TILE, &tmP, FULL(s), roff + x.h * D + 64 * hf, y);
+            if (!CORE) tma_load_2d(st + (NH + hf) * TILE, &tmP, FULL(s), roff + x.h * D + 64 * hf, y);
           }
           last_s[s] = j + 1;
         }
@@ -219,7 +228,7 @@ __global__ void __launch_bounds__(RCfg<D>::NTH, 1)
         bool ok = true;
         for (int t = 0; t < x.ntl; ++t, ++j) {
           const int s = j % RST, ab = j % NG;
-          if (!mbar_wait(FULL(s), (j / RST) & 1, fail)) { ok = false; break; }
+          if (!mbar_wait(CORE ? PHI(s) : FULL(s), (j / RST) & 1, fail)) { ok = false; break; }
           if (j >= NG && !mbar_wait(ACCE(ab), ((j / NG) - 1) & 1, fail)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sq = sbase + O_ST + s * STAGE;
@@ -273,6 +282,76 @@ __global__ void __launch_bounds__(RCfg<D>::NTH, 1)
         uint8_t* sr = smem + O_ST + s * STAGE + NH * TILE;
         const int rel = t * RT + i;
         const bool valid = rel < x.nval, store = rel < x.nrows;
+        if (CORE) {
+          // phi(q) in place over this group's copy of q, den = z . phi(q) on the way
+          mbar_wait(FULL(s), (j / RST) & 1, fail);
+          float den = 0.f;
+          uint8_t* sqw = smem + O_ST + s * STAGE;
+#pragma unroll
+          for (int c = 0; c < 8 * NH; ++c) {
+            uint4* qp = reinterpret_cast<uint4*>(sqw + (c >> 3) * TILE + swz_off(i, c & 7));
+            float qv[8];
+            unpack8(*qp, qv);
+            uint32_t w[4];
+#pragma unroll
+            for (int jj = 0; jj < 8; jj += 2) {
+              const float p0 = phi_f(qv[jj]), p1 = phi_f(qv[jj + 1]);
+              const uint32_t pk = pack_bf16(p0, p1);
+              // den from the bf16 values the MMA multiplies with
+              den = fmaf(bf_lo(pk), zb[8 * c + jj], den);
+              den = fmaf(bf_hi(pk), zb[8 * c + jj + 1], den);
+              w[jj / 2] = pk;
+            }
+            *qp = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(PHI(s));
+          const float inv = valid ? 1.f / den : 0.f;
+          const float cv = valid ? 1.f : 0.f;
+          mbar_wait(ACCF(grp), (j / NG) & 1, fail);
+          tc_fence_after();
+          // o = O'/den + c over phi(q) of this row, 32 columns at a time
+#pragma unroll
+          for (int hh = 0; hh < D / 32; ++hh) {
+            uint32_t o[32];
+            tmem_ld32(tl + 32 * hh, o);
+            if (hh == D / 32 - 1) {  // the accumulator is read: hand it back
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(ACCE(grp));
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int cc = 4 * hh + c;
+              uint32_t w[4];
+#pragma unroll
+              for (int jj = 0; jj < 8; jj += 2) {
+                const int F = 8 * cc + jj;
+                w[jj / 2] = pack_bf16(fmaf(__uint_as_float(o[8 * c + jj]), inv, cv * cb[F]),
+                                      fmaf(__uint_as_float(o[8 * c + jj + 1]), inv, cv * cb[F + 1]));
+              }
+              *reinterpret_cast<uint4*>(sqw + (cc >> 3) * TILE + swz_off(i, cc & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+          __syncwarp();
+          {
+            const int ch = lane & 7;
+#pragma unroll
+            for (int hf = 0; hf < NH; ++hf)
+#pragma unroll
+              for (int it = 0; it < 8; ++it) {
+                const int rr = wq * 32 + 4 * it + (lane >> 3), rl = t * RT + rr;
+                const uint4 v = *reinterpret_cast<const uint4*>(sqw + hf * TILE + swz_off(rr, ch));
+                if (rl < x.nrows)
+                  *reinterpret_cast<uint4*>(out + (x.rb + rl) * a.ldo + (size_t)x.h * D + 64 * hf + 8 * ch) = v;
+              }
+          }
+          if (a.den && store) a.den[(x.rb + rel) * a.H + x.h] = valid ? den : 0.f;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(EMPTY(s));
+          continue;
+        }
         mbar_wait(ACCF(grp), (j / NG) & 1, fail);
         tc_fence_after();
         // O' columns 0..31 load under den = z . phi(q) (the row's phi(q) in shared memory)
@@ -363,19 +442,19 @@ __global__ void __launch_bounds__(RCfg<D>::NTH, 1)
   if (bad && tid == 0 && a.err_out) atomicOr(a.err_out, kErrTimeout);
 }
 
-template <int D>
+template <int D, bool CORE>
 cudaError_t launch_readout_tc_d(const ReadoutArgs& a, int n_tiles, long long roff, cudaStream_t st) {
-  using C = RCfg<D>;
+  using C = RCfg<D, CORE>;
   CUtensorMap tmP, tmS;
   if (!make_map(&tmP, a.q, (uint64_t)a.ldq, (uint64_t)a.seq.T, (uint64_t)a.ldq, 64, RT, false) ||
       !make_map(&tmS, a.state_bf, (uint64_t)state_bf_ld(D), (uint64_t)a.seq.n_seq * a.H * D,
                 (uint64_t)state_bf_ld(D), 64, D, false))
     return cudaErrorNotSupported;
-  cudaError_t e = cudaFuncSetAttribute(k_readout_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(k_readout_tc<D, CORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_units = n_tiles * a.H;
   const int grid = n_units < sm_count() ? n_units : sm_count();
-  return launch_pdl(k_readout_tc<D>, dim3(grid), dim3(C::NTH), C::SMEM, st, a, tmP, tmS, (int)roff, n_tiles, n_units);
+  return launch_pdl(k_readout_tc<D, CORE>, dim3(grid), dim3(C::NTH), C::SMEM, st, a, tmP, tmS, (int)roff, n_tiles, n_units);
 }
 
 }  // namespace
@@ -386,7 +465,17 @@ cudaError_t launch_readout_tc(const ReadoutArgs& a, int n_tiles, cudaStream_t st
   if ((a.dh != 64 && a.dh != 128) || !a.pre || a.ldr != a.ldq || roff < 0 || roff % 8 || !al16(a.q) ||
       !al16(a.out) || !al16(a.state_bf) || a.ldq % 8 || a.ldo % 8 || a.seq.T <= 0 || n_tiles <= 0 || a.den)
     return cudaErrorNotSupported;
-  return a.dh == 64 ? launch_readout_tc_d<64>(a, n_tiles, roff, st) : launch_readout_tc_d<128>(a, n_tiles, roff, st);
+  return a.dh == 64 ? launch_readout_tc_d<64, false>(a, n_tiles, roff, st)
+                    : launch_readout_tc_d<128, false>(a, n_tiles, roff, st);
+}
+
+cudaError_t launch_readout_core_tc(const ReadoutArgs& a, int n_tiles, cudaStream_t st) {
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  if ((a.dh != 64 && a.dh != 128) || a.pre || a.r || !al16(a.q) || !al16(a.out) || !al16(a.state_bf) ||
+      a.ldq % 8 || a.ldo % 8 || a.seq.T <= 0 || n_tiles <= 0 || a.tiles.tile % RT)
+    return cudaErrorNotSupported;
+  return a.dh == 64 ? launch_readout_tc_d<64, true>(a, n_tiles, 0, st)
+                    : launch_readout_tc_d<128, true>(a, n_tiles, 0, st);
 }
 
 }  // namespace gbla

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libgbla.so")
 GBLA_OK, GBLA_ERR_INVALID_ARG, GBLA_ERR_UNSUPPORTED, GBLA_ERR_WORKSPACE, GBLA_ERR_CUDA, GBLA_ERR_DEVICE_CHECK = \
     0, -1, -2, -3, -4, -5
 GBLA_ERR_DEVICE_TIMEOUT = -6
-GBLA_POLICY_AUTO, GBLA_POLICY_TC = 0, 1
+GBLA_POLICY_AUTO, GBLA_POLICY_TC, GBLA_POLICY_MMA = 0, 1, 2
 GBLA_F32, GBLA_BF16 = 0, 1
 GBLA_GATE_SIGMOID, GBLA_GATE_SOFTMAX = 0, 1
 GBLA_OP_FORWARD, GBLA_OP_BACKWARD, GBLA_OP_CORE_FORWARD, GBLA_OP_CORE_BACKWARD, GBLA_OP_DECAY_FORWARD = 0, 1, 2, 3, 4
@@ -279,7 +279,7 @@ def gbla_diag_bounded_wait(ws: torch.Tensor, polls: int = 4096) -> int:
 
 
 def gbla_set_kernel_policy(policy: int) -> None:
-    """GBLA_POLICY_AUTO (default) or GBLA_POLICY_TC for this thread's later calls (see gbla.h)."""
+    """GBLA_POLICY_AUTO (default), GBLA_POLICY_TC or GBLA_POLICY_MMA for this thread's later calls (see gbla.h)."""
     _check(lib().gbla_set_kernel_policy(policy), "gbla_set_kernel_policy")
 
 

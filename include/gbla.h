@@ -281,9 +281,11 @@ int gbla_profiling_read(const char** names, float* ms, int cap);
  * tensor cores only when every SM gets at least 20 of its 256-row tiles, and
  * on mma.sync otherwise.  GBLA_POLICY_TC takes the tcgen05 kernel wherever it
  * applies (d_h and gate permitting), whatever the size: for tests that check
- * those kernels on small shapes.  Results agree within the tolerances either
- * way.  GBLA_ERR_INVALID_ARG for another value. */
-typedef enum { GBLA_POLICY_AUTO = 0, GBLA_POLICY_TC = 1 } gbla_policy;
+ * those kernels on small shapes.  GBLA_POLICY_MMA takes the mma.sync kernel
+ * of every step that has one beside its tcgen05 kernel: for tests of the
+ * mma.sync kernels at the shapes AUTO runs on tcgen05.  Results agree within
+ * the tolerances either way.  GBLA_ERR_INVALID_ARG for another value. */
+typedef enum { GBLA_POLICY_AUTO = 0, GBLA_POLICY_TC = 1, GBLA_POLICY_MMA = 2 } gbla_policy;
 gbla_status gbla_set_kernel_policy(int policy);
 
 #ifdef __cplusplus

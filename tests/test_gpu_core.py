@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from generative_retrieval_encoder_gb300 import build, gbla
-from gbla_cases import TOL, core_case, f64, max_err, valid_rows
+from gbla_cases import TOL, core_case, f64, launch_names, max_err, valid_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -144,3 +144,40 @@ def test_nan_inputs_propagate_without_crash():
     o, _, _ = gbla.bla_core_forward(shape, D["q"], D["k"], D["v"], D["g"])
     torch.cuda.synchronize()
     assert torch.isnan(o[:, 3]).all()
+
+
+# (policy, variant the bf16 core readout runs under it); shapes with a ragged
+# tail, a one-token sequence and, at d_h = 128, varlen lengths
+READOUT_CASES = [
+    ("tc", 64, [700, 1, 300], None),
+    ("mma", 64, [700, 1, 300], None),
+    ("tc", 128, None, [3, 1500, 0, 31, 129]),
+    ("mma", 128, None, [3, 1500, 0, 31, 129]),
+]
+
+
+@pytest.mark.parametrize("case", READOUT_CASES, ids=[f"{c[0]}-dh{c[1]}" for c in READOUT_CASES])
+def test_core_forward_readout_variants(case):
+    """The core forward's readout on tcgen05 (phi applied to q in shared
+    memory) and, under GBLA_POLICY_MMA, on mma.sync: each matches the oracle,
+    and the variant that ran is the one asked for."""
+    variant, dh, sl, lens = case
+    B, L = (3, 700) if sl else (1, 0)
+    shape, D, R, (st, ln), T = core_case("bf16", B, L, 2, dh, seed=400 + READOUT_CASES.index(case), seq_lens=sl,
+                                         lengths=lens)
+    gbla.gbla_set_kernel_policy(gbla.GBLA_POLICY_TC if variant == "tc" else gbla.GBLA_POLICY_MMA)
+    try:
+        res = {}
+        names = launch_names(lambda: res.update(zip(("o", "den", "state"),
+                                                     gbla.bla_core_forward(shape, D["q"], D["k"], D["v"], D["g"],
+                                                                           den=True))))
+        torch.cuda.synchronize()
+    finally:
+        gbla.gbla_set_kernel_policy(gbla.GBLA_POLICY_TC)
+    assert f"readout[{variant}]" in names, names
+    ro, rden, _ = oracle.core_forward(R["q"], R["k"], R["v"], R["g"], st, ln, 2, dh)
+    m = valid_rows(st, ln, T)
+    go, gden = f64(res["o"]), f64(res["den"])
+    assert max_err(go[m], ro[m], scale=np.abs(R["v"][m]).max()) <= TOL["bf16"]
+    assert max_err(gden[m], rden[m]) <= TOL["bf16"]
+    assert (go[~m] == 0).all() and (gden[~m] == 0).all()
