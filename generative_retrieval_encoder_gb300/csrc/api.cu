@@ -392,6 +392,38 @@ cudaError_t launch_bwd_kv_chunks_bf16(const BwdKVArgs& kv, const Tiling& chunks,
   return launch_bwd_kv_bf16(kc, n_chunks, st);
 }
 
+// The core's query-side backward: tcgen05 where it applies (d_h = 64; unless
+// the policy asks for mma.sync), else the mma.sync kernel.
+cudaError_t launch_bwd_q_core_bf16(const BwdQArgs& q, int hd, int n_tiles, const Ctx& c, const char** nm) {
+  if (g_policy != GBLA_POLICY_MMA) {
+    int parts = 0;
+    const cudaError_t e = launch_bwd_q_tc(q, hd, n_tiles, &parts, c.st);
+    if (e != cudaErrorNotSupported) {
+      *nm = "bwd_q[tc]";
+      return e;
+    }
+    (void)cudaGetLastError();
+  }
+  *nm = "bwd_q[mma]";
+  return launch_bwd_q_bf16(q, false, c.p.n_chunks, c.st);
+}
+
+// The core's key-side backward: tcgen05 where it applies (unless the policy
+// asks for mma.sync), else the mma.sync kernel over the chunks.
+cudaError_t launch_bwd_kv_core_bf16(const BwdKVArgs& kv, int n_tiles, const Ctx& c, const char** nm) {
+  if (g_policy != GBLA_POLICY_MMA) {
+    int parts = 0;
+    const cudaError_t e = launch_bwd_kv_tc(kv, n_tiles, &parts, c.st);
+    if (e != cudaErrorNotSupported) {
+      *nm = "bwd_kv[tc]";
+      return e;
+    }
+    (void)cudaGetLastError();
+  }
+  *nm = "bwd_kv[mma]";
+  return launch_bwd_kv_chunks_bf16(kv, c.chunks, c.p.n_chunks, c.st);
+}
+
 cudaError_t launch_bwd_kv_layer_bf16(const BwdKVArgs& kv, int n_tiles, const Tiling& chunks, int n_chunks,
                                      int* bg_rows, cudaStream_t st, const char** nm) {
   if (g_policy != GBLA_POLICY_MMA) {
@@ -729,9 +761,11 @@ gbla_status bla_core_backward(const gbla_shape* shape, const void* q, const void
   a.dq = dq; a.lddq = p.HD;
   a.partial = at<float>(ws, c.l.partial); a.counters = at<int>(ws, c.l.cnt_b);
   a.dstate = at<float>(ws, c.l.dstate); a.dstate_bf = at<bf16>(ws, c.l.dstate_bf);
-  a.H = p.H; a.dh = p.dh; a.seq = c.seq; a.chunks = c.chunks; a.err = c.kerr;
-  GBLA_CHECK(p.f32 ? launch_bwd_q_f32(a, false, p.n_chunks, c.st) : launch_bwd_q_bf16(a, false, p.n_chunks, c.st),
-             p.f32 ? "bwd_q[f32]" : "bwd_q[mma]");
+  a.H = p.H; a.dh = p.dh; a.seq = c.seq; a.chunks = c.chunks; a.tiles = c.tiles; a.err = c.kerr; a.err_out = c.err;
+  a.partial_slots = partial_slots(p);
+  const char* nmq = "bwd_q[f32]";
+  GBLA_CHECK(p.f32 ? launch_bwd_q_f32(a, false, p.n_chunks, c.st) : launch_bwd_q_core_bf16(a, p.HD, p.n_tiles, c, &nmq),
+             nmq);
   BwdKVArgs kv{};
   kv.k = k; kv.ldk = p.HD; kv.v = v; kv.ldv = p.HD;
   kv.g = g; kv.ldg = p.H; kv.gate_kind = GATE_VALUES;
@@ -739,8 +773,8 @@ gbla_status bla_core_backward(const gbla_shape* shape, const void* q, const void
   kv.dk = dk; kv.lddk = p.HD; kv.dv = dv; kv.lddv = p.HD;
   kv.ds = dg; kv.ldds = p.H; kv.gate_grad = GG_DG;
   kv.H = p.H; kv.dh = p.dh; kv.seq = c.seq; kv.tiles = c.tiles; kv.err = c.kerr;
-  GBLA_CHECK(p.f32 ? launch_bwd_kv_f32(kv, p.n_tiles, c.st) : launch_bwd_kv_chunks_bf16(kv, c.chunks, p.n_chunks, c.st),
-             p.f32 ? "bwd_kv[f32]" : "bwd_kv[mma]");
+  const char* nm = "bwd_kv[f32]";
+  GBLA_CHECK(p.f32 ? launch_bwd_kv_f32(kv, p.n_tiles, c.st) : launch_bwd_kv_core_bf16(kv, p.n_tiles, c, &nm), nm);
   return GBLA_OK;
 }
 

@@ -25,6 +25,11 @@
 //                    lines.
 // The gate multiplies dv after the MMA, so both MMAs read the loaded tiles.
 //
+// Core form (CORE = true, the core entry point's backward of Eq. 5): k and v
+// as given (two tensors), the gate's values, and dg_j itself out in fp32.  The
+// epilogue group that owns an MMA tile first rewrites its rows of the k tile
+// as phi(k) in place, and the MMAs wait for that rewrite instead of the copy.
+//
 // Every mbarrier wait is bounded; after one gives up, the kernel finishes its
 // loops without waiting, sets the timeout bit of the error word, waits
 // (bounded) for its copies and MMAs, frees its TMEM and returns.
@@ -39,7 +44,7 @@ constexpr int KT = 128;                  // rows per MMA tile
 constexpr int TILE = KT * 128;           // one 64-column atom of a tile: [128 rows][64 bf16], 16 KB
 
 // Shapes and shared-memory layout by head width D (64 or 128).
-template <int D>
+template <int D, bool CORE>
 struct KCfg {
   static constexpr int NH = D / 64;                 // 64-column atoms of a row
   static constexpr int KST = D == 64 ? 6 : 2;       // ring stages (phi(k) atoms | v atoms)
@@ -52,8 +57,8 @@ struct KCfg {
   static constexpr int O_ST = 0;
   static constexpr int O_S = O_ST + KST * STAGE;    // two dS buffers
   static constexpr int O_BAR = O_S + 2 * SBUF;
-  // full[KST], empty[KST], sfull[2], sfree[2], accf[NG], acce[NG], drain
-  static constexpr int NBAR = 2 * KST + 4 + 2 * NG + 1;
+  // full[KST], empty[KST], sfull[2], sfree[2], accf[NG], acce[NG], drain, phi[KST] (core)
+  static constexpr int NBAR = 3 * KST + 4 + 2 * NG + 1;
   static constexpr int O_DZ = O_BAR + 8 * NBAR;     // [group][2 buffers][dz'' D] fp32
   static constexpr int O_RED = O_DZ + 4 * NG * 2 * D;  // [group][4 warps] ds sums
   static constexpr int O_M = O_RED + 4 * NG * 4;    // [group][2 buffers] maximum logit (softmax gate)
@@ -94,17 +99,18 @@ __device__ __forceinline__ Unit unit_at(const BwdKVArgs& a, int u, int n_units_p
   return x;
 }
 
-template <int D>
-__global__ void __launch_bounds__(KCfg<D>::NTH, 1)
-    k_bwd_kv_tc(const BwdKVArgs a, const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmS,
-                int voff, int n_units_per_head, int n_units) {
-  using C = KCfg<D>;
+template <int D, bool CORE>
+__global__ void __launch_bounds__(KCfg<D, CORE>::NTH, 1)
+    k_bwd_kv_tc(const BwdKVArgs a, const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmV,
+                const __grid_constant__ CUtensorMap tmS, int n_units_per_head, int n_units) {
+  using C = KCfg<D, CORE>;
   constexpr int NH = C::NH, KST = C::KST, NG = C::NG, STAGE = C::STAGE, SBUF = C::SBUF, EW = C::EW,
                 NTH = C::NTH, O_ST = C::O_ST, O_S = C::O_S, O_BAR = C::O_BAR, O_DZ = C::O_DZ, O_RED = C::O_RED,
                 O_M = C::O_M, O_SLOT = C::O_SLOT, O_FAIL = C::O_FAIL, TMEM_COLS = C::TMEM_COLS;
   (void)NTH;
   if (threadIdx.x == 0) {  // the descriptors load while the previous kernel finishes
     tma_prefetch_map(&tmP);
+    tma_prefetch_map(&tmV);
     tma_prefetch_map(&tmS);
   }
   pdl_enter();  // the previous kernel's outputs are visible from here on
@@ -125,6 +131,7 @@ __global__ void __launch_bounds__(KCfg<D>::NTH, 1)
   auto ACCF = [&](int g) { return bar0 + 8 * (2 * KST + 4 + g); };
   auto ACCE = [&](int g) { return bar0 + 8 * (2 * KST + 4 + NG + g); };
   const uint32_t DRAIN = bar0 + 8 * (2 * KST + 4 + 2 * NG);
+  auto PHI = [&](int s) { return bar0 + 8 * (2 * KST + 4 + 2 * NG + 1 + s); };  // core: phi(k) written
   float* dzs = reinterpret_cast<float*>(smem + O_DZ);
   float* red = reinterpret_cast<float*>(smem + O_RED);
   float* mgs = reinterpret_cast<float*>(smem + O_M);
@@ -136,6 +143,7 @@ __global__ void __launch_bounds__(KCfg<D>::NTH, 1)
     for (int s = 0; s < KST; ++s) {
       mbar_init(FULL(s), 1);
       mbar_init(EMPTY(s), 1 + 4);  // the MMA commit + the four warps of the tile's group
+      if (CORE) mbar_init(PHI(s), 4);  // the four warps of the tile's group
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(SFULL(k), 1);
@@ -185,7 +193,7 @@ __global__ void __launch_bounds__(KCfg<D>::NTH, 1)
 #pragma unroll
           for (int hf = 0; hf < NH; ++hf) {
             tma_load_2d(st + hf * TILE, &tmP, FULL(s), x.h * D + 64 * hf, y);
-            tma_load_2d(st + (NH + hf) * TILE, &tmP, FULL(s), voff + x.h * D + 64 * hf, y);
+            tma_load_2d(st + (NH + hf) * TILE, &tmV, FULL(s), x.h * D + 64 * hf, y);
           }
           last_s[s] = j + 1;
         }
@@ -216,7 +224,7 @@ __global__ void __launch_bounds__(KCfg<D>::NTH, 1)
         bool ok = true;
         for (int t = 0; t < x.ntl; ++t, ++j) {
           const int s = j % KST, g = j % NG;
-          if (!mbar_wait(FULL(s), (j / KST) & 1, fail)) { ok = false; break; }
+          if (!mbar_wait(CORE ? PHI(s) : FULL(s), (j / KST) & 1, fail)) { ok = false; break; }
           if (j >= NG && !mbar_wait(ACCE(g), ((j / NG) - 1) & 1, fail)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sk = sbase + O_ST + s * STAGE, sv = sk + NH * TILE;
@@ -282,6 +290,20 @@ __global__ void __launch_bounds__(KCfg<D>::NTH, 1)
         const size_t row = x.rb + rel;
         const float gin = valid ? __ldg(a.g + row * a.ldg + x.h) : 0.f;
         const float g = logits ? (valid ? __expf(gin - mseq) : 0.f) : gin;
+        if (CORE) {  // phi(k) in place over this group's rows of the k tile
+          mbar_wait(FULL(s), (j / KST) & 1, fail);
+#pragma unroll
+          for (int c = 0; c < 8 * NH; ++c) {
+            uint4* kp = reinterpret_cast<uint4*>(sk + (c >> 3) * TILE + swz_off(i, c & 7));
+            float kv[8];
+            unpack8(*kp, kv);
+            *kp = make_uint4(pack_bf16(phi_f(kv[0]), phi_f(kv[1])), pack_bf16(phi_f(kv[2]), phi_f(kv[3])),
+                             pack_bf16(phi_f(kv[4]), phi_f(kv[5])), pack_bf16(phi_f(kv[6]), phi_f(kv[7])));
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(PHI(s));
+        }
         mbar_wait(ACCF(grp), (j / NG) & 1, fail);
         tc_fence_after();
         // dk~ = D1 + dz'', dg = phi(k) . dk~, dk = g dk~ min(1, phi(k)) -> the phi(k) row;
@@ -334,9 +356,14 @@ __global__ void __launch_bounds__(KCfg<D>::NTH, 1)
             *reinterpret_cast<uint4*>(sv + (cc >> 3) * TILE + swz_off(i, cc & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
-        // the gate-logit gradient
-        const float ds = valid ? (logits ? dg * g : dg * g * (1.f - g)) : 0.f;
-        if (store) reinterpret_cast<bf16*>(a.ds)[row * a.ldds + x.h] = __float2bfloat16_rn(ds);
+        // the gate-logit gradient (core: dL/dg itself, fp32)
+        const float ds = valid ? (CORE ? dg : logits ? dg * g : dg * g * (1.f - g)) : 0.f;
+        if (store) {
+          if (CORE)
+            reinterpret_cast<float*>(a.ds)[row * a.ldds + x.h] = ds;
+          else
+            reinterpret_cast<bf16*>(a.ds)[row * a.ldds + x.h] = __float2bfloat16_rn(ds);
+        }
         // the warp's 32 rows of dk and dv leave as whole 128-byte lines
         __syncwarp();
         {
@@ -379,35 +406,39 @@ __global__ void __launch_bounds__(KCfg<D>::NTH, 1)
   if (bad && tid == 0 && a.err_out) atomicOr(a.err_out, kErrTimeout);
 }
 
-template <int D>
-cudaError_t launch_bwd_kv_tc_d(const BwdKVArgs& a, int n_tiles, long long voff, int* nparts, cudaStream_t st) {
-  using C = KCfg<D>;
-  CUtensorMap tmP, tmS;
-  if (!make_map(&tmP, a.k, (uint64_t)(voff + a.H * D), (uint64_t)a.seq.T, (uint64_t)a.ldk, 64, KT, false) ||
+template <int D, bool CORE>
+cudaError_t launch_bwd_kv_tc_d(const BwdKVArgs& a, int n_tiles, int* nparts, cudaStream_t st) {
+  using C = KCfg<D, CORE>;
+  CUtensorMap tmP, tmV, tmS;
+  if (!make_map(&tmP, a.k, (uint64_t)(a.H * D), (uint64_t)a.seq.T, (uint64_t)a.ldk, 64, KT, false) ||
+      !make_map(&tmV, a.v, (uint64_t)(a.H * D), (uint64_t)a.seq.T, (uint64_t)a.ldv, 64, KT, false) ||
       !make_map(&tmS, a.dstate_bf, (uint64_t)state_bf_ld(D), (uint64_t)a.seq.n_seq * a.H * D,
                 (uint64_t)state_bf_ld(D), 64, D, false))
     return cudaErrorNotSupported;
-  cudaError_t e = cudaFuncSetAttribute(k_bwd_kv_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(k_bwd_kv_tc<D, CORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_units = n_tiles * a.H;
   const int grid = n_units < sm_count() ? n_units : sm_count();
   *nparts = n_tiles * (a.tiles.tile / KT);
-  return launch_pdl(k_bwd_kv_tc<D>, dim3(grid), dim3(C::NTH), C::SMEM, st, a, tmP, tmS, (int)voff, n_tiles, n_units);
+  return launch_pdl(k_bwd_kv_tc<D, CORE>, dim3(grid), dim3(C::NTH), C::SMEM, st, a, tmP, tmV, tmS, n_tiles, n_units);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_kv_tc(const BwdKVArgs& a, int n_tiles, int* nparts, cudaStream_t st) {
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
-  const long long voff = ((const bf16*)a.v - (const bf16*)a.k);
   const bool sig = a.gate_kind == GATE_VALUES && a.gate_grad == GG_SIGMOID;
   const bool soft = a.gate_kind == GATE_LOGITS && a.gate_grad == GG_SOFTMAX && a.state_m;
-  if ((a.dh != 64 && a.dh != 128) || !a.pre || !(sig || soft) || a.ldv != a.ldk || voff < 0 || voff % 8 ||
-      !al16(a.k) || !al16(a.dk) || !al16(a.dv) || !al16(a.dstate_bf) || a.ldk % 8 || a.lddk % 8 || a.lddv % 8 ||
+  const bool core = !a.pre && a.gate_kind == GATE_VALUES && a.gate_grad == GG_DG && !a.bg_part;
+  if ((a.dh != 64 && a.dh != 128) || !(a.pre ? (sig || soft) : core) || !al16(a.k) || !al16(a.v) ||
+      !al16(a.dk) || !al16(a.dv) || !al16(a.dstate_bf) || a.ldk % 8 || a.ldv % 8 || a.lddk % 8 || a.lddv % 8 ||
       a.seq.T <= 0 || n_tiles <= 0 || a.tiles.tile % KT || a.zero_cols_to > a.zero_cols_from)
     return cudaErrorNotSupported;
-  return a.dh == 64 ? launch_bwd_kv_tc_d<64>(a, n_tiles, voff, nparts, st)
-                    : launch_bwd_kv_tc_d<128>(a, n_tiles, voff, nparts, st);
+  if (core)
+    return a.dh == 64 ? launch_bwd_kv_tc_d<64, true>(a, n_tiles, nparts, st)
+                      : launch_bwd_kv_tc_d<128, true>(a, n_tiles, nparts, st);
+  return a.dh == 64 ? launch_bwd_kv_tc_d<64, false>(a, n_tiles, nparts, st)
+                    : launch_bwd_kv_tc_d<128, false>(a, n_tiles, nparts, st);
 }
 
 }  // namespace gbla

@@ -37,6 +37,15 @@
 // same stage (each thread owns its row's columns), which then serve as the A
 // operand of (d) and (e).
 //
+// Core form (CORE = true, the core entry point's backward of Eq. 5): q and
+// d_o as given, no gate: do = d_o, so
+//   dn = d_o / den,   dden = -(d_o . O') / den^2,   den = z . phi(q),
+// one pass sums z . phi(q) and d_o . O' over the row (exchanged like the
+// layer's sums), a second writes dn.  The stage holds q and d_o (the third
+// tile only carries dden for (e)).  phi(q) is written over q in shared memory
+// one tile ahead, while the compute warps wait for (d) of the tile before, and
+// (a) waits for that rewrite.  No dgamma.
+//
 // Every mbarrier wait is bounded; after one gives up, the kernel finishes its
 // loops without waiting (uniform control flow, so no barrier is left
 // waiting), sets the timeout bit of the error word, waits (bounded) for its
@@ -60,7 +69,7 @@ constexpr int BLD = state_bf_ld(QD);  // bf16 state row
 constexpr int O_S = 0;                       // S' [e][f] (8 KB)
 constexpr int O_ST = O_S + 8192;             // stages (1024-aligned)
 constexpr int O_BAR = O_ST + QST * STAGE;
-constexpr int NBAR = 2 * QST + 4;            // full, empty, a_done, dn_ready, d_done, s_ready
+constexpr int NBAR = 3 * QST + 4;            // full, empty, a_done, dn_ready, d_done, s_ready, phi (core)
 constexpr int O_F = O_BAR + 8 * NBAR;        // gamma, centre, z (fp32), row exchange [3][2][128]
 constexpr int O_SLOT = O_F + 4 * (3 * QD + 3 * 2 * QT);
 constexpr int O_FAIL = O_SLOT + 4;
@@ -135,6 +144,7 @@ __device__ __forceinline__ void tmem_wait16(uint32_t (&r)[16]) {
   tmem_tie16(r);
 }
 
+template <bool CORE>
 __global__ void __launch_bounds__(NTH, 2)
     k_bwd_q_tc(const BwdQArgs a, const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmY,
                int roff, int upt, int spt, int n_units) {
@@ -154,7 +164,8 @@ __global__ void __launch_bounds__(NTH, 2)
   QTile cur;
   int ucur = next_unit(a, u0, u1, upt, spt, cur);
   if (ucur >= u1) {  // no rows in this range: a zero dgamma partial
-    for (int f = tid; f < QD; f += NTH) a.gamma_part[(size_t)blockIdx.x * QD + f] = 0.f;
+    if (!CORE)
+      for (int f = tid; f < QD; f += NTH) a.gamma_part[(size_t)blockIdx.x * QD + f] = 0.f;
     return;
   }
 
@@ -168,6 +179,7 @@ __global__ void __launch_bounds__(NTH, 2)
   const uint32_t bar0 = sbase + O_BAR;
   const uint32_t A_DONE = bar0 + 8 * (2 * QST), DN_READY = A_DONE + 8, D_DONE = A_DONE + 16, S_READY = A_DONE + 24;
   auto FULL = [&](int s) { return bar0 + 8 * s; };
+  auto PHI = [&](int s) { return bar0 + 8 * (2 * QST + 4 + s); };  // core: phi(q) written over q
   auto EMPTY = [&](int s) { return bar0 + 8 * (QST + s); };
   const bool issuer = tid == NCT;  // lane 0 of warp 8
 
@@ -179,10 +191,10 @@ __global__ void __launch_bounds__(NTH, 2)
     const int s = ld_k % QST;
     const uint32_t st = sbase + O_ST + s * STAGE;
     const int y = (int)ld_x.rb;
-    mbar_expect_tx(FULL(s), 3 * TILE);
+    mbar_expect_tx(FULL(s), (CORE ? 2 : 3) * TILE);
     tma_load_2d(st, &tmP, FULL(s), ld_x.h * QD, y);
     tma_load_2d(st + TILE, &tmY, FULL(s), ld_x.h * QD, y);
-    tma_load_2d(st + 2 * TILE, &tmP, FULL(s), roff + ld_x.h * QD, y);
+    if (!CORE) tma_load_2d(st + 2 * TILE, &tmP, FULL(s), roff + ld_x.h * QD, y);
     issued[s] = ld_k + 1;
     ++ld_k;
     ld_u = next_unit(a, ld_u + 1, u1, upt, spt, ld_x);
@@ -196,6 +208,8 @@ __global__ void __launch_bounds__(NTH, 2)
     mbar_init(DN_READY, EW);
     mbar_init(D_DONE, 1);
     mbar_init(S_READY, EW);
+    if (CORE)
+      for (int s = 0; s < QST; ++s) mbar_init(PHI(s), EW);
     mbar_init_fence();
     *fail = 0;
     load_next();
@@ -230,7 +244,7 @@ __global__ void __launch_bounds__(NTH, 2)
     if (lane == 0) {
       // (a): K = e.  A = phi(Q) K-major (+32 B per 16 e); B = S' N-major (16 e-rows = 2048 B).
       auto issue_a = [&](int k) {
-        if (!mbar_wait(FULL(k % QST), (k / QST) & 1, fail)) return;
+        if (!mbar_wait(CORE ? PHI(k % QST) : FULL(k % QST), (k / QST) & 1, fail)) return;
         tc_fence_after();
         const uint32_t sq = sbase + O_ST + (k % QST) * STAGE;
         const uint32_t id_a = idesc_bf16(QT, QD, false, true);
@@ -264,8 +278,9 @@ __global__ void __launch_bounds__(NTH, 2)
             tc_mma(tmem + 64, sdesc(sy + 32 * kk, 16, 1024), sdesc(sS + 32 * kk, 16, 1024), id_d, kk > 0);
           tc_commit(D_DONE);
           // (a) of the next tile before (e): epilogue 2 and the next pass 1 wait
-          // on (d) and (a); (e) only gates the reuse of this stage.
-          if (same) issue_a(k + 1);
+          // on (d) and (a); (e) only gates the reuse of this stage.  (Core: after
+          // (e), since (a) waits for the rewrite of q the compute warps do next.)
+          if (same && !CORE) issue_a(k + 1);
           // (e): K = rows.  A = [dn | dden ...] M-major, its two 64-wide halves the
           // dy and r tiles (one tile apart); B = phi(Q) N-major.
 #pragma unroll
@@ -273,6 +288,7 @@ __global__ void __launch_bounds__(NTH, 2)
             tc_mma(tmem + 128, sdesc(sy + 2048 * kk, TILE, 1024), sdesc(sq + 2048 * kk, 8192, 1024), id_e,
                    (k == kseg && kk == 0) ? 0u : 1u);
           tc_commit(EMPTY(s));
+          if (same && CORE) issue_a(k + 1);
         }
         // the tile after next into this stage once it is free
         if (ld_k == k + QST && ld_u < u1 && mbar_wait(EMPTY(s), (k / QST) & 1, fail)) load_next();
@@ -298,10 +314,28 @@ __global__ void __launch_bounds__(NTH, 2)
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
     // rs and 1/den of this thread's row of a tile (0 on rows outside the sequence: u = dn = 0 there)
     auto rsinv_of = [&](const QTile& x) {
-      return i < x.nval ? __ldg(reinterpret_cast<const float2*>(a.rsinv + 2 * ((x.rb + i) * H + x.h)))
-                        : make_float2(0.f, 0.f);
+      return (!CORE && i < x.nval) ? __ldg(reinterpret_cast<const float2*>(a.rsinv + 2 * ((x.rb + i) * H + x.h)))
+                                   : make_float2(0.f, 0.f);
+    };
+    // core: phi(q) over q in tile kt's stage, this thread's 32 columns of its row
+    auto phi_rows = [&](int kt) {
+      const int st = kt % QST;
+      mbar_wait(FULL(st), (kt / QST) & 1, fail);
+      uint8_t* tq = smem + O_ST + st * STAGE;
+#pragma unroll
+      for (int ch = 0; ch < CPT / 8; ++ch) {
+        uint4* qp = reinterpret_cast<uint4*>(tq + swz_off(i, (f0 >> 3) + ch));
+        float v[8];
+        unpack8(*qp, v);
+        *qp = make_uint4(pack_bf16(phi_f(v[0]), phi_f(v[1])), pack_bf16(phi_f(v[2]), phi_f(v[3])),
+                         pack_bf16(phi_f(v[4]), phi_f(v[5])), pack_bf16(phi_f(v[6]), phi_f(v[7])));
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(PHI(st));
     };
     float2 ri_cur = rsinv_of(cur);
+    if (CORE) phi_rows(0);
     int k = 0;
     while (true) {
       QTile nxt;
@@ -317,103 +351,147 @@ __global__ void __launch_bounds__(NTH, 2)
       const float rs = ri_cur.x, inv = ri_cur.y;
       mbar_wait(A_DONE, k & 1, fail);
       tc_fence_after();
-      // pass 1 in rounds of 16 columns: dr, dgamma, du (into the r tile);
-      // sums m = du . u, D1 = du . o', D2 = u . o'.
-      float m = 0.f, D1 = 0.f, D2 = 0.f;
+      float dden;
+      if constexpr (CORE) {
+        // z . phi(q) and d_o . O' over this thread's columns, in rounds of 16
+        float dp = 0.f, D1 = 0.f;
 #pragma unroll
-      for (int rd = 0; rd < NR; ++rd) {
-        const int fr = f0 + RC * rd;
-        uint32_t o[RC], g[RC];
-        tmem_ld16_async(tl + fr, o);
-        if (k > 0) {
-          tmem_ld16_async(tl + 192 + fr, g);
-          tmem_wait16(o);
-          tmem_tie16(g);
-        } else {
-          tmem_wait16(o);
+        for (int rd = 0; rd < NR; ++rd) {
+          const int fr = f0 + RC * rd;
+          uint32_t o[RC];
+          tmem_ld16(tl + fr, o);
 #pragma unroll
-          for (int j = 0; j < RC; ++j) g[j] = 0u;
-        }
+          for (int ch = 0; ch < RC / 8; ++ch) {
+            const int f = fr + 8 * ch, cc = f >> 3;
+            float qv[8], yv[8];
+            unpack8(*reinterpret_cast<const uint4*>(sq + swz_off(i, cc)), qv);
+            unpack8(*reinterpret_cast<const uint4*>(sy + swz_off(i, cc)), yv);
 #pragma unroll
-        for (int ch = 0; ch < RC / 8; ++ch) {
-          const int f = fr + 8 * ch, cc = f >> 3;
-          float yv[8], rv[8];
-          unpack8(*reinterpret_cast<const uint4*>(sy + swz_off(i, cc)), yv);
-          unpack8(*reinterpret_cast<const uint4*>(sr + swz_off(i, cc)), rv);
-          uint32_t dup[4], drp[4];
-#pragma unroll
-          for (int j = 0; j < 8; j += 2) {
-            float du2[2], dr2[2];
-#pragma unroll
-            for (int w = 0; w < 2; ++w) {
-              const int jj = j + w, kk = 8 * ch + jj;
-              const float op = __uint_as_float(o[kk]) * inv;  // centred o'
-              const float u = (op + cen[f + jj]) * rs;
-              const float r = rv[jj], dy = yv[jj];
-              const float sg = sigmoid_fast(r);
-              const float av = r * sg;
-              const float dyg = dy * gam[f + jj];
-              du2[w] = dyg * av;
-              g[kk] = __float_as_uint(fmaf(dy * av, u, __uint_as_float(g[kk])));
-              dr2[w] = dyg * u * sg * fmaf(r, 1.f - sg, 1.f);
-              m = fmaf(du2[w], u, m);
-              D1 = fmaf(du2[w], op, D1);
-              D2 = fmaf(u, op, D2);
+            for (int jj = 0; jj < 8; ++jj) {
+              dp = fmaf(qv[jj], zf[f + jj], dp);
+              D1 = fmaf(yv[jj], __uint_as_float(o[8 * ch + jj]), D1);
             }
-            dup[j / 2] = pack_bf16(du2[0], du2[1]);
-            drp[j / 2] = pack_bf16(dr2[0], dr2[1]);
           }
-          *reinterpret_cast<uint4*>(sr + swz_off(i, cc)) = make_uint4(dup[0], dup[1], dup[2], dup[3]);
-          if (store)
-            *reinterpret_cast<uint4*>((bf16*)a.dr + row * a.lddr + (size_t)h * QD + f) =
-                make_uint4(drp[0], drp[1], drp[2], drp[3]);
         }
-        tmem_st16(tl + 192 + fr, g);
-      }
-      // the row's two column ranges, added in a fixed order
-      xch[(0 + part) * QT + i] = m;
-      xch[(2 + part) * QT + i] = D1;
-      xch[(4 + part) * QT + i] = D2;
-      named_bar(1, NCT);
-      m = xch[0 * QT + i] + xch[1 * QT + i];
-      D1 = xch[2 * QT + i] + xch[3 * QT + i];
-      D2 = xch[4 * QT + i] + xch[5 * QT + i];
-      m *= 1.f / QD;
-      const float dden = -rs * fmaf(-m, D2, D1) * inv;
-      // pass 2: dn = rs (du - u m) / den -> the dy tile
+        // the row's two column ranges, added in a fixed order
+        xch[(0 + part) * QT + i] = dp;
+        xch[(2 + part) * QT + i] = D1;
+        named_bar(1, NCT);
+        const float den = xch[0 * QT + i] + xch[1 * QT + i];
+        const float invd = i < cur.nval ? 1.f / den : 0.f;
+        dden = -(xch[2 * QT + i] + xch[3 * QT + i]) * invd * invd;
+        // dn = d_o / den -> the dy tile
 #pragma unroll
-      for (int rd = 0; rd < NR; ++rd) {
-        const int fr = f0 + RC * rd;
-        uint32_t o[RC];
-        tmem_ld16(tl + fr, o);  // O' again
-#pragma unroll
-        for (int ch = 0; ch < RC / 8; ++ch) {
-          const int f = fr + 8 * ch, cc = f >> 3;
-          float du[8];
-          unpack8(*reinterpret_cast<const uint4*>(sr + swz_off(i, cc)), du);
-          uint32_t dn[4];
-#pragma unroll
-          for (int j = 0; j < 8; j += 2) {
-            float d2[2];
-#pragma unroll
-            for (int w = 0; w < 2; ++w) {
-              const int jj = j + w;
-              const float u = fmaf(__uint_as_float(o[8 * ch + jj]), inv, cen[f + jj]) * rs;
-              d2[w] = rs * fmaf(-u, m, du[jj]) * inv;
+        for (int ch = 0; ch < CPT / 8; ++ch) {
+          const int cc = (f0 >> 3) + ch;
+          uint4* yp = reinterpret_cast<uint4*>(sy + swz_off(i, cc));
+          float yv[8];
+          unpack8(*yp, yv);
+          *yp = make_uint4(pack_bf16(yv[0] * invd, yv[1] * invd), pack_bf16(yv[2] * invd, yv[3] * invd),
+                           pack_bf16(yv[4] * invd, yv[5] * invd), pack_bf16(yv[6] * invd, yv[7] * invd));
+        }
+        // dden in column 64 of [dn | dden] (first element of the third tile's row)
+        if (part == 0) *reinterpret_cast<uint4*>(sr + swz_off(i, 0)) = make_uint4(pack_bf16(dden, 0.f), 0u, 0u, 0u);
+      } else {
+        // pass 1 in rounds of 16 columns: dr, dgamma, du (into the r tile);
+        // sums m = du . u, D1 = du . o', D2 = u . o'.
+        float m = 0.f, D1 = 0.f, D2 = 0.f;
+  #pragma unroll
+        for (int rd = 0; rd < NR; ++rd) {
+          const int fr = f0 + RC * rd;
+          uint32_t o[RC], g[RC];
+          tmem_ld16_async(tl + fr, o);
+          if (k > 0) {
+            tmem_ld16_async(tl + 192 + fr, g);
+            tmem_wait16(o);
+            tmem_tie16(g);
+          } else {
+            tmem_wait16(o);
+  #pragma unroll
+            for (int j = 0; j < RC; ++j) g[j] = 0u;
+          }
+  #pragma unroll
+          for (int ch = 0; ch < RC / 8; ++ch) {
+            const int f = fr + 8 * ch, cc = f >> 3;
+            float yv[8], rv[8];
+            unpack8(*reinterpret_cast<const uint4*>(sy + swz_off(i, cc)), yv);
+            unpack8(*reinterpret_cast<const uint4*>(sr + swz_off(i, cc)), rv);
+            uint32_t dup[4], drp[4];
+  #pragma unroll
+            for (int j = 0; j < 8; j += 2) {
+              float du2[2], dr2[2];
+  #pragma unroll
+              for (int w = 0; w < 2; ++w) {
+                const int jj = j + w, kk = 8 * ch + jj;
+                const float op = __uint_as_float(o[kk]) * inv;  // centred o'
+                const float u = (op + cen[f + jj]) * rs;
+                const float r = rv[jj], dy = yv[jj];
+                const float sg = sigmoid_fast(r);
+                const float av = r * sg;
+                const float dyg = dy * gam[f + jj];
+                du2[w] = dyg * av;
+                g[kk] = __float_as_uint(fmaf(dy * av, u, __uint_as_float(g[kk])));
+                dr2[w] = dyg * u * sg * fmaf(r, 1.f - sg, 1.f);
+                m = fmaf(du2[w], u, m);
+                D1 = fmaf(du2[w], op, D1);
+                D2 = fmaf(u, op, D2);
+              }
+              dup[j / 2] = pack_bf16(du2[0], du2[1]);
+              drp[j / 2] = pack_bf16(dr2[0], dr2[1]);
             }
-            dn[j / 2] = pack_bf16(d2[0], d2[1]);
+            *reinterpret_cast<uint4*>(sr + swz_off(i, cc)) = make_uint4(dup[0], dup[1], dup[2], dup[3]);
+            if (store)
+              *reinterpret_cast<uint4*>((bf16*)a.dr + row * a.lddr + (size_t)h * QD + f) =
+                  make_uint4(drp[0], drp[1], drp[2], drp[3]);
           }
-          *reinterpret_cast<uint4*>(sy + swz_off(i, cc)) = make_uint4(dn[0], dn[1], dn[2], dn[3]);
+          tmem_st16(tl + 192 + fr, g);
         }
+        // the row's two column ranges, added in a fixed order
+        xch[(0 + part) * QT + i] = m;
+        xch[(2 + part) * QT + i] = D1;
+        xch[(4 + part) * QT + i] = D2;
+        named_bar(1, NCT);
+        m = xch[0 * QT + i] + xch[1 * QT + i];
+        D1 = xch[2 * QT + i] + xch[3 * QT + i];
+        D2 = xch[4 * QT + i] + xch[5 * QT + i];
+        m *= 1.f / QD;
+        dden = -rs * fmaf(-m, D2, D1) * inv;
+        // pass 2: dn = rs (du - u m) / den -> the dy tile
+  #pragma unroll
+        for (int rd = 0; rd < NR; ++rd) {
+          const int fr = f0 + RC * rd;
+          uint32_t o[RC];
+          tmem_ld16(tl + fr, o);  // O' again
+  #pragma unroll
+          for (int ch = 0; ch < RC / 8; ++ch) {
+            const int f = fr + 8 * ch, cc = f >> 3;
+            float du[8];
+            unpack8(*reinterpret_cast<const uint4*>(sr + swz_off(i, cc)), du);
+            uint32_t dn[4];
+  #pragma unroll
+            for (int j = 0; j < 8; j += 2) {
+              float d2[2];
+  #pragma unroll
+              for (int w = 0; w < 2; ++w) {
+                const int jj = j + w;
+                const float u = fmaf(__uint_as_float(o[8 * ch + jj]), inv, cen[f + jj]) * rs;
+                d2[w] = rs * fmaf(-u, m, du[jj]) * inv;
+              }
+              dn[j / 2] = pack_bf16(d2[0], d2[1]);
+            }
+            *reinterpret_cast<uint4*>(sy + swz_off(i, cc)) = make_uint4(dn[0], dn[1], dn[2], dn[3]);
+          }
+        }
+        // dden in column 64 of [dn | dden] (first element of the r tile's row);
+        // that chunk's du was consumed above by this row's first column range.
+        if (part == 0) *reinterpret_cast<uint4*>(sr + swz_off(i, 0)) = make_uint4(pack_bf16(dden, 0.f), 0u, 0u, 0u);
       }
-      // dden in column 64 of [dn | dden] (first element of the r tile's row);
-      // that chunk's du was consumed above by this row's first column range.
-      if (part == 0) *reinterpret_cast<uint4*>(sr + swz_off(i, 0)) = make_uint4(pack_bf16(dden, 0.f), 0u, 0u, 0u);
-      tmem_st_wait();
+      if (!CORE) tmem_st_wait();
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(DN_READY);
+      if (CORE && has_next) phi_rows(k + 1);  // q of the next tile, while (d) runs
       // epilogue 2: dq = (dq~ + dden z) min(1, phi(q))
       mbar_wait(D_DONE, k & 1, fail);
       tc_fence_after();
@@ -500,7 +578,7 @@ __global__ void __launch_bounds__(NTH, 2)
 
   // dgamma: per-lane sums in TMEM, reduced over the 128 lanes in a fixed order
   float* red = reinterpret_cast<float*>(smem + O_ST);  // [128][65]: the stages are free now
-  if (!bad && tid < NCT) {
+  if (!CORE && !bad && tid < NCT) {
     const int q = warp & 3, f0 = (warp >> 2) * CPT, i = q * 32 + lane;
 #pragma unroll
     for (int rd = 0; rd < NR; ++rd) {
@@ -517,6 +595,7 @@ __global__ void __launch_bounds__(NTH, 2)
     if (tid == 0 && a.err_out) atomicOr(a.err_out, kErrTimeout);
     return;
   }
+  if (CORE) return;
   float* red4 = red + QT * (QD + 1);
   if (tid < NCT) {
     const int f = tid & (QD - 1), qr = tid / QD;
@@ -533,10 +612,12 @@ __global__ void __launch_bounds__(NTH, 2)
 
 cudaError_t launch_bwd_q_tc(const BwdQArgs& a, int hd, int n_tiles, int* nparts, cudaStream_t st) {
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
-  const long long roff = ((const bf16*)a.r - (const bf16*)a.q);
-  if (a.dh != QD || !a.pre || !a.rsinv || hd % 8 || a.ldr != a.ldq || roff < 0 || roff % 8 ||
-      !al16(a.q) || !al16(a.dy) || !al16(a.dq) || !al16(a.dr) || !al16(a.partial) || a.ldq % 8 || a.lddy % 8 ||
-      a.lddq % 8 || a.lddr % 8 || a.seq.T <= 0 || n_tiles <= 0 || a.tiles.tile % QT)
+  const bool core = !a.pre && !a.r && !a.rsinv && !a.rms_w && !a.dr && !a.gamma_part;
+  const long long roff = core ? 0 : ((const bf16*)a.r - (const bf16*)a.q);
+  if (a.dh != QD || hd % 8 || !al16(a.q) || !al16(a.dy) || !al16(a.dq) || !al16(a.partial) || a.ldq % 8 ||
+      a.lddy % 8 || a.lddq % 8 || a.seq.T <= 0 || n_tiles <= 0 || a.tiles.tile % QT)
+    return cudaErrorNotSupported;
+  if (!core && (!a.pre || !a.rsinv || a.ldr != a.ldq || roff < 0 || roff % 8 || !al16(a.dr) || a.lddr % 8))
     return cudaErrorNotSupported;
   const int spt = a.tiles.tile / QT, upt = n_tiles * spt, n_units = upt * a.H;
   int grid = n_units < 2 * sm_count() ? n_units : 2 * sm_count();  // two CTAs per SM
@@ -549,12 +630,13 @@ cudaError_t launch_bwd_q_tc(const BwdQArgs& a, int hd, int n_tiles, int* nparts,
   if (!make_map(&tmP, a.q, (uint64_t)a.ldq, (uint64_t)a.seq.T, (uint64_t)a.ldq, 64, QT, false) ||
       !make_map(&tmY, a.dy, (uint64_t)a.lddy, (uint64_t)a.seq.T, (uint64_t)a.lddy, 64, QT, false))
     return cudaErrorNotSupported;
-  cudaError_t e = cudaFuncSetAttribute(k_bwd_q_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  auto kern = core ? k_bwd_q_tc<true> : k_bwd_q_tc<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_bwd_q_tc, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   *nparts = grid;
-  return launch_pdl(k_bwd_q_tc, dim3(grid), dim3(NTH), SMEM, st, a, tmP, tmY, (int)roff, upt, spt, n_units);
+  return launch_pdl(kern, dim3(grid), dim3(NTH), SMEM, st, a, tmP, tmY, (int)roff, upt, spt, n_units);
 }
 
 }  // namespace gbla

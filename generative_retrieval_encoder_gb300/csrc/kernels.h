@@ -167,22 +167,25 @@ cudaError_t launch_reduce_bf16(const ReduceArgs& a, int grid_x, cudaStream_t st)
 cudaError_t launch_reduce_tc(const ReduceArgs& a, int n_tiles, cudaStream_t st);
 cudaError_t launch_readout_bf16(const ReadoutArgs& a, bool norm, int grid_x, cudaStream_t st);
 cudaError_t launch_bwd_q_bf16(const BwdQArgs& a, bool norm, int grid_x, cudaStream_t st);
-// tcgen05 query-side backward (bwd_q_tc.cu): d_h = 64, the layer's RMSNorm
-// epilogue, phi(q) stored (pre); cudaErrorNotSupported otherwise.
+// tcgen05 query-side backward (bwd_q_tc.cu): d_h = 64; the layer's RMSNorm
+// epilogue with phi(q) stored (pre), or the core form (q as given: no pre, r,
+// rsinv, rms_w, dr or gamma_part); cudaErrorNotSupported otherwise.
 // Its CTAs (two per SM) take contiguous ranges of the (128-row tile, head)
 // units of a.tiles (n_tiles tiles); *nparts = the dgamma partial rows written.
 cudaError_t launch_bwd_q_tc(const BwdQArgs& a, int hd, int n_tiles, int* nparts, cudaStream_t st);
 // The same at d_h = 128 (bwd_q_tc128.cu), one CTA per SM.
 cudaError_t launch_bwd_q_tc128(const BwdQArgs& a, int hd, int n_tiles, int* nparts, cudaStream_t st);
-// tcgen05 readout with the RmsNorm gate (readout_tc.cu): d_h = 64, phi(q)
-// stored (pre), no den output; cudaErrorNotSupported otherwise.
+// tcgen05 readout with the RmsNorm gate (readout_tc.cu): d_h = 64 or 128,
+// phi(q) stored (pre), no den output; cudaErrorNotSupported otherwise.
 cudaError_t launch_readout_tc(const ReadoutArgs& a, int n_tiles, cudaStream_t st);
 // The core form on tcgen05 (q as given, phi applied in shared memory, o and den
 // out, no gate); bf16, d_h = 64 or 128.  cudaErrorNotSupported otherwise.
 cudaError_t launch_readout_core_tc(const ReadoutArgs& a, int n_tiles, cudaStream_t st);
-// tcgen05 key-side backward (bwd_kv_tc.cu): d_h = 64, phi(k) stored, sigmoid
-// gate (ds = dg g (1 - g)) or softmax logits (ds = dg g, g = exp(s - m));
-// db_g partials in *nparts rows of bg_part.  cudaErrorNotSupported otherwise.
+// tcgen05 key-side backward (bwd_kv_tc.cu): d_h = 64 or 128; phi(k) stored
+// with the sigmoid gate (ds = dg g (1 - g)) or softmax logits (ds = dg g,
+// g = exp(s - m)) and db_g partials in *nparts rows of bg_part; or the core
+// form (k as given, gate values, dg out in fp32, no bg_part).
+// cudaErrorNotSupported otherwise.
 cudaError_t launch_bwd_kv_tc(const BwdKVArgs& a, int n_tiles, int* nparts, cudaStream_t st);
 cudaError_t launch_bwd_kv_bf16(const BwdKVArgs& a, int grid_x, cudaStream_t st);
 

@@ -181,3 +181,44 @@ def test_core_forward_readout_variants(case):
     assert max_err(go[m], ro[m], scale=np.abs(R["v"][m]).max()) <= TOL["bf16"]
     assert max_err(gden[m], rden[m]) <= TOL["bf16"]
     assert (go[~m] == 0).all() and (gden[~m] == 0).all()
+
+
+# (policy, d_h, B, L, seq_lens, varlen lengths) of the bf16 core backward
+BACKWARD_VARIANT_CASES = [
+    ("tc", 64, 3, 700, [700, 1, 300], None),
+    ("mma", 64, 3, 700, [700, 1, 300], None),
+    ("tc", 64, 1, 0, None, [5, 0, 1500, 1, 64, 129, 384]),
+    ("tc", 128, 1, 0, None, [3, 1500, 0, 31, 129]),
+]
+
+
+@pytest.mark.parametrize("case", BACKWARD_VARIANT_CASES,
+                         ids=[f"{c[0]}-dh{c[1]}-" + ("varlen" if c[5] else "pad") for c in BACKWARD_VARIANT_CASES])
+def test_core_backward_variants(case):
+    """The core backward on tcgen05 (phi applied to q and k in shared memory;
+    the query side at d_h = 64, the key side at 64 and 128) and, under
+    GBLA_POLICY_MMA, on mma.sync: each matches the oracle, and the kernels
+    that ran are the ones asked for."""
+    variant, dh, B, L, sl, lens = case
+    shape, D, R, (st, ln), T = core_case("bf16", B, L, 2, dh, seed=500 + BACKWARD_VARIANT_CASES.index(case),
+                                         seq_lens=sl, lengths=lens)
+    gbla.gbla_set_kernel_policy(gbla.GBLA_POLICY_TC if variant == "tc" else gbla.GBLA_POLICY_MMA)
+    try:
+        res = {}
+        names = launch_names(lambda: res.update(zip(("dq", "dk", "dv", "dg"), gbla.bla_core_backward(
+            shape, D["q"], D["k"], D["v"], D["g"], D["d_o"]))))
+        torch.cuda.synchronize()
+    finally:
+        gbla.gbla_set_kernel_policy(gbla.GBLA_POLICY_TC)
+    assert f"bwd_kv[{variant}]" in names, names
+    assert f"bwd_q[{variant if dh == 64 else 'mma'}]" in names, names
+    ref = oracle.core_backward(R["q"], R["k"], R["v"], R["g"], R["d_o"], st, ln, 2, dh)
+    m = valid_rows(st, ln, T)
+    floor = 1e-3 * np.abs(R["d_o"]).max() * np.abs(R["v"]).max()  # one-token sequences: see above
+    for name, want in zip(("dq", "dk", "dv", "dg"), ref):
+        got = f64(res[name])
+        assert np.isfinite(got).all(), name
+        if m.any():
+            scale = max(np.abs(want[m]).max(), floor)
+            assert max_err(got[m], want[m], scale) <= TOL["bf16"], (name, max_err(got[m], want[m], scale))
+        assert (got[~m] == 0).all(), name
