@@ -32,27 +32,27 @@ L2_BYTES = 129 * 2 ** 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM bytes per launch from ncu captures (dram__bytes_read.sum + dram__bytes_write.sum),
-# keyed by launch name: (bytes, workload name, sha1 of the kernel's source file when captured).
-# A source change since the capture makes the figure stale: it is then reported as null.
+# keyed by launch name with its variant, "step[variant]": (bytes, workload name, sha1 of
+# the kernel's source file when captured).  A source change since the capture makes the
+# figure stale: it is then reported as null.
 NCU_TRAFFIC: dict = {
-    "projection gemm": (280607232, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "96f0c0d32571"),
-    "dx~ gemm": (328179968, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "96f0c0d32571"),
-    "dW gemm": (347604736, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "96f0c0d32571"),
-    "bwd_q": (317969408, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "f2d22e6ad57a"),
-    "readout": (171571712, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "6f790bb002a8"),
-    "reduce": (139569152, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "46d7c17b681f"),
-    "bwd_kv": (230319104, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "78f218ea5b14"),
-    "conv": (83937536, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "80d3b995dceb"),
-    "conv bwd": (168216576, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "80d3b995dceb"),
+    "projection gemm[tc]": (281015296, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "7a83a7a9d951"),
+    "dx~ gemm[tc]": (329495040, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "7a83a7a9d951"),
+    "dW gemm[tc]": (347428608, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "7a83a7a9d951"),
+    "bwd_q[tc]": (316208896, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "fb0d0c90244c"),
+    "readout[tc]": (170566400, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "c281bb0f589d"),
+    "bwd_kv[tc]": (231275776, "GBLA layer bf16 B=32 L=2048 d=512 H=8 d_h=64", "f0e90d3dc144"),
 }
-KERNEL_SOURCE = {"projection gemm": "gemm_tc.cu", "dx~ gemm": "gemm_tc.cu", "dW gemm": "gemm_tc.cu",
-                 "reduce": "reduce_tc.cu", "readout": "readout_tc.cu", "bwd_q": "bwd_q_tc.cu",
-                 "bwd_kv": "bwd_kv_tc.cu", "conv": "conv.cu", "conv bwd": "conv.cu",
-                 "param grads": "layer_misc.cu"}
+KERNEL_SOURCE = {"projection gemm[tc]": "gemm_tc.cu", "dx~ gemm[tc]": "gemm_tc.cu", "dW gemm[tc]": "gemm_tc.cu",
+                 "reduce[tc]": "reduce_tc.cu", "reduce[mma]": "core_bf16.cu", "readout[tc]": "readout_tc.cu",
+                 "bwd_q[tc]": "bwd_q_tc.cu", "bwd_kv[tc]": "bwd_kv_tc.cu", "conv[bulk]": "conv.cu",
+                 "conv bwd[bulk]": "conv.cu", "param grads": "layer_misc.cu"}
 
 
-def source_sha(name: str) -> str | None:
-    f = KERNEL_SOURCE.get(name)
+def source_sha(key: str) -> str | None:
+    """The hash of the source file of a launch ("step[variant]"): traffic
+    measured on another revision of the kernel does not apply."""
+    f = KERNEL_SOURCE.get(key)
     if f is None:
         return None
     p = os.path.join(ROOT, "generative_retrieval_encoder_gb300", "csrc", f)
@@ -546,8 +546,9 @@ def run_ours(args, wl, rank: int, world: int, local_rank: int):
     achieved = amount / (kern[dom] * 1e-3) / (1e9 if bound == "hbm" else 1e12)
     peak = peaks["hbm_gbs"] if bound == "hbm" else peaks["bf16_tflops_sustained"]
     traffic = None
-    t = NCU_TRAFFIC.get(dom)
-    if t and t[1] == wl.name and t[2] == source_sha(dom):
+    dkey = f"{dom}[{variant[dom]}]" if dom in variant else dom
+    t = NCU_TRAFFIC.get(dkey)
+    if t and t[1] == wl.name and t[2] == source_sha(dkey):
         traffic = t[0]
     roof = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak,
             "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "frac": achieved / peak, "traffic": traffic,

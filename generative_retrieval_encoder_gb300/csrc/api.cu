@@ -456,15 +456,17 @@ cudaError_t launch_bwd_q_layer_bf16(const BwdQArgs& q, int hd, int n_chunks, int
 }
 
 // The bf16 state reduction: the tcgen05 kernel where it applies (gate values,
-// d_h = 64) and each SM streams at least 20 of its 256-row tiles, else the
-// mma.sync kernel (softmax logits, other d_h; and shorter batches, where the
-// tcgen05 kernel's fixed start and final drain outweigh its faster stream:
-// measured 51 against 47 us at 13 tiles an SM, 80 against 81 at 27, 129
-// against 132 at 54).
+// d_h = 64) and either each SM streams at least 20 of its 256-row tiles or
+// phi(k) is not stored (the core entry points: the mma.sync kernel then
+// applies phi in registers, 65 against 61 us at 13 tiles an SM), else the
+// mma.sync kernel (softmax logits, other d_h; and shorter batches of the
+// layer, where the tcgen05 kernel's fixed start and final drain outweigh its
+// faster stream: measured 51 against 47 us at 13 tiles an SM, 80 against 81
+// at 27, 129 against 132 at 54).
 cudaError_t launch_reduce_layer_bf16(const ReduceArgs& a, int n_chunks, int n_tiles, int sms, cudaStream_t st,
                                      const char** nm) {
   const long long units = (long long)a.seq.T * a.H / 256;
-  if ((units >= 20LL * sms && g_policy != GBLA_POLICY_MMA) || g_policy == GBLA_POLICY_TC) {
+  if (((units >= 20LL * sms || !a.pre) && g_policy != GBLA_POLICY_MMA) || g_policy == GBLA_POLICY_TC) {
     *nm = "reduce[tc]";
     const cudaError_t e = launch_reduce_tc(a, n_tiles, st);
     if (e != cudaErrorNotSupported) return e;
