@@ -284,8 +284,9 @@ __global__ void __launch_bounds__(256) k_conv_bwd(const ConvArgs a, int rows_per
 }
 
 // Wp[c][n] = [W_q | W_k | W_v | W_r | w_g | 0][c][n] for n < np, 16 bytes
-// per thread (grid-stride).  np and H*dh are multiples of the vector width, so
-// a vector lies in one block; `vec`: the W_* rows are 16-byte aligned.
+// per thread: row c = blockIdx.y, vectors blockIdx.x * 256 + threadIdx.x of it
+// (no 64-bit index division).  np and H*dh are multiples of the vector width,
+// so a vector lies in one block; `vec`: the W_* rows are 16-byte aligned.
 template <typename T>
 __global__ void __launch_bounds__(256) k_pack(const T* Wq, const T* Wk, const T* Wv, const T* Wr, const T* wg,
                                               int d, int H, int dh, T* Wp, int np, int vec, uint32_t* zero,
@@ -293,14 +294,13 @@ __global__ void __launch_bounds__(256) k_pack(const T* Wq, const T* Wk, const T*
   pdl_enter();  // the previous kernel's outputs are visible from here on
   constexpr int V = 16 / sizeof(T);
   typedef uint4 U;
-  if (zero && blockIdx.x == 0)
+  if (zero && blockIdx.x == 0 && blockIdx.y == 0)
     for (int i = threadIdx.x; i < zero_words; i += blockDim.x) zero[i] = 0u;
   const int HD = H * dh, npv = np / V;
   const T* Ws[4] = {Wq, Wk, Wv, Wr};
-  const long long total = (long long)d * npv;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int c = (int)(i / npv), n = (int)(i % npv) * V;
+  const int c = blockIdx.y;
+  for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < npv; v += gridDim.x * blockDim.x) {
+    const int n = v * V;
     const int m = n / HD, j = n - m * HD;
     U u;
     if (m < 4 && vec) {
@@ -369,7 +369,6 @@ __global__ void __launch_bounds__(1024) k_colsum(const ColsumJobs js) {
 }
 
 
-int grid_for(size_t n) { const size_t g = (n + 255) / 256; return (int)(g < 2432 ? (g > 0 ? g : 1) : 2432); }
 
 // ------------------------------------------------------------ diagnostic
 // The bounded mbarrier wait of the tensor-core kernels, run out on purpose:
@@ -442,8 +441,8 @@ cudaError_t launch_pack_weights(const void* const* W, const void* w_g, int d, in
   const int zn = (int)(zero_bytes / 4);
   int vec = 1;
   for (int m = 0; m < 4; ++m) vec &= ((uintptr_t)W[m] & 15) == 0;
-  const long long vecs = (long long)d * np / (f32 ? 4 : 8);
-  const unsigned grid = (unsigned)std::max(1LL, std::min((vecs + 255) / 256, (long long)sm_count() * 8));
+  const int npv = np / (f32 ? 4 : 8);
+  const dim3 grid((unsigned)std::max(1, (npv + 255) / 256), (unsigned)std::max(1, d));
   if (f32)
     return launch_pdl(k_pack<float>, dim3(grid), dim3(256), 0, st, (const float*)W[0], (const float*)W[1],
                       (const float*)W[2], (const float*)W[3], (const float*)w_g, d, H, dh, (float*)Wp, np, vec, zw, zn);
