@@ -55,6 +55,7 @@ def _load():
             lib.oracle_core_backward.argtypes = seq + [_D] * 9
             lib.oracle_decay_core_explicit.argtypes = seq + [_D] * 7
             lib.oracle_decay_core_rnn.argtypes = seq + [_D] * 6
+            lib.oracle_sa_forward.argtypes = seq + [_D] * 5
             lib.oracle_conv1d.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, _I64, _I64] + [_D] * 4
             layer = ([ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _I64, _I64]
                      + [_D] * 10 + [ctypes.c_int, ctypes.c_double])
@@ -160,6 +161,17 @@ def decay_core_rnn(q, k, v, g, lam, start, ln, H: int, dh: int):
     o = np.zeros((T, H * dh))
     _load().oracle_decay_core_rnn(T, H, dh, len(start), ps, pl, _p(q), _p(k), _p(v), _p(g), _p(lam), _p(o))
     return o
+
+
+def sa_forward(q, k, v, start, ln, H: int, dh: int):
+    """Bidirectional softmax attention, Eq. 1 (oracle_sa_forward): returns
+    (o [T, H*dh], lse [T, H]); rows in no sequence are zero."""
+    q, k, v = map(_f64, (q, k, v))
+    T = q.shape[0]
+    start, ln, ps, pl = _seqargs(start, ln)
+    o = np.zeros((T, H * dh)); lse = np.zeros((T, H))
+    _load().oracle_sa_forward(T, H, dh, len(start), ps, pl, _p(q), _p(k), _p(v), _p(o), _p(lse))
+    return o, lse
 
 
 def core_backward(q, k, v, g, d_o, start, ln, H: int, dh: int):

@@ -20,6 +20,9 @@
  * The core under LION's decay masks (Lion-d, Lion-s; LION notes, mask
  * construction and instantiated models) is stated the same two ways:
  * oracle_decay_core_explicit (the definition) and oracle_decay_core_rnn.
+ * The bidirectional softmax attention of the SA blocks of the hybrid
+ * [SA, LA, LA] encoder (GBLA notes, "Core method" 1, Eq. 1, and the hybrid
+ * encoder paragraph) is oracle_sa_forward, Eq. 1 written out per query.
  *
  * Readings where the pages are silent (each one is listed in the design notes):
  *   phi(x) = elu(x) + 1 with alpha = 1, no 1/sqrt(d_h) scale;
@@ -275,6 +278,48 @@ void oracle_decay_core_explicit(int64_t T, int H, int dh, int n_seq,
       }
   free(pq);
   free(pk);
+}
+
+/*
+ * Bidirectional softmax attention, Eq. 1 of the GBLA notes ("Core method" 1):
+ *   o_i = sum_j exp(q_i . k_j / sqrt(d_h)) v_j / sum_j exp(q_i . k_j / sqrt(d_h))
+ * over every key j of query i's sequence (no mask: both directions), per head.
+ * The largest score of the row is subtracted inside the exponentials (it
+ * cancels between numerator and denominator); lse_i = m_i + log of the
+ * denominator (the log-sum-exp of the scaled scores) is returned when lse is
+ * not NULL.  Rows in no sequence are left untouched.
+ */
+void oracle_sa_forward(int64_t T, int H, int dh, int n_seq,
+                       const int64_t* start, const int64_t* len,
+                       const double* q, const double* k, const double* v, double* o, double* lse) {
+  const int64_t ld = (int64_t)H * dh;
+  const double scale = 1.0 / sqrt((double)dh);
+#pragma omp parallel for collapse(2) schedule(dynamic)
+  for (int b = 0; b < n_seq; ++b)
+    for (int h = 0; h < H; ++h) {
+      double* sc = (double*)malloc(sizeof(double) * (size_t)(len[b] > 0 ? len[b] : 1));
+      for (int64_t i = start[b]; i < start[b] + len[b]; ++i) {
+        double m = -INFINITY;
+        for (int64_t j = start[b]; j < start[b] + len[b]; ++j) {
+          double s = 0.0;
+          for (int e = 0; e < dh; ++e) s += q[i * ld + h * dh + e] * k[j * ld + h * dh + e];
+          s *= scale;
+          sc[j - start[b]] = s;
+          if (s > m) m = s;
+        }
+        double num[1024];
+        double den = 0.0;
+        for (int f = 0; f < dh; ++f) num[f] = 0.0;
+        for (int64_t j = start[b]; j < start[b] + len[b]; ++j) {
+          const double w = exp(sc[j - start[b]] - m);
+          for (int f = 0; f < dh; ++f) num[f] += w * v[j * ld + h * dh + f];
+          den += w;
+        }
+        for (int f = 0; f < dh; ++f) o[i * ld + h * dh + f] = num[f] / den;
+        if (lse) lse[i * H + h] = m + log(den);
+      }
+      free(sc);
+    }
 }
 
 /*

@@ -104,3 +104,14 @@ def test_layer_worked_example(name):
     for key in ("g", "o", "y"):
         if key in c:
             np.testing.assert_allclose(out[key], c[key], rtol=0, atol=1e-14, err_msg=f"{name}: {key}")
+
+
+@pytest.mark.parametrize("name", [n for n in CASES if n.startswith("sa_")])
+def test_sa_worked_example(name):
+    c = CASES[name]
+    H, dh = int(c["shape"]["H"]), int(c["shape"]["dh"])
+    T = c["q"].shape[0]
+    start, ln = oracle.seqs(B=1, L=T)
+    o, lse = oracle.sa_forward(c["q"], c["k"], c["v"], start, ln, H, dh)
+    np.testing.assert_allclose(o, c["o"], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, c["lse"], rtol=1e-14, atol=0)

@@ -390,3 +390,71 @@ def test_decay_core_outputs_are_convex_combinations_and_sequences_independent():
         s1, l1 = oracle.seqs(1, int(n))
         alone, _ = oracle.decay_core_forward(q[a:a + n], k[a:a + n], v[a:a + n], g[a:a + n], lam[a:a + n], s1, l1, 1, 4)
         np.testing.assert_allclose(o[a:a + n], alone, rtol=1e-13, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# Bidirectional softmax attention (GBLA notes, "Core method" 1, Eq. 1)
+
+
+def _rand_qkv(T, H, dh, seed):
+    r = np.random.default_rng(seed)
+    return tuple(r.standard_normal((T, H * dh)) for _ in range(3))
+
+
+@pytest.mark.parametrize("lens", [[7], [1, 33, 5], [64, 64]])
+def test_sa_equals_torch_scaled_dot_product_attention(lens):
+    """Eq. 1 per sequence equals the library's scaled-dot-product attention
+    (torch, fp64, no mask, scale 1/sqrt(d_h)), head by head."""
+    H, dh = 2, 16
+    T = sum(lens)
+    q, k, v = _rand_qkv(T, H, dh, 31)
+    st, ln = oracle.seqs(cu_seqlens=np.concatenate([[0], np.cumsum(lens)]).tolist())
+    o, lse = oracle.sa_forward(q, k, v, st, ln, H, dh)
+    for s, n in zip(st, ln):
+        for h in range(H):
+            sl = slice(h * dh, (h + 1) * dh)
+            t = lambda a: torch.tensor(a[s:s + n, sl])[None, None]
+            ref = F.scaled_dot_product_attention(t(q), t(k), t(v))[0, 0].numpy()
+            np.testing.assert_allclose(o[s:s + n, sl], ref, rtol=1e-12, atol=1e-12)
+            scores = t(q)[0, 0] @ t(k)[0, 0].T / np.sqrt(dh)
+            np.testing.assert_allclose(lse[s:s + n, h], torch.logsumexp(scores, dim=1).numpy(), rtol=1e-12)
+
+
+def test_sa_single_key_and_identical_keys():
+    """One key: the weight is 1, o = v.  Identical keys: equal weights, o is
+    the mean of the values of the sequence."""
+    q, k, v = _rand_qkv(13, 2, 8, 32)
+    st, ln = oracle.seqs(cu_seqlens=[0, 1, 13])
+    kk = k.copy()
+    kk[1:13] = kk[1]
+    o, _ = oracle.sa_forward(q, kk, v, st, ln, 2, 8)
+    np.testing.assert_allclose(o[0], v[0], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(o[1:13], np.broadcast_to(v[1:13].mean(axis=0), (12, 16)), rtol=1e-12, atol=1e-12)
+
+
+def test_sa_hard_limit_selects_the_best_key():
+    """Scaling the queries up makes the weights one-hot on each query's
+    largest score: o_i tends to v of that key (checked at a large scale)."""
+    q, k, v = _rand_qkv(20, 1, 8, 33)
+    st, ln = oracle.seqs(1, 20)
+    o, _ = oracle.sa_forward(q * 1e4, k, v, st, ln, 1, 8)
+    best = np.argmax(q @ k.T, axis=1)
+    np.testing.assert_allclose(o, v[best], rtol=0, atol=1e-9)
+
+
+def test_sa_key_permutation_convexity_and_independence():
+    """Permuting the keys and values of a sequence together leaves o unchanged;
+    each output coordinate lies between the sequence's smallest and largest
+    value coordinate; a packed sequence equals itself alone."""
+    q, k, v = _rand_qkv(50, 2, 8, 34)
+    st, ln = oracle.seqs(cu_seqlens=[0, 20, 50])
+    o, _ = oracle.sa_forward(q, k, v, st, ln, 2, 8)
+    perm = np.concatenate([np.random.default_rng(35).permutation(20), 20 + np.random.default_rng(36).permutation(30)])
+    o2, _ = oracle.sa_forward(q, k[perm], v[perm], st, ln, 2, 8)
+    np.testing.assert_allclose(o2, o, rtol=1e-12, atol=1e-12)
+    for s, n in zip(st, ln):
+        assert (o[s:s + n] <= v[s:s + n].max(axis=0) + 1e-12).all()
+        assert (o[s:s + n] >= v[s:s + n].min(axis=0) - 1e-12).all()
+    st1, ln1 = oracle.seqs(1, 30)
+    o3, _ = oracle.sa_forward(q[20:], k[20:], v[20:], st1, ln1, 2, 8)
+    np.testing.assert_allclose(o3, o[20:], rtol=1e-13, atol=1e-13)
