@@ -147,6 +147,12 @@ struct Layout {
   size_t total;
 };
 
+// 256-query blocks (per sequence) of the softmax attention.
+constexpr int kSaBlock = 256;
+int sa_blocks(const Plan& p) {
+  return p.mode == SEQ_VARLEN ? cdiv(p.T, kSaBlock) + p.n_seq : cdiv(p.L, kSaBlock) * p.n_seq;
+}
+
 // Chunks (128 rows, per sequence) of the decay core.
 int decay_chunks(const Plan& p) {
   return p.mode == SEQ_VARLEN ? cdiv(p.T, kDecayChunk) + p.n_seq : cdiv(p.L, kDecayChunk) * p.n_seq;
@@ -196,8 +202,10 @@ Layout ws_layout(const Plan& p, int op) {
     l.pre_c = c.take((size_t)(p.n_seq + 1) * 4);
     l.pre_t = c.take((size_t)(p.n_seq + 1) * 4);
   }
-  l.partial = c.take((size_t)partial_slots(p) * p.dh * state_ld(p.dh) * 4);
-  l.partial_m = c.take((size_t)p.n_chunks * p.H * 4);
+  if (op != GBLA_OP_SA_FORWARD) {  // split-L partial states (every kernel but the softmax attention)
+    l.partial = c.take((size_t)partial_slots(p) * p.dh * state_ld(p.dh) * 4);
+    l.partial_m = c.take((size_t)p.n_chunks * p.H * 4);
+  }
   if (op == GBLA_OP_FORWARD) {  // inference forward keeps its activations here
     l.state = c.take(state_bytes(p));
     l.state_bf = c.take(state_bf_bytes(p));
@@ -218,6 +226,8 @@ Layout ws_layout(const Plan& p, int op) {
     // db_g partial rows: two per tile (tcgen05 kernel) or one per chunk
     l.bg_part = c.take((size_t)std::max(2 * p.n_tiles, p.n_chunks) * p.H * 4);
     l.conv_part = c.take((size_t)p.conv_blocks * p.d * 5 * 4);
+  } else if (op == GBLA_OP_SA_FORWARD) {
+    if (p.mode == SEQ_VARLEN) l.pre_d = c.take((size_t)(p.n_seq + 1) * 4);
   } else if (op == GBLA_OP_DECAY_FORWARD) {
     const size_t ch = (size_t)decay_chunks(p) * p.H;
     if (p.mode == SEQ_VARLEN) l.pre_d = c.take((size_t)(p.n_seq + 1) * 4);
@@ -512,7 +522,7 @@ gbla_status gbla_validate_shape(const gbla_shape* shape) {
 size_t gbla_workspace_size(const gbla_shape* shape, int op) {
   Plan p;
   if (make_plan(shape, p) != GBLA_OK) return 0;
-  if (op < GBLA_OP_FORWARD || op > GBLA_OP_DECAY_FORWARD) return 0;
+  if (op < GBLA_OP_FORWARD || op > GBLA_OP_SA_FORWARD) return 0;
   return ws_layout(p, op).total;
 }
 
@@ -811,6 +821,32 @@ gbla_status bla_decay_core_forward(const gbla_shape* shape, const void* q, const
   GBLA_CHECK(launch_decay_states(a, decay_chunks(p), c.st), "decay states[mma]");
   GBLA_CHECK(launch_decay_scan(a, p.n_seq, c.st), "decay scan");
   GBLA_CHECK(launch_decay_out(a, decay_chunks(p), c.st), "decay out[mma]");
+  return GBLA_OK;
+}
+
+gbla_status sa_core_forward(const gbla_shape* shape, const void* q, const void* k, const void* v, void* o, void* ws,
+                            size_t ws_bytes, void* stream) {
+  for (const void* ptr : {q, k, v, (const void*)o})
+    if (!ptr || !aligned16(ptr)) return GBLA_ERR_INVALID_ARG;
+  Plan p0;
+  gbla_status r = make_plan(shape, p0);
+  if (r != GBLA_OK) return r;
+  if (p0.f32 || p0.dh != 64) return GBLA_ERR_UNSUPPORTED;
+  Ctx c;
+  if ((r = begin(shape, GBLA_OP_SA_FORWARD, ws, ws_bytes, stream, c)) != GBLA_OK) return r;
+  const Plan& p = c.p;
+  SaArgs a{};
+  a.q = q; a.k = k; a.v = v; a.o = o; a.ld = p.HD;
+  a.H = p.H; a.dh = p.dh; a.seq = c.seq; a.err = c.kerr; a.err_out = c.err;
+  a.tiles.tile = kSaBlock;
+  a.tiles.per_seq = p.mode == SEQ_VARLEN ? 0 : cdiv(p.L, kSaBlock);
+  a.tiles.prefix = p.mode == SEQ_VARLEN ? at<int32_t>(ws, c.l.pre_d) : nullptr;
+  if (p.mode == SEQ_VARLEN) {
+    const int ts[1] = {kSaBlock};
+    int32_t* pre[1] = {at<int32_t>(ws, c.l.pre_d)};
+    GBLA_CHECK(launch_plan(c.seq, 1, ts, pre, c.err, c.st), "plan");
+  }
+  GBLA_CHECK(launch_sa_fwd_tc(a, sa_blocks(p), c.st), "sa[tc]");
   return GBLA_OK;
 }
 

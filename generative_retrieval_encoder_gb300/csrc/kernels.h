@@ -89,6 +89,17 @@ struct BwdQArgs {
   int* err_out;                     // tcgen05 kernel: timeout bit of the workspace error word
 };
 
+// Bidirectional softmax attention (Eq. 1), the SA blocks of the hybrid encoder.
+struct SaArgs {
+  const void* q; const void* k; const void* v;  // [T, ld] bf16; head h at columns h*dh
+  void* o;                                      // [T, ld] bf16
+  int64_t ld;
+  int H, dh;
+  SeqDesc seq; Tiling tiles;                    // tiles of 256 queries (two MMA tiles)
+  const int* err;
+  int* err_out;                                 // timeout bit of the workspace error word
+};
+
 struct BwdKVArgs {
   int pre;                          // k holds phi(k)
   const void* k; int64_t ldk;
@@ -188,6 +199,10 @@ cudaError_t launch_readout_core_tc(const ReadoutArgs& a, int n_tiles, cudaStream
 // cudaErrorNotSupported otherwise.
 cudaError_t launch_bwd_kv_tc(const BwdKVArgs& a, int n_tiles, int* nparts, cudaStream_t st);
 cudaError_t launch_bwd_kv_bf16(const BwdKVArgs& a, int grid_x, cudaStream_t st);
+// tcgen05 softmax attention forward (sa_tc.cu): bf16, d_h = 64, one CTA per
+// (256-query block, head), n_blocks blocks (past the last: nothing).
+// cudaErrorNotSupported otherwise.
+cudaError_t launch_sa_fwd_tc(const SaArgs& a, int n_blocks, cudaStream_t st);
 
 cudaError_t launch_reduce_f32(const ReduceArgs& a, int grid_x, cudaStream_t st);
 cudaError_t launch_readout_f32(const ReadoutArgs& a, bool norm, int grid_x, cudaStream_t st);

@@ -22,12 +22,13 @@ GBLA_POLICY_AUTO, GBLA_POLICY_TC, GBLA_POLICY_MMA = 0, 1, 2
 GBLA_F32, GBLA_BF16 = 0, 1
 GBLA_GATE_SIGMOID, GBLA_GATE_SOFTMAX = 0, 1
 GBLA_OP_FORWARD, GBLA_OP_BACKWARD, GBLA_OP_CORE_FORWARD, GBLA_OP_CORE_BACKWARD, GBLA_OP_DECAY_FORWARD = 0, 1, 2, 3, 4
+GBLA_OP_SA_FORWARD = 5
 
 EXPORTS = ("gbla_workspace_size", "gbla_saved_size", "gbla_validate_shape", "gbla_forward", "gbla_backward",
            "bla_core_forward", "bla_core_backward", "gbla_check_device_status", "gbla_status_string",
            "gbla_last_error", "gbla_version", "gbla_profiling_enable", "gbla_profiling_read",
            "bla_core_forward_noalloc", "bla_core_noalloc_check_device_status", "gbla_diag_bounded_wait",
-           "gbla_set_kernel_policy", "bla_decay_core_forward")
+           "gbla_set_kernel_policy", "bla_decay_core_forward", "sa_core_forward")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -75,6 +76,8 @@ def lib() -> ctypes.CDLL:
         L.bla_core_backward.restype = ctypes.c_int
         L.bla_decay_core_forward.argtypes = [sp] + [vp] * 8 + [sz, vp]
         L.bla_decay_core_forward.restype = ctypes.c_int
+        L.sa_core_forward.argtypes = [sp] + [vp] * 5 + [sz, vp]
+        L.sa_core_forward.restype = ctypes.c_int
         L.bla_core_forward_noalloc.argtypes = [sp] + [vp] * 8
         L.bla_core_forward_noalloc.restype = ctypes.c_int
         L.bla_core_noalloc_check_device_status.argtypes = [vp]
@@ -241,6 +244,18 @@ def bla_decay_core_forward(shape: Shape, q, k, v, g, lam, o=None, den=None, ws=N
                                       _stream())
     _check(st, "bla_decay_core_forward")
     return o, den
+
+
+def sa_core_forward(shape: Shape, q, k, v, o=None, ws=None):
+    """The bidirectional softmax attention of the SA blocks (Eq. 1, see gbla.h): returns o."""
+    if o is None:
+        o = torch.empty_like(q)
+    if ws is None:
+        ws = workspace(shape, GBLA_OP_SA_FORWARD, q.device)
+    st = lib().sa_core_forward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(ws), ws.numel(),
+                               _stream())
+    _check(st, "sa_core_forward")
+    return o
 
 
 def bla_core_forward_noalloc(shape: Shape, q, k, v, g, o, den=None, state=None) -> int:

@@ -84,7 +84,8 @@ typedef enum {
   GBLA_OP_BACKWARD = 1,       /* gbla_backward                               */
   GBLA_OP_CORE_FORWARD = 2,   /* bla_core_forward                            */
   GBLA_OP_CORE_BACKWARD = 3,  /* bla_core_backward                           */
-  GBLA_OP_DECAY_FORWARD = 4   /* bla_decay_core_forward                      */
+  GBLA_OP_DECAY_FORWARD = 4,  /* bla_decay_core_forward                      */
+  GBLA_OP_SA_FORWARD = 5      /* sa_core_forward                             */
 } gbla_op;
 
 typedef struct {
@@ -203,6 +204,25 @@ gbla_status bla_decay_core_forward(const gbla_shape* shape, const void* q,
                                    const void* k, const void* v, const float* g,
                                    const float* lam, void* o, float* den,
                                    void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The attention of the SA blocks of the hybrid [SA, LA, LA] encoder: the
+ * bidirectional softmax attention of Eq. 1 ("Gated Bidirectional Linear
+ * Attention for Generative Retrieval", Core method 1; the hybrid encoder
+ * interleaves one such block with two GBLA blocks):
+ *   o_i = sum_j exp(q_i . k_j / sqrt(d_h)) v_j / sum_j exp(q_i . k_j / sqrt(d_h))
+ * over every key j of query i's sequence, per head (no mask: both
+ * directions).  Quadratic in the sequence length: the baseline the pages
+ * compare GBLA with (Table 5, single-layer latency).
+ *   q, k, v, o (bf16) [rows, H*d_h], head h at columns h*d_h .. h*d_h+d_h-1.
+ *   Rows of a padded slot past its sequence get o = 0.
+ *   bf16 I/O and d_h = 64 only (GBLA_ERR_UNSUPPORTED otherwise).  Workspace:
+ *   gbla_workspace_size(shape, GBLA_OP_SA_FORWARD).  The shape's d, gate and
+ *   rms_eps are ignored.
+ */
+gbla_status sa_core_forward(const gbla_shape* shape, const void* q,
+                            const void* k, const void* v, void* o, void* ws,
+                            size_t ws_bytes, void* stream);
 
 /*
  * bla_core_forward without a caller workspace (the pages have no counterpart:
