@@ -9,9 +9,10 @@
 // and b that share every key and value tile of the sequence.  Per key tile
 // j (128 keys):
 //   S_t = Q_t K_j^T                  tcgen05 -> TMEM (128 columns per tile t)
-//   softmax (one thread per query row, running maximum m and sum l in the
-//   log2 domain): P_t = 2^(S_t log2(e)/sqrt(d_h) - m) in bf16 into shared memory,
-//   the accumulator rescaled by 2^(m_old - m_new) when the maximum moved
+//   softmax (one thread per query row, a reference m of the exponentials and
+//   the sum l in the log2 domain): P_t = 2^(S_t log2(e)/sqrt(d_h) - m) in bf16
+//   into shared memory; m moves (and the accumulator is rescaled by
+//   2^(m_old - m_new)) only when the row's maximum passes m by more than 8
 //   O_t += P_t V_j                   tcgen05 -> TMEM (64 columns per tile t)
 // and o = O / l at the end.  Roles: a producer warp (TMA: the two Q tiles,
 // then K_j and V_j through a 3-stage ring), an MMA warp that alternates the
@@ -219,10 +220,14 @@ __global__ void __launch_bounds__(NTH, 1)
     const int i = wq * 32 + lane;            // row of the tile = TMEM lane
     const uint32_t lrow = (uint32_t)(wq * 32) << 16;
     const float sl2 = 1.4426950408889634f / 8.f;  // log2(e) / sqrt(d_h)
-    float m = -INFINITY, l = 0.f;                 // running maximum (log2 domain) and sum
+    // m: the reference of the exponentials (log2 domain), moved only when the
+    // row's maximum exceeds it by more than 8, so that most key tiles need no
+    // rescale of O; the weights then stay below 2^8, well inside bf16 and fp32.
+    float m = -INFINITY, l = 0.f;
     uint8_t* pt = smem + O_P + t * 2 * TILE;
     for (int j = 0; j < nk; ++j) {
-      const int kv = u.len - j * BK;  // valid keys of this tile (>= 1)
+      const int kv = u.len - j * BK;  // valid keys of this tile (>= 1; >= BK but for the last)
+      const bool full = kv >= BK;
       mbar_wait(SFULL(t), j & 1, fail);
       tc_fence_after();
       // pass 1: the row's maximum over the valid keys
@@ -231,18 +236,25 @@ __global__ void __launch_bounds__(NTH, 1)
       for (int c4 = 0; c4 < BK / 32; ++c4) {
         uint32_t sv[32];
         tmem_ld32(tS(t) + lrow + 32 * c4, sv);
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (32 * c4 + c < kv) mx = fmaxf(mx, __uint_as_float(sv[c]));
+          for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (32 * c4 + c < kv) mx = fmaxf(mx, __uint_as_float(sv[c]));
+        }
       }
-      const float mnew = fmaxf(m, mx * sl2);
-      const float alpha = ex2(m - mnew);  // 0 on the first tile (m = -inf)
+      const float mt = mx * sl2;
+      const bool move = mt > m + 8.f;  // always on the first tile (m = -inf)
+      const float mnew = move ? mt : m;
+      const float alpha = ex2(m - mnew);  // 0 on the first tile, 1 when m stays
       m = mnew;
       // the accumulator and P_t are free once PV_t of the previous tile is done
       if (j > 0) {
         mbar_wait(OREADY(t), (j - 1) & 1, fail);
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {  // rescale O_t by 2^(m_old - m_new)
+        if (__any_sync(0xffffffffu, move)) {  // rescale O_t by 2^(m_old - m_new)
 #pragma unroll
           for (int c2 = 0; c2 < D / 32; ++c2) {
             uint32_t ov[32];
@@ -266,10 +278,14 @@ __global__ void __launch_bounds__(NTH, 1)
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
             const int c = 8 * c8 + e, key = 32 * c4 + c;
-            const float p0 = key < kv ? ex2(fmaf(__uint_as_float(sv[c]), sl2, -m)) : 0.f;
-            const float p1 = key + 1 < kv ? ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, -m)) : 0.f;
+            float p0 = ex2(fmaf(__uint_as_float(sv[c]), sl2, -m));
+            float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, -m));
+            if (!full) {
+              p0 = key < kv ? p0 : 0.f;
+              p1 = key + 1 < kv ? p1 : 0.f;
+            }
+            ps += p0 + p1;
             w[e / 2] = pack_bf16(p0, p1);
-            ps += bf_lo(w[e / 2]) + bf_hi(w[e / 2]);  // the rounded weights the MMA multiplies with
           }
           const int chunk = 4 * c4 + c8;  // 16-byte chunk of the row's 128 keys
           *reinterpret_cast<uint4*>(pt + (chunk >> 3) * TILE + swz_off(i, chunk & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
