@@ -252,6 +252,48 @@ def l_scaling(wl, dev, timed, tokens: int = 262144, steps: int = 3):
     return out
 
 
+def sa_vs_gbla(wl, dev, timed, flush, peaks, B: int = 8, steps: int = 3):
+    """Single-layer forward latency at batch 8 and L = 2k .. 32k (the pages'
+    Table 5 setting): the SA blocks' softmax attention (sa_core_forward, Eq. 1;
+    TFLOP/s on 4 B H L^2 d_h flops), the GBLA core (bla_core_forward) and the
+    whole GBLA layer forward (gbla_forward, inference: no saved activations),
+    with the ratio SA / GBLA layer."""
+    import torch
+    from generative_retrieval_encoder_gb300 import gbla
+    from generative_retrieval_encoder_gb300.workloads import Workload
+    out = {"B": B, "H": wl.H, "d_h": wl.dh, "d": wl.d, "by_L": {}}
+    for L in (2048, 4096, 8192, 16384, 32768):
+        w = Workload(f"latency L={L}", B, L, wl.d, wl.H, wl.dh, pattern=True, seed=1004)
+        shape, x_h, _, P = make_inputs(w, dev)
+        x = x_h.to(dev)
+        T = B * L
+        r = torch.Generator().manual_seed(1005)
+        q, k, v = (torch.randn(T, w.H * w.dh, generator=r).to(torch.bfloat16).to(dev) for _ in range(3))
+        g = (torch.rand(T, w.H, generator=r) * 0.98 + 0.01).to(dev)
+        o = torch.empty_like(q)
+        y = torch.empty(T, w.H * w.dh, dtype=x.dtype, device=dev)
+        ws_s = gbla.workspace(shape, gbla.GBLA_OP_SA_FORWARD, dev)
+        ws_c = gbla.workspace(shape, gbla.GBLA_OP_CORE_FORWARD, dev)
+        ws_f = gbla.workspace(shape, gbla.GBLA_OP_FORWARD, dev)
+        fns = {"sa_ms": lambda: gbla.sa_core_forward(shape, q, k, v, o=o, ws=ws_s),
+               "gbla_core_ms": lambda: gbla.bla_core_forward(shape, q, k, v, g, o=o, ws=ws_c),
+               "gbla_layer_ms": lambda: gbla.gbla_forward(shape, x, P, y=y, ws=ws_f)}
+        e = {}
+        for name, fn in fns.items():
+            for _ in range(2):
+                fn()
+            torch.cuda.synchronize()
+            e[name] = round(timed(fn, steps), 4)
+        fl = 4.0 * B * w.H * L * L * w.dh
+        e["sa_tflops"] = round(fl / (e["sa_ms"] * 1e-3) / 1e12, 1)
+        e["sa_frac_of_bf16"] = round(e["sa_tflops"] / peaks["bf16_tflops_sustained"], 3)
+        e["sa_over_gbla_layer"] = round(e["sa_ms"] / e["gbla_layer_ms"], 2)
+        out["by_L"][L] = e
+        del x, q, k, v, g, o, y, ws_s, ws_c, ws_f
+        torch.cuda.empty_cache()
+    return out
+
+
 def profile(fn, flush, reps: int = 3):
     """Per-launch times (library CUDA events on the launching stream) of fn,
     averaged over reps runs: ({step name: ms}, {step name: kernel variant})."""
@@ -327,7 +369,8 @@ def core_lines(wl, dev, timed, flush, peaks, steps: int = 10):
     tokens and heads: tokens/s and HBM rate on their algorithmic bytes per
     token-head (core forward 8 d_h + 4: q, k, v, g in, o out; backward
     14 d_h + 8: q, k, v, g, do in, dq, dk, dv, dg out; decay forward
-    8 d_h + 8: q, k, v, g, lambda in, o out)."""
+    8 d_h + 8: q, k, v, g, lambda in, o out); and the SA blocks' softmax
+    attention (sa_core_forward) with its tensor rate."""
     import torch
     from generative_retrieval_encoder_gb300 import gbla
     B, L, H, dh = wl.B, wl.L, wl.H, wl.dh
@@ -341,10 +384,12 @@ def core_lines(wl, dev, timed, flush, peaks, steps: int = 10):
     ws_f = gbla.workspace(shape, gbla.GBLA_OP_CORE_FORWARD, dev)
     ws_b = gbla.workspace(shape, gbla.GBLA_OP_CORE_BACKWARD, dev)
     ws_d = gbla.workspace(shape, gbla.GBLA_OP_DECAY_FORWARD, dev)
+    ws_s = gbla.workspace(shape, gbla.GBLA_OP_SA_FORWARD, dev)
     fwd = lambda: gbla.bla_core_forward(shape, q, k, v, g, o=o, ws=ws_f)
     bwd = lambda: gbla.bla_core_backward(shape, q, k, v, g, d_o, ws=ws_b)
     dec = lambda: gbla.bla_decay_core_forward(shape, q, k, v, g, lam, o=o, ws=ws_d)
-    for fn in (fwd, bwd, dec):
+    sa = lambda: gbla.sa_core_forward(shape, q, k, v, o=o, ws=ws_s)
+    for fn in (fwd, bwd, dec, sa):
         for _ in range(3):
             fn()
     torch.cuda.synchronize()
@@ -359,7 +404,12 @@ def core_lines(wl, dev, timed, flush, peaks, steps: int = 10):
                      "frac": round(th * per_th / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3),
                      "kernels": {n: roof_entry(n, t, None, None, peaks, variant.get(n))
                                  for n, t in sorted(kern.items(), key=lambda kv: -kv[1]) if n != "memset"}}
-    del q, k, v, d_o, g, lam, o, ws_f, ws_b, ws_d
+    ms = timed(sa, steps)  # the SA blocks' softmax attention (Eq. 1): tensor-bound, 4 B H L^2 d_h flops
+    fl = 4.0 * B * H * L * L * dh
+    out["sa_forward"] = {"ms": round(ms, 4), "tokens_per_s": T / (ms * 1e-3), "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+                         "frac": round(fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"], 3),
+                         "peak": "measured (cuBLAS bf16, sustained)"}
+    del q, k, v, d_o, g, lam, o, ws_f, ws_b, ws_d, ws_s
     torch.cuda.empty_cache()
     return out
 
@@ -535,6 +585,7 @@ def run_ours(args, wl, rank: int, world: int, local_rank: int):
     peaks, peak_src = load_peaks()
     extra = other_workloads(dev, timed, flush, peaks) if args.scaling and wl.name == workloads()["train2k"].name else None
     core = core_lines(wl, dev, timed, flush, peaks) if wl.dh == 64 and wl.dtype == "bf16" and wl.lengths() is None else None
+    sa_lat = sa_vs_gbla(wl, dev, timed, flush, peaks) if args.scaling and wl.name == workloads()["train2k"].name else None
 
     if rank != 0:
         return
@@ -585,7 +636,8 @@ def run_ours(args, wl, rank: int, world: int, local_rank: int):
             "clocks": clk.summary(),
             "l_scaling": scaling,
             "other_workloads": extra,
-            "cores": core}
+            "cores": core,
+            "sa_vs_gbla": sa_lat}
     print(json.dumps(line), flush=True)
 
 
