@@ -15,10 +15,10 @@
 //   2^(m_old - m_new)) only when the row's maximum passes m by more than 8
 //   O_t += P_t V_j                   tcgen05 -> TMEM (64 columns per tile t)
 // and o = O / l at the end.  Roles: a producer warp (TMA: the two Q tiles,
-// then K_j and V_j through a 3-stage ring), an MMA warp that alternates the
-// two tiles (PV_a(j), S_a(j+1), PV_b(j), S_b(j+1): the tensor cores work on
-// one tile while the other tile's softmax runs), and two groups of four
-// softmax warps (tile a, tile b).  Keys past the end of the sequence are
+// then K_j and V_j through a 3-stage ring), an MMA warp (S_a(j+1), S_b(j+1)
+// as soon as the softmax holds S(j) in registers, then PV_a(j), PV_b(j): the
+// tensor cores compute the next scores while the softmax of the current ones
+// runs), and two groups of four softmax warps (tile a, tile b).  Keys past the end of the sequence are
 // masked; queries past it are computed but not stored, and rows of a padded
 // slot past the sequence receive zeros.
 //
@@ -192,22 +192,24 @@ __global__ void __launch_bounds__(NTH, 1)
         issue_s(1, 0);
       }
       for (int j = 0; j < nk && ok; ++j) {
-        const bool more = j + 1 < nk;
-        for (int t = 0; t < 2 && ok; ++t) {
-          ok = mbar_wait(PFULL(t), j & 1, fail);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(t, j);
-          if (t == 1) tc_commit(KVEMPTY(j % KST));  // every MMA on stage j % KST is issued
-          if (more) {
-            // S_t of the next key tile, once the softmax has read this one
-            ok = (t == 1 || mbar_wait(KVFULL((j + 1) % KST), ((j + 1) / KST) & 1, fail)) &&
-                 mbar_wait(SFREE(t), j & 1, fail);
+        // S_t of the next key tile as soon as the softmax holds this one in
+        // registers, then PV_t of this tile once its P is written
+        if (j + 1 < nk) {
+          ok = mbar_wait(KVFULL((j + 1) % KST), ((j + 1) / KST) & 1, fail);
+          for (int t = 0; t < 2 && ok; ++t) {
+            ok = mbar_wait(SFREE(t), j & 1, fail);
             if (!ok) break;
             tc_fence_after();
             issue_s(t, j + 1);
           }
         }
+        for (int t = 0; t < 2 && ok; ++t) {
+          ok = mbar_wait(PFULL(t), j & 1, fail);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, j);
+        }
+        if (ok) tc_commit(KVEMPTY(j % KST));  // every MMA on stage j % KST is issued
       }
       // every MMA issued above has finished once the last OREADY completes
       for (int t = 0; t < 2; ++t)
@@ -230,19 +232,27 @@ __global__ void __launch_bounds__(NTH, 1)
       const bool full = kv >= BK;
       mbar_wait(SFULL(t), j & 1, fail);
       tc_fence_after();
-      // pass 1: the row's maximum over the valid keys
+      // the row's 128 scores into registers, one wait; S_t is then free for the next tile
+      uint32_t sv[BK / 32][32];
+#pragma unroll
+      for (int c4 = 0; c4 < BK / 32; ++c4) tmem_ld32_async(tS(t) + lrow + 32 * c4, sv[c4]);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+      for (int c4 = 0; c4 < BK / 32; ++c4) tmem_tie32(sv[c4]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(SFREE(t));
+      // the row's maximum over the valid keys
       float mx = -INFINITY;
 #pragma unroll
       for (int c4 = 0; c4 < BK / 32; ++c4) {
-        uint32_t sv[32];
-        tmem_ld32(tS(t) + lrow + 32 * c4, sv);
         if (full) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
+          for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(sv[c4][c]));
         } else {
 #pragma unroll
           for (int c = 0; c < 32; ++c)
-            if (32 * c4 + c < kv) mx = fmaxf(mx, __uint_as_float(sv[c]));
+            if (32 * c4 + c < kv) mx = fmaxf(mx, __uint_as_float(sv[c4][c]));
         }
       }
       const float mt = mx * sl2;
@@ -266,20 +276,18 @@ __global__ void __launch_bounds__(NTH, 1)
           tmem_st_wait();
         }
       }
-      // pass 2: P = 2^(s log2(e)/sqrt(d_h) - m) in bf16, and its sum
+      // P = 2^(s log2(e)/sqrt(d_h) - m) in bf16, and its sum
       float ps = 0.f;
 #pragma unroll
       for (int c4 = 0; c4 < BK / 32; ++c4) {
-        uint32_t sv[32];
-        tmem_ld32(tS(t) + lrow + 32 * c4, sv);
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8) {
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
             const int c = 8 * c8 + e, key = 32 * c4 + c;
-            float p0 = ex2(fmaf(__uint_as_float(sv[c]), sl2, -m));
-            float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, -m));
+            float p0 = ex2(fmaf(__uint_as_float(sv[c4][c]), sl2, -m));
+            float p1 = ex2(fmaf(__uint_as_float(sv[c4][c + 1]), sl2, -m));
             if (!full) {
               p0 = key < kv ? p0 : 0.f;
               p1 = key + 1 < kv ? p1 : 0.f;
@@ -295,10 +303,7 @@ __global__ void __launch_bounds__(NTH, 1)
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(SFREE(t));
-        mbar_arrive(PFULL(t));
-      }
+      if (lane == 0) mbar_arrive(PFULL(t));
     }
     // o = O / l, staged over the tile's Q rows (every S_t has been computed), stored as whole lines
     mbar_wait(OREADY(t), (nk - 1) & 1, fail);
