@@ -13,8 +13,10 @@
 //   the sum l in the log2 domain): P_t = 2^(S_t log2(e)/sqrt(d_h) - m) in bf16
 //   into shared memory; m moves (and the accumulator is rescaled by
 //   2^(m_old - m_new)) only when the row's maximum passes m by more than 8
-//   O_t += P_t V_j                   tcgen05 -> TMEM (64 columns per tile t)
-// and o = O / l at the end.  Roles: a producer warp (TMA: the two Q tiles,
+//   [O_t | l_t] += P_t [V_j | 1]     tcgen05 -> TMEM (80 columns per tile t)
+// and o = O / l at the end: the sum l accumulates on the tensor cores from
+// the same bf16 weights as the numerator (a constant block with a column of
+// ones is B's second atom).  Roles: a producer warp (TMA: the two Q tiles,
 // then K_j and V_j through a 3-stage ring), an MMA warp (S_a(j+1), S_b(j+1)
 // as soon as the softmax holds S(j) in registers, then PV_a(j), PV_b(j): the
 // tensor cores compute the next scores while the softmax of the current ones
@@ -40,13 +42,15 @@ constexpr int KST = 3;                // K / V ring stages
 constexpr int O_Q = 0;                          // Q_a | Q_b
 constexpr int O_KV = O_Q + 2 * TILE;            // KST x (K | V)
 constexpr int O_P = O_KV + KST * 2 * TILE;      // P_a | P_b, each two 64-key atoms
-constexpr int O_BAR = O_P + 2 * 2 * TILE;
+constexpr int O_ONE = O_P + 2 * 2 * TILE;      // [128 key rows][64]: 1 in column 0, the sum column of PV
+constexpr int O_BAR = O_ONE + TILE;
 // qfull, kvfull[KST], kvempty[KST], sfull[2], sfree[2], pfull[2], oready[2]
 constexpr int NBAR = 1 + 2 * KST + 8;
 constexpr int O_SLOT = O_BAR + 8 * NBAR;
 constexpr int O_FAIL = O_SLOT + 4;
 constexpr int SMEM = O_FAIL + 4 + 1024;         // + alignment slack
-constexpr int TMEM_COLS = 512;                  // S_a | S_b | O_a | O_b (128 + 128 + 64 + 64)
+constexpr int ON = D + 16;                      // PV's N: the 64 value columns and the sum column (+ pad)
+constexpr int TMEM_COLS = 512;                  // S_a | S_b | O_a | O_b (128 + 128 + 80 + 80)
 constexpr int NSW = 8;                          // softmax warps (4 a tile)
 constexpr int NTH = (NSW + 2) * 32;
 static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -128,12 +132,19 @@ __global__ void __launch_bounds__(NTH, 1)
     *fail = 0;
   }
   if (warp == NSW + 1) tmem_alloc(smem_u32(slot), TMEM_COLS);
+  // the ones block: bf16 1.0 in column 0 of each row (its swizzled chunk), 0 elsewhere
+  for (int idx = tid; idx < 128 * 8; idx += NTH) {
+    const int r = idx >> 3, c = idx & 7;
+    *reinterpret_cast<uint4*>(smem + O_ONE + r * 128 + c * 16) =
+        make_uint4(c == (r & 7) ? 0x3F80u : 0u, 0u, 0u, 0u);
+  }
+  fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *slot;
   auto tS = [&](int t) { return tmem + 128 * t; };
-  auto tO = [&](int t) { return tmem + 256 + 64 * t; };
+  auto tO = [&](int t) { return tmem + 256 + ON * t; };
   auto sQ = [&](int t) { return sbase + O_Q + t * TILE; };
   auto sK = [&](int s) { return sbase + O_KV + s * 2 * TILE; };
   auto sV = [&](int s) { return sbase + O_KV + s * 2 * TILE + TILE; };
@@ -167,7 +178,7 @@ __global__ void __launch_bounds__(NTH, 1)
   } else if (warp == NSW + 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16(BQ, BK, false, false), id_o = idesc_bf16(BQ, D, false, true);
+      const uint32_t id_s = idesc_bf16(BQ, BK, false, false), id_o = idesc_bf16(BQ, ON, false, true);
       // S_t = Q_t K_j^T: K = d_h.  A = Q_t K-major (+32 B per 16 features); B = K_j K-major (rows = keys).
       auto issue_s = [&](int t, int j) {
         const int s = j % KST;
@@ -176,12 +187,14 @@ __global__ void __launch_bounds__(NTH, 1)
           tc_mma(tS(t), sdesc(sQ(t) + 32 * kk, 16, 1024), sdesc(sK(s) + 32 * kk, 16, 1024), id_s, kk > 0);
         tc_commit(SFULL(t));
       };
-      // O_t += P_t V_j: K = keys.  A = P_t K-major (two 64-key atoms); B = V_j N-major (16 key rows = 2048 B).
+      // [O_t | l_t] += P_t [V_j | 1]: K = keys.  A = P_t K-major (two 64-key atoms); B N-major
+      // (16 key rows = 2048 B), its second 64-column atom the ones block (LBO apart).
       auto issue_pv = [&](int t, int j) {
         const int s = j % KST;
+        const uint32_t lbo = sbase + O_ONE - sV(s);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          tc_mma(tO(t), sdesc(sP(t) + (kk >> 2) * TILE + 32 * (kk & 3), 16, 1024), sdesc(sV(s) + 2048 * kk, 8192, 1024),
+          tc_mma(tO(t), sdesc(sP(t) + (kk >> 2) * TILE + 32 * (kk & 3), 16, 1024), sdesc(sV(s) + 2048 * kk, lbo, 1024),
                  id_o, (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(OREADY(t));
       };
@@ -225,7 +238,7 @@ __global__ void __launch_bounds__(NTH, 1)
     // m: the reference of the exponentials (log2 domain), moved only when the
     // row's maximum exceeds it by more than 8, so that most key tiles need no
     // rescale of O; the weights then stay below 2^8, well inside bf16 and fp32.
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY;
     uint8_t* pt = smem + O_P + t * 2 * TILE;
     for (int j = 0; j < nk; ++j) {
       const int kv = u.len - j * BK;  // valid keys of this tile (>= 1; >= BK but for the last)
@@ -264,7 +277,7 @@ __global__ void __launch_bounds__(NTH, 1)
       if (j > 0) {
         mbar_wait(OREADY(t), (j - 1) & 1, fail);
         tc_fence_after();
-        if (__any_sync(0xffffffffu, move)) {  // rescale O_t by 2^(m_old - m_new)
+        if (__any_sync(0xffffffffu, move)) {  // rescale [O_t | l_t] by 2^(m_old - m_new)
 #pragma unroll
           for (int c2 = 0; c2 < D / 32; ++c2) {
             uint32_t ov[32];
@@ -273,11 +286,14 @@ __global__ void __launch_bounds__(NTH, 1)
             for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
             tmem_st32(tO(t) + lrow + 32 * c2, ov);
           }
+          uint32_t lv[8];
+          tmem_ld8(tO(t) + lrow + D, lv);
+          lv[0] = __float_as_uint(__uint_as_float(lv[0]) * alpha);
+          tmem_st8(tO(t) + lrow + D, lv);
           tmem_st_wait();
         }
       }
-      // P = 2^(s log2(e)/sqrt(d_h) - m) in bf16, and its sum
-      float ps = 0.f;
+      // P = 2^(s log2(e)/sqrt(d_h) - m) in bf16
 #pragma unroll
       for (int c4 = 0; c4 < BK / 32; ++c4) {
 #pragma unroll
@@ -292,14 +308,12 @@ __global__ void __launch_bounds__(NTH, 1)
               p0 = key < kv ? p0 : 0.f;
               p1 = key + 1 < kv ? p1 : 0.f;
             }
-            ps += p0 + p1;
             w[e / 2] = pack_bf16(p0, p1);
           }
           const int chunk = 4 * c4 + c8;  // 16-byte chunk of the row's 128 keys
           *reinterpret_cast<uint4*>(pt + (chunk >> 3) * TILE + swz_off(i, chunk & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-      l = l * alpha + ps;
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -308,7 +322,9 @@ __global__ void __launch_bounds__(NTH, 1)
     // o = O / l, staged over the tile's Q rows (every S_t has been computed), stored as whole lines
     mbar_wait(OREADY(t), (nk - 1) & 1, fail);
     tc_fence_after();
-    const float inv = 1.f / l;
+    uint32_t lv[8];
+    tmem_ld8(tO(t) + lrow + D, lv);
+    const float inv = 1.f / __uint_as_float(lv[0]);
     uint8_t* qt = smem + O_Q + t * TILE;
 #pragma unroll
     for (int c2 = 0; c2 < D / 32; ++c2) {
