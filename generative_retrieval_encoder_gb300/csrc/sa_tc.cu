@@ -58,6 +58,12 @@ static_assert(SMEM <= 227 * 1024, "shared memory");
 __device__ __forceinline__ uint32_t swz_off(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
+// max(a, b, c): the three-input form of max.f32
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -261,7 +267,7 @@ __global__ void __launch_bounds__(NTH, 1)
       for (int c4 = 0; c4 < BK / 32; ++c4) {
         if (full) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(sv[c4][c]));
+          for (int c = 0; c < 32; c += 2) mx = max3(mx, __uint_as_float(sv[c4][c]), __uint_as_float(sv[c4][c + 1]));
         } else {
 #pragma unroll
           for (int c = 0; c < 32; ++c)
@@ -302,8 +308,11 @@ __global__ void __launch_bounds__(NTH, 1)
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
             const int c = 8 * c8 + e, key = 32 * c4 + c;
-            float p0 = ex2(fmaf(__uint_as_float(sv[c4][c]), sl2, -m));
-            float p1 = ex2(fmaf(__uint_as_float(sv[c4][c + 1]), sl2, -m));
+            // both exponents in one packed fma
+            const float2 xa = __ffma2_rn(make_float2(__uint_as_float(sv[c4][c]), __uint_as_float(sv[c4][c + 1])),
+                                         make_float2(sl2, sl2), make_float2(-m, -m));
+            float p0 = ex2(xa.x);
+            float p1 = ex2(xa.y);
             if (!full) {
               p0 = key < kv ? p0 : 0.f;
               p1 = key + 1 < kv ? p1 : 0.f;
