@@ -231,8 +231,8 @@ Layout ws_layout(const Plan& p, int op) {
   } else if (op == GBLA_OP_DECAY_FORWARD) {
     const size_t ch = (size_t)decay_chunks(p) * p.H;
     if (p.mode == SEQ_VARLEN) l.pre_d = c.take((size_t)(p.n_seq + 1) * 4);
-    l.LF = c.take(ch * p.dh * state_ld(p.dh) * 4);
-    l.LB = c.take(ch * p.dh * state_ld(p.dh) * 4);
+    l.LF = c.take(ch * p.dh * state_ld(p.dh) * 2);
+    l.LB = c.take(ch * p.dh * state_ld(p.dh) * 2);
     l.lamc = c.take(ch * 4);
     l.HF = c.take(ch * p.dh * state_bf_ld(p.dh) * 2);
     l.HB = c.take(ch * p.dh * state_bf_ld(p.dh) * 2);
@@ -807,7 +807,7 @@ gbla_status bla_decay_core_forward(const gbla_shape* shape, const void* q, const
   a.q = q; a.k = k; a.v = v; a.ld = p.HD;
   a.g = g; a.lam = lam; a.ldg = p.H;
   a.o = o; a.den = den;
-  a.LF = at<float>(ws, c.l.LF); a.LB = at<float>(ws, c.l.LB); a.Lam = at<float>(ws, c.l.lamc);
+  a.LF = at<bf16>(ws, c.l.LF); a.LB = at<bf16>(ws, c.l.LB); a.Lam = at<float>(ws, c.l.lamc);
   a.HF = at<bf16>(ws, c.l.HF); a.HB = at<bf16>(ws, c.l.HB);
   a.H = p.H; a.dh = p.dh; a.seq = c.seq; a.err = c.kerr;
   a.tiles.tile = kDecayChunk;

@@ -23,7 +23,9 @@
 // Three kernels: the chunks' local states (k_decay_states), the two scans per
 // (sequence, head) (k_decay_scan), the outputs per chunk (k_decay_out).  The
 // contractions run on tensor cores (mma.sync m16n8k16, bf16 operands, fp32
-// accumulation); the scans and decays in fp32.  d_h = 64, bf16 I/O.
+// accumulation); the scans and decays in fp32.  The chunk states L and the
+// scanned states H pass between the kernels in bf16 (the rounding of the
+// tensor-core operands they become).  d_h = 64, bf16 I/O.
 #include <algorithm>
 
 #include "common.cuh"
@@ -37,7 +39,7 @@ constexpr int DD = 64;                  // d_h
 constexpr int CC = 128;                 // rows per chunk
 constexpr int CPR = DD / 8;             // 16-byte chunks in a row of 64 bf16
 constexpr int TBYTES = CC * DD * 2;     // one [128 rows][64] bf16 tile, 16 KB
-constexpr int SLD = state_ld(DD);       // fp32 chunk-state row: 64 S + z + pad (72)
+constexpr int SLD = state_ld(DD);       // chunk-state row (bf16): 64 S + z + pad (72)
 constexpr int HLD = DD + 16;            // bf16 scan-state row: 64 S + z + pad (80)
 constexpr unsigned FULLM = 0xffffffffu;
 
@@ -97,7 +99,7 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const bf16* src, int64_t
 }
 
 // ======================================================================
-// k_decay_states: per (chunk, head), L^F and L^B (fp32 [64][72], z in column
+// k_decay_states: per (chunk, head), L^F and L^B (bf16 [64][72], z in column
 // 64) and Lambda_c.  8 warps: warp (wm, kg) owns state rows e in
 // [16 wm, 16 wm + 16) and the 16-row key steps kk = kg (mod 2).
 // ======================================================================
@@ -177,8 +179,8 @@ __global__ void __launch_bounds__(256) k_decay_states(const DecayArgs a) {
   __syncthreads();
   if (kg == 0) {
     const size_t slot = (size_t)blockIdx.x * H + h;
-    float* PF = a.LF + slot * DD * SLD;
-    float* PB = a.LB + slot * DD * SLD;
+    bf16* PF = a.LF + slot * DD * SLD;
+    bf16* PB = a.LB + slot * DD * SLD;
     const int e = wm * 16 + (lane >> 2);
 #pragma unroll
     for (int n = 0; n < 9; ++n) {
@@ -190,10 +192,10 @@ __global__ void __launch_bounds__(256) k_decay_states(const DecayArgs a) {
       }
       const int f = n * 8 + 2 * t4;  // n = 8: column 64 holds z, 65..71 are zero
       const bool zc = n < 8 || t4 == 0;
-      *reinterpret_cast<float2*>(PF + e * SLD + f) = zc ? make_float2(vF[0], n < 8 ? vF[1] : 0.f) : make_float2(0.f, 0.f);
-      *reinterpret_cast<float2*>(PF + (e + 8) * SLD + f) = zc ? make_float2(vF[2], n < 8 ? vF[3] : 0.f) : make_float2(0.f, 0.f);
-      *reinterpret_cast<float2*>(PB + e * SLD + f) = zc ? make_float2(vB[0], n < 8 ? vB[1] : 0.f) : make_float2(0.f, 0.f);
-      *reinterpret_cast<float2*>(PB + (e + 8) * SLD + f) = zc ? make_float2(vB[2], n < 8 ? vB[3] : 0.f) : make_float2(0.f, 0.f);
+      *reinterpret_cast<uint32_t*>(PF + e * SLD + f) = zc ? pack_bf16(vF[0], n < 8 ? vF[1] : 0.f) : 0u;
+      *reinterpret_cast<uint32_t*>(PF + (e + 8) * SLD + f) = zc ? pack_bf16(vF[2], n < 8 ? vF[3] : 0.f) : 0u;
+      *reinterpret_cast<uint32_t*>(PB + e * SLD + f) = zc ? pack_bf16(vB[0], n < 8 ? vB[1] : 0.f) : 0u;
+      *reinterpret_cast<uint32_t*>(PB + (e + 8) * SLD + f) = zc ? pack_bf16(vB[2], n < 8 ? vB[3] : 0.f) : 0u;
     }
     if (tid == 0) a.Lam[slot] = __expf(Ae);
   }
@@ -202,8 +204,9 @@ __global__ void __launch_bounds__(256) k_decay_states(const DecayArgs a) {
 // ======================================================================
 // k_decay_scan: per (sequence, head), the forward and the backward scan over
 // the sequence's chunks; writes the bf16 states H^F_c, H^B_c [64][80] that
-// chunk c's outputs read.  Each thread owns elements i, i + 256, ... of the
-// [64][72] state; the next chunk's L loads under the current update.
+// chunk c's outputs read.  Each thread owns the bf16 pairs i, i + 256, ... of
+// the [64][72] chunk state (fp32 running sums); the next chunk's L loads under
+// the current update.
 // ======================================================================
 __global__ void __launch_bounds__(256) k_decay_scan(const DecayArgs a) {
   pdl_enter();
@@ -211,35 +214,40 @@ __global__ void __launch_bounds__(256) k_decay_scan(const DecayArgs a) {
   const int b = blockIdx.x, h = blockIdx.y, H = a.H;
   int first, cnt;
   seq_tiles(a.seq, a.tiles, b, first, cnt);
-  constexpr int PER = (DD * SLD + 255) / 256;  // 18
+  constexpr int NP = DD * SLD / 2;             // bf16 pairs of a state (SLD is even: no pair straddles a row)
+  constexpr int PER = (NP + 255) / 256;        // 9
   for (int dir = 0; dir < 2; ++dir) {
-    const float* L = dir == 0 ? a.LF : a.LB;
+    const uint32_t* L = reinterpret_cast<const uint32_t*>(dir == 0 ? a.LF : a.LB);
     bf16* Hs = dir == 0 ? a.HF : a.HB;
-    float st[PER];
+    float st[PER][2];
 #pragma unroll
-    for (int q = 0; q < PER; ++q) st[q] = 0.f;
+    for (int q = 0; q < PER; ++q) st[q][0] = st[q][1] = 0.f;
     for (int s = 0; s < cnt; ++s) {
       const int cidx = first + (dir == 0 ? s : cnt - 1 - s);
       const size_t slot = (size_t)cidx * H + h;
-      float lv[PER];
+      uint32_t lv[PER];
 #pragma unroll
       for (int q = 0; q < PER; ++q) {
         const int i = threadIdx.x + 256 * q;
-        lv[q] = i < DD * SLD ? __ldcg(L + slot * DD * SLD + i) : 0.f;
+        lv[q] = i < NP ? __ldcg(L + slot * NP + i) : 0u;
       }
       const float lam = __ldcg(a.Lam + slot);
       // the state this chunk reads: chunks before it (forward) or after it (backward)
 #pragma unroll
       for (int q = 0; q < PER; ++q) {
         const int i = threadIdx.x + 256 * q;
-        if (i < DD * SLD) {
-          const int e = i / SLD, f = i % SLD;
-          Hs[slot * DD * HLD + (size_t)e * HLD + f] = __float2bfloat16_rn(f <= DD ? st[q] : 0.f);
-          st[q] = fmaf(lam, st[q], lv[q]);
+        if (i < NP) {
+          const int e = (2 * i) / SLD, f = (2 * i) % SLD;  // f even: columns f, f + 1
+          *reinterpret_cast<uint32_t*>(Hs + slot * DD * HLD + (size_t)e * HLD + f) =
+              pack_bf16(f <= DD ? st[q][0] : 0.f, f + 1 <= DD ? st[q][1] : 0.f);
+          st[q][0] = fmaf(lam, st[q][0], bf_lo(lv[q]));
+          st[q][1] = fmaf(lam, st[q][1], bf_hi(lv[q]));
         }
       }
-      for (int i = threadIdx.x; i < DD * (HLD - SLD); i += 256)
-        Hs[slot * DD * HLD + (size_t)(i / (HLD - SLD)) * HLD + SLD + i % (HLD - SLD)] = __float2bfloat16_rn(0.f);
+      for (int i = threadIdx.x; i < DD * (HLD - SLD) / 2; i += 256) {
+        const int e = i / ((HLD - SLD) / 2), f = SLD + 2 * (i % ((HLD - SLD) / 2));
+        *reinterpret_cast<uint32_t*>(Hs + slot * DD * HLD + (size_t)e * HLD + f) = 0u;
+      }
     }
   }
 }

@@ -161,7 +161,7 @@ struct DecayArgs {
   const void* q; const void* k; const void* v; int64_t ld;  // [rows, ld], head h at column h*dh
   const float* g; const float* lam; int64_t ldg;            // [rows, ldg]
   void* o; float* den;                                      // o like q; den [rows, ldg] or null
-  float* LF; float* LB; float* Lam;                         // chunk states [chunks*H][dh][dh+8] fp32, decays [chunks*H]
+  bf16* LF; bf16* LB; float* Lam;                           // chunk states [chunks*H][dh][dh+8] bf16, decays [chunks*H]
   bf16* HF; bf16* HB;                                       // scan states [chunks*H][dh][dh+16] bf16
   int H, dh;
   SeqDesc seq; Tiling tiles;                                // tiles: the 128-row chunks
