@@ -183,58 +183,58 @@ __global__ void __launch_bounds__(NTH, 1)
     }
   } else if (warp == NSW + 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t id_s = idesc_bf16(BQ, BK, false, false), id_o = idesc_bf16(BQ, ON, false, true);
-      // S_t = Q_t K_j^T: K = d_h.  A = Q_t K-major (+32 B per 16 features); B = K_j K-major (rows = keys).
-      auto issue_s = [&](int t, int j) {
-        const int s = j % KST;
+    // The whole warp runs the loop, so that its waits and descriptor arithmetic
+    // stay warp-uniform; one lane issues the MMAs and commits.
+    const uint32_t id_s = idesc_bf16(BQ, BK, false, false), id_o = idesc_bf16(BQ, ON, false, true);
+    auto issue_s = [&](int t, int j) {
+      const uint64_t da = sdesc(sQ(t), 16, 1024), db = sdesc(sK(j % KST), 16, 1024);
+      if (lane == 0) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma(tS(t), sdesc(sQ(t) + 32 * kk, 16, 1024), sdesc(sK(s) + 32 * kk, 16, 1024), id_s, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk) tc_mma(tS(t), da + 2 * kk, db + 2 * kk, id_s, kk > 0);
         tc_commit(SFULL(t));
-      };
-      // [O_t | l_t] += P_t [V_j | 1]: K = keys.  A = P_t K-major (two 64-key atoms); B N-major
-      // (16 key rows = 2048 B), its second 64-column atom the ones block (LBO apart).
-      auto issue_pv = [&](int t, int j) {
-        const int s = j % KST;
-        const uint32_t lbo = sbase + O_ONE - sV(s);
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int t, int j) {
+      const int s = j % KST;
+      const uint64_t da = sdesc(sP(t), 16, 1024), db = sdesc(sV(s), sbase + O_ONE - sV(s), 1024);
+      const uint32_t acc0 = j > 0 ? 1u : 0u;
+      if (lane == 0) {
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          tc_mma(tO(t), sdesc(sP(t) + (kk >> 2) * TILE + 32 * (kk & 3), 16, 1024), sdesc(sV(s) + 2048 * kk, lbo, 1024),
-                 id_o, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma(tO(t), da + (kk >> 2) * (TILE >> 4) + 2 * (kk & 3), db + 128 * kk, id_o, kk > 0 ? 1u : acc0);
         tc_commit(OREADY(t));
-      };
-      bool ok = mbar_wait(QFULL, 0, fail) && mbar_wait(KVFULL(0), 0, fail);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, 0);
-        issue_s(1, 0);
       }
-      for (int j = 0; j < nk && ok; ++j) {
-        // S_t of the next key tile as soon as the softmax holds this one in
-        // registers, then PV_t of this tile once its P is written
-        if (j + 1 < nk) {
-          ok = mbar_wait(KVFULL((j + 1) % KST), ((j + 1) / KST) & 1, fail);
-          for (int t = 0; t < 2 && ok; ++t) {
-            ok = mbar_wait(SFREE(t), j & 1, fail);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(t, j + 1);
-          }
-        }
+      __syncwarp();
+    };
+    bool ok = mbar_wait(QFULL, 0, fail) && mbar_wait(KVFULL(0), 0, fail);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0, 0);
+      issue_s(1, 0);
+    }
+    for (int j = 0; j < nk && ok; ++j) {
+      if (j + 1 < nk) {
+        ok = mbar_wait(KVFULL((j + 1) % KST), ((j + 1) / KST) & 1, fail);
         for (int t = 0; t < 2 && ok; ++t) {
-          ok = mbar_wait(PFULL(t), j & 1, fail);
+          ok = mbar_wait(SFREE(t), j & 1, fail);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(t, j);
+          issue_s(t, j + 1);
         }
-        if (ok) tc_commit(KVEMPTY(j % KST));  // every MMA on stage j % KST is issued
       }
-      // every MMA issued above has finished once the last OREADY completes
-      for (int t = 0; t < 2; ++t)
-        for (uint32_t it = 0; it < kPollLimit && !mbar_try_wait(OREADY(t), (uint32_t)(nk - 1) & 1) && !*fail; ++it) {
-        }
+      for (int t = 0; t < 2 && ok; ++t) {
+        ok = mbar_wait(PFULL(t), j & 1, fail);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(t, j);
+      }
+      if (ok && lane == 0) tc_commit(KVEMPTY(j % KST));
+      __syncwarp();
     }
+    for (int t = 0; t < 2; ++t)
+      for (uint32_t it = 0; it < kPollLimit && !mbar_try_wait(OREADY(t), (uint32_t)(nk - 1) & 1) && !*fail; ++it) {
+      }
   } else {
     // --------------------------------------------------------- softmax
     const int t = warp >> 2, wq = warp & 3;  // query tile, TMEM lane quarter
