@@ -17,10 +17,12 @@
 // and o = O / l at the end: the sum l accumulates on the tensor cores from
 // the same bf16 weights as the numerator (a constant block with a column of
 // ones is B's second atom).  Roles: a producer warp (TMA: the two Q tiles,
-// then K_j and V_j through a 3-stage ring), an MMA warp (S_a(j+1), S_b(j+1)
-// as soon as the softmax holds S(j) in registers, then PV_a(j), PV_b(j): the
-// tensor cores compute the next scores while the softmax of the current ones
-// runs), and two groups of four softmax warps (tile a, tile b).  Keys past the end of the sequence are
+// then K_j and V_j through a 3-stage ring), an S warp (S_a(j+1), S_b(j+1) as
+// soon as the softmax holds S(j) in registers: the tensor cores compute the
+// next scores while the softmax of the current ones runs), a PV warp (PV_a(j),
+// PV_b(j) once P is written; two issuing threads issue the short MMAs twice
+// as fast as one), and two groups of four softmax warps (tile a, tile b).
+// Keys past the end of the sequence are
 // masked; queries past it are computed but not stored, and rows of a padded
 // slot past the sequence receive zeros.
 //
@@ -52,7 +54,7 @@ constexpr int SMEM = O_FAIL + 4 + 1024;         // + alignment slack
 constexpr int ON = D + 16;                      // PV's N: the 64 value columns and the sum column (+ pad)
 constexpr int TMEM_COLS = 512;                  // S_a | S_b | O_a | O_b (128 + 128 + 80 + 80)
 constexpr int NSW = 8;                          // softmax warps (4 a tile)
-constexpr int NTH = (NSW + 2) * 32;
+constexpr int NTH = (NSW + 3) * 32;             // + producer, S issuer, PV issuer
 static_assert(SMEM <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ uint32_t swz_off(int row, int chunk) {
@@ -126,7 +128,7 @@ __global__ void __launch_bounds__(NTH, 1)
     mbar_init(QFULL, 1);
     for (int s = 0; s < KST; ++s) {
       mbar_init(KVFULL(s), 1);
-      mbar_init(KVEMPTY(s), 1);  // the commit after the stage's last PV
+      mbar_init(KVEMPTY(s), 2);  // the commits after the stage's last S and last PV
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(SFULL(t), 1);
@@ -182,10 +184,14 @@ __global__ void __launch_bounds__(NTH, 1)
       }
     }
   } else if (warp == NSW + 1) {
-    // ---------------------------------------------------------- MMA issuer
-    // The whole warp runs the loop, so that its waits and descriptor arithmetic
-    // stay warp-uniform; one lane issues the MMAs and commits.
-    const uint32_t id_s = idesc_bf16(BQ, BK, false, false), id_o = idesc_bf16(BQ, ON, false, true);
+    // ------------------------------------------------------------ S issuer
+    // S and PV have one issuing warp each: a thread issues an MMA about every
+    // 50 cycles, so that one thread alone cannot keep up with MMAs this short
+    // (64 and 52 cycles of tensor-core work).  The whole warp runs each loop,
+    // so that its waits and descriptor arithmetic stay warp-uniform; one lane
+    // issues the MMAs and commits.
+    const uint32_t id_s = idesc_bf16(BQ, BK, false, false);
+    // S_t = Q_t K_j^T: K = d_h.  A = Q_t K-major (+32 B per 16 features); B = K_j K-major (rows = keys).
     auto issue_s = [&](int t, int j) {
       const uint64_t da = sdesc(sQ(t), 16, 1024), db = sdesc(sK(j % KST), 16, 1024);
       if (lane == 0) {
@@ -195,6 +201,24 @@ __global__ void __launch_bounds__(NTH, 1)
       }
       __syncwarp();
     };
+    bool ok = mbar_wait(QFULL, 0, fail) && mbar_wait(KVFULL(0), 0, fail);
+    for (int j = 0; j < nk && ok; ++j) {
+      // S_t(j) once the softmax holds S_t(j - 1) in registers
+      if (j > 0) ok = mbar_wait(KVFULL(j % KST), (j / KST) & 1, fail);
+      for (int t = 0; t < 2 && ok; ++t) {
+        if (j > 0) ok = mbar_wait(SFREE(t), (j - 1) & 1, fail);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(t, j);
+      }
+      if (ok && lane == 0) tc_commit(KVEMPTY(j % KST));  // K_j read by both tiles' S
+      __syncwarp();
+    }
+  } else if (warp == NSW + 2) {
+    // ----------------------------------------------------------- PV issuer
+    const uint32_t id_o = idesc_bf16(BQ, ON, false, true);
+    // [O_t | l_t] += P_t [V_j | 1]: K = keys.  A = P_t K-major (two 64-key atoms); B N-major
+    // (16 key rows = 2048 B), its second 64-column atom the ones block (LBO apart).
     auto issue_pv = [&](int t, int j) {
       const int s = j % KST;
       const uint64_t da = sdesc(sP(t), 16, 1024), db = sdesc(sV(s), sbase + O_ONE - sV(s), 1024);
@@ -207,31 +231,19 @@ __global__ void __launch_bounds__(NTH, 1)
       }
       __syncwarp();
     };
-    bool ok = mbar_wait(QFULL, 0, fail) && mbar_wait(KVFULL(0), 0, fail);
-    if (ok) {
-      tc_fence_after();
-      issue_s(0, 0);
-      issue_s(1, 0);
-    }
+    bool ok = true;
     for (int j = 0; j < nk && ok; ++j) {
-      if (j + 1 < nk) {
-        ok = mbar_wait(KVFULL((j + 1) % KST), ((j + 1) / KST) & 1, fail);
-        for (int t = 0; t < 2 && ok; ++t) {
-          ok = mbar_wait(SFREE(t), j & 1, fail);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(t, j + 1);
-        }
-      }
+      ok = mbar_wait(KVFULL(j % KST), (j / KST) & 1, fail);  // V_j in shared memory
       for (int t = 0; t < 2 && ok; ++t) {
         ok = mbar_wait(PFULL(t), j & 1, fail);
         if (!ok) break;
         tc_fence_after();
         issue_pv(t, j);
       }
-      if (ok && lane == 0) tc_commit(KVEMPTY(j % KST));
+      if (ok && lane == 0) tc_commit(KVEMPTY(j % KST));  // V_j read by both tiles' PV
       __syncwarp();
     }
+    // every MMA this warp issued has finished once the last OREADY completes
     for (int t = 0; t < 2; ++t)
       for (uint32_t it = 0; it < kPollLimit && !mbar_try_wait(OREADY(t), (uint32_t)(nk - 1) & 1) && !*fail; ++it) {
       }
@@ -279,6 +291,24 @@ __global__ void __launch_bounds__(NTH, 1)
       const float mnew = move ? mt : m;
       const float alpha = ex2(m - mnew);  // 0 on the first tile, 1 when m stays
       m = mnew;
+      // P = 2^(s log2(e)/sqrt(d_h) - m) in bf16, into registers before the wait below
+      uint32_t pw[BK / 2];
+#pragma unroll
+      for (int c4 = 0; c4 < BK / 32; ++c4) {
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const int key = 32 * c4 + c;
+          const float2 xa = __ffma2_rn(make_float2(__uint_as_float(sv[c4][c]), __uint_as_float(sv[c4][c + 1])),
+                                       make_float2(sl2, sl2), make_float2(-m, -m));
+          float p0 = ex2(xa.x);
+          float p1 = ex2(xa.y);
+          if (!full) {
+            p0 = key < kv ? p0 : 0.f;
+            p1 = key + 1 < kv ? p1 : 0.f;
+          }
+          pw[key / 2] = pack_bf16(p0, p1);
+        }
+      }
       // the accumulator and P_t are free once PV_t of the previous tile is done
       if (j > 0) {
         mbar_wait(OREADY(t), (j - 1) & 1, fail);
@@ -299,30 +329,10 @@ __global__ void __launch_bounds__(NTH, 1)
           tmem_st_wait();
         }
       }
-      // P = 2^(s log2(e)/sqrt(d_h) - m) in bf16
 #pragma unroll
-      for (int c4 = 0; c4 < BK / 32; ++c4) {
-#pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const int c = 8 * c8 + e, key = 32 * c4 + c;
-            // both exponents in one packed fma
-            const float2 xa = __ffma2_rn(make_float2(__uint_as_float(sv[c4][c]), __uint_as_float(sv[c4][c + 1])),
-                                         make_float2(sl2, sl2), make_float2(-m, -m));
-            float p0 = ex2(xa.x);
-            float p1 = ex2(xa.y);
-            if (!full) {
-              p0 = key < kv ? p0 : 0.f;
-              p1 = key + 1 < kv ? p1 : 0.f;
-            }
-            w[e / 2] = pack_bf16(p0, p1);
-          }
-          const int chunk = 4 * c4 + c8;  // 16-byte chunk of the row's 128 keys
-          *reinterpret_cast<uint4*>(pt + (chunk >> 3) * TILE + swz_off(i, chunk & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      }
+      for (int chunk = 0; chunk < BK / 8; ++chunk)
+        *reinterpret_cast<uint4*>(pt + (chunk >> 3) * TILE + swz_off(i, chunk & 7)) =
+            make_uint4(pw[4 * chunk], pw[4 * chunk + 1], pw[4 * chunk + 2], pw[4 * chunk + 3]);
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
