@@ -99,6 +99,35 @@ def test_host_argument_errors_launch_nothing(L):
     assert L.gbla_check_device_status(None, None) == gbla.GBLA_ERR_WORKSPACE
 
 
+def test_decay_and_sa_entry_points_host_errors(L):
+    """bla_decay_core_forward and sa_core_forward: workspace sizes that grow
+    with the shape, and null or misaligned pointers, short workspaces and
+    unsupported shapes refused as statuses before any CUDA call."""
+    fake = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 2)
+    s = gbla.make_shape(2, 300, 128, 2, 64)
+    big = gbla.make_shape(8, 4096, 512, 8, 64)
+    for op in (gbla.GBLA_OP_DECAY_FORWARD, gbla.GBLA_OP_SA_FORWARD):
+        assert 0 < gbla.gbla_workspace_size(s, op) <= gbla.gbla_workspace_size(big, op)
+    n = gbla.gbla_workspace_size(s, gbla.GBLA_OP_SA_FORWARD)
+    assert L.sa_core_forward(ctypes.byref(s), None, fake, fake, fake, fake, n, None) == gbla.GBLA_ERR_INVALID_ARG
+    assert L.sa_core_forward(ctypes.byref(s), fake, fake, odd, fake, fake, n, None) == gbla.GBLA_ERR_INVALID_ARG
+    assert L.sa_core_forward(ctypes.byref(s), fake, fake, fake, None, fake, n, None) == gbla.GBLA_ERR_INVALID_ARG
+    assert L.sa_core_forward(ctypes.byref(s), fake, fake, fake, fake, fake, n - 1, None) == gbla.GBLA_ERR_WORKSPACE
+    assert L.sa_core_forward(ctypes.byref(s), fake, fake, fake, fake, None, n, None) == gbla.GBLA_ERR_WORKSPACE
+    for bad in (gbla.make_shape(2, 300, 64, 2, 32), gbla.make_shape(2, 300, 128, 2, 64, dtype="f32")):
+        st = L.sa_core_forward(ctypes.byref(bad), fake, fake, fake, fake, fake, 1 << 30, None)
+        assert st == gbla.GBLA_ERR_UNSUPPORTED  # bf16 and d_h = 64 only
+    n = gbla.gbla_workspace_size(s, gbla.GBLA_OP_DECAY_FORWARD)
+    args = lambda q=fake, lam=fake: (q, fake, fake, fake, lam, fake, None)
+    assert L.bla_decay_core_forward(ctypes.byref(s), *args(lam=None), fake, n, None) == gbla.GBLA_ERR_INVALID_ARG
+    assert L.bla_decay_core_forward(ctypes.byref(s), *args(q=odd), fake, n, None) == gbla.GBLA_ERR_INVALID_ARG
+    assert L.bla_decay_core_forward(ctypes.byref(s), *args(), fake, n - 1, None) == gbla.GBLA_ERR_WORKSPACE
+    s32 = gbla.make_shape(2, 300, 64, 2, 32)
+    st = L.bla_decay_core_forward(ctypes.byref(s32), *args(), fake, 1 << 30, None)
+    assert st == gbla.GBLA_ERR_UNSUPPORTED
+
+
 def test_diag_and_noalloc_host_errors(L):
     """Host-side errors of the diagnostic and the no-allocation entry points:
     statuses, no launch, no out-of-range access of the per-device address
