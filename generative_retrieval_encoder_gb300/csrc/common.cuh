@@ -114,7 +114,6 @@ __device__ __forceinline__ int slot_rows(const SeqDesc& s, int nvalid) {
 __device__ __forceinline__ float phi_f(float x) { return x > 0.f ? x + 1.f : __expf(x); }
 // phi'(x): 1 for x > 0, e^x otherwise.
 __device__ __forceinline__ float dphi_f(float x) { return x > 0.f ? 1.f : __expf(x); }
-__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + __expf(-x)); }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

@@ -90,13 +90,6 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
-// Arrives on the mbarrier at the same offset in each CTA of `mask` once the
-// MMAs issued so far by this thread have completed.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-               ::"r"(bar), "h"(mask)
-               : "memory");
-}
 // M = 256 MMA of a CTA pair, issued by the even CTA: A rows 0..127 and the
 // first half of B's N columns from its shared memory, the rest from the
 // peer's at the same offsets; D rows 0..127 in its TMEM, 128..255 in the peer's.
