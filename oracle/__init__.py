@@ -56,6 +56,7 @@ def _load():
             lib.oracle_decay_core_explicit.argtypes = seq + [_D] * 7
             lib.oracle_decay_core_rnn.argtypes = seq + [_D] * 6
             lib.oracle_sa_forward.argtypes = seq + [_D] * 5
+            lib.oracle_sa_rows.argtypes = seq + [_D] * 3 + [ctypes.c_int, _I64, ctypes.POINTER(ctypes.c_int), _D]
             lib.oracle_conv1d.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, _I64, _I64] + [_D] * 4
             layer = ([ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _I64, _I64]
                      + [_D] * 10 + [ctypes.c_int, ctypes.c_double])
@@ -172,6 +173,21 @@ def sa_forward(q, k, v, start, ln, H: int, dh: int):
     o = np.zeros((T, H * dh)); lse = np.zeros((T, H))
     _load().oracle_sa_forward(T, H, dh, len(start), ps, pl, _p(q), _p(k), _p(v), _p(o), _p(lse))
     return o, lse
+
+
+def sa_rows(q, k, v, start, ln, H: int, dh: int, rows, heads):
+    """Eq. 1 at chosen (query row, head) pairs only (oracle_sa_rows): o [n, dh],
+    zeros for a row in no sequence."""
+    q, k, v = map(_f64, (q, k, v))
+    T = q.shape[0]
+    start, ln, ps, pl = _seqargs(start, ln)
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    hh = np.ascontiguousarray(heads, dtype=np.int32)
+    assert r.shape == hh.shape and r.ndim == 1
+    o = np.zeros((len(r), dh))
+    _load().oracle_sa_rows(T, H, dh, len(start), ps, pl, _p(q), _p(k), _p(v), len(r),
+                           r.ctypes.data_as(_I64), hh.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), _p(o))
+    return o
 
 
 def core_backward(q, k, v, g, d_o, start, ln, H: int, dh: int):

@@ -22,7 +22,8 @@
  * oracle_decay_core_explicit (the definition) and oracle_decay_core_rnn.
  * The bidirectional softmax attention of the SA blocks of the hybrid
  * [SA, LA, LA] encoder (GBLA notes, "Core method" 1, Eq. 1, and the hybrid
- * encoder paragraph) is oracle_sa_forward, Eq. 1 written out per query.
+ * encoder paragraph) is oracle_sa_forward, Eq. 1 written out per query, and
+ * oracle_sa_rows the same at chosen (query, head) pairs of long sequences.
  *
  * Readings where the pages are silent (each one is listed in the design notes):
  *   phi(x) = elu(x) + 1 with alpha = 1, no 1/sqrt(d_h) scale;
@@ -320,6 +321,47 @@ void oracle_sa_forward(int64_t T, int H, int dh, int n_seq,
       }
       free(sc);
     }
+}
+
+/*
+ * Eq. 1 at chosen (query row, head) pairs only, for sequences too long to
+ * compute every row: the same sum as oracle_sa_forward, one query at a time.
+ * Pair p is row rows[p] of head heads[p]; its d_h outputs go to o[p*dh ..];
+ * a row in no sequence gives zeros.
+ */
+void oracle_sa_rows(int64_t T, int H, int dh, int n_seq, const int64_t* start, const int64_t* len,
+                    const double* q, const double* k, const double* v, int n, const int64_t* rows,
+                    const int* heads, double* o) {
+  const int64_t ld = (int64_t)H * dh;
+  const double scale = 1.0 / sqrt((double)dh);
+#pragma omp parallel for schedule(dynamic)
+  for (int p = 0; p < n; ++p) {
+    const int64_t i = rows[p];
+    const int h = heads[p];
+    double* out = o + (int64_t)p * dh;
+    for (int f = 0; f < dh; ++f) out[f] = 0.0;
+    int b = -1;
+    for (int s = 0; s < n_seq && b < 0; ++s)
+      if (i >= start[s] && i < start[s] + len[s]) b = s;
+    if (b < 0 || i < 0 || i >= T || h < 0 || h >= H) continue;
+    double* sc = (double*)malloc(sizeof(double) * (size_t)len[b]);
+    double m = -INFINITY;
+    for (int64_t j = start[b]; j < start[b] + len[b]; ++j) {
+      double s = 0.0;
+      for (int e = 0; e < dh; ++e) s += q[i * ld + h * dh + e] * k[j * ld + h * dh + e];
+      s *= scale;
+      sc[j - start[b]] = s;
+      if (s > m) m = s;
+    }
+    double den = 0.0;
+    for (int64_t j = start[b]; j < start[b] + len[b]; ++j) {
+      const double w = exp(sc[j - start[b]] - m);
+      for (int f = 0; f < dh; ++f) out[f] += w * v[j * ld + h * dh + f];
+      den += w;
+    }
+    for (int f = 0; f < dh; ++f) out[f] /= den;
+    free(sc);
+  }
 }
 
 /*

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from generative_retrieval_encoder_gb300 import build, gbla
-from gbla_cases import TOL, core_case, f64, launch_names, max_err, valid_rows
+from gbla_cases import TOL, core_case, dev, f64, launch_names, max_err, valid_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -66,6 +66,32 @@ def test_sa_long_sequence():
     torch.cuda.synchronize()
     ro, _ = oracle.sa_forward(R["q"], R["k"], R["v"], st, ln, H, 64)
     assert max_err(o, ro, scale=np.abs(R["v"]).max()) <= TOL["bf16"]
+
+
+def test_sa_bench_size_sampled_rows():
+    """The launch the benchmark times at its largest size, B = 8 sequences of
+    L = 32768 tokens, H = 8, d_h = 64, against the oracle at 96 sampled
+    (query, head) pairs: first and last rows of the first and last sequence,
+    rows on both sides of the kernel's 128-key and 256-query tile edges, and
+    random rows (every other row's sum over 32768 keys is out of the oracle's
+    reach at this size)."""
+    B, L, H, dh = 8, 32768, 8, 64
+    T = B * L
+    r = torch.Generator().manual_seed(660)
+    D = {n: dev(torch.randn(T, H * dh, generator=r), "bf16") for n in ("q", "k", "v")}
+    shape = gbla.make_shape(B, L, H * dh, H, dh)
+    go = gbla.sa_core_forward(shape, D["q"], D["k"], D["v"])
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(661)
+    edges = [0, 127, 128, 255, 256, 511, 512, L - 1]
+    rows = np.array([b * L + e for b in (0, B - 1) for e in edges] + rng.integers(0, T, 80).tolist())
+    heads = rng.integers(0, H, len(rows))
+    R = {n: f64(D[n]) for n in ("q", "k", "v")}
+    st, ln = oracle.seqs(B, L)
+    ref = oracle.sa_rows(R["q"], R["k"], R["v"], st, ln, H, dh, rows, heads)
+    got = np.stack([f64(go[int(i), int(h) * dh:(int(h) + 1) * dh]) for i, h in zip(rows, heads)])
+    assert np.isfinite(got).all()
+    assert max_err(got, ref, scale=np.abs(R["v"]).max()) <= TOL["bf16"]
 
 
 def test_sa_is_deterministic_and_equals_sequence_alone():

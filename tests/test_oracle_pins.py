@@ -420,6 +420,34 @@ def test_sa_equals_torch_scaled_dot_product_attention(lens):
             np.testing.assert_allclose(lse[s:s + n, h], torch.logsumexp(scores, dim=1).numpy(), rtol=1e-12)
 
 
+def test_sa_rows_equal_torch_scaled_dot_product_attention():
+    """The sampled-row form (Eq. 1 at chosen query, head pairs, for sequences
+    too long for every row) equals the library's scaled-dot-product attention
+    at each pair, over ragged packed sequences; a row in no sequence (padding
+    past the last one) gives zeros."""
+    H, dh = 3, 16
+    lens = [1, 37, 130, 64]
+    T = sum(lens) + 5  # five padding rows at the end
+    q, k, v = _rand_qkv(T, H, dh, 37)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    st, ln = oracle.seqs(cu_seqlens=cu.tolist())
+    rng = np.random.default_rng(38)
+    rows = np.concatenate([[0, 1, 37, 38, 167, 168, 231, T - 1], rng.integers(0, T, 24)])
+    heads = rng.integers(0, H, len(rows))
+    o = oracle.sa_rows(q, k, v, st, ln, H, dh, rows, heads)
+    for p, (i, h) in enumerate(zip(rows, heads)):
+        b = np.searchsorted(cu, i, side="right") - 1
+        if b >= len(lens):
+            assert (o[p] == 0).all()
+            continue
+        s, n = cu[b], lens[b]
+        sl = slice(h * dh, (h + 1) * dh)
+        tq = torch.tensor(q[i:i + 1, sl])[None, None]
+        tk, tv = (torch.tensor(a[s:s + n, sl])[None, None] for a in (k, v))
+        ref = F.scaled_dot_product_attention(tq, tk, tv)[0, 0, 0].numpy()
+        np.testing.assert_allclose(o[p], ref, rtol=1e-12, atol=1e-12)
+
+
 def test_sa_single_key_and_identical_keys():
     """One key: the weight is 1, o = v.  Identical keys: equal weights, o is
     the mean of the values of the sequence."""
